@@ -1,0 +1,345 @@
+/*
+ * rssm.h -- C ABI of librssm.so: ReplaySSM decode for Mamba2 and gated delta net
+ * on GB300 (sm_103a).
+ *
+ * ReplaySSM keeps, per state slot, a frozen checkpoint S0 of the recurrent state
+ * plus a ring of the last L steps' inputs. A decode step computes its output from
+ * S0 and the ring instead of reading and writing the whole state; the state is
+ * folded and written back only on flush rows (every L steps, or when forced).
+ *
+ * Pages this interface follows (cited by title and section):
+ *   [M2]   "ReplaySSM: cache SSM inputs for faster Mamba2 standard decode"
+ *          (vLLM PR 48018 report): 功能与动机 (motivation), 实现拆解 items 1-3
+ *          (precompute + output kernels, ring append, per-row write_pos/is_flush
+ *          from the metadata builder), 关键源码片段 (the kernel call with
+ *          ssm_state, x, dt, A, B, C, D, x_cache, dt_cache, B_cache, write_pos,
+ *          is_flush, state_batch_indices, out, dt_bias, dt_softplus).
+ *   [FI]   "[Mamba] Add FlashInfer ReplaySSM backend" (vLLM PR 52506 report):
+ *          实现拆解 items 1-2 (ring cursor update/reset kernels; one cursor
+ *          advance shared by all layers of a cache group).
+ *   [GDN]  "GDN ReplaySSM decode (Part A of RFC 28511)" (SGLang PR 28451 report):
+ *          实现拆解 items 1-3 (decode kernel over the (d, k, g) ring, flush every L
+ *          steps, CUDA-graph-safe write_pos and force-flush buffers).
+ *   [SPEC] "[GDN] Support ReplaySSM Ring Spec-Verify" (SGLang PR 28695 report):
+ *          实现拆解 items 2-4 (circular ring, cursors write_pos / cache_base /
+ *          is_flush, spec verify kernel, exact fold from raw inputs, commit that
+ *          only advances cursors), 关键源码片段 (ring length >= 2 x drafts).
+ *
+ * Conventions for every entry point:
+ *   - Every pointer argument is a DEVICE pointer owned by the caller, 16-byte
+ *     aligned, to a dense row-major array with the layout stated below. The
+ *     library allocates nothing and keeps no reference after the call returns.
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream). No call synchronises or reads device data on the host, so
+ *     every call may be captured in a CUDA graph.
+ *   - Arguments are validated on the host before anything is launched; a call
+ *     that returns an error has launched nothing and changed nothing.
+ *   - Return value: RSSM_OK, or an RSSM_ERR_* code (rssm_status_string()).
+ *   - Device-detected problems cannot be returned synchronously. Where a call
+ *     takes `int32_t* dev_err` (nullable), a kernel that finds a row with a cache
+ *     index >= num_slots, or a cursor outside [0, L), skips that row and ORs an
+ *     RSSM_DEVERR_* bit into *dev_err. Rows whose cache index is negative are
+ *     padding (as in padded CUDA-graph batches): they are skipped silently and
+ *     their outputs are left untouched.
+ *   - Two rows of one call must not name the same slot (undefined result).
+ *   - Shapes named: b = batch row, s = slot = cache_indices[b], H = nheads,
+ *     P = headdim, N = dstate, G = ngroups, L = ring length; for the gated delta
+ *     net HV = value heads, HK = key heads, K = key dim, V = value dim.
+ *
+ * Storage dtypes: RSSM_F32 (IEEE float32) or RSSM_BF16 (bfloat16). State stores
+ * round to nearest, ties to even. All arithmetic accumulates in float32.
+ */
+#ifndef RSSM_H
+#define RSSM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st* rssm_stream_t;
+
+#define RSSM_ABI_VERSION 1
+
+enum rssm_status {
+    RSSM_OK = 0,
+    RSSM_ERR_INVALID_ARG = 1, /* null or misaligned pointer, bad enum, negative size */
+    RSSM_ERR_UNSUPPORTED = 2, /* shape or dtype this build has no kernel for */
+    RSSM_ERR_CONFIG = 3,      /* inconsistent configuration (nheads % ngroups, L < 1, L < 2T ...) */
+    RSSM_ERR_CUDA = 4         /* the CUDA runtime reported an error at launch */
+};
+
+enum rssm_dtype { RSSM_F32 = 0, RSSM_BF16 = 1 };
+
+/* Bits ORed into *dev_err by kernels. */
+enum rssm_dev_error {
+    RSSM_DEVERR_SLOT = 1,    /* a row's cache index was >= num_slots; the row was skipped */
+    RSSM_DEVERR_CURSOR = 2,  /* a row's write_pos / count was outside the ring; row skipped */
+    RSSM_DEVERR_TIMEOUT = 4  /* a bounded wait on an asynchronous copy expired; kernel stopped */
+};
+
+/* Cursor modes of rssm_advance_cursors. */
+enum rssm_cursor_mode {
+    RSSM_CURSOR_STANDARD = 0,
+    RSSM_CURSOR_SPEC_COMMIT = 1,
+    RSSM_CURSOR_RESET = 2
+};
+
+/* Text for a status code (static storage; never NULL). */
+const char* rssm_status_string(int status);
+
+/* RSSM_ABI_VERSION of the loaded library. */
+int rssm_abi_version(void);
+
+/* ------------------------------------------------------------------------- */
+/* Cursors                                                                    */
+/* ------------------------------------------------------------------------- */
+
+/* rssm_advance_cursors -- per-row ring cursors, computed on the device so that a
+ * captured decode step needs no host metadata. One launch serves every layer
+ * that shares the slots ([FI] 实现拆解 item 2: one tracker advance per cache
+ * group; [M2] 实现拆解 item 3: write_pos / is_flush per decode row).
+ *
+ * RSSM_CURSOR_STANDARD ([M2], [GDN] 实现拆解 item 2). For each row b with
+ *   s = cache_indices[b] >= 0:  w = slot_wp[s];
+ *   f = (w == L-1) || (force_flush && force_flush[b]);
+ *   row_wp[b] = w; row_flush[b] = f; slot_wp[s] = f ? 0 : w + 1.
+ *   Padding rows get row_wp = 0, row_flush = 0. Entry w of the ring is the
+ *   current step; a flush folds entries 0..w into the checkpoint.
+ *   Uses slot_wp [num_slots], cache_indices [batch], force_flush [batch]
+ *   (nullable), row_wp [batch], row_flush [batch]. slot_base, slot_flush,
+ *   num_accepted, T unused (may be NULL / 0).
+ *
+ * RSSM_CURSOR_SPEC_COMMIT ([SPEC] 实现拆解 item 4: the commit only advances
+ *   cursors). Per slot: slot_wp = committed unfolded entry count cnt, slot_base =
+ *   ring position of the oldest unfolded entry, slot_flush = fold pending. For
+ *   each row with s >= 0:
+ *     if slot_flush[s]: slot_base[s] = (slot_base[s] + slot_wp[s]) % L; slot_wp[s] = 0;
+ *     slot_wp[s] += num_accepted[b];   (0 <= num_accepted[b] <= T)
+ *     slot_flush[s] = (slot_wp[s] + T > L);
+ *   and, when given, row_wp[b] / row_flush[b] receive the new cnt / flush.
+ *   Must follow the rssm_gdn_spec_verify call of the same round.
+ *
+ * RSSM_CURSOR_RESET ([FI] reset_replayssm_ring_trackers; [SPEC] cursor reset at
+ *   slot (re)use): for each row with s >= 0, slot_wp[s] = 0 and, when given,
+ *   slot_base[s] = 0, slot_flush[s] = 0.
+ *
+ * Errors: RSSM_ERR_INVALID_ARG for a NULL required pointer; RSSM_ERR_CONFIG for
+ * L < 1, or, in SPEC_COMMIT, T < 1 or L < 2T. A num_accepted outside [0, T] or a
+ * stored cursor outside the ring sets RSSM_DEVERR_CURSOR and leaves that slot. */
+int rssm_advance_cursors(int mode, int32_t* slot_wp, int32_t* slot_base, uint8_t* slot_flush,
+                         const int32_t* cache_indices, const uint8_t* force_flush,
+                         const int32_t* num_accepted, int32_t batch, int32_t num_slots,
+                         int32_t L, int32_t T, int32_t* row_wp, uint8_t* row_flush,
+                         int32_t* dev_err, rssm_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
+/* Mamba2                                                                     */
+/* ------------------------------------------------------------------------- */
+
+typedef struct rssm_mamba2_dims {
+    int32_t batch;       /* rows in this call (>= 0) */
+    int32_t nheads;      /* H */
+    int32_t headdim;     /* P: 64 or 128 */
+    int32_t dstate;      /* N: 64 or 128 */
+    int32_t ngroups;     /* G: H % G == 0; heads h*G/H .. share group h / (H/G) */
+    int32_t ring_len;    /* L >= 1 */
+    int32_t num_slots;   /* slots in the state pool and the rings */
+    int32_t state_dtype; /* RSSM_F32 | RSSM_BF16: state pool */
+    int32_t act_dtype;   /* RSSM_F32 | RSSM_BF16: x, z, B, C, ring_x, ring_B */
+    int32_t out_dtype;   /* RSSM_F32 | RSSM_BF16: y */
+} rssm_mamba2_dims;
+
+/* Layouts (row-major, dense):
+ *   state   [num_slots][H][P][N]  state_dtype   checkpoint S0 per slot
+ *   ring_x  [num_slots][H][L][P]  act_dtype     x of each ring entry
+ *   ring_dt [num_slots][H][L]     float32       dt = softplus(dt_raw + dt_bias) per entry
+ *   ring_B  [num_slots][G][L][N]  act_dtype     B of each ring entry
+ *   x, z    [batch][H][P]         act_dtype
+ *   dt_raw  [batch][H]            float32
+ *   B, C    [batch][G][N]         act_dtype
+ *   A, D, dt_bias [H]             float32
+ *   y       [batch][H][P]         out_dtype
+ *   cache_indices [batch] int32; row_wp [batch] int32; row_flush [batch] uint8
+ *   (as produced by rssm_advance_cursors STANDARD). */
+
+/* rssm_ring_append -- write the current step's (x, dt, B) into ring entry
+ * row_wp[b] of slot cache_indices[b] ([M2] 关键符号 append_replayssm_ring;
+ * 实现拆解 item 2: x_cache, dt_cache, B_cache). The stored dt is
+ * softplus(dt_raw + dt_bias[h]) when dt_softplus is non-zero, else
+ * dt_raw + dt_bias[h]; dt_bias may be NULL (zero). Heads of one group write the
+ * group's B once. */
+int rssm_ring_append(const rssm_mamba2_dims* dims, const void* x, const float* dt_raw,
+                     const float* dt_bias, int dt_softplus, const void* B,
+                     const int32_t* cache_indices, const int32_t* row_wp, void* ring_x,
+                     float* ring_dt, void* ring_B, int32_t* dev_err, rssm_stream_t stream);
+
+/* Bytes of device workspace rssm_mamba2_precompute / rssm_mamba2_decode need
+ * (per-(row, head) coefficient tables, float32). 0 for an invalid dims. */
+size_t rssm_mamba2_workspace_size(const rssm_mamba2_dims* dims);
+
+/* rssm_mamba2_precompute -- per-row scalar tables for the output kernel ([M2]
+ * 实现拆解 item 1: the precompute kernel). For row b, head h, entries i = 0..w
+ * (w = row_wp[b]), with dA_j = exp(A[h] * dt_j) and dt_j read from ring_dt:
+ *   P_i  = prod_{j=i+1..w} dA_j  (= exp(A[h] * sum_{j>i} dt_j)),
+ *   Pm1  = prod_{j=0..w} dA_j,
+ *   bc_i = B_i . C_t over dstate (B_i from ring_B, group of h),
+ *   coef_i = P_i dt_i bc_i, a_i = P_i dt_i;
+ * stored per (b, h) as [coef_0..coef_{L-1}, a_0..a_{L-1}, Pm1, pad] in workspace.
+ * The ring must already hold the current entry (rssm_ring_append). */
+int rssm_mamba2_precompute(const rssm_mamba2_dims* dims, const float* A, const void* C,
+                           const float* ring_dt, const void* ring_B,
+                           const int32_t* cache_indices, const int32_t* row_wp,
+                           void* workspace, size_t workspace_bytes, int32_t* dev_err,
+                           rssm_stream_t stream);
+
+/* rssm_mamba2_output -- the fused output / flush kernel ([M2] 实现拆解 item 1:
+ * output kernel branching per row on is_flush; 功能与动机: most steps read the
+ * output from checkpoint + buffer, the full state is written back every L
+ * steps). Streams each (row, head) checkpoint tile S0 once:
+ *   y[p] = Pm1 * sum_n S0[p][n] C[n] + sum_{i=0..w} coef_i x_i[p] + D[h] x_w[p],
+ *   y[p] *= silu(z[p])   (z nullable)
+ * and, on flush rows, stores state[s][h] = Pm1 * S0 + sum_i a_i x_i B_i^T
+ * rounded to state_dtype. Needs the tables of rssm_mamba2_precompute. */
+int rssm_mamba2_output(const rssm_mamba2_dims* dims, void* state, const void* C, const float* D,
+                       const void* z, const void* ring_x, const void* ring_B,
+                       const int32_t* cache_indices, const int32_t* row_wp,
+                       const uint8_t* row_flush, const void* workspace, size_t workspace_bytes,
+                       void* y, int32_t* dev_err, rssm_stream_t stream);
+
+/* rssm_mamba2_decode -- rssm_mamba2_precompute then rssm_mamba2_output (the
+ * selective_state_update_replayssm_output_only call of [M2] 关键源码片段). */
+int rssm_mamba2_decode(const rssm_mamba2_dims* dims, void* state, const float* A, const void* C,
+                       const float* D, const void* z, const void* ring_x, const float* ring_dt,
+                       const void* ring_B, const int32_t* cache_indices, const int32_t* row_wp,
+                       const uint8_t* row_flush, void* workspace, size_t workspace_bytes,
+                       void* y, int32_t* dev_err, rssm_stream_t stream);
+
+/* rssm_mamba2_full_state_update -- the conventional decode step that reads and
+ * writes the whole state every step ([M2] 关键源码片段, the baseline
+ * selective_state_update branch). For each row with s >= 0, head h:
+ *   dt = softplus(dt_raw + dt_bias) (or without softplus), dA = exp(A[h] dt),
+ *   h = dA h + dt x B^T (stored rounded to state_dtype),
+ *   y = (h C + D x) * silu(z)  (from the unrounded h; z nullable).
+ * ring_len is ignored. */
+int rssm_mamba2_full_state_update(const rssm_mamba2_dims* dims, void* state, const void* x,
+                                  const float* dt_raw, const float* dt_bias, int dt_softplus,
+                                  const float* A, const void* B, const void* C, const float* D,
+                                  const void* z, const int32_t* cache_indices, void* y,
+                                  int32_t* dev_err, rssm_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
+/* Gated delta net                                                            */
+/* ------------------------------------------------------------------------- */
+
+typedef struct rssm_gdn_dims {
+    int32_t batch;       /* rows in this call (>= 0) */
+    int32_t num_v_heads; /* HV */
+    int32_t num_k_heads; /* HK: HV % HK == 0; value head hv reads key head hv / (HV/HK) */
+    int32_t head_k_dim;  /* K: 128 */
+    int32_t head_v_dim;  /* V: multiple of 64 */
+    int32_t ring_len;    /* L >= 1 */
+    int32_t num_slots;
+    int32_t act_dtype;   /* RSSM_F32 | RSSM_BF16: q, k, v, ring_k, ring_v */
+    int32_t out_dtype;   /* RSSM_F32 | RSSM_BF16: o */
+} rssm_gdn_dims;
+
+/* Layouts (row-major, dense); the state is float32 ([SPEC] 风险与影响: the
+ * ReplaySSM path keeps an fp32 checkpoint):
+ *   state   [num_slots][HV][V][K] float32  checkpoint S0 per slot
+ *   ring_d  [num_slots][HV][L][V] float32  d_i = beta_i (v_i - g_i S_{i-1} k_i)
+ *   ring_k  [num_slots][HK][L][K] act_dtype
+ *   ring_g  [num_slots][HV][L]    float32  gate value g_i in (0, 1]
+ *   q, k    [batch][HK][K] act_dtype; v [batch][HV][V] act_dtype
+ *   beta, g [batch][HV] float32; o [batch][HV][V] out_dtype
+ * The recurrence is S <- g S + beta (v - g S k) k^T, o = S q ([GDN] 功能与动机:
+ * the conventional kernel reads and writes S[HV, V, K] every step). */
+
+/* rssm_gdn_ring_append -- write k and g of the current step into ring entry
+ * row_wp[b] ([GDN] 实现拆解 item 1, the (d, k, g) ring). d is produced by the
+ * output kernel, which needs the state. */
+int rssm_gdn_ring_append(const rssm_gdn_dims* dims, const void* k, const float* g,
+                         const int32_t* cache_indices, const int32_t* row_wp, void* ring_k,
+                         float* ring_g, int32_t* dev_err, rssm_stream_t stream);
+
+size_t rssm_gdn_workspace_size(const rssm_gdn_dims* dims);
+
+/* rssm_gdn_precompute -- per-row scalar tables. For row b, value head hv, key head
+ * kh, w = row_wp[b], ring entries i < w and the current gate g_t = g[b][hv]:
+ *   kk_i = k_i . k_t,  kq_i = k_i . q_t,  kq_t = k_t . q_t   (key head kh)
+ *   gamma_i = prod_{j=i+1..w-1} g_j,  Gu = prod_{j<w} g_j,  Go = g_t Gu,
+ *   Gamma_i = prod_{j=i+1..w} g_j (with g_w = g_t; Gamma_w = 1)
+ * stored per (b, hv) as [gamma_i kk_i (L), Gamma_i kq_i (L), Gamma_i (L), Gu, Go,
+ * kq_t, beta_t, g_t, pad]. */
+int rssm_gdn_precompute(const rssm_gdn_dims* dims, const void* q, const void* k,
+                        const float* beta, const float* g, const void* ring_k,
+                        const float* ring_g, const int32_t* cache_indices, const int32_t* row_wp,
+                        void* workspace, size_t workspace_bytes, int32_t* dev_err,
+                        rssm_stream_t stream);
+
+/* rssm_gdn_output -- fused GDN output / flush ([GDN] 实现拆解 item 1). Streams
+ * S0[s][hv] once, computing a = S0 k_t and c = S0 q_t per value row, then
+ *   u   = Gu a + sum_{i<w} gamma_i kk_i d_i       (= S_{t-1} k_t)
+ *   d_t = beta_t (v_t - g_t u)                     (written to ring_d entry w)
+ *   o   = Go c + sum_{i<w} Gamma_i kq_i d_i + kq_t d_t
+ * and on flush rows stores S = Go S0 + sum_{i<=w} Gamma_i d_i k_i^T. */
+int rssm_gdn_output(const rssm_gdn_dims* dims, float* state, const void* v,
+                    const void* ring_k, float* ring_d, const int32_t* cache_indices,
+                    const int32_t* row_wp, const uint8_t* row_flush, const void* workspace,
+                    size_t workspace_bytes, void* o, int32_t* dev_err, rssm_stream_t stream);
+
+/* rssm_gdn_decode -- rssm_gdn_precompute then rssm_gdn_output. */
+int rssm_gdn_decode(const rssm_gdn_dims* dims, float* state, const void* q, const void* k,
+                    const void* v, const float* beta, const float* g, const void* ring_k,
+                    const float* ring_g, float* ring_d, const int32_t* cache_indices,
+                    const int32_t* row_wp, const uint8_t* row_flush, void* workspace,
+                    size_t workspace_bytes, void* o, int32_t* dev_err, rssm_stream_t stream);
+
+/* rssm_gdn_full_state_decode -- the conventional GDN decode step: read S, apply
+ * S <- g S + beta (v - g S k) k^T, write S, o = S q. ring_len is ignored. */
+int rssm_gdn_full_state_decode(const rssm_gdn_dims* dims, float* state, const void* q,
+                               const void* k, const void* v, const float* beta, const float* g,
+                               const int32_t* cache_indices, void* o, int32_t* dev_err,
+                               rssm_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
+/* Gated delta net: speculative verify                                        */
+/* ------------------------------------------------------------------------- */
+
+/* rssm_gdn_spec_verify -- score a linear chain of T draft tokens per row from the
+ * checkpoint and the circular ring, without materialising per-draft states
+ * ([SPEC] 实现拆解 item 3, gdn_replayssm_spec_circular_kernel), after first
+ * folding, for slots whose fold is pending, the committed entries into the
+ * checkpoint by replaying the recurrence sequentially from the raw inputs
+ * ([SPEC] 实现拆解 item 3, gdn_replayssm_exact_fold_kernel; 评论区精华: the exact
+ * fold removed the long-output drift). Two launches: fold, then verify.
+ *
+ * Cursors (read only here; see RSSM_CURSOR_SPEC_COMMIT): slot_wp = cnt,
+ * slot_base = base, slot_flush = fold pending. Committed entries sit at ring
+ * positions (base + i) % L, i < cnt. With a pending fold the effective history
+ * is empty and base' = (base + cnt) % L. Draft j is written at position
+ * (base + cnt + j) % L (d, k, g and the raw v, beta used by a later fold).
+ *
+ * Inputs per draft: q, k [batch][T][HK][K], v [batch][T][HV][V] (act_dtype),
+ * beta, g [batch][T][HV] float32. Output o [batch][T][HV][V] (out_dtype): draft
+ * j's output after the history and drafts 0..j.
+ * Extra rings: ring_v [num_slots][HV][L][V] act_dtype (raw v), ring_beta
+ * [num_slots][HV][L] float32. ring_k doubles as the raw k ring (the kernel takes k
+ * as given; no normalisation happens inside).
+ * Errors: RSSM_ERR_CONFIG when T < 1 or L < 2T ([SPEC] 关键源码片段, server_args:
+ * the ring must hold at least twice the drafts). */
+int rssm_gdn_spec_verify(const rssm_gdn_dims* dims, int32_t T, float* state, const void* q,
+                         const void* k, const void* v, const float* beta, const float* g,
+                         float* ring_d, void* ring_k, float* ring_g, void* ring_v,
+                         float* ring_beta, const int32_t* cache_indices, const int32_t* slot_wp,
+                         const int32_t* slot_base, const uint8_t* slot_flush, void* o,
+                         int32_t* dev_err, rssm_stream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RSSM_H */

@@ -1,0 +1,227 @@
+"""ctypes binding over librssm.so: one Python function per C-ABI entry point,
+same names, argument marshalling only (tensors -> device pointers, None -> NULL,
+the current torch stream when none is given). Every computation happens in the
+library's CUDA kernels; there is no fallback path. A non-zero status raises
+RSSMError.
+"""
+import ctypes
+import os
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "librssm.so")
+
+RSSM_OK, RSSM_ERR_INVALID_ARG, RSSM_ERR_UNSUPPORTED, RSSM_ERR_CONFIG, RSSM_ERR_CUDA = range(5)
+RSSM_F32, RSSM_BF16 = 0, 1
+RSSM_DEVERR_SLOT, RSSM_DEVERR_CURSOR, RSSM_DEVERR_TIMEOUT = 1, 2, 4
+RSSM_CURSOR_STANDARD, RSSM_CURSOR_SPEC_COMMIT, RSSM_CURSOR_RESET = 0, 1, 2
+
+# every symbol include/rssm.h declares
+EXPORTS = (
+    "rssm_status_string", "rssm_abi_version", "rssm_advance_cursors", "rssm_ring_append",
+    "rssm_mamba2_workspace_size", "rssm_mamba2_precompute", "rssm_mamba2_output",
+    "rssm_mamba2_decode", "rssm_mamba2_full_state_update", "rssm_gdn_ring_append",
+    "rssm_gdn_workspace_size", "rssm_gdn_precompute", "rssm_gdn_output", "rssm_gdn_decode",
+    "rssm_gdn_full_state_decode", "rssm_gdn_spec_verify",
+)
+
+
+class RSSMError(RuntimeError):
+    def __init__(self, fn, status):
+        self.status = status
+        msg = _lib.rssm_status_string(status).decode() if _lib else str(status)
+        super().__init__("%s failed: %s (status %d)" % (fn, msg, status))
+
+
+class Mamba2Dims(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "batch", "nheads", "headdim", "dstate", "ngroups", "ring_len", "num_slots",
+        "state_dtype", "act_dtype", "out_dtype")]
+
+
+class GDNDims(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_int32) for n in (
+        "batch", "num_v_heads", "num_k_heads", "head_k_dim", "head_v_dim", "ring_len",
+        "num_slots", "act_dtype", "out_dtype")]
+
+
+_lib = None
+_VP = ctypes.c_void_p
+_I = ctypes.c_int
+_I32 = ctypes.c_int32
+_SZ = ctypes.c_size_t
+
+
+def _declare(L):
+    m2 = ctypes.POINTER(Mamba2Dims)
+    gd = ctypes.POINTER(GDNDims)
+    sig = {
+        "rssm_status_string": (ctypes.c_char_p, [_I]),
+        "rssm_abi_version": (_I, []),
+        "rssm_advance_cursors": (_I, [_I, _VP, _VP, _VP, _VP, _VP, _VP, _I32, _I32, _I32, _I32,
+                                      _VP, _VP, _VP, _VP]),
+        "rssm_ring_append": (_I, [m2, _VP, _VP, _VP, _I, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
+        "rssm_mamba2_workspace_size": (_SZ, [m2]),
+        "rssm_mamba2_precompute": (_I, [m2, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _VP]),
+        "rssm_mamba2_output": (_I, [m2, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ,
+                                    _VP, _VP, _VP]),
+        "rssm_mamba2_decode": (_I, [m2, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                    _VP, _SZ, _VP, _VP, _VP]),
+        "rssm_mamba2_full_state_update": (_I, [m2, _VP, _VP, _VP, _VP, _I, _VP, _VP, _VP, _VP,
+                                               _VP, _VP, _VP, _VP, _VP]),
+        "rssm_gdn_ring_append": (_I, [gd, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
+        "rssm_gdn_workspace_size": (_SZ, [gd]),
+        "rssm_gdn_precompute": (_I, [gd, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP,
+                                     _VP]),
+        "rssm_gdn_output": (_I, [gd, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _VP, _VP]),
+        "rssm_gdn_decode": (_I, [gd, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                 _VP, _SZ, _VP, _VP, _VP]),
+        "rssm_gdn_full_state_decode": (_I, [gd, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                            _VP]),
+        "rssm_gdn_spec_verify": (_I, [gd, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                      _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
+    }
+    for name, (res, args) in sig.items():
+        f = getattr(L, name)
+        f.restype = res
+        f.argtypes = args
+
+
+def lib():
+    """The loaded librssm.so. Raises if it has not been built: there is no
+    fallback implementation."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError("librssm.so is not built (run ssm_linear_attention_gb300/build.py "
+                              "or __graft_entry__.build()); there is no CPU fallback")
+        L = ctypes.CDLL(LIB_PATH)
+        _declare(L)
+        _lib = L
+    return _lib
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _call(name, *args):
+    rc = getattr(lib(), name)(*args)
+    if rc != RSSM_OK:
+        raise RSSMError(name, rc)
+
+
+def rssm_status_string(status):
+    return lib().rssm_status_string(status).decode()
+
+
+def rssm_abi_version():
+    return lib().rssm_abi_version()
+
+
+def rssm_advance_cursors(mode, slot_wp, slot_base, slot_flush, cache_indices, force_flush,
+                         num_accepted, batch, num_slots, L, T, row_wp, row_flush, dev_err=None,
+                         stream=None):
+    _call("rssm_advance_cursors", mode, _ptr(slot_wp), _ptr(slot_base), _ptr(slot_flush),
+          _ptr(cache_indices), _ptr(force_flush), _ptr(num_accepted), batch, num_slots, L, T,
+          _ptr(row_wp), _ptr(row_flush), _ptr(dev_err), _stream(stream))
+
+
+def rssm_ring_append(dims, x, dt_raw, dt_bias, dt_softplus, B, cache_indices, row_wp, ring_x,
+                     ring_dt, ring_B, dev_err=None, stream=None):
+    _call("rssm_ring_append", ctypes.byref(dims), _ptr(x), _ptr(dt_raw), _ptr(dt_bias),
+          int(dt_softplus), _ptr(B), _ptr(cache_indices), _ptr(row_wp), _ptr(ring_x),
+          _ptr(ring_dt), _ptr(ring_B), _ptr(dev_err), _stream(stream))
+
+
+def rssm_mamba2_workspace_size(dims):
+    return lib().rssm_mamba2_workspace_size(ctypes.byref(dims))
+
+
+def rssm_mamba2_precompute(dims, A, C, ring_dt, ring_B, cache_indices, row_wp, workspace,
+                           workspace_bytes, dev_err=None, stream=None):
+    _call("rssm_mamba2_precompute", ctypes.byref(dims), _ptr(A), _ptr(C), _ptr(ring_dt),
+          _ptr(ring_B), _ptr(cache_indices), _ptr(row_wp), _ptr(workspace), workspace_bytes,
+          _ptr(dev_err), _stream(stream))
+
+
+def rssm_mamba2_output(dims, state, C, D, z, ring_x, ring_B, cache_indices, row_wp, row_flush,
+                       workspace, workspace_bytes, y, dev_err=None, stream=None):
+    _call("rssm_mamba2_output", ctypes.byref(dims), _ptr(state), _ptr(C), _ptr(D), _ptr(z),
+          _ptr(ring_x), _ptr(ring_B), _ptr(cache_indices), _ptr(row_wp), _ptr(row_flush),
+          _ptr(workspace), workspace_bytes, _ptr(y), _ptr(dev_err), _stream(stream))
+
+
+def rssm_mamba2_decode(dims, state, A, C, D, z, ring_x, ring_dt, ring_B, cache_indices, row_wp,
+                       row_flush, workspace, workspace_bytes, y, dev_err=None, stream=None):
+    _call("rssm_mamba2_decode", ctypes.byref(dims), _ptr(state), _ptr(A), _ptr(C), _ptr(D),
+          _ptr(z), _ptr(ring_x), _ptr(ring_dt), _ptr(ring_B), _ptr(cache_indices), _ptr(row_wp),
+          _ptr(row_flush), _ptr(workspace), workspace_bytes, _ptr(y), _ptr(dev_err),
+          _stream(stream))
+
+
+def rssm_mamba2_full_state_update(dims, state, x, dt_raw, dt_bias, dt_softplus, A, B, C, D, z,
+                                  cache_indices, y, dev_err=None, stream=None):
+    _call("rssm_mamba2_full_state_update", ctypes.byref(dims), _ptr(state), _ptr(x),
+          _ptr(dt_raw), _ptr(dt_bias), int(dt_softplus), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+          _ptr(z), _ptr(cache_indices), _ptr(y), _ptr(dev_err), _stream(stream))
+
+
+def rssm_gdn_ring_append(dims, k, g, cache_indices, row_wp, ring_k, ring_g, dev_err=None,
+                         stream=None):
+    _call("rssm_gdn_ring_append", ctypes.byref(dims), _ptr(k), _ptr(g), _ptr(cache_indices),
+          _ptr(row_wp), _ptr(ring_k), _ptr(ring_g), _ptr(dev_err), _stream(stream))
+
+
+def rssm_gdn_workspace_size(dims):
+    return lib().rssm_gdn_workspace_size(ctypes.byref(dims))
+
+
+def rssm_gdn_precompute(dims, q, k, beta, g, ring_k, ring_g, cache_indices, row_wp, workspace,
+                        workspace_bytes, dev_err=None, stream=None):
+    _call("rssm_gdn_precompute", ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(beta), _ptr(g),
+          _ptr(ring_k), _ptr(ring_g), _ptr(cache_indices), _ptr(row_wp), _ptr(workspace),
+          workspace_bytes, _ptr(dev_err), _stream(stream))
+
+
+def rssm_gdn_output(dims, state, v, ring_k, ring_d, cache_indices, row_wp, row_flush, workspace,
+                    workspace_bytes, o, dev_err=None, stream=None):
+    _call("rssm_gdn_output", ctypes.byref(dims), _ptr(state), _ptr(v), _ptr(ring_k),
+          _ptr(ring_d), _ptr(cache_indices), _ptr(row_wp), _ptr(row_flush), _ptr(workspace),
+          workspace_bytes, _ptr(o), _ptr(dev_err), _stream(stream))
+
+
+def rssm_gdn_decode(dims, state, q, k, v, beta, g, ring_k, ring_g, ring_d, cache_indices, row_wp,
+                    row_flush, workspace, workspace_bytes, o, dev_err=None, stream=None):
+    _call("rssm_gdn_decode", ctypes.byref(dims), _ptr(state), _ptr(q), _ptr(k), _ptr(v),
+          _ptr(beta), _ptr(g), _ptr(ring_k), _ptr(ring_g), _ptr(ring_d), _ptr(cache_indices),
+          _ptr(row_wp), _ptr(row_flush), _ptr(workspace), workspace_bytes, _ptr(o),
+          _ptr(dev_err), _stream(stream))
+
+
+def rssm_gdn_full_state_decode(dims, state, q, k, v, beta, g, cache_indices, o, dev_err=None,
+                               stream=None):
+    _call("rssm_gdn_full_state_decode", ctypes.byref(dims), _ptr(state), _ptr(q), _ptr(k),
+          _ptr(v), _ptr(beta), _ptr(g), _ptr(cache_indices), _ptr(o), _ptr(dev_err),
+          _stream(stream))
+
+
+def rssm_gdn_spec_verify(dims, T, state, q, k, v, beta, g, ring_d, ring_k, ring_g, ring_v,
+                         ring_beta, cache_indices, slot_wp, slot_base, slot_flush, o,
+                         dev_err=None, stream=None):
+    _call("rssm_gdn_spec_verify", ctypes.byref(dims), T, _ptr(state), _ptr(q), _ptr(k), _ptr(v),
+          _ptr(beta), _ptr(g), _ptr(ring_d), _ptr(ring_k), _ptr(ring_g), _ptr(ring_v),
+          _ptr(ring_beta), _ptr(cache_indices), _ptr(slot_wp), _ptr(slot_base), _ptr(slot_flush),
+          _ptr(o), _ptr(dev_err), _stream(stream))

@@ -1,0 +1,206 @@
+// api.cu -- status strings, device facts, and the cursor kernel of librssm.
+//
+// The cursor kernel gives every decode row its ring write position and flush flag
+// on the device, so a captured step needs no host metadata ([M2] "ReplaySSM:
+// cache SSM inputs for faster Mamba2 standard decode", 实现拆解 item 3;
+// [GDN] "GDN ReplaySSM decode (Part A of RFC 28511)", 实现拆解 item 2; [SPEC]
+// "[GDN] Support ReplaySSM Ring Spec-Verify", 实现拆解 items 2 and 4; [FI]
+// "[Mamba] Add FlashInfer ReplaySSM backend", 实现拆解 item 1).
+#include <atomic>
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace rssm {
+
+namespace {
+constexpr int kMaxDevices = 64;
+DeviceInfo g_info[kMaxDevices];
+std::once_flag g_info_once[kMaxDevices];
+bool g_info_ok[kMaxDevices];
+
+struct SmemEntry {
+    const void* kernel;
+    int device;
+    int bytes;
+};
+std::mutex g_smem_mu;
+SmemEntry g_smem[512];
+int g_smem_n = 0;
+}  // namespace
+
+bool device_info(DeviceInfo* out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return false;
+    }
+    std::call_once(g_info_once[dev], [dev]() {
+        DeviceInfo d{};
+        bool ok = cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev) ==
+                      cudaSuccess &&
+                  cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin,
+                                         dev) == cudaSuccess &&
+                  cudaDeviceGetAttribute(&d.smem_per_sm,
+                                         cudaDevAttrMaxSharedMemoryPerMultiprocessor,
+                                         dev) == cudaSuccess;
+        if (!ok) cudaGetLastError();
+        g_info[dev] = d;
+        g_info_ok[dev] = ok;
+    });
+    *out = g_info[dev];
+    return g_info_ok[dev];
+}
+
+bool ensure_smem_limit(const void* kernel, int bytes) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    std::lock_guard<std::mutex> lk(g_smem_mu);
+    for (int i = 0; i < g_smem_n; ++i)
+        if (g_smem[i].kernel == kernel && g_smem[i].device == dev) {
+            if (g_smem[i].bytes >= bytes) return true;
+            if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+                cudaSuccess) {
+                cudaGetLastError();
+                return false;
+            }
+            g_smem[i].bytes = bytes;
+            return true;
+        }
+    if (cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes) !=
+        cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (g_smem_n < 512) g_smem[g_smem_n++] = SmemEntry{kernel, dev, bytes};
+    return true;
+}
+
+bool pick_pipe_shape(const DeviceInfo& di, int stage_bytes, int fixed_bytes, int max_stages,
+                     PipeShape* out) {
+    // 1 KB per resident CTA is reserved by the hardware.
+    for (int ctas = 2; ctas >= 1; --ctas) {
+        int budget = di.smem_per_sm / ctas - 1024;
+        if (budget > di.max_smem_optin) budget = di.max_smem_optin;
+        int st = (budget - fixed_bytes) / stage_bytes;
+        if (st > max_stages) st = max_stages;
+        const int need = ctas == 2 ? 3 : 2;
+        if (st >= need) {
+            out->stages = st;
+            out->ctas_per_sm = ctas;
+            out->smem_bytes = fixed_bytes + st * stage_bytes;
+            return true;
+        }
+    }
+    return false;
+}
+
+// ----------------------------------------------------------------------------
+// cursor kernel
+// ----------------------------------------------------------------------------
+
+__global__ void cursor_kernel(int mode, int32_t* __restrict__ slot_wp, int32_t* __restrict__ slot_base,
+                              uint8_t* __restrict__ slot_flush, const int32_t* __restrict__ ci,
+                              const uint8_t* __restrict__ force, const int32_t* __restrict__ acc,
+                              int batch, int num_slots, int L, int T, int32_t* __restrict__ row_wp,
+                              uint8_t* __restrict__ row_flush, int32_t* __restrict__ dev_err) {
+    const int b = blockIdx.x * blockDim.x + threadIdx.x;
+    if (b >= batch) return;
+    const int s = ci[b];
+    if (s < 0) {
+        if (mode == RSSM_CURSOR_STANDARD) {
+            row_wp[b] = 0;
+            row_flush[b] = 0;
+        }
+        return;
+    }
+    if (s >= num_slots) {
+        set_dev_err(dev_err, RSSM_DEVERR_SLOT);
+        if (mode == RSSM_CURSOR_STANDARD) {
+            row_wp[b] = 0;
+            row_flush[b] = 0;
+        }
+        return;
+    }
+    if (mode == RSSM_CURSOR_STANDARD) {
+        const int w = slot_wp[s];
+        if (w < 0 || w >= L) {
+            set_dev_err(dev_err, RSSM_DEVERR_CURSOR);
+            row_wp[b] = 0;
+            row_flush[b] = 0;
+            return;
+        }
+        const int f = (w == L - 1) || (force != nullptr && force[b] != 0);
+        row_wp[b] = w;
+        row_flush[b] = static_cast<uint8_t>(f);
+        slot_wp[s] = f ? 0 : w + 1;
+    } else if (mode == RSSM_CURSOR_SPEC_COMMIT) {
+        int cnt = slot_wp[s];
+        int base = slot_base[s];
+        const int a = acc[b];
+        if (cnt < 0 || cnt > L || base < 0 || base >= L || a < 0 || a > T) {
+            set_dev_err(dev_err, RSSM_DEVERR_CURSOR);
+            return;
+        }
+        if (slot_flush[s]) {
+            base = (base + cnt) % L;
+            cnt = 0;
+        }
+        cnt += a;
+        const int f = cnt + T > L;
+        slot_wp[s] = cnt;
+        slot_base[s] = base;
+        slot_flush[s] = static_cast<uint8_t>(f);
+        if (row_wp) row_wp[b] = cnt;
+        if (row_flush) row_flush[b] = static_cast<uint8_t>(f);
+    } else {  // RESET
+        slot_wp[s] = 0;
+        if (slot_base) slot_base[s] = 0;
+        if (slot_flush) slot_flush[s] = 0;
+    }
+}
+
+}  // namespace rssm
+
+using namespace rssm;
+
+extern "C" const char* rssm_status_string(int status) {
+    switch (status) {
+        case RSSM_OK: return "ok";
+        case RSSM_ERR_INVALID_ARG: return "invalid argument (null or misaligned pointer, bad enum or size)";
+        case RSSM_ERR_UNSUPPORTED: return "unsupported shape or dtype for this build";
+        case RSSM_ERR_CONFIG: return "inconsistent configuration";
+        case RSSM_ERR_CUDA: return "CUDA launch error";
+        default: return "unknown status";
+    }
+}
+
+extern "C" int rssm_abi_version(void) { return RSSM_ABI_VERSION; }
+
+extern "C" int rssm_advance_cursors(int mode, int32_t* slot_wp, int32_t* slot_base,
+                                    uint8_t* slot_flush, const int32_t* cache_indices,
+                                    const uint8_t* force_flush, const int32_t* num_accepted,
+                                    int32_t batch, int32_t num_slots, int32_t L, int32_t T,
+                                    int32_t* row_wp, uint8_t* row_flush, int32_t* dev_err,
+                                    rssm_stream_t stream) {
+    if (batch < 0 || num_slots < 0) return RSSM_ERR_INVALID_ARG;
+    if (mode != RSSM_CURSOR_STANDARD && mode != RSSM_CURSOR_SPEC_COMMIT && mode != RSSM_CURSOR_RESET)
+        return RSSM_ERR_INVALID_ARG;
+    if (L < 1) return RSSM_ERR_CONFIG;
+    if (batch == 0) return RSSM_OK;
+    if (!slot_wp || !cache_indices) return RSSM_ERR_INVALID_ARG;
+    if (mode == RSSM_CURSOR_STANDARD && (!row_wp || !row_flush)) return RSSM_ERR_INVALID_ARG;
+    if (mode == RSSM_CURSOR_SPEC_COMMIT) {
+        if (!slot_base || !slot_flush || !num_accepted) return RSSM_ERR_INVALID_ARG;
+        if (T < 1 || L < 2 * T) return RSSM_ERR_CONFIG;
+    }
+    const int threads = 256;
+    cursor_kernel<<<(batch + threads - 1) / threads, threads, 0, (cudaStream_t)stream>>>(
+        mode, slot_wp, slot_base, slot_flush, cache_indices, force_flush, num_accepted, batch,
+        num_slots, L, T, row_wp, row_flush, dev_err);
+    return launch_status();
+}

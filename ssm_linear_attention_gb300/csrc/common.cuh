@@ -1,0 +1,208 @@
+// common.cuh -- device helpers shared by the ReplaySSM kernels (sm_103a).
+//
+// * 1-D TMA bulk copies (cp.async.bulk) global -> shared, completing on an
+//   mbarrier transaction count; no cluster multicast anywhere.
+// * mbarrier waits bounded by %globaltimer: a wait that does not complete within
+//   RSSM_WAIT_NS sets RSSM_DEVERR_TIMEOUT and the kernel winds down instead of
+//   spinning forever.
+// * bfloat16 <-> float32 packing (bf16 is the top half of a float32; widening is
+//   exact, narrowing uses the round-to-nearest-even intrinsic).
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "rssm.h"
+
+#define RSSM_WAIT_NS 2000000000ull  // 2 s
+
+namespace rssm {
+
+// ----------------------------------------------------------------------------
+// shared-memory addresses, mbarriers, bulk copies
+// ----------------------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+}
+
+// Make barrier initialisation visible to the async (TMA) proxy.
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Wait for phase `parity` of `bar` to complete; false when RSSM_WAIT_NS elapsed.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if (global_ns() - t0 > RSSM_WAIT_NS) return false;
+    }
+}
+
+// L2 policy: the checkpoint tiles are read once per step; let them leave L2
+// first so rings, tables and per-row inputs stay resident.
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// 1-D bulk copy global -> shared, completion counted on `bar` (bytes % 16 == 0,
+// both addresses 16-byte aligned).
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32_t bytes,
+                                              uint64_t* bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], "
+        "%2, [%3], %4;" ::"r"(smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ void set_dev_err(int32_t* dev_err, int bit) {
+    if (dev_err) atomicOr(dev_err, bit);
+}
+
+// ----------------------------------------------------------------------------
+// bfloat16 / float32 element access
+// ----------------------------------------------------------------------------
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xFFFF0000u); }
+__device__ __forceinline__ float bf16_to_f(uint16_t v) { return __uint_as_float(uint32_t(v) << 16); }
+
+__device__ __forceinline__ uint16_t f_to_bf16(float f) {
+    return __bfloat16_as_ushort(__float2bfloat16_rn(f));
+}
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+    return uint32_t(f_to_bf16(lo)) | (uint32_t(f_to_bf16(hi)) << 16);
+}
+
+// Load 8 consecutive elements (bf16 when is_bf16, else f32) starting at p (16-byte
+// aligned for bf16, 32-byte for f32) into f[0..7].
+__device__ __forceinline__ void load8(const void* p, bool is_bf16, float* f) {
+    if (is_bf16) {
+        const uint4 v = *reinterpret_cast<const uint4*>(p);
+        f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x); f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+        f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z); f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
+    } else {
+        const float4 a = reinterpret_cast<const float4*>(p)[0];
+        const float4 b = reinterpret_cast<const float4*>(p)[1];
+        f[0] = a.x; f[1] = a.y; f[2] = a.z; f[3] = a.w; f[4] = b.x; f[5] = b.y; f[6] = b.z; f[7] = b.w;
+    }
+}
+
+__device__ __forceinline__ void store8(void* p, bool is_bf16, const float* f) {
+    if (is_bf16) {
+        uint4 v;
+        v.x = pack_bf16x2(f[0], f[1]); v.y = pack_bf16x2(f[2], f[3]);
+        v.z = pack_bf16x2(f[4], f[5]); v.w = pack_bf16x2(f[6], f[7]);
+        *reinterpret_cast<uint4*>(p) = v;
+    } else {
+        reinterpret_cast<float4*>(p)[0] = make_float4(f[0], f[1], f[2], f[3]);
+        reinterpret_cast<float4*>(p)[1] = make_float4(f[4], f[5], f[6], f[7]);
+    }
+}
+
+__device__ __forceinline__ float load1(const void* base, long idx, bool is_bf16) {
+    return is_bf16 ? bf16_to_f(reinterpret_cast<const uint16_t*>(base)[idx])
+                   : reinterpret_cast<const float*>(base)[idx];
+}
+
+__device__ __forceinline__ void store1(void* base, long idx, bool is_bf16, float v) {
+    if (is_bf16) reinterpret_cast<uint16_t*>(base)[idx] = f_to_bf16(v);
+    else reinterpret_cast<float*>(base)[idx] = v;
+}
+
+// State element types for templated kernels.
+struct StF32 {
+    static constexpr int bytes = 4;
+    static constexpr bool bf16 = false;
+};
+struct StBF16 {
+    static constexpr int bytes = 2;
+    static constexpr bool bf16 = true;
+};
+
+// softplus(x) = log(1 + e^x); above 20 the correction is below float32 resolution.
+__device__ __forceinline__ float softplus_f(float x) { return x > 20.f ? x : log1pf(expf(x)); }
+
+__device__ __forceinline__ float silu_f(float z) { return z / (1.f + expf(-z)); }
+
+// ----------------------------------------------------------------------------
+// warp reduce-scatter
+// ----------------------------------------------------------------------------
+
+// `v[0..CNT)` holds partial sums on each lane of a group of GRP consecutive lanes
+// (GRP a power of two <= 32, CNT a power of two <= GRP). Afterwards v[0] on every
+// lane holds the group total of entry index `out_idx` (returned), where lanes
+// whose low bits (below GRP/CNT) differ hold the same entry.
+template <int CNT, int GRP>
+__device__ __forceinline__ int reduce_scatter(float* v) {
+    static_assert((CNT & (CNT - 1)) == 0 && (GRP & (GRP - 1)) == 0 && CNT <= GRP, "shape");
+    const int lane = threadIdx.x & 31;
+    int idx = 0;
+    int c = CNT;
+#pragma unroll
+    for (int o = GRP / 2; o >= 1; o >>= 1) {
+        if (c > 1) {
+            const bool upper = (lane & o) != 0;
+            const int h = c / 2;
+#pragma unroll
+            for (int i = 0; i < CNT / 2; ++i) {
+                if (i < h) {
+                    const float send = upper ? v[i] : v[i + h];
+                    const float keep = upper ? v[i + h] : v[i];
+                    v[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                }
+            }
+            if (upper) idx += h;
+            c = h;
+        } else {
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], o);
+        }
+    }
+    return idx;
+}
+
+}  // namespace rssm

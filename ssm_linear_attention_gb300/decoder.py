@@ -1,0 +1,295 @@
+"""Decode-step runners over the C ABI.
+
+Each runner owns the device buffers of one layer's ReplaySSM state on the current
+CUDA device (allocated with torch: the slot-indexed checkpoint pool, the input
+rings, the per-slot cursors, the per-row cursor outputs, the workspace), and a
+step is the sequence of librssm calls the method needs, in stream order:
+
+  Mamba2 decode:  rssm_advance_cursors (STANDARD) -> rssm_ring_append ->
+                  rssm_mamba2_precompute -> rssm_mamba2_output
+  GDN decode:     rssm_advance_cursors (STANDARD) -> rssm_gdn_ring_append ->
+                  rssm_gdn_precompute -> rssm_gdn_output
+  GDN spec:       rssm_gdn_spec_verify (fold + verify), then
+                  rssm_advance_cursors (SPEC_COMMIT) with the accepted counts
+
+No host synchronisation happens inside a step, so a step can be captured in a
+CUDA graph. Several layers that share slots can share one cursor advance
+(``advance=False`` on all but one layer, with ``row_wp`` / ``row_flush`` shared).
+"""
+import torch
+
+from . import _binding as B
+
+__all__ = ["torch_dtype_code", "Mamba2ReplayDecoder", "Mamba2FullStateDecoder",
+           "GDNReplayDecoder", "GDNFullStateDecoder", "GDNSpecVerifier"]
+
+
+def torch_dtype_code(dt: torch.dtype) -> int:
+    if dt == torch.float32:
+        return B.RSSM_F32
+    if dt == torch.bfloat16:
+        return B.RSSM_BF16
+    raise TypeError("unsupported dtype %s (float32 or bfloat16)" % dt)
+
+
+class Mamba2ReplayDecoder:
+    """ReplaySSM Mamba2 decode for one layer.
+
+    Buffers: state [num_slots, H, P, N] (state_dtype), ring_x [num_slots, H, L, P],
+    ring_dt [num_slots, H, L] float32, ring_B [num_slots, G, L, N], slot_wp
+    [num_slots] int32, and per-row row_wp / row_flush / workspace / y for up to
+    max_batch rows."""
+
+    def __init__(self, nheads, headdim, dstate, ngroups, ring_len, num_slots, max_batch, A, D,
+                 dt_bias=None, dt_softplus=True, state_dtype=torch.bfloat16,
+                 act_dtype=torch.bfloat16, out_dtype=torch.bfloat16, device=None):
+        dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+        self.H, self.P, self.N, self.G, self.L = nheads, headdim, dstate, ngroups, ring_len
+        self.num_slots, self.max_batch = num_slots, max_batch
+        self.state_dtype, self.act_dtype, self.out_dtype = state_dtype, act_dtype, out_dtype
+        self.dt_softplus = dt_softplus
+        f32 = dict(device=dev, dtype=torch.float32)
+        self.A = torch.as_tensor(A, **f32).contiguous()
+        self.D = torch.as_tensor(D, **f32).contiguous()
+        self.dt_bias = None if dt_bias is None else torch.as_tensor(dt_bias, **f32).contiguous()
+        self.state = torch.zeros(num_slots, nheads, headdim, dstate, device=dev, dtype=state_dtype)
+        self.ring_x = torch.zeros(num_slots, nheads, ring_len, headdim, device=dev, dtype=act_dtype)
+        self.ring_dt = torch.zeros(num_slots, nheads, ring_len, **f32)
+        self.ring_B = torch.zeros(num_slots, ngroups, ring_len, dstate, device=dev, dtype=act_dtype)
+        self.slot_wp = torch.zeros(num_slots, device=dev, dtype=torch.int32)
+        self.row_wp = torch.zeros(max_batch, device=dev, dtype=torch.int32)
+        self.row_flush = torch.zeros(max_batch, device=dev, dtype=torch.uint8)
+        self.dev_err = torch.zeros(4, device=dev, dtype=torch.int32)
+        self.ws_bytes = B.rssm_mamba2_workspace_size(self.dims(max_batch))
+        self.workspace = torch.empty(max(self.ws_bytes, 16), device=dev, dtype=torch.uint8)
+        self.y = torch.empty(max_batch, nheads, headdim, device=dev, dtype=out_dtype)
+
+    def dims(self, batch):
+        return B.Mamba2Dims(batch, self.H, self.P, self.N, self.G, self.L, self.num_slots,
+                            torch_dtype_code(self.state_dtype), torch_dtype_code(self.act_dtype),
+                            torch_dtype_code(self.out_dtype))
+
+    # individual stages (bench.py times them separately)
+    def advance(self, cache_indices, force_flush=None, stream=None):
+        b = cache_indices.shape[0]
+        B.rssm_advance_cursors(B.RSSM_CURSOR_STANDARD, self.slot_wp, None, None, cache_indices,
+                               force_flush, None, b, self.num_slots, self.L, 0, self.row_wp,
+                               self.row_flush, self.dev_err, stream)
+
+    def append(self, x, dt_raw, Bm, cache_indices, stream=None):
+        B.rssm_ring_append(self.dims(x.shape[0]), x, dt_raw, self.dt_bias, self.dt_softplus, Bm,
+                           cache_indices, self.row_wp, self.ring_x, self.ring_dt, self.ring_B,
+                           self.dev_err, stream)
+
+    def precompute(self, C, cache_indices, stream=None):
+        B.rssm_mamba2_precompute(self.dims(C.shape[0]), self.A, C, self.ring_dt, self.ring_B,
+                                 cache_indices, self.row_wp, self.workspace, self.ws_bytes,
+                                 self.dev_err, stream)
+
+    def output(self, C, z, cache_indices, y=None, stream=None):
+        b = C.shape[0]
+        y = self.y[:b] if y is None else y
+        B.rssm_mamba2_output(self.dims(b), self.state, C, self.D, z, self.ring_x, self.ring_B,
+                             cache_indices, self.row_wp, self.row_flush, self.workspace,
+                             self.ws_bytes, y, self.dev_err, stream)
+        return y
+
+    def step(self, x, dt_raw, Bm, C, z, cache_indices, force_flush=None, y=None, stream=None,
+             advance=True):
+        """One decode step for rows cache_indices (padding rows: -1). Returns y [b, H, P]."""
+        if advance:
+            self.advance(cache_indices, force_flush, stream)
+        self.append(x, dt_raw, Bm, cache_indices, stream)
+        self.precompute(C, cache_indices, stream)
+        return self.output(C, z, cache_indices, y, stream)
+
+    def reset_slots(self, slots, stream=None):
+        B.rssm_advance_cursors(B.RSSM_CURSOR_RESET, self.slot_wp, None, None, slots, None, None,
+                               slots.shape[0], self.num_slots, self.L, 0, None, None, self.dev_err,
+                               stream)
+
+
+class Mamba2FullStateDecoder:
+    """The conventional Mamba2 decode step (whole state read and written every step)."""
+
+    def __init__(self, nheads, headdim, dstate, ngroups, num_slots, max_batch, A, D, dt_bias=None,
+                 dt_softplus=True, state_dtype=torch.bfloat16, act_dtype=torch.bfloat16,
+                 out_dtype=torch.bfloat16, device=None):
+        dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+        self.H, self.P, self.N, self.G = nheads, headdim, dstate, ngroups
+        self.num_slots = num_slots
+        self.state_dtype, self.act_dtype, self.out_dtype = state_dtype, act_dtype, out_dtype
+        self.dt_softplus = dt_softplus
+        f32 = dict(device=dev, dtype=torch.float32)
+        self.A = torch.as_tensor(A, **f32).contiguous()
+        self.D = torch.as_tensor(D, **f32).contiguous()
+        self.dt_bias = None if dt_bias is None else torch.as_tensor(dt_bias, **f32).contiguous()
+        self.state = torch.zeros(num_slots, nheads, headdim, dstate, device=dev, dtype=state_dtype)
+        self.dev_err = torch.zeros(4, device=dev, dtype=torch.int32)
+        self.y = torch.empty(max_batch, nheads, headdim, device=dev, dtype=out_dtype)
+
+    def dims(self, batch):
+        return B.Mamba2Dims(batch, self.H, self.P, self.N, self.G, 1, self.num_slots,
+                            torch_dtype_code(self.state_dtype), torch_dtype_code(self.act_dtype),
+                            torch_dtype_code(self.out_dtype))
+
+    def step(self, x, dt_raw, Bm, C, z, cache_indices, y=None, stream=None):
+        b = x.shape[0]
+        y = self.y[:b] if y is None else y
+        B.rssm_mamba2_full_state_update(self.dims(b), self.state, x, dt_raw, self.dt_bias,
+                                        self.dt_softplus, self.A, Bm, C, self.D, z, cache_indices,
+                                        y, self.dev_err, stream)
+        return y
+
+
+class GDNReplayDecoder:
+    """ReplaySSM gated-delta-net decode for one layer.
+
+    Buffers: state [num_slots, HV, V, K] float32, ring_d [num_slots, HV, L, V]
+    float32, ring_k [num_slots, HK, L, K] (act dtype), ring_g [num_slots, HV, L]
+    float32, slot_wp [num_slots] int32."""
+
+    def __init__(self, num_v_heads, num_k_heads, head_k_dim, head_v_dim, ring_len, num_slots,
+                 max_batch, act_dtype=torch.bfloat16, out_dtype=torch.bfloat16, device=None):
+        dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+        self.HV, self.HK, self.K, self.V, self.L = (num_v_heads, num_k_heads, head_k_dim,
+                                                    head_v_dim, ring_len)
+        self.num_slots, self.max_batch = num_slots, max_batch
+        self.act_dtype, self.out_dtype = act_dtype, out_dtype
+        f32 = dict(device=dev, dtype=torch.float32)
+        self.state = torch.zeros(num_slots, num_v_heads, head_v_dim, head_k_dim, **f32)
+        self.ring_d = torch.zeros(num_slots, num_v_heads, ring_len, head_v_dim, **f32)
+        self.ring_k = torch.zeros(num_slots, num_k_heads, ring_len, head_k_dim, device=dev,
+                                  dtype=act_dtype)
+        self.ring_g = torch.zeros(num_slots, num_v_heads, ring_len, **f32)
+        self.slot_wp = torch.zeros(num_slots, device=dev, dtype=torch.int32)
+        self.row_wp = torch.zeros(max_batch, device=dev, dtype=torch.int32)
+        self.row_flush = torch.zeros(max_batch, device=dev, dtype=torch.uint8)
+        self.dev_err = torch.zeros(4, device=dev, dtype=torch.int32)
+        self.ws_bytes = B.rssm_gdn_workspace_size(self.dims(max_batch))
+        self.workspace = torch.empty(max(self.ws_bytes, 16), device=dev, dtype=torch.uint8)
+        self.o = torch.empty(max_batch, num_v_heads, head_v_dim, device=dev, dtype=out_dtype)
+
+    def dims(self, batch):
+        return B.GDNDims(batch, self.HV, self.HK, self.K, self.V, self.L, self.num_slots,
+                         torch_dtype_code(self.act_dtype), torch_dtype_code(self.out_dtype))
+
+    def advance(self, cache_indices, force_flush=None, stream=None):
+        b = cache_indices.shape[0]
+        B.rssm_advance_cursors(B.RSSM_CURSOR_STANDARD, self.slot_wp, None, None, cache_indices,
+                               force_flush, None, b, self.num_slots, self.L, 0, self.row_wp,
+                               self.row_flush, self.dev_err, stream)
+
+    def append(self, k, g, cache_indices, stream=None):
+        B.rssm_gdn_ring_append(self.dims(k.shape[0]), k, g, cache_indices, self.row_wp,
+                               self.ring_k, self.ring_g, self.dev_err, stream)
+
+    def precompute(self, q, k, beta, g, cache_indices, stream=None):
+        B.rssm_gdn_precompute(self.dims(q.shape[0]), q, k, beta, g, self.ring_k, self.ring_g,
+                              cache_indices, self.row_wp, self.workspace, self.ws_bytes,
+                              self.dev_err, stream)
+
+    def output(self, v, cache_indices, o=None, stream=None):
+        b = v.shape[0]
+        o = self.o[:b] if o is None else o
+        B.rssm_gdn_output(self.dims(b), self.state, v, self.ring_k, self.ring_d, cache_indices,
+                          self.row_wp, self.row_flush, self.workspace, self.ws_bytes, o,
+                          self.dev_err, stream)
+        return o
+
+    def step(self, q, k, v, beta, g, cache_indices, force_flush=None, o=None, stream=None,
+             advance=True):
+        if advance:
+            self.advance(cache_indices, force_flush, stream)
+        self.append(k, g, cache_indices, stream)
+        self.precompute(q, k, beta, g, cache_indices, stream)
+        return self.output(v, cache_indices, o, stream)
+
+    def reset_slots(self, slots, stream=None):
+        B.rssm_advance_cursors(B.RSSM_CURSOR_RESET, self.slot_wp, None, None, slots, None, None,
+                               slots.shape[0], self.num_slots, self.L, 0, None, None, self.dev_err,
+                               stream)
+
+
+class GDNFullStateDecoder:
+    """The conventional gated-delta-net decode step (state read and written every step)."""
+
+    def __init__(self, num_v_heads, num_k_heads, head_k_dim, head_v_dim, num_slots, max_batch,
+                 act_dtype=torch.bfloat16, out_dtype=torch.bfloat16, device=None):
+        dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+        self.HV, self.HK, self.K, self.V = num_v_heads, num_k_heads, head_k_dim, head_v_dim
+        self.num_slots = num_slots
+        self.act_dtype, self.out_dtype = act_dtype, out_dtype
+        self.state = torch.zeros(num_slots, num_v_heads, head_v_dim, head_k_dim, device=dev,
+                                 dtype=torch.float32)
+        self.dev_err = torch.zeros(4, device=dev, dtype=torch.int32)
+        self.o = torch.empty(max_batch, num_v_heads, head_v_dim, device=dev, dtype=out_dtype)
+
+    def dims(self, batch):
+        return B.GDNDims(batch, self.HV, self.HK, self.K, self.V, 1, self.num_slots,
+                         torch_dtype_code(self.act_dtype), torch_dtype_code(self.out_dtype))
+
+    def step(self, q, k, v, beta, g, cache_indices, o=None, stream=None):
+        b = q.shape[0]
+        o = self.o[:b] if o is None else o
+        B.rssm_gdn_full_state_decode(self.dims(b), self.state, q, k, v, beta, g, cache_indices, o,
+                                     self.dev_err, stream)
+        return o
+
+
+class GDNSpecVerifier:
+    """ReplaySSM speculative verify for the gated delta net (linear draft chain of T).
+
+    Buffers: state [num_slots, HV, V, K] float32; rings d [.., HV, L, V] f32,
+    k [.., HK, L, K], g [.., HV, L] f32, raw v [.., HV, L, V], beta [.., HV, L] f32;
+    per-slot cursors cnt (slot_wp), base, flush."""
+
+    def __init__(self, num_v_heads, num_k_heads, head_k_dim, head_v_dim, ring_len, T, num_slots,
+                 max_batch, act_dtype=torch.bfloat16, out_dtype=torch.bfloat16, device=None):
+        dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+        self.HV, self.HK, self.K, self.V, self.L, self.T = (num_v_heads, num_k_heads, head_k_dim,
+                                                           head_v_dim, ring_len, T)
+        self.num_slots = num_slots
+        self.act_dtype, self.out_dtype = act_dtype, out_dtype
+        f32 = dict(device=dev, dtype=torch.float32)
+        self.state = torch.zeros(num_slots, num_v_heads, head_v_dim, head_k_dim, **f32)
+        self.ring_d = torch.zeros(num_slots, num_v_heads, ring_len, head_v_dim, **f32)
+        self.ring_k = torch.zeros(num_slots, num_k_heads, ring_len, head_k_dim, device=dev,
+                                  dtype=act_dtype)
+        self.ring_g = torch.zeros(num_slots, num_v_heads, ring_len, **f32)
+        self.ring_v = torch.zeros(num_slots, num_v_heads, ring_len, head_v_dim, device=dev,
+                                  dtype=act_dtype)
+        self.ring_beta = torch.zeros(num_slots, num_v_heads, ring_len, **f32)
+        self.slot_cnt = torch.zeros(num_slots, device=dev, dtype=torch.int32)
+        self.slot_base = torch.zeros(num_slots, device=dev, dtype=torch.int32)
+        self.slot_flush = torch.zeros(num_slots, device=dev, dtype=torch.uint8)
+        self.row_cnt = torch.zeros(max_batch, device=dev, dtype=torch.int32)
+        self.row_flush = torch.zeros(max_batch, device=dev, dtype=torch.uint8)
+        self.dev_err = torch.zeros(4, device=dev, dtype=torch.int32)
+        self.o = torch.empty(max_batch, T, num_v_heads, head_v_dim, device=dev, dtype=out_dtype)
+
+    def dims(self, batch):
+        return B.GDNDims(batch, self.HV, self.HK, self.K, self.V, self.L, self.num_slots,
+                         torch_dtype_code(self.act_dtype), torch_dtype_code(self.out_dtype))
+
+    def verify(self, q, k, v, beta, g, cache_indices, o=None, stream=None):
+        """Per-draft outputs o [b, T, HV, V] for draft inputs [b, T, ...]."""
+        b = q.shape[0]
+        o = self.o[:b] if o is None else o
+        B.rssm_gdn_spec_verify(self.dims(b), self.T, self.state, q, k, v, beta, g, self.ring_d,
+                               self.ring_k, self.ring_g, self.ring_v, self.ring_beta,
+                               cache_indices, self.slot_cnt, self.slot_base, self.slot_flush, o,
+                               self.dev_err, stream)
+        return o
+
+    def commit(self, cache_indices, num_accepted, stream=None):
+        b = cache_indices.shape[0]
+        B.rssm_advance_cursors(B.RSSM_CURSOR_SPEC_COMMIT, self.slot_cnt, self.slot_base,
+                               self.slot_flush, cache_indices, None, num_accepted, b,
+                               self.num_slots, self.L, self.T, self.row_cnt[:b], self.row_flush[:b],
+                               self.dev_err, stream)
+
+    def reset_slots(self, slots, stream=None):
+        B.rssm_advance_cursors(B.RSSM_CURSOR_RESET, self.slot_cnt, self.slot_base,
+                               self.slot_flush, slots, None, None, slots.shape[0], self.num_slots,
+                               self.L, self.T, None, None, self.dev_err, stream)

@@ -1,0 +1,112 @@
+"""The C-ABI library loads, exports every symbol include/rssm.h declares, and
+rejects bad arguments on the host before any launch (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import ssm_linear_attention_gb300 as ssm
+from ssm_linear_attention_gb300 import _binding as B
+from ssm_linear_attention_gb300 import build as rbuild
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include",
+                      "rssm.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    rbuild.build()
+    return ssm.lib()
+
+
+def declared_symbols():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(rssm_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_and_binding_agree():
+    assert declared_symbols() == sorted(B.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    raw = ctypes.CDLL(B.LIB_PATH)
+    for name in declared_symbols():
+        assert hasattr(raw, name), name
+
+
+def test_abi_version_and_status_strings(lib):
+    assert ssm.rssm_abi_version() == 1
+    for st in range(5):
+        assert ssm.rssm_status_string(st)
+    assert ssm.rssm_status_string(99) == "unknown status"
+
+
+def _m2(**kw):
+    d = dict(batch=4, nheads=8, headdim=64, dstate=128, ngroups=2, ring_len=4, num_slots=8,
+             state_dtype=B.RSSM_BF16, act_dtype=B.RSSM_BF16, out_dtype=B.RSSM_F32)
+    d.update(kw)
+    return B.Mamba2Dims(**d)
+
+
+FAKE = 0x10000  # aligned non-null address; never dereferenced (validation fails first)
+
+
+def _rc(name, *args):
+    return getattr(ssm.lib(), name)(*args)
+
+
+def test_cursor_validation(lib):
+    L = ssm.lib()
+    assert L.rssm_advance_cursors(9, FAKE, None, None, FAKE, None, None, 4, 8, 4, 0, FAKE, FAKE,
+                                  None, None) == B.RSSM_ERR_INVALID_ARG
+    assert L.rssm_advance_cursors(0, FAKE, None, None, FAKE, None, None, 4, 8, 0, 0, FAKE, FAKE,
+                                  None, None) == B.RSSM_ERR_CONFIG
+    assert L.rssm_advance_cursors(0, None, None, None, FAKE, None, None, 4, 8, 4, 0, FAKE, FAKE,
+                                  None, None) == B.RSSM_ERR_INVALID_ARG
+    assert L.rssm_advance_cursors(0, FAKE, None, None, FAKE, None, None, 4, 8, 4, 0, None, FAKE,
+                                  None, None) == B.RSSM_ERR_INVALID_ARG
+    # spec commit: ring must hold twice the drafts
+    assert L.rssm_advance_cursors(1, FAKE, FAKE, FAKE, FAKE, None, FAKE, 4, 8, 7, 4, None, None,
+                                  None, None) == B.RSSM_ERR_CONFIG
+    assert L.rssm_advance_cursors(1, FAKE, None, FAKE, FAKE, None, FAKE, 4, 8, 8, 4, None, None,
+                                  None, None) == B.RSSM_ERR_INVALID_ARG
+    # empty batch is a no-op, even with null buffers
+    assert L.rssm_advance_cursors(0, None, None, None, None, None, None, 0, 8, 4, 0, None, None,
+                                  None, None) == B.RSSM_OK
+
+
+def test_mamba2_validation(lib):
+    d = _m2()
+    by = ctypes.byref
+    assert B.rssm_mamba2_workspace_size(d) == 4 * 8 * 12 * 4
+    assert B.rssm_mamba2_workspace_size(_m2(ngroups=3)) == 0
+    # shapes
+    for bad, code in [(dict(ngroups=3), B.RSSM_ERR_CONFIG), (dict(ring_len=0), B.RSSM_ERR_CONFIG),
+                      (dict(headdim=32), B.RSSM_ERR_UNSUPPORTED),
+                      (dict(dstate=96), B.RSSM_ERR_UNSUPPORTED),
+                      (dict(state_dtype=7), B.RSSM_ERR_INVALID_ARG),
+                      (dict(batch=-1), B.RSSM_ERR_INVALID_ARG)]:
+        dd = _m2(**bad)
+        assert _rc("rssm_ring_append", by(dd), FAKE, FAKE, None, 1, FAKE, FAKE, FAKE, FAKE, FAKE,
+                   FAKE, None, None) == code
+        assert _rc("rssm_mamba2_output", by(dd), FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE,
+                   FAKE, FAKE, 1 << 20, FAKE, None, None) == code
+    # null / misaligned pointers
+    assert _rc("rssm_ring_append", by(d), None, FAKE, None, 1, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+               None, None) == B.RSSM_ERR_INVALID_ARG
+    assert _rc("rssm_mamba2_output", by(d), FAKE + 4, FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE,
+               FAKE, FAKE, 1 << 20, FAKE, None, None) == B.RSSM_ERR_INVALID_ARG
+    # workspace too small
+    assert _rc("rssm_mamba2_decode", by(d), FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE,
+               FAKE, FAKE, FAKE, 16, FAKE, None, None) == B.RSSM_ERR_INVALID_ARG
+    assert _rc("rssm_mamba2_full_state_update", by(d), FAKE, FAKE, FAKE, None, 1, FAKE, FAKE, None,
+               FAKE, None, FAKE, FAKE, None, None) == B.RSSM_ERR_INVALID_ARG
+
+
+def test_binding_raises_with_status(lib):
+    with pytest.raises(ssm.RSSMError) as ei:
+        ssm.rssm_advance_cursors(0, FAKE, None, None, FAKE, None, None, 4, 8, 0, 0, FAKE, FAKE,
+                                 None, stream=0)
+    assert ei.value.status == B.RSSM_ERR_CONFIG
