@@ -285,8 +285,9 @@ int rssm_gdn_precompute(const rssm_gdn_dims* dims, const void* q, const void* k,
  *   u   = Gu a + sum_{i<w} gamma_i kk_i d_i       (= S_{t-1} k_t)
  *   d_t = beta_t (v_t - g_t u)                     (written to ring_d entry w)
  *   o   = Go c + sum_{i<w} Gamma_i kq_i d_i + kq_t d_t
- * and on flush rows stores S = Go S0 + sum_{i<=w} Gamma_i d_i k_i^T. */
-int rssm_gdn_output(const rssm_gdn_dims* dims, float* state, const void* v,
+ * and on flush rows stores S = Go S0 + sum_{i<=w} Gamma_i d_i k_i^T. k_t is read
+ * from ring_k entry w (rssm_gdn_ring_append), q_t from q [batch][HK][K]. */
+int rssm_gdn_output(const rssm_gdn_dims* dims, float* state, const void* q, const void* v,
                     const void* ring_k, float* ring_d, const int32_t* cache_indices,
                     const int32_t* row_wp, const uint8_t* row_flush, const void* workspace,
                     size_t workspace_bytes, void* o, int32_t* dev_err, rssm_stream_t stream);
@@ -309,34 +310,48 @@ int rssm_gdn_full_state_decode(const rssm_gdn_dims* dims, float* state, const vo
 /* Gated delta net: speculative verify                                        */
 /* ------------------------------------------------------------------------- */
 
+/* Bytes of device workspace rssm_gdn_spec_verify needs for T drafts (per-(row,
+ * value head) coefficient tables, float32). 0 for invalid dims or T. */
+size_t rssm_gdn_spec_workspace_size(const rssm_gdn_dims* dims, int32_t T);
+
 /* rssm_gdn_spec_verify -- score a linear chain of T draft tokens per row from the
  * checkpoint and the circular ring, without materialising per-draft states
  * ([SPEC] 实现拆解 item 3, gdn_replayssm_spec_circular_kernel), after first
  * folding, for slots whose fold is pending, the committed entries into the
  * checkpoint by replaying the recurrence sequentially from the raw inputs
  * ([SPEC] 实现拆解 item 3, gdn_replayssm_exact_fold_kernel; 评论区精华: the exact
- * fold removed the long-output drift). Two launches: fold, then verify.
+ * fold removed the long-output drift). Three launches: exact fold; precompute
+ * (key dot products and gate products into `workspace`, and the ring entries of
+ * the drafts that do not depend on the state: k, g, beta); verify.
  *
  * Cursors (read only here; see RSSM_CURSOR_SPEC_COMMIT): slot_wp = cnt,
  * slot_base = base, slot_flush = fold pending. Committed entries sit at ring
  * positions (base + i) % L, i < cnt. With a pending fold the effective history
  * is empty and base' = (base + cnt) % L. Draft j is written at position
- * (base + cnt + j) % L (d, k, g and the raw v, beta used by a later fold).
+ * (base + cnt + j) % L (d, k, g, and the raw v and beta a later fold replays).
+ * Draft j's output is that of the recurrence after the history and drafts 0..j;
+ * with u_j = S_{m-1} k_j and m = history + j, the chain is evaluated as
+ *   u_j = Gu_j (S0 k_j) + sum_{i<m} (prod_{l=i+1..m-1} gate_l)(k_i . k_j) d_i
+ *   d_m = beta_j (v_j - g_j u_j)
+ *   o_j = Go_j (S0 q_j) + sum_{i<=m} (prod_{l=i+1..m} gate_l)(k_i . q_j) d_i
+ * where entries i < history are ring entries and the rest earlier drafts.
  *
  * Inputs per draft: q, k [batch][T][HK][K], v [batch][T][HV][V] (act_dtype),
- * beta, g [batch][T][HV] float32. Output o [batch][T][HV][V] (out_dtype): draft
- * j's output after the history and drafts 0..j.
+ * beta, g [batch][T][HV] float32. Output o [batch][T][HV][V] (out_dtype).
  * Extra rings: ring_v [num_slots][HV][L][V] act_dtype (raw v), ring_beta
  * [num_slots][HV][L] float32. ring_k doubles as the raw k ring (the kernel takes k
  * as given; no normalisation happens inside).
  * Errors: RSSM_ERR_CONFIG when T < 1 or L < 2T ([SPEC] 关键源码片段, server_args:
- * the ring must hold at least twice the drafts). */
+ * the ring must hold at least twice the drafts); RSSM_ERR_UNSUPPORTED for T > 8.
+ * A slot whose count breaks cnt + T <= L (without a pending fold) is skipped and
+ * flagged RSSM_DEVERR_CURSOR. */
 int rssm_gdn_spec_verify(const rssm_gdn_dims* dims, int32_t T, float* state, const void* q,
                          const void* k, const void* v, const float* beta, const float* g,
                          float* ring_d, void* ring_k, float* ring_g, void* ring_v,
                          float* ring_beta, const int32_t* cache_indices, const int32_t* slot_wp,
-                         const int32_t* slot_base, const uint8_t* slot_flush, void* o,
-                         int32_t* dev_err, rssm_stream_t stream);
+                         const int32_t* slot_base, const uint8_t* slot_flush, void* workspace,
+                         size_t workspace_bytes, void* o, int32_t* dev_err,
+                         rssm_stream_t stream);
 
 #ifdef __cplusplus
 }

@@ -21,7 +21,7 @@ EXPORTS = (
     "rssm_mamba2_workspace_size", "rssm_mamba2_precompute", "rssm_mamba2_output",
     "rssm_mamba2_decode", "rssm_mamba2_full_state_update", "rssm_gdn_ring_append",
     "rssm_gdn_workspace_size", "rssm_gdn_precompute", "rssm_gdn_output", "rssm_gdn_decode",
-    "rssm_gdn_full_state_decode", "rssm_gdn_spec_verify",
+    "rssm_gdn_full_state_decode", "rssm_gdn_spec_workspace_size", "rssm_gdn_spec_verify",
 )
 
 
@@ -72,13 +72,15 @@ def _declare(L):
         "rssm_gdn_workspace_size": (_SZ, [gd]),
         "rssm_gdn_precompute": (_I, [gd, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP,
                                      _VP]),
-        "rssm_gdn_output": (_I, [gd, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _VP, _VP]),
+        "rssm_gdn_output": (_I, [gd, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _VP,
+                                 _VP]),
         "rssm_gdn_decode": (_I, [gd, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                  _VP, _SZ, _VP, _VP, _VP]),
         "rssm_gdn_full_state_decode": (_I, [gd, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                             _VP]),
+        "rssm_gdn_spec_workspace_size": (_SZ, [gd, _I32]),
         "rssm_gdn_spec_verify": (_I, [gd, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
-                                      _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
+                                      _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _VP, _VP]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -196,9 +198,9 @@ def rssm_gdn_precompute(dims, q, k, beta, g, ring_k, ring_g, cache_indices, row_
           workspace_bytes, _ptr(dev_err), _stream(stream))
 
 
-def rssm_gdn_output(dims, state, v, ring_k, ring_d, cache_indices, row_wp, row_flush, workspace,
-                    workspace_bytes, o, dev_err=None, stream=None):
-    _call("rssm_gdn_output", ctypes.byref(dims), _ptr(state), _ptr(v), _ptr(ring_k),
+def rssm_gdn_output(dims, state, q, v, ring_k, ring_d, cache_indices, row_wp, row_flush,
+                    workspace, workspace_bytes, o, dev_err=None, stream=None):
+    _call("rssm_gdn_output", ctypes.byref(dims), _ptr(state), _ptr(q), _ptr(v), _ptr(ring_k),
           _ptr(ring_d), _ptr(cache_indices), _ptr(row_wp), _ptr(row_flush), _ptr(workspace),
           workspace_bytes, _ptr(o), _ptr(dev_err), _stream(stream))
 
@@ -218,10 +220,14 @@ def rssm_gdn_full_state_decode(dims, state, q, k, v, beta, g, cache_indices, o, 
           _stream(stream))
 
 
+def rssm_gdn_spec_workspace_size(dims, T):
+    return lib().rssm_gdn_spec_workspace_size(ctypes.byref(dims), T)
+
+
 def rssm_gdn_spec_verify(dims, T, state, q, k, v, beta, g, ring_d, ring_k, ring_g, ring_v,
-                         ring_beta, cache_indices, slot_wp, slot_base, slot_flush, o,
-                         dev_err=None, stream=None):
+                         ring_beta, cache_indices, slot_wp, slot_base, slot_flush, workspace,
+                         workspace_bytes, o, dev_err=None, stream=None):
     _call("rssm_gdn_spec_verify", ctypes.byref(dims), T, _ptr(state), _ptr(q), _ptr(k), _ptr(v),
           _ptr(beta), _ptr(g), _ptr(ring_d), _ptr(ring_k), _ptr(ring_g), _ptr(ring_v),
           _ptr(ring_beta), _ptr(cache_indices), _ptr(slot_wp), _ptr(slot_base), _ptr(slot_flush),
-          _ptr(o), _ptr(dev_err), _stream(stream))
+          _ptr(workspace), workspace_bytes, _ptr(o), _ptr(dev_err), _stream(stream))

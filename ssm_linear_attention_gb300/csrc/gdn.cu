@@ -1,0 +1,703 @@
+// gdn.cu -- ReplaySSM decode for the gated delta net on sm_103a.
+//
+// Pages followed: [GDN] "GDN ReplaySSM decode (Part A of RFC 28511)" (SGLang PR
+// 28451 report): 功能与动机 (the conventional decode kernel reads and writes the
+// full state [HV, V, K] every step and is bandwidth bound at batch >= 64;
+// ReplaySSM removes the per-step state write), 实现拆解 item 1 (the decode kernel
+// reconstructs non-flush outputs from the checkpoint S0 plus the (d, k, g) ring
+// and flushes the full state every L steps), 实现拆解 item 3 (the ring tensors
+// d, k, g per slot). [SPEC] "[GDN] Support ReplaySSM Ring Spec-Verify",
+// 风险与影响: the checkpoint is fp32.
+//
+// Recurrence per value head (key head kh = hv / (HV/HK)):
+//   S <- g S + beta (v - g S k) k^T,  o = S q.
+// Unrolled from the checkpoint S0 over ring entries i < w and the current step:
+//   u   = S_{t-1} k_t = Gu (S0 k_t) + sum_{i<w} gamma_i (k_i . k_t) d_i
+//   d_t = beta_t (v_t - g_t u)
+//   o   = Go (S0 q_t) + sum_{i<w} Gamma_i (k_i . q_t) d_i + (k_t . q_t) d_t
+//   flush: S = Go S0 + sum_{i<=w} Gamma_i d_i k_i^T
+// with gamma_i = prod_{j=i+1..w-1} g_j, Gamma_i = g_t gamma_i (Gamma_w = 1),
+// Gu = prod_{j<w} g_j, Go = g_t Gu.
+//
+// Work item of the output kernel = (row, value head, block of 64 value rows): a
+// 32 KB fp32 tile of S0. Each warp owns 16 value rows; a lane holds 4 key columns
+// of a row (16-byte shared loads), so the two dot products per row reduce across
+// the warp with one 32-way reduce-scatter.
+#include "common.cuh"
+#include "internal.h"
+
+namespace rssm {
+namespace gdn {
+
+constexpr int kThreads = 128;
+constexpr int KD = 128;  // key dim handled by these kernels
+constexpr int VB = 64;   // value rows per work item
+constexpr int kMaxStages = 8;
+constexpr int kFixedSmem = 1024;
+constexpr int TILE = VB * KD * 4;
+
+__host__ __device__ inline int tbl_floats(int L) { return (3 * L + 5 + 3) & ~3; }
+
+struct Meta {
+    int valid, s, b, hv, vb, w, f, pad;
+    float beta, g;
+};
+
+__device__ __forceinline__ void mbar_arrive_plain(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// 4 consecutive elements (bf16 or f32) at element index i.
+__device__ __forceinline__ void load4(const void* base, int i, bool bf, float* f) {
+    if (bf) {
+        const uint2 v = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(base) + i);
+        f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x); f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+    } else {
+        const float4 v = *reinterpret_cast<const float4*>(static_cast<const float*>(base) + i);
+        f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
+    }
+}
+
+// ----------------------------------------------------------------------------
+// ring append (k, g)
+// ----------------------------------------------------------------------------
+
+__global__ void ring_append_kernel(int HV, int HK, int L, int num_slots, int act_bf16,
+                                   const void* __restrict__ k, const float* __restrict__ g,
+                                   const int32_t* __restrict__ ci, const int32_t* __restrict__ row_wp,
+                                   void* __restrict__ ring_k, float* __restrict__ ring_g,
+                                   int32_t* __restrict__ dev_err) {
+    const int b = blockIdx.x;
+    const int s = ci[b];
+    if (s < 0) return;
+    if (s >= num_slots) {
+        if (threadIdx.x == 0) set_dev_err(dev_err, RSSM_DEVERR_SLOT);
+        return;
+    }
+    const int w = row_wp[b];
+    if (w < 0 || w >= L) {
+        if (threadIdx.x == 0) set_dev_err(dev_err, RSSM_DEVERR_CURSOR);
+        return;
+    }
+    const int sa = act_bf16 ? 2 : 4;
+    const int kc = KD * sa / 16;
+    const uint4* ks = reinterpret_cast<const uint4*>(static_cast<const char*>(k) + (size_t)b * HK * KD * sa);
+    for (int c = threadIdx.x; c < HK * kc; c += blockDim.x) {
+        const int kh = c / kc, j = c % kc;
+        reinterpret_cast<uint4*>(static_cast<char*>(ring_k) + (((size_t)s * HK + kh) * L + w) * KD * sa)[j] =
+            ks[c];
+    }
+    for (int hv = threadIdx.x; hv < HV; hv += blockDim.x)
+        ring_g[((size_t)s * HV + hv) * L + w] = g[(size_t)b * HV + hv];
+}
+
+// ----------------------------------------------------------------------------
+// precompute
+// ----------------------------------------------------------------------------
+
+__global__ void precompute_kernel(int HV, int HK, int L, int num_slots, int act_bf16,
+                                  const void* __restrict__ q, const void* __restrict__ k,
+                                  const float* __restrict__ beta, const float* __restrict__ g,
+                                  const void* __restrict__ ring_k, const float* __restrict__ ring_g,
+                                  const int32_t* __restrict__ ci, const int32_t* __restrict__ row_wp,
+                                  float* __restrict__ ws) {
+    extern __shared__ __align__(16) float psm[];
+    const int b = blockIdx.x;
+    const int s = ci[b];
+    if (s < 0 || s >= num_slots) return;
+    const int w = row_wp[b];
+    if (w < 0 || w >= L) return;
+    const int TBL = tbl_floats(L);
+    float* kk = psm;                 // [HK][L]
+    float* kq = kk + HK * L;         // [HK][L]
+    float* kqt = kq + HK * L;        // [HK]
+    float* tbl = psm + ((2 * HK * L + HK + 3) & ~3);  // [HV][TBL]
+    const int sa = act_bf16 ? 2 : 4;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+
+    for (int pair = warp; pair < HK * (w + 1); pair += nwarps) {
+        const int kh = pair / (w + 1), i = pair % (w + 1);
+        float kt[4], qt[4];
+        load4(static_cast<const char*>(k) + ((size_t)b * HK + kh) * KD * sa, lane * 4, act_bf16, kt);
+        load4(static_cast<const char*>(q) + ((size_t)b * HK + kh) * KD * sa, lane * 4, act_bf16, qt);
+        float a1 = 0.f, a2 = 0.f;
+        if (i < w) {
+            float ki[4];
+            load4(static_cast<const char*>(ring_k) + (((size_t)s * HK + kh) * L + i) * KD * sa,
+                  lane * 4, act_bf16, ki);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                a1 = fmaf(ki[e], kt[e], a1);
+                a2 = fmaf(ki[e], qt[e], a2);
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < 4; ++e) a2 = fmaf(kt[e], qt[e], a2);
+        }
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) {
+            a1 += __shfl_xor_sync(0xffffffffu, a1, o);
+            a2 += __shfl_xor_sync(0xffffffffu, a2, o);
+        }
+        if (lane == 0) {
+            if (i < w) {
+                kk[kh * L + i] = a1;
+                kq[kh * L + i] = a2;
+            } else {
+                kqt[kh] = a2;
+            }
+        }
+    }
+    __syncthreads();
+    const int vpk = HV / HK;
+    for (int hv = threadIdx.x; hv < HV; hv += blockDim.x) {
+        const int kh = hv / vpk;
+        const float gt = g[(size_t)b * HV + hv];
+        const float bt = beta[(size_t)b * HV + hv];
+        const float* gr = ring_g + ((size_t)s * HV + hv) * L;
+        float* t = tbl + hv * TBL;
+        float gam = 1.f;  // prod_{j=i+1..w-1} g_j
+        for (int i = w - 1; i >= 0; --i) {
+            const float Gi = gt * gam;
+            t[i] = gam * kk[kh * L + i];
+            t[L + i] = Gi * kq[kh * L + i];
+            t[2 * L + i] = Gi;
+            gam *= gr[i];
+        }
+        for (int i = w; i < L; ++i) {
+            t[i] = 0.f;
+            t[L + i] = 0.f;
+            t[2 * L + i] = (i == w) ? 1.f : 0.f;
+        }
+        t[3 * L] = gam;
+        t[3 * L + 1] = gt * gam;
+        t[3 * L + 2] = kqt[kh];
+        t[3 * L + 3] = bt;
+        t[3 * L + 4] = gt;
+        for (int i = 3 * L + 5; i < TBL; ++i) t[i] = 0.f;
+    }
+    __syncthreads();
+    float4* dst = reinterpret_cast<float4*>(ws + (size_t)b * HV * TBL);
+    const float4* src = reinterpret_cast<const float4*>(tbl);
+    for (int c = threadIdx.x; c < HV * TBL / 4; c += blockDim.x) dst[c] = src[c];
+}
+
+// ----------------------------------------------------------------------------
+// output / flush (persistent, TMA bulk pipeline)
+// ----------------------------------------------------------------------------
+
+struct OutArgs {
+    float* state;
+    const void* q;
+    const void* v;
+    const void* ring_k;
+    float* ring_d;
+    const int32_t* ci;
+    const int32_t* row_wp;
+    const uint8_t* row_flush;
+    const float* ws;
+    void* o;
+    int32_t* dev_err;
+    int batch, HV, HK, V, L, num_slots, act_bf16, out_bf16;
+    int stages, stage_bytes;
+    int off_k, off_q, off_v, off_d, off_tbl;
+};
+
+struct RowMeta {
+    int b, s, w, f;
+};
+
+__global__ void __launch_bounds__(kThreads) output_kernel(const OutArgs a) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
+    Meta* meta = reinterpret_cast<Meta*>(smem + 128);
+    int* abort_flag = reinterpret_cast<int*>(smem + 128 + kMaxStages * sizeof(Meta));
+    uint8_t* stage0 = smem + kFixedSmem;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int HV = a.HV, HK = a.HK, V = a.V, L = a.L;
+    const int NVB = V / VB;
+    const int sa = a.act_bf16 ? 2 : 4;
+    const int TBL = tbl_floats(L);
+    const int n_items = a.batch * HV * NVB;
+    const int stages = a.stages;
+    const int per_row = HV * NVB;
+
+    if (tid == 0) {
+        for (int st = 0; st < stages; ++st) mbar_init(&bars[st], 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    uint64_t pol = 0;
+    RowMeta pf{-1, 0, 0, 0};
+    auto load_row = [&](int b) {
+        RowMeta r{b, a.ci[b], 0, 0};
+        if (r.s >= 0 && r.s < a.num_slots) {
+            r.w = a.row_wp[b];
+            r.f = a.row_flush[b];
+        }
+        return r;
+    };
+    auto issue = [&](int k) {
+        const int item = blockIdx.x + k * gridDim.x;
+        if (item >= n_items) return;
+        const int st = k % stages;
+        uint8_t* sb = stage0 + st * a.stage_bytes;
+        const int b = item / per_row;
+        const int rem = item - b * per_row;
+        const int hv = rem / NVB, vb = rem - (rem / NVB) * NVB;
+        const RowMeta r = (pf.b == b) ? pf : load_row(b);
+        const int nxt = item + gridDim.x;
+        if (nxt < n_items) pf = load_row(nxt / per_row);
+        Meta m;
+        m.b = b; m.hv = hv; m.vb = vb; m.s = r.s; m.w = r.w; m.f = r.f; m.valid = 0; m.pad = 0;
+        m.beta = 0.f; m.g = 0.f;
+        if (r.s >= a.num_slots) {
+            set_dev_err(a.dev_err, RSSM_DEVERR_SLOT);
+        } else if (r.s >= 0) {
+            if (r.w < 0 || r.w >= L) set_dev_err(a.dev_err, RSSM_DEVERR_CURSOR);
+            else m.valid = 1;
+        }
+        meta[st] = m;
+        if (!m.valid) {
+            mbar_arrive_plain(&bars[st]);
+            return;
+        }
+        const int kh = hv / (HV / HK);
+        const int w = r.w;
+        const uint32_t kb = KD * sa;
+        const uint32_t kbytes = r.f ? (w + 1) * kb : kb;
+        const uint32_t tx = TILE + kbytes + kb + VB * sa + w * VB * 4 + TBL * 4;
+        mbar_arrive_expect_tx(&bars[st], tx);
+        const size_t tile_off = (((size_t)r.s * HV + hv) * V + (size_t)vb * VB) * KD;
+        bulk_g2s_hint(sb, a.state + tile_off, TILE, &bars[st], pol);
+        const char* kr = static_cast<const char*>(a.ring_k) + ((size_t)r.s * HK + kh) * L * kb;
+        if (r.f) bulk_g2s(sb + a.off_k, kr, kbytes, &bars[st]);
+        else bulk_g2s(sb + a.off_k + w * kb, kr + (size_t)w * kb, kb, &bars[st]);
+        bulk_g2s(sb + a.off_q, static_cast<const char*>(a.q) + ((size_t)b * HK + kh) * kb, kb,
+                 &bars[st]);
+        bulk_g2s(sb + a.off_v,
+                 static_cast<const char*>(a.v) + (((size_t)b * HV + hv) * V + (size_t)vb * VB) * sa,
+                 VB * sa, &bars[st]);
+        const float* dr = a.ring_d + (((size_t)r.s * HV + hv) * L) * V + (size_t)vb * VB;
+        for (int i = 0; i < w; ++i)
+            bulk_g2s(sb + a.off_d + i * VB * 4, dr + (size_t)i * V, VB * 4, &bars[st]);
+        bulk_g2s(sb + a.off_tbl, a.ws + ((size_t)b * HV + hv) * TBL, TBL * 4, &bars[st]);
+    };
+    if (tid == 0) {
+        pol = policy_evict_first();
+        for (int k = 0; k < stages; ++k) issue(k);
+    }
+
+    int k = 0;
+    for (;; ++k) {
+        const int item = blockIdx.x + k * gridDim.x;
+        if (item >= n_items) break;
+        const int st = k % stages;
+        const uint32_t par = (k / stages) & 1;
+        // all threads agree on the outcome, so the branch below stays uniform
+        const bool ok = __syncthreads_and(mbar_wait_bounded(&bars[st], par) ? 1 : 0) != 0;
+        if (!ok) {
+            *abort_flag = 1;
+            set_dev_err(a.dev_err, RSSM_DEVERR_TIMEOUT);
+        }
+        const Meta m = meta[st];
+        if (ok && m.valid) {
+            const uint8_t* sb = stage0 + st * a.stage_bytes;
+            const float* tile = reinterpret_cast<const float*>(sb);
+            const uint8_t* kring = sb + a.off_k;
+            const float* dring = reinterpret_cast<const float*>(sb + a.off_d);
+            const float* t = reinterpret_cast<const float*>(sb + a.off_tbl);
+            const int w = m.w;
+            float k4[4], q4[4];
+            load4(kring + (size_t)w * KD * sa, lane * 4, a.act_bf16, k4);
+            load4(sb + a.off_q, lane * 4, a.act_bf16, q4);
+            float part[32];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const float4 s4 = *reinterpret_cast<const float4*>(tile + (warp + 4 * j) * KD + lane * 4);
+                part[j] = s4.x * k4[0] + s4.y * k4[1] + s4.z * k4[2] + s4.w * k4[3];
+                part[16 + j] = s4.x * q4[0] + s4.y * q4[1] + s4.z * q4[2] + s4.w * q4[3];
+            }
+            reduce_scatter<32, 32>(part);  // lane l now holds entry l
+            const float cdot = __shfl_down_sync(0xffffffffu, part[0], 16);
+            const float Gu = t[3 * L], Go = t[3 * L + 1], kqt = t[3 * L + 2];
+            const float bt = t[3 * L + 3], gt = t[3 * L + 4];
+            float dt_new = 0.f;
+            const int r = warp + 4 * (lane & 15);
+            if (lane < 16) {
+                float u = Gu * part[0];
+                float oo = Go * cdot;
+                for (int i = 0; i < w; ++i) {
+                    const float di = dring[i * VB + r];
+                    u = fmaf(t[i], di, u);
+                    oo = fmaf(t[L + i], di, oo);
+                }
+                const float vr = load1(sb + a.off_v, r, a.act_bf16);
+                dt_new = bt * (vr - gt * u);
+                oo = fmaf(kqt, dt_new, oo);
+                const size_t vi = (size_t)m.vb * VB + r;
+                store1(a.o, ((size_t)m.b * HV + m.hv) * V + vi, a.out_bf16, oo);
+                a.ring_d[(((size_t)m.s * HV + m.hv) * L + w) * V + vi] = dt_new;
+            }
+            if (m.f) {
+                float dcur[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) dcur[j] = __shfl_sync(0xffffffffu, dt_new, j);
+                float acc[16][4];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const float4 s4 = *reinterpret_cast<const float4*>(tile + (warp + 4 * j) * KD + lane * 4);
+                    acc[j][0] = Go * s4.x; acc[j][1] = Go * s4.y;
+                    acc[j][2] = Go * s4.z; acc[j][3] = Go * s4.w;
+                }
+                for (int i = 0; i <= w; ++i) {
+                    float ki[4];
+                    load4(kring + (size_t)i * KD * sa, lane * 4, a.act_bf16, ki);
+                    const float ti = t[2 * L + i];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float dj = (i < w) ? dring[i * VB + warp + 4 * j] : dcur[j];
+                        const float c = ti * dj;
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) acc[j][e] = fmaf(c, ki[e], acc[j][e]);
+                    }
+                }
+                float* dst = a.state + (((size_t)m.s * HV + m.hv) * V + (size_t)m.vb * VB) * KD;
+#pragma unroll
+                for (int j = 0; j < 16; ++j)
+                    *reinterpret_cast<float4*>(dst + (warp + 4 * j) * KD + lane * 4) =
+                        make_float4(acc[j][0], acc[j][1], acc[j][2], acc[j][3]);
+            }
+        }
+        __syncthreads();
+        if (*abort_flag) break;
+        if (tid == 0) issue(k + stages);
+    }
+    if (*abort_flag && tid == 0) {
+        for (int j = k; j < k + stages; ++j) {
+            const int item = blockIdx.x + j * gridDim.x;
+            if (item >= n_items) break;
+            mbar_wait_bounded(&bars[j % stages], (j / stages) & 1);
+        }
+    }
+}
+
+// ----------------------------------------------------------------------------
+// full-state decode (the conventional kernel)
+// ----------------------------------------------------------------------------
+
+struct FullArgs {
+    float* state;
+    const void* q;
+    const void* k;
+    const void* v;
+    const float* beta;
+    const float* g;
+    const int32_t* ci;
+    void* o;
+    int32_t* dev_err;
+    int batch, HV, HK, V, num_slots, act_bf16, out_bf16;
+    int stages, stage_bytes;
+    int off_k, off_q, off_v;
+};
+
+__global__ void __launch_bounds__(kThreads) full_state_kernel(const FullArgs a) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
+    Meta* meta = reinterpret_cast<Meta*>(smem + 128);
+    int* abort_flag = reinterpret_cast<int*>(smem + 128 + kMaxStages * sizeof(Meta));
+    uint8_t* stage0 = smem + kFixedSmem;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int HV = a.HV, HK = a.HK, V = a.V;
+    const int NVB = V / VB;
+    const int sa = a.act_bf16 ? 2 : 4;
+    const int n_items = a.batch * HV * NVB;
+    const int stages = a.stages;
+    const int per_row = HV * NVB;
+
+    if (tid == 0) {
+        for (int st = 0; st < stages; ++st) mbar_init(&bars[st], 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    uint64_t pol = 0;
+    auto issue = [&](int k) {
+        const int item = blockIdx.x + k * gridDim.x;
+        if (item >= n_items) return;
+        const int st = k % stages;
+        uint8_t* sb = stage0 + st * a.stage_bytes;
+        const int b = item / per_row;
+        const int rem = item - b * per_row;
+        const int hv = rem / NVB, vb = rem - (rem / NVB) * NVB;
+        const int s = a.ci[b];
+        Meta m;
+        m.b = b; m.hv = hv; m.vb = vb; m.s = s; m.w = 0; m.f = 0; m.valid = 0; m.pad = 0;
+        m.beta = 0.f; m.g = 0.f;
+        if (s >= a.num_slots) set_dev_err(a.dev_err, RSSM_DEVERR_SLOT);
+        else if (s >= 0) m.valid = 1;
+        if (m.valid) {
+            m.beta = a.beta[(size_t)b * HV + hv];
+            m.g = a.g[(size_t)b * HV + hv];
+        }
+        meta[st] = m;
+        if (!m.valid) {
+            mbar_arrive_plain(&bars[st]);
+            return;
+        }
+        const int kh = hv / (HV / HK);
+        const uint32_t kb = KD * sa;
+        mbar_arrive_expect_tx(&bars[st], TILE + 2 * kb + VB * sa);
+        bulk_g2s_hint(sb, a.state + (((size_t)s * HV + hv) * V + (size_t)vb * VB) * KD, TILE, &bars[st],
+                      pol);
+        bulk_g2s(sb + a.off_k, static_cast<const char*>(a.k) + ((size_t)b * HK + kh) * kb, kb, &bars[st]);
+        bulk_g2s(sb + a.off_q, static_cast<const char*>(a.q) + ((size_t)b * HK + kh) * kb, kb, &bars[st]);
+        bulk_g2s(sb + a.off_v,
+                 static_cast<const char*>(a.v) + (((size_t)b * HV + hv) * V + (size_t)vb * VB) * sa,
+                 VB * sa, &bars[st]);
+    };
+    if (tid == 0) {
+        pol = policy_evict_first();
+        for (int k = 0; k < stages; ++k) issue(k);
+    }
+
+    int k = 0;
+    for (;; ++k) {
+        const int item = blockIdx.x + k * gridDim.x;
+        if (item >= n_items) break;
+        const int st = k % stages;
+        const uint32_t par = (k / stages) & 1;
+        // all threads agree on the outcome, so the branch below stays uniform
+        const bool ok = __syncthreads_and(mbar_wait_bounded(&bars[st], par) ? 1 : 0) != 0;
+        if (!ok) {
+            *abort_flag = 1;
+            set_dev_err(a.dev_err, RSSM_DEVERR_TIMEOUT);
+        }
+        const Meta m = meta[st];
+        if (ok && m.valid) {
+            const uint8_t* sb = stage0 + st * a.stage_bytes;
+            const float* tile = reinterpret_cast<const float*>(sb);
+            float k4[4], q4[4];
+            load4(sb + a.off_k, lane * 4, a.act_bf16, k4);
+            load4(sb + a.off_q, lane * 4, a.act_bf16, q4);
+            float kq = k4[0] * q4[0] + k4[1] * q4[1] + k4[2] * q4[2] + k4[3] * q4[3];
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, o);
+            float part[32];
+            float4 rows[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const float4 s4 = *reinterpret_cast<const float4*>(tile + (warp + 4 * j) * KD + lane * 4);
+                rows[j] = s4;
+                part[j] = s4.x * k4[0] + s4.y * k4[1] + s4.z * k4[2] + s4.w * k4[3];
+                part[16 + j] = s4.x * q4[0] + s4.y * q4[1] + s4.z * q4[2] + s4.w * q4[3];
+            }
+            reduce_scatter<32, 32>(part);
+            const float cdot = __shfl_down_sync(0xffffffffu, part[0], 16);
+            const int r = warp + 4 * (lane & 15);
+            float dnew = 0.f;
+            if (lane < 16) {
+                const float vr = load1(sb + a.off_v, r, a.act_bf16);
+                dnew = m.beta * (vr - m.g * part[0]);
+                const float oo = m.g * cdot + dnew * kq;
+                store1(a.o, ((size_t)m.b * HV + m.hv) * V + (size_t)m.vb * VB + r, a.out_bf16, oo);
+            }
+            float* dst = a.state + (((size_t)m.s * HV + m.hv) * V + (size_t)m.vb * VB) * KD;
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                const float dj = __shfl_sync(0xffffffffu, dnew, j);
+                float4 s4 = rows[j];
+                s4.x = fmaf(m.g, s4.x, dj * k4[0]);
+                s4.y = fmaf(m.g, s4.y, dj * k4[1]);
+                s4.z = fmaf(m.g, s4.z, dj * k4[2]);
+                s4.w = fmaf(m.g, s4.w, dj * k4[3]);
+                *reinterpret_cast<float4*>(dst + (warp + 4 * j) * KD + lane * 4) = s4;
+            }
+        }
+        __syncthreads();
+        if (*abort_flag) break;
+        if (tid == 0) issue(k + stages);
+    }
+    if (*abort_flag && tid == 0) {
+        for (int j = k; j < k + stages; ++j) {
+            const int item = blockIdx.x + j * gridDim.x;
+            if (item >= n_items) break;
+            mbar_wait_bounded(&bars[j % stages], (j / stages) & 1);
+        }
+    }
+}
+
+// ----------------------------------------------------------------------------
+// host side
+// ----------------------------------------------------------------------------
+
+int check_dims(const rssm_gdn_dims* d) {
+    if (!d) return RSSM_ERR_INVALID_ARG;
+    if (d->batch < 0 || d->num_v_heads <= 0 || d->num_k_heads <= 0 || d->head_k_dim <= 0 ||
+        d->head_v_dim <= 0 || d->num_slots <= 0)
+        return RSSM_ERR_INVALID_ARG;
+    if (!ok_dtype(d->act_dtype) || !ok_dtype(d->out_dtype)) return RSSM_ERR_INVALID_ARG;
+    if (d->ring_len < 1 || d->num_v_heads % d->num_k_heads) return RSSM_ERR_CONFIG;
+    if (d->head_k_dim != KD || d->head_v_dim % VB) return RSSM_ERR_UNSUPPORTED;
+    return RSSM_OK;
+}
+
+}  // namespace gdn
+}  // namespace rssm
+
+using namespace rssm;
+
+extern "C" int rssm_gdn_ring_append(const rssm_gdn_dims* d, const void* k, const float* g,
+                                    const int32_t* cache_indices, const int32_t* row_wp,
+                                    void* ring_k, float* ring_g, int32_t* dev_err,
+                                    rssm_stream_t stream) {
+    int rc = gdn::check_dims(d);
+    if (rc) return rc;
+    if (d->batch == 0) return RSSM_OK;
+    if (!ok_ptr(k) || !ok_ptr(g) || !ok_ptr(cache_indices) || !ok_ptr(row_wp) || !ok_ptr(ring_k) ||
+        !ok_ptr(ring_g))
+        return RSSM_ERR_INVALID_ARG;
+    gdn::ring_append_kernel<<<d->batch, 128, 0, (cudaStream_t)stream>>>(
+        d->num_v_heads, d->num_k_heads, d->ring_len, d->num_slots, d->act_dtype == RSSM_BF16, k, g,
+        cache_indices, row_wp, ring_k, ring_g, dev_err);
+    return launch_status();
+}
+
+extern "C" size_t rssm_gdn_workspace_size(const rssm_gdn_dims* d) {
+    if (gdn::check_dims(d)) return 0;
+    return (size_t)d->batch * d->num_v_heads * gdn::tbl_floats(d->ring_len) * sizeof(float);
+}
+
+extern "C" int rssm_gdn_precompute(const rssm_gdn_dims* d, const void* q, const void* k,
+                                   const float* beta, const float* g, const void* ring_k,
+                                   const float* ring_g, const int32_t* cache_indices,
+                                   const int32_t* row_wp, void* workspace, size_t workspace_bytes,
+                                   int32_t* dev_err, rssm_stream_t stream) {
+    (void)dev_err;
+    int rc = gdn::check_dims(d);
+    if (rc) return rc;
+    if (d->batch == 0) return RSSM_OK;
+    if (!ok_ptr(q) || !ok_ptr(k) || !ok_ptr(beta) || !ok_ptr(g) || !ok_ptr(ring_k) ||
+        !ok_ptr(ring_g) || !ok_ptr(cache_indices) || !ok_ptr(row_wp) || !ok_ptr(workspace))
+        return RSSM_ERR_INVALID_ARG;
+    if (workspace_bytes < rssm_gdn_workspace_size(d)) return RSSM_ERR_INVALID_ARG;
+    const int L = d->ring_len, HK = d->num_k_heads;
+    const int smem = (((2 * HK * L + HK + 3) & ~3) + d->num_v_heads * gdn::tbl_floats(L)) * 4;
+    DeviceInfo di;
+    if (!device_info(&di)) return RSSM_ERR_CUDA;
+    if (smem > di.max_smem_optin) return RSSM_ERR_UNSUPPORTED;
+    if (smem > 48 * 1024 &&
+        !ensure_smem_limit(reinterpret_cast<const void*>(gdn::precompute_kernel), smem))
+        return RSSM_ERR_CUDA;
+    gdn::precompute_kernel<<<d->batch, 128, smem, (cudaStream_t)stream>>>(
+        d->num_v_heads, HK, L, d->num_slots, d->act_dtype == RSSM_BF16, q, k, beta, g, ring_k, ring_g,
+        cache_indices, row_wp, static_cast<float*>(workspace));
+    return launch_status();
+}
+
+extern "C" int rssm_gdn_output(const rssm_gdn_dims* d, float* state, const void* q, const void* v,
+                               const void* ring_k, float* ring_d, const int32_t* cache_indices,
+                               const int32_t* row_wp, const uint8_t* row_flush,
+                               const void* workspace, size_t workspace_bytes, void* o,
+                               int32_t* dev_err, rssm_stream_t stream) {
+    int rc = gdn::check_dims(d);
+    if (rc) return rc;
+    if (d->batch == 0) return RSSM_OK;
+    if (!ok_ptr(state) || !ok_ptr(q) || !ok_ptr(v) || !ok_ptr(ring_k) || !ok_ptr(ring_d) ||
+        !ok_ptr(cache_indices) || !ok_ptr(row_wp) || !ok_ptr(row_flush) || !ok_ptr(workspace) ||
+        !ok_ptr(o))
+        return RSSM_ERR_INVALID_ARG;
+    if (workspace_bytes < rssm_gdn_workspace_size(d)) return RSSM_ERR_INVALID_ARG;
+    DeviceInfo di;
+    if (!device_info(&di)) return RSSM_ERR_CUDA;
+    gdn::OutArgs a{};
+    a.state = state; a.q = q; a.v = v; a.ring_k = ring_k; a.ring_d = ring_d; a.ci = cache_indices;
+    a.row_wp = row_wp; a.row_flush = row_flush; a.ws = static_cast<const float*>(workspace);
+    a.o = o; a.dev_err = dev_err;
+    a.batch = d->batch; a.HV = d->num_v_heads; a.HK = d->num_k_heads; a.V = d->head_v_dim;
+    a.L = d->ring_len; a.num_slots = d->num_slots; a.act_bf16 = d->act_dtype == RSSM_BF16;
+    a.out_bf16 = d->out_dtype == RSSM_BF16;
+    const int sa = a.act_bf16 ? 2 : 4;
+    int off = gdn::TILE;
+    a.off_k = off;   off += a.L * gdn::KD * sa;
+    a.off_q = off;   off += gdn::KD * sa;
+    a.off_v = off;   off += gdn::VB * sa;
+    a.off_v = (a.off_v + 15) & ~15;
+    off = (off + 15) & ~15;
+    a.off_d = off;   off += a.L * gdn::VB * 4;
+    a.off_tbl = off; off += gdn::tbl_floats(a.L) * 4;
+    a.stage_bytes = (off + 127) & ~127;
+    PipeShape ps;
+    if (!pick_pipe_shape(di, a.stage_bytes, gdn::kFixedSmem, gdn::kMaxStages, &ps))
+        return RSSM_ERR_UNSUPPORTED;
+    a.stages = ps.stages;
+    if (!ensure_smem_limit(reinterpret_cast<const void*>(gdn::output_kernel), ps.smem_bytes))
+        return RSSM_ERR_CUDA;
+    const long items = (long)d->batch * d->num_v_heads * (d->head_v_dim / gdn::VB);
+    long grid = (long)di.sm_count * ps.ctas_per_sm;
+    if (grid > items) grid = items;
+    gdn::output_kernel<<<(int)grid, gdn::kThreads, ps.smem_bytes, (cudaStream_t)stream>>>(a);
+    return launch_status();
+}
+
+extern "C" int rssm_gdn_decode(const rssm_gdn_dims* d, float* state, const void* q, const void* k,
+                               const void* v, const float* beta, const float* g,
+                               const void* ring_k, const float* ring_g, float* ring_d,
+                               const int32_t* cache_indices, const int32_t* row_wp,
+                               const uint8_t* row_flush, void* workspace, size_t workspace_bytes,
+                               void* o, int32_t* dev_err, rssm_stream_t stream) {
+    int rc = gdn::check_dims(d);
+    if (rc) return rc;
+    if (d->batch == 0) return RSSM_OK;
+    if (!ok_ptr(state) || !ok_ptr(q) || !ok_ptr(k) || !ok_ptr(v) || !ok_ptr(beta) || !ok_ptr(g) ||
+        !ok_ptr(ring_k) || !ok_ptr(ring_g) || !ok_ptr(ring_d) || !ok_ptr(cache_indices) ||
+        !ok_ptr(row_wp) || !ok_ptr(row_flush) || !ok_ptr(workspace) || !ok_ptr(o))
+        return RSSM_ERR_INVALID_ARG;
+    rc = rssm_gdn_precompute(d, q, k, beta, g, ring_k, ring_g, cache_indices, row_wp, workspace,
+                             workspace_bytes, dev_err, stream);
+    if (rc) return rc;
+    return rssm_gdn_output(d, state, q, v, ring_k, ring_d, cache_indices, row_wp, row_flush,
+                           workspace, workspace_bytes, o, dev_err, stream);
+}
+
+extern "C" int rssm_gdn_full_state_decode(const rssm_gdn_dims* d, float* state, const void* q,
+                                          const void* k, const void* v, const float* beta,
+                                          const float* g, const int32_t* cache_indices, void* o,
+                                          int32_t* dev_err, rssm_stream_t stream) {
+    int rc = gdn::check_dims(d);
+    if (rc) return rc;
+    if (d->batch == 0) return RSSM_OK;
+    if (!ok_ptr(state) || !ok_ptr(q) || !ok_ptr(k) || !ok_ptr(v) || !ok_ptr(beta) || !ok_ptr(g) ||
+        !ok_ptr(cache_indices) || !ok_ptr(o))
+        return RSSM_ERR_INVALID_ARG;
+    DeviceInfo di;
+    if (!device_info(&di)) return RSSM_ERR_CUDA;
+    gdn::FullArgs a{};
+    a.state = state; a.q = q; a.k = k; a.v = v; a.beta = beta; a.g = g; a.ci = cache_indices;
+    a.o = o; a.dev_err = dev_err;
+    a.batch = d->batch; a.HV = d->num_v_heads; a.HK = d->num_k_heads; a.V = d->head_v_dim;
+    a.num_slots = d->num_slots; a.act_bf16 = d->act_dtype == RSSM_BF16;
+    a.out_bf16 = d->out_dtype == RSSM_BF16;
+    const int sa = a.act_bf16 ? 2 : 4;
+    int off = gdn::TILE;
+    a.off_k = off; off += gdn::KD * sa;
+    a.off_q = off; off += gdn::KD * sa;
+    a.off_v = off; off += gdn::VB * sa;
+    a.stage_bytes = (off + 127) & ~127;
+    PipeShape ps;
+    if (!pick_pipe_shape(di, a.stage_bytes, gdn::kFixedSmem, gdn::kMaxStages, &ps))
+        return RSSM_ERR_UNSUPPORTED;
+    a.stages = ps.stages;
+    if (!ensure_smem_limit(reinterpret_cast<const void*>(gdn::full_state_kernel), ps.smem_bytes))
+        return RSSM_ERR_CUDA;
+    const long items = (long)d->batch * d->num_v_heads * (d->head_v_dim / gdn::VB);
+    long grid = (long)di.sm_count * ps.ctas_per_sm;
+    if (grid > items) grid = items;
+    gdn::full_state_kernel<<<(int)grid, gdn::kThreads, ps.smem_bytes, (cudaStream_t)stream>>>(a);
+    return launch_status();
+}

@@ -1,0 +1,569 @@
+// gdn_spec.cu -- ReplaySSM speculative verify for the gated delta net (sm_103a).
+//
+// Pages followed: [SPEC] "[GDN] Support ReplaySSM Ring Spec-Verify" (SGLang PR
+// 28695 report): 功能与动机 (the per-draft full-state snapshots of the
+// recurrent verify are the bulk of spec-decode memory), 实现拆解 item 2 (ring
+// tensors d/k/g plus raw v/k and beta, cursors write_pos / cache_base /
+// is_flush per slot), item 3 (gdn_replayssm_spec_circular_kernel reconstructs
+// per-draft outputs from the frozen checkpoint + circular ring;
+// gdn_replayssm_exact_fold_kernel replays the recurrent update sequentially
+// from the raw inputs at a flush), item 4 (the commit only advances cursors),
+// 评论区精华 (the exact fold fixed the long-output drift; ring length >= 2 x
+// drafts).
+//
+// Launches of one verify round:
+//   fold_kernel        one CTA per (row, value head, 64-row block) of a slot with
+//                      a pending fold: S0 rows in registers, cnt sequential
+//                      delta-rule updates from ring k, raw v, beta, g; S0 stored.
+//   spec_pre_kernel    one CTA per row: dot products of every live key (history
+//                      and drafts) with the drafts' keys and queries, products of
+//                      gates, into a per-(row, value head) table; writes the
+//                      drafts' k, g, beta into the ring.
+//   verify_kernel<DP>  persistent TMA pipeline over (row, value head, 64-row
+//                      block) tiles of S0: the 2T dot products per value row,
+//                      then the draft chain per row; writes o, and d and raw v
+//                      of the drafts into the ring.
+// A fold must precede the verify in a separate launch: the drafts of the same
+// round may land on ring positions whose raw entries the fold still reads.
+#include "common.cuh"
+#include "internal.h"
+
+namespace rssm {
+namespace spec {
+
+constexpr int kThreads = 128;
+constexpr int KD = 128;
+constexpr int VB = 64;
+constexpr int TILE = VB * KD * 4;
+constexpr int kMaxStages = 8;
+constexpr int kMaxT = 8;
+
+// table per (row, value head): au[T][L], ao[T][L], Gu[T], Go[T], beta[T], g[T], c, base'
+__host__ __device__ inline int tbl_floats(int L, int T) { return (2 * T * L + 4 * T + 2 + 3) & ~3; }
+
+__device__ __forceinline__ void load4(const void* base, int i, bool bf, float* f) {
+    if (bf) {
+        const uint2 v = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(base) + i);
+        f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x); f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+    } else {
+        const float4 v = *reinterpret_cast<const float4*>(static_cast<const float*>(base) + i);
+        f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
+    }
+}
+
+__device__ __forceinline__ void mbar_arrive_plain(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+// Effective history of a slot at verify time: (count, oldest position); false when
+// the cursors are outside the ring.
+__device__ __forceinline__ bool history(int cnt, int base, int flush, int L, int T, int* c,
+                                        int* base_eff) {
+    if (cnt < 0 || cnt > L || base < 0 || base >= L) return false;
+    if (flush) {
+        *c = 0;
+        *base_eff = (base + cnt) % L;
+    } else {
+        *c = cnt;
+        *base_eff = base;
+    }
+    return *c + T <= L;
+}
+
+// ----------------------------------------------------------------------------
+// exact fold
+// ----------------------------------------------------------------------------
+
+struct FoldArgs {
+    float* state;
+    const void* ring_k;
+    const void* ring_v;
+    const float* ring_g;
+    const float* ring_beta;
+    const int32_t* ci;
+    const int32_t* slot_wp;
+    const int32_t* slot_base;
+    const uint8_t* slot_flush;
+    int32_t* dev_err;
+    int HV, HK, V, L, num_slots, act_bf16;
+};
+
+__global__ void __launch_bounds__(kThreads) fold_kernel(const FoldArgs a) {
+    const int NVB = a.V / VB;
+    const int item = blockIdx.x;
+    const int b = item / (a.HV * NVB);
+    const int rem = item - b * a.HV * NVB;
+    const int hv = rem / NVB, vb = rem - (rem / NVB) * NVB;
+    const int s = a.ci[b];
+    if (s < 0 || s >= a.num_slots) return;  // verify reports bad slots
+    if (!a.slot_flush[s]) return;
+    const int cnt = a.slot_wp[s], base = a.slot_base[s];
+    if (cnt <= 0 || cnt > a.L || base < 0 || base >= a.L) return;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int kh = hv / (a.HV / a.HK);
+    const int sa = a.act_bf16 ? 2 : 4;
+    float* tile = a.state + (((size_t)s * a.HV + hv) * a.V + (size_t)vb * VB) * KD;
+    float S[16][4];
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+        const float4 v4 = *reinterpret_cast<const float4*>(tile + (warp + 4 * j) * KD + lane * 4);
+        S[j][0] = v4.x; S[j][1] = v4.y; S[j][2] = v4.z; S[j][3] = v4.w;
+    }
+    for (int e = 0; e < cnt; ++e) {
+        const int pos = (base + e) % a.L;
+        float k4[4];
+        load4(static_cast<const char*>(a.ring_k) + (((size_t)s * a.HK + kh) * a.L + pos) * KD * sa,
+              lane * 4, a.act_bf16, k4);
+        const float be = a.ring_beta[((size_t)s * a.HV + hv) * a.L + pos];
+        const float ge = a.ring_g[((size_t)s * a.HV + hv) * a.L + pos];
+        // this lane's value row for the broadcast below: rows warp + 4*(lane>>1)
+        const float vown = load1(a.ring_v, (((size_t)s * a.HV + hv) * a.L + pos) * a.V +
+                                               (size_t)vb * VB + warp + 4 * ((lane >> 1) & 15),
+                                 a.act_bf16);
+        float part[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j)
+            part[j] = S[j][0] * k4[0] + S[j][1] * k4[1] + S[j][2] * k4[2] + S[j][3] * k4[3];
+        const int idx = reduce_scatter<16, 32>(part);  // lanes 2i, 2i+1 hold row i's sum
+        const float dmine = be * (vown - ge * part[0]);
+        (void)idx;
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const float dj = __shfl_sync(0xffffffffu, dmine, 2 * j);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) S[j][c] = fmaf(ge, S[j][c], dj * k4[c]);
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < 16; ++j)
+        *reinterpret_cast<float4*>(tile + (warp + 4 * j) * KD + lane * 4) =
+            make_float4(S[j][0], S[j][1], S[j][2], S[j][3]);
+}
+
+// ----------------------------------------------------------------------------
+// spec precompute (one CTA per row)
+// ----------------------------------------------------------------------------
+
+struct PreArgs {
+    const void* q;
+    const void* k;
+    const float* beta;
+    const float* g;
+    void* ring_k;
+    float* ring_g;
+    float* ring_beta;
+    const int32_t* ci;
+    const int32_t* slot_wp;
+    const int32_t* slot_base;
+    const uint8_t* slot_flush;
+    float* ws;
+    int32_t* dev_err;
+    int T, HV, HK, L, num_slots, act_bf16;
+};
+
+__global__ void spec_pre_kernel(const PreArgs a) {
+    extern __shared__ __align__(16) float psm[];
+    const int b = blockIdx.x;
+    const int s = a.ci[b];
+    if (s < 0 || s >= a.num_slots) return;
+    const int T = a.T, L = a.L, HV = a.HV, HK = a.HK;
+    int c, base_eff;
+    if (!history(a.slot_wp[s], a.slot_base[s], a.slot_flush[s], L, T, &c, &base_eff)) return;
+    const int nk = c + T;                 // live keys: history then drafts
+    float* KK = psm;                      // [HK][L][T]   k_i . k_j
+    float* KQ = KK + HK * L * T;          // [HK][L][T]   k_i . q_j
+    const int sa = a.act_bf16 ? 2 : 4;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    const char* kin = static_cast<const char*>(a.k);
+    const char* qin = static_cast<const char*>(a.q);
+
+    // one warp per (key head, key): 2T dot products against the drafts
+    for (int task = warp; task < HK * nk; task += nwarps) {
+        const int kh = task / nk, i = task - (task / nk) * nk;
+        float ki[4];
+        if (i < c) {
+            const int pos = (base_eff + i) % L;
+            load4(static_cast<const char*>(a.ring_k) + (((size_t)s * HK + kh) * L + pos) * KD * sa,
+                  lane * 4, a.act_bf16, ki);
+        } else {
+            load4(kin + (((size_t)b * T + (i - c)) * HK + kh) * KD * sa, lane * 4, a.act_bf16, ki);
+        }
+        for (int j = 0; j < T; ++j) {
+            float kj[4], qj[4];
+            load4(kin + (((size_t)b * T + j) * HK + kh) * KD * sa, lane * 4, a.act_bf16, kj);
+            load4(qin + (((size_t)b * T + j) * HK + kh) * KD * sa, lane * 4, a.act_bf16, qj);
+            float d1 = 0.f, d2 = 0.f;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                d1 = fmaf(ki[e], kj[e], d1);
+                d2 = fmaf(ki[e], qj[e], d2);
+            }
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) {
+                d1 += __shfl_xor_sync(0xffffffffu, d1, o);
+                d2 += __shfl_xor_sync(0xffffffffu, d2, o);
+            }
+            if (lane == 0) {
+                KK[(kh * L + i) * T + j] = d1;
+                KQ[(kh * L + i) * T + j] = d2;
+            }
+        }
+    }
+    // the drafts' S-independent ring entries: k (per key head), g and beta (per value head)
+    const int kc = KD * sa / 16;
+    for (int x = threadIdx.x; x < T * HK * kc; x += blockDim.x) {
+        const int j = x / (HK * kc), r = x - j * HK * kc;
+        const int kh = r / kc, part = r - kh * kc;
+        const int pos = (base_eff + c + j) % L;
+        reinterpret_cast<uint4*>(static_cast<char*>(a.ring_k) +
+                                 (((size_t)s * HK + kh) * L + pos) * KD * sa)[part] =
+            reinterpret_cast<const uint4*>(kin + (((size_t)b * T + j) * HK + kh) * KD * sa)[part];
+    }
+    for (int x = threadIdx.x; x < T * HV; x += blockDim.x) {
+        const int j = x / HV, hv = x - j * HV;
+        const int pos = (base_eff + c + j) % L;
+        a.ring_g[((size_t)s * HV + hv) * L + pos] = a.g[((size_t)b * T + j) * HV + hv];
+        a.ring_beta[((size_t)s * HV + hv) * L + pos] = a.beta[((size_t)b * T + j) * HV + hv];
+    }
+    __syncthreads();
+
+    // coefficient table per (value head, draft)
+    const int TB = tbl_floats(L, T);
+    const int vpk = HV / HK;
+    for (int x = threadIdx.x; x < HV * T; x += blockDim.x) {
+        const int hv = x / T, j = x - (x / T) * T;
+        const int kh = hv / vpk;
+        float* t = a.ws + ((size_t)b * HV + hv) * TB;
+        const float* gr = a.ring_g + ((size_t)s * HV + hv) * L;
+        auto gate = [&](int m) -> float {
+            return m < c ? gr[(base_eff + m) % L] : a.g[((size_t)b * T + (m - c)) * HV + hv];
+        };
+        const int m = c + j;
+        float* au = t + j * L;
+        float* ao = t + T * L + j * L;
+        // ao_i = prod_{l=i+1..m} gate_l * (k_i . q_j), i <= m
+        // au_i = prod_{l=i+1..m-1} gate_l * (k_i . k_j), i < m
+        float pq = 1.f, pk = 1.f;
+        for (int i = m; i >= 0; --i) {
+            ao[i] = pq * KQ[(kh * L + i) * T + j];
+            if (i < m) {
+                au[i] = pk * KK[(kh * L + i) * T + j];
+                pk *= gate(i);
+            }
+            pq *= gate(i);
+        }
+        for (int i = m + 1; i < L; ++i) {
+            ao[i] = 0.f;
+            au[i] = 0.f;
+        }
+        if (m < L) au[m] = 0.f;
+        // pk = prod_{l<m} gate_l (Gu), pq = prod_{l<=m} gate_l (Go)
+        t[2 * T * L + j] = pk;
+        t[2 * T * L + T + j] = pq;
+        t[2 * T * L + 2 * T + j] = a.beta[((size_t)b * T + j) * HV + hv];
+        t[2 * T * L + 3 * T + j] = a.g[((size_t)b * T + j) * HV + hv];
+        if (j == 0) {
+            t[2 * T * L + 4 * T] = __int_as_float(c);
+            t[2 * T * L + 4 * T + 1] = __int_as_float(base_eff);
+        }
+    }
+}
+
+// ----------------------------------------------------------------------------
+// verify (persistent, TMA bulk pipeline)
+// ----------------------------------------------------------------------------
+
+struct VerArgs {
+    const float* state;
+    const void* q;
+    const void* k;
+    const void* v;
+    float* ring_d;
+    void* ring_v;
+    const int32_t* ci;
+    const int32_t* slot_wp;
+    const int32_t* slot_base;
+    const uint8_t* slot_flush;
+    const float* ws;
+    void* o;
+    int32_t* dev_err;
+    int batch, T, HV, HK, V, L, num_slots, act_bf16, out_bf16;
+    int stages, stage_bytes, work_off;
+    int off_kq, off_v, off_d, off_tbl;
+};
+
+struct VMeta {
+    int valid, s, b, hv, vb, c, base_eff, pad;
+};
+
+template <int DP>
+__global__ void __launch_bounds__(kThreads) verify_kernel(const VerArgs a) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
+    VMeta* meta = reinterpret_cast<VMeta*>(smem + 128);
+    int* abort_flag = reinterpret_cast<int*>(smem + 128 + kMaxStages * sizeof(VMeta));
+    float* W = reinterpret_cast<float*>(smem + a.work_off);      // [2T][VB] S0 dots
+    float* Dd = W + 2 * kMaxT * VB;                              // [T][VB] draft d
+    uint8_t* stage0 = smem + a.work_off + 3 * kMaxT * VB * 4;
+
+    constexpr int RC = 32 / DP;  // value rows per reduce-scatter chunk
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int T = a.T, HV = a.HV, HK = a.HK, V = a.V, L = a.L;
+    const int NVB = V / VB;
+    const int sa = a.act_bf16 ? 2 : 4;
+    const int TB = tbl_floats(L, T);
+    const int per_row = HV * NVB;
+    const int n_items = a.batch * per_row;
+    const int stages = a.stages;
+
+    if (tid == 0) {
+        for (int st = 0; st < stages; ++st) mbar_init(&bars[st], 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    uint64_t pol = 0;
+    auto issue = [&](int kk) {
+        const int item = blockIdx.x + kk * gridDim.x;
+        if (item >= n_items) return;
+        const int st = kk % stages;
+        uint8_t* sb = stage0 + st * a.stage_bytes;
+        const int b = item / per_row;
+        const int rem = item - b * per_row;
+        const int hv = rem / NVB, vb = rem - (rem / NVB) * NVB;
+        const int s = a.ci[b];
+        VMeta m{0, s, b, hv, vb, 0, 0, 0};
+        if (s >= a.num_slots) {
+            set_dev_err(a.dev_err, RSSM_DEVERR_SLOT);
+        } else if (s >= 0) {
+            int c, be;
+            if (history(a.slot_wp[s], a.slot_base[s], a.slot_flush[s], L, T, &c, &be)) {
+                m.valid = 1;
+                m.c = c;
+                m.base_eff = be;
+            } else {
+                set_dev_err(a.dev_err, RSSM_DEVERR_CURSOR);
+            }
+        }
+        meta[st] = m;
+        if (!m.valid) {
+            mbar_arrive_plain(&bars[st]);
+            return;
+        }
+        const int kh = hv / (HV / HK);
+        const uint32_t kb = KD * sa;
+        const uint32_t tx = TILE + 2 * T * kb + T * VB * sa + m.c * VB * 4 + TB * 4;
+        mbar_arrive_expect_tx(&bars[st], tx);
+        bulk_g2s_hint(sb, a.state + (((size_t)s * HV + hv) * V + (size_t)vb * VB) * KD, TILE, &bars[st],
+                      pol);
+        for (int j = 0; j < T; ++j) {
+            const size_t src = (((size_t)b * T + j) * HK + kh) * kb;
+            bulk_g2s(sb + a.off_kq + (2 * j) * kb, static_cast<const char*>(a.k) + src, kb, &bars[st]);
+            bulk_g2s(sb + a.off_kq + (2 * j + 1) * kb, static_cast<const char*>(a.q) + src, kb,
+                     &bars[st]);
+            bulk_g2s(sb + a.off_v + j * VB * sa,
+                     static_cast<const char*>(a.v) +
+                         ((((size_t)b * T + j) * HV + hv) * V + (size_t)vb * VB) * sa,
+                     VB * sa, &bars[st]);
+        }
+        const float* dr = a.ring_d + ((size_t)s * HV + hv) * L * V + (size_t)vb * VB;
+        for (int i = 0; i < m.c; ++i)
+            bulk_g2s(sb + a.off_d + i * VB * 4, dr + (size_t)((m.base_eff + i) % L) * V, VB * 4,
+                     &bars[st]);
+        bulk_g2s(sb + a.off_tbl, a.ws + ((size_t)b * HV + hv) * TB, TB * 4, &bars[st]);
+    };
+    if (tid == 0) {
+        pol = policy_evict_first();
+        for (int kk = 0; kk < stages; ++kk) issue(kk);
+    }
+
+    int kk = 0;
+    for (;; ++kk) {
+        const int item = blockIdx.x + kk * gridDim.x;
+        if (item >= n_items) break;
+        const int st = kk % stages;
+        const uint32_t par = (kk / stages) & 1;
+        // all threads agree on the outcome, so the branch below stays uniform
+        const bool ok = __syncthreads_and(mbar_wait_bounded(&bars[st], par) ? 1 : 0) != 0;
+        if (!ok) {
+            *abort_flag = 1;
+            set_dev_err(a.dev_err, RSSM_DEVERR_TIMEOUT);
+        }
+        const VMeta m = meta[st];
+        if (ok && m.valid) {
+            const uint8_t* sb = stage0 + st * a.stage_bytes;
+            const float* tile = reinterpret_cast<const float*>(sb);
+            const uint8_t* kq = sb + a.off_kq;
+            // phase A: S0 . k_j and S0 . q_j for every value row
+            float vec[DP][4];
+#pragma unroll
+            for (int d = 0; d < DP; ++d) {
+                if (d < 2 * T) {
+                    load4(kq + (size_t)d * KD * sa, lane * 4, a.act_bf16, vec[d]);
+                } else {
+                    vec[d][0] = vec[d][1] = vec[d][2] = vec[d][3] = 0.f;
+                }
+            }
+#pragma unroll
+            for (int ch = 0; ch < 16 / RC; ++ch) {
+                float part[32];
+#pragma unroll
+                for (int jr = 0; jr < RC; ++jr) {
+                    const int r = warp + 4 * (ch * RC + jr);
+                    const float4 s4 = *reinterpret_cast<const float4*>(tile + r * KD + lane * 4);
+#pragma unroll
+                    for (int d = 0; d < DP; ++d)
+                        part[jr * DP + d] =
+                            s4.x * vec[d][0] + s4.y * vec[d][1] + s4.z * vec[d][2] + s4.w * vec[d][3];
+                }
+                reduce_scatter<32, 32>(part);  // lane l holds entry l
+                const int jr = lane / DP, d = lane % DP;
+                if (d < 2 * T) W[d * VB + warp + 4 * (ch * RC + jr)] = part[0];
+            }
+            __syncthreads();
+            // phase B: the draft chain, one thread per value row
+            if (tid < VB) {
+                const int r = tid;
+                const float* t = reinterpret_cast<const float*>(sb + a.off_tbl);
+                const float* dh = reinterpret_cast<const float*>(sb + a.off_d);
+                const int c = m.c;
+                const size_t vi = (size_t)m.vb * VB + r;
+                for (int j = 0; j < T; ++j) {
+                    const float* au = t + j * L;
+                    const float* ao = t + T * L + j * L;
+                    const int mm = c + j;
+                    float u = t[2 * T * L + j] * W[(2 * j) * VB + r];
+                    float oo = t[2 * T * L + T + j] * W[(2 * j + 1) * VB + r];
+                    for (int i = 0; i < c; ++i) {
+                        const float di = dh[i * VB + r];
+                        u = fmaf(au[i], di, u);
+                        oo = fmaf(ao[i], di, oo);
+                    }
+                    for (int i = c; i < mm; ++i) {
+                        const float di = Dd[(i - c) * VB + r];
+                        u = fmaf(au[i], di, u);
+                        oo = fmaf(ao[i], di, oo);
+                    }
+                    const float vr = load1(sb + a.off_v + j * VB * sa, r, a.act_bf16);
+                    const float dn = t[2 * T * L + 2 * T + j] * (vr - t[2 * T * L + 3 * T + j] * u);
+                    Dd[j * VB + r] = dn;
+                    oo = fmaf(ao[mm], dn, oo);
+                    const int pos = (m.base_eff + c + j) % L;
+                    store1(a.o, (((size_t)m.b * T + j) * HV + m.hv) * V + vi, a.out_bf16, oo);
+                    a.ring_d[(((size_t)m.s * HV + m.hv) * L + pos) * V + vi] = dn;
+                    store1(a.ring_v, (((size_t)m.s * HV + m.hv) * L + pos) * V + vi, a.act_bf16, vr);
+                }
+            }
+        }
+        __syncthreads();
+        if (*abort_flag) break;
+        if (tid == 0) issue(kk + stages);
+    }
+    if (*abort_flag && tid == 0) {
+        for (int j = kk; j < kk + stages; ++j) {
+            const int item = blockIdx.x + j * gridDim.x;
+            if (item >= n_items) break;
+            mbar_wait_bounded(&bars[j % stages], (j / stages) & 1);
+        }
+    }
+}
+
+}  // namespace spec
+}  // namespace rssm
+
+using namespace rssm;
+
+extern "C" size_t rssm_gdn_spec_workspace_size(const rssm_gdn_dims* d, int32_t T) {
+    if (!d || d->batch < 0 || d->num_v_heads <= 0 || d->ring_len < 1 || T < 1 || T > spec::kMaxT)
+        return 0;
+    return (size_t)d->batch * d->num_v_heads * spec::tbl_floats(d->ring_len, T) * sizeof(float);
+}
+
+extern "C" int rssm_gdn_spec_verify(const rssm_gdn_dims* d, int32_t T, float* state, const void* q,
+                                    const void* k, const void* v, const float* beta,
+                                    const float* g, float* ring_d, void* ring_k, float* ring_g,
+                                    void* ring_v, float* ring_beta, const int32_t* cache_indices,
+                                    const int32_t* slot_wp, const int32_t* slot_base,
+                                    const uint8_t* slot_flush, void* workspace,
+                                    size_t workspace_bytes, void* o, int32_t* dev_err,
+                                    rssm_stream_t stream) {
+    if (!d) return RSSM_ERR_INVALID_ARG;
+    if (d->batch < 0 || d->num_v_heads <= 0 || d->num_k_heads <= 0 || d->head_k_dim <= 0 ||
+        d->head_v_dim <= 0 || d->num_slots <= 0 || !ok_dtype(d->act_dtype) || !ok_dtype(d->out_dtype))
+        return RSSM_ERR_INVALID_ARG;
+    if (d->ring_len < 1 || d->num_v_heads % d->num_k_heads || T < 1 || d->ring_len < 2 * T)
+        return RSSM_ERR_CONFIG;
+    if (d->head_k_dim != spec::KD || d->head_v_dim % spec::VB || T > spec::kMaxT)
+        return RSSM_ERR_UNSUPPORTED;
+    if (d->batch == 0) return RSSM_OK;
+    if (!ok_ptr(state) || !ok_ptr(q) || !ok_ptr(k) || !ok_ptr(v) || !ok_ptr(beta) || !ok_ptr(g) ||
+        !ok_ptr(ring_d) || !ok_ptr(ring_k) || !ok_ptr(ring_g) || !ok_ptr(ring_v) ||
+        !ok_ptr(ring_beta) || !ok_ptr(cache_indices) || !ok_ptr(slot_wp) || !ok_ptr(slot_base) ||
+        !ok_ptr(slot_flush) || !ok_ptr(workspace) || !ok_ptr(o))
+        return RSSM_ERR_INVALID_ARG;
+    if (workspace_bytes < rssm_gdn_spec_workspace_size(d, T)) return RSSM_ERR_INVALID_ARG;
+    DeviceInfo di;
+    if (!device_info(&di)) return RSSM_ERR_CUDA;
+    cudaStream_t st = (cudaStream_t)stream;
+    const int HV = d->num_v_heads, HK = d->num_k_heads, V = d->head_v_dim, L = d->ring_len;
+    const int NVB = V / spec::VB;
+    const bool abf = d->act_dtype == RSSM_BF16;
+    const int sa = abf ? 2 : 4;
+
+    // 1. exact fold of slots with a pending fold
+    spec::FoldArgs fa{state, ring_k, ring_v, ring_g, ring_beta, cache_indices, slot_wp, slot_base,
+                      slot_flush, dev_err, HV, HK, V, L, d->num_slots, abf};
+    spec::fold_kernel<<<d->batch * HV * NVB, spec::kThreads, 0, st>>>(fa);
+    if (launch_status()) return RSSM_ERR_CUDA;
+
+    // 2. precompute: key dots, gate products, S-independent ring entries
+    const int psmem = 2 * HK * L * T * 4;
+    if (psmem > di.max_smem_optin) return RSSM_ERR_UNSUPPORTED;
+    if (psmem > 48 * 1024 &&
+        !ensure_smem_limit(reinterpret_cast<const void*>(spec::spec_pre_kernel), psmem))
+        return RSSM_ERR_CUDA;
+    spec::PreArgs pa{q, k, beta, g, ring_k, ring_g, ring_beta, cache_indices, slot_wp, slot_base,
+                     slot_flush, static_cast<float*>(workspace), dev_err, T, HV, HK, L,
+                     d->num_slots, abf};
+    spec::spec_pre_kernel<<<d->batch, 256, psmem, st>>>(pa);
+    if (launch_status()) return RSSM_ERR_CUDA;
+
+    // 3. verify
+    spec::VerArgs va{};
+    va.state = state; va.q = q; va.k = k; va.v = v; va.ring_d = ring_d; va.ring_v = ring_v;
+    va.ci = cache_indices; va.slot_wp = slot_wp; va.slot_base = slot_base; va.slot_flush = slot_flush;
+    va.ws = static_cast<const float*>(workspace); va.o = o; va.dev_err = dev_err;
+    va.batch = d->batch; va.T = T; va.HV = HV; va.HK = HK; va.V = V; va.L = L;
+    va.num_slots = d->num_slots; va.act_bf16 = abf; va.out_bf16 = d->out_dtype == RSSM_BF16;
+    int off = spec::TILE;
+    va.off_kq = off;  off += 2 * T * spec::KD * sa;
+    va.off_v = off;   off += T * spec::VB * sa;
+    va.off_d = off;   off += L * spec::VB * 4;
+    va.off_tbl = off; off += spec::tbl_floats(L, T) * 4;
+    va.stage_bytes = (off + 127) & ~127;
+    va.work_off = 1024;
+    const int fixed = va.work_off + 3 * spec::kMaxT * spec::VB * 4;
+    PipeShape ps;
+    if (!pick_pipe_shape(di, va.stage_bytes, fixed, spec::kMaxStages, &ps)) return RSSM_ERR_UNSUPPORTED;
+    va.stages = ps.stages;
+    const long items = (long)d->batch * HV * NVB;
+    long grid = (long)di.sm_count * ps.ctas_per_sm;
+    if (grid > items) grid = items;
+    const void* kfn;
+    const int dp = T <= 1 ? 2 : (T <= 2 ? 4 : (T <= 4 ? 8 : 16));
+    switch (dp) {
+        case 2: kfn = reinterpret_cast<const void*>(spec::verify_kernel<2>); break;
+        case 4: kfn = reinterpret_cast<const void*>(spec::verify_kernel<4>); break;
+        case 8: kfn = reinterpret_cast<const void*>(spec::verify_kernel<8>); break;
+        default: kfn = reinterpret_cast<const void*>(spec::verify_kernel<16>); break;
+    }
+    if (!ensure_smem_limit(kfn, ps.smem_bytes)) return RSSM_ERR_CUDA;
+    switch (dp) {
+        case 2: spec::verify_kernel<2><<<(int)grid, spec::kThreads, ps.smem_bytes, st>>>(va); break;
+        case 4: spec::verify_kernel<4><<<(int)grid, spec::kThreads, ps.smem_bytes, st>>>(va); break;
+        case 8: spec::verify_kernel<8><<<(int)grid, spec::kThreads, ps.smem_bytes, st>>>(va); break;
+        default: spec::verify_kernel<16><<<(int)grid, spec::kThreads, ps.smem_bytes, st>>>(va); break;
+    }
+    return launch_status();
+}

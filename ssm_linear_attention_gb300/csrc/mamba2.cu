@@ -300,7 +300,8 @@ __global__ void __launch_bounds__(kThreads) output_kernel(const OutArgs a) {
         if (item >= n_items) break;
         const int st = k % stages;
         const uint32_t par = (k / stages) & 1;
-        const bool ok = mbar_wait_bounded(&bars[st], par);
+        // all threads agree on the outcome, so the branch below stays uniform
+        const bool ok = __syncthreads_and(mbar_wait_bounded(&bars[st], par) ? 1 : 0) != 0;
         if (!ok) {
             *abort_flag = 1;
             set_dev_err(a.dev_err, RSSM_DEVERR_TIMEOUT);
@@ -463,7 +464,8 @@ __global__ void __launch_bounds__(kThreads) full_state_kernel(const FullArgs a) 
         if (item >= n_items) break;
         const int st = k % stages;
         const uint32_t par = (k / stages) & 1;
-        const bool ok = mbar_wait_bounded(&bars[st], par);
+        // all threads agree on the outcome, so the branch below stays uniform
+        const bool ok = __syncthreads_and(mbar_wait_bounded(&bars[st], par) ? 1 : 0) != 0;
         if (!ok) {
             *abort_flag = 1;
             set_dev_err(a.dev_err, RSSM_DEVERR_TIMEOUT);

@@ -189,10 +189,10 @@ class GDNReplayDecoder:
                               cache_indices, self.row_wp, self.workspace, self.ws_bytes,
                               self.dev_err, stream)
 
-    def output(self, v, cache_indices, o=None, stream=None):
+    def output(self, q, v, cache_indices, o=None, stream=None):
         b = v.shape[0]
         o = self.o[:b] if o is None else o
-        B.rssm_gdn_output(self.dims(b), self.state, v, self.ring_k, self.ring_d, cache_indices,
+        B.rssm_gdn_output(self.dims(b), self.state, q, v, self.ring_k, self.ring_d, cache_indices,
                           self.row_wp, self.row_flush, self.workspace, self.ws_bytes, o,
                           self.dev_err, stream)
         return o
@@ -203,7 +203,7 @@ class GDNReplayDecoder:
             self.advance(cache_indices, force_flush, stream)
         self.append(k, g, cache_indices, stream)
         self.precompute(q, k, beta, g, cache_indices, stream)
-        return self.output(v, cache_indices, o, stream)
+        return self.output(q, v, cache_indices, o, stream)
 
     def reset_slots(self, slots, stream=None):
         B.rssm_advance_cursors(B.RSSM_CURSOR_RESET, self.slot_wp, None, None, slots, None, None,
@@ -267,6 +267,8 @@ class GDNSpecVerifier:
         self.row_flush = torch.zeros(max_batch, device=dev, dtype=torch.uint8)
         self.dev_err = torch.zeros(4, device=dev, dtype=torch.int32)
         self.o = torch.empty(max_batch, T, num_v_heads, head_v_dim, device=dev, dtype=out_dtype)
+        self.ws_bytes = B.rssm_gdn_spec_workspace_size(self.dims(max_batch), T)
+        self.workspace = torch.empty(max(self.ws_bytes, 16), device=dev, dtype=torch.uint8)
 
     def dims(self, batch):
         return B.GDNDims(batch, self.HV, self.HK, self.K, self.V, self.L, self.num_slots,
@@ -278,8 +280,8 @@ class GDNSpecVerifier:
         o = self.o[:b] if o is None else o
         B.rssm_gdn_spec_verify(self.dims(b), self.T, self.state, q, k, v, beta, g, self.ring_d,
                                self.ring_k, self.ring_g, self.ring_v, self.ring_beta,
-                               cache_indices, self.slot_cnt, self.slot_base, self.slot_flush, o,
-                               self.dev_err, stream)
+                               cache_indices, self.slot_cnt, self.slot_base, self.slot_flush,
+                               self.workspace, self.ws_bytes, o, self.dev_err, stream)
         return o
 
     def commit(self, cache_indices, num_accepted, stream=None):

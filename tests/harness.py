@@ -135,3 +135,79 @@ def cursor_reference(wl, steps=None):
         wps.append(rw)
         fls.append(rf)
     return np.array(wps), np.array(fls), np.array(slot_wp)
+
+
+# --------------------------------------------------------------------------- #
+# gated delta net                                                             #
+# --------------------------------------------------------------------------- #
+
+def make_gdn_decoder(wl, out_dtype=torch.float32, full_state=False):
+    from ssm_linear_attention_gb300 import GDNFullStateDecoder, GDNReplayDecoder
+    ad = torch_dt(wl.act_dtype)
+    if full_state:
+        dec = GDNFullStateDecoder(wl.num_v_heads, wl.num_k_heads, wl.head_k_dim, wl.head_v_dim,
+                                  wl.num_slots, max(wl.batch, 1), act_dtype=ad, out_dtype=out_dtype)
+    else:
+        dec = GDNReplayDecoder(wl.num_v_heads, wl.num_k_heads, wl.head_k_dim, wl.head_v_dim, wl.L,
+                               wl.num_slots, max(wl.batch, 1), act_dtype=ad, out_dtype=out_dtype)
+    for s in wl.cache_indices():
+        dec.state[int(s)] = to_dev(wl.slot_state(int(s)), torch.float32)
+    return dec
+
+
+def gdn_inputs_dev(wl, inp):
+    ad = torch_dt(wl.act_dtype)
+    return (to_dev(inp["q"], ad), to_dev(inp["k"], ad), to_dev(inp["v"], ad),
+            to_dev(inp["beta"], torch.float32), to_dev(inp["g"], torch.float32))
+
+
+def run_gpu_gdn(wl, steps=None, out_dtype=torch.float32, full_state=False, rows=None):
+    steps = wl.steps if steps is None else steps
+    dec = make_gdn_decoder(wl, out_dtype, full_state)
+    rows = np.arange(wl.batch) if rows is None else np.asarray(rows)
+    for j in range(wl.max_history()):
+        q, k, v, be, g = gdn_inputs_dev(wl, wl.history_inputs(j))
+        dec.step(q, k, v, be, g, to_dev(wl.history_ci(j), torch.int32))
+    ci_d = to_dev(wl.cache_indices(), torch.int32)
+    os_, wps, fls = [], [], []
+    sel = torch.as_tensor(rows, device="cuda")
+    for t in range(steps):
+        q, k, v, be, g = gdn_inputs_dev(wl, wl.step_inputs(t))
+        if full_state:
+            o = dec.step(q, k, v, be, g, ci_d)
+        else:
+            f = wl.force_mask(t)
+            o = dec.step(q, k, v, be, g, ci_d, None if f is None else to_dev(f, torch.uint8))
+            wps.append(dec.row_wp[: wl.batch].cpu().numpy().copy())
+            fls.append(dec.row_flush[: wl.batch].cpu().numpy().copy())
+        os_.append(o[sel].float().cpu().numpy().astype(np.float64))
+    torch.cuda.synchronize()
+    return dict(o=os_, row_wp=np.array(wps), row_flush=np.array(fls), dec=dec)
+
+
+def run_gpu_spec(wl, rounds=None, out_dtype=torch.float32, rows=None):
+    from ssm_linear_attention_gb300 import GDNSpecVerifier
+    rounds = wl.rounds if rounds is None else rounds
+    ad = torch_dt(wl.act_dtype)
+    ver = GDNSpecVerifier(wl.num_v_heads, wl.num_k_heads, wl.head_k_dim, wl.head_v_dim, wl.L,
+                          wl.T, wl.num_slots, max(wl.batch, 1), act_dtype=ad, out_dtype=out_dtype)
+    ci = wl.cache_indices()
+    for s in ci:
+        ver.state[int(s)] = to_dev(wl.slot_state(int(s)), torch.float32)
+    rows = np.arange(wl.batch) if rows is None else np.asarray(rows)
+    sel = torch.as_tensor(rows, device="cuda")
+    ci_d = to_dev(ci, torch.int32)
+    cidx = torch.as_tensor(ci.astype(np.int64), device="cuda")
+    outs, curs = [], []
+    for r in range(rounds):
+        curs.append((ver.slot_cnt[cidx].cpu().numpy(), ver.slot_base[cidx].cpu().numpy(),
+                     ver.slot_flush[cidx].cpu().numpy()))
+        q, k, v, be, g = gdn_inputs_dev(wl, wl.round_inputs(r))
+        o = ver.verify(q, k, v, be, g, ci_d)
+        outs.append(o[sel].float().cpu().numpy().astype(np.float64))
+        ver.commit(ci_d, to_dev(wl.accepted(r), torch.int32))
+    curs.append((ver.slot_cnt[cidx].cpu().numpy(), ver.slot_base[cidx].cpu().numpy(),
+                 ver.slot_flush[cidx].cpu().numpy()))
+    torch.cuda.synchronize()
+    c = np.array(curs, dtype=np.int64)   # [rounds+1, 3, batch]
+    return dict(o=outs, cnt=c[:, 0], base=c[:, 1], flush=c[:, 2], ver=ver)

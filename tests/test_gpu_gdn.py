@@ -1,0 +1,137 @@
+"""GPU parity: gated-delta-net ReplaySSM decode, full-state decode and speculative
+verify vs the oracle (fp32 state: e <= 1e-4; cursors bit-exact)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import rssm_workloads as W
+from oracle import cursors
+from tests import harness as Hn
+
+pytestmark = pytest.mark.gpu
+
+TOL = 1e-4
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    assert torch.cuda.is_available(), "the gpu tests need a CUDA device"
+    import ssm_linear_attention_gb300 as ssm
+    ssm.lib()
+
+
+def _gdn_cursor_ref(wl, steps):
+    slot_wp = [0] * wl.num_slots
+    for j in range(wl.max_history()):
+        cursors.advance_standard(slot_wp, wl.history_ci(j), None, wl.L)
+    wps, fls = [], []
+    for t in range(steps):
+        rw, rf = cursors.advance_standard(slot_wp, wl.cache_indices(), wl.force_mask(t), wl.L)
+        wps.append(rw)
+        fls.append(rf)
+    return np.array(wps), np.array(fls)
+
+
+def _check_gdn(wl, rows, steps, out_dtype=torch.float32):
+    g = Hn.run_gpu_gdn(wl, steps=steps, out_dtype=out_dtype, rows=rows)
+    ref = oracle.gdn_run(wl, rows=rows, steps=steps, mode="replay")
+    cw, cf = _gdn_cursor_ref(wl, steps)
+    assert np.array_equal(g["row_wp"], cw) and np.array_equal(g["row_flush"], cf)
+    for t in range(steps):
+        if out_dtype == torch.bfloat16:
+            d = np.abs(g["o"][t] - ref["o"][t])
+            assert np.all(d <= TOL * np.maximum(1, np.abs(ref["o"][t])) + Hn.bf16_spacing(ref["o"][t]))
+        else:
+            e = Hn.err(g["o"][t], ref["o"][t])
+            assert e <= TOL, "step %d: o error %.3g" % (t, e)
+    ci = wl.cache_indices()
+    st = g["dec"].state[torch.as_tensor(ci[rows].astype(np.int64), device="cuda")].cpu().numpy()
+    ok, e, _ = Hn.state_ok(st, ref["ckpt"], "fp32")
+    assert ok, "checkpoint error %.3g" % e
+    assert int(g["dec"].dev_err.abs().sum()) == 0
+
+
+def test_gdn_small_desync_with_forced_flushes():
+    wl = W.gdn_decode(batch=6, num_v_heads=4, num_k_heads=2, num_slots=12, L=4, steps=14,
+                      wp_mode="uniform", force_rate=0.15)
+    _check_gdn(wl, rows=np.arange(6), steps=14)
+
+
+def test_gdn_decode_config_sampled_rows():
+    # batch 256, HV 32, HK 16, K = V = 128, L 16, 64 steps, fp32 state N(0, 0.05)
+    wl = W.gdn_decode()
+    _check_gdn(wl, rows=[0, 77, 255], steps=wl.steps)
+
+
+def test_gdn_decode_bf16_output_desync():
+    wl = W.gdn_decode(batch=64, num_slots=128, steps=20, wp_mode="uniform")
+    _check_gdn(wl, rows=[1, 40, 63], steps=20, out_dtype=torch.bfloat16)
+
+
+@pytest.mark.parametrize("L", [1, 2, 8])
+def test_gdn_ring_lengths_and_v256(L):
+    wl = W.gdn_decode(batch=5, num_v_heads=4, num_k_heads=4, head_v_dim=256, num_slots=9, L=L,
+                      steps=10, wp_mode="uniform", act_dtype="fp32")
+    _check_gdn(wl, rows=np.arange(5), steps=10)
+
+
+def test_gdn_full_state_kernel():
+    wl = W.gdn_decode(batch=12, num_slots=20, steps=6)
+    g = Hn.run_gpu_gdn(wl, steps=6, full_state=True)
+    ref = oracle.gdn_run(wl, steps=6, mode="full")
+    for t in range(6):
+        assert Hn.err(g["o"][t], ref["o"][t]) <= TOL
+    ci = wl.cache_indices()
+    st = g["dec"].state[torch.as_tensor(ci.astype(np.int64), device="cuda")].cpu().numpy()
+    assert Hn.state_ok(st, ref["ckpt"], "fp32")[0]
+
+
+def _check_spec(wl, rows, rounds):
+    g = Hn.run_gpu_spec(wl, rounds=rounds, rows=rows)
+    ref = oracle.gdn_spec_run(wl, rows=rows, rounds=rounds)
+    # cursors: bit-exact against the integer model for every row
+    cnt, base, fl = [0] * wl.num_slots, [0] * wl.num_slots, [0] * wl.num_slots
+    ci = wl.cache_indices()
+    for r in range(rounds + 1):
+        assert np.array_equal(g["cnt"][r], [cnt[s] for s in ci]), r
+        assert np.array_equal(g["base"][r], [base[s] for s in ci]), r
+        assert np.array_equal(g["flush"][r], [fl[s] for s in ci]), r
+        if r < rounds:
+            cursors.spec_commit(cnt, base, fl, ci, wl.accepted(r), wl.L, wl.T)
+    worst = 0.0
+    for r in range(rounds):
+        e = Hn.err(g["o"][r], ref["o"][r])
+        worst = max(worst, e)
+        assert e <= TOL, "round %d: draft output error %.3g" % (r, e)
+    st = g["ver"].state[torch.as_tensor(ci[rows].astype(np.int64), device="cuda")].cpu().numpy()
+    ok, e, _ = Hn.state_ok(st, ref["ckpt"], "fp32")
+    assert ok, "folded checkpoint error %.3g" % e
+    assert int(g["ver"].dev_err.abs().sum()) == 0
+    return worst
+
+
+def test_spec_small_all_rows():
+    wl = W.gdn_spec(batch=5, num_v_heads=4, num_k_heads=2, num_slots=10, L=8, T=4, rounds=16)
+    _check_spec(wl, rows=np.arange(5), rounds=16)
+
+
+@pytest.mark.parametrize("T,L", [(1, 2), (2, 5), (3, 8), (8, 16)])
+def test_spec_draft_lengths(T, L):
+    wl = W.gdn_spec(batch=4, num_v_heads=2, num_k_heads=1, num_slots=8, L=L, T=T, rounds=12,
+                    act_dtype="fp32")
+    _check_spec(wl, rows=np.arange(4), rounds=12)
+
+
+def test_spec_config_sampled_rows():
+    # batch 128, T 4, HV 32, HK 16, K = V = 128, L 16, 32 rounds, accepted ~ U{0..4}
+    wl = W.gdn_spec()
+    _check_spec(wl, rows=[0, 64, 127], rounds=wl.rounds)
+
+
+def test_spec_rejects_short_ring():
+    import ssm_linear_attention_gb300 as ssm
+    wl = W.gdn_spec(batch=2, num_v_heads=2, num_k_heads=1, num_slots=4, L=7, T=4, rounds=1)
+    with pytest.raises(ssm.RSSMError) as ei:
+        Hn.run_gpu_spec(wl, rounds=1)
+    assert ei.value.status == ssm.RSSM_ERR_CONFIG
