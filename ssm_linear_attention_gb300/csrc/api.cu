@@ -80,19 +80,24 @@ bool ensure_smem_limit(const void* kernel, int bytes) {
     return true;
 }
 
-bool pick_pipe_shape(const DeviceInfo& di, int stage_bytes, int fixed_bytes, int max_stages,
-                     PipeShape* out) {
-    // 1 KB per resident CTA is reserved by the hardware.
-    for (int ctas = 2; ctas >= 1; --ctas) {
-        int budget = di.smem_per_sm / ctas - 1024;
-        if (budget > di.max_smem_optin) budget = di.max_smem_optin;
-        int st = (budget - fixed_bytes) / stage_bytes;
-        if (st > max_stages) st = max_stages;
-        const int need = ctas == 2 ? 3 : 2;
-        if (st >= need) {
-            out->stages = st;
-            out->ctas_per_sm = ctas;
-            out->smem_bytes = fixed_bytes + st * stage_bytes;
+bool pick_pipe(const DeviceInfo& di, int stage_bytes, int warp_scratch, int tile_bytes, int header,
+               int max_stages, int group_warps, int max_groups, PipeCfg* out) {
+    const int budget = di.max_smem_optin;
+    int want = (65536 + tile_bytes - 1) / tile_bytes;
+    if (want < 2) want = 2;
+    for (int ng = max_groups; ng >= 1; --ng) {
+        const int scratch_off = header;
+        const int stage_off = (scratch_off + ng * group_warps * warp_scratch + 127) & ~127;
+        int stages = (budget - stage_off) / stage_bytes;
+        if (stages > max_stages) stages = max_stages;
+        stages -= stages % ng;  // each stage always belongs to the same group
+        const bool ok = ng > 1 ? (stages - ng >= want) : (stages >= 2);
+        if (ok) {
+            out->stages = stages;
+            out->groups = ng;
+            out->stage_off = stage_off;
+            out->scratch_off = scratch_off;
+            out->smem_bytes = stage_off + stages * stage_bytes;
             return true;
         }
     }

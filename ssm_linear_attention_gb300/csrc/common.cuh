@@ -144,6 +144,24 @@ __device__ __forceinline__ void store8(void* p, bool is_bf16, const float* f) {
     }
 }
 
+// acc + sum_{j<8} s_j c_j for 8 bf16 pairs packed in two uint4: each product is
+// formed from the bf16 operands by a mixed-precision fma (f32 accumulate, one
+// rounding per step), so no widening instruction is needed.
+__device__ __forceinline__ float dot8_bf16(const uint4 s, const uint4 c, float acc) {
+    asm("{\n\t.reg .b16 a0, a1, a2, a3, a4, a5, a6, a7, b0, b1, b2, b3, b4, b5, b6, b7;\n\t"
+        "mov.b32 {a0, a1}, %1;\n\tmov.b32 {a2, a3}, %2;\n\t"
+        "mov.b32 {a4, a5}, %3;\n\tmov.b32 {a6, a7}, %4;\n\t"
+        "mov.b32 {b0, b1}, %5;\n\tmov.b32 {b2, b3}, %6;\n\t"
+        "mov.b32 {b4, b5}, %7;\n\tmov.b32 {b6, b7}, %8;\n\t"
+        "fma.rn.f32.bf16 %0, a0, b0, %0;\n\tfma.rn.f32.bf16 %0, a1, b1, %0;\n\t"
+        "fma.rn.f32.bf16 %0, a2, b2, %0;\n\tfma.rn.f32.bf16 %0, a3, b3, %0;\n\t"
+        "fma.rn.f32.bf16 %0, a4, b4, %0;\n\tfma.rn.f32.bf16 %0, a5, b5, %0;\n\t"
+        "fma.rn.f32.bf16 %0, a6, b6, %0;\n\tfma.rn.f32.bf16 %0, a7, b7, %0;\n\t}"
+        : "+f"(acc)
+        : "r"(s.x), "r"(s.y), "r"(s.z), "r"(s.w), "r"(c.x), "r"(c.y), "r"(c.z), "r"(c.w));
+    return acc;
+}
+
 __device__ __forceinline__ float load1(const void* base, long idx, bool is_bf16) {
     return is_bf16 ? bf16_to_f(reinterpret_cast<const uint16_t*>(base)[idx])
                    : reinterpret_cast<const float*>(base)[idx];

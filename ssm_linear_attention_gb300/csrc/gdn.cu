@@ -25,27 +25,16 @@
 // the warp with one 32-way reduce-scatter.
 #include "common.cuh"
 #include "internal.h"
+#include "pipeline.cuh"
 
 namespace rssm {
 namespace gdn {
 
-constexpr int kThreads = 128;
 constexpr int KD = 128;  // key dim handled by these kernels
 constexpr int VB = 64;   // value rows per work item
-constexpr int kMaxStages = 8;
-constexpr int kFixedSmem = 1024;
 constexpr int TILE = VB * KD * 4;
 
 __host__ __device__ inline int tbl_floats(int L) { return (3 * L + 5 + 3) & ~3; }
-
-struct Meta {
-    int valid, s, b, hv, vb, w, f, pad;
-    float beta, g;
-};
-
-__device__ __forceinline__ void mbar_arrive_plain(uint64_t* bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
 
 // 4 consecutive elements (bf16 or f32) at element index i.
 __device__ __forceinline__ void load4(const void* base, int i, bool bf, float* f) {
@@ -95,12 +84,11 @@ __global__ void ring_append_kernel(int HV, int HK, int L, int num_slots, int act
 // precompute
 // ----------------------------------------------------------------------------
 
-__global__ void precompute_kernel(int HV, int HK, int L, int num_slots, int act_bf16,
-                                  const void* __restrict__ q, const void* __restrict__ k,
-                                  const float* __restrict__ beta, const float* __restrict__ g,
-                                  const void* __restrict__ ring_k, const float* __restrict__ ring_g,
-                                  const int32_t* __restrict__ ci, const int32_t* __restrict__ row_wp,
-                                  float* __restrict__ ws) {
+__global__ void __launch_bounds__(256) precompute_kernel(
+    int HV, int HK, int L, int num_slots, int act_bf16, const void* __restrict__ q,
+    const void* __restrict__ k, const float* __restrict__ beta, const float* __restrict__ g,
+    const void* __restrict__ ring_k, const float* __restrict__ ring_g, const int32_t* __restrict__ ci,
+    const int32_t* __restrict__ row_wp, float* __restrict__ ws) {
     extern __shared__ __align__(16) float psm[];
     const int b = blockIdx.x;
     const int s = ci[b];
@@ -108,44 +96,43 @@ __global__ void precompute_kernel(int HV, int HK, int L, int num_slots, int act_
     const int w = row_wp[b];
     if (w < 0 || w >= L) return;
     const int TBL = tbl_floats(L);
-    float* kk = psm;                 // [HK][L]
-    float* kq = kk + HK * L;         // [HK][L]
-    float* kqt = kq + HK * L;        // [HK]
-    float* tbl = psm + ((2 * HK * L + HK + 3) & ~3);  // [HV][TBL]
     const int sa = act_bf16 ? 2 : 4;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    float* kt = psm;              // [HK][KD]
+    float* qt = kt + HK * KD;     // [HK][KD]
+    float* kk = qt + HK * KD;     // [HK][L]
+    float* kq = kk + HK * L;      // [HK][L]
+    float* kqt = kq + HK * L;     // [HK]
+    float* tbl = psm + ((2 * HK * KD + 2 * HK * L + HK + 3) & ~3);  // [HV][TBL]
 
-    for (int pair = warp; pair < HK * (w + 1); pair += nwarps) {
-        const int kh = pair / (w + 1), i = pair % (w + 1);
-        float kt[4], qt[4];
-        load4(static_cast<const char*>(k) + ((size_t)b * HK + kh) * KD * sa, lane * 4, act_bf16, kt);
-        load4(static_cast<const char*>(q) + ((size_t)b * HK + kh) * KD * sa, lane * 4, act_bf16, qt);
+    for (int e = threadIdx.x * 8; e < HK * KD; e += blockDim.x * 8) {
+        load8(static_cast<const char*>(k) + ((size_t)b * HK * KD + e) * sa, act_bf16, kt + e);
+        load8(static_cast<const char*>(q) + ((size_t)b * HK * KD + e) * sa, act_bf16, qt + e);
+    }
+    __syncthreads();
+
+    // one thread per (key head, entry i <= w): kk_i = k_i . k_t, kq_i = k_i . q_t
+    // (i < w, from the ring), kq_t = k_t . q_t (i == w)
+    for (int task = threadIdx.x; task < HK * (w + 1); task += blockDim.x) {
+        const int kh = task / (w + 1), i = task - (task / (w + 1)) * (w + 1);
+        const float* ktk = kt + kh * KD;
+        const float* qtk = qt + kh * KD;
         float a1 = 0.f, a2 = 0.f;
         if (i < w) {
-            float ki[4];
-            load4(static_cast<const char*>(ring_k) + (((size_t)s * HK + kh) * L + i) * KD * sa,
-                  lane * 4, act_bf16, ki);
+            const char* ki = static_cast<const char*>(ring_k) + (((size_t)s * HK + kh) * L + i) * KD * sa;
+            for (int e = 0; e < KD; e += 8) {
+                float k8[8];
+                load8(ki + e * sa, act_bf16, k8);
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                a1 = fmaf(ki[e], kt[e], a1);
-                a2 = fmaf(ki[e], qt[e], a2);
+                for (int j = 0; j < 8; ++j) {
+                    a1 = fmaf(k8[j], ktk[e + j], a1);
+                    a2 = fmaf(k8[j], qtk[e + j], a2);
+                }
             }
+            kk[kh * L + i] = a1;
+            kq[kh * L + i] = a2;
         } else {
-#pragma unroll
-            for (int e = 0; e < 4; ++e) a2 = fmaf(kt[e], qt[e], a2);
-        }
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) {
-            a1 += __shfl_xor_sync(0xffffffffu, a1, o);
-            a2 += __shfl_xor_sync(0xffffffffu, a2, o);
-        }
-        if (lane == 0) {
-            if (i < w) {
-                kk[kh * L + i] = a1;
-                kq[kh * L + i] = a2;
-            } else {
-                kqt[kh] = a2;
-            }
+            for (int e = 0; e < KD; ++e) a2 = fmaf(ktk[e], qtk[e], a2);
+            kqt[kh] = a2;
         }
     }
     __syncthreads();
@@ -183,354 +170,290 @@ __global__ void precompute_kernel(int HV, int HK, int L, int num_slots, int act_
 }
 
 // ----------------------------------------------------------------------------
-// output / flush (persistent, TMA bulk pipeline)
+// output / flush and full-state decode (warp-specialised pipeline)
 // ----------------------------------------------------------------------------
+//
+// A group of two consumer warps owns a (row, value head, 64-row block) tile, 32
+// value rows per warp; lane l holds key columns 4l..4l+3 of every row, so one
+// 16-byte shared load per lane reads one value row. The two dot products per row
+// (with k_t and q_t) of 16 rows reduce with one 32-way reduce-scatter; lanes 0..15
+// then own rows base + lane.
 
-struct OutArgs {
-    float* state;
-    const void* q;
-    const void* v;
-    const void* ring_k;
-    float* ring_d;
-    const int32_t* ci;
-    const int32_t* row_wp;
-    const uint8_t* row_flush;
-    const float* ws;
-    void* o;
-    int32_t* dev_err;
-    int batch, HV, HK, V, L, num_slots, act_bf16, out_bf16;
-    int stages, stage_bytes;
-    int off_k, off_q, off_v, off_d, off_tbl;
-};
+constexpr int kGroupWarps = 2;
+constexpr int RW = VB / kGroupWarps;  // value rows per warp
 
-struct RowMeta {
-    int b, s, w, f;
-};
-
-__global__ void __launch_bounds__(kThreads) output_kernel(const OutArgs a) {
-    extern __shared__ __align__(128) uint8_t smem[];
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
-    Meta* meta = reinterpret_cast<Meta*>(smem + 128);
-    int* abort_flag = reinterpret_cast<int*>(smem + 128 + kMaxStages * sizeof(Meta));
-    uint8_t* stage0 = smem + kFixedSmem;
-
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int HV = a.HV, HK = a.HK, V = a.V, L = a.L;
-    const int NVB = V / VB;
-    const int sa = a.act_bf16 ? 2 : 4;
-    const int TBL = tbl_floats(L);
-    const int n_items = a.batch * HV * NVB;
-    const int stages = a.stages;
-    const int per_row = HV * NVB;
-
-    if (tid == 0) {
-        for (int st = 0; st < stages; ++st) mbar_init(&bars[st], 1);
-        *abort_flag = 0;
-        fence_barrier_init();
-    }
-    __syncthreads();
-
-    uint64_t pol = 0;
-    RowMeta pf{-1, 0, 0, 0};
-    auto load_row = [&](int b) {
-        RowMeta r{b, a.ci[b], 0, 0};
-        if (r.s >= 0 && r.s < a.num_slots) {
-            r.w = a.row_wp[b];
-            r.f = a.row_flush[b];
-        }
-        return r;
+struct OutPolicy {
+    static constexpr int kGroup = kGroupWarps;
+    struct Args {
+        float* state;
+        const void* q;
+        const void* v;
+        const void* ring_k;
+        float* ring_d;
+        const int32_t* ci;
+        const int32_t* row_wp;
+        const uint8_t* row_flush;
+        const float* ws;
+        void* o;
+        int32_t* dev_err;
+        int batch, HV, HK, V, L, num_slots, act_bf16, out_bf16;
+        int stages, stage_bytes, stage_off, scratch_off, warp_scratch;
+        int off_k, off_q, off_v, off_d, off_tbl;
     };
-    auto issue = [&](int k) {
-        const int item = blockIdx.x + k * gridDim.x;
-        if (item >= n_items) return;
-        const int st = k % stages;
-        uint8_t* sb = stage0 + st * a.stage_bytes;
-        const int b = item / per_row;
-        const int rem = item - b * per_row;
+    struct Meta {
+        int valid, s, b, hv, vb, w, f;
+    };
+
+    static __device__ int n_items(const Args& a) { return a.batch * a.HV * (a.V / VB); }
+
+    static __device__ int4 prefetch(const Args& a, int item) {
+        const int b = item / (a.HV * (a.V / VB));
+        const int s = a.ci[b];
+        int w = 0, f = 0;
+        if (s >= 0 && s < a.num_slots) {
+            w = a.row_wp[b];
+            f = a.row_flush[b];
+        }
+        return make_int4(s, w, f, b);
+    }
+
+    static __device__ void issue(const Args& a, int item, int4 r, Meta* meta, uint8_t* sb,
+                                 uint64_t* full, uint64_t pol) {
+        const int NVB = a.V / VB;
+        const int b = r.w;
+        const int rem = item - b * a.HV * NVB;
         const int hv = rem / NVB, vb = rem - (rem / NVB) * NVB;
-        const RowMeta r = (pf.b == b) ? pf : load_row(b);
-        const int nxt = item + gridDim.x;
-        if (nxt < n_items) pf = load_row(nxt / per_row);
-        Meta m;
-        m.b = b; m.hv = hv; m.vb = vb; m.s = r.s; m.w = r.w; m.f = r.f; m.valid = 0; m.pad = 0;
-        m.beta = 0.f; m.g = 0.f;
-        if (r.s >= a.num_slots) {
+        Meta m{0, r.x, b, hv, vb, r.y, r.z};
+        if (r.x >= a.num_slots) {
             set_dev_err(a.dev_err, RSSM_DEVERR_SLOT);
-        } else if (r.s >= 0) {
-            if (r.w < 0 || r.w >= L) set_dev_err(a.dev_err, RSSM_DEVERR_CURSOR);
+        } else if (r.x >= 0) {
+            if (r.y < 0 || r.y >= a.L) set_dev_err(a.dev_err, RSSM_DEVERR_CURSOR);
             else m.valid = 1;
         }
-        meta[st] = m;
+        *meta = m;
         if (!m.valid) {
-            mbar_arrive_plain(&bars[st]);
+            mbar_arrive_plain(full);
             return;
         }
-        const int kh = hv / (HV / HK);
-        const int w = r.w;
+        const int sa = a.act_bf16 ? 2 : 4;
+        const int L = a.L, w = m.w;
+        const int kh = hv / (a.HV / a.HK);
+        const int TBL = tbl_floats(L);
         const uint32_t kb = KD * sa;
-        const uint32_t kbytes = r.f ? (w + 1) * kb : kb;
-        const uint32_t tx = TILE + kbytes + kb + VB * sa + w * VB * 4 + TBL * 4;
-        mbar_arrive_expect_tx(&bars[st], tx);
-        const size_t tile_off = (((size_t)r.s * HV + hv) * V + (size_t)vb * VB) * KD;
-        bulk_g2s_hint(sb, a.state + tile_off, TILE, &bars[st], pol);
-        const char* kr = static_cast<const char*>(a.ring_k) + ((size_t)r.s * HK + kh) * L * kb;
-        if (r.f) bulk_g2s(sb + a.off_k, kr, kbytes, &bars[st]);
-        else bulk_g2s(sb + a.off_k + w * kb, kr + (size_t)w * kb, kb, &bars[st]);
-        bulk_g2s(sb + a.off_q, static_cast<const char*>(a.q) + ((size_t)b * HK + kh) * kb, kb,
-                 &bars[st]);
+        const uint32_t kbytes = m.f ? (w + 1) * kb : kb;
+        mbar_arrive_expect_tx(full, TILE + kbytes + kb + VB * sa + w * VB * 4 + TBL * 4);
+        bulk_g2s_hint(sb, a.state + (((size_t)m.s * a.HV + hv) * a.V + (size_t)vb * VB) * KD, TILE,
+                      full, pol);
+        const char* kr = static_cast<const char*>(a.ring_k) + ((size_t)m.s * a.HK + kh) * L * kb;
+        if (m.f) bulk_g2s(sb + a.off_k, kr, kbytes, full);
+        else bulk_g2s(sb + a.off_k + w * kb, kr + (size_t)w * kb, kb, full);
+        bulk_g2s(sb + a.off_q, static_cast<const char*>(a.q) + ((size_t)b * a.HK + kh) * kb, kb, full);
         bulk_g2s(sb + a.off_v,
-                 static_cast<const char*>(a.v) + (((size_t)b * HV + hv) * V + (size_t)vb * VB) * sa,
-                 VB * sa, &bars[st]);
-        const float* dr = a.ring_d + (((size_t)r.s * HV + hv) * L) * V + (size_t)vb * VB;
-        for (int i = 0; i < w; ++i)
-            bulk_g2s(sb + a.off_d + i * VB * 4, dr + (size_t)i * V, VB * 4, &bars[st]);
-        bulk_g2s(sb + a.off_tbl, a.ws + ((size_t)b * HV + hv) * TBL, TBL * 4, &bars[st]);
-    };
-    if (tid == 0) {
-        pol = policy_evict_first();
-        for (int k = 0; k < stages; ++k) issue(k);
+                 static_cast<const char*>(a.v) + (((size_t)b * a.HV + hv) * a.V + (size_t)vb * VB) * sa,
+                 VB * sa, full);
+        const float* dr = a.ring_d + (((size_t)m.s * a.HV + hv) * L) * a.V + (size_t)vb * VB;
+        for (int i = 0; i < w; ++i) bulk_g2s(sb + a.off_d + i * VB * 4, dr + (size_t)i * a.V, VB * 4, full);
+        bulk_g2s(sb + a.off_tbl, a.ws + ((size_t)b * a.HV + hv) * TBL, TBL * 4, full);
     }
 
-    int k = 0;
-    for (;; ++k) {
-        const int item = blockIdx.x + k * gridDim.x;
-        if (item >= n_items) break;
-        const int st = k % stages;
-        const uint32_t par = (k / stages) & 1;
-        // all threads agree on the outcome, so the branch below stays uniform
-        const bool ok = __syncthreads_and(mbar_wait_bounded(&bars[st], par) ? 1 : 0) != 0;
-        if (!ok) {
-            *abort_flag = 1;
-            set_dev_err(a.dev_err, RSSM_DEVERR_TIMEOUT);
-        }
-        const Meta m = meta[st];
-        if (ok && m.valid) {
-            const uint8_t* sb = stage0 + st * a.stage_bytes;
-            const float* tile = reinterpret_cast<const float*>(sb);
-            const uint8_t* kring = sb + a.off_k;
-            const float* dring = reinterpret_cast<const float*>(sb + a.off_d);
-            const float* t = reinterpret_cast<const float*>(sb + a.off_tbl);
-            const int w = m.w;
-            float k4[4], q4[4];
-            load4(kring + (size_t)w * KD * sa, lane * 4, a.act_bf16, k4);
-            load4(sb + a.off_q, lane * 4, a.act_bf16, q4);
+    static __device__ void consume(const Args& a, int, const Meta& m, const uint8_t* sb, uint8_t*,
+                                   int lane, int wi) {
+        if (!m.valid) return;
+        const bool bf = a.act_bf16;
+        const int sa = bf ? 2 : 4;
+        const int L = a.L, w = m.w;
+        const int rbase = wi * RW;
+        const float* tile = reinterpret_cast<const float*>(sb);
+        const uint8_t* kring = sb + a.off_k;
+        const float* dring = reinterpret_cast<const float*>(sb + a.off_d);
+        const float* t = reinterpret_cast<const float*>(sb + a.off_tbl);
+        float k4[4], q4[4];
+        load4(kring + (size_t)w * KD * sa, lane * 4, bf, k4);
+        load4(sb + a.off_q, lane * 4, bf, q4);
+        constexpr int NCHK = RW / 16;
+        float av[NCHK], cv[NCHK];
+#pragma unroll
+        for (int ch = 0; ch < NCHK; ++ch) {
             float part[32];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-                const float4 s4 = *reinterpret_cast<const float4*>(tile + (warp + 4 * j) * KD + lane * 4);
+                const float4 s4 =
+                    *reinterpret_cast<const float4*>(tile + (rbase + ch * 16 + j) * KD + lane * 4);
                 part[j] = s4.x * k4[0] + s4.y * k4[1] + s4.z * k4[2] + s4.w * k4[3];
                 part[16 + j] = s4.x * q4[0] + s4.y * q4[1] + s4.z * q4[2] + s4.w * q4[3];
             }
-            reduce_scatter<32, 32>(part);  // lane l now holds entry l
-            const float cdot = __shfl_down_sync(0xffffffffu, part[0], 16);
-            const float Gu = t[3 * L], Go = t[3 * L + 1], kqt = t[3 * L + 2];
-            const float bt = t[3 * L + 3], gt = t[3 * L + 4];
-            float dt_new = 0.f;
-            const int r = warp + 4 * (lane & 15);
+            reduce_scatter<32, 32>(part);  // lane l holds entry l
+            av[ch] = part[0];
+            cv[ch] = __shfl_down_sync(kFull, part[0], 16);
+        }
+        const float Gu = t[3 * L], Go = t[3 * L + 1], kqt = t[3 * L + 2];
+        const float bt = t[3 * L + 3], gt = t[3 * L + 4];
+        float dtv[NCHK];
+#pragma unroll
+        for (int ch = 0; ch < NCHK; ++ch) {
+            dtv[ch] = 0.f;
             if (lane < 16) {
-                float u = Gu * part[0];
-                float oo = Go * cdot;
+                const int r = rbase + ch * 16 + lane;
+                float u = Gu * av[ch];
+                float oo = Go * cv[ch];
                 for (int i = 0; i < w; ++i) {
                     const float di = dring[i * VB + r];
                     u = fmaf(t[i], di, u);
                     oo = fmaf(t[L + i], di, oo);
                 }
-                const float vr = load1(sb + a.off_v, r, a.act_bf16);
-                dt_new = bt * (vr - gt * u);
-                oo = fmaf(kqt, dt_new, oo);
+                const float dn = bt * (load1(sb + a.off_v, r, bf) - gt * u);
+                oo = fmaf(kqt, dn, oo);
                 const size_t vi = (size_t)m.vb * VB + r;
-                store1(a.o, ((size_t)m.b * HV + m.hv) * V + vi, a.out_bf16, oo);
-                a.ring_d[(((size_t)m.s * HV + m.hv) * L + w) * V + vi] = dt_new;
+                store1(a.o, ((size_t)m.b * a.HV + m.hv) * a.V + vi, a.out_bf16, oo);
+                a.ring_d[(((size_t)m.s * a.HV + m.hv) * L + w) * a.V + vi] = dn;
+                dtv[ch] = dn;
             }
-            if (m.f) {
-                float dcur[16];
+        }
+        if (m.f) {
+            // S = Go S0 + sum_{i<=w} Gamma_i d_i k_i^T (d_w = this step's d)
+            float* dst = a.state + (((size_t)m.s * a.HV + m.hv) * a.V + (size_t)m.vb * VB) * KD;
+#pragma unroll 1
+            for (int hb = 0; hb < 2 * NCHK; ++hb) {  // blocks of 8 value rows
+                const int r0 = rbase + hb * 8;
+                const float dsrc = (hb >> 1) == 0 ? dtv[0] : dtv[NCHK - 1];
+                float dcur[8];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) dcur[j] = __shfl_sync(0xffffffffu, dt_new, j);
-                float acc[16][4];
+                for (int j = 0; j < 8; ++j) dcur[j] = __shfl_sync(kFull, dsrc, (hb & 1) * 8 + j);
+                float acc[8][4];
 #pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const float4 s4 = *reinterpret_cast<const float4*>(tile + (warp + 4 * j) * KD + lane * 4);
+                for (int j = 0; j < 8; ++j) {
+                    const float4 s4 = *reinterpret_cast<const float4*>(tile + (r0 + j) * KD + lane * 4);
                     acc[j][0] = Go * s4.x; acc[j][1] = Go * s4.y;
                     acc[j][2] = Go * s4.z; acc[j][3] = Go * s4.w;
                 }
                 for (int i = 0; i <= w; ++i) {
                     float ki[4];
-                    load4(kring + (size_t)i * KD * sa, lane * 4, a.act_bf16, ki);
+                    load4(kring + (size_t)i * KD * sa, lane * 4, bf, ki);
                     const float ti = t[2 * L + i];
 #pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const float dj = (i < w) ? dring[i * VB + warp + 4 * j] : dcur[j];
+                    for (int j = 0; j < 8; ++j) {
+                        const float dj = (i < w) ? dring[i * VB + r0 + j] : dcur[j];
                         const float c = ti * dj;
 #pragma unroll
                         for (int e = 0; e < 4; ++e) acc[j][e] = fmaf(c, ki[e], acc[j][e]);
                     }
                 }
-                float* dst = a.state + (((size_t)m.s * HV + m.hv) * V + (size_t)m.vb * VB) * KD;
 #pragma unroll
-                for (int j = 0; j < 16; ++j)
-                    *reinterpret_cast<float4*>(dst + (warp + 4 * j) * KD + lane * 4) =
+                for (int j = 0; j < 8; ++j)
+                    *reinterpret_cast<float4*>(dst + (r0 + j) * KD + lane * 4) =
                         make_float4(acc[j][0], acc[j][1], acc[j][2], acc[j][3]);
             }
         }
-        __syncthreads();
-        if (*abort_flag) break;
-        if (tid == 0) issue(k + stages);
     }
-    if (*abort_flag && tid == 0) {
-        for (int j = k; j < k + stages; ++j) {
-            const int item = blockIdx.x + j * gridDim.x;
-            if (item >= n_items) break;
-            mbar_wait_bounded(&bars[j % stages], (j / stages) & 1);
-        }
-    }
-}
-
-// ----------------------------------------------------------------------------
-// full-state decode (the conventional kernel)
-// ----------------------------------------------------------------------------
-
-struct FullArgs {
-    float* state;
-    const void* q;
-    const void* k;
-    const void* v;
-    const float* beta;
-    const float* g;
-    const int32_t* ci;
-    void* o;
-    int32_t* dev_err;
-    int batch, HV, HK, V, num_slots, act_bf16, out_bf16;
-    int stages, stage_bytes;
-    int off_k, off_q, off_v;
 };
 
-__global__ void __launch_bounds__(kThreads) full_state_kernel(const FullArgs a) {
-    extern __shared__ __align__(128) uint8_t smem[];
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
-    Meta* meta = reinterpret_cast<Meta*>(smem + 128);
-    int* abort_flag = reinterpret_cast<int*>(smem + 128 + kMaxStages * sizeof(Meta));
-    uint8_t* stage0 = smem + kFixedSmem;
+struct FullPolicy {
+    static constexpr int kGroup = kGroupWarps;
+    struct Args {
+        float* state;
+        const void* q;
+        const void* k;
+        const void* v;
+        const float* beta;
+        const float* g;
+        const int32_t* ci;
+        void* o;
+        int32_t* dev_err;
+        int batch, HV, HK, V, num_slots, act_bf16, out_bf16;
+        int stages, stage_bytes, stage_off, scratch_off, warp_scratch;
+        int off_k, off_q, off_v;
+    };
+    struct Meta {
+        int valid, s, b, hv, vb;
+        float beta, g;
+    };
 
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int HV = a.HV, HK = a.HK, V = a.V;
-    const int NVB = V / VB;
-    const int sa = a.act_bf16 ? 2 : 4;
-    const int n_items = a.batch * HV * NVB;
-    const int stages = a.stages;
-    const int per_row = HV * NVB;
+    static __device__ int n_items(const Args& a) { return a.batch * a.HV * (a.V / VB); }
 
-    if (tid == 0) {
-        for (int st = 0; st < stages; ++st) mbar_init(&bars[st], 1);
-        *abort_flag = 0;
-        fence_barrier_init();
-    }
-    __syncthreads();
-
-    uint64_t pol = 0;
-    auto issue = [&](int k) {
-        const int item = blockIdx.x + k * gridDim.x;
-        if (item >= n_items) return;
-        const int st = k % stages;
-        uint8_t* sb = stage0 + st * a.stage_bytes;
-        const int b = item / per_row;
-        const int rem = item - b * per_row;
-        const int hv = rem / NVB, vb = rem - (rem / NVB) * NVB;
+    static __device__ int4 prefetch(const Args& a, int item) {
+        const int NVB = a.V / VB;
+        const int b = item / (a.HV * NVB);
+        const int hv = (item - b * a.HV * NVB) / NVB;
         const int s = a.ci[b];
-        Meta m;
-        m.b = b; m.hv = hv; m.vb = vb; m.s = s; m.w = 0; m.f = 0; m.valid = 0; m.pad = 0;
-        m.beta = 0.f; m.g = 0.f;
-        if (s >= a.num_slots) set_dev_err(a.dev_err, RSSM_DEVERR_SLOT);
-        else if (s >= 0) m.valid = 1;
-        if (m.valid) {
-            m.beta = a.beta[(size_t)b * HV + hv];
-            m.g = a.g[(size_t)b * HV + hv];
+        float be = 0.f, gg = 0.f;
+        if (s >= 0 && s < a.num_slots) {
+            be = a.beta[(size_t)b * a.HV + hv];
+            gg = a.g[(size_t)b * a.HV + hv];
         }
-        meta[st] = m;
+        return make_int4(s, b, __float_as_int(be), __float_as_int(gg));
+    }
+
+    static __device__ void issue(const Args& a, int item, int4 r, Meta* meta, uint8_t* sb,
+                                 uint64_t* full, uint64_t pol) {
+        const int NVB = a.V / VB;
+        const int b = r.y;
+        const int rem = item - b * a.HV * NVB;
+        const int hv = rem / NVB, vb = rem - (rem / NVB) * NVB;
+        Meta m{0, r.x, b, hv, vb, __int_as_float(r.z), __int_as_float(r.w)};
+        if (r.x >= a.num_slots) set_dev_err(a.dev_err, RSSM_DEVERR_SLOT);
+        else if (r.x >= 0) m.valid = 1;
+        *meta = m;
         if (!m.valid) {
-            mbar_arrive_plain(&bars[st]);
+            mbar_arrive_plain(full);
             return;
         }
-        const int kh = hv / (HV / HK);
+        const int sa = a.act_bf16 ? 2 : 4;
+        const int kh = hv / (a.HV / a.HK);
         const uint32_t kb = KD * sa;
-        mbar_arrive_expect_tx(&bars[st], TILE + 2 * kb + VB * sa);
-        bulk_g2s_hint(sb, a.state + (((size_t)s * HV + hv) * V + (size_t)vb * VB) * KD, TILE, &bars[st],
-                      pol);
-        bulk_g2s(sb + a.off_k, static_cast<const char*>(a.k) + ((size_t)b * HK + kh) * kb, kb, &bars[st]);
-        bulk_g2s(sb + a.off_q, static_cast<const char*>(a.q) + ((size_t)b * HK + kh) * kb, kb, &bars[st]);
+        mbar_arrive_expect_tx(full, TILE + 2 * kb + VB * sa);
+        bulk_g2s_hint(sb, a.state + (((size_t)m.s * a.HV + hv) * a.V + (size_t)vb * VB) * KD, TILE,
+                      full, pol);
+        bulk_g2s(sb + a.off_k, static_cast<const char*>(a.k) + ((size_t)b * a.HK + kh) * kb, kb, full);
+        bulk_g2s(sb + a.off_q, static_cast<const char*>(a.q) + ((size_t)b * a.HK + kh) * kb, kb, full);
         bulk_g2s(sb + a.off_v,
-                 static_cast<const char*>(a.v) + (((size_t)b * HV + hv) * V + (size_t)vb * VB) * sa,
-                 VB * sa, &bars[st]);
-    };
-    if (tid == 0) {
-        pol = policy_evict_first();
-        for (int k = 0; k < stages; ++k) issue(k);
+                 static_cast<const char*>(a.v) + (((size_t)b * a.HV + hv) * a.V + (size_t)vb * VB) * sa,
+                 VB * sa, full);
     }
 
-    int k = 0;
-    for (;; ++k) {
-        const int item = blockIdx.x + k * gridDim.x;
-        if (item >= n_items) break;
-        const int st = k % stages;
-        const uint32_t par = (k / stages) & 1;
-        // all threads agree on the outcome, so the branch below stays uniform
-        const bool ok = __syncthreads_and(mbar_wait_bounded(&bars[st], par) ? 1 : 0) != 0;
-        if (!ok) {
-            *abort_flag = 1;
-            set_dev_err(a.dev_err, RSSM_DEVERR_TIMEOUT);
-        }
-        const Meta m = meta[st];
-        if (ok && m.valid) {
-            const uint8_t* sb = stage0 + st * a.stage_bytes;
-            const float* tile = reinterpret_cast<const float*>(sb);
-            float k4[4], q4[4];
-            load4(sb + a.off_k, lane * 4, a.act_bf16, k4);
-            load4(sb + a.off_q, lane * 4, a.act_bf16, q4);
-            float kq = k4[0] * q4[0] + k4[1] * q4[1] + k4[2] * q4[2] + k4[3] * q4[3];
+    static __device__ void consume(const Args& a, int, const Meta& m, const uint8_t* sb, uint8_t*,
+                                   int lane, int wi) {
+        if (!m.valid) return;
+        const bool bf = a.act_bf16;
+        const float* tile = reinterpret_cast<const float*>(sb);
+        float k4[4], q4[4];
+        load4(sb + a.off_k, lane * 4, bf, k4);
+        load4(sb + a.off_q, lane * 4, bf, q4);
+        float kq = k4[0] * q4[0] + k4[1] * q4[1] + k4[2] * q4[2] + k4[3] * q4[3];
 #pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) kq += __shfl_xor_sync(0xffffffffu, kq, o);
+        for (int o = 16; o >= 1; o >>= 1) kq += __shfl_xor_sync(kFull, kq, o);
+        float* dst = a.state + (((size_t)m.s * a.HV + m.hv) * a.V + (size_t)m.vb * VB) * KD;
+#pragma unroll 1
+        for (int ch = 0; ch < RW / 16; ++ch) {
+            const int r0 = wi * RW + ch * 16;
             float part[32];
-            float4 rows[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-                const float4 s4 = *reinterpret_cast<const float4*>(tile + (warp + 4 * j) * KD + lane * 4);
-                rows[j] = s4;
+                const float4 s4 = *reinterpret_cast<const float4*>(tile + (r0 + j) * KD + lane * 4);
                 part[j] = s4.x * k4[0] + s4.y * k4[1] + s4.z * k4[2] + s4.w * k4[3];
                 part[16 + j] = s4.x * q4[0] + s4.y * q4[1] + s4.z * q4[2] + s4.w * q4[3];
             }
             reduce_scatter<32, 32>(part);
-            const float cdot = __shfl_down_sync(0xffffffffu, part[0], 16);
-            const int r = warp + 4 * (lane & 15);
-            float dnew = 0.f;
+            const float cdot = __shfl_down_sync(kFull, part[0], 16);
+            float dn = 0.f;
             if (lane < 16) {
-                const float vr = load1(sb + a.off_v, r, a.act_bf16);
-                dnew = m.beta * (vr - m.g * part[0]);
-                const float oo = m.g * cdot + dnew * kq;
-                store1(a.o, ((size_t)m.b * HV + m.hv) * V + (size_t)m.vb * VB + r, a.out_bf16, oo);
+                const int r = r0 + lane;
+                dn = m.beta * (load1(sb + a.off_v, r, bf) - m.g * part[0]);
+                const float oo = m.g * cdot + dn * kq;
+                store1(a.o, ((size_t)m.b * a.HV + m.hv) * a.V + (size_t)m.vb * VB + r, a.out_bf16, oo);
             }
-            float* dst = a.state + (((size_t)m.s * HV + m.hv) * V + (size_t)m.vb * VB) * KD;
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
-                const float dj = __shfl_sync(0xffffffffu, dnew, j);
-                float4 s4 = rows[j];
+                const float dj = __shfl_sync(kFull, dn, j);
+                float4 s4 = *reinterpret_cast<const float4*>(tile + (r0 + j) * KD + lane * 4);
                 s4.x = fmaf(m.g, s4.x, dj * k4[0]);
                 s4.y = fmaf(m.g, s4.y, dj * k4[1]);
                 s4.z = fmaf(m.g, s4.z, dj * k4[2]);
                 s4.w = fmaf(m.g, s4.w, dj * k4[3]);
-                *reinterpret_cast<float4*>(dst + (warp + 4 * j) * KD + lane * 4) = s4;
+                *reinterpret_cast<float4*>(dst + (r0 + j) * KD + lane * 4) = s4;
             }
         }
-        __syncthreads();
-        if (*abort_flag) break;
-        if (tid == 0) issue(k + stages);
     }
-    if (*abort_flag && tid == 0) {
-        for (int j = k; j < k + stages; ++j) {
-            const int item = blockIdx.x + j * gridDim.x;
-            if (item >= n_items) break;
-            mbar_wait_bounded(&bars[j % stages], (j / stages) & 1);
-        }
-    }
-}
+};
 
 // ----------------------------------------------------------------------------
 // host side
@@ -587,14 +510,15 @@ extern "C" int rssm_gdn_precompute(const rssm_gdn_dims* d, const void* q, const 
         return RSSM_ERR_INVALID_ARG;
     if (workspace_bytes < rssm_gdn_workspace_size(d)) return RSSM_ERR_INVALID_ARG;
     const int L = d->ring_len, HK = d->num_k_heads;
-    const int smem = (((2 * HK * L + HK + 3) & ~3) + d->num_v_heads * gdn::tbl_floats(L)) * 4;
+    const int smem =
+        (((2 * HK * gdn::KD + 2 * HK * L + HK + 3) & ~3) + d->num_v_heads * gdn::tbl_floats(L)) * 4;
     DeviceInfo di;
     if (!device_info(&di)) return RSSM_ERR_CUDA;
     if (smem > di.max_smem_optin) return RSSM_ERR_UNSUPPORTED;
     if (smem > 48 * 1024 &&
         !ensure_smem_limit(reinterpret_cast<const void*>(gdn::precompute_kernel), smem))
         return RSSM_ERR_CUDA;
-    gdn::precompute_kernel<<<d->batch, 128, smem, (cudaStream_t)stream>>>(
+    gdn::precompute_kernel<<<d->batch, 256, smem, (cudaStream_t)stream>>>(
         d->num_v_heads, HK, L, d->num_slots, d->act_dtype == RSSM_BF16, q, k, beta, g, ring_k, ring_g,
         cache_indices, row_wp, static_cast<float*>(workspace));
     return launch_status();
@@ -613,9 +537,7 @@ extern "C" int rssm_gdn_output(const rssm_gdn_dims* d, float* state, const void*
         !ok_ptr(o))
         return RSSM_ERR_INVALID_ARG;
     if (workspace_bytes < rssm_gdn_workspace_size(d)) return RSSM_ERR_INVALID_ARG;
-    DeviceInfo di;
-    if (!device_info(&di)) return RSSM_ERR_CUDA;
-    gdn::OutArgs a{};
+    gdn::OutPolicy::Args a{};
     a.state = state; a.q = q; a.v = v; a.ring_k = ring_k; a.ring_d = ring_d; a.ci = cache_indices;
     a.row_wp = row_wp; a.row_flush = row_flush; a.ws = static_cast<const float*>(workspace);
     a.o = o; a.dev_err = dev_err;
@@ -627,22 +549,12 @@ extern "C" int rssm_gdn_output(const rssm_gdn_dims* d, float* state, const void*
     a.off_k = off;   off += a.L * gdn::KD * sa;
     a.off_q = off;   off += gdn::KD * sa;
     a.off_v = off;   off += gdn::VB * sa;
-    a.off_v = (a.off_v + 15) & ~15;
-    off = (off + 15) & ~15;
     a.off_d = off;   off += a.L * gdn::VB * 4;
     a.off_tbl = off; off += gdn::tbl_floats(a.L) * 4;
-    a.stage_bytes = (off + 127) & ~127;
-    PipeShape ps;
-    if (!pick_pipe_shape(di, a.stage_bytes, gdn::kFixedSmem, gdn::kMaxStages, &ps))
-        return RSSM_ERR_UNSUPPORTED;
-    a.stages = ps.stages;
-    if (!ensure_smem_limit(reinterpret_cast<const void*>(gdn::output_kernel), ps.smem_bytes))
-        return RSSM_ERR_CUDA;
-    const long items = (long)d->batch * d->num_v_heads * (d->head_v_dim / gdn::VB);
-    long grid = (long)di.sm_count * ps.ctas_per_sm;
-    if (grid > items) grid = items;
-    gdn::output_kernel<<<(int)grid, gdn::kThreads, ps.smem_bytes, (cudaStream_t)stream>>>(a);
-    return launch_status();
+    const int stage_bytes = (off + 127) & ~127;
+    return launch_pipe<gdn::OutPolicy>(a, stage_bytes, 0, gdn::TILE,
+                                       (long)d->batch * d->num_v_heads * (d->head_v_dim / gdn::VB),
+                                       (cudaStream_t)stream);
 }
 
 extern "C" int rssm_gdn_decode(const rssm_gdn_dims* d, float* state, const void* q, const void* k,
@@ -675,9 +587,7 @@ extern "C" int rssm_gdn_full_state_decode(const rssm_gdn_dims* d, float* state, 
     if (!ok_ptr(state) || !ok_ptr(q) || !ok_ptr(k) || !ok_ptr(v) || !ok_ptr(beta) || !ok_ptr(g) ||
         !ok_ptr(cache_indices) || !ok_ptr(o))
         return RSSM_ERR_INVALID_ARG;
-    DeviceInfo di;
-    if (!device_info(&di)) return RSSM_ERR_CUDA;
-    gdn::FullArgs a{};
+    gdn::FullPolicy::Args a{};
     a.state = state; a.q = q; a.k = k; a.v = v; a.beta = beta; a.g = g; a.ci = cache_indices;
     a.o = o; a.dev_err = dev_err;
     a.batch = d->batch; a.HV = d->num_v_heads; a.HK = d->num_k_heads; a.V = d->head_v_dim;
@@ -688,16 +598,8 @@ extern "C" int rssm_gdn_full_state_decode(const rssm_gdn_dims* d, float* state, 
     a.off_k = off; off += gdn::KD * sa;
     a.off_q = off; off += gdn::KD * sa;
     a.off_v = off; off += gdn::VB * sa;
-    a.stage_bytes = (off + 127) & ~127;
-    PipeShape ps;
-    if (!pick_pipe_shape(di, a.stage_bytes, gdn::kFixedSmem, gdn::kMaxStages, &ps))
-        return RSSM_ERR_UNSUPPORTED;
-    a.stages = ps.stages;
-    if (!ensure_smem_limit(reinterpret_cast<const void*>(gdn::full_state_kernel), ps.smem_bytes))
-        return RSSM_ERR_CUDA;
-    const long items = (long)d->batch * d->num_v_heads * (d->head_v_dim / gdn::VB);
-    long grid = (long)di.sm_count * ps.ctas_per_sm;
-    if (grid > items) grid = items;
-    gdn::full_state_kernel<<<(int)grid, gdn::kThreads, ps.smem_bytes, (cudaStream_t)stream>>>(a);
-    return launch_status();
+    const int stage_bytes = (off + 127) & ~127;
+    return launch_pipe<gdn::FullPolicy>(a, stage_bytes, 0, gdn::TILE,
+                                        (long)d->batch * d->num_v_heads * (d->head_v_dim / gdn::VB),
+                                        (cudaStream_t)stream);
 }

@@ -27,6 +27,7 @@
 // round may land on ring positions whose raw entries the fold still reads.
 #include "common.cuh"
 #include "internal.h"
+#include "pipeline.cuh"
 
 namespace rssm {
 namespace spec {
@@ -35,7 +36,6 @@ constexpr int kThreads = 128;
 constexpr int KD = 128;
 constexpr int VB = 64;
 constexpr int TILE = VB * KD * 4;
-constexpr int kMaxStages = 8;
 constexpr int kMaxT = 8;
 
 // table per (row, value head): au[T][L], ao[T][L], Gu[T], Go[T], beta[T], g[T], c, base'
@@ -49,10 +49,6 @@ __device__ __forceinline__ void load4(const void* base, int i, bool bf, float* f
         const float4 v = *reinterpret_cast<const float4*>(static_cast<const float*>(base) + i);
         f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
     }
-}
-
-__device__ __forceinline__ void mbar_arrive_plain(uint64_t* bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
 // Effective history of a slot at verify time: (count, oldest position); false when
@@ -270,204 +266,164 @@ __global__ void spec_pre_kernel(const PreArgs a) {
 }
 
 // ----------------------------------------------------------------------------
-// verify (persistent, TMA bulk pipeline)
+// verify (warp-specialised pipeline, one consumer warp per tile)
 // ----------------------------------------------------------------------------
 
-struct VerArgs {
-    const float* state;
-    const void* q;
-    const void* k;
-    const void* v;
-    float* ring_d;
-    void* ring_v;
-    const int32_t* ci;
-    const int32_t* slot_wp;
-    const int32_t* slot_base;
-    const uint8_t* slot_flush;
-    const float* ws;
-    void* o;
-    int32_t* dev_err;
-    int batch, T, HV, HK, V, L, num_slots, act_bf16, out_bf16;
-    int stages, stage_bytes, work_off;
-    int off_kq, off_v, off_d, off_tbl;
-};
-
-struct VMeta {
-    int valid, s, b, hv, vb, c, base_eff, pad;
-};
+constexpr int kGroupWarps = 2;
+constexpr int RW = VB / kGroupWarps;              // value rows per warp
+constexpr int kWarpScratch = 3 * kMaxT * RW * 4;  // W [2T][RW] S0 dots, Dd [T][RW] draft d
 
 template <int DP>
-__global__ void __launch_bounds__(kThreads) verify_kernel(const VerArgs a) {
-    extern __shared__ __align__(128) uint8_t smem[];
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
-    VMeta* meta = reinterpret_cast<VMeta*>(smem + 128);
-    int* abort_flag = reinterpret_cast<int*>(smem + 128 + kMaxStages * sizeof(VMeta));
-    float* W = reinterpret_cast<float*>(smem + a.work_off);      // [2T][VB] S0 dots
-    float* Dd = W + 2 * kMaxT * VB;                              // [T][VB] draft d
-    uint8_t* stage0 = smem + a.work_off + 3 * kMaxT * VB * 4;
+struct VerPolicy {
+    static constexpr int kGroup = kGroupWarps;
+    struct Args {
+        const float* state;
+        const void* q;
+        const void* k;
+        const void* v;
+        float* ring_d;
+        void* ring_v;
+        const int32_t* ci;
+        const int32_t* slot_wp;
+        const int32_t* slot_base;
+        const uint8_t* slot_flush;
+        const float* ws;
+        void* o;
+        int32_t* dev_err;
+        int batch, T, HV, HK, V, L, num_slots, act_bf16, out_bf16;
+        int stages, stage_bytes, stage_off, scratch_off, warp_scratch;
+        int off_kq, off_v, off_d, off_tbl;
+    };
+    struct Meta {
+        int valid, s, b, hv, vb, c, base_eff;
+    };
 
-    constexpr int RC = 32 / DP;  // value rows per reduce-scatter chunk
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int T = a.T, HV = a.HV, HK = a.HK, V = a.V, L = a.L;
-    const int NVB = V / VB;
-    const int sa = a.act_bf16 ? 2 : 4;
-    const int TB = tbl_floats(L, T);
-    const int per_row = HV * NVB;
-    const int n_items = a.batch * per_row;
-    const int stages = a.stages;
+    static __device__ int n_items(const Args& a) { return a.batch * a.HV * (a.V / VB); }
 
-    if (tid == 0) {
-        for (int st = 0; st < stages; ++st) mbar_init(&bars[st], 1);
-        *abort_flag = 0;
-        fence_barrier_init();
-    }
-    __syncthreads();
-
-    uint64_t pol = 0;
-    auto issue = [&](int kk) {
-        const int item = blockIdx.x + kk * gridDim.x;
-        if (item >= n_items) return;
-        const int st = kk % stages;
-        uint8_t* sb = stage0 + st * a.stage_bytes;
-        const int b = item / per_row;
-        const int rem = item - b * per_row;
-        const int hv = rem / NVB, vb = rem - (rem / NVB) * NVB;
+    // (slot, history count or -1 when the cursors are bad, oldest position, row)
+    static __device__ int4 prefetch(const Args& a, int item) {
+        const int b = item / (a.HV * (a.V / VB));
         const int s = a.ci[b];
-        VMeta m{0, s, b, hv, vb, 0, 0, 0};
-        if (s >= a.num_slots) {
-            set_dev_err(a.dev_err, RSSM_DEVERR_SLOT);
-        } else if (s >= 0) {
-            int c, be;
-            if (history(a.slot_wp[s], a.slot_base[s], a.slot_flush[s], L, T, &c, &be)) {
-                m.valid = 1;
-                m.c = c;
-                m.base_eff = be;
-            } else {
-                set_dev_err(a.dev_err, RSSM_DEVERR_CURSOR);
-            }
+        int c = 0, be = 0;
+        if (s >= 0 && s < a.num_slots) {
+            if (!history(a.slot_wp[s], a.slot_base[s], a.slot_flush[s], a.L, a.T, &c, &be)) c = -1;
         }
-        meta[st] = m;
+        return make_int4(s, c, be, b);
+    }
+
+    static __device__ void issue(const Args& a, int item, int4 r, Meta* meta, uint8_t* sb,
+                                 uint64_t* full, uint64_t pol) {
+        const int NVB = a.V / VB;
+        const int b = r.w;
+        const int rem = item - b * a.HV * NVB;
+        const int hv = rem / NVB, vb = rem - (rem / NVB) * NVB;
+        Meta m{0, r.x, b, hv, vb, r.y, r.z};
+        if (r.x >= a.num_slots) {
+            set_dev_err(a.dev_err, RSSM_DEVERR_SLOT);
+        } else if (r.x >= 0) {
+            if (r.y < 0) set_dev_err(a.dev_err, RSSM_DEVERR_CURSOR);
+            else m.valid = 1;
+        }
+        *meta = m;
         if (!m.valid) {
-            mbar_arrive_plain(&bars[st]);
+            mbar_arrive_plain(full);
             return;
         }
-        const int kh = hv / (HV / HK);
+        const int T = a.T, L = a.L;
+        const int sa = a.act_bf16 ? 2 : 4;
+        const int kh = hv / (a.HV / a.HK);
+        const int TB = tbl_floats(L, T);
         const uint32_t kb = KD * sa;
-        const uint32_t tx = TILE + 2 * T * kb + T * VB * sa + m.c * VB * 4 + TB * 4;
-        mbar_arrive_expect_tx(&bars[st], tx);
-        bulk_g2s_hint(sb, a.state + (((size_t)s * HV + hv) * V + (size_t)vb * VB) * KD, TILE, &bars[st],
-                      pol);
+        mbar_arrive_expect_tx(full, TILE + 2 * T * kb + T * VB * sa + m.c * VB * 4 + TB * 4);
+        bulk_g2s_hint(sb, a.state + (((size_t)m.s * a.HV + hv) * a.V + (size_t)vb * VB) * KD, TILE,
+                      full, pol);
         for (int j = 0; j < T; ++j) {
-            const size_t src = (((size_t)b * T + j) * HK + kh) * kb;
-            bulk_g2s(sb + a.off_kq + (2 * j) * kb, static_cast<const char*>(a.k) + src, kb, &bars[st]);
-            bulk_g2s(sb + a.off_kq + (2 * j + 1) * kb, static_cast<const char*>(a.q) + src, kb,
-                     &bars[st]);
+            const size_t src = (((size_t)b * T + j) * a.HK + kh) * kb;
+            bulk_g2s(sb + a.off_kq + (2 * j) * kb, static_cast<const char*>(a.k) + src, kb, full);
+            bulk_g2s(sb + a.off_kq + (2 * j + 1) * kb, static_cast<const char*>(a.q) + src, kb, full);
             bulk_g2s(sb + a.off_v + j * VB * sa,
                      static_cast<const char*>(a.v) +
-                         ((((size_t)b * T + j) * HV + hv) * V + (size_t)vb * VB) * sa,
-                     VB * sa, &bars[st]);
+                         ((((size_t)b * T + j) * a.HV + hv) * a.V + (size_t)vb * VB) * sa,
+                     VB * sa, full);
         }
-        const float* dr = a.ring_d + ((size_t)s * HV + hv) * L * V + (size_t)vb * VB;
+        const float* dr = a.ring_d + ((size_t)m.s * a.HV + hv) * L * a.V + (size_t)vb * VB;
         for (int i = 0; i < m.c; ++i)
-            bulk_g2s(sb + a.off_d + i * VB * 4, dr + (size_t)((m.base_eff + i) % L) * V, VB * 4,
-                     &bars[st]);
-        bulk_g2s(sb + a.off_tbl, a.ws + ((size_t)b * HV + hv) * TB, TB * 4, &bars[st]);
-    };
-    if (tid == 0) {
-        pol = policy_evict_first();
-        for (int kk = 0; kk < stages; ++kk) issue(kk);
+            bulk_g2s(sb + a.off_d + i * VB * 4, dr + (size_t)((m.base_eff + i) % L) * a.V, VB * 4, full);
+        bulk_g2s(sb + a.off_tbl, a.ws + ((size_t)b * a.HV + hv) * TB, TB * 4, full);
     }
 
-    int kk = 0;
-    for (;; ++kk) {
-        const int item = blockIdx.x + kk * gridDim.x;
-        if (item >= n_items) break;
-        const int st = kk % stages;
-        const uint32_t par = (kk / stages) & 1;
-        // all threads agree on the outcome, so the branch below stays uniform
-        const bool ok = __syncthreads_and(mbar_wait_bounded(&bars[st], par) ? 1 : 0) != 0;
-        if (!ok) {
-            *abort_flag = 1;
-            set_dev_err(a.dev_err, RSSM_DEVERR_TIMEOUT);
-        }
-        const VMeta m = meta[st];
-        if (ok && m.valid) {
-            const uint8_t* sb = stage0 + st * a.stage_bytes;
-            const float* tile = reinterpret_cast<const float*>(sb);
-            const uint8_t* kq = sb + a.off_kq;
-            // phase A: S0 . k_j and S0 . q_j for every value row
-            float vec[DP][4];
+    static __device__ void consume(const Args& a, int, const Meta& m, const uint8_t* sb,
+                                   uint8_t* scratch, int lane, int wi) {
+        if (!m.valid) return;
+        constexpr int RC = 32 / DP;  // value rows per reduce-scatter
+        const bool bf = a.act_bf16;
+        const int sa = bf ? 2 : 4;
+        const int T = a.T, L = a.L, c = m.c;
+        const int rbase = wi * RW;
+        const float* tile = reinterpret_cast<const float*>(sb);
+        const uint8_t* kq = sb + a.off_kq;
+        float* W = reinterpret_cast<float*>(scratch);  // [2T][RW]
+        float* Dd = W + 2 * kMaxT * RW;                // [T][RW]
+        // phase A: S0 . k_j and S0 . q_j for this warp's value rows
+        float vec[DP][4];
 #pragma unroll
-            for (int d = 0; d < DP; ++d) {
-                if (d < 2 * T) {
-                    load4(kq + (size_t)d * KD * sa, lane * 4, a.act_bf16, vec[d]);
-                } else {
-                    vec[d][0] = vec[d][1] = vec[d][2] = vec[d][3] = 0.f;
-                }
-            }
-#pragma unroll
-            for (int ch = 0; ch < 16 / RC; ++ch) {
-                float part[32];
-#pragma unroll
-                for (int jr = 0; jr < RC; ++jr) {
-                    const int r = warp + 4 * (ch * RC + jr);
-                    const float4 s4 = *reinterpret_cast<const float4*>(tile + r * KD + lane * 4);
-#pragma unroll
-                    for (int d = 0; d < DP; ++d)
-                        part[jr * DP + d] =
-                            s4.x * vec[d][0] + s4.y * vec[d][1] + s4.z * vec[d][2] + s4.w * vec[d][3];
-                }
-                reduce_scatter<32, 32>(part);  // lane l holds entry l
-                const int jr = lane / DP, d = lane % DP;
-                if (d < 2 * T) W[d * VB + warp + 4 * (ch * RC + jr)] = part[0];
-            }
-            __syncthreads();
-            // phase B: the draft chain, one thread per value row
-            if (tid < VB) {
-                const int r = tid;
-                const float* t = reinterpret_cast<const float*>(sb + a.off_tbl);
-                const float* dh = reinterpret_cast<const float*>(sb + a.off_d);
-                const int c = m.c;
-                const size_t vi = (size_t)m.vb * VB + r;
-                for (int j = 0; j < T; ++j) {
-                    const float* au = t + j * L;
-                    const float* ao = t + T * L + j * L;
-                    const int mm = c + j;
-                    float u = t[2 * T * L + j] * W[(2 * j) * VB + r];
-                    float oo = t[2 * T * L + T + j] * W[(2 * j + 1) * VB + r];
-                    for (int i = 0; i < c; ++i) {
-                        const float di = dh[i * VB + r];
-                        u = fmaf(au[i], di, u);
-                        oo = fmaf(ao[i], di, oo);
-                    }
-                    for (int i = c; i < mm; ++i) {
-                        const float di = Dd[(i - c) * VB + r];
-                        u = fmaf(au[i], di, u);
-                        oo = fmaf(ao[i], di, oo);
-                    }
-                    const float vr = load1(sb + a.off_v + j * VB * sa, r, a.act_bf16);
-                    const float dn = t[2 * T * L + 2 * T + j] * (vr - t[2 * T * L + 3 * T + j] * u);
-                    Dd[j * VB + r] = dn;
-                    oo = fmaf(ao[mm], dn, oo);
-                    const int pos = (m.base_eff + c + j) % L;
-                    store1(a.o, (((size_t)m.b * T + j) * HV + m.hv) * V + vi, a.out_bf16, oo);
-                    a.ring_d[(((size_t)m.s * HV + m.hv) * L + pos) * V + vi] = dn;
-                    store1(a.ring_v, (((size_t)m.s * HV + m.hv) * L + pos) * V + vi, a.act_bf16, vr);
-                }
+        for (int d = 0; d < DP; ++d) {
+            if (d < 2 * T) {
+                load4(kq + (size_t)d * KD * sa, lane * 4, bf, vec[d]);
+            } else {
+                vec[d][0] = vec[d][1] = vec[d][2] = vec[d][3] = 0.f;
             }
         }
-        __syncthreads();
-        if (*abort_flag) break;
-        if (tid == 0) issue(kk + stages);
+#pragma unroll 1
+        for (int ch = 0; ch < RW / RC; ++ch) {
+            float part[32];
+#pragma unroll
+            for (int jr = 0; jr < RC; ++jr) {
+                const float4 s4 =
+                    *reinterpret_cast<const float4*>(tile + (rbase + ch * RC + jr) * KD + lane * 4);
+#pragma unroll
+                for (int d = 0; d < DP; ++d)
+                    part[jr * DP + d] =
+                        s4.x * vec[d][0] + s4.y * vec[d][1] + s4.z * vec[d][2] + s4.w * vec[d][3];
+            }
+            reduce_scatter<32, 32>(part);  // lane l holds entry l
+            const int jr = lane / DP, d = lane % DP;
+            if (d < 2 * T) W[d * RW + ch * RC + jr] = part[0];
+        }
+        __syncwarp();
+        // phase B: the draft chain, one value row per lane
+        const float* t = reinterpret_cast<const float*>(sb + a.off_tbl);
+        const float* dh = reinterpret_cast<const float*>(sb + a.off_d);
+        const int r = rbase + lane;
+        const size_t vi = (size_t)m.vb * VB + r;
+        for (int j = 0; j < T; ++j) {
+            const float* au = t + j * L;
+            const float* ao = t + T * L + j * L;
+            const int mm = c + j;
+            float u = t[2 * T * L + j] * W[(2 * j) * RW + lane];
+            float oo = t[2 * T * L + T + j] * W[(2 * j + 1) * RW + lane];
+            for (int i = 0; i < c; ++i) {
+                const float di = dh[i * VB + r];
+                u = fmaf(au[i], di, u);
+                oo = fmaf(ao[i], di, oo);
+            }
+            for (int i = c; i < mm; ++i) {
+                const float di = Dd[(i - c) * RW + lane];
+                u = fmaf(au[i], di, u);
+                oo = fmaf(ao[i], di, oo);
+            }
+            const float vr = load1(sb + a.off_v + j * VB * sa, r, bf);
+            const float dn = t[2 * T * L + 2 * T + j] * (vr - t[2 * T * L + 3 * T + j] * u);
+            Dd[j * RW + lane] = dn;
+            oo = fmaf(ao[mm], dn, oo);
+            const int pos = (m.base_eff + c + j) % L;
+            store1(a.o, (((size_t)m.b * T + j) * a.HV + m.hv) * a.V + vi, a.out_bf16, oo);
+            a.ring_d[(((size_t)m.s * a.HV + m.hv) * L + pos) * a.V + vi] = dn;
+            store1(a.ring_v, (((size_t)m.s * a.HV + m.hv) * L + pos) * a.V + vi, bf, vr);
+        }
+        __syncwarp();
     }
-    if (*abort_flag && tid == 0) {
-        for (int j = kk; j < kk + stages; ++j) {
-            const int item = blockIdx.x + j * gridDim.x;
-            if (item >= n_items) break;
-            mbar_wait_bounded(&bars[j % stages], (j / stages) & 1);
-        }
-    }
-}
+};
 
 }  // namespace spec
 }  // namespace rssm
@@ -530,40 +486,39 @@ extern "C" int rssm_gdn_spec_verify(const rssm_gdn_dims* d, int32_t T, float* st
     if (launch_status()) return RSSM_ERR_CUDA;
 
     // 3. verify
-    spec::VerArgs va{};
-    va.state = state; va.q = q; va.k = k; va.v = v; va.ring_d = ring_d; va.ring_v = ring_v;
-    va.ci = cache_indices; va.slot_wp = slot_wp; va.slot_base = slot_base; va.slot_flush = slot_flush;
-    va.ws = static_cast<const float*>(workspace); va.o = o; va.dev_err = dev_err;
-    va.batch = d->batch; va.T = T; va.HV = HV; va.HK = HK; va.V = V; va.L = L;
-    va.num_slots = d->num_slots; va.act_bf16 = abf; va.out_bf16 = d->out_dtype == RSSM_BF16;
+    const int TBs = spec::tbl_floats(L, T);
     int off = spec::TILE;
-    va.off_kq = off;  off += 2 * T * spec::KD * sa;
-    va.off_v = off;   off += T * spec::VB * sa;
-    va.off_d = off;   off += L * spec::VB * 4;
-    va.off_tbl = off; off += spec::tbl_floats(L, T) * 4;
-    va.stage_bytes = (off + 127) & ~127;
-    va.work_off = 1024;
-    const int fixed = va.work_off + 3 * spec::kMaxT * spec::VB * 4;
-    PipeShape ps;
-    if (!pick_pipe_shape(di, va.stage_bytes, fixed, spec::kMaxStages, &ps)) return RSSM_ERR_UNSUPPORTED;
-    va.stages = ps.stages;
+    const int off_kq = off; off += 2 * T * spec::KD * sa;
+    const int off_v = off;  off += T * spec::VB * sa;
+    const int off_d = off;  off += L * spec::VB * 4;
+    const int off_tbl = off; off += TBs * 4;
+    const int stage_bytes = (off + 127) & ~127;
     const long items = (long)d->batch * HV * NVB;
-    long grid = (long)di.sm_count * ps.ctas_per_sm;
-    if (grid > items) grid = items;
-    const void* kfn;
-    const int dp = T <= 1 ? 2 : (T <= 2 ? 4 : (T <= 4 ? 8 : 16));
-    switch (dp) {
-        case 2: kfn = reinterpret_cast<const void*>(spec::verify_kernel<2>); break;
-        case 4: kfn = reinterpret_cast<const void*>(spec::verify_kernel<4>); break;
-        case 8: kfn = reinterpret_cast<const void*>(spec::verify_kernel<8>); break;
-        default: kfn = reinterpret_cast<const void*>(spec::verify_kernel<16>); break;
+    auto fill = [&](auto& va) {
+        va.state = state; va.q = q; va.k = k; va.v = v; va.ring_d = ring_d; va.ring_v = ring_v;
+        va.ci = cache_indices; va.slot_wp = slot_wp; va.slot_base = slot_base;
+        va.slot_flush = slot_flush; va.ws = static_cast<const float*>(workspace); va.o = o;
+        va.dev_err = dev_err; va.batch = d->batch; va.T = T; va.HV = HV; va.HK = HK; va.V = V;
+        va.L = L; va.num_slots = d->num_slots; va.act_bf16 = abf;
+        va.out_bf16 = d->out_dtype == RSSM_BF16;
+        va.off_kq = off_kq; va.off_v = off_v; va.off_d = off_d; va.off_tbl = off_tbl;
+    };
+    if (T <= 1) {
+        spec::VerPolicy<2>::Args va{};
+        fill(va);
+        return launch_pipe<spec::VerPolicy<2>>(va, stage_bytes, spec::kWarpScratch, spec::TILE, items, st);
     }
-    if (!ensure_smem_limit(kfn, ps.smem_bytes)) return RSSM_ERR_CUDA;
-    switch (dp) {
-        case 2: spec::verify_kernel<2><<<(int)grid, spec::kThreads, ps.smem_bytes, st>>>(va); break;
-        case 4: spec::verify_kernel<4><<<(int)grid, spec::kThreads, ps.smem_bytes, st>>>(va); break;
-        case 8: spec::verify_kernel<8><<<(int)grid, spec::kThreads, ps.smem_bytes, st>>>(va); break;
-        default: spec::verify_kernel<16><<<(int)grid, spec::kThreads, ps.smem_bytes, st>>>(va); break;
+    if (T <= 2) {
+        spec::VerPolicy<4>::Args va{};
+        fill(va);
+        return launch_pipe<spec::VerPolicy<4>>(va, stage_bytes, spec::kWarpScratch, spec::TILE, items, st);
     }
-    return launch_status();
+    if (T <= 4) {
+        spec::VerPolicy<8>::Args va{};
+        fill(va);
+        return launch_pipe<spec::VerPolicy<8>>(va, stage_bytes, spec::kWarpScratch, spec::TILE, items, st);
+    }
+    spec::VerPolicy<16>::Args va{};
+    fill(va);
+    return launch_pipe<spec::VerPolicy<16>>(va, stage_bytes, spec::kWarpScratch, spec::TILE, items, st);
 }

@@ -32,15 +32,20 @@ inline int launch_status() {
     return cudaGetLastError() == cudaSuccess ? RSSM_OK : RSSM_ERR_CUDA;
 }
 
-// Pick a persistent-grid shape for a streaming kernel with `stage_bytes` per
-// pipeline stage plus `fixed_bytes` of other shared memory: prefer two resident
-// CTAs per SM with >= 3 stages each, else one CTA with >= 2 stages.
-struct PipeShape {
+// Shape of a warp-specialised pipeline (pipeline.cuh): one CTA per SM with
+// `groups` consumer groups of `group_warps` warps and one producer warp, `stages`
+// shared-memory stages of `stage_bytes` (a multiple of `groups`), and
+// `warp_scratch` bytes of private scratch per consumer warp. Chosen so that, with
+// every group busy on one stage, the remaining stages keep at least 64 KB (and at
+// least two tiles) of copies in flight; more groups are preferred.
+struct PipeCfg {
     int stages;
-    int ctas_per_sm;
+    int groups;
     int smem_bytes;
+    int stage_off;
+    int scratch_off;
 };
-bool pick_pipe_shape(const DeviceInfo& di, int stage_bytes, int fixed_bytes, int max_stages,
-                     PipeShape* out);
+bool pick_pipe(const DeviceInfo& di, int stage_bytes, int warp_scratch, int tile_bytes, int header,
+               int max_stages, int group_warps, int max_groups, PipeCfg* out);
 
 }  // namespace rssm

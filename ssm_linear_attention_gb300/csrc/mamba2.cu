@@ -28,20 +28,12 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "pipeline.cuh"
 
 namespace rssm {
 namespace m2 {
 
-constexpr int kThreads = 128;
-constexpr int kMaxStages = 8;
-constexpr int kFixedSmem = 1024;  // barriers + per-stage metadata, before the stages
-
 __host__ __device__ inline int tbl_floats(int L) { return (2 * L + 1 + 3) & ~3; }
-
-struct Meta {
-    int valid, s, b, h, w, f;
-    float dt, dA;
-};
 
 // ----------------------------------------------------------------------------
 // ring append
@@ -94,11 +86,10 @@ __global__ void ring_append_kernel(int H, int P, int N, int G, int L, int num_sl
 // precompute: per-(row, head) coefficient tables
 // ----------------------------------------------------------------------------
 
-__global__ void precompute_kernel(int H, int N, int G, int L, int num_slots, int act_bf16,
-                                  const float* __restrict__ A, const void* __restrict__ C,
-                                  const float* __restrict__ ring_dt, const void* __restrict__ ring_B,
-                                  const int32_t* __restrict__ ci, const int32_t* __restrict__ row_wp,
-                                  float* __restrict__ ws) {
+__global__ void __launch_bounds__(256) precompute_kernel(
+    int H, int N, int G, int L, int num_slots, int act_bf16, const float* __restrict__ A,
+    const void* __restrict__ C, const float* __restrict__ ring_dt, const void* __restrict__ ring_B,
+    const int32_t* __restrict__ ci, const int32_t* __restrict__ row_wp, float* __restrict__ ws) {
     extern __shared__ __align__(16) float psm[];
     const int b = blockIdx.x;
     const int s = ci[b];
@@ -106,22 +97,32 @@ __global__ void precompute_kernel(int H, int N, int G, int L, int num_slots, int
     const int w = row_wp[b];
     if (w < 0 || w >= L) return;
     const int TBL = tbl_floats(L);
-    const int bc_len = (G * L + 3) & ~3;
-    float* bc = psm;           // [G][L]
-    float* tbl = psm + bc_len;  // [H][TBL]
     const int sa = act_bf16 ? 2 : 4;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    float* cs = psm;                              // [G][N] C_t in fp32
+    float* bc = cs + G * N;                       // [G][L]
+    float* tbl = psm + ((G * N + G * L + 3) & ~3);  // [H][TBL]
 
-    // B_i . C_t for every group and live entry i = 0..w
-    for (int pair = warp; pair < G * (w + 1); pair += nwarps) {
-        const int g = pair / (w + 1), i = pair % (w + 1);
+    for (int e = threadIdx.x * 8; e < G * N; e += blockDim.x * 8)
+        load8(static_cast<const char*>(C) + ((size_t)b * G * N + e) * sa, act_bf16, cs + e);
+    __syncthreads();
+
+    // bc[g][i] = B_i . C_t: one thread per (group, entry), whole dot product
+    for (int pair = threadIdx.x; pair < G * (w + 1); pair += blockDim.x) {
+        const int g = pair / (w + 1), i = pair - (pair / (w + 1)) * (w + 1);
         const char* Bi = static_cast<const char*>(ring_B) + (((size_t)s * G + g) * L + i) * N * sa;
-        const char* Ct = static_cast<const char*>(C) + ((size_t)b * G + g) * N * sa;
-        float acc = 0.f;
-        for (int n = lane; n < N; n += 32) acc += load1(Bi, n, act_bf16) * load1(Ct, n, act_bf16);
+        const float* cg = cs + g * N;
+        float acc0 = 0.f, acc1 = 0.f;
+        for (int n = 0; n < N; n += 16) {
+            float b8[8], b9[8];
+            load8(Bi + n * sa, act_bf16, b8);
+            load8(Bi + (n + 8) * sa, act_bf16, b9);
 #pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        if (lane == 0) bc[g * L + i] = acc;
+            for (int j = 0; j < 8; ++j) {
+                acc0 = fmaf(b8[j], cg[n + j], acc0);
+                acc1 = fmaf(b9[j], cg[n + 8 + j], acc1);
+            }
+        }
+        bc[g * L + i] = acc0 + acc1;
     }
     __syncthreads();
 
@@ -154,365 +155,311 @@ __global__ void precompute_kernel(int H, int N, int G, int L, int num_slots, int
 }
 
 // ----------------------------------------------------------------------------
-// persistent streaming kernels
+// streaming kernels (warp-specialised pipeline, one consumer warp per tile)
 // ----------------------------------------------------------------------------
+//
+// Tile (row b, head h): P x N state elements, consumed by a group of two warps
+// that take half of the headdim rows each. A lane owns 8 consecutive dstate
+// columns q = lane % (N/8) and every (32 / (N/8))-th row of its warp's half
+// starting at lane / (N/8); one 16-byte shared load per lane covers 32 / (N/8)
+// rows. Dot products over dstate reduce across the N/8 lanes of a row with
+// reduce-scatters, after which every lane holds whole results for P/64 rows.
+// With a bf16 state and bf16 C the products are mixed-precision fmas on the
+// packed bf16 operands.
 
-struct OutArgs {
-    void* state;
-    const void* C;
-    const float* D;
-    const void* z;
-    const void* ring_x;
-    const void* ring_B;
-    const int32_t* ci;
-    const int32_t* row_wp;
-    const uint8_t* row_flush;
-    const float* ws;
-    void* y;
-    int32_t* dev_err;
-    int batch, H, G, L, num_slots, act_bf16, out_bf16;
-    int stages, stage_bytes;
-    int off_x, off_C, off_z, off_tbl, off_B;
-};
+constexpr int kGroupWarps = 2;  // warps sharing one tile (half the headdim rows each)
 
-struct FullArgs {
-    void* state;
-    const void* x;
-    const float* dt_raw;
-    const float* dt_bias;
-    const float* A;
-    const void* B;
-    const void* C;
-    const float* D;
-    const void* z;
-    const int32_t* ci;
-    void* y;
-    int32_t* dev_err;
-    int batch, H, G, num_slots, act_bf16, out_bf16, softplus;
-    int stages, stage_bytes;
-    int off_x, off_B, off_C, off_z;
-};
-
-__device__ __forceinline__ void mbar_arrive_plain(uint64_t* bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
-
-// Row metadata prefetch for the producer thread: one item ahead.
-struct RowMeta {
-    int b, s, w, f;
+template <int P, int N, class ST>
+struct TileShape {
+    static constexpr int SS = ST::bytes;
+    static constexpr int TILE = P * N * SS;
+    static constexpr int PW = P / kGroupWarps;  // rows per warp
+    static constexpr int NQ = N / 8;            // lanes per row
+    static constexpr int RPI = 32 / NQ;         // rows per load instruction
+    static constexpr int ITER = PW / RPI;       // loads per lane
+    static constexpr int NCH = ITER / NQ;       // rows per lane after the reduce-scatters
+    static_assert(NCH >= 1 && ITER % NQ == 0, "tile shape");
 };
 
 template <int P, int N, class ST>
-__global__ void __launch_bounds__(kThreads) output_kernel(const OutArgs a) {
-    extern __shared__ __align__(128) uint8_t smem[];
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
-    Meta* meta = reinterpret_cast<Meta*>(smem + 128);
-    int* abort_flag = reinterpret_cast<int*>(smem + 128 + kMaxStages * sizeof(Meta));
-    uint8_t* stage0 = smem + kFixedSmem;
-
-    constexpr int SS = ST::bytes;
-    constexpr int TILE = P * N * SS;
-    constexpr int NQ = N / 8;             // lanes per state row (8 elements each)
-    constexpr int RP = kThreads / NQ;     // rows per pass
-    constexpr int KR = P / RP;            // rows per thread
-    constexpr int DUP = NQ / KR;          // lanes holding the same reduced row
-    static_assert(KR >= 1 && KR <= NQ, "tile shape");
-
-    const int tid = threadIdx.x;
-    const int H = a.H, L = a.L, G = a.G;
-    const int sa = a.act_bf16 ? 2 : 4;
-    const int TBL = tbl_floats(L);
-    const int n_items = a.batch * H;
-    const int stages = a.stages;
-
-    if (tid == 0) {
-        for (int st = 0; st < stages; ++st) mbar_init(&bars[st], 1);
-        *abort_flag = 0;
-        fence_barrier_init();
-    }
-    __syncthreads();
-
-    // ---- producer (thread 0) ----
-    uint64_t pol = 0;
-    RowMeta pf{-1, 0, 0, 0};
-    auto load_row = [&](int b) {
-        RowMeta r{b, a.ci[b], 0, 0};
-        if (r.s >= 0 && r.s < a.num_slots) {
-            r.w = a.row_wp[b];
-            r.f = a.row_flush[b];
-        }
-        return r;
+struct OutPolicy {
+    using Sh = TileShape<P, N, ST>;
+    static constexpr int kGroup = kGroupWarps;
+    struct Args {
+        void* state;
+        const void* C;
+        const float* D;
+        const void* z;
+        const void* ring_x;
+        const void* ring_B;
+        const int32_t* ci;
+        const int32_t* row_wp;
+        const uint8_t* row_flush;
+        const float* ws;
+        void* y;
+        int32_t* dev_err;
+        int batch, H, G, L, num_slots, act_bf16, out_bf16;
+        int stages, stage_bytes, stage_off, scratch_off, warp_scratch;
+        int off_x, off_C, off_z, off_tbl;
     };
-    auto issue = [&](int k) {
-        const int item = blockIdx.x + k * gridDim.x;
-        if (item >= n_items) return;
-        const int st = k % stages;
-        uint8_t* sb = stage0 + st * a.stage_bytes;
-        const int b = item / H, h = item - (item / H) * H;
-        const RowMeta r = (pf.b == b) ? pf : load_row(b);
-        const int nxt = item + gridDim.x;
-        if (nxt < n_items) pf = load_row(nxt / H);
-        Meta m;
-        m.b = b; m.h = h; m.s = r.s; m.w = r.w; m.f = r.f; m.valid = 0; m.dt = 0.f; m.dA = 0.f;
-        if (r.s >= a.num_slots) {
+    struct Meta {
+        int valid, s, b, h, w, f;
+    };
+
+    static __device__ int n_items(const Args& a) { return a.batch * a.H; }
+
+    static __device__ int4 prefetch(const Args& a, int item) {
+        const int b = item / a.H;
+        const int s = a.ci[b];
+        int w = 0, f = 0;
+        if (s >= 0 && s < a.num_slots) {
+            w = a.row_wp[b];
+            f = a.row_flush[b];
+        }
+        return make_int4(s, w, f, b);
+    }
+
+    static __device__ void issue(const Args& a, int item, int4 r, Meta* meta, uint8_t* sb,
+                                 uint64_t* full, uint64_t pol) {
+        const int b = r.w, h = item - r.w * a.H;
+        Meta m{0, r.x, b, h, r.y, r.z};
+        if (r.x >= a.num_slots) {
             set_dev_err(a.dev_err, RSSM_DEVERR_SLOT);
-        } else if (r.s >= 0) {
-            if (r.w < 0 || r.w >= L) set_dev_err(a.dev_err, RSSM_DEVERR_CURSOR);
+        } else if (r.x >= 0) {
+            if (r.y < 0 || r.y >= a.L) set_dev_err(a.dev_err, RSSM_DEVERR_CURSOR);
             else m.valid = 1;
         }
-        meta[st] = m;
+        *meta = m;
         if (!m.valid) {
-            mbar_arrive_plain(&bars[st]);
+            mbar_arrive_plain(full);
             return;
         }
-        const int g = h / (H / G);
-        const int w = r.w;
-        const uint32_t xbytes = (w + 1) * P * sa;
-        const uint32_t bbytes = r.f ? (w + 1) * N * sa : 0;
-        const uint32_t tx = TILE + xbytes + N * sa + (a.z ? P * sa : 0) + TBL * 4 + bbytes;
-        mbar_arrive_expect_tx(&bars[st], tx);
-        const char* state = static_cast<const char*>(a.state);
-        bulk_g2s_hint(sb, state + ((size_t)r.s * H + h) * TILE, TILE, &bars[st], pol);
+        const int sa = a.act_bf16 ? 2 : 4;
+        const int g = h / (a.H / a.G);
+        const int TBL = tbl_floats(a.L);
+        const uint32_t xbytes = (m.w + 1) * P * sa;
+        mbar_arrive_expect_tx(full, Sh::TILE + xbytes + N * sa + (a.z ? P * sa : 0) + TBL * 4);
+        bulk_g2s_hint(sb, static_cast<const char*>(a.state) + ((size_t)m.s * a.H + h) * Sh::TILE,
+                      Sh::TILE, full, pol);
         bulk_g2s(sb + a.off_x,
-                 static_cast<const char*>(a.ring_x) + ((size_t)r.s * H + h) * L * P * sa, xbytes,
-                 &bars[st]);
-        bulk_g2s(sb + a.off_C, static_cast<const char*>(a.C) + ((size_t)b * G + g) * N * sa, N * sa,
-                 &bars[st]);
+                 static_cast<const char*>(a.ring_x) + ((size_t)m.s * a.H + h) * a.L * P * sa, xbytes,
+                 full);
+        bulk_g2s(sb + a.off_C, static_cast<const char*>(a.C) + ((size_t)b * a.G + g) * N * sa, N * sa,
+                 full);
         if (a.z)
-            bulk_g2s(sb + a.off_z, static_cast<const char*>(a.z) + ((size_t)b * H + h) * P * sa,
-                     P * sa, &bars[st]);
-        bulk_g2s(sb + a.off_tbl, a.ws + ((size_t)b * H + h) * TBL, TBL * 4, &bars[st]);
-        if (r.f)
-            bulk_g2s(sb + a.off_B,
-                     static_cast<const char*>(a.ring_B) + ((size_t)r.s * G + g) * L * N * sa, bbytes,
-                     &bars[st]);
-    };
-    if (tid == 0) {
-        pol = policy_evict_first();
-        for (int k = 0; k < stages; ++k) issue(k);
+            bulk_g2s(sb + a.off_z, static_cast<const char*>(a.z) + ((size_t)b * a.H + h) * P * sa,
+                     P * sa, full);
+        bulk_g2s(sb + a.off_tbl, a.ws + ((size_t)b * a.H + h) * TBL, TBL * 4, full);
     }
 
-    // ---- consumers (all threads) ----
-    const int q = tid % NQ, r0 = tid / NQ;
-    int k = 0;
-    for (;; ++k) {
-        const int item = blockIdx.x + k * gridDim.x;
-        if (item >= n_items) break;
-        const int st = k % stages;
-        const uint32_t par = (k / stages) & 1;
-        // all threads agree on the outcome, so the branch below stays uniform
-        const bool ok = __syncthreads_and(mbar_wait_bounded(&bars[st], par) ? 1 : 0) != 0;
-        if (!ok) {
-            *abort_flag = 1;
-            set_dev_err(a.dev_err, RSSM_DEVERR_TIMEOUT);
-        }
-        const Meta m = meta[st];
-        if (ok && m.valid) {
-            const uint8_t* sb = stage0 + st * a.stage_bytes;
-            const float* tbl = reinterpret_cast<const float*>(sb + a.off_tbl);
-            const uint8_t* xr = sb + a.off_x;
+    static __device__ void consume(const Args& a, int, const Meta& m, const uint8_t* sb,
+                                   uint8_t* scratch, int lane, int wi) {
+        if (!m.valid) return;
+        const bool bf = a.act_bf16;
+        const int sa = bf ? 2 : 4;
+        const int L = a.L, w = m.w;
+        const int q = lane % Sh::NQ, hr = lane / Sh::NQ;
+        const int row0 = wi * Sh::PW + hr;  // this lane's rows: row0 + RPI * t
+        const float* tbl = reinterpret_cast<const float*>(sb + a.off_tbl);
+        const uint8_t* xr = sb + a.off_x;
+        float part[Sh::ITER];
+        if (ST::bf16 && bf) {
+            const uint4 cpk = *reinterpret_cast<const uint4*>(sb + a.off_C + q * 16);
+#pragma unroll
+            for (int t = 0; t < Sh::ITER; ++t) {
+                const int p = row0 + Sh::RPI * t;
+                const uint4 s8 = *reinterpret_cast<const uint4*>(sb + ((size_t)p * N + q * 8) * Sh::SS);
+                part[t] = dot8_bf16(s8, cpk, 0.f);
+            }
+        } else {
             float c[8];
-            load8(sb + a.off_C + q * 8 * sa, a.act_bf16, c);
-            float part[KR];
+            load8(sb + a.off_C + q * 8 * sa, bf, c);
 #pragma unroll
-            for (int kk = 0; kk < KR; ++kk) {
-                const int p = r0 + RP * kk;
+            for (int t = 0; t < Sh::ITER; ++t) {
+                const int p = row0 + Sh::RPI * t;
                 float s8[8];
-                load8(sb + ((size_t)p * N + q * 8) * SS, ST::bf16, s8);
-                float acc = 0.f;
+                load8(sb + ((size_t)p * N + q * 8) * Sh::SS, ST::bf16, s8);
+                float acc = s8[0] * c[0];
 #pragma unroll
-                for (int j = 0; j < 8; ++j) acc = fmaf(s8[j], c[j], acc);
-                part[kk] = acc;
+                for (int j = 1; j < 8; ++j) acc = fmaf(s8[j], c[j], acc);
+                part[t] = acc;
             }
-            const int kidx = reduce_scatter<KR, NQ>(part);
-            const float Pm1 = tbl[2 * L];
-            const int w = m.w;
-            if ((q & (DUP - 1)) == 0) {
-                const int p = r0 + RP * kidx;
-                float acc = Pm1 * part[0];
-                for (int i = 0; i <= w; ++i) acc = fmaf(tbl[i], load1(xr, i * P + p, a.act_bf16), acc);
-                acc = fmaf(__ldg(a.D + m.h), load1(xr, w * P + p, a.act_bf16), acc);
-                if (a.z) acc *= silu_f(load1(sb + a.off_z, p, a.act_bf16));
-                store1(a.y, ((size_t)m.b * H + m.h) * P + p, a.out_bf16, acc);
-            }
-            if (m.f) {
-                // S_new = Pm1 * S0 + sum_{i<=w} a_i x_i B_i^T, stored rounded to the state dtype
-                const float* av = tbl + L;
-                const uint8_t* br = sb + a.off_B;
-                char* dst_tile = static_cast<char*>(a.state) + ((size_t)m.s * H + m.h) * TILE;
-                constexpr int RC = KR < 8 ? KR : 8;
+        }
 #pragma unroll
-                for (int kc = 0; kc < KR; kc += RC) {
-                    float acc[RC][8];
+        for (int ch = 0; ch < Sh::NCH; ++ch) reduce_scatter<Sh::NQ, Sh::NQ>(part + ch * Sh::NQ);
+        const float Pm1 = tbl[2 * L];
+        const float Dh = __ldg(a.D + m.h);
+#pragma unroll
+        for (int ch = 0; ch < Sh::NCH; ++ch) {
+            const int p = row0 + Sh::RPI * (ch * Sh::NQ + q);
+            float acc = Pm1 * part[ch * Sh::NQ];
+            float acc2 = 0.f;
+            int i = 0;
+#pragma unroll 1
+            for (; i + 1 <= w; i += 2) {
+                acc = fmaf(tbl[i], load1(xr, i * P + p, bf), acc);
+                acc2 = fmaf(tbl[i + 1], load1(xr, (i + 1) * P + p, bf), acc2);
+            }
+            if (i == w) acc = fmaf(tbl[w], load1(xr, w * P + p, bf), acc);
+            acc += acc2;
+            acc = fmaf(Dh, load1(xr, w * P + p, bf), acc);
+            if (a.z) acc *= silu_f(load1(sb + a.off_z, p, bf));
+            store1(a.y, ((size_t)m.b * a.H + m.h) * P + p, a.out_bf16, acc);
+        }
+        if (m.f) {
+            // S = Pm1 * S0 + sum_{i<=w} a_i x_i B_i^T, stored rounded to the state dtype.
+            // The group's ring B entries go to this warp's scratch first.
+            const int g = m.h / (a.H / a.G);
+            const uint4* src = reinterpret_cast<const uint4*>(
+                static_cast<const char*>(a.ring_B) + ((size_t)m.s * a.G + g) * L * N * sa);
+            uint4* dst = reinterpret_cast<uint4*>(scratch);
+            const int nchunk = (w + 1) * N * sa / 16;
+            for (int c2 = lane; c2 < nchunk; c2 += 32) dst[c2] = src[c2];
+            __syncwarp();
+            const float* av = tbl + L;
+            char* tile_out = static_cast<char*>(a.state) + ((size_t)m.s * a.H + m.h) * Sh::TILE;
+            constexpr int RC = Sh::ITER < 8 ? Sh::ITER : 8;
+#pragma unroll 1
+            for (int t0 = 0; t0 < Sh::ITER; t0 += RC) {
+                float acc[RC][8];
+#pragma unroll
+                for (int r = 0; r < RC; ++r) {
+                    const int p = row0 + Sh::RPI * (t0 + r);
+                    float s8[8];
+                    load8(sb + ((size_t)p * N + q * 8) * Sh::SS, ST::bf16, s8);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) acc[r][j] = Pm1 * s8[j];
+                }
+                for (int i = 0; i <= w; ++i) {
+                    float bi[8];
+                    load8(scratch + ((size_t)i * N + q * 8) * sa, bf, bi);
+                    const float ai = av[i];
 #pragma unroll
                     for (int r = 0; r < RC; ++r) {
-                        const int p = r0 + RP * (kc + r);
-                        float s8[8];
-                        load8(sb + ((size_t)p * N + q * 8) * SS, ST::bf16, s8);
+                        const int p = row0 + Sh::RPI * (t0 + r);
+                        const float ax = ai * load1(xr, i * P + p, bf);
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) acc[r][j] = Pm1 * s8[j];
-                    }
-                    for (int i = 0; i <= w; ++i) {
-                        float bi[8];
-                        load8(br + ((size_t)i * N + q * 8) * sa, a.act_bf16, bi);
-                        const float ai = av[i];
-#pragma unroll
-                        for (int r = 0; r < RC; ++r) {
-                            const int p = r0 + RP * (kc + r);
-                            const float ax = ai * load1(xr, i * P + p, a.act_bf16);
-#pragma unroll
-                            for (int j = 0; j < 8; ++j) acc[r][j] = fmaf(ax, bi[j], acc[r][j]);
-                        }
-                    }
-#pragma unroll
-                    for (int r = 0; r < RC; ++r) {
-                        const int p = r0 + RP * (kc + r);
-                        store8(dst_tile + ((size_t)p * N + q * 8) * SS, ST::bf16, acc[r]);
+                        for (int j = 0; j < 8; ++j) acc[r][j] = fmaf(ax, bi[j], acc[r][j]);
                     }
                 }
+#pragma unroll
+                for (int r = 0; r < RC; ++r) {
+                    const int p = row0 + Sh::RPI * (t0 + r);
+                    store8(tile_out + ((size_t)p * N + q * 8) * Sh::SS, ST::bf16, acc[r]);
+                }
             }
-        }
-        __syncthreads();
-        if (*abort_flag) break;
-        if (tid == 0) issue(k + stages);
-    }
-    // wind down after a timeout: wait (bounded) for copies still in flight
-    if (*abort_flag && tid == 0) {
-        for (int j = k; j < k + stages; ++j) {
-            const int item = blockIdx.x + j * gridDim.x;
-            if (item >= n_items) break;
-            mbar_wait_bounded(&bars[j % stages], (j / stages) & 1);
+            __syncwarp();
         }
     }
-}
+};
 
 template <int P, int N, class ST>
-__global__ void __launch_bounds__(kThreads) full_state_kernel(const FullArgs a) {
-    extern __shared__ __align__(128) uint8_t smem[];
-    uint64_t* bars = reinterpret_cast<uint64_t*>(smem);
-    Meta* meta = reinterpret_cast<Meta*>(smem + 128);
-    int* abort_flag = reinterpret_cast<int*>(smem + 128 + kMaxStages * sizeof(Meta));
-    uint8_t* stage0 = smem + kFixedSmem;
+struct FullPolicy {
+    using Sh = TileShape<P, N, ST>;
+    static constexpr int kGroup = kGroupWarps;
+    struct Args {
+        void* state;
+        const void* x;
+        const float* dt_raw;
+        const float* dt_bias;
+        const float* A;
+        const void* B;
+        const void* C;
+        const float* D;
+        const void* z;
+        const int32_t* ci;
+        void* y;
+        int32_t* dev_err;
+        int batch, H, G, num_slots, act_bf16, out_bf16, softplus;
+        int stages, stage_bytes, stage_off, scratch_off, warp_scratch;
+        int off_x, off_B, off_C, off_z;
+    };
+    struct Meta {
+        int valid, s, b, h;
+        float dt, dA;
+    };
 
-    constexpr int SS = ST::bytes;
-    constexpr int TILE = P * N * SS;
-    constexpr int NQ = N / 8;
-    constexpr int RP = kThreads / NQ;
-    constexpr int KR = P / RP;
-    constexpr int DUP = NQ / KR;
+    static __device__ int n_items(const Args& a) { return a.batch * a.H; }
 
-    const int tid = threadIdx.x;
-    const int H = a.H, G = a.G;
-    const int sa = a.act_bf16 ? 2 : 4;
-    const int n_items = a.batch * H;
-    const int stages = a.stages;
-
-    if (tid == 0) {
-        for (int st = 0; st < stages; ++st) mbar_init(&bars[st], 1);
-        *abort_flag = 0;
-        fence_barrier_init();
-    }
-    __syncthreads();
-
-    uint64_t pol = 0;
-    auto issue = [&](int k) {
-        const int item = blockIdx.x + k * gridDim.x;
-        if (item >= n_items) return;
-        const int st = k % stages;
-        uint8_t* sb = stage0 + st * a.stage_bytes;
-        const int b = item / H, h = item - (item / H) * H;
+    // dt = softplus(dt_raw + dt_bias) and dA = exp(A dt), computed by the producer lanes
+    static __device__ int4 prefetch(const Args& a, int item) {
+        const int b = item / a.H, h = item - (item / a.H) * a.H;
         const int s = a.ci[b];
-        Meta m;
-        m.b = b; m.h = h; m.s = s; m.w = 0; m.f = 0; m.valid = 0; m.dt = 0.f; m.dA = 0.f;
-        if (s >= a.num_slots) set_dev_err(a.dev_err, RSSM_DEVERR_SLOT);
-        else if (s >= 0) m.valid = 1;
-        if (m.valid) {
-            float dt = a.dt_raw[(size_t)b * H + h] + (a.dt_bias ? a.dt_bias[h] : 0.f);
+        float dt = 0.f, dA = 0.f;
+        if (s >= 0 && s < a.num_slots) {
+            dt = a.dt_raw[(size_t)b * a.H + h] + (a.dt_bias ? a.dt_bias[h] : 0.f);
             if (a.softplus) dt = softplus_f(dt);
-            m.dt = dt;
-            m.dA = expf(a.A[h] * dt);
+            dA = expf(a.A[h] * dt);
         }
-        meta[st] = m;
+        return make_int4(s, b, __float_as_int(dt), __float_as_int(dA));
+    }
+
+    static __device__ void issue(const Args& a, int item, int4 r, Meta* meta, uint8_t* sb,
+                                 uint64_t* full, uint64_t pol) {
+        const int b = r.y, h = item - r.y * a.H;
+        Meta m{0, r.x, b, h, __int_as_float(r.z), __int_as_float(r.w)};
+        if (r.x >= a.num_slots) set_dev_err(a.dev_err, RSSM_DEVERR_SLOT);
+        else if (r.x >= 0) m.valid = 1;
+        *meta = m;
         if (!m.valid) {
-            mbar_arrive_plain(&bars[st]);
+            mbar_arrive_plain(full);
             return;
         }
-        const int g = h / (H / G);
-        const uint32_t tx = TILE + P * sa + 2 * N * sa + (a.z ? P * sa : 0);
-        mbar_arrive_expect_tx(&bars[st], tx);
-        bulk_g2s_hint(sb, static_cast<const char*>(a.state) + ((size_t)s * H + h) * TILE, TILE,
-                      &bars[st], pol);
-        bulk_g2s(sb + a.off_x, static_cast<const char*>(a.x) + ((size_t)b * H + h) * P * sa, P * sa,
-                 &bars[st]);
-        bulk_g2s(sb + a.off_B, static_cast<const char*>(a.B) + ((size_t)b * G + g) * N * sa, N * sa,
-                 &bars[st]);
-        bulk_g2s(sb + a.off_C, static_cast<const char*>(a.C) + ((size_t)b * G + g) * N * sa, N * sa,
-                 &bars[st]);
+        const int sa = a.act_bf16 ? 2 : 4;
+        const int g = h / (a.H / a.G);
+        mbar_arrive_expect_tx(full, Sh::TILE + P * sa + 2 * N * sa + (a.z ? P * sa : 0));
+        bulk_g2s_hint(sb, static_cast<const char*>(a.state) + ((size_t)m.s * a.H + h) * Sh::TILE,
+                      Sh::TILE, full, pol);
+        bulk_g2s(sb + a.off_x, static_cast<const char*>(a.x) + ((size_t)b * a.H + h) * P * sa, P * sa,
+                 full);
+        bulk_g2s(sb + a.off_B, static_cast<const char*>(a.B) + ((size_t)b * a.G + g) * N * sa, N * sa,
+                 full);
+        bulk_g2s(sb + a.off_C, static_cast<const char*>(a.C) + ((size_t)b * a.G + g) * N * sa, N * sa,
+                 full);
         if (a.z)
-            bulk_g2s(sb + a.off_z, static_cast<const char*>(a.z) + ((size_t)b * H + h) * P * sa,
-                     P * sa, &bars[st]);
-    };
-    if (tid == 0) {
-        pol = policy_evict_first();
-        for (int k = 0; k < stages; ++k) issue(k);
+            bulk_g2s(sb + a.off_z, static_cast<const char*>(a.z) + ((size_t)b * a.H + h) * P * sa,
+                     P * sa, full);
     }
 
-    const int q = tid % NQ, r0 = tid / NQ;
-    int k = 0;
-    for (;; ++k) {
-        const int item = blockIdx.x + k * gridDim.x;
-        if (item >= n_items) break;
-        const int st = k % stages;
-        const uint32_t par = (k / stages) & 1;
-        // all threads agree on the outcome, so the branch below stays uniform
-        const bool ok = __syncthreads_and(mbar_wait_bounded(&bars[st], par) ? 1 : 0) != 0;
-        if (!ok) {
-            *abort_flag = 1;
-            set_dev_err(a.dev_err, RSSM_DEVERR_TIMEOUT);
-        }
-        const Meta m = meta[st];
-        if (ok && m.valid) {
-            const uint8_t* sb = stage0 + st * a.stage_bytes;
-            float c[8], bq[8];
-            load8(sb + a.off_C + q * 8 * sa, a.act_bf16, c);
-            load8(sb + a.off_B + q * 8 * sa, a.act_bf16, bq);
-            char* dst_tile = static_cast<char*>(a.state) + ((size_t)m.s * H + m.h) * TILE;
-            float part[KR];
+    static __device__ void consume(const Args& a, int, const Meta& m, const uint8_t* sb, uint8_t*,
+                                   int lane, int wi) {
+        if (!m.valid) return;
+        const bool bf = a.act_bf16;
+        const int sa = bf ? 2 : 4;
+        const int q = lane % Sh::NQ, hr = lane / Sh::NQ;
+        const int row0 = wi * Sh::PW + hr;
+        float c[8], bq[8];
+        load8(sb + a.off_C + q * 8 * sa, bf, c);
+        load8(sb + a.off_B + q * 8 * sa, bf, bq);
+        char* tile_out = static_cast<char*>(a.state) + ((size_t)m.s * a.H + m.h) * Sh::TILE;
+        float part[Sh::ITER];
 #pragma unroll
-            for (int kk = 0; kk < KR; ++kk) {
-                const int p = r0 + RP * kk;
-                float s8[8];
-                load8(sb + ((size_t)p * N + q * 8) * SS, ST::bf16, s8);
-                const float dx = m.dt * load1(sb + a.off_x, p, a.act_bf16);
-                float acc = 0.f;
+        for (int t = 0; t < Sh::ITER; ++t) {
+            const int p = row0 + Sh::RPI * t;
+            float s8[8];
+            load8(sb + ((size_t)p * N + q * 8) * Sh::SS, ST::bf16, s8);
+            const float dx = m.dt * load1(sb + a.off_x, p, bf);
+            float acc = 0.f;
 #pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    s8[j] = fmaf(m.dA, s8[j], dx * bq[j]);
-                    acc = fmaf(s8[j], c[j], acc);
-                }
-                part[kk] = acc;
-                store8(dst_tile + ((size_t)p * N + q * 8) * SS, ST::bf16, s8);
+            for (int j = 0; j < 8; ++j) {
+                s8[j] = fmaf(m.dA, s8[j], dx * bq[j]);
+                acc = fmaf(s8[j], c[j], acc);
             }
-            const int kidx = reduce_scatter<KR, NQ>(part);
-            if ((q & (DUP - 1)) == 0) {
-                const int p = r0 + RP * kidx;
-                float acc = fmaf(__ldg(a.D + m.h), load1(sb + a.off_x, p, a.act_bf16), part[0]);
-                if (a.z) acc *= silu_f(load1(sb + a.off_z, p, a.act_bf16));
-                store1(a.y, ((size_t)m.b * H + m.h) * P + p, a.out_bf16, acc);
-            }
+            part[t] = acc;
+            store8(tile_out + ((size_t)p * N + q * 8) * Sh::SS, ST::bf16, s8);
         }
-        __syncthreads();
-        if (*abort_flag) break;
-        if (tid == 0) issue(k + stages);
-    }
-    if (*abort_flag && tid == 0) {
-        for (int j = k; j < k + stages; ++j) {
-            const int item = blockIdx.x + j * gridDim.x;
-            if (item >= n_items) break;
-            mbar_wait_bounded(&bars[j % stages], (j / stages) & 1);
+#pragma unroll
+        for (int ch = 0; ch < Sh::NCH; ++ch) reduce_scatter<Sh::NQ, Sh::NQ>(part + ch * Sh::NQ);
+        const float Dh = __ldg(a.D + m.h);
+#pragma unroll
+        for (int ch = 0; ch < Sh::NCH; ++ch) {
+            const int p = row0 + Sh::RPI * (ch * Sh::NQ + q);
+            float acc = fmaf(Dh, load1(sb + a.off_x, p, bf), part[ch * Sh::NQ]);
+            if (a.z) acc *= silu_f(load1(sb + a.off_z, p, bf));
+            store1(a.y, ((size_t)m.b * a.H + m.h) * P + p, a.out_bf16, acc);
         }
     }
-}
+};
 
 // ----------------------------------------------------------------------------
 // host side
@@ -531,6 +478,7 @@ int check_dims(const rssm_mamba2_dims* d) {
     return RSSM_OK;
 }
 
+
 template <class F>
 int dispatch_pn(int P, int N, int state_dtype, F&& f) {
 #define RSSM_M2_CASE(PP, NN)                                                        \
@@ -546,59 +494,62 @@ int dispatch_pn(int P, int N, int state_dtype, F&& f) {
     return RSSM_ERR_UNSUPPORTED;
 }
 
+// Generic launch arguments, copied into each policy's Args by go<>().
+struct OutCommon {
+    void* state; const void* C; const float* D; const void* z; const void* ring_x; const void* ring_B;
+    const int32_t* ci; const int32_t* row_wp; const uint8_t* row_flush; const float* ws; void* y;
+    int32_t* dev_err; int batch, H, G, L, num_slots, act_bf16, out_bf16;
+};
+
 struct OutLaunch {
-    OutArgs a;
+    OutCommon c;
     cudaStream_t stream;
     template <int P, int N, class ST>
     int go() {
-        DeviceInfo di;
-        if (!device_info(&di)) return RSSM_ERR_CUDA;
-        const int sa = a.act_bf16 ? 2 : 4;
-        const int L = a.L;
-        int off = P * N * ST::bytes;
-        a.off_x = off;   off += L * P * sa;
+        using Pol = OutPolicy<P, N, ST>;
+        typename Pol::Args a{};
+        a.state = c.state; a.C = c.C; a.D = c.D; a.z = c.z; a.ring_x = c.ring_x; a.ring_B = c.ring_B;
+        a.ci = c.ci; a.row_wp = c.row_wp; a.row_flush = c.row_flush; a.ws = c.ws; a.y = c.y;
+        a.dev_err = c.dev_err; a.batch = c.batch; a.H = c.H; a.G = c.G; a.L = c.L;
+        a.num_slots = c.num_slots; a.act_bf16 = c.act_bf16; a.out_bf16 = c.out_bf16;
+        const int sa = c.act_bf16 ? 2 : 4;
+        int off = Pol::Sh::TILE;
+        a.off_x = off;   off += c.L * P * sa;
         a.off_C = off;   off += N * sa;
         a.off_z = off;   off += P * sa;
-        a.off_tbl = off; off += tbl_floats(L) * 4;
-        a.off_B = off;   off += L * N * sa;
-        a.stage_bytes = (off + 127) & ~127;
-        PipeShape ps;
-        if (!pick_pipe_shape(di, a.stage_bytes, kFixedSmem, kMaxStages, &ps)) return RSSM_ERR_UNSUPPORTED;
-        a.stages = ps.stages;
-        const void* kfn = reinterpret_cast<const void*>(output_kernel<P, N, ST>);
-        if (!ensure_smem_limit(kfn, ps.smem_bytes)) return RSSM_ERR_CUDA;
-        const long items = (long)a.batch * a.H;
-        long grid = (long)di.sm_count * ps.ctas_per_sm;
-        if (grid > items) grid = items;
-        output_kernel<P, N, ST><<<(int)grid, kThreads, ps.smem_bytes, stream>>>(a);
-        return launch_status();
+        a.off_tbl = off; off += tbl_floats(c.L) * 4;
+        const int stage_bytes = (off + 127) & ~127;
+        const int warp_scratch = (c.L * N * sa + 127) & ~127;
+        return launch_pipe<Pol>(a, stage_bytes, warp_scratch, Pol::Sh::TILE, (long)c.batch * c.H,
+                                stream);
     }
 };
 
+struct FullCommon {
+    void* state; const void* x; const float* dt_raw; const float* dt_bias; const float* A;
+    const void* B; const void* C; const float* D; const void* z; const int32_t* ci; void* y;
+    int32_t* dev_err; int batch, H, G, num_slots, act_bf16, out_bf16, softplus;
+};
+
 struct FullLaunch {
-    FullArgs a;
+    FullCommon c;
     cudaStream_t stream;
     template <int P, int N, class ST>
     int go() {
-        DeviceInfo di;
-        if (!device_info(&di)) return RSSM_ERR_CUDA;
-        const int sa = a.act_bf16 ? 2 : 4;
-        int off = P * N * ST::bytes;
+        using Pol = FullPolicy<P, N, ST>;
+        typename Pol::Args a{};
+        a.state = c.state; a.x = c.x; a.dt_raw = c.dt_raw; a.dt_bias = c.dt_bias; a.A = c.A;
+        a.B = c.B; a.C = c.C; a.D = c.D; a.z = c.z; a.ci = c.ci; a.y = c.y; a.dev_err = c.dev_err;
+        a.batch = c.batch; a.H = c.H; a.G = c.G; a.num_slots = c.num_slots;
+        a.act_bf16 = c.act_bf16; a.out_bf16 = c.out_bf16; a.softplus = c.softplus;
+        const int sa = c.act_bf16 ? 2 : 4;
+        int off = Pol::Sh::TILE;
         a.off_x = off; off += P * sa;
         a.off_B = off; off += N * sa;
         a.off_C = off; off += N * sa;
         a.off_z = off; off += P * sa;
-        a.stage_bytes = (off + 127) & ~127;
-        PipeShape ps;
-        if (!pick_pipe_shape(di, a.stage_bytes, kFixedSmem, kMaxStages, &ps)) return RSSM_ERR_UNSUPPORTED;
-        a.stages = ps.stages;
-        const void* kfn = reinterpret_cast<const void*>(full_state_kernel<P, N, ST>);
-        if (!ensure_smem_limit(kfn, ps.smem_bytes)) return RSSM_ERR_CUDA;
-        const long items = (long)a.batch * a.H;
-        long grid = (long)di.sm_count * ps.ctas_per_sm;
-        if (grid > items) grid = items;
-        full_state_kernel<P, N, ST><<<(int)grid, kThreads, ps.smem_bytes, stream>>>(a);
-        return launch_status();
+        const int stage_bytes = (off + 127) & ~127;
+        return launch_pipe<Pol>(a, stage_bytes, 0, Pol::Sh::TILE, (long)c.batch * c.H, stream);
     }
 };
 
@@ -645,14 +596,15 @@ extern "C" int rssm_mamba2_precompute(const rssm_mamba2_dims* d, const float* A,
         return RSSM_ERR_INVALID_ARG;
     if (workspace_bytes < rssm_mamba2_workspace_size(d)) return RSSM_ERR_INVALID_ARG;
     const int L = d->ring_len;
-    const int smem = (((d->ngroups * L + 3) & ~3) + d->nheads * m2::tbl_floats(L)) * 4;
+    const int smem =
+        (((d->ngroups * d->dstate + d->ngroups * L + 3) & ~3) + d->nheads * m2::tbl_floats(L)) * 4;
     DeviceInfo di;
     if (!device_info(&di)) return RSSM_ERR_CUDA;
     if (smem > di.max_smem_optin) return RSSM_ERR_UNSUPPORTED;
     if (smem > 48 * 1024 &&
         !ensure_smem_limit(reinterpret_cast<const void*>(m2::precompute_kernel), smem))
         return RSSM_ERR_CUDA;
-    m2::precompute_kernel<<<d->batch, 128, smem, (cudaStream_t)stream>>>(
+    m2::precompute_kernel<<<d->batch, 256, smem, (cudaStream_t)stream>>>(
         d->nheads, d->dstate, d->ngroups, L, d->num_slots, d->act_dtype == RSSM_BF16, A, C, ring_dt,
         ring_B, cache_indices, row_wp, static_cast<float*>(workspace));
     return launch_status();
@@ -674,7 +626,7 @@ extern "C" int rssm_mamba2_output(const rssm_mamba2_dims* d, void* state, const 
     if (workspace_bytes < rssm_mamba2_workspace_size(d)) return RSSM_ERR_INVALID_ARG;
     m2::OutLaunch l{};
     l.stream = (cudaStream_t)stream;
-    m2::OutArgs& a = l.a;
+    m2::OutCommon& a = l.c;
     a.state = state; a.C = C; a.D = D; a.z = z; a.ring_x = ring_x; a.ring_B = ring_B;
     a.ci = cache_indices; a.row_wp = row_wp; a.row_flush = row_flush;
     a.ws = static_cast<const float*>(workspace); a.y = y; a.dev_err = dev_err;
@@ -719,7 +671,7 @@ extern "C" int rssm_mamba2_full_state_update(const rssm_mamba2_dims* d, void* st
         return RSSM_ERR_INVALID_ARG;
     m2::FullLaunch l{};
     l.stream = (cudaStream_t)stream;
-    m2::FullArgs& a = l.a;
+    m2::FullCommon& a = l.c;
     a.state = state; a.x = x; a.dt_raw = dt_raw; a.dt_bias = dt_bias; a.A = A; a.B = B; a.C = C;
     a.D = D; a.z = z; a.ci = cache_indices; a.y = y; a.dev_err = dev_err;
     a.batch = d->batch; a.H = d->nheads; a.G = d->ngroups; a.num_slots = d->num_slots;

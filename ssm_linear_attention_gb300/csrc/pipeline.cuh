@@ -1,0 +1,176 @@
+// pipeline.cuh -- persistent, warp-specialised streaming pipeline for sm_103a.
+//
+// One CTA per SM. The last warp is the producer: its lanes prefetch the row
+// metadata of the next 32 work items in parallel, and lane 0 fills a ring of
+// shared-memory stages with 1-D TMA bulk copies (global -> shared, completion
+// counted on the stage's "full" mbarrier). Every other warp is a consumer that
+// owns whole work items: it waits on the stage's full barrier, computes, and
+// releases the stage on its "empty" barrier. There is no CTA-wide barrier in the
+// loop, so consumer warps run independently and the copies for the next items
+// are in flight while the current ones are computed.
+//
+// Consumer warps form groups of K::kGroup warps; a group owns a work item and its
+// warps split the item's rows between them. Work item k of a CTA is global item
+// blockIdx.x + k * gridDim.x, lives in stage k % stages and is consumed by group
+// k % groups. The stage count is a multiple of the group count, so a stage is
+// always consumed by the same group and its uses complete strictly in order
+// (an mbarrier parity wait cannot tell use u from use u + 2).
+//
+// Every wait is bounded (RSSM_WAIT_NS); a wait that expires sets an abort flag
+// and RSSM_DEVERR_TIMEOUT, and all warps wind down.
+//
+// A kernel policy K provides:
+//   struct Args  (kernel arguments; must contain int stages, stage_bytes,
+//                 stage_off, scratch_off, warp_scratch; int32_t* dev_err)
+//   struct Meta  (per-stage metadata written by the producer, <= 64 bytes)
+//   static __device__ int  n_items(const Args&);
+//   static __device__ int4 prefetch(const Args&, int item);     any lane
+//   static __device__ void issue(const Args&, int item, int4 info, Meta* meta,
+//                                uint8_t* stage, uint64_t* full, uint64_t policy);
+//                                (lane 0; arrives on `full` exactly once)
+//   static __device__ void consume(const Args&, int item, const Meta&,
+//                                  const uint8_t* stage, uint8_t* scratch, int lane,
+//                                  int wi);   (whole consumer warp; wi = warp in group)
+//   static constexpr int kGroup;            (warps per consumer group)
+#pragma once
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace rssm {
+
+constexpr int kPipeMaxStages = 16;
+constexpr int kPipeMetaBytes = 64;
+constexpr int kPipeHeader = 2048;  // barriers + metadata + control, before the scratch
+constexpr unsigned kFull = 0xffffffffu;
+
+__device__ __forceinline__ void mbar_arrive_plain(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
+}
+
+constexpr int kPipeMaxGroups = 4;
+
+template <class K>
+__global__ void __launch_bounds__(32 * (kPipeMaxGroups * K::kGroup + 1), 1)
+    pipe_kernel(const typename K::Args a) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    static_assert(sizeof(typename K::Meta) <= kPipeMetaBytes, "meta too large");
+    uint64_t* fullb = reinterpret_cast<uint64_t*>(smem);
+    uint64_t* emptyb = fullb + kPipeMaxStages;
+    uint8_t* meta_base = smem + 256;
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 256 + kPipeMaxStages * kPipeMetaBytes);
+    uint8_t* stage0 = smem + a.stage_off;
+
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int nc = (blockDim.x >> 5) - 1;  // consumer warps
+    const int ng = nc / K::kGroup;         // consumer groups
+    const int NST = a.stages;
+    const int n = K::n_items(a);
+
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < NST; ++st) {
+            mbar_init(&fullb[st], 1);
+            mbar_init(&emptyb[st], K::kGroup);
+        }
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == nc) {
+        // ---------------- producer warp ----------------
+        const uint64_t pol = policy_evict_first();
+        for (int k0 = 0;; k0 += 32) {
+            const int my_item = blockIdx.x + (k0 + lane) * gridDim.x;
+            int4 info = make_int4(0, 0, 0, 0);
+            if (my_item < n) info = K::prefetch(a, my_item);
+            int stop = 0;
+            for (int j = 0; j < 32; ++j) {
+                const int k = k0 + j;
+                const int item = blockIdx.x + k * gridDim.x;
+                if (item >= n) {
+                    stop = 1;
+                    break;
+                }
+                int4 r;
+                r.x = __shfl_sync(kFull, info.x, j);
+                r.y = __shfl_sync(kFull, info.y, j);
+                r.z = __shfl_sync(kFull, info.z, j);
+                r.w = __shfl_sync(kFull, info.w, j);
+                int bad = 0;
+                if (lane == 0) {
+                    const int st = k % NST;
+                    bool ok = true;
+                    if (k >= NST) ok = mbar_wait_bounded(&emptyb[st], ((k / NST) - 1) & 1);
+                    if (!ok) {
+                        *abort_flag = 1;
+                        set_dev_err(a.dev_err, RSSM_DEVERR_TIMEOUT);
+                    }
+                    if (*abort_flag) {
+                        bad = 1;
+                    } else {
+                        K::issue(a, item, r,
+                                 reinterpret_cast<typename K::Meta*>(meta_base + st * kPipeMetaBytes),
+                                 stage0 + (size_t)st * a.stage_bytes, &fullb[st], pol);
+                    }
+                }
+                if (__shfl_sync(kFull, bad, 0)) {
+                    stop = 1;
+                    break;
+                }
+            }
+            if (stop) break;
+        }
+        return;
+    }
+
+    // ---------------- consumer warps ----------------
+    uint8_t* scratch = smem + a.scratch_off + warp * a.warp_scratch;
+    const int wi = warp % K::kGroup;
+    for (int k = warp / K::kGroup;; k += ng) {
+        const int item = blockIdx.x + k * gridDim.x;
+        if (item >= n) break;
+        const int st = k % NST;
+        const bool ok = __all_sync(kFull, mbar_wait_bounded(&fullb[st], (k / NST) & 1));
+        if (!ok) {
+            if (lane == 0) {
+                *abort_flag = 1;
+                set_dev_err(a.dev_err, RSSM_DEVERR_TIMEOUT);
+            }
+            break;
+        }
+        const typename K::Meta m =
+            *reinterpret_cast<const typename K::Meta*>(meta_base + st * kPipeMetaBytes);
+        K::consume(a, item, m, stage0 + (size_t)st * a.stage_bytes, scratch, lane, wi);
+        __syncwarp();
+        if (lane == 0) mbar_arrive_plain(&emptyb[st]);
+        if (*abort_flag) break;
+    }
+}
+
+// Host side: pick the pipeline shape, raise the shared-memory limit once, launch
+// one CTA per SM (fewer when there are fewer items).
+template <class K>
+int launch_pipe(typename K::Args a, int stage_bytes, int warp_scratch, int tile_bytes, long n_items,
+                cudaStream_t stream) {
+    if (n_items <= 0) return RSSM_OK;
+    DeviceInfo di;
+    if (!device_info(&di)) return RSSM_ERR_CUDA;
+    PipeCfg pc;
+    if (!pick_pipe(di, stage_bytes, warp_scratch, tile_bytes, kPipeHeader, kPipeMaxStages,
+                   K::kGroup, kPipeMaxGroups, &pc))
+        return RSSM_ERR_UNSUPPORTED;
+    a.stages = pc.stages;
+    a.stage_bytes = stage_bytes;
+    a.stage_off = pc.stage_off;
+    a.scratch_off = pc.scratch_off;
+    a.warp_scratch = warp_scratch;
+    const void* kfn = reinterpret_cast<const void*>(pipe_kernel<K>);
+    if (!ensure_smem_limit(kfn, pc.smem_bytes)) return RSSM_ERR_CUDA;
+    long grid = di.sm_count;
+    if (grid > n_items) grid = n_items;
+    pipe_kernel<K><<<(int)grid, 32 * (pc.groups * K::kGroup + 1), pc.smem_bytes, stream>>>(a);
+    return launch_status();
+}
+
+}  // namespace rssm
