@@ -200,7 +200,7 @@ struct OutPolicy {
         int32_t* dev_err;
         int batch, H, G, L, num_slots, act_bf16, out_bf16;
         int stages, stage_bytes, stage_off, scratch_off, warp_scratch;
-        int off_x, off_C, off_z, off_tbl;
+        int off_x, off_C, off_z, off_tbl, off_B;
     };
     struct Meta {
         int valid, s, b, h, w, f;
@@ -238,7 +238,8 @@ struct OutPolicy {
         const int g = h / (a.H / a.G);
         const int TBL = tbl_floats(a.L);
         const uint32_t xbytes = (m.w + 1) * P * sa;
-        mbar_arrive_expect_tx(full, Sh::TILE + xbytes + N * sa + (a.z ? P * sa : 0) + TBL * 4);
+        const uint32_t bbytes = m.f ? (m.w + 1) * N * sa : 0;
+        mbar_arrive_expect_tx(full, Sh::TILE + xbytes + N * sa + (a.z ? P * sa : 0) + TBL * 4 + bbytes);
         bulk_g2s_hint(sb, static_cast<const char*>(a.state) + ((size_t)m.s * a.H + h) * Sh::TILE,
                       Sh::TILE, full, pol);
         bulk_g2s(sb + a.off_x,
@@ -250,10 +251,14 @@ struct OutPolicy {
             bulk_g2s(sb + a.off_z, static_cast<const char*>(a.z) + ((size_t)b * a.H + h) * P * sa,
                      P * sa, full);
         bulk_g2s(sb + a.off_tbl, a.ws + ((size_t)b * a.H + h) * TBL, TBL * 4, full);
+        if (m.f)
+            bulk_g2s(sb + a.off_B,
+                     static_cast<const char*>(a.ring_B) + ((size_t)m.s * a.G + g) * a.L * N * sa,
+                     bbytes, full);
     }
 
-    static __device__ void consume(const Args& a, int, const Meta& m, const uint8_t* sb,
-                                   uint8_t* scratch, int lane, int wi) {
+    static __device__ void consume(const Args& a, int, const Meta& m, const uint8_t* sb, uint8_t*,
+                                   int lane, int wi) {
         if (!m.valid) return;
         const bool bf = a.act_bf16;
         const int sa = bf ? 2 : 4;
@@ -307,15 +312,8 @@ struct OutPolicy {
             store1(a.y, ((size_t)m.b * a.H + m.h) * P + p, a.out_bf16, acc);
         }
         if (m.f) {
-            // S = Pm1 * S0 + sum_{i<=w} a_i x_i B_i^T, stored rounded to the state dtype.
-            // The group's ring B entries go to this warp's scratch first.
-            const int g = m.h / (a.H / a.G);
-            const uint4* src = reinterpret_cast<const uint4*>(
-                static_cast<const char*>(a.ring_B) + ((size_t)m.s * a.G + g) * L * N * sa);
-            uint4* dst = reinterpret_cast<uint4*>(scratch);
-            const int nchunk = (w + 1) * N * sa / 16;
-            for (int c2 = lane; c2 < nchunk; c2 += 32) dst[c2] = src[c2];
-            __syncwarp();
+            // S = Pm1 * S0 + sum_{i<=w} a_i x_i B_i^T, stored rounded to the state dtype
+            const uint8_t* br = sb + a.off_B;
             const float* av = tbl + L;
             char* tile_out = static_cast<char*>(a.state) + ((size_t)m.s * a.H + m.h) * Sh::TILE;
             constexpr int RC = Sh::ITER < 8 ? Sh::ITER : 8;
@@ -332,7 +330,7 @@ struct OutPolicy {
                 }
                 for (int i = 0; i <= w; ++i) {
                     float bi[8];
-                    load8(scratch + ((size_t)i * N + q * 8) * sa, bf, bi);
+                    load8(br + ((size_t)i * N + q * 8) * sa, bf, bi);
                     const float ai = av[i];
 #pragma unroll
                     for (int r = 0; r < RC; ++r) {
@@ -348,7 +346,6 @@ struct OutPolicy {
                     store8(tile_out + ((size_t)p * N + q * 8) * Sh::SS, ST::bf16, acc[r]);
                 }
             }
-            __syncwarp();
         }
     }
 };
@@ -518,10 +515,9 @@ struct OutLaunch {
         a.off_C = off;   off += N * sa;
         a.off_z = off;   off += P * sa;
         a.off_tbl = off; off += tbl_floats(c.L) * 4;
+        a.off_B = off;   off += c.L * N * sa;
         const int stage_bytes = (off + 127) & ~127;
-        const int warp_scratch = (c.L * N * sa + 127) & ~127;
-        return launch_pipe<Pol>(a, stage_bytes, warp_scratch, Pol::Sh::TILE, (long)c.batch * c.H,
-                                stream);
+        return launch_pipe<Pol>(a, stage_bytes, 0, Pol::Sh::TILE, (long)c.batch * c.H, stream);
     }
 };
 

@@ -1,28 +1,28 @@
 // pipeline.cuh -- persistent, warp-specialised streaming pipeline for sm_103a.
 //
-// One CTA per SM. The last warp is the producer: its lanes prefetch the row
-// metadata of the next 32 work items in parallel, and lane 0 fills a ring of
-// shared-memory stages with 1-D TMA bulk copies (global -> shared, completion
-// counted on the stage's "full" mbarrier). Every other warp is a consumer that
-// owns whole work items: it waits on the stage's full barrier, computes, and
-// releases the stage on its "empty" barrier. There is no CTA-wide barrier in the
-// loop, so consumer warps run independently and the copies for the next items
-// are in flight while the current ones are computed.
-//
-// Consumer warps form groups of K::kGroup warps; a group owns a work item and its
-// warps split the item's rows between them. Work item k of a CTA is global item
-// blockIdx.x + k * gridDim.x, lives in stage k % stages and is consumed by group
-// k % groups. The stage count is a multiple of the group count, so a stage is
-// always consumed by the same group and its uses complete strictly in order
-// (an mbarrier parity wait cannot tell use u from use u + 2).
+// One CTA per SM holds `groups` independent pipelines. Each pipeline has one
+// producer warp and one consumer group of K::kGroup warps:
+//   * the producer's lanes prefetch the row metadata of its next 32 work items
+//     in parallel, and lane 0 fills the group's shared-memory stages with 1-D TMA
+//     bulk copies (global -> shared, completion counted on the stage's "full"
+//     mbarrier);
+//   * the consumer warps wait on a stage's full barrier, split the item's rows
+//     between them, and release the stage on its "empty" barrier.
+// Pipeline g owns the CTA's work items k = g, g + groups, ... and the stages
+// g, g + groups, ...; its u-th item uses stage g + groups * (u % stages_per_group).
+// A stage is therefore only ever used by one pipeline, in order, so mbarrier
+// parity waits are unambiguous. A producer lane needs several hundred cycles to
+// issue a tile's copies; with one producer per group the issue rate scales with
+// the groups, and an expensive item (a flush) only delays its own pipeline.
 //
 // Every wait is bounded (RSSM_WAIT_NS); a wait that expires sets an abort flag
 // and RSSM_DEVERR_TIMEOUT, and all warps wind down.
 //
 // A kernel policy K provides:
+//   static constexpr int kGroup;          warps per consumer group
 //   struct Args  (kernel arguments; must contain int stages, stage_bytes,
 //                 stage_off, scratch_off, warp_scratch; int32_t* dev_err)
-//   struct Meta  (per-stage metadata written by the producer, <= 64 bytes)
+//   struct Meta  (per-item metadata written by the producer, <= 64 bytes)
 //   static __device__ int  n_items(const Args&);
 //   static __device__ int4 prefetch(const Args&, int item);     any lane
 //   static __device__ void issue(const Args&, int item, int4 info, Meta* meta,
@@ -31,7 +31,6 @@
 //   static __device__ void consume(const Args&, int item, const Meta&,
 //                                  const uint8_t* stage, uint8_t* scratch, int lane,
 //                                  int wi);   (whole consumer warp; wi = warp in group)
-//   static constexpr int kGroup;            (warps per consumer group)
 #pragma once
 
 #include "common.cuh"
@@ -41,6 +40,7 @@ namespace rssm {
 
 constexpr int kPipeMaxStages = 16;
 constexpr int kPipeMetaBytes = 64;
+constexpr int kPipeMaxGroups = 4;
 constexpr int kPipeHeader = 2048;  // barriers + metadata + control, before the scratch
 constexpr unsigned kFull = 0xffffffffu;
 
@@ -48,24 +48,27 @@ __device__ __forceinline__ void mbar_arrive_plain(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
-constexpr int kPipeMaxGroups = 4;
-
 template <class K>
-__global__ void __launch_bounds__(32 * (kPipeMaxGroups * K::kGroup + 1), 1)
+__global__ void __launch_bounds__(32 * kPipeMaxGroups * (K::kGroup + 1), 1)
     pipe_kernel(const typename K::Args a) {
     extern __shared__ __align__(128) uint8_t smem[];
     static_assert(sizeof(typename K::Meta) <= kPipeMetaBytes, "meta too large");
     uint64_t* fullb = reinterpret_cast<uint64_t*>(smem);
     uint64_t* emptyb = fullb + kPipeMaxStages;
     uint8_t* meta_base = smem + 256;
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + 256 + kPipeMaxStages * kPipeMetaBytes);
+    volatile int* abort_flag =
+        reinterpret_cast<volatile int*>(smem + 256 + kPipeMaxStages * kPipeMetaBytes);
     uint8_t* stage0 = smem + a.stage_off;
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int nc = (blockDim.x >> 5) - 1;  // consumer warps
-    const int ng = nc / K::kGroup;         // consumer groups
+    const int ng = (blockDim.x >> 5) / (K::kGroup + 1);  // pipelines
+    const int nc = ng * K::kGroup;                        // consumer warps come first
     const int NST = a.stages;
+    const int spg = NST / ng;  // stages per pipeline
     const int n = K::n_items(a);
+    auto meta_of = [&](int st) {
+        return reinterpret_cast<typename K::Meta*>(meta_base + st * kPipeMetaBytes);
+    };
 
     if (threadIdx.x == 0) {
         for (int st = 0; st < NST; ++st) {
@@ -77,17 +80,18 @@ __global__ void __launch_bounds__(32 * (kPipeMaxGroups * K::kGroup + 1), 1)
     }
     __syncthreads();
 
-    if (warp == nc) {
-        // ---------------- producer warp ----------------
+    if (warp >= nc) {
+        // ---------------- producer warp of pipeline g ----------------
+        const int g = warp - nc;
         const uint64_t pol = policy_evict_first();
-        for (int k0 = 0;; k0 += 32) {
-            const int my_item = blockIdx.x + (k0 + lane) * gridDim.x;
+        int pos = 0, lap = 0;  // next stage of this pipeline, completed laps of its stages
+        for (int u0 = 0;; u0 += 32) {
+            const int my_item = blockIdx.x + (g + (u0 + lane) * ng) * gridDim.x;
             int4 info = make_int4(0, 0, 0, 0);
             if (my_item < n) info = K::prefetch(a, my_item);
             int stop = 0;
             for (int j = 0; j < 32; ++j) {
-                const int k = k0 + j;
-                const int item = blockIdx.x + k * gridDim.x;
+                const int item = blockIdx.x + (g + (u0 + j) * ng) * gridDim.x;
                 if (item >= n) {
                     stop = 1;
                     break;
@@ -99,20 +103,20 @@ __global__ void __launch_bounds__(32 * (kPipeMaxGroups * K::kGroup + 1), 1)
                 r.w = __shfl_sync(kFull, info.w, j);
                 int bad = 0;
                 if (lane == 0) {
-                    const int st = k % NST;
-                    bool ok = true;
-                    if (k >= NST) ok = mbar_wait_bounded(&emptyb[st], ((k / NST) - 1) & 1);
-                    if (!ok) {
+                    const int st = g + ng * pos;
+                    if (lap > 0 && !mbar_wait_bounded(&emptyb[st], (lap - 1) & 1)) {
                         *abort_flag = 1;
                         set_dev_err(a.dev_err, RSSM_DEVERR_TIMEOUT);
                     }
-                    if (*abort_flag) {
+                    if (*abort_flag)
                         bad = 1;
-                    } else {
-                        K::issue(a, item, r,
-                                 reinterpret_cast<typename K::Meta*>(meta_base + st * kPipeMetaBytes),
-                                 stage0 + (size_t)st * a.stage_bytes, &fullb[st], pol);
-                    }
+                    else
+                        K::issue(a, item, r, meta_of(st), stage0 + (size_t)st * a.stage_bytes,
+                                 &fullb[st], pol);
+                }
+                if (++pos == spg) {
+                    pos = 0;
+                    ++lap;
                 }
                 if (__shfl_sync(kFull, bad, 0)) {
                     stop = 1;
@@ -124,14 +128,15 @@ __global__ void __launch_bounds__(32 * (kPipeMaxGroups * K::kGroup + 1), 1)
         return;
     }
 
-    // ---------------- consumer warps ----------------
+    // ---------------- consumer warps of pipeline g ----------------
     uint8_t* scratch = smem + a.scratch_off + warp * a.warp_scratch;
-    const int wi = warp % K::kGroup;
-    for (int k = warp / K::kGroup;; k += ng) {
-        const int item = blockIdx.x + k * gridDim.x;
+    const int g = warp / K::kGroup, wi = warp % K::kGroup;
+    int pos = 0, lap = 0;
+    for (int u = 0;; ++u) {
+        const int item = blockIdx.x + (g + u * ng) * gridDim.x;
         if (item >= n) break;
-        const int st = k % NST;
-        const bool ok = __all_sync(kFull, mbar_wait_bounded(&fullb[st], (k / NST) & 1));
+        const int st = g + ng * pos;
+        const bool ok = __all_sync(kFull, mbar_wait_bounded(&fullb[st], lap & 1));
         if (!ok) {
             if (lane == 0) {
                 *abort_flag = 1;
@@ -139,11 +144,14 @@ __global__ void __launch_bounds__(32 * (kPipeMaxGroups * K::kGroup + 1), 1)
             }
             break;
         }
-        const typename K::Meta m =
-            *reinterpret_cast<const typename K::Meta*>(meta_base + st * kPipeMetaBytes);
+        const typename K::Meta m = *meta_of(st);
         K::consume(a, item, m, stage0 + (size_t)st * a.stage_bytes, scratch, lane, wi);
         __syncwarp();
         if (lane == 0) mbar_arrive_plain(&emptyb[st]);
+        if (++pos == spg) {
+            pos = 0;
+            ++lap;
+        }
         if (*abort_flag) break;
     }
 }
@@ -169,7 +177,7 @@ int launch_pipe(typename K::Args a, int stage_bytes, int warp_scratch, int tile_
     if (!ensure_smem_limit(kfn, pc.smem_bytes)) return RSSM_ERR_CUDA;
     long grid = di.sm_count;
     if (grid > n_items) grid = n_items;
-    pipe_kernel<K><<<(int)grid, 32 * (pc.groups * K::kGroup + 1), pc.smem_bytes, stream>>>(a);
+    pipe_kernel<K><<<(int)grid, 32 * pc.groups * (K::kGroup + 1), pc.smem_bytes, stream>>>(a);
     return launch_status();
 }
 
