@@ -218,6 +218,37 @@ int rssm_mamba2_decode(const rssm_mamba2_dims* dims, void* state, const float* A
                        const uint8_t* row_flush, void* workspace, size_t workspace_bytes,
                        void* y, int32_t* dev_err, rssm_stream_t stream);
 
+/* Size of the device array rssm_mamba2_decode_noalloc keeps its workspace in. */
+#define RSSM_NOALLOC_WORKSPACE_BYTES (16u << 20)
+
+/* rssm_mamba2_decode_noalloc -- rssm_mamba2_decode for callers that cannot allocate
+ * device memory. The pages have no counterpart: this is an interface for such
+ * callers, not part of the method. Some callers cannot provide the workspace that
+ * rssm_mamba2_decode needs -- a plug-in inside a host application that owns every
+ * device allocation, an engine whose device memory budget is fixed at start-up, a
+ * caller on a latency-critical path that must never enter the allocator. This
+ * entry point takes the same inputs and outputs (all device pointers, caller
+ * owned) but no workspace: the coefficient tables live in a fixed array of
+ * RSSM_NOALLOC_WORKSPACE_BYTES (16 MiB) inside the library's device image, held
+ * by every GPU that loads the library until the process exits. It allocates
+ * nothing and calls no allocating routine.
+ *   - Limit: rssm_mamba2_workspace_size(dims) must not exceed the array
+ *     (batch * nheads * round4(2L + 1) * 4 bytes; batch 512 x 128 heads at L = 16
+ *     needs 9 MiB); larger sizes return RSSM_ERR_UNSUPPORTED before any launch.
+ *   - Set-up: the first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call before
+ *     any stream capture. A failed look-up returns RSSM_ERR_CUDA.
+ *   - Sharing: every call on a device uses the same array and leaves its contents
+ *     there; nothing in it needs to start at zero. Calls whose executions overlap on
+ *     the GPU race on it, so keep them in one stream or order them.
+ * Other arguments, results and errors are those of rssm_mamba2_decode. */
+int rssm_mamba2_decode_noalloc(const rssm_mamba2_dims* dims, void* state, const float* A,
+                               const void* C, const float* D, const void* z, const void* ring_x,
+                               const float* ring_dt, const void* ring_B,
+                               const int32_t* cache_indices, const int32_t* row_wp,
+                               const uint8_t* row_flush, void* y, int32_t* dev_err,
+                               rssm_stream_t stream);
+
 /* rssm_mamba2_full_state_update -- the conventional decode step that reads and
  * writes the whole state every step ([M2] 关键源码片段, the baseline
  * selective_state_update branch). For each row with s >= 0, head h:

@@ -14,12 +14,14 @@ RSSM_OK, RSSM_ERR_INVALID_ARG, RSSM_ERR_UNSUPPORTED, RSSM_ERR_CONFIG, RSSM_ERR_C
 RSSM_F32, RSSM_BF16 = 0, 1
 RSSM_DEVERR_SLOT, RSSM_DEVERR_CURSOR, RSSM_DEVERR_TIMEOUT = 1, 2, 4
 RSSM_CURSOR_STANDARD, RSSM_CURSOR_SPEC_COMMIT, RSSM_CURSOR_RESET = 0, 1, 2
+RSSM_NOALLOC_WORKSPACE_BYTES = 16 << 20
 
 # every symbol include/rssm.h declares
 EXPORTS = (
     "rssm_status_string", "rssm_abi_version", "rssm_advance_cursors", "rssm_ring_append",
     "rssm_mamba2_workspace_size", "rssm_mamba2_precompute", "rssm_mamba2_output",
-    "rssm_mamba2_decode", "rssm_mamba2_full_state_update", "rssm_gdn_ring_append",
+    "rssm_mamba2_decode", "rssm_mamba2_decode_noalloc", "rssm_mamba2_full_state_update",
+    "rssm_gdn_ring_append",
     "rssm_gdn_workspace_size", "rssm_gdn_precompute", "rssm_gdn_output", "rssm_gdn_decode",
     "rssm_gdn_full_state_decode", "rssm_gdn_spec_workspace_size", "rssm_gdn_spec_verify",
 )
@@ -66,6 +68,8 @@ def _declare(L):
                                     _VP, _VP, _VP]),
         "rssm_mamba2_decode": (_I, [m2, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                     _VP, _SZ, _VP, _VP, _VP]),
+        "rssm_mamba2_decode_noalloc": (_I, [m2, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                            _VP, _VP, _VP, _VP]),
         "rssm_mamba2_full_state_update": (_I, [m2, _VP, _VP, _VP, _VP, _I, _VP, _VP, _VP, _VP,
                                                _VP, _VP, _VP, _VP, _VP]),
         "rssm_gdn_ring_append": (_I, [gd, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
@@ -172,6 +176,16 @@ def rssm_mamba2_decode(dims, state, A, C, D, z, ring_x, ring_dt, ring_B, cache_i
           _ptr(z), _ptr(ring_x), _ptr(ring_dt), _ptr(ring_B), _ptr(cache_indices), _ptr(row_wp),
           _ptr(row_flush), _ptr(workspace), workspace_bytes, _ptr(y), _ptr(dev_err),
           _stream(stream))
+
+
+def rssm_mamba2_decode_noalloc(dims, state, A, C, D, z, ring_x, ring_dt, ring_B, cache_indices,
+                               row_wp, row_flush, y, dev_err=None, stream=None):
+    """rssm_mamba2_decode without a workspace argument, for callers that cannot
+    allocate device memory: the tables live in the library's fixed device array
+    (RSSM_NOALLOC_WORKSPACE_BYTES). Calls that overlap on the GPU share that array."""
+    _call("rssm_mamba2_decode_noalloc", ctypes.byref(dims), _ptr(state), _ptr(A), _ptr(C), _ptr(D),
+          _ptr(z), _ptr(ring_x), _ptr(ring_dt), _ptr(ring_B), _ptr(cache_indices), _ptr(row_wp),
+          _ptr(row_flush), _ptr(y), _ptr(dev_err), _stream(stream))
 
 
 def rssm_mamba2_full_state_update(dims, state, x, dt_raw, dt_bias, dt_softplus, A, B, C, D, z,
