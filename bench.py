@@ -1,17 +1,23 @@
-"""Benchmark: ReplaySSM Mamba2 decode at batch 512 on GB300.
+"""Benchmark: ReplaySSM decode on GB300.
 
-Workload (one step = one decode step of one layer for the whole batch: cursor
-advance, ring append, precompute, output/flush): batch 512, nheads 128,
-headdim 64, dstate 128, ngroups 8, ring L 16, bf16 checkpoint pool of 1024
-slots ~ N(0, 0.1), cache indices = first 512 of a seeded permutation,
-desynchronised initial write_pos ~ U{0..15}, x/z/B/C bf16, dt/A/D fp32, bf16
-output. 64 distinct seeded input sets are resident in HBM and cycled.
+Default workload (`--workload mamba2`), the headline line: Mamba2 decode at batch
+512, nheads 128, headdim 64, dstate 128, ngroups 8, ring L 16, bf16 checkpoint
+pool of 1024 slots ~ N(0, 0.1), cache indices = first 512 of a seeded
+permutation, desynchronised initial write_pos ~ U{0..15}, x/z/B/C bf16, dt/A/D
+fp32, bf16 output; 64 distinct seeded input sets resident in HBM and cycled. One
+step = cursor advance, ring append, precompute, output/flush for the whole batch.
+The same line carries the gated-delta-net decode (`gdn_decode`) and speculative
+verify (`gdn_spec`) results of their own workloads as sub-objects.
 
-Prints ONE JSON line (rank 0):
+Each step is replayed from CUDA graphs: one graph holds cursor advance + ring
+append + precompute, a second the output kernel, and CUDA events recorded on the
+stream between them time the output kernel inside the timed region.
+
+Keys of the JSON line (rank 0):
   value       decode rows/s over all ranks (device-timed, inputs resident)
-  e2e         same metric through the public API with pinned host buffers:
-              host->device copy of each step's inputs and device->host copy of
-              y inside the timed region
+  e2e         same metric through the public API (Mamba2ReplayDecoder.step) with
+              pinned host buffers: host->device copy of each step's inputs and
+              device->host copy of y inside the timed region
   roofline    output kernel: algorithmic bytes per launch / CUDA-event duration
               of that kernel inside the timed region, against the measured HBM
               copy bandwidth
@@ -20,7 +26,10 @@ Prints ONE JSON line (rank 0):
   full_state  the in-house conventional kernel (whole state read+written per
               step) on an identical pool, same inputs
 
---impl reference runs the oracle arm (the only reference implementation this
+`--workload gdn` / `--workload spec` print the gated-delta-net lines as the main
+line; `--workload sweep` prints one line per point of the Mamba2 sweep (batch x L
+x state dtype, 5% forced flushes), each with the full-state kernel beside it.
+`--impl reference` runs the oracle arm (the only reference implementation this
 method has here) on the same metric and workload.
 Multi-GPU (torchrun): every rank runs its own independent replica of the
 workload (rows are independent; no collective on the data path), timing is
@@ -58,8 +67,12 @@ def parse():
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-full-state", action="store_true")
     ap.add_argument("--seed", type=int, default=0)
-    ap.add_argument("--batch", type=int, default=512)
-    ap.add_argument("--num-slots", type=int, default=1024)
+    ap.add_argument("--batch", type=int, default=None)
+    ap.add_argument("--num-slots", type=int, default=None)
+    ap.add_argument("--workload", default="mamba2", choices=["mamba2", "gdn", "spec", "sweep"])
+    ap.add_argument("--no-gdn", action="store_true",
+                    help="mamba2 line only (skip the gdn_decode / gdn_spec sub-objects)")
+    ap.add_argument("--sweep-steps", type=int, default=200)
     return ap.parse_args()
 
 
@@ -209,22 +222,139 @@ def read_peaks():
     return 6800.0, "fallback"
 
 
-def traffic_record(kernel_src):
-    """DRAM bytes per launch of the output kernel from the committed ncu summary,
-    valid only while the kernel source is unchanged (sha256 recorded beside it)."""
+def traffic_record(kernel_src, profile):
+    """DRAM bytes per launch of a kernel from its committed ncu summary, valid only
+    while the kernel source is unchanged (sha256 recorded beside it)."""
     src = os.path.join(ROOT, "ssm_linear_attention_gb300", "csrc", kernel_src)
-    prof = os.path.join(ROOT, "profiles", "mamba2_output_kernel_batch512.md")
+    prof = os.path.join(ROOT, "profiles", profile)
     if not (os.path.exists(src) and os.path.exists(prof)):
         return None
     sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
     rec = {}
     for line in open(prof):
-        if ":" in line and line.strip().startswith(("source_sha256", "traffic_bytes_per_launch")):
+        if ":" in line and line.strip().strip("-* `").startswith(("source_sha256",
+                                                                   "traffic_bytes_per_launch")):
             k, v = line.split(":", 1)
-            rec[k.strip().strip("`- ")] = v.strip().strip("`")
+            rec[k.strip().strip("-* `")] = v.strip().strip("`")
     if rec.get("source_sha256") == sha and rec.get("traffic_bytes_per_launch"):
-        return int(rec["traffic_bytes_per_launch"])
+        return int(float(rec["traffic_bytes_per_launch"]))
     return None
+
+
+def gdn_output_bytes(wl, row_wp, row_flush, out_bytes=2):
+    """Algorithmic bytes of one GDN output-kernel launch: checkpoint read, d entries
+    0..w-1, this step's k (from the ring), q, v, the d write, o, and on flush rows
+    the state write and the earlier k entries. The tables are excluded."""
+    HV, HK, K, V = wl.num_v_heads, wl.num_k_heads, wl.head_k_dim, wl.head_v_dim
+    sa = 2 if wl.act_dtype == "bf16" else 4
+    w = row_wp.astype(np.int64)
+    f = row_flush.astype(np.int64)
+    per_row = (HV * V * K * 4 + w * HV * V * 4 + HV * V * 4 + 2 * HK * K * sa + HV * V * sa
+               + HV * V * out_bytes + f * (HV * V * K * 4 + w * HK * K * sa))
+    return int(per_row.sum())
+
+
+def gdn_full_bytes(wl, batch, out_bytes=2):
+    HV, HK, K, V = wl.num_v_heads, wl.num_k_heads, wl.head_k_dim, wl.head_v_dim
+    sa = 2 if wl.act_dtype == "bf16" else 4
+    return batch * (2 * HV * V * K * 4 + 2 * HK * K * sa + HV * V * sa + 2 * HV * 4
+                    + HV * V * out_bytes)
+
+
+def spec_round_bytes(wl, hist, fold, out_bytes=2):
+    """Algorithmic bytes of one verify round (fold + verify) per row, given the
+    history count and pending-fold flag of each row, as (verify, fold) totals.
+    Verify: checkpoint read, the drafts' q, k, v, beta, g, the history d entries,
+    the drafts' d, raw v, k, g, beta written to the rings, o. Fold: state read and
+    write plus the committed entries' k, raw v, beta, g."""
+    HV, HK, K, V, T = wl.num_v_heads, wl.num_k_heads, wl.head_k_dim, wl.head_v_dim, wl.T
+    sa = 2 if wl.act_dtype == "bf16" else 4
+    c = hist.astype(np.int64)
+    verify = (HV * V * K * 4 + T * (2 * HK * K * sa + HV * V * sa + 2 * HV * 4)
+              + c * HV * V * 4 + T * (HV * V * 4 + HV * V * sa + HK * K * sa + 2 * HV * 4)
+              + T * HV * V * out_bytes)
+    return int(verify.sum()), int(fold["bytes"])
+
+
+def simulate_spec(wl, ci, accepted_seq, L, T):
+    """Per-round (history count, pending fold, fold bytes) for a sequence of
+    accepted counts, following the commit rule (a pending fold retires the
+    committed run, then cnt += accepted and flush = cnt + T > L). Bookkeeping for
+    the byte count; the kernels keep their own cursors on the device."""
+    HV, HK, K, V = wl.num_v_heads, wl.num_k_heads, wl.head_k_dim, wl.head_v_dim
+    sa = 2 if wl.act_dtype == "bf16" else 4
+    n = wl.num_slots
+    cnt = np.zeros(n, np.int64)
+    base = np.zeros(n, np.int64)
+    flush = np.zeros(n, np.int64)
+    out = []
+    for acc in accepted_seq:
+        fl = flush[ci].copy()
+        cr = cnt[ci].copy()
+        hist = np.where(fl == 1, 0, cr)
+        fold_b = int((fl * (2 * HV * V * K * 4 + cr * (HK * K * sa + HV * V * sa + 2 * HV * 4))).sum())
+        out.append((hist, fl, {"bytes": fold_b}))
+        base[ci] = np.where(fl == 1, (base[ci] + cr) % L, base[ci])
+        cnt[ci] = np.where(fl == 1, 0, cr) + acc
+        flush[ci] = (cnt[ci] + T > L).astype(np.int64)
+    return out, cnt
+
+
+# --------------------------------------------------------------------------- #
+# CUDA graphs and the timed loop                                              #
+# --------------------------------------------------------------------------- #
+
+def _graphs(fns):
+    """Capture each zero-argument callable into its own CUDA graph."""
+    import torch
+    out = []
+    for fn in fns:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        out.append(g)
+    torch.cuda.synchronize()
+    return out
+
+
+def _bus_id(dev):
+    import torch
+    try:
+        p = torch.cuda.get_device_properties(dev)
+        return "%08x:%02x:%02x" % (getattr(p, "pci_domain_id", 0), p.pci_bus_id, p.pci_device_id)
+    except Exception:
+        return None
+
+
+def _timed_graphs(pre, main, K, dist, dev, offset=0, clocks=True):
+    """Replay K steps: pre[k % G] (may be None), an event, main[k % G], an event.
+    Returns (elapsed ms of the whole region, max over ranks; per-step main ms;
+    clock record)."""
+    import torch
+    stream = torch.cuda.current_stream()
+    G = len(main)
+    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist.barrier()
+    torch.cuda.synchronize()
+    clk = ClockSampler() if clocks else None
+    if clk:
+        time.sleep(0.3)
+    start.record(stream)
+    for k in range(K):
+        j = (k + offset) % G
+        if pre is not None:
+            pre[j].replay()
+        ev_a[k].record(stream)
+        main[j].replay()
+        ev_b[k].record(stream)
+    end.record(stream)
+    torch.cuda.synchronize()
+    dist.barrier()
+    rec = clk.stop(_bus_id(dev)) if clk else None
+    per = [a.elapsed_time(b) for a, b in zip(ev_a, ev_b)]
+    return dist.max(start.elapsed_time(end)), per, rec
 
 
 # --------------------------------------------------------------------------- #
@@ -261,20 +391,54 @@ def cpu_oracle_rate(wl, seconds, max_rows=64):
     return rate, nth, sample
 
 
+def cpu_oracle_rate_gdn(wl, seconds, max_rows=16):
+    """The float64 GDN recurrence on a sample of rows (rows/s, threads, sample)."""
+    import oracle
+    nth = oracle.default_threads()
+    rows = np.arange(min(max_rows, wl.batch))
+    ci = wl.cache_indices()
+    state = np.ascontiguousarray(
+        np.stack([wl.slot_state(int(ci[r])) for r in rows]).astype(np.float64))
+    inputs = []
+    for t in range(4):
+        inp = wl.step_inputs(t)
+        inputs.append({k: np.ascontiguousarray(v[rows], dtype=np.float64) for k, v in inp.items()})
+    loc = np.arange(len(rows), dtype=np.int32)
+    done, t0 = 0, time.perf_counter()
+    while True:
+        inp = inputs[done % len(inputs)]
+        oracle.gdn_step(state, inp["q"], inp["k"], inp["v"], inp["beta"], inp["g"], loc,
+                        nthreads=nth)
+        done += 1
+        el = time.perf_counter() - t0
+        if done >= 2 and el >= seconds:
+            break
+    rate = done * len(rows) / el
+    sample = "%d rows x %d steps of the float64 gated delta recurrence (%.1f s)" % (len(rows),
+                                                                                    done, el)
+    return rate, nth, sample
+
+
 # --------------------------------------------------------------------------- #
-# main arm                                                                    #
+# Mamba2 (headline)                                                           #
 # --------------------------------------------------------------------------- #
 
-def run_ours(args, dist):
+def _device(dist):
+    import torch
+    dev = torch.device("cuda", dist.local if dist.world > 1 else 0)
+    torch.cuda.set_device(dev)
+    return dev
+
+
+def run_mamba2(args, dist):
     import torch
 
     import rssm_workloads as W
     import ssm_linear_attention_gb300 as ssm
 
-    dev = torch.device("cuda", dist.local if dist.world > 1 else 0)
-    torch.cuda.set_device(dev)
+    dev = _device(dist)
     ssm.lib()
-    wl = W.mamba2_large(batch=args.batch, num_slots=args.num_slots,
+    wl = W.mamba2_large(batch=args.batch or 512, num_slots=args.num_slots or 1024,
                         seed=shard_seed(args.seed, dist.rank))
     prm = wl.params()
     bf = torch.bfloat16
@@ -297,62 +461,50 @@ def run_ours(args, dist):
     sets = [to_dev(wl.step_inputs(t)) for t in range(args.input_sets)]
     torch.cuda.synchronize()
 
-    def one_step(k):
-        x, dt, Bm, C, z = sets[k % len(sets)]
-        dec.advance(ci)
-        dec.append(x, dt, Bm, ci)
-        dec.precompute(C, ci)
-        return dec.output(C, z, ci)
+    K = args.steps
+    G = min(len(sets), max(K, 1))
 
-    for k in range(args.warmup):
-        one_step(k)
+    def pre_fn(j):
+        x, dt, Bm, C, z = sets[j]
+
+        def f():
+            dec.advance(ci)
+            dec.append(x, dt, Bm, ci)
+            dec.precompute(C, ci)
+        return f
+
+    def out_fn(j):
+        x, dt, Bm, C, z = sets[j]
+        return lambda: dec.output(C, z, ci)
+
+    # eager warm-up (sets shared-memory limits, first-use costs), then capture
+    for k in range(max(args.warmup, 3)):
+        pre_fn(k % G)()
+        out_fn(k % G)()
+    torch.cuda.synchronize()
+    g_pre = _graphs([pre_fn(j) for j in range(G)])
+    g_out = _graphs([out_fn(j) for j in range(G)])
+    # capture does not run the work: warm up the graphs themselves
+    for k in range(max(args.warmup, 3)):
+        g_pre[k % G].replay()
+        g_out[k % G].replay()
     torch.cuda.synchronize()
     slot_wp0 = dec.slot_wp.cpu().numpy().astype(np.int64)
 
-    K = args.steps
-    stream = torch.cuda.current_stream()
-    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    dist.barrier()
-    torch.cuda.synchronize()
-    clk = ClockSampler()
-    time.sleep(0.3)
-    start.record(stream)
-    for k in range(K):
-        x, dt, Bm, C, z = sets[(k + args.warmup) % len(sets)]
-        dec.advance(ci)
-        dec.append(x, dt, Bm, ci)
-        dec.precompute(C, ci)
-        ev_a[k].record(stream)
-        dec.output(C, z, ci)
-        ev_b[k].record(stream)
-    end.record(stream)
-    torch.cuda.synchronize()
-    dist.barrier()
-    bus = None
-    try:
-        p = torch.cuda.get_device_properties(dev)
-        bus = "%08x:%02x:%02x" % (getattr(p, "pci_domain_id", 0), p.pci_bus_id, p.pci_device_id)
-    except Exception:
-        bus = None
-    clocks = clk.stop(bus)
-    elapsed_ms = start.elapsed_time(end)
-    out_ms = [a.elapsed_time(b) for a, b in zip(ev_a, ev_b)]
-    max_ms = dist.max(elapsed_ms)
+    elapsed, out_ms, clocks = _timed_graphs(g_pre, g_out, K, dist, dev, offset=args.warmup)
     assert int(dec.dev_err.abs().sum().item()) == 0, "device error flag set during the bench"
+    del g_pre, g_out
 
-    ms_step = max_ms / K
+    ms_step = elapsed / K
     rows_s = dist.world * wl.batch / (ms_step * 1e-3)
 
-    # algorithmic bytes
     curs = simulate_cursors(slot_wp0, ci_np, wl.L, K)
     out_b = np.mean([output_kernel_bytes(wl, w, f) for w, f in curs])
     step_b = np.mean([step_bytes(wl, w, f) for w, f in curs])
     out_avg_ms = float(np.mean(out_ms))
     peak, peak_kind = read_peaks()
     achieved = out_b / (out_avg_ms * 1e-3) / 1e9
-    traffic = traffic_record("mamba2.cu")
+    traffic = traffic_record("mamba2.cu", "mamba2_output_kernel_batch512.md")
 
     # end to end through the public API with pinned host buffers
     e2e = None
@@ -369,27 +521,29 @@ def run_ours(args, dist):
         y_host = torch.empty(wl.batch, wl.nheads, wl.headdim, dtype=bf).pin_memory()
         h2d = sum(v.numel() * v.element_size() for v in host_sets[0].values())
         d2h = y_host.numel() * y_host.element_size()
-        for k in range(3):
+        stream = torch.cuda.current_stream()
+
+        def e2e_step(k):
             hs = host_sets[k % len(host_sets)]
             for k2 in dsts:
                 dsts[k2].copy_(hs[k2], non_blocking=True)
             y = dec.step(dsts["x"], dsts["dt_raw"], dsts["B"], dsts["C"], dsts["z"], ci)
             y_host.copy_(y, non_blocking=True)
+
+        for k in range(3):
+            e2e_step(k)
         torch.cuda.synchronize()
         dist.barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         for k in range(args.e2e_steps):
-            hs = host_sets[k % len(host_sets)]
-            for k2 in dsts:
-                dsts[k2].copy_(hs[k2], non_blocking=True)
-            y = dec.step(dsts["x"], dsts["dt_raw"], dsts["B"], dsts["C"], dsts["z"], ci)
-            y_host.copy_(y, non_blocking=True)
+            e2e_step(k)
         e1.record(stream)
         torch.cuda.synchronize()
         e_ms = dist.max(e0.elapsed_time(e1)) / args.e2e_steps
         e2e = {"value": dist.world * wl.batch / (e_ms * 1e-3), "unit": UNIT,
-               "ms_per_step": e_ms, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+               "ms_per_step": e_ms, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "api": "Mamba2ReplayDecoder.step (eager, 4 C-ABI calls per step)"}
 
     # the in-house conventional kernel on an identical pool
     full = None
@@ -400,24 +554,24 @@ def run_ours(args, dist):
                                           out_dtype=bf, device=dev)
         fdec.state.copy_(dec.state)
         del dec
-        for k in range(args.warmup):
-            x, dt, Bm, C, z = sets[k % len(sets)]
-            fdec.step(x, dt, Bm, C, z, ci)
+
+        def full_fn(j):
+            x, dt, Bm, C, z = sets[j]
+            return lambda: fdec.step(x, dt, Bm, C, z, ci)
+
+        for k in range(max(args.warmup, 3)):
+            full_fn(k % G)()
         torch.cuda.synchronize()
+        g_full = _graphs([full_fn(j) for j in range(G)])
         Kf = max(50, K // 4)
-        f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        dist.barrier()
-        f0.record(stream)
-        for k in range(Kf):
-            x, dt, Bm, C, z = sets[k % len(sets)]
-            fdec.step(x, dt, Bm, C, z, ci)
-        f1.record(stream)
-        torch.cuda.synchronize()
-        f_ms = dist.max(f0.elapsed_time(f1)) / Kf
+        f_el, f_per, _ = _timed_graphs(None, g_full, Kf, dist, dev, clocks=False)
+        del g_full
+        f_ms = f_el / Kf
         fb = full_state_bytes(wl, wl.batch)
         full = {"ms_per_step": f_ms, "us_per_step": f_ms * 1e3,
                 "rows_per_s": dist.world * wl.batch / (f_ms * 1e-3),
-                "achieved_gbs": fb / (f_ms * 1e-3) / 1e9, "bytes_per_step": fb,
+                "achieved_gbs": fb / (float(np.mean(f_per)) * 1e-3) / 1e9, "bytes_per_step": fb,
+                "hbm_frac": fb / (float(np.mean(f_per)) * 1e-3) / 1e9 / peak,
                 "replay_speedup": f_ms / ms_step}
 
     cpu = None
@@ -435,6 +589,7 @@ def run_ours(args, dist):
                    "dstate": wl.dstate, "ngroups": wl.ngroups, "ring_len": wl.L,
                    "state_dtype": "bf16", "act_dtype": "bf16", "out_dtype": "bf16",
                    "parallelism": "independent replica per gpu (dp%d)" % dist.world,
+                   "timing": "CUDA graphs: advance+append+precompute | output, events between",
                    "l2": "inputs larger than L2: 1.07 GB of checkpoint tiles streamed per step"},
         "achieved_hbm_gbs": step_b / (ms_step * 1e-3) / 1e9,
         "hbm_frac_step": step_b / (ms_step * 1e-3) / 1e9 / peak,
@@ -452,12 +607,341 @@ def run_ours(args, dist):
     return line
 
 
+# --------------------------------------------------------------------------- #
+# gated delta net: decode                                                     #
+# --------------------------------------------------------------------------- #
+
+GDN_WORKLOAD = ("gdn replayssm decode: batch 256, HV 32, HK 16, K=V 128, L 16, fp32 state pool "
+                "512 slots ~N(0,0.05), bf16 q/k/v, fp32 beta/g")
+
+
+def run_gdn(args, dist, sub=False):
+    import torch
+
+    import rssm_workloads as W
+    import ssm_linear_attention_gb300 as ssm
+
+    dev = _device(dist)
+    ssm.lib()
+    kw = {}
+    if not sub and args.batch:
+        kw["batch"] = args.batch
+    if not sub and args.num_slots:
+        kw["num_slots"] = args.num_slots
+    wl = W.gdn_decode(seed=shard_seed(args.seed, dist.rank), **kw)
+    bf = torch.bfloat16
+    ci_np = wl.cache_indices()
+    ci = torch.from_numpy(ci_np).to(dev)
+    dec = ssm.GDNReplayDecoder(wl.num_v_heads, wl.num_k_heads, wl.head_k_dim, wl.head_v_dim, wl.L,
+                               wl.num_slots, wl.batch, act_dtype=bf, out_dtype=bf, device=dev)
+    for s in ci_np:
+        dec.state[int(s)] = torch.from_numpy(wl.slot_state(int(s))).to(dev)
+
+    def to_dev(inp):
+        return [torch.from_numpy(inp[k]).to(dev, bf if k in ("q", "k", "v") else torch.float32)
+                for k in ("q", "k", "v", "beta", "g")]
+
+    for j in range(wl.max_history()):
+        dec.step(*to_dev(wl.history_inputs(j)), torch.from_numpy(wl.history_ci(j)).to(dev))
+    nsets = min(args.input_sets, 32)
+    sets = [to_dev(wl.step_inputs(t)) for t in range(nsets)]
+    torch.cuda.synchronize()
+    K = args.steps
+    G = min(len(sets), max(K, 1))
+
+    def pre_fn(j):
+        q, k, v, beta, g = sets[j]
+
+        def f():
+            dec.advance(ci)
+            dec.append(k, g, ci)
+            dec.precompute(q, k, beta, g, ci)
+        return f
+
+    def out_fn(j):
+        q, k, v, beta, g = sets[j]
+        return lambda: dec.output(q, v, ci)
+
+    for k in range(max(args.warmup, 3)):
+        pre_fn(k % G)()
+        out_fn(k % G)()
+    torch.cuda.synchronize()
+    g_pre = _graphs([pre_fn(j) for j in range(G)])
+    g_out = _graphs([out_fn(j) for j in range(G)])
+    for k in range(max(args.warmup, 3)):
+        g_pre[k % G].replay()
+        g_out[k % G].replay()
+    torch.cuda.synchronize()
+    slot_wp0 = dec.slot_wp.cpu().numpy().astype(np.int64)
+    elapsed, out_ms, clocks = _timed_graphs(g_pre, g_out, K, dist, dev, offset=args.warmup,
+                                            clocks=not sub)
+    assert int(dec.dev_err.abs().sum().item()) == 0, "device error flag set during the gdn bench"
+    del g_pre, g_out
+    ms_step = elapsed / K
+    rows_s = dist.world * wl.batch / (ms_step * 1e-3)
+    curs = simulate_cursors(slot_wp0, ci_np, wl.L, K)
+    out_b = np.mean([gdn_output_bytes(wl, w, f) for w, f in curs])
+    out_avg_ms = float(np.mean(out_ms))
+    peak, peak_kind = read_peaks()
+    achieved = out_b / (out_avg_ms * 1e-3) / 1e9
+
+    full = None
+    if not args.no_full_state:
+        fdec = ssm.GDNFullStateDecoder(wl.num_v_heads, wl.num_k_heads, wl.head_k_dim,
+                                       wl.head_v_dim, wl.num_slots, wl.batch, act_dtype=bf,
+                                       out_dtype=bf, device=dev)
+        fdec.state.copy_(dec.state)
+        del dec
+
+        def full_fn(j):
+            q, k, v, beta, g = sets[j]
+            return lambda: fdec.step(q, k, v, beta, g, ci)
+
+        for k in range(max(args.warmup, 3)):
+            full_fn(k % G)()
+        torch.cuda.synchronize()
+        g_full = _graphs([full_fn(j) for j in range(G)])
+        Kf = max(50, K // 4)
+        f_el, f_per, _ = _timed_graphs(None, g_full, Kf, dist, dev, clocks=False)
+        del g_full
+        f_ms = f_el / Kf
+        fb = gdn_full_bytes(wl, wl.batch)
+        full = {"ms_per_step": f_ms, "us_per_step": f_ms * 1e3,
+                "rows_per_s": dist.world * wl.batch / (f_ms * 1e-3),
+                "achieved_gbs": fb / (float(np.mean(f_per)) * 1e-3) / 1e9, "bytes_per_step": fb,
+                "hbm_frac": fb / (float(np.mean(f_per)) * 1e-3) / 1e9 / peak,
+                "replay_speedup": f_ms / ms_step}
+
+    line = {
+        "metric": "gdn decode rows/s and µs/step at batch %d; achieved HBM GB/s" % wl.batch,
+        "value": rows_s, "unit": UNIT, "n_gpus": dist.world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms_step, "us_per_step": ms_step * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": GDN_WORKLOAD, "global_batch": dist.world * wl.batch,
+                   "batch_per_gpu": wl.batch, "HV": wl.num_v_heads, "HK": wl.num_k_heads,
+                   "K": wl.head_k_dim, "V": wl.head_v_dim, "ring_len": wl.L,
+                   "timing": "CUDA graphs: advance+append+precompute | output, events between",
+                   "l2": "inputs larger than L2: 537 MB of fp32 checkpoint tiles per step"},
+        "roofline": {"bound": "hbm", "kernel": "gdn output kernel (fp32 state, 32-row tiles)",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_source": peak_kind,
+                     "traffic": traffic_record("gdn.cu", "gdn_output_kernel_batch256.md"),
+                     "algorithmic_bytes_per_launch": int(out_b), "avg_launch_ms": out_avg_ms},
+        "full_state": full,
+        "gpu_launches": 4 * K,
+        "clocks": clocks,
+    }
+    if not sub and dist.rank == 0 and dist.world == 1 and not args.no_cpu:
+        rate, nth, sample = cpu_oracle_rate_gdn(wl, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": nth, "kind": "oracle",
+                                "sample": sample}
+    return line
+
+
+# --------------------------------------------------------------------------- #
+# gated delta net: speculative verify                                         #
+# --------------------------------------------------------------------------- #
+
+SPEC_WORKLOAD = ("gdn replayssm spec verify: batch 128, T 4 drafts, HV 32, HK 16, K=V 128, L 16, "
+                 "fp32 state pool 256 slots, accepted ~U{0..4}")
+
+
+def run_spec(args, dist, sub=False):
+    import torch
+
+    import rssm_workloads as W
+    import ssm_linear_attention_gb300 as ssm
+
+    dev = _device(dist)
+    ssm.lib()
+    kw = {}
+    if not sub and args.batch:
+        kw["batch"] = args.batch
+    if not sub and args.num_slots:
+        kw["num_slots"] = args.num_slots
+    wl = W.gdn_spec(seed=shard_seed(args.seed, dist.rank), **kw)
+    bf = torch.bfloat16
+    T, L = wl.T, wl.L
+    ci_np = wl.cache_indices()
+    ci = torch.from_numpy(ci_np).to(dev)
+    ver = ssm.GDNSpecVerifier(wl.num_v_heads, wl.num_k_heads, wl.head_k_dim, wl.head_v_dim, L, T,
+                              wl.num_slots, wl.batch, act_dtype=bf, out_dtype=bf, device=dev)
+    for s in ci_np:
+        ver.state[int(s)] = torch.from_numpy(wl.slot_state(int(s))).to(dev)
+    nsets = min(args.input_sets, 32)
+    sets, accs = [], []
+    for r in range(nsets):
+        inp = wl.round_inputs(r)
+        sets.append([torch.from_numpy(inp[k]).to(dev, bf if k in ("q", "k", "v") else torch.float32)
+                     for k in ("q", "k", "v", "beta", "g")])
+        accs.append(wl.accepted(r))
+    acc_dev = [torch.from_numpy(a).to(dev) for a in accs]
+    torch.cuda.synchronize()
+    K = args.steps
+    G = min(nsets, max(K, 1))
+
+    def round_fn(j):
+        q, k, v, beta, g = sets[j]
+
+        def f():
+            ver.verify(q, k, v, beta, g, ci)
+            ver.commit(ci, acc_dev[j])
+        return f
+
+    W0 = max(args.warmup, 3)
+    for k in range(W0):
+        round_fn(k % G)()
+    torch.cuda.synchronize()
+    graphs = _graphs([round_fn(j) for j in range(G)])
+    for k in range(W0):
+        graphs[(W0 + k) % G].replay()
+    torch.cuda.synchronize()
+    offset = 2 * W0
+    elapsed, per, clocks = _timed_graphs(None, graphs, K, dist, dev, offset=offset,
+                                         clocks=not sub)
+    assert int(ver.dev_err.abs().sum().item()) == 0, "device error flag set during the spec bench"
+    del graphs
+    ms_round = elapsed / K
+    # byte count from the cursor sequence of all rounds run so far
+    seq = [accs[k % G] for k in range(offset + K)]
+    sim, cnt_end = simulate_spec(wl, ci_np, seq, L, T)
+    dev_cnt = ver.slot_cnt.cpu().numpy().astype(np.int64)
+    assert np.array_equal(dev_cnt[ci_np], cnt_end[ci_np]), "spec cursor bookkeeping disagrees"
+    vb, fb = [], []
+    for hist, fl, fold in sim[offset:]:
+        v_b, f_b = spec_round_bytes(wl, hist, fold)
+        vb.append(v_b)
+        fb.append(f_b)
+    round_b = float(np.mean(vb)) + float(np.mean(fb))
+    peak, peak_kind = read_peaks()
+    per_ms = float(np.mean(per))
+    line = {
+        "metric": "gdn spec verify rows/s and µs/round at batch %d, T %d" % (wl.batch, T),
+        "value": dist.world * wl.batch / (ms_round * 1e-3), "unit": UNIT,
+        "draft_tokens_per_s": dist.world * wl.batch * T / (ms_round * 1e-3),
+        "n_gpus": dist.world, "steps": K, "warmup": W0, "ms_per_step": ms_round,
+        "us_per_round": ms_round * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": SPEC_WORKLOAD, "global_batch": dist.world * wl.batch,
+                   "batch_per_gpu": wl.batch, "T": T, "ring_len": L,
+                   "timing": "one CUDA graph per round (fold, precompute, verify, commit)",
+                   "l2": "inputs larger than L2: 268 MB of fp32 checkpoint per round"},
+        "roofline": {"bound": "hbm", "kernel": "spec round (fold + precompute + verify + commit)",
+                     "achieved": round_b / (per_ms * 1e-3) / 1e9, "peak": peak, "unit": "GB/s",
+                     "frac": round_b / (per_ms * 1e-3) / 1e9 / peak, "peak_source": peak_kind,
+                     "traffic": None, "algorithmic_bytes_per_round": int(round_b),
+                     "verify_bytes": float(np.mean(vb)), "fold_bytes": float(np.mean(fb))},
+        "gpu_launches": 4 * K,
+        "clocks": clocks,
+    }
+    return line
+
+
+# --------------------------------------------------------------------------- #
+# Mamba2 sweep                                                                #
+# --------------------------------------------------------------------------- #
+
+SWEEP_BATCH = (1, 16, 64, 128, 256, 512, 1024)
+SWEEP_L = (1, 4, 8, 16)
+SWEEP_DT = ("fp32", "bf16")
+
+
+def run_sweep(args, dist):
+    """One JSON line per (batch, L, state dtype): the ReplaySSM step (one CUDA graph
+    per step) and the full-state kernel on an identical pool, with 5% of rows per
+    step force-flushed. Pools are filled on the device from a seeded generator."""
+    import torch
+
+    import rssm_workloads as W
+    import ssm_linear_attention_gb300 as ssm
+
+    dev = _device(dist)
+    ssm.lib()
+    peak, _ = read_peaks()
+    bf = torch.bfloat16
+    K = args.sweep_steps
+    for sdt in SWEEP_DT:
+        st = torch.float32 if sdt == "fp32" else bf
+        for L in SWEEP_L:
+            for batch in SWEEP_BATCH:
+                wl = W.mamba2_sweep(batch, L, sdt, seed=shard_seed(args.seed, dist.rank))
+                prm = wl.params()
+                ci_np = wl.cache_indices()
+                ci = torch.from_numpy(ci_np).to(dev)
+                dec = ssm.Mamba2ReplayDecoder(wl.nheads, wl.headdim, wl.dstate, wl.ngroups, L,
+                                              wl.num_slots, batch, prm["A"], prm["D"],
+                                              prm["dt_bias"], state_dtype=st, act_dtype=bf,
+                                              out_dtype=bf, device=dev)
+                gen = torch.Generator(device=dev)
+                gen.manual_seed(shard_seed(args.seed, dist.rank) + batch * 131 + L)
+                dec.state.normal_(0.0, 0.1, generator=gen)
+                nsets = 8
+                sets = []
+                for t in range(nsets):
+                    inp = wl.step_inputs(t)
+                    xs = [torch.from_numpy(inp[k]).to(dev, bf if k != "dt_raw" else torch.float32)
+                          for k in ("x", "dt_raw", "B", "C", "z")]
+                    fm = wl.force_mask(t)
+                    xs.append(None if fm is None else torch.from_numpy(fm).to(dev))
+                    sets.append(xs)
+                torch.cuda.synchronize()
+
+                def rep_fn(j):
+                    x, dt, Bm, C, z, fm = sets[j]
+                    return lambda: dec.step(x, dt, Bm, C, z, ci, force_flush=fm)
+
+                for k in range(3):
+                    rep_fn(k % nsets)()
+                g_rep = _graphs([rep_fn(j) for j in range(nsets)])
+                for k in range(3):
+                    g_rep[k].replay()
+                el, _, _ = _timed_graphs(None, g_rep, K, dist, dev, clocks=False)
+                assert int(dec.dev_err.abs().sum().item()) == 0
+                del g_rep
+                rep_ms = el / K
+                # bytes: flush rate from the step pattern (w == L-1 or forced)
+                fdec = ssm.Mamba2FullStateDecoder(wl.nheads, wl.headdim, wl.dstate, wl.ngroups,
+                                                  wl.num_slots, batch, prm["A"], prm["D"],
+                                                  prm["dt_bias"], state_dtype=st, act_dtype=bf,
+                                                  out_dtype=bf, device=dev)
+                fdec.state.copy_(dec.state)
+                del dec
+
+                def full_fn(j):
+                    x, dt, Bm, C, z, fm = sets[j]
+                    return lambda: fdec.step(x, dt, Bm, C, z, ci)
+
+                for k in range(3):
+                    full_fn(k % nsets)()
+                g_full = _graphs([full_fn(j) for j in range(nsets)])
+                for k in range(3):
+                    g_full[k].replay()
+                fel, _, _ = _timed_graphs(None, g_full, K, dist, dev, clocks=False)
+                del g_full, fdec
+                full_ms = fel / K
+                fb = full_state_bytes(wl, batch)
+                line = {"metric": "mamba2 sweep point", "workload": "sweep", "batch": batch,
+                        "ring_len": L, "state_dtype": sdt, "steps": K, "n_gpus": dist.world,
+                        "replay_us_per_step": rep_ms * 1e3,
+                        "replay_rows_per_s": dist.world * batch / (rep_ms * 1e-3),
+                        "full_state_us_per_step": full_ms * 1e3,
+                        "full_state_gbs": fb / (full_ms * 1e-3) / 1e9,
+                        "full_state_hbm_frac": fb / (full_ms * 1e-3) / 1e9 / peak,
+                        "replay_speedup": full_ms / rep_ms,
+                        "timing": "one CUDA graph per step (4 launches); full state one graph"}
+                if dist.rank == 0:
+                    print(json.dumps(line), flush=True)
+                del sets
+                torch.cuda.empty_cache()
+    return None
+
+
 def run_reference(args, dist):
     """The oracle arm: the float64 CPU recurrence on this host's cores; each step a
     bounded sample of the workload's rows."""
     import rssm_workloads as W
     import oracle
-    wl = W.mamba2_large(batch=args.batch, seed=args.seed)
+    wl = W.mamba2_large(batch=args.batch or 512, seed=args.seed)
     prm = wl.params()
     rows = np.arange(16)
     ci = wl.cache_indices()
@@ -508,9 +992,18 @@ def main():
             if args.steps > 50:
                 args.steps = 50
             line = run_reference(args, dist)
+        elif args.workload == "gdn":
+            line = run_gdn(args, dist)
+        elif args.workload == "spec":
+            line = run_spec(args, dist)
+        elif args.workload == "sweep":
+            line = run_sweep(args, dist)
         else:
-            line = run_ours(args, dist)
-        if dist.rank == 0:
+            line = run_mamba2(args, dist)
+            if not args.no_gdn:
+                line["gdn_decode"] = run_gdn(args, dist, sub=True)
+                line["gdn_spec"] = run_spec(args, dist, sub=True)
+        if dist.rank == 0 and line is not None:
             print(json.dumps(line), flush=True)
     finally:
         dist.close()

@@ -271,7 +271,7 @@ typedef struct rssm_gdn_dims {
     int32_t num_v_heads; /* HV */
     int32_t num_k_heads; /* HK: HV % HK == 0; value head hv reads key head hv / (HV/HK) */
     int32_t head_k_dim;  /* K: 128 */
-    int32_t head_v_dim;  /* V: multiple of 64 */
+    int32_t head_v_dim;  /* V: multiple of 32 */
     int32_t ring_len;    /* L >= 1 */
     int32_t num_slots;
     int32_t act_dtype;   /* RSSM_F32 | RSSM_BF16: q, k, v, ring_k, ring_v */
@@ -281,7 +281,8 @@ typedef struct rssm_gdn_dims {
 /* Layouts (row-major, dense); the state is float32 ([SPEC] 风险与影响: the
  * ReplaySSM path keeps an fp32 checkpoint):
  *   state   [num_slots][HV][V][K] float32  checkpoint S0 per slot
- *   ring_d  [num_slots][HV][L][V] float32  d_i = beta_i (v_i - g_i S_{i-1} k_i)
+ *   ring_d  [num_slots][HV][V/32][L][32] float32  d_i = beta_i (v_i - g_i S_{i-1} k_i),
+ *           value rows in blocks of 32 (one block's L entries are contiguous)
  *   ring_k  [num_slots][HK][L][K] act_dtype
  *   ring_g  [num_slots][HV][L]    float32  gate value g_i in (0, 1]
  *   q, k    [batch][HK][K] act_dtype; v [batch][HV][V] act_dtype

@@ -19,10 +19,12 @@
 // with gamma_i = prod_{j=i+1..w-1} g_j, Gamma_i = g_t gamma_i (Gamma_w = 1),
 // Gu = prod_{j<w} g_j, Go = g_t Gu.
 //
-// Work item of the output kernel = (row, value head, block of 64 value rows): a
-// 32 KB fp32 tile of S0. Each warp owns 16 value rows; a lane holds 4 key columns
-// of a row (16-byte shared loads), so the two dot products per row reduce across
-// the warp with one 32-way reduce-scatter.
+// Work item of the output kernel = (row, value head, block of 32 value rows): a
+// 16 KB fp32 tile of S0, read by a group of two consumer warps. Each warp owns 16
+// value rows; a lane holds 4 key columns of a row (16-byte shared loads), so the
+// two dot products per row reduce across the warp with one 32-way reduce-scatter.
+// The d ring is stored in blocks of 32 value rows, so a block's history entries
+// arrive with one bulk copy.
 #include "common.cuh"
 #include "internal.h"
 #include "pipeline.cuh"
@@ -31,7 +33,7 @@ namespace rssm {
 namespace gdn {
 
 constexpr int KD = 128;  // key dim handled by these kernels
-constexpr int VB = 64;   // value rows per work item
+constexpr int VB = 32;   // value rows per work item (a 16 KB fp32 tile)
 constexpr int TILE = VB * KD * 4;
 
 __host__ __device__ inline int tbl_floats(int L) { return (3 * L + 5 + 3) & ~3; }
@@ -103,11 +105,13 @@ __global__ void __launch_bounds__(256) precompute_kernel(
     float* kq = kk + HK * L;      // [HK][L]
     float* kqt = kq + HK * L;     // [HK]
     float* tbl = psm + ((2 * HK * KD + 2 * HK * L + HK + 3) & ~3);  // [HV][TBL]
+    float* gs = tbl + HV * TBL;                                       // gate ring [HV][L]
 
     for (int e = threadIdx.x * 8; e < HK * KD; e += blockDim.x * 8) {
         load8(static_cast<const char*>(k) + ((size_t)b * HK * KD + e) * sa, act_bf16, kt + e);
         load8(static_cast<const char*>(q) + ((size_t)b * HK * KD + e) * sa, act_bf16, qt + e);
     }
+    for (int e = threadIdx.x; e < HV * L; e += blockDim.x) gs[e] = ring_g[(size_t)s * HV * L + e];
     __syncthreads();
 
     // one thread per (key head, entry i <= w): kk_i = k_i . k_t, kq_i = k_i . q_t
@@ -141,7 +145,7 @@ __global__ void __launch_bounds__(256) precompute_kernel(
         const int kh = hv / vpk;
         const float gt = g[(size_t)b * HV + hv];
         const float bt = beta[(size_t)b * HV + hv];
-        const float* gr = ring_g + ((size_t)s * HV + hv) * L;
+        const float* gr = gs + hv * L;
         float* t = tbl + hv * TBL;
         float gam = 1.f;  // prod_{j=i+1..w-1} g_j
         for (int i = w - 1; i >= 0; --i) {
@@ -173,7 +177,7 @@ __global__ void __launch_bounds__(256) precompute_kernel(
 // output / flush and full-state decode (warp-specialised pipeline)
 // ----------------------------------------------------------------------------
 //
-// A group of two consumer warps owns a (row, value head, 64-row block) tile, 32
+// A group of two consumer warps owns a (row, value head, 32-row block) tile, 16
 // value rows per warp; lane l holds key columns 4l..4l+3 of every row, so one
 // 16-byte shared load per lane reads one value row. The two dot products per row
 // (with k_t and q_t) of 16 rows reduce with one 32-way reduce-scatter; lanes 0..15
@@ -251,8 +255,10 @@ struct OutPolicy {
         bulk_g2s(sb + a.off_v,
                  static_cast<const char*>(a.v) + (((size_t)b * a.HV + hv) * a.V + (size_t)vb * VB) * sa,
                  VB * sa, full);
-        const float* dr = a.ring_d + (((size_t)m.s * a.HV + hv) * L) * a.V + (size_t)vb * VB;
-        for (int i = 0; i < w; ++i) bulk_g2s(sb + a.off_d + i * VB * 4, dr + (size_t)i * a.V, VB * 4, full);
+        // ring d is blocked by 32 value rows: the block's entries 0..w-1 are contiguous
+        if (w > 0)
+            bulk_g2s(sb + a.off_d, a.ring_d + ((((size_t)m.s * a.HV + hv) * NVB + vb) * L) * VB,
+                     w * VB * 4, full);
         bulk_g2s(sb + a.off_tbl, a.ws + ((size_t)b * a.HV + hv) * TBL, TBL * 4, full);
     }
 
@@ -305,7 +311,7 @@ struct OutPolicy {
                 oo = fmaf(kqt, dn, oo);
                 const size_t vi = (size_t)m.vb * VB + r;
                 store1(a.o, ((size_t)m.b * a.HV + m.hv) * a.V + vi, a.out_bf16, oo);
-                a.ring_d[(((size_t)m.s * a.HV + m.hv) * L + w) * a.V + vi] = dn;
+                a.ring_d[((((size_t)m.s * a.HV + m.hv) * (a.V / VB) + m.vb) * L + w) * VB + r] = dn;
                 dtv[ch] = dn;
             }
         }
@@ -510,8 +516,8 @@ extern "C" int rssm_gdn_precompute(const rssm_gdn_dims* d, const void* q, const 
         return RSSM_ERR_INVALID_ARG;
     if (workspace_bytes < rssm_gdn_workspace_size(d)) return RSSM_ERR_INVALID_ARG;
     const int L = d->ring_len, HK = d->num_k_heads;
-    const int smem =
-        (((2 * HK * gdn::KD + 2 * HK * L + HK + 3) & ~3) + d->num_v_heads * gdn::tbl_floats(L)) * 4;
+    const int smem = (((2 * HK * gdn::KD + 2 * HK * L + HK + 3) & ~3) +
+                      d->num_v_heads * gdn::tbl_floats(L) + d->num_v_heads * L) * 4;
     DeviceInfo di;
     if (!device_info(&di)) return RSSM_ERR_CUDA;
     if (smem > di.max_smem_optin) return RSSM_ERR_UNSUPPORTED;

@@ -12,14 +12,15 @@
 // drafts).
 //
 // Launches of one verify round:
-//   fold_kernel        one CTA per (row, value head, 64-row block) of a slot with
-//                      a pending fold: S0 rows in registers, cnt sequential
-//                      delta-rule updates from ring k, raw v, beta, g; S0 stored.
-//   spec_pre_kernel    one CTA per row: dot products of every live key (history
-//                      and drafts) with the drafts' keys and queries, products of
-//                      gates, into a per-(row, value head) table; writes the
-//                      drafts' k, g, beta into the ring.
-//   verify_kernel<DP>  persistent TMA pipeline over (row, value head, 64-row
+//   fold_kernel        one CTA per (row, value head, 32-row block) of a slot with
+//                      a pending fold: S0 rows in registers, the committed entries
+//                      staged in shared memory, cnt sequential delta-rule updates
+//                      from ring k, raw v, beta, g; S0 stored.
+//   spec_pre_kernel    one CTA per (row, key head): dot products of every live key
+//                      (history and drafts) with the drafts' keys and queries,
+//                      products of gates, into a per-(row, value head) table;
+//                      writes the drafts' k, g, beta into the ring.
+//   verify_kernel<DP>  persistent TMA pipeline over (row, value head, 32-row
 //                      block) tiles of S0: the 2T dot products per value row,
 //                      then the draft chain per row; writes o, and d and raw v
 //                      of the drafts into the ring.
@@ -34,7 +35,7 @@ namespace spec {
 
 constexpr int kThreads = 128;
 constexpr int KD = 128;
-constexpr int VB = 64;
+constexpr int VB = 32;  // value rows per work item (a 16 KB fp32 tile)
 constexpr int TILE = VB * KD * 4;
 constexpr int kMaxT = 8;
 
@@ -84,7 +85,18 @@ struct FoldArgs {
     int HV, HK, V, L, num_slots, act_bf16;
 };
 
+// One CTA (4 warps) per (row, value head, VB-row block) of a slot with a pending
+// fold. Warp w owns rows w + 4j (j < VB/4) of the block; a lane holds key columns
+// 4l..4l+3 of each, so the block's S0 rows sit in registers. The committed
+// entries (k, raw v, beta, g) are staged in shared memory, 16 at a time, then
+// replayed in order: u = S k (one reduce-scatter), d = beta (v - g u),
+// S = g S + d k^T.
+constexpr int kFoldRows = VB / 4;  // rows per warp
+
 __global__ void __launch_bounds__(kThreads) fold_kernel(const FoldArgs a) {
+    __shared__ __align__(16) float ks[16 * KD];  // k of up to 16 entries
+    __shared__ float vs[16 * VB];                // raw v of the block's rows
+    __shared__ float bs[16], gs[16];
     const int NVB = a.V / VB;
     const int item = blockIdx.x;
     const int b = item / (a.HV * NVB);
@@ -97,41 +109,56 @@ __global__ void __launch_bounds__(kThreads) fold_kernel(const FoldArgs a) {
     if (cnt <= 0 || cnt > a.L || base < 0 || base >= a.L) return;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int kh = hv / (a.HV / a.HK);
-    const int sa = a.act_bf16 ? 2 : 4;
     float* tile = a.state + (((size_t)s * a.HV + hv) * a.V + (size_t)vb * VB) * KD;
-    float S[16][4];
+    float S[kFoldRows][4];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
+    for (int j = 0; j < kFoldRows; ++j) {
         const float4 v4 = *reinterpret_cast<const float4*>(tile + (warp + 4 * j) * KD + lane * 4);
         S[j][0] = v4.x; S[j][1] = v4.y; S[j][2] = v4.z; S[j][3] = v4.w;
     }
-    for (int e = 0; e < cnt; ++e) {
-        const int pos = (base + e) % a.L;
-        float k4[4];
-        load4(static_cast<const char*>(a.ring_k) + (((size_t)s * a.HK + kh) * a.L + pos) * KD * sa,
-              lane * 4, a.act_bf16, k4);
-        const float be = a.ring_beta[((size_t)s * a.HV + hv) * a.L + pos];
-        const float ge = a.ring_g[((size_t)s * a.HV + hv) * a.L + pos];
-        // this lane's value row for the broadcast below: rows warp + 4*(lane>>1)
-        const float vown = load1(a.ring_v, (((size_t)s * a.HV + hv) * a.L + pos) * a.V +
-                                               (size_t)vb * VB + warp + 4 * ((lane >> 1) & 15),
-                                 a.act_bf16);
-        float part[16];
+    constexpr int SH = 32 / kFoldRows;  // lanes holding the same row after the reduce
+    for (int e0 = 0; e0 < cnt; e0 += 16) {  // entries in chunks of 16, in order
+        const int ne = cnt - e0 < 16 ? cnt - e0 : 16;
+        __syncthreads();  // the previous chunk is no longer read
+        for (int e = threadIdx.x; e < ne * KD; e += blockDim.x) {
+            const int i = e / KD, c = e - (e / KD) * KD;
+            const int pos = (base + e0 + i) % a.L;
+            ks[e] = load1(a.ring_k, (((size_t)s * a.HK + kh) * a.L + pos) * KD + c, a.act_bf16);
+        }
+        for (int e = threadIdx.x; e < ne * VB; e += blockDim.x) {
+            const int i = e / VB, r = e - (e / VB) * VB;
+            const int pos = (base + e0 + i) % a.L;
+            vs[e] = load1(a.ring_v, (((size_t)s * a.HV + hv) * a.L + pos) * a.V + (size_t)vb * VB + r,
+                          a.act_bf16);
+        }
+        if (threadIdx.x < ne) {
+            const int pos = (base + e0 + threadIdx.x) % a.L;
+            bs[threadIdx.x] = a.ring_beta[((size_t)s * a.HV + hv) * a.L + pos];
+            gs[threadIdx.x] = a.ring_g[((size_t)s * a.HV + hv) * a.L + pos];
+        }
+        __syncthreads();
+        for (int e = 0; e < ne; ++e) {
+            const float4 k4 = *reinterpret_cast<const float4*>(ks + e * KD + lane * 4);
+            const float be = bs[e], ge = gs[e];
+            float part[kFoldRows];
 #pragma unroll
-        for (int j = 0; j < 16; ++j)
-            part[j] = S[j][0] * k4[0] + S[j][1] * k4[1] + S[j][2] * k4[2] + S[j][3] * k4[3];
-        const int idx = reduce_scatter<16, 32>(part);  // lanes 2i, 2i+1 hold row i's sum
-        const float dmine = be * (vown - ge * part[0]);
-        (void)idx;
+            for (int j = 0; j < kFoldRows; ++j)
+                part[j] = S[j][0] * k4.x + S[j][1] * k4.y + S[j][2] * k4.z + S[j][3] * k4.w;
+            reduce_scatter<kFoldRows, 32>(part);  // lanes SH*i .. SH*i+SH-1 hold row i's sum
+            const int jr = lane / SH;
+            const float dmine = be * (vs[e * VB + warp + 4 * jr] - ge * part[0]);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const float dj = __shfl_sync(0xffffffffu, dmine, 2 * j);
-#pragma unroll
-            for (int c = 0; c < 4; ++c) S[j][c] = fmaf(ge, S[j][c], dj * k4[c]);
+            for (int j = 0; j < kFoldRows; ++j) {
+                const float dj = __shfl_sync(0xffffffffu, dmine, SH * j);
+                S[j][0] = fmaf(ge, S[j][0], dj * k4.x);
+                S[j][1] = fmaf(ge, S[j][1], dj * k4.y);
+                S[j][2] = fmaf(ge, S[j][2], dj * k4.z);
+                S[j][3] = fmaf(ge, S[j][3], dj * k4.w);
+            }
         }
     }
 #pragma unroll
-    for (int j = 0; j < 16; ++j)
+    for (int j = 0; j < kFoldRows; ++j)
         *reinterpret_cast<float4*>(tile + (warp + 4 * j) * KD + lane * 4) =
             make_float4(S[j][0], S[j][1], S[j][2], S[j][3]);
 }
@@ -157,83 +184,94 @@ struct PreArgs {
     int T, HV, HK, L, num_slots, act_bf16;
 };
 
+// One CTA per (row, key head): the dot products of every live key (history, then
+// drafts) with the drafts' keys and queries, the coefficient tables of the value
+// heads that read this key head, and the drafts' ring entries k (this key head),
+// g and beta (its value heads).
 __global__ void spec_pre_kernel(const PreArgs a) {
     extern __shared__ __align__(16) float psm[];
-    const int b = blockIdx.x;
+    const int b = blockIdx.x / a.HK, kh = blockIdx.x - (blockIdx.x / a.HK) * a.HK;
     const int s = a.ci[b];
     if (s < 0 || s >= a.num_slots) return;
     const int T = a.T, L = a.L, HV = a.HV, HK = a.HK;
     int c, base_eff;
     if (!history(a.slot_wp[s], a.slot_base[s], a.slot_flush[s], L, T, &c, &base_eff)) return;
-    const int nk = c + T;                 // live keys: history then drafts
-    float* KK = psm;                      // [HK][L][T]   k_i . k_j
-    float* KQ = KK + HK * L * T;          // [HK][L][T]   k_i . q_j
+    const int nk = c + T;       // live keys: history then drafts
+    const int vpk = HV / HK;
+    float* KK = psm;            // [L][T]   k_i . k_j
+    float* KQ = KK + L * T;     // [L][T]   k_i . q_j
+    float* gts = KQ + L * T;    // [vpk][L] gate of every live entry (history, drafts)
     const int sa = a.act_bf16 ? 2 : 4;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
     const char* kin = static_cast<const char*>(a.k);
     const char* qin = static_cast<const char*>(a.q);
 
-    // one warp per (key head, key): 2T dot products against the drafts
-    for (int task = warp; task < HK * nk; task += nwarps) {
-        const int kh = task / nk, i = task - (task / nk) * nk;
+    // the drafts' keys and queries, 4 columns per lane, held in registers
+    float kd[kMaxT][4], qd[kMaxT][4];
+#pragma unroll
+    for (int j = 0; j < kMaxT; ++j) {
+        if (j < T) {
+            load4(kin + (((size_t)b * T + j) * HK + kh) * KD * sa, lane * 4, a.act_bf16, kd[j]);
+            load4(qin + (((size_t)b * T + j) * HK + kh) * KD * sa, lane * 4, a.act_bf16, qd[j]);
+        }
+    }
+    for (int i = warp; i < nk; i += nwarps) {
         float ki[4];
         if (i < c) {
             const int pos = (base_eff + i) % L;
             load4(static_cast<const char*>(a.ring_k) + (((size_t)s * HK + kh) * L + pos) * KD * sa,
                   lane * 4, a.act_bf16, ki);
         } else {
-            load4(kin + (((size_t)b * T + (i - c)) * HK + kh) * KD * sa, lane * 4, a.act_bf16, ki);
+            ki[0] = kd[0][0]; ki[1] = kd[0][1]; ki[2] = kd[0][2]; ki[3] = kd[0][3];
+#pragma unroll
+            for (int j = 1; j < kMaxT; ++j)
+                if (j == i - c) { ki[0] = kd[j][0]; ki[1] = kd[j][1]; ki[2] = kd[j][2]; ki[3] = kd[j][3]; }
         }
-        for (int j = 0; j < T; ++j) {
-            float kj[4], qj[4];
-            load4(kin + (((size_t)b * T + j) * HK + kh) * KD * sa, lane * 4, a.act_bf16, kj);
-            load4(qin + (((size_t)b * T + j) * HK + kh) * KD * sa, lane * 4, a.act_bf16, qj);
-            float d1 = 0.f, d2 = 0.f;
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                d1 = fmaf(ki[e], kj[e], d1);
-                d2 = fmaf(ki[e], qj[e], d2);
-            }
+        for (int j = 0; j < kMaxT; ++j) {
+            if (j < T) {
+                float d1 = ki[0] * kd[j][0] + ki[1] * kd[j][1] + ki[2] * kd[j][2] + ki[3] * kd[j][3];
+                float d2 = ki[0] * qd[j][0] + ki[1] * qd[j][1] + ki[2] * qd[j][2] + ki[3] * qd[j][3];
 #pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) {
-                d1 += __shfl_xor_sync(0xffffffffu, d1, o);
-                d2 += __shfl_xor_sync(0xffffffffu, d2, o);
-            }
-            if (lane == 0) {
-                KK[(kh * L + i) * T + j] = d1;
-                KQ[(kh * L + i) * T + j] = d2;
+                for (int o = 16; o >= 1; o >>= 1) {
+                    d1 += __shfl_xor_sync(0xffffffffu, d1, o);
+                    d2 += __shfl_xor_sync(0xffffffffu, d2, o);
+                }
+                if (lane == 0) {
+                    KK[i * T + j] = d1;
+                    KQ[i * T + j] = d2;
+                }
             }
         }
     }
-    // the drafts' S-independent ring entries: k (per key head), g and beta (per value head)
+    // gates of the live entries of this key head's value heads, staged once
+    for (int x = threadIdx.x; x < vpk * nk; x += blockDim.x) {
+        const int hl = x / nk, m = x - (x / nk) * nk, hv = kh * vpk + hl;
+        gts[hl * L + m] = m < c ? a.ring_g[((size_t)s * HV + hv) * L + (base_eff + m) % L]
+                                : a.g[((size_t)b * T + (m - c)) * HV + hv];
+    }
+    // the drafts' S-independent ring entries
     const int kc = KD * sa / 16;
-    for (int x = threadIdx.x; x < T * HK * kc; x += blockDim.x) {
-        const int j = x / (HK * kc), r = x - j * HK * kc;
-        const int kh = r / kc, part = r - kh * kc;
+    for (int x = threadIdx.x; x < T * kc; x += blockDim.x) {
+        const int j = x / kc, part = x - (x / kc) * kc;
         const int pos = (base_eff + c + j) % L;
-        reinterpret_cast<uint4*>(static_cast<char*>(a.ring_k) +
-                                 (((size_t)s * HK + kh) * L + pos) * KD * sa)[part] =
+        reinterpret_cast<uint4*>(static_cast<char*>(a.ring_k) + (((size_t)s * HK + kh) * L + pos) * KD * sa)[part] =
             reinterpret_cast<const uint4*>(kin + (((size_t)b * T + j) * HK + kh) * KD * sa)[part];
     }
-    for (int x = threadIdx.x; x < T * HV; x += blockDim.x) {
-        const int j = x / HV, hv = x - j * HV;
+    for (int x = threadIdx.x; x < T * vpk; x += blockDim.x) {
+        const int j = x / vpk, hv = kh * vpk + (x - (x / vpk) * vpk);
         const int pos = (base_eff + c + j) % L;
         a.ring_g[((size_t)s * HV + hv) * L + pos] = a.g[((size_t)b * T + j) * HV + hv];
         a.ring_beta[((size_t)s * HV + hv) * L + pos] = a.beta[((size_t)b * T + j) * HV + hv];
     }
     __syncthreads();
 
-    // coefficient table per (value head, draft)
+    // coefficient table per (value head of this key head, draft)
     const int TB = tbl_floats(L, T);
-    const int vpk = HV / HK;
-    for (int x = threadIdx.x; x < HV * T; x += blockDim.x) {
-        const int hv = x / T, j = x - (x / T) * T;
-        const int kh = hv / vpk;
+    for (int x = threadIdx.x; x < vpk * T; x += blockDim.x) {
+        const int hl = x / T, j = x - (x / T) * T, hv = kh * vpk + hl;
         float* t = a.ws + ((size_t)b * HV + hv) * TB;
-        const float* gr = a.ring_g + ((size_t)s * HV + hv) * L;
-        auto gate = [&](int m) -> float {
-            return m < c ? gr[(base_eff + m) % L] : a.g[((size_t)b * T + (m - c)) * HV + hv];
-        };
+        const float* gl = gts + hl * L;
         const int m = c + j;
         float* au = t + j * L;
         float* ao = t + T * L + j * L;
@@ -241,12 +279,12 @@ __global__ void spec_pre_kernel(const PreArgs a) {
         // au_i = prod_{l=i+1..m-1} gate_l * (k_i . k_j), i < m
         float pq = 1.f, pk = 1.f;
         for (int i = m; i >= 0; --i) {
-            ao[i] = pq * KQ[(kh * L + i) * T + j];
+            ao[i] = pq * KQ[i * T + j];
             if (i < m) {
-                au[i] = pk * KK[(kh * L + i) * T + j];
-                pk *= gate(i);
+                au[i] = pk * KK[i * T + j];
+                pk *= gl[i];
             }
-            pq *= gate(i);
+            pq *= gl[i];
         }
         for (int i = m + 1; i < L; ++i) {
             ao[i] = 0.f;
@@ -346,9 +384,11 @@ struct VerPolicy {
                          ((((size_t)b * T + j) * a.HV + hv) * a.V + (size_t)vb * VB) * sa,
                      VB * sa, full);
         }
-        const float* dr = a.ring_d + ((size_t)m.s * a.HV + hv) * L * a.V + (size_t)vb * VB;
-        for (int i = 0; i < m.c; ++i)
-            bulk_g2s(sb + a.off_d + i * VB * 4, dr + (size_t)((m.base_eff + i) % L) * a.V, VB * 4, full);
+        // ring d is blocked by 32 value rows; the history entries are at most two runs
+        const float* dr = a.ring_d + (((size_t)m.s * a.HV + hv) * NVB + vb) * L * VB;
+        const int run1 = m.base_eff + m.c <= L ? m.c : L - m.base_eff;
+        if (run1 > 0) bulk_g2s(sb + a.off_d, dr + (size_t)m.base_eff * VB, run1 * VB * 4, full);
+        if (m.c > run1) bulk_g2s(sb + a.off_d + run1 * VB * 4, dr, (m.c - run1) * VB * 4, full);
         bulk_g2s(sb + a.off_tbl, a.ws + ((size_t)b * a.HV + hv) * TB, TB * 4, full);
     }
 
@@ -396,7 +436,7 @@ struct VerPolicy {
         const float* dh = reinterpret_cast<const float*>(sb + a.off_d);
         const int r = rbase + lane;
         const size_t vi = (size_t)m.vb * VB + r;
-        for (int j = 0; j < T; ++j) {
+        for (int j = 0; j < T && lane < RW; ++j) {
             const float* au = t + j * L;
             const float* ao = t + T * L + j * L;
             const int mm = c + j;
@@ -418,7 +458,7 @@ struct VerPolicy {
             oo = fmaf(ao[mm], dn, oo);
             const int pos = (m.base_eff + c + j) % L;
             store1(a.o, (((size_t)m.b * T + j) * a.HV + m.hv) * a.V + vi, a.out_bf16, oo);
-            a.ring_d[(((size_t)m.s * a.HV + m.hv) * L + pos) * a.V + vi] = dn;
+            a.ring_d[((((size_t)m.s * a.HV + m.hv) * (a.V / VB) + m.vb) * L + pos) * VB + r] = dn;
             store1(a.ring_v, (((size_t)m.s * a.HV + m.hv) * L + pos) * a.V + vi, bf, vr);
         }
         __syncwarp();
@@ -474,7 +514,7 @@ extern "C" int rssm_gdn_spec_verify(const rssm_gdn_dims* d, int32_t T, float* st
     if (launch_status()) return RSSM_ERR_CUDA;
 
     // 2. precompute: key dots, gate products, S-independent ring entries
-    const int psmem = 2 * HK * L * T * 4;
+    const int psmem = (2 * L * T + (HV / HK) * L) * 4;
     if (psmem > di.max_smem_optin) return RSSM_ERR_UNSUPPORTED;
     if (psmem > 48 * 1024 &&
         !ensure_smem_limit(reinterpret_cast<const void*>(spec::spec_pre_kernel), psmem))
@@ -482,7 +522,7 @@ extern "C" int rssm_gdn_spec_verify(const rssm_gdn_dims* d, int32_t T, float* st
     spec::PreArgs pa{q, k, beta, g, ring_k, ring_g, ring_beta, cache_indices, slot_wp, slot_base,
                      slot_flush, static_cast<float*>(workspace), dev_err, T, HV, HK, L,
                      d->num_slots, abf};
-    spec::spec_pre_kernel<<<d->batch, 256, psmem, st>>>(pa);
+    spec::spec_pre_kernel<<<d->batch * HK, 128, psmem, st>>>(pa);
     if (launch_status()) return RSSM_ERR_CUDA;
 
     // 3. verify

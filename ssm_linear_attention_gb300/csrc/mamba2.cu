@@ -12,16 +12,19 @@
 // Kernels:
 //   ring_append_kernel    one CTA per row: x, dt = softplus(dt_raw + dt_bias), B
 //                         into ring entry w.
-//   precompute_kernel     one CTA per row: B_i . C_t per group, decay suffix
+//   precompute_kernel     one CTA per row: B_i . C_t per group (runs staged in
+//                         shared memory), decay suffix
 //                         products per head, written as per-(row, head) tables.
 //   output_kernel<P,N,ST> persistent, one work item = one (row, head) checkpoint
-//                         tile. A single thread feeds a multi-stage ring of shared
-//                         memory buffers with 1-D TMA bulk copies (tile, ring x
-//                         entries, C, z, table, and on flush rows the ring B
-//                         entries) completing on one mbarrier per stage; 128
-//                         threads reduce the tile against C with 16-byte shared
-//                         loads and a warp reduce-scatter, and flush rows fold the
-//                         ring into the tile in registers and store it.
+//                         tile. Per CTA several independent pipelines, each a
+//                         producer warp feeding its own ring of shared-memory
+//                         stages with 1-D TMA bulk copies (tile, ring x entries,
+//                         C, z, table, and on flush rows the ring B entries)
+//                         that complete on one mbarrier per stage, and a group of
+//                         two consumer warps that reduce the tile against C with
+//                         16-byte shared loads and warp reduce-scatters; flush
+//                         rows fold the ring into the tile in registers and
+//                         store it.
 //   full_state_kernel<P,N,ST>  the conventional step (read tile, update, write
 //                         tile, output) on the same pipeline.
 #include <cstdio>
@@ -98,44 +101,51 @@ __global__ void __launch_bounds__(256) precompute_kernel(
     if (w < 0 || w >= L) return;
     const int TBL = tbl_floats(L);
     const int sa = act_bf16 ? 2 : 4;
-    float* cs = psm;                              // [G][N] C_t in fp32
-    float* bc = cs + G * N;                       // [G][L]
-    float* tbl = psm + ((G * N + G * L + 3) & ~3);  // [H][TBL]
+    const int hpg = H / G;
+    float* cs = psm;                                         // [G][N] C_t in fp32
+    float* dts = cs + G * N;                                 // [H][L] dt of entries 0..w
+    float* bc = dts + H * L;                                 // [G][L] B_i . C_t
+    float* tbl = psm + ((G * N + H * L + G * L + 3) & ~3);   // [H][TBL]
+    char* braw = reinterpret_cast<char*>(tbl + H * TBL);     // [G][w+1][N] raw B entries
 
+    // stage C_t, the dt run and the B run of every group with coalesced loads
     for (int e = threadIdx.x * 8; e < G * N; e += blockDim.x * 8)
         load8(static_cast<const char*>(C) + ((size_t)b * G * N + e) * sa, act_bf16, cs + e);
+    for (int e = threadIdx.x; e < H * (w + 1); e += blockDim.x) {
+        const int h = e / (w + 1), i = e - (e / (w + 1)) * (w + 1);
+        dts[h * L + i] = ring_dt[((size_t)s * H + h) * L + i];
+    }
+    const int run16 = (w + 1) * N * sa / 16;  // 16-byte chunks of one group's run
+    for (int e = threadIdx.x; e < G * run16; e += blockDim.x) {
+        const int g = e / run16, c = e - (e / run16) * run16;
+        reinterpret_cast<uint4*>(braw)[e] = reinterpret_cast<const uint4*>(
+            static_cast<const char*>(ring_B) + ((size_t)s * G + g) * L * N * sa)[c];
+    }
     __syncthreads();
 
-    // bc[g][i] = B_i . C_t: one thread per (group, entry), whole dot product
-    for (int pair = threadIdx.x; pair < G * (w + 1); pair += blockDim.x) {
+    // bc[g][i] = B_i . C_t: one warp per (group, entry), lanes over dstate
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    for (int pair = warp; pair < G * (w + 1); pair += nwarps) {
         const int g = pair / (w + 1), i = pair - (pair / (w + 1)) * (w + 1);
-        const char* Bi = static_cast<const char*>(ring_B) + (((size_t)s * G + g) * L + i) * N * sa;
+        const char* Bi = braw + (size_t)(g * (w + 1) + i) * N * sa;
         const float* cg = cs + g * N;
-        float acc0 = 0.f, acc1 = 0.f;
-        for (int n = 0; n < N; n += 16) {
-            float b8[8], b9[8];
-            load8(Bi + n * sa, act_bf16, b8);
-            load8(Bi + (n + 8) * sa, act_bf16, b9);
+        float acc = 0.f;
+        for (int n = lane; n < N; n += 32) acc = fmaf(load1(Bi, n, act_bf16), cg[n], acc);
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                acc0 = fmaf(b8[j], cg[n + j], acc0);
-                acc1 = fmaf(b9[j], cg[n + 8 + j], acc1);
-            }
-        }
-        bc[g * L + i] = acc0 + acc1;
+        for (int o = 16; o >= 1; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (lane == 0) bc[g * L + i] = acc;
     }
     __syncthreads();
 
     // P_i = exp(A_h * sum_{j>i} dt_j); coef_i = P_i dt_i bc_i; a_i = P_i dt_i; Pm1
-    const int hpg = H / G;
     for (int h = threadIdx.x; h < H; h += blockDim.x) {
         const int g = h / hpg;
-        const float* dts = ring_dt + ((size_t)s * H + h) * L;
+        const float* dh = dts + h * L;
         float* t = tbl + h * TBL;
         const float Ah = A[h];
         float suffix = 0.f;
         for (int i = w; i >= 0; --i) {
-            const float dti = dts[i];
+            const float dti = dh[i];
             const float Pi = expf(Ah * suffix);
             t[i] = Pi * dti * bc[g * L + i];
             t[L + i] = Pi * dti;
@@ -592,8 +602,10 @@ extern "C" int rssm_mamba2_precompute(const rssm_mamba2_dims* d, const float* A,
         return RSSM_ERR_INVALID_ARG;
     if (workspace_bytes < rssm_mamba2_workspace_size(d)) return RSSM_ERR_INVALID_ARG;
     const int L = d->ring_len;
-    const int smem =
-        (((d->ngroups * d->dstate + d->ngroups * L + 3) & ~3) + d->nheads * m2::tbl_floats(L)) * 4;
+    const int sa = d->act_dtype == RSSM_BF16 ? 2 : 4;
+    const int smem = (((d->ngroups * d->dstate + d->nheads * L + d->ngroups * L + 3) & ~3) +
+                      d->nheads * m2::tbl_floats(L)) * 4 +
+                     d->ngroups * L * d->dstate * sa;
     DeviceInfo di;
     if (!device_info(&di)) return RSSM_ERR_CUDA;
     if (smem > di.max_smem_optin) return RSSM_ERR_UNSUPPORTED;

@@ -145,8 +145,8 @@ class Mamba2FullStateDecoder:
 class GDNReplayDecoder:
     """ReplaySSM gated-delta-net decode for one layer.
 
-    Buffers: state [num_slots, HV, V, K] float32, ring_d [num_slots, HV, L, V]
-    float32, ring_k [num_slots, HK, L, K] (act dtype), ring_g [num_slots, HV, L]
+    Buffers: state [num_slots, HV, V, K] float32, ring_d [num_slots, HV, V/32, L, 32]
+    float32 (value rows in blocks of 32), ring_k [num_slots, HK, L, K] (act dtype), ring_g [num_slots, HV, L]
     float32, slot_wp [num_slots] int32."""
 
     def __init__(self, num_v_heads, num_k_heads, head_k_dim, head_v_dim, ring_len, num_slots,
@@ -158,7 +158,7 @@ class GDNReplayDecoder:
         self.act_dtype, self.out_dtype = act_dtype, out_dtype
         f32 = dict(device=dev, dtype=torch.float32)
         self.state = torch.zeros(num_slots, num_v_heads, head_v_dim, head_k_dim, **f32)
-        self.ring_d = torch.zeros(num_slots, num_v_heads, ring_len, head_v_dim, **f32)
+        self.ring_d = torch.zeros(num_slots, num_v_heads, head_v_dim // 32, ring_len, 32, **f32)
         self.ring_k = torch.zeros(num_slots, num_k_heads, ring_len, head_k_dim, device=dev,
                                   dtype=act_dtype)
         self.ring_g = torch.zeros(num_slots, num_v_heads, ring_len, **f32)
@@ -240,7 +240,7 @@ class GDNFullStateDecoder:
 class GDNSpecVerifier:
     """ReplaySSM speculative verify for the gated delta net (linear draft chain of T).
 
-    Buffers: state [num_slots, HV, V, K] float32; rings d [.., HV, L, V] f32,
+    Buffers: state [num_slots, HV, V, K] float32; rings d [.., HV, V/32, L, 32] f32,
     k [.., HK, L, K], g [.., HV, L] f32, raw v [.., HV, L, V], beta [.., HV, L] f32;
     per-slot cursors cnt (slot_wp), base, flush."""
 
@@ -253,7 +253,7 @@ class GDNSpecVerifier:
         self.act_dtype, self.out_dtype = act_dtype, out_dtype
         f32 = dict(device=dev, dtype=torch.float32)
         self.state = torch.zeros(num_slots, num_v_heads, head_v_dim, head_k_dim, **f32)
-        self.ring_d = torch.zeros(num_slots, num_v_heads, ring_len, head_v_dim, **f32)
+        self.ring_d = torch.zeros(num_slots, num_v_heads, head_v_dim // 32, ring_len, 32, **f32)
         self.ring_k = torch.zeros(num_slots, num_k_heads, ring_len, head_k_dim, device=dev,
                                   dtype=act_dtype)
         self.ring_g = torch.zeros(num_slots, num_v_heads, ring_len, **f32)
