@@ -9,9 +9,10 @@ step = cursor advance, ring append, precompute, output/flush for the whole batch
 The same line carries the gated-delta-net decode (`gdn_decode`) and speculative
 verify (`gdn_spec`) results of their own workloads as sub-objects.
 
-Each step is replayed from CUDA graphs: one graph holds cursor advance + ring
-append + precompute, a second the output kernel, and CUDA events recorded on the
-stream between them time the output kernel inside the timed region.
+Each step is replayed from CUDA graphs: one graph holds the fused prologue (cursor
+advance + ring append + tables, one launch), a second the output kernel, and CUDA
+events recorded on the stream between them time the output kernel inside the
+timed region.
 
 Keys of the JSON line (rank 0):
   value       decode rows/s over all ranks (device-timed, inputs resident)
@@ -467,11 +468,7 @@ def run_mamba2(args, dist):
     def pre_fn(j):
         x, dt, Bm, C, z = sets[j]
 
-        def f():
-            dec.advance(ci)
-            dec.append(x, dt, Bm, ci)
-            dec.precompute(C, ci)
-        return f
+        return lambda: dec.prepare(x, dt, Bm, C, ci)
 
     def out_fn(j):
         x, dt, Bm, C, z = sets[j]
@@ -543,7 +540,7 @@ def run_mamba2(args, dist):
         e_ms = dist.max(e0.elapsed_time(e1)) / args.e2e_steps
         e2e = {"value": dist.world * wl.batch / (e_ms * 1e-3), "unit": UNIT,
                "ms_per_step": e_ms, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "api": "Mamba2ReplayDecoder.step (eager, 4 C-ABI calls per step)"}
+               "api": "Mamba2ReplayDecoder.step (eager; one rssm_mamba2_step call, 2 launches)"}
 
     # the in-house conventional kernel on an identical pool
     full = None
@@ -589,7 +586,7 @@ def run_mamba2(args, dist):
                    "dstate": wl.dstate, "ngroups": wl.ngroups, "ring_len": wl.L,
                    "state_dtype": "bf16", "act_dtype": "bf16", "out_dtype": "bf16",
                    "parallelism": "independent replica per gpu (dp%d)" % dist.world,
-                   "timing": "CUDA graphs: advance+append+precompute | output, events between",
+                   "timing": "CUDA graphs: prepare (cursor+append+tables) | output, events between",
                    "l2": "inputs larger than L2: 1.07 GB of checkpoint tiles streamed per step"},
         "achieved_hbm_gbs": step_b / (ms_step * 1e-3) / 1e9,
         "hbm_frac_step": step_b / (ms_step * 1e-3) / 1e9 / peak,
@@ -601,7 +598,7 @@ def run_mamba2(args, dist):
         "full_state": full,
         "e2e": e2e,
         "cpu_baseline": cpu,
-        "gpu_launches": 4 * K,
+        "gpu_launches": 2 * K,
         "clocks": clocks,
     }
     return line
@@ -652,11 +649,7 @@ def run_gdn(args, dist, sub=False):
     def pre_fn(j):
         q, k, v, beta, g = sets[j]
 
-        def f():
-            dec.advance(ci)
-            dec.append(k, g, ci)
-            dec.precompute(q, k, beta, g, ci)
-        return f
+        return lambda: dec.prepare(q, k, beta, g, ci)
 
     def out_fn(j):
         q, k, v, beta, g = sets[j]
@@ -720,7 +713,7 @@ def run_gdn(args, dist, sub=False):
         "config": {"workload": GDN_WORKLOAD, "global_batch": dist.world * wl.batch,
                    "batch_per_gpu": wl.batch, "HV": wl.num_v_heads, "HK": wl.num_k_heads,
                    "K": wl.head_k_dim, "V": wl.head_v_dim, "ring_len": wl.L,
-                   "timing": "CUDA graphs: advance+append+precompute | output, events between",
+                   "timing": "CUDA graphs: prepare (cursor+append+tables) | output, events between",
                    "l2": "inputs larger than L2: 537 MB of fp32 checkpoint tiles per step"},
         "roofline": {"bound": "hbm", "kernel": "gdn output kernel (fp32 state, 32-row tiles)",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
@@ -728,7 +721,7 @@ def run_gdn(args, dist, sub=False):
                      "traffic": traffic_record("gdn.cu", "gdn_output_kernel_batch256.md"),
                      "algorithmic_bytes_per_launch": int(out_b), "avg_launch_ms": out_avg_ms},
         "full_state": full,
-        "gpu_launches": 4 * K,
+        "gpu_launches": 2 * K,
         "clocks": clocks,
     }
     if not sub and dist.rank == 0 and dist.world == 1 and not args.no_cpu:
@@ -928,7 +921,7 @@ def run_sweep(args, dist):
                         "full_state_gbs": fb / (full_ms * 1e-3) / 1e9,
                         "full_state_hbm_frac": fb / (full_ms * 1e-3) / 1e9 / peak,
                         "replay_speedup": full_ms / rep_ms,
-                        "timing": "one CUDA graph per step (4 launches); full state one graph"}
+                        "timing": "one CUDA graph per step (2 launches); full state one graph"}
                 if dist.rank == 0:
                     print(json.dumps(line), flush=True)
                 del sets

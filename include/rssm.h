@@ -218,6 +218,36 @@ int rssm_mamba2_decode(const rssm_mamba2_dims* dims, void* state, const float* A
                        const uint8_t* row_flush, void* workspace, size_t workspace_bytes,
                        void* y, int32_t* dev_err, rssm_stream_t stream);
 
+/* rssm_mamba2_prepare -- the per-row prologue of one decode step in ONE launch
+ * (one CTA per row): the STANDARD cursor step of rssm_advance_cursors (when
+ * advance != 0), rssm_ring_append, then rssm_mamba2_precompute. Results are
+ * those of the three calls in that order ([M2] 实现拆解 items 1 and 3: the
+ * per-row precompute runs before the output kernel, write_pos / is_flush per
+ * row). With advance == 0 the row cursors come from an earlier
+ * rssm_advance_cursors (layers that share one advance); slot_wp, force_flush and
+ * row_flush are then unused (may be NULL). Arguments and layouts as in those
+ * calls; errors as theirs. */
+int rssm_mamba2_prepare(const rssm_mamba2_dims* dims, int advance, const uint8_t* force_flush,
+                        int32_t* slot_wp, int32_t* row_wp, uint8_t* row_flush, const void* x,
+                        const float* dt_raw, const float* dt_bias, int dt_softplus,
+                        const void* B, const float* A, const void* C,
+                        const int32_t* cache_indices, void* ring_x, float* ring_dt,
+                        void* ring_B, void* workspace, size_t workspace_bytes,
+                        int32_t* dev_err, rssm_stream_t stream);
+
+/* rssm_mamba2_step -- one whole ReplaySSM decode step in two launches:
+ * rssm_mamba2_prepare then rssm_mamba2_output ([M2] 关键源码片段: the decode
+ * path calls the ReplaySSM update once per step in place of
+ * selective_state_update). row_flush is always required (the output kernel reads
+ * it). Arguments, layouts and errors as in those two calls. */
+int rssm_mamba2_step(const rssm_mamba2_dims* dims, int advance, const uint8_t* force_flush,
+                     int32_t* slot_wp, int32_t* row_wp, uint8_t* row_flush, void* state,
+                     const void* x, const float* dt_raw, const float* dt_bias, int dt_softplus,
+                     const float* A, const void* B, const void* C, const float* D, const void* z,
+                     const int32_t* cache_indices, void* ring_x, float* ring_dt, void* ring_B,
+                     void* workspace, size_t workspace_bytes, void* y, int32_t* dev_err,
+                     rssm_stream_t stream);
+
 /* Size of the device array rssm_mamba2_decode_noalloc keeps its workspace in. */
 #define RSSM_NOALLOC_WORKSPACE_BYTES (16u << 20)
 
@@ -330,6 +360,30 @@ int rssm_gdn_decode(const rssm_gdn_dims* dims, float* state, const void* q, cons
                     const float* ring_g, float* ring_d, const int32_t* cache_indices,
                     const int32_t* row_wp, const uint8_t* row_flush, void* workspace,
                     size_t workspace_bytes, void* o, int32_t* dev_err, rssm_stream_t stream);
+
+/* rssm_gdn_prepare -- the per-row prologue of one GDN decode step in ONE launch
+ * (one CTA per row): the STANDARD cursor step of rssm_advance_cursors (when
+ * advance != 0), rssm_gdn_ring_append, then rssm_gdn_precompute; results are
+ * those of the three calls in that order ([GDN] 实现拆解 items 1 and 2: the
+ * decode kernel's inputs are the ring and per-row cursors with a forced-flush
+ * mask). With advance == 0 the row cursors come from an earlier
+ * rssm_advance_cursors; slot_wp, force_flush and row_flush are then unused (may
+ * be NULL). Arguments, layouts and errors as in those calls. */
+int rssm_gdn_prepare(const rssm_gdn_dims* dims, int advance, const uint8_t* force_flush,
+                     int32_t* slot_wp, int32_t* row_wp, uint8_t* row_flush, const void* q,
+                     const void* k, const float* beta, const float* g,
+                     const int32_t* cache_indices, void* ring_k, float* ring_g, void* workspace,
+                     size_t workspace_bytes, int32_t* dev_err, rssm_stream_t stream);
+
+/* rssm_gdn_step -- one whole GDN ReplaySSM decode step in two launches:
+ * rssm_gdn_prepare then rssm_gdn_output. row_flush is always required.
+ * Arguments, layouts and errors as in those two calls. */
+int rssm_gdn_step(const rssm_gdn_dims* dims, int advance, const uint8_t* force_flush,
+                  int32_t* slot_wp, int32_t* row_wp, uint8_t* row_flush, float* state,
+                  const void* q, const void* k, const void* v, const float* beta, const float* g,
+                  const int32_t* cache_indices, void* ring_k, float* ring_g, float* ring_d,
+                  void* workspace, size_t workspace_bytes, void* o, int32_t* dev_err,
+                  rssm_stream_t stream);
 
 /* rssm_gdn_full_state_decode -- the conventional GDN decode step: read S, apply
  * S <- g S + beta (v - g S k) k^T, write S, o = S q. ring_len is ignored. */

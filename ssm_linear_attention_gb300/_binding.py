@@ -20,9 +20,11 @@ RSSM_NOALLOC_WORKSPACE_BYTES = 16 << 20
 EXPORTS = (
     "rssm_status_string", "rssm_abi_version", "rssm_advance_cursors", "rssm_ring_append",
     "rssm_mamba2_workspace_size", "rssm_mamba2_precompute", "rssm_mamba2_output",
-    "rssm_mamba2_decode", "rssm_mamba2_decode_noalloc", "rssm_mamba2_full_state_update",
+    "rssm_mamba2_decode", "rssm_mamba2_decode_noalloc", "rssm_mamba2_prepare", "rssm_mamba2_step",
+    "rssm_mamba2_full_state_update",
     "rssm_gdn_ring_append",
     "rssm_gdn_workspace_size", "rssm_gdn_precompute", "rssm_gdn_output", "rssm_gdn_decode",
+    "rssm_gdn_prepare", "rssm_gdn_step",
     "rssm_gdn_full_state_decode", "rssm_gdn_spec_workspace_size", "rssm_gdn_spec_verify",
 )
 
@@ -70,6 +72,10 @@ def _declare(L):
                                     _VP, _SZ, _VP, _VP, _VP]),
         "rssm_mamba2_decode_noalloc": (_I, [m2, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                             _VP, _VP, _VP, _VP]),
+        "rssm_mamba2_prepare": (_I, [m2, _I, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _VP, _VP, _VP,
+                                     _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _VP]),
+        "rssm_mamba2_step": (_I, [m2, _I, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _VP, _VP,
+                                  _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _VP, _VP]),
         "rssm_mamba2_full_state_update": (_I, [m2, _VP, _VP, _VP, _VP, _I, _VP, _VP, _VP, _VP,
                                                _VP, _VP, _VP, _VP, _VP]),
         "rssm_gdn_ring_append": (_I, [gd, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
@@ -80,6 +86,10 @@ def _declare(L):
                                  _VP]),
         "rssm_gdn_decode": (_I, [gd, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                  _VP, _SZ, _VP, _VP, _VP]),
+        "rssm_gdn_prepare": (_I, [gd, _I, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                  _VP, _SZ, _VP, _VP]),
+        "rssm_gdn_step": (_I, [gd, _I, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                               _VP, _VP, _VP, _VP, _SZ, _VP, _VP, _VP]),
         "rssm_gdn_full_state_decode": (_I, [gd, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                             _VP]),
         "rssm_gdn_spec_workspace_size": (_SZ, [gd, _I32]),
@@ -188,6 +198,26 @@ def rssm_mamba2_decode_noalloc(dims, state, A, C, D, z, ring_x, ring_dt, ring_B,
           _ptr(row_flush), _ptr(y), _ptr(dev_err), _stream(stream))
 
 
+def rssm_mamba2_prepare(dims, advance, force_flush, slot_wp, row_wp, row_flush, x, dt_raw,
+                        dt_bias, dt_softplus, B, A, C, cache_indices, ring_x, ring_dt, ring_B,
+                        workspace, workspace_bytes, dev_err=None, stream=None):
+    _call("rssm_mamba2_prepare", ctypes.byref(dims), int(advance), _ptr(force_flush),
+          _ptr(slot_wp), _ptr(row_wp), _ptr(row_flush), _ptr(x), _ptr(dt_raw), _ptr(dt_bias),
+          int(dt_softplus), _ptr(B), _ptr(A), _ptr(C), _ptr(cache_indices), _ptr(ring_x),
+          _ptr(ring_dt), _ptr(ring_B), _ptr(workspace), workspace_bytes, _ptr(dev_err),
+          _stream(stream))
+
+
+def rssm_mamba2_step(dims, advance, force_flush, slot_wp, row_wp, row_flush, state, x, dt_raw,
+                     dt_bias, dt_softplus, A, B, C, D, z, cache_indices, ring_x, ring_dt, ring_B,
+                     workspace, workspace_bytes, y, dev_err=None, stream=None):
+    _call("rssm_mamba2_step", ctypes.byref(dims), int(advance), _ptr(force_flush), _ptr(slot_wp),
+          _ptr(row_wp), _ptr(row_flush), _ptr(state), _ptr(x), _ptr(dt_raw), _ptr(dt_bias),
+          int(dt_softplus), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z), _ptr(cache_indices),
+          _ptr(ring_x), _ptr(ring_dt), _ptr(ring_B), _ptr(workspace), workspace_bytes, _ptr(y),
+          _ptr(dev_err), _stream(stream))
+
+
 def rssm_mamba2_full_state_update(dims, state, x, dt_raw, dt_bias, dt_softplus, A, B, C, D, z,
                                   cache_indices, y, dev_err=None, stream=None):
     _call("rssm_mamba2_full_state_update", ctypes.byref(dims), _ptr(state), _ptr(x),
@@ -225,6 +255,24 @@ def rssm_gdn_decode(dims, state, q, k, v, beta, g, ring_k, ring_g, ring_d, cache
           _ptr(beta), _ptr(g), _ptr(ring_k), _ptr(ring_g), _ptr(ring_d), _ptr(cache_indices),
           _ptr(row_wp), _ptr(row_flush), _ptr(workspace), workspace_bytes, _ptr(o),
           _ptr(dev_err), _stream(stream))
+
+
+def rssm_gdn_prepare(dims, advance, force_flush, slot_wp, row_wp, row_flush, q, k, beta, g,
+                     cache_indices, ring_k, ring_g, workspace, workspace_bytes, dev_err=None,
+                     stream=None):
+    _call("rssm_gdn_prepare", ctypes.byref(dims), int(advance), _ptr(force_flush), _ptr(slot_wp),
+          _ptr(row_wp), _ptr(row_flush), _ptr(q), _ptr(k), _ptr(beta), _ptr(g),
+          _ptr(cache_indices), _ptr(ring_k), _ptr(ring_g), _ptr(workspace), workspace_bytes,
+          _ptr(dev_err), _stream(stream))
+
+
+def rssm_gdn_step(dims, advance, force_flush, slot_wp, row_wp, row_flush, state, q, k, v, beta, g,
+                  cache_indices, ring_k, ring_g, ring_d, workspace, workspace_bytes, o,
+                  dev_err=None, stream=None):
+    _call("rssm_gdn_step", ctypes.byref(dims), int(advance), _ptr(force_flush), _ptr(slot_wp),
+          _ptr(row_wp), _ptr(row_flush), _ptr(state), _ptr(q), _ptr(k), _ptr(v), _ptr(beta),
+          _ptr(g), _ptr(cache_indices), _ptr(ring_k), _ptr(ring_g), _ptr(ring_d), _ptr(workspace),
+          workspace_bytes, _ptr(o), _ptr(dev_err), _stream(stream))
 
 
 def rssm_gdn_full_state_decode(dims, state, q, k, v, beta, g, cache_indices, o, dev_err=None,

@@ -10,6 +10,7 @@
 #include <mutex>
 
 #include "common.cuh"
+#include "cursor.cuh"
 #include "internal.h"
 
 namespace rssm {
@@ -116,34 +117,16 @@ __global__ void cursor_kernel(int mode, int32_t* __restrict__ slot_wp, int32_t* 
     const int b = blockIdx.x * blockDim.x + threadIdx.x;
     if (b >= batch) return;
     const int s = ci[b];
-    if (s < 0) {
-        if (mode == RSSM_CURSOR_STANDARD) {
-            row_wp[b] = 0;
-            row_flush[b] = 0;
-        }
+    if (mode == RSSM_CURSOR_STANDARD) {
+        standard_cursor(b, s, num_slots, L, slot_wp, force, row_wp, row_flush, dev_err);
         return;
     }
+    if (s < 0) return;
     if (s >= num_slots) {
         set_dev_err(dev_err, RSSM_DEVERR_SLOT);
-        if (mode == RSSM_CURSOR_STANDARD) {
-            row_wp[b] = 0;
-            row_flush[b] = 0;
-        }
         return;
     }
-    if (mode == RSSM_CURSOR_STANDARD) {
-        const int w = slot_wp[s];
-        if (w < 0 || w >= L) {
-            set_dev_err(dev_err, RSSM_DEVERR_CURSOR);
-            row_wp[b] = 0;
-            row_flush[b] = 0;
-            return;
-        }
-        const int f = (w == L - 1) || (force != nullptr && force[b] != 0);
-        row_wp[b] = w;
-        row_flush[b] = static_cast<uint8_t>(f);
-        slot_wp[s] = f ? 0 : w + 1;
-    } else if (mode == RSSM_CURSOR_SPEC_COMMIT) {
+    if (mode == RSSM_CURSOR_SPEC_COMMIT) {
         int cnt = slot_wp[s];
         int base = slot_base[s];
         const int a = acc[b];

@@ -167,6 +167,18 @@ __device__ __forceinline__ float load1(const void* base, long idx, bool is_bf16)
                    : reinterpret_cast<const float*>(base)[idx];
 }
 
+// 4 consecutive elements (bf16 when bf, else f32) at element index i of base
+// (8-byte aligned for bf16, 16-byte for f32) into f[0..3].
+__device__ __forceinline__ void load4(const void* base, int i, bool bf, float* f) {
+    if (bf) {
+        const uint2 v = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(base) + i);
+        f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x); f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+    } else {
+        const float4 v = *reinterpret_cast<const float4*>(static_cast<const float*>(base) + i);
+        f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
+    }
+}
+
 __device__ __forceinline__ void store1(void* base, long idx, bool is_bf16, float v) {
     if (is_bf16) reinterpret_cast<uint16_t*>(base)[idx] = f_to_bf16(v);
     else reinterpret_cast<float*>(base)[idx] = v;

@@ -24,154 +24,15 @@
 // value rows; a lane holds 4 key columns of a row (16-byte shared loads), so the
 // two dot products per row reduce across the warp with one 32-way reduce-scatter.
 // The d ring is stored in blocks of 32 value rows, so a block's history entries
-// arrive with one bulk copy.
+// arrive with one bulk copy. The per-row prologue kernels (ring append, tables)
+// are in gdn_prologue.cu.
 #include "common.cuh"
+#include "gdn.cuh"
 #include "internal.h"
 #include "pipeline.cuh"
 
 namespace rssm {
 namespace gdn {
-
-constexpr int KD = 128;  // key dim handled by these kernels
-constexpr int VB = 32;   // value rows per work item (a 16 KB fp32 tile)
-constexpr int TILE = VB * KD * 4;
-
-__host__ __device__ inline int tbl_floats(int L) { return (3 * L + 5 + 3) & ~3; }
-
-// 4 consecutive elements (bf16 or f32) at element index i.
-__device__ __forceinline__ void load4(const void* base, int i, bool bf, float* f) {
-    if (bf) {
-        const uint2 v = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(base) + i);
-        f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x); f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
-    } else {
-        const float4 v = *reinterpret_cast<const float4*>(static_cast<const float*>(base) + i);
-        f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
-    }
-}
-
-// ----------------------------------------------------------------------------
-// ring append (k, g)
-// ----------------------------------------------------------------------------
-
-__global__ void ring_append_kernel(int HV, int HK, int L, int num_slots, int act_bf16,
-                                   const void* __restrict__ k, const float* __restrict__ g,
-                                   const int32_t* __restrict__ ci, const int32_t* __restrict__ row_wp,
-                                   void* __restrict__ ring_k, float* __restrict__ ring_g,
-                                   int32_t* __restrict__ dev_err) {
-    const int b = blockIdx.x;
-    const int s = ci[b];
-    if (s < 0) return;
-    if (s >= num_slots) {
-        if (threadIdx.x == 0) set_dev_err(dev_err, RSSM_DEVERR_SLOT);
-        return;
-    }
-    const int w = row_wp[b];
-    if (w < 0 || w >= L) {
-        if (threadIdx.x == 0) set_dev_err(dev_err, RSSM_DEVERR_CURSOR);
-        return;
-    }
-    const int sa = act_bf16 ? 2 : 4;
-    const int kc = KD * sa / 16;
-    const uint4* ks = reinterpret_cast<const uint4*>(static_cast<const char*>(k) + (size_t)b * HK * KD * sa);
-    for (int c = threadIdx.x; c < HK * kc; c += blockDim.x) {
-        const int kh = c / kc, j = c % kc;
-        reinterpret_cast<uint4*>(static_cast<char*>(ring_k) + (((size_t)s * HK + kh) * L + w) * KD * sa)[j] =
-            ks[c];
-    }
-    for (int hv = threadIdx.x; hv < HV; hv += blockDim.x)
-        ring_g[((size_t)s * HV + hv) * L + w] = g[(size_t)b * HV + hv];
-}
-
-// ----------------------------------------------------------------------------
-// precompute
-// ----------------------------------------------------------------------------
-
-__global__ void __launch_bounds__(256) precompute_kernel(
-    int HV, int HK, int L, int num_slots, int act_bf16, const void* __restrict__ q,
-    const void* __restrict__ k, const float* __restrict__ beta, const float* __restrict__ g,
-    const void* __restrict__ ring_k, const float* __restrict__ ring_g, const int32_t* __restrict__ ci,
-    const int32_t* __restrict__ row_wp, float* __restrict__ ws) {
-    extern __shared__ __align__(16) float psm[];
-    const int b = blockIdx.x;
-    const int s = ci[b];
-    if (s < 0 || s >= num_slots) return;
-    const int w = row_wp[b];
-    if (w < 0 || w >= L) return;
-    const int TBL = tbl_floats(L);
-    const int sa = act_bf16 ? 2 : 4;
-    float* kt = psm;              // [HK][KD]
-    float* qt = kt + HK * KD;     // [HK][KD]
-    float* kk = qt + HK * KD;     // [HK][L]
-    float* kq = kk + HK * L;      // [HK][L]
-    float* kqt = kq + HK * L;     // [HK]
-    float* tbl = psm + ((2 * HK * KD + 2 * HK * L + HK + 3) & ~3);  // [HV][TBL]
-    float* gs = tbl + HV * TBL;                                       // gate ring [HV][L]
-
-    for (int e = threadIdx.x * 8; e < HK * KD; e += blockDim.x * 8) {
-        load8(static_cast<const char*>(k) + ((size_t)b * HK * KD + e) * sa, act_bf16, kt + e);
-        load8(static_cast<const char*>(q) + ((size_t)b * HK * KD + e) * sa, act_bf16, qt + e);
-    }
-    for (int e = threadIdx.x; e < HV * L; e += blockDim.x) gs[e] = ring_g[(size_t)s * HV * L + e];
-    __syncthreads();
-
-    // one thread per (key head, entry i <= w): kk_i = k_i . k_t, kq_i = k_i . q_t
-    // (i < w, from the ring), kq_t = k_t . q_t (i == w)
-    for (int task = threadIdx.x; task < HK * (w + 1); task += blockDim.x) {
-        const int kh = task / (w + 1), i = task - (task / (w + 1)) * (w + 1);
-        const float* ktk = kt + kh * KD;
-        const float* qtk = qt + kh * KD;
-        float a1 = 0.f, a2 = 0.f;
-        if (i < w) {
-            const char* ki = static_cast<const char*>(ring_k) + (((size_t)s * HK + kh) * L + i) * KD * sa;
-            for (int e = 0; e < KD; e += 8) {
-                float k8[8];
-                load8(ki + e * sa, act_bf16, k8);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    a1 = fmaf(k8[j], ktk[e + j], a1);
-                    a2 = fmaf(k8[j], qtk[e + j], a2);
-                }
-            }
-            kk[kh * L + i] = a1;
-            kq[kh * L + i] = a2;
-        } else {
-            for (int e = 0; e < KD; ++e) a2 = fmaf(ktk[e], qtk[e], a2);
-            kqt[kh] = a2;
-        }
-    }
-    __syncthreads();
-    const int vpk = HV / HK;
-    for (int hv = threadIdx.x; hv < HV; hv += blockDim.x) {
-        const int kh = hv / vpk;
-        const float gt = g[(size_t)b * HV + hv];
-        const float bt = beta[(size_t)b * HV + hv];
-        const float* gr = gs + hv * L;
-        float* t = tbl + hv * TBL;
-        float gam = 1.f;  // prod_{j=i+1..w-1} g_j
-        for (int i = w - 1; i >= 0; --i) {
-            const float Gi = gt * gam;
-            t[i] = gam * kk[kh * L + i];
-            t[L + i] = Gi * kq[kh * L + i];
-            t[2 * L + i] = Gi;
-            gam *= gr[i];
-        }
-        for (int i = w; i < L; ++i) {
-            t[i] = 0.f;
-            t[L + i] = 0.f;
-            t[2 * L + i] = (i == w) ? 1.f : 0.f;
-        }
-        t[3 * L] = gam;
-        t[3 * L + 1] = gt * gam;
-        t[3 * L + 2] = kqt[kh];
-        t[3 * L + 3] = bt;
-        t[3 * L + 4] = gt;
-        for (int i = 3 * L + 5; i < TBL; ++i) t[i] = 0.f;
-    }
-    __syncthreads();
-    float4* dst = reinterpret_cast<float4*>(ws + (size_t)b * HV * TBL);
-    const float4* src = reinterpret_cast<const float4*>(tbl);
-    for (int c = threadIdx.x; c < HV * TBL / 4; c += blockDim.x) dst[c] = src[c];
-}
 
 // ----------------------------------------------------------------------------
 // output / flush and full-state decode (warp-specialised pipeline)
@@ -481,55 +342,6 @@ int check_dims(const rssm_gdn_dims* d) {
 
 using namespace rssm;
 
-extern "C" int rssm_gdn_ring_append(const rssm_gdn_dims* d, const void* k, const float* g,
-                                    const int32_t* cache_indices, const int32_t* row_wp,
-                                    void* ring_k, float* ring_g, int32_t* dev_err,
-                                    rssm_stream_t stream) {
-    int rc = gdn::check_dims(d);
-    if (rc) return rc;
-    if (d->batch == 0) return RSSM_OK;
-    if (!ok_ptr(k) || !ok_ptr(g) || !ok_ptr(cache_indices) || !ok_ptr(row_wp) || !ok_ptr(ring_k) ||
-        !ok_ptr(ring_g))
-        return RSSM_ERR_INVALID_ARG;
-    gdn::ring_append_kernel<<<d->batch, 128, 0, (cudaStream_t)stream>>>(
-        d->num_v_heads, d->num_k_heads, d->ring_len, d->num_slots, d->act_dtype == RSSM_BF16, k, g,
-        cache_indices, row_wp, ring_k, ring_g, dev_err);
-    return launch_status();
-}
-
-extern "C" size_t rssm_gdn_workspace_size(const rssm_gdn_dims* d) {
-    if (gdn::check_dims(d)) return 0;
-    return (size_t)d->batch * d->num_v_heads * gdn::tbl_floats(d->ring_len) * sizeof(float);
-}
-
-extern "C" int rssm_gdn_precompute(const rssm_gdn_dims* d, const void* q, const void* k,
-                                   const float* beta, const float* g, const void* ring_k,
-                                   const float* ring_g, const int32_t* cache_indices,
-                                   const int32_t* row_wp, void* workspace, size_t workspace_bytes,
-                                   int32_t* dev_err, rssm_stream_t stream) {
-    (void)dev_err;
-    int rc = gdn::check_dims(d);
-    if (rc) return rc;
-    if (d->batch == 0) return RSSM_OK;
-    if (!ok_ptr(q) || !ok_ptr(k) || !ok_ptr(beta) || !ok_ptr(g) || !ok_ptr(ring_k) ||
-        !ok_ptr(ring_g) || !ok_ptr(cache_indices) || !ok_ptr(row_wp) || !ok_ptr(workspace))
-        return RSSM_ERR_INVALID_ARG;
-    if (workspace_bytes < rssm_gdn_workspace_size(d)) return RSSM_ERR_INVALID_ARG;
-    const int L = d->ring_len, HK = d->num_k_heads;
-    const int smem = (((2 * HK * gdn::KD + 2 * HK * L + HK + 3) & ~3) +
-                      d->num_v_heads * gdn::tbl_floats(L) + d->num_v_heads * L) * 4;
-    DeviceInfo di;
-    if (!device_info(&di)) return RSSM_ERR_CUDA;
-    if (smem > di.max_smem_optin) return RSSM_ERR_UNSUPPORTED;
-    if (smem > 48 * 1024 &&
-        !ensure_smem_limit(reinterpret_cast<const void*>(gdn::precompute_kernel), smem))
-        return RSSM_ERR_CUDA;
-    gdn::precompute_kernel<<<d->batch, 256, smem, (cudaStream_t)stream>>>(
-        d->num_v_heads, HK, L, d->num_slots, d->act_dtype == RSSM_BF16, q, k, beta, g, ring_k, ring_g,
-        cache_indices, row_wp, static_cast<float*>(workspace));
-    return launch_status();
-}
-
 extern "C" int rssm_gdn_output(const rssm_gdn_dims* d, float* state, const void* q, const void* v,
                                const void* ring_k, float* ring_d, const int32_t* cache_indices,
                                const int32_t* row_wp, const uint8_t* row_flush,
@@ -578,6 +390,26 @@ extern "C" int rssm_gdn_decode(const rssm_gdn_dims* d, float* state, const void*
         return RSSM_ERR_INVALID_ARG;
     rc = rssm_gdn_precompute(d, q, k, beta, g, ring_k, ring_g, cache_indices, row_wp, workspace,
                              workspace_bytes, dev_err, stream);
+    if (rc) return rc;
+    return rssm_gdn_output(d, state, q, v, ring_k, ring_d, cache_indices, row_wp, row_flush,
+                           workspace, workspace_bytes, o, dev_err, stream);
+}
+
+extern "C" int rssm_gdn_step(const rssm_gdn_dims* d, int advance, const uint8_t* force_flush,
+                             int32_t* slot_wp, int32_t* row_wp, uint8_t* row_flush, float* state,
+                             const void* q, const void* k, const void* v, const float* beta,
+                             const float* g, const int32_t* cache_indices, void* ring_k,
+                             float* ring_g, float* ring_d, void* workspace,
+                             size_t workspace_bytes, void* o, int32_t* dev_err,
+                             rssm_stream_t stream) {
+    int rc = gdn::check_dims(d);
+    if (rc) return rc;
+    if (d->batch == 0) return RSSM_OK;
+    if (!ok_ptr(state) || !ok_ptr(v) || !ok_ptr(ring_d) || !ok_ptr(o) || !ok_ptr(row_flush))
+        return RSSM_ERR_INVALID_ARG;
+    rc = rssm_gdn_prepare(d, advance, force_flush, slot_wp, row_wp, row_flush, q, k, beta, g,
+                          cache_indices, ring_k, ring_g, workspace, workspace_bytes, dev_err,
+                          stream);
     if (rc) return rc;
     return rssm_gdn_output(d, state, q, v, ring_k, ring_d, cache_indices, row_wp, row_flush,
                            workspace, workspace_bytes, o, dev_err, stream);

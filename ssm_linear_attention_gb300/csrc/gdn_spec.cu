@@ -42,16 +42,6 @@ constexpr int kMaxT = 8;
 // table per (row, value head): au[T][L], ao[T][L], Gu[T], Go[T], beta[T], g[T], c, base'
 __host__ __device__ inline int tbl_floats(int L, int T) { return (2 * T * L + 4 * T + 2 + 3) & ~3; }
 
-__device__ __forceinline__ void load4(const void* base, int i, bool bf, float* f) {
-    if (bf) {
-        const uint2 v = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(base) + i);
-        f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x); f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
-    } else {
-        const float4 v = *reinterpret_cast<const float4*>(static_cast<const float*>(base) + i);
-        f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
-    }
-}
-
 // Effective history of a slot at verify time: (count, oldest position); false when
 // the cursors are outside the ring.
 __device__ __forceinline__ bool history(int cnt, int base, int flush, int L, int T, int* c,

@@ -9,12 +9,7 @@
 // (argument lists of the ReplaySSM call and of the baseline
 // selective_state_update).
 //
-// Kernels:
-//   ring_append_kernel    one CTA per row: x, dt = softplus(dt_raw + dt_bias), B
-//                         into ring entry w.
-//   precompute_kernel     one CTA per row: B_i . C_t per group (runs staged in
-//                         shared memory), decay suffix
-//                         products per head, written as per-(row, head) tables.
+// Kernels (the per-row prologue kernels are in mamba2_prologue.cu):
 //   output_kernel<P,N,ST> persistent, one work item = one (row, head) checkpoint
 //                         tile. Per CTA several independent pipelines, each a
 //                         producer warp feeding its own ring of shared-memory
@@ -31,138 +26,12 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "mamba2.cuh"
 #include "pipeline.cuh"
 
 namespace rssm {
 namespace m2 {
 
-__host__ __device__ inline int tbl_floats(int L) { return (2 * L + 1 + 3) & ~3; }
-
-// ----------------------------------------------------------------------------
-// ring append
-// ----------------------------------------------------------------------------
-
-__global__ void ring_append_kernel(int H, int P, int N, int G, int L, int num_slots, int act_bf16,
-                                   const void* __restrict__ x, const float* __restrict__ dt_raw,
-                                   const float* __restrict__ dt_bias, int softplus,
-                                   const void* __restrict__ B, const int32_t* __restrict__ ci,
-                                   const int32_t* __restrict__ row_wp, void* __restrict__ ring_x,
-                                   float* __restrict__ ring_dt, void* __restrict__ ring_B,
-                                   int32_t* __restrict__ dev_err) {
-    const int b = blockIdx.x;
-    const int s = ci[b];
-    if (s < 0) return;
-    if (s >= num_slots) {
-        if (threadIdx.x == 0) set_dev_err(dev_err, RSSM_DEVERR_SLOT);
-        return;
-    }
-    const int w = row_wp[b];
-    if (w < 0 || w >= L) {
-        if (threadIdx.x == 0) set_dev_err(dev_err, RSSM_DEVERR_CURSOR);
-        return;
-    }
-    const int sa = act_bf16 ? 2 : 4;
-    const int xc = P * sa / 16;  // 16-byte chunks per head row
-    const uint4* xs = reinterpret_cast<const uint4*>(static_cast<const char*>(x) + (size_t)b * H * P * sa);
-    for (int c = threadIdx.x; c < H * xc; c += blockDim.x) {
-        const int h = c / xc, j = c % xc;
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<char*>(ring_x) +
-                                              (((size_t)s * H + h) * L + w) * P * sa) + j;
-        *dst = xs[c];
-    }
-    for (int h = threadIdx.x; h < H; h += blockDim.x) {
-        float v = dt_raw[(size_t)b * H + h] + (dt_bias ? dt_bias[h] : 0.f);
-        if (softplus) v = softplus_f(v);
-        ring_dt[((size_t)s * H + h) * L + w] = v;
-    }
-    const int bc = N * sa / 16;
-    const uint4* bs = reinterpret_cast<const uint4*>(static_cast<const char*>(B) + (size_t)b * G * N * sa);
-    for (int c = threadIdx.x; c < G * bc; c += blockDim.x) {
-        const int g = c / bc, j = c % bc;
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<char*>(ring_B) +
-                                              (((size_t)s * G + g) * L + w) * N * sa) + j;
-        *dst = bs[c];
-    }
-}
-
-// ----------------------------------------------------------------------------
-// precompute: per-(row, head) coefficient tables
-// ----------------------------------------------------------------------------
-
-__global__ void __launch_bounds__(256) precompute_kernel(
-    int H, int N, int G, int L, int num_slots, int act_bf16, const float* __restrict__ A,
-    const void* __restrict__ C, const float* __restrict__ ring_dt, const void* __restrict__ ring_B,
-    const int32_t* __restrict__ ci, const int32_t* __restrict__ row_wp, float* __restrict__ ws) {
-    extern __shared__ __align__(16) float psm[];
-    const int b = blockIdx.x;
-    const int s = ci[b];
-    if (s < 0 || s >= num_slots) return;  // the output kernel reports bad slots
-    const int w = row_wp[b];
-    if (w < 0 || w >= L) return;
-    const int TBL = tbl_floats(L);
-    const int sa = act_bf16 ? 2 : 4;
-    const int hpg = H / G;
-    float* cs = psm;                                         // [G][N] C_t in fp32
-    float* dts = cs + G * N;                                 // [H][L] dt of entries 0..w
-    float* bc = dts + H * L;                                 // [G][L] B_i . C_t
-    float* tbl = psm + ((G * N + H * L + G * L + 3) & ~3);   // [H][TBL]
-    char* braw = reinterpret_cast<char*>(tbl + H * TBL);     // [G][w+1][N] raw B entries
-
-    // stage C_t, the dt run and the B run of every group with coalesced loads
-    for (int e = threadIdx.x * 8; e < G * N; e += blockDim.x * 8)
-        load8(static_cast<const char*>(C) + ((size_t)b * G * N + e) * sa, act_bf16, cs + e);
-    for (int e = threadIdx.x; e < H * (w + 1); e += blockDim.x) {
-        const int h = e / (w + 1), i = e - (e / (w + 1)) * (w + 1);
-        dts[h * L + i] = ring_dt[((size_t)s * H + h) * L + i];
-    }
-    const int run16 = (w + 1) * N * sa / 16;  // 16-byte chunks of one group's run
-    for (int e = threadIdx.x; e < G * run16; e += blockDim.x) {
-        const int g = e / run16, c = e - (e / run16) * run16;
-        reinterpret_cast<uint4*>(braw)[e] = reinterpret_cast<const uint4*>(
-            static_cast<const char*>(ring_B) + ((size_t)s * G + g) * L * N * sa)[c];
-    }
-    __syncthreads();
-
-    // bc[g][i] = B_i . C_t: one warp per (group, entry), lanes over dstate
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-    for (int pair = warp; pair < G * (w + 1); pair += nwarps) {
-        const int g = pair / (w + 1), i = pair - (pair / (w + 1)) * (w + 1);
-        const char* Bi = braw + (size_t)(g * (w + 1) + i) * N * sa;
-        const float* cg = cs + g * N;
-        float acc = 0.f;
-        for (int n = lane; n < N; n += 32) acc = fmaf(load1(Bi, n, act_bf16), cg[n], acc);
-#pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        if (lane == 0) bc[g * L + i] = acc;
-    }
-    __syncthreads();
-
-    // P_i = exp(A_h * sum_{j>i} dt_j); coef_i = P_i dt_i bc_i; a_i = P_i dt_i; Pm1
-    for (int h = threadIdx.x; h < H; h += blockDim.x) {
-        const int g = h / hpg;
-        const float* dh = dts + h * L;
-        float* t = tbl + h * TBL;
-        const float Ah = A[h];
-        float suffix = 0.f;
-        for (int i = w; i >= 0; --i) {
-            const float dti = dh[i];
-            const float Pi = expf(Ah * suffix);
-            t[i] = Pi * dti * bc[g * L + i];
-            t[L + i] = Pi * dti;
-            suffix += dti;
-        }
-        for (int i = w + 1; i < L; ++i) {
-            t[i] = 0.f;
-            t[L + i] = 0.f;
-        }
-        t[2 * L] = expf(Ah * suffix);
-        for (int i = 2 * L + 1; i < TBL; ++i) t[i] = 0.f;
-    }
-    __syncthreads();
-    float4* dst = reinterpret_cast<float4*>(ws + (size_t)b * H * TBL);
-    const float4* src = reinterpret_cast<const float4*>(tbl);
-    for (int c = threadIdx.x; c < H * TBL / 4; c += blockDim.x) dst[c] = src[c];
-}
 
 // ----------------------------------------------------------------------------
 // streaming kernels (warp-specialised pipeline, one consumer warp per tile)
@@ -564,60 +433,6 @@ struct FullLaunch {
 
 using namespace rssm;
 
-extern "C" int rssm_ring_append(const rssm_mamba2_dims* d, const void* x, const float* dt_raw,
-                                const float* dt_bias, int dt_softplus, const void* B,
-                                const int32_t* cache_indices, const int32_t* row_wp, void* ring_x,
-                                float* ring_dt, void* ring_B, int32_t* dev_err,
-                                rssm_stream_t stream) {
-    int rc = m2::check_dims(d);
-    if (rc) return rc;
-    if (d->batch == 0) return RSSM_OK;
-    if (!ok_ptr(x) || !ok_ptr(dt_raw) || !ok_opt_ptr(dt_bias) || !ok_ptr(B) ||
-        !ok_ptr(cache_indices) || !ok_ptr(row_wp) || !ok_ptr(ring_x) || !ok_ptr(ring_dt) ||
-        !ok_ptr(ring_B))
-        return RSSM_ERR_INVALID_ARG;
-    m2::ring_append_kernel<<<d->batch, 256, 0, (cudaStream_t)stream>>>(
-        d->nheads, d->headdim, d->dstate, d->ngroups, d->ring_len, d->num_slots,
-        d->act_dtype == RSSM_BF16, x, dt_raw, dt_bias, dt_softplus, B, cache_indices, row_wp, ring_x,
-        ring_dt, ring_B, dev_err);
-    return launch_status();
-}
-
-extern "C" size_t rssm_mamba2_workspace_size(const rssm_mamba2_dims* d) {
-    if (m2::check_dims(d)) return 0;
-    return (size_t)d->batch * d->nheads * m2::tbl_floats(d->ring_len) * sizeof(float);
-}
-
-extern "C" int rssm_mamba2_precompute(const rssm_mamba2_dims* d, const float* A, const void* C,
-                                      const float* ring_dt, const void* ring_B,
-                                      const int32_t* cache_indices, const int32_t* row_wp,
-                                      void* workspace, size_t workspace_bytes, int32_t* dev_err,
-                                      rssm_stream_t stream) {
-    (void)dev_err;
-    int rc = m2::check_dims(d);
-    if (rc) return rc;
-    if (d->batch == 0) return RSSM_OK;
-    if (!ok_ptr(A) || !ok_ptr(C) || !ok_ptr(ring_dt) || !ok_ptr(ring_B) || !ok_ptr(cache_indices) ||
-        !ok_ptr(row_wp) || !ok_ptr(workspace))
-        return RSSM_ERR_INVALID_ARG;
-    if (workspace_bytes < rssm_mamba2_workspace_size(d)) return RSSM_ERR_INVALID_ARG;
-    const int L = d->ring_len;
-    const int sa = d->act_dtype == RSSM_BF16 ? 2 : 4;
-    const int smem = (((d->ngroups * d->dstate + d->nheads * L + d->ngroups * L + 3) & ~3) +
-                      d->nheads * m2::tbl_floats(L)) * 4 +
-                     d->ngroups * L * d->dstate * sa;
-    DeviceInfo di;
-    if (!device_info(&di)) return RSSM_ERR_CUDA;
-    if (smem > di.max_smem_optin) return RSSM_ERR_UNSUPPORTED;
-    if (smem > 48 * 1024 &&
-        !ensure_smem_limit(reinterpret_cast<const void*>(m2::precompute_kernel), smem))
-        return RSSM_ERR_CUDA;
-    m2::precompute_kernel<<<d->batch, 256, smem, (cudaStream_t)stream>>>(
-        d->nheads, d->dstate, d->ngroups, L, d->num_slots, d->act_dtype == RSSM_BF16, A, C, ring_dt,
-        ring_B, cache_indices, row_wp, static_cast<float*>(workspace));
-    return launch_status();
-}
-
 extern "C" int rssm_mamba2_output(const rssm_mamba2_dims* d, void* state, const void* C,
                                   const float* D, const void* z, const void* ring_x,
                                   const void* ring_B, const int32_t* cache_indices,
@@ -659,6 +474,27 @@ extern "C" int rssm_mamba2_decode(const rssm_mamba2_dims* d, void* state, const 
         return RSSM_ERR_INVALID_ARG;
     rc = rssm_mamba2_precompute(d, A, C, ring_dt, ring_B, cache_indices, row_wp, workspace,
                                 workspace_bytes, dev_err, stream);
+    if (rc) return rc;
+    return rssm_mamba2_output(d, state, C, D, z, ring_x, ring_B, cache_indices, row_wp, row_flush,
+                              workspace, workspace_bytes, y, dev_err, stream);
+}
+
+extern "C" int rssm_mamba2_step(const rssm_mamba2_dims* d, int advance, const uint8_t* force_flush,
+                                int32_t* slot_wp, int32_t* row_wp, uint8_t* row_flush, void* state,
+                                const void* x, const float* dt_raw, const float* dt_bias,
+                                int dt_softplus, const float* A, const void* B, const void* C,
+                                const float* D, const void* z, const int32_t* cache_indices,
+                                void* ring_x, float* ring_dt, void* ring_B, void* workspace,
+                                size_t workspace_bytes, void* y, int32_t* dev_err,
+                                rssm_stream_t stream) {
+    int rc = m2::check_dims(d);
+    if (rc) return rc;
+    if (d->batch == 0) return RSSM_OK;
+    if (!ok_ptr(state) || !ok_ptr(D) || !ok_opt_ptr(z) || !ok_ptr(y) || !ok_ptr(row_flush))
+        return RSSM_ERR_INVALID_ARG;
+    rc = rssm_mamba2_prepare(d, advance, force_flush, slot_wp, row_wp, row_flush, x, dt_raw, dt_bias,
+                             dt_softplus, B, A, C, cache_indices, ring_x, ring_dt, ring_B,
+                             workspace, workspace_bytes, dev_err, stream);
     if (rc) return rc;
     return rssm_mamba2_output(d, state, C, D, z, ring_x, ring_B, cache_indices, row_wp, row_flush,
                               workspace, workspace_bytes, y, dev_err, stream);

@@ -5,10 +5,14 @@ CUDA device (allocated with torch: the slot-indexed checkpoint pool, the input
 rings, the per-slot cursors, the per-row cursor outputs, the workspace), and a
 step is the sequence of librssm calls the method needs, in stream order:
 
-  Mamba2 decode:  rssm_advance_cursors (STANDARD) -> rssm_ring_append ->
+  Mamba2 decode:  rssm_mamba2_step = rssm_mamba2_prepare (cursor advance,
+                  ring append, tables: one launch) -> rssm_mamba2_output; or the
+                  four calls rssm_advance_cursors (STANDARD) -> rssm_ring_append ->
                   rssm_mamba2_precompute -> rssm_mamba2_output
-  GDN decode:     rssm_advance_cursors (STANDARD) -> rssm_gdn_ring_append ->
-                  rssm_gdn_precompute -> rssm_gdn_output
+  GDN decode:     rssm_gdn_step = rssm_gdn_prepare (one launch) ->
+                  rssm_gdn_output; or the four calls rssm_advance_cursors
+                  (STANDARD) -> rssm_gdn_ring_append -> rssm_gdn_precompute ->
+                  rssm_gdn_output
   GDN spec:       rssm_gdn_spec_verify (fold + verify), then
                   rssm_advance_cursors (SPEC_COMMIT) with the accepted counts
 
@@ -94,9 +98,30 @@ class Mamba2ReplayDecoder:
                              self.ws_bytes, y, self.dev_err, stream)
         return y
 
+    def prepare(self, x, dt_raw, Bm, C, cache_indices, force_flush=None, stream=None,
+                advance=True):
+        """Cursor advance (unless advance=False), ring append and tables in one launch."""
+        B.rssm_mamba2_prepare(self.dims(x.shape[0]), advance, force_flush, self.slot_wp,
+                              self.row_wp, self.row_flush, x, dt_raw, self.dt_bias,
+                              self.dt_softplus, Bm, self.A, C, cache_indices, self.ring_x,
+                              self.ring_dt, self.ring_B, self.workspace, self.ws_bytes,
+                              self.dev_err, stream)
+
     def step(self, x, dt_raw, Bm, C, z, cache_indices, force_flush=None, y=None, stream=None,
              advance=True):
-        """One decode step for rows cache_indices (padding rows: -1). Returns y [b, H, P]."""
+        """One decode step for rows cache_indices (padding rows: -1), as one
+        rssm_mamba2_step call (two launches). Returns y [b, H, P]."""
+        b = x.shape[0]
+        y = self.y[:b] if y is None else y
+        B.rssm_mamba2_step(self.dims(b), advance, force_flush, self.slot_wp, self.row_wp,
+                           self.row_flush, self.state, x, dt_raw, self.dt_bias, self.dt_softplus,
+                           self.A, Bm, C, self.D, z, cache_indices, self.ring_x, self.ring_dt,
+                           self.ring_B, self.workspace, self.ws_bytes, y, self.dev_err, stream)
+        return y
+
+    def step_staged(self, x, dt_raw, Bm, C, z, cache_indices, force_flush=None, y=None,
+                    stream=None, advance=True):
+        """The same step as four calls (cursor, append, precompute, output)."""
         if advance:
             self.advance(cache_indices, force_flush, stream)
         self.append(x, dt_raw, Bm, cache_indices, stream)
@@ -197,8 +222,26 @@ class GDNReplayDecoder:
                           self.dev_err, stream)
         return o
 
+    def prepare(self, q, k, beta, g, cache_indices, force_flush=None, stream=None, advance=True):
+        """Cursor advance (unless advance=False), ring append and tables in one launch."""
+        B.rssm_gdn_prepare(self.dims(q.shape[0]), advance, force_flush, self.slot_wp, self.row_wp,
+                           self.row_flush, q, k, beta, g, cache_indices, self.ring_k, self.ring_g,
+                           self.workspace, self.ws_bytes, self.dev_err, stream)
+
     def step(self, q, k, v, beta, g, cache_indices, force_flush=None, o=None, stream=None,
              advance=True):
+        """One decode step as one rssm_gdn_step call (two launches). Returns o [b, HV, V]."""
+        b = q.shape[0]
+        o = self.o[:b] if o is None else o
+        B.rssm_gdn_step(self.dims(b), advance, force_flush, self.slot_wp, self.row_wp,
+                        self.row_flush, self.state, q, k, v, beta, g, cache_indices, self.ring_k,
+                        self.ring_g, self.ring_d, self.workspace, self.ws_bytes, o, self.dev_err,
+                        stream)
+        return o
+
+    def step_staged(self, q, k, v, beta, g, cache_indices, force_flush=None, o=None, stream=None,
+                    advance=True):
+        """The same step as four calls (cursor, append, precompute, output)."""
         if advance:
             self.advance(cache_indices, force_flush, stream)
         self.append(k, g, cache_indices, stream)
