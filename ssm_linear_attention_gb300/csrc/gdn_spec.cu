@@ -12,20 +12,25 @@
 // drafts).
 //
 // Launches of one verify round:
-//   fold_kernel        one CTA per (row, value head, 32-row block) of a slot with
-//                      a pending fold: S0 rows in registers, the committed entries
-//                      staged in shared memory, cnt sequential delta-rule updates
-//                      from ring k, raw v, beta, g; S0 stored.
-//   spec_pre_kernel    one CTA per (row, key head): dot products of every live key
-//                      (history and drafts) with the drafts' keys and queries,
-//                      products of gates, into a per-(row, value head) table;
-//                      writes the drafts' k, g, beta into the ring.
-//   verify_kernel<DP>  persistent TMA pipeline over (row, value head, 32-row
+//   prologue_kernel    two kinds of CTA in one grid, independent of each other:
+//     fold role        one CTA per (row, value head, 32-row block) of a slot with
+//                      a pending fold: S0 rows in registers (4 threads per row),
+//                      the committed entries staged in shared memory, cnt
+//                      sequential delta-rule updates from ring k, raw v, beta, g;
+//                      S0 stored.
+//     table role       one CTA per (row, key head): dot products of every live
+//                      key (history and drafts) with the drafts' keys and
+//                      queries, products of gates, into a per-(row, value head)
+//                      table.
+//   verify_kernel<T>   persistent TMA pipeline over (row, value head, 32-row
 //                      block) tiles of S0: the 2T dot products per value row,
-//                      then the draft chain per row; writes o, and d and raw v
-//                      of the drafts into the ring.
-// A fold must precede the verify in a separate launch: the drafts of the same
-// round may land on ring positions whose raw entries the fold still reads.
+//                      then the draft chain per row; writes o, the drafts' d and
+//                      raw v, and (one item per row and head) the drafts' k, g
+//                      and beta into the ring.
+// The fold must finish before any draft is written into the ring: with a
+// pending fold the drafts land on ring positions whose raw entries the fold
+// reads. The table role reads only history entries, which no draft overwrites,
+// so it shares the fold's launch; every ring write happens in the verify launch.
 #include "common.cuh"
 #include "internal.h"
 #include "pipeline.cuh"
@@ -38,6 +43,7 @@ constexpr int KD = 128;
 constexpr int VB = 32;  // value rows per work item (a 16 KB fp32 tile)
 constexpr int TILE = VB * KD * 4;
 constexpr int kMaxT = 8;
+constexpr int kFoldChunk = 16;  // committed entries staged per pass of the fold
 
 // table per (row, value head): au[T][L], ao[T][L], Gu[T], Go[T], beta[T], g[T], c, base'
 __host__ __device__ inline int tbl_floats(int L, int T) { return (2 * T * L + 4 * T + 2 + 3) & ~3; }
@@ -58,11 +64,15 @@ __device__ __forceinline__ bool history(int cnt, int base, int flush, int L, int
 }
 
 // ----------------------------------------------------------------------------
-// exact fold
+// prologue: exact fold + tables
 // ----------------------------------------------------------------------------
 
-struct FoldArgs {
+struct ProArgs {
     float* state;
+    const void* q;
+    const void* k;
+    const float* beta;
+    const float* g;
     const void* ring_k;
     const void* ring_v;
     const float* ring_g;
@@ -71,202 +81,186 @@ struct FoldArgs {
     const int32_t* slot_wp;
     const int32_t* slot_base;
     const uint8_t* slot_flush;
-    int32_t* dev_err;
-    int HV, HK, V, L, num_slots, act_bf16;
+    float* ws;
+    int T, HV, HK, V, L, num_slots, act_bf16;
+    int n_fold;  // fold CTAs (batch * HV * V/VB); table CTAs follow
 };
 
-// One CTA (4 warps) per (row, value head, VB-row block) of a slot with a pending
-// fold. Warp w owns rows w + 4j (j < VB/4) of the block; a lane holds key columns
-// 4l..4l+3 of each, so the block's S0 rows sit in registers. The committed
-// entries (k, raw v, beta, g) are staged in shared memory, 16 at a time, then
-// replayed in order: u = S k (one reduce-scatter), d = beta (v - g u),
-// S = g S + d k^T.
-constexpr int kFoldRows = VB / 4;  // rows per warp
+// Shared memory of the fold role (floats): k [16][KD], raw v [16][VB], beta, g.
+__host__ __device__ inline int fold_smem_floats() { return kFoldChunk * (KD + VB + 2); }
 
-__global__ void __launch_bounds__(kThreads) fold_kernel(const FoldArgs a) {
-    __shared__ __align__(16) float ks[16 * KD];  // k of up to 16 entries
-    __shared__ float vs[16 * VB];                // raw v of the block's rows
-    __shared__ float bs[16], gs[16];
+// Shared memory of the table role (floats): KK [L][T], KQ [L][T], gates
+// [HV/HK][L], the drafts' k and q [T][2][KD].
+__host__ __device__ inline int pre_smem_floats(int L, int T, int vpk) {
+    return ((2 * L * T + vpk * L + 3) & ~3) + 2 * T * KD;
+}
+
+// Exact fold of one (row, value head, 32-row block) tile. Thread t owns row t/4
+// and the 4-column chunks q, q+4, ..., q+28 (q = t%4) of it, so a row's dot
+// product needs two shuffles; the committed entries are replayed in order:
+// u = S k, d = beta (v - g u), S = g S + d k^T.
+__device__ void fold_tile(const ProArgs& a, int item, float* sm) {
     const int NVB = a.V / VB;
-    const int item = blockIdx.x;
     const int b = item / (a.HV * NVB);
     const int rem = item - b * a.HV * NVB;
     const int hv = rem / NVB, vb = rem - (rem / NVB) * NVB;
     const int s = a.ci[b];
-    if (s < 0 || s >= a.num_slots) return;  // verify reports bad slots
+    if (s < 0 || s >= a.num_slots) return;  // the verify reports bad slots
     if (!a.slot_flush[s]) return;
     const int cnt = a.slot_wp[s], base = a.slot_base[s];
     if (cnt <= 0 || cnt > a.L || base < 0 || base >= a.L) return;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const bool bf = a.act_bf16;
+    const int sa = bf ? 2 : 4;
+    const int L = a.L;
+    const int t = threadIdx.x, r = t >> 2, qd = t & 3;
     const int kh = hv / (a.HV / a.HK);
+    float* ks = sm;                       // [16][KD]
+    float* vs = ks + kFoldChunk * KD;     // [16][VB]
+    float* bs = vs + kFoldChunk * VB;     // [16]
+    float* gs = bs + kFoldChunk;          // [16]
     float* tile = a.state + (((size_t)s * a.HV + hv) * a.V + (size_t)vb * VB) * KD;
-    float S[kFoldRows][4];
+    float S[8][4];
 #pragma unroll
-    for (int j = 0; j < kFoldRows; ++j) {
-        const float4 v4 = *reinterpret_cast<const float4*>(tile + (warp + 4 * j) * KD + lane * 4);
-        S[j][0] = v4.x; S[j][1] = v4.y; S[j][2] = v4.z; S[j][3] = v4.w;
+    for (int u = 0; u < 8; ++u) {
+        const float4 v4 = *reinterpret_cast<const float4*>(tile + r * KD + (qd + 4 * u) * 4);
+        S[u][0] = v4.x; S[u][1] = v4.y; S[u][2] = v4.z; S[u][3] = v4.w;
     }
-    constexpr int SH = 32 / kFoldRows;  // lanes holding the same row after the reduce
-    for (int e0 = 0; e0 < cnt; e0 += 16) {  // entries in chunks of 16, in order
-        const int ne = cnt - e0 < 16 ? cnt - e0 : 16;
+    const char* kr = static_cast<const char*>(a.ring_k) + ((size_t)s * a.HK + kh) * L * KD * sa;
+    for (int e0 = 0; e0 < cnt; e0 += kFoldChunk) {
+        const int ne = cnt - e0 < kFoldChunk ? cnt - e0 : kFoldChunk;
         __syncthreads();  // the previous chunk is no longer read
-        for (int e = threadIdx.x; e < ne * KD; e += blockDim.x) {
-            const int i = e / KD, c = e - (e / KD) * KD;
-            const int pos = (base + e0 + i) % a.L;
-            ks[e] = load1(a.ring_k, (((size_t)s * a.HK + kh) * a.L + pos) * KD + c, a.act_bf16);
+        for (int e = t; e < ne * (KD / 4); e += blockDim.x) {
+            const int i = e / (KD / 4), c4 = e - (e / (KD / 4)) * (KD / 4);
+            const int pos = (base + e0 + i) % L;
+            float f[4];
+            load4(kr + (size_t)pos * KD * sa, c4 * 4, bf, f);
+            *reinterpret_cast<float4*>(ks + i * KD + c4 * 4) = make_float4(f[0], f[1], f[2], f[3]);
         }
-        for (int e = threadIdx.x; e < ne * VB; e += blockDim.x) {
-            const int i = e / VB, r = e - (e / VB) * VB;
-            const int pos = (base + e0 + i) % a.L;
-            vs[e] = load1(a.ring_v, (((size_t)s * a.HV + hv) * a.L + pos) * a.V + (size_t)vb * VB + r,
-                          a.act_bf16);
+        for (int e = t; e < ne * (VB / 4); e += blockDim.x) {
+            const int i = e / (VB / 4), c4 = e - (e / (VB / 4)) * (VB / 4);
+            const int pos = (base + e0 + i) % L;
+            float f[4];
+            load4(static_cast<const char*>(a.ring_v) +
+                      ((((size_t)s * a.HV + hv) * L + pos) * a.V + (size_t)vb * VB) * sa,
+                  c4 * 4, bf, f);
+            *reinterpret_cast<float4*>(vs + i * VB + c4 * 4) = make_float4(f[0], f[1], f[2], f[3]);
         }
-        if (threadIdx.x < ne) {
-            const int pos = (base + e0 + threadIdx.x) % a.L;
-            bs[threadIdx.x] = a.ring_beta[((size_t)s * a.HV + hv) * a.L + pos];
-            gs[threadIdx.x] = a.ring_g[((size_t)s * a.HV + hv) * a.L + pos];
+        if (t < ne) {
+            const int pos = (base + e0 + t) % L;
+            bs[t] = a.ring_beta[((size_t)s * a.HV + hv) * L + pos];
+            gs[t] = a.ring_g[((size_t)s * a.HV + hv) * L + pos];
         }
         __syncthreads();
-        for (int e = 0; e < ne; ++e) {
-            const float4 k4 = *reinterpret_cast<const float4*>(ks + e * KD + lane * 4);
-            const float be = bs[e], ge = gs[e];
-            float part[kFoldRows];
+        for (int i = 0; i < ne; ++i) {
+            float4 k4[8];
 #pragma unroll
-            for (int j = 0; j < kFoldRows; ++j)
-                part[j] = S[j][0] * k4.x + S[j][1] * k4.y + S[j][2] * k4.z + S[j][3] * k4.w;
-            reduce_scatter<kFoldRows, 32>(part);  // lanes SH*i .. SH*i+SH-1 hold row i's sum
-            const int jr = lane / SH;
-            const float dmine = be * (vs[e * VB + warp + 4 * jr] - ge * part[0]);
+            for (int u = 0; u < 8; ++u)
+                k4[u] = *reinterpret_cast<const float4*>(ks + i * KD + (qd + 4 * u) * 4);
+            float p0 = 0.f, p1 = 0.f;
 #pragma unroll
-            for (int j = 0; j < kFoldRows; ++j) {
-                const float dj = __shfl_sync(0xffffffffu, dmine, SH * j);
-                S[j][0] = fmaf(ge, S[j][0], dj * k4.x);
-                S[j][1] = fmaf(ge, S[j][1], dj * k4.y);
-                S[j][2] = fmaf(ge, S[j][2], dj * k4.z);
-                S[j][3] = fmaf(ge, S[j][3], dj * k4.w);
+            for (int u = 0; u < 8; u += 2) {
+                p0 = fmaf(S[u][0], k4[u].x, p0); p0 = fmaf(S[u][1], k4[u].y, p0);
+                p0 = fmaf(S[u][2], k4[u].z, p0); p0 = fmaf(S[u][3], k4[u].w, p0);
+                p1 = fmaf(S[u + 1][0], k4[u + 1].x, p1); p1 = fmaf(S[u + 1][1], k4[u + 1].y, p1);
+                p1 = fmaf(S[u + 1][2], k4[u + 1].z, p1); p1 = fmaf(S[u + 1][3], k4[u + 1].w, p1);
+            }
+            float part = p0 + p1;
+            part += __shfl_xor_sync(kFull, part, 1);
+            part += __shfl_xor_sync(kFull, part, 2);
+            const float ge = gs[i];
+            const float dn = bs[i] * (vs[i * VB + r] - ge * part);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                S[u][0] = fmaf(ge, S[u][0], dn * k4[u].x);
+                S[u][1] = fmaf(ge, S[u][1], dn * k4[u].y);
+                S[u][2] = fmaf(ge, S[u][2], dn * k4[u].z);
+                S[u][3] = fmaf(ge, S[u][3], dn * k4[u].w);
             }
         }
     }
 #pragma unroll
-    for (int j = 0; j < kFoldRows; ++j)
-        *reinterpret_cast<float4*>(tile + (warp + 4 * j) * KD + lane * 4) =
-            make_float4(S[j][0], S[j][1], S[j][2], S[j][3]);
+    for (int u = 0; u < 8; ++u)
+        *reinterpret_cast<float4*>(tile + r * KD + (qd + 4 * u) * 4) =
+            make_float4(S[u][0], S[u][1], S[u][2], S[u][3]);
 }
 
-// ----------------------------------------------------------------------------
-// spec precompute (one CTA per row)
-// ----------------------------------------------------------------------------
-
-struct PreArgs {
-    const void* q;
-    const void* k;
-    const float* beta;
-    const float* g;
-    void* ring_k;
-    float* ring_g;
-    float* ring_beta;
-    const int32_t* ci;
-    const int32_t* slot_wp;
-    const int32_t* slot_base;
-    const uint8_t* slot_flush;
-    float* ws;
-    int32_t* dev_err;
-    int T, HV, HK, L, num_slots, act_bf16;
-};
-
-// One CTA per (row, key head): the dot products of every live key (history, then
-// drafts) with the drafts' keys and queries, the coefficient tables of the value
-// heads that read this key head, and the drafts' ring entries k (this key head),
-// g and beta (its value heads).
-__global__ void spec_pre_kernel(const PreArgs a) {
-    extern __shared__ __align__(16) float psm[];
-    const int b = blockIdx.x / a.HK, kh = blockIdx.x - (blockIdx.x / a.HK) * a.HK;
+// Tables of one (row, key head): the dot products of every live key (history,
+// then drafts) with the drafts' keys and queries, then, per value head of this
+// key head and draft j (m = history + j):
+//   ao_i = prod_{l=i+1..m} gate_l (k_i . q_j), i <= m
+//   au_i = prod_{l=i+1..m-1} gate_l (k_i . k_j), i < m
+//   Gu = prod_{l<m} gate_l, Go = prod_{l<=m} gate_l, beta_j, g_j.
+template <int T>
+__device__ void pre_head(const ProArgs& a, int idx, float* sm) {
+    constexpr int NV = 2 * T;
+    constexpr int NVP = NV <= 2 ? 2 : (NV <= 4 ? 4 : (NV <= 8 ? 8 : 16));
+    const int b = idx / a.HK, kh = idx - (idx / a.HK) * a.HK;
     const int s = a.ci[b];
     if (s < 0 || s >= a.num_slots) return;
-    const int T = a.T, L = a.L, HV = a.HV, HK = a.HK;
+    const int L = a.L, HV = a.HV, HK = a.HK;
     int c, base_eff;
     if (!history(a.slot_wp[s], a.slot_base[s], a.slot_flush[s], L, T, &c, &base_eff)) return;
-    const int nk = c + T;       // live keys: history then drafts
+    const int nk = c + T;  // live keys: history then drafts
     const int vpk = HV / HK;
-    float* KK = psm;            // [L][T]   k_i . k_j
-    float* KQ = KK + L * T;     // [L][T]   k_i . q_j
-    float* gts = KQ + L * T;    // [vpk][L] gate of every live entry (history, drafts)
-    const int sa = a.act_bf16 ? 2 : 4;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-    const char* kin = static_cast<const char*>(a.k);
-    const char* qin = static_cast<const char*>(a.q);
+    const bool bf = a.act_bf16;
+    const int sa = bf ? 2 : 4;
+    float* KK = sm;                                   // [L][T]   k_i . k_j
+    float* KQ = KK + L * T;                           // [L][T]   k_i . q_j
+    float* gts = KQ + L * T;                          // [vpk][L] gates of the live entries
+    float* kdq = sm + ((2 * L * T + vpk * L + 3) & ~3);  // [T][2][KD] drafts' k, q
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5, nwarps = blockDim.x >> 5;
 
-    // the drafts' keys and queries, 4 columns per lane, held in registers
-    float kd[kMaxT][4], qd[kMaxT][4];
-#pragma unroll
-    for (int j = 0; j < kMaxT; ++j) {
-        if (j < T) {
-            load4(kin + (((size_t)b * T + j) * HK + kh) * KD * sa, lane * 4, a.act_bf16, kd[j]);
-            load4(qin + (((size_t)b * T + j) * HK + kh) * KD * sa, lane * 4, a.act_bf16, qd[j]);
-        }
+    for (int e = t; e < NV * (KD / 4); e += blockDim.x) {
+        const int jv = e / (KD / 4), c4 = e - (e / (KD / 4)) * (KD / 4);
+        const int j = jv >> 1;
+        const void* src = (jv & 1) ? a.q : a.k;
+        float f[4];
+        load4(static_cast<const char*>(src) + (((size_t)b * T + j) * HK + kh) * KD * sa, c4 * 4, bf, f);
+        *reinterpret_cast<float4*>(kdq + jv * KD + c4 * 4) = make_float4(f[0], f[1], f[2], f[3]);
     }
-    for (int i = warp; i < nk; i += nwarps) {
-        float ki[4];
-        if (i < c) {
-            const int pos = (base_eff + i) % L;
-            load4(static_cast<const char*>(a.ring_k) + (((size_t)s * HK + kh) * L + pos) * KD * sa,
-                  lane * 4, a.act_bf16, ki);
-        } else {
-            ki[0] = kd[0][0]; ki[1] = kd[0][1]; ki[2] = kd[0][2]; ki[3] = kd[0][3];
-#pragma unroll
-            for (int j = 1; j < kMaxT; ++j)
-                if (j == i - c) { ki[0] = kd[j][0]; ki[1] = kd[j][1]; ki[2] = kd[j][2]; ki[3] = kd[j][3]; }
-        }
-#pragma unroll
-        for (int j = 0; j < kMaxT; ++j) {
-            if (j < T) {
-                float d1 = ki[0] * kd[j][0] + ki[1] * kd[j][1] + ki[2] * kd[j][2] + ki[3] * kd[j][3];
-                float d2 = ki[0] * qd[j][0] + ki[1] * qd[j][1] + ki[2] * qd[j][2] + ki[3] * qd[j][3];
-#pragma unroll
-                for (int o = 16; o >= 1; o >>= 1) {
-                    d1 += __shfl_xor_sync(0xffffffffu, d1, o);
-                    d2 += __shfl_xor_sync(0xffffffffu, d2, o);
-                }
-                if (lane == 0) {
-                    KK[i * T + j] = d1;
-                    KQ[i * T + j] = d2;
-                }
-            }
-        }
-    }
-    // gates of the live entries of this key head's value heads, staged once
-    for (int x = threadIdx.x; x < vpk * nk; x += blockDim.x) {
+    for (int x = t; x < vpk * nk; x += blockDim.x) {
         const int hl = x / nk, m = x - (x / nk) * nk, hv = kh * vpk + hl;
         gts[hl * L + m] = m < c ? a.ring_g[((size_t)s * HV + hv) * L + (base_eff + m) % L]
                                 : a.g[((size_t)b * T + (m - c)) * HV + hv];
     }
-    // the drafts' S-independent ring entries
-    const int kc = KD * sa / 16;
-    for (int x = threadIdx.x; x < T * kc; x += blockDim.x) {
-        const int j = x / kc, part = x - (x / kc) * kc;
-        const int pos = (base_eff + c + j) % L;
-        reinterpret_cast<uint4*>(static_cast<char*>(a.ring_k) + (((size_t)s * HK + kh) * L + pos) * KD * sa)[part] =
-            reinterpret_cast<const uint4*>(kin + (((size_t)b * T + j) * HK + kh) * KD * sa)[part];
-    }
-    for (int x = threadIdx.x; x < T * vpk; x += blockDim.x) {
-        const int j = x / vpk, hv = kh * vpk + (x - (x / vpk) * vpk);
-        const int pos = (base_eff + c + j) % L;
-        a.ring_g[((size_t)s * HV + hv) * L + pos] = a.g[((size_t)b * T + j) * HV + hv];
-        a.ring_beta[((size_t)s * HV + hv) * L + pos] = a.beta[((size_t)b * T + j) * HV + hv];
+    __syncthreads();
+
+    // a warp per live key: lane holds 4 columns; the 2T dots reduce with one
+    // reduce-scatter (entry 2j: k_i . k_j, entry 2j+1: k_i . q_j)
+    const char* kr = static_cast<const char*>(a.ring_k) + ((size_t)s * HK + kh) * L * KD * sa;
+    for (int i = warp; i < nk; i += nwarps) {
+        float ki[4];
+        if (i < c) {
+            load4(kr + (size_t)((base_eff + i) % L) * KD * sa, lane * 4, bf, ki);
+        } else {
+            const float4 v = *reinterpret_cast<const float4*>(kdq + (2 * (i - c)) * KD + lane * 4);
+            ki[0] = v.x; ki[1] = v.y; ki[2] = v.z; ki[3] = v.w;
+        }
+        float part[NVP];
+#pragma unroll
+        for (int d = 0; d < NVP; ++d) {
+            part[d] = 0.f;
+            if (d < NV) {
+                const float4 v = *reinterpret_cast<const float4*>(kdq + d * KD + lane * 4);
+                part[d] = ki[0] * v.x + ki[1] * v.y + ki[2] * v.z + ki[3] * v.w;
+            }
+        }
+        const int e = reduce_scatter<NVP, 32>(part);
+        if ((lane & (32 / NVP - 1)) == 0 && e < NV) {
+            if (e & 1) KQ[i * T + (e >> 1)] = part[0];
+            else KK[i * T + (e >> 1)] = part[0];
+        }
     }
     __syncthreads();
 
-    // coefficient table per (value head of this key head, draft)
     const int TB = tbl_floats(L, T);
-    for (int x = threadIdx.x; x < vpk * T; x += blockDim.x) {
+    for (int x = t; x < vpk * T; x += blockDim.x) {
         const int hl = x / T, j = x - (x / T) * T, hv = kh * vpk + hl;
-        float* t = a.ws + ((size_t)b * HV + hv) * TB;
+        float* tb = a.ws + ((size_t)b * HV + hv) * TB;
         const float* gl = gts + hl * L;
         const int m = c + j;
-        float* au = t + j * L;
-        float* ao = t + T * L + j * L;
-        // ao_i = prod_{l=i+1..m} gate_l * (k_i . q_j), i <= m
-        // au_i = prod_{l=i+1..m-1} gate_l * (k_i . k_j), i < m
+        float* au = tb + j * L;
+        float* ao = tb + T * L + j * L;
         float pq = 1.f, pk = 1.f;
         for (int i = m; i >= 0; --i) {
             ao[i] = pq * KQ[i * T + j];
@@ -281,29 +275,38 @@ __global__ void spec_pre_kernel(const PreArgs a) {
             au[i] = 0.f;
         }
         if (m < L) au[m] = 0.f;
-        // pk = prod_{l<m} gate_l (Gu), pq = prod_{l<=m} gate_l (Go)
-        t[2 * T * L + j] = pk;
-        t[2 * T * L + T + j] = pq;
-        t[2 * T * L + 2 * T + j] = a.beta[((size_t)b * T + j) * HV + hv];
-        t[2 * T * L + 3 * T + j] = a.g[((size_t)b * T + j) * HV + hv];
+        tb[2 * T * L + j] = pk;
+        tb[2 * T * L + T + j] = pq;
+        tb[2 * T * L + 2 * T + j] = a.beta[((size_t)b * T + j) * HV + hv];
+        tb[2 * T * L + 3 * T + j] = a.g[((size_t)b * T + j) * HV + hv];
         if (j == 0) {
-            t[2 * T * L + 4 * T] = __int_as_float(c);
-            t[2 * T * L + 4 * T + 1] = __int_as_float(base_eff);
+            tb[2 * T * L + 4 * T] = __int_as_float(c);
+            tb[2 * T * L + 4 * T + 1] = __int_as_float(base_eff);
         }
     }
 }
 
+template <int T>
+__global__ void __launch_bounds__(kThreads) prologue_kernel(const ProArgs a) {
+    extern __shared__ __align__(16) float psm[];
+    if ((int)blockIdx.x < a.n_fold) fold_tile(a, blockIdx.x, psm);
+    else pre_head<T>(a, blockIdx.x - a.n_fold, psm);
+}
+
 // ----------------------------------------------------------------------------
-// verify (warp-specialised pipeline, one consumer warp per tile)
+// verify (warp-specialised pipeline, two consumer warps per tile)
 // ----------------------------------------------------------------------------
 
 constexpr int kGroupWarps = 2;
-constexpr int RW = VB / kGroupWarps;              // value rows per warp
-constexpr int kWarpScratch = 3 * kMaxT * RW * 4;  // W [2T][RW] S0 dots, Dd [T][RW] draft d
+constexpr int RW = VB / kGroupWarps;          // value rows per warp
+constexpr int kWarpScratch = 2 * kMaxT * RW * 4;  // W [2T][RW]: S0 . k_j, S0 . q_j
 
-template <int DP>
+template <int T>
 struct VerPolicy {
     static constexpr int kGroup = kGroupWarps;
+    static constexpr int NV = 2 * T;  // vectors k_0, q_0, k_1, q_1, ...
+    static constexpr int NG = (NV + 7) / 8;
+    static constexpr int NVP = NV <= 2 ? 2 : (NV <= 4 ? 4 : 8);
     struct Args {
         const float* state;
         const void* q;
@@ -311,6 +314,9 @@ struct VerPolicy {
         const void* v;
         float* ring_d;
         void* ring_v;
+        void* ring_k;
+        float* ring_g;
+        float* ring_beta;
         const int32_t* ci;
         const int32_t* slot_wp;
         const int32_t* slot_base;
@@ -318,7 +324,7 @@ struct VerPolicy {
         const float* ws;
         void* o;
         int32_t* dev_err;
-        int batch, T, HV, HK, V, L, num_slots, act_bf16, out_bf16;
+        int batch, HV, HK, V, L, num_slots, act_bf16, out_bf16;
         int stages, stage_bytes, stage_off, scratch_off, warp_scratch;
         int off_kq, off_v, off_d, off_tbl;
     };
@@ -334,7 +340,7 @@ struct VerPolicy {
         const int s = a.ci[b];
         int c = 0, be = 0;
         if (s >= 0 && s < a.num_slots) {
-            if (!history(a.slot_wp[s], a.slot_base[s], a.slot_flush[s], a.L, a.T, &c, &be)) c = -1;
+            if (!history(a.slot_wp[s], a.slot_base[s], a.slot_flush[s], a.L, T, &c, &be)) c = -1;
         }
         return make_int4(s, c, be, b);
     }
@@ -357,7 +363,7 @@ struct VerPolicy {
             mbar_arrive_plain(full);
             return;
         }
-        const int T = a.T, L = a.L;
+        const int L = a.L;
         const int sa = a.act_bf16 ? 2 : 4;
         const int kh = hv / (a.HV / a.HK);
         const int TB = tbl_floats(L, T);
@@ -385,71 +391,128 @@ struct VerPolicy {
     static __device__ void consume(const Args& a, int, const Meta& m, const uint8_t* sb,
                                    uint8_t* scratch, int lane, int wi) {
         if (!m.valid) return;
-        constexpr int RC = 32 / DP;  // value rows per reduce-scatter
         const bool bf = a.act_bf16;
         const int sa = bf ? 2 : 4;
-        const int T = a.T, L = a.L, c = m.c;
-        const int rbase = wi * RW;
-        const float* tile = reinterpret_cast<const float*>(sb);
+        const int L = a.L, c = m.c;
+        const float* tw = reinterpret_cast<const float*>(sb) + wi * RW * KD;  // this warp's rows
         const uint8_t* kq = sb + a.off_kq;
         float* W = reinterpret_cast<float*>(scratch);  // [2T][RW]
-        float* Dd = W + 2 * kMaxT * RW;                // [T][RW]
-        // phase A: S0 . k_j and S0 . q_j for this warp's value rows
-        float vec[DP][4];
+
+        // phase A: W[d][row] = S0_row . vec_d. Lane (rg, cg) = (lane/8, lane%8) owns
+        // rows rg + 4i (i < 4) and the 4-column chunks at cg*4 + 32u (u < 4): within
+        // each quarter-warp the 16-byte shared loads touch 32 distinct banks, and the
+        // sums reduce across the 8 lanes of a row group.
+        const int cg = lane & 7, rg = lane >> 3;
 #pragma unroll
-        for (int d = 0; d < DP; ++d) {
-            if (d < 2 * T) {
-                load4(kq + (size_t)d * KD * sa, lane * 4, bf, vec[d]);
-            } else {
-                vec[d][0] = vec[d][1] = vec[d][2] = vec[d][3] = 0.f;
+        for (int g8 = 0; g8 < NG; ++g8) {
+            float acc[4][NVP];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+#pragma unroll
+                for (int d = 0; d < NVP; ++d) acc[i][d] = 0.f;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int col = cg * 4 + 32 * u;
+                float vv[NVP][4];
+#pragma unroll
+                for (int d = 0; d < NVP; ++d) {
+                    if (g8 * 8 + d < NV) load4(kq + (size_t)(g8 * 8 + d) * KD * sa, col, bf, vv[d]);
+                }
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const float4 s4 = *reinterpret_cast<const float4*>(tw + (rg + 4 * i) * KD + col);
+#pragma unroll
+                    for (int d = 0; d < NVP; ++d) {
+                        if (g8 * 8 + d < NV) {
+                            float x = acc[i][d];
+                            x = fmaf(s4.x, vv[d][0], x);
+                            x = fmaf(s4.y, vv[d][1], x);
+                            x = fmaf(s4.z, vv[d][2], x);
+                            x = fmaf(s4.w, vv[d][3], x);
+                            acc[i][d] = x;
+                        }
+                    }
+                }
             }
-        }
-#pragma unroll 1
-        for (int ch = 0; ch < RW / RC; ++ch) {
-            float part[32];
 #pragma unroll
-            for (int jr = 0; jr < RC; ++jr) {
-                const float4 s4 =
-                    *reinterpret_cast<const float4*>(tile + (rbase + ch * RC + jr) * KD + lane * 4);
-#pragma unroll
-                for (int d = 0; d < DP; ++d)
-                    part[jr * DP + d] =
-                        s4.x * vec[d][0] + s4.y * vec[d][1] + s4.z * vec[d][2] + s4.w * vec[d][3];
+            for (int i = 0; i < 4; ++i) {
+                const int e = g8 * 8 + reduce_scatter<NVP, 8>(acc[i]);
+                if ((cg & (8 / NVP - 1)) == 0 && e < NV) W[e * RW + rg + 4 * i] = acc[i][0];
             }
-            reduce_scatter<32, 32>(part);  // lane l holds entry l
-            const int jr = lane / DP, d = lane % DP;
-            if (d < 2 * T) W[d * RW + ch * RC + jr] = part[0];
         }
         __syncwarp();
-        // phase B: the draft chain, one value row per lane
-        const float* t = reinterpret_cast<const float*>(sb + a.off_tbl);
+
+        // phase B: the draft chain. Lanes r and r+16 share value row r of this warp:
+        // each sums half of the history (even / odd entries), then both run the
+        // chain; the low lane stores o, the high lane the drafts' d and raw v.
+        const float* tb = reinterpret_cast<const float*>(sb + a.off_tbl);
         const float* dh = reinterpret_cast<const float*>(sb + a.off_d);
-        const int r = rbase + lane;
-        const size_t vi = (size_t)m.vb * VB + r;
-        for (int j = 0; j < T && lane < RW; ++j) {
-            const float* au = t + j * L;
-            const float* ao = t + T * L + j * L;
-            const int mm = c + j;
-            float u = t[2 * T * L + j] * W[(2 * j) * RW + lane];
-            float oo = t[2 * T * L + T + j] * W[(2 * j + 1) * RW + lane];
-            for (int i = 0; i < c; ++i) {
-                const float di = dh[i * VB + r];
-                u = fmaf(au[i], di, u);
-                oo = fmaf(ao[i], di, oo);
+        const int r = lane & 15, h = lane >> 4;
+        const int rr = wi * RW + r;  // row within the tile
+        const size_t vi = (size_t)m.vb * VB + rr;
+        float hu[T], ho[T];
+#pragma unroll
+        for (int j = 0; j < T; ++j) hu[j] = ho[j] = 0.f;
+        for (int i = h; i < c; i += 2) {
+            const float di = dh[i * VB + rr];
+#pragma unroll
+            for (int j = 0; j < T; ++j) {
+                hu[j] = fmaf(tb[j * L + i], di, hu[j]);
+                ho[j] = fmaf(tb[T * L + j * L + i], di, ho[j]);
             }
-            for (int i = c; i < mm; ++i) {
-                const float di = Dd[(i - c) * RW + lane];
-                u = fmaf(au[i], di, u);
-                oo = fmaf(ao[i], di, oo);
+        }
+#pragma unroll
+        for (int j = 0; j < T; ++j) {
+            hu[j] += __shfl_xor_sync(kFull, hu[j], 16);
+            ho[j] += __shfl_xor_sync(kFull, ho[j], 16);
+        }
+        const float* ex = tb + 2 * T * L;  // Gu[T], Go[T], beta[T], g[T]
+        float dd[T];
+#pragma unroll
+        for (int j = 0; j < T; ++j) {
+            const float* au = tb + j * L + c;          // au over the drafts' entries
+            const float* ao = tb + T * L + j * L + c;
+            float u = fmaf(ex[j], W[(2 * j) * RW + r], hu[j]);
+            float oo = fmaf(ex[T + j], W[(2 * j + 1) * RW + r], ho[j]);
+#pragma unroll
+            for (int jj = 0; jj < j; ++jj) {
+                u = fmaf(au[jj], dd[jj], u);
+                oo = fmaf(ao[jj], dd[jj], oo);
             }
-            const float vr = load1(sb + a.off_v + j * VB * sa, r, bf);
-            const float dn = t[2 * T * L + 2 * T + j] * (vr - t[2 * T * L + 3 * T + j] * u);
-            Dd[j * RW + lane] = dn;
-            oo = fmaf(ao[mm], dn, oo);
+            const float vr = load1(sb + a.off_v + j * VB * sa, rr, bf);
+            const float dn = ex[2 * T + j] * (vr - ex[3 * T + j] * u);
+            dd[j] = dn;
+            oo = fmaf(ao[j], dn, oo);
             const int pos = (m.base_eff + c + j) % L;
-            store1(a.o, (((size_t)m.b * T + j) * a.HV + m.hv) * a.V + vi, a.out_bf16, oo);
-            a.ring_d[((((size_t)m.s * a.HV + m.hv) * (a.V / VB) + m.vb) * L + pos) * VB + r] = dn;
-            store1(a.ring_v, (((size_t)m.s * a.HV + m.hv) * L + pos) * a.V + vi, bf, vr);
+            if (h == 0) {
+                store1(a.o, (((size_t)m.b * T + j) * a.HV + m.hv) * a.V + vi, a.out_bf16, oo);
+            } else {
+                a.ring_d[((((size_t)m.s * a.HV + m.hv) * (a.V / VB) + m.vb) * L + pos) * VB + rr] = dn;
+                store1(a.ring_v, (((size_t)m.s * a.HV + m.hv) * L + pos) * a.V + vi, bf, vr);
+            }
+        }
+
+        // the drafts' g and beta (first tile of each value head) and k (first tile
+        // of the first value head of each key head) into the ring
+        if (wi == 0 && m.vb == 0) {
+            const int pos0 = m.base_eff + c;
+            if (lane < T) {
+                const int pos = (pos0 + lane) % L;
+                a.ring_g[((size_t)m.s * a.HV + m.hv) * L + pos] = ex[3 * T + lane];
+                a.ring_beta[((size_t)m.s * a.HV + m.hv) * L + pos] = ex[2 * T + lane];
+            }
+            const int vpk = a.HV / a.HK;
+            if (m.hv % vpk == 0) {
+                const int kh = m.hv / vpk;
+                const int kc = KD * sa / 16;
+                for (int x = lane; x < T * kc; x += 32) {
+                    const int j = x / kc, part = x - (x / kc) * kc;
+                    const int pos = (pos0 + j) % L;
+                    reinterpret_cast<uint4*>(static_cast<char*>(a.ring_k) +
+                                             (((size_t)m.s * a.HK + kh) * L + pos) * KD * sa)[part] =
+                        reinterpret_cast<const uint4*>(kq + (size_t)(2 * j) * KD * sa)[part];
+                }
+            }
         }
         __syncwarp();
     }
@@ -459,6 +522,64 @@ struct VerPolicy {
 }  // namespace rssm
 
 using namespace rssm;
+
+namespace {
+
+template <int T>
+int spec_launch(const rssm_gdn_dims* d, float* state, const void* q, const void* k, const void* v,
+                const float* beta, const float* g, float* ring_d, void* ring_k, float* ring_g,
+                void* ring_v, float* ring_beta, const int32_t* cache_indices,
+                const int32_t* slot_wp, const int32_t* slot_base, const uint8_t* slot_flush,
+                void* workspace, void* o, int32_t* dev_err, cudaStream_t st) {
+    DeviceInfo di;
+    if (!device_info(&di)) return RSSM_ERR_CUDA;
+    const int HV = d->num_v_heads, HK = d->num_k_heads, V = d->head_v_dim, L = d->ring_len;
+    const int NVB = V / spec::VB;
+    const bool abf = d->act_dtype == RSSM_BF16;
+    const int sa = abf ? 2 : 4;
+
+    // 1. exact fold of slots with a pending fold, and the tables
+    int psm = spec::pre_smem_floats(L, T, HV / HK);
+    if (psm < spec::fold_smem_floats()) psm = spec::fold_smem_floats();
+    const int psmem = psm * 4;
+    if (psmem > di.max_smem_optin) return RSSM_ERR_UNSUPPORTED;
+    if (psmem > 48 * 1024 &&
+        !ensure_smem_limit(reinterpret_cast<const void*>(spec::prologue_kernel<T>), psmem))
+        return RSSM_ERR_CUDA;
+    spec::ProArgs pa{};
+    pa.state = state; pa.q = q; pa.k = k; pa.beta = beta; pa.g = g; pa.ring_k = ring_k;
+    pa.ring_v = ring_v; pa.ring_g = ring_g; pa.ring_beta = ring_beta; pa.ci = cache_indices;
+    pa.slot_wp = slot_wp; pa.slot_base = slot_base; pa.slot_flush = slot_flush;
+    pa.ws = static_cast<float*>(workspace);
+    pa.T = T; pa.HV = HV; pa.HK = HK; pa.V = V; pa.L = L; pa.num_slots = d->num_slots;
+    pa.act_bf16 = abf;
+    pa.n_fold = d->batch * HV * NVB;
+    const long blocks = (long)pa.n_fold + (long)d->batch * HK;
+    spec::prologue_kernel<T><<<(unsigned)blocks, spec::kThreads, psmem, st>>>(pa);
+    if (launch_status()) return RSSM_ERR_CUDA;
+
+    // 2. verify
+    const int TBs = spec::tbl_floats(L, T);
+    int off = spec::TILE;
+    const int off_kq = off; off += 2 * T * spec::KD * sa;
+    const int off_v = off;  off += T * spec::VB * sa;
+    const int off_d = off;  off += L * spec::VB * 4;
+    const int off_tbl = off; off += TBs * 4;
+    const int stage_bytes = (off + 127) & ~127;
+    typename spec::VerPolicy<T>::Args va{};
+    va.state = state; va.q = q; va.k = k; va.v = v; va.ring_d = ring_d; va.ring_v = ring_v;
+    va.ring_k = ring_k; va.ring_g = ring_g; va.ring_beta = ring_beta;
+    va.ci = cache_indices; va.slot_wp = slot_wp; va.slot_base = slot_base;
+    va.slot_flush = slot_flush; va.ws = static_cast<const float*>(workspace); va.o = o;
+    va.dev_err = dev_err; va.batch = d->batch; va.HV = HV; va.HK = HK; va.V = V;
+    va.L = L; va.num_slots = d->num_slots; va.act_bf16 = abf;
+    va.out_bf16 = d->out_dtype == RSSM_BF16;
+    va.off_kq = off_kq; va.off_v = off_v; va.off_d = off_d; va.off_tbl = off_tbl;
+    return launch_pipe<spec::VerPolicy<T>>(va, stage_bytes, spec::kWarpScratch, spec::TILE,
+                                           (long)d->batch * HV * NVB, st);
+}
+
+}  // namespace
 
 extern "C" size_t rssm_gdn_spec_workspace_size(const rssm_gdn_dims* d, int32_t T) {
     if (!d || d->batch < 0 || d->num_v_heads <= 0 || d->ring_len < 1 || T < 1 || T > spec::kMaxT)
@@ -489,66 +610,23 @@ extern "C" int rssm_gdn_spec_verify(const rssm_gdn_dims* d, int32_t T, float* st
         !ok_ptr(slot_flush) || !ok_ptr(workspace) || !ok_ptr(o))
         return RSSM_ERR_INVALID_ARG;
     if (workspace_bytes < rssm_gdn_spec_workspace_size(d, T)) return RSSM_ERR_INVALID_ARG;
-    DeviceInfo di;
-    if (!device_info(&di)) return RSSM_ERR_CUDA;
     cudaStream_t st = (cudaStream_t)stream;
-    const int HV = d->num_v_heads, HK = d->num_k_heads, V = d->head_v_dim, L = d->ring_len;
-    const int NVB = V / spec::VB;
-    const bool abf = d->act_dtype == RSSM_BF16;
-    const int sa = abf ? 2 : 4;
-
-    // 1. exact fold of slots with a pending fold
-    spec::FoldArgs fa{state, ring_k, ring_v, ring_g, ring_beta, cache_indices, slot_wp, slot_base,
-                      slot_flush, dev_err, HV, HK, V, L, d->num_slots, abf};
-    spec::fold_kernel<<<d->batch * HV * NVB, spec::kThreads, 0, st>>>(fa);
-    if (launch_status()) return RSSM_ERR_CUDA;
-
-    // 2. precompute: key dots, gate products, S-independent ring entries
-    const int psmem = (2 * L * T + (HV / HK) * L) * 4;
-    if (psmem > di.max_smem_optin) return RSSM_ERR_UNSUPPORTED;
-    if (psmem > 48 * 1024 &&
-        !ensure_smem_limit(reinterpret_cast<const void*>(spec::spec_pre_kernel), psmem))
-        return RSSM_ERR_CUDA;
-    spec::PreArgs pa{q, k, beta, g, ring_k, ring_g, ring_beta, cache_indices, slot_wp, slot_base,
-                     slot_flush, static_cast<float*>(workspace), dev_err, T, HV, HK, L,
-                     d->num_slots, abf};
-    spec::spec_pre_kernel<<<d->batch * HK, 128, psmem, st>>>(pa);
-    if (launch_status()) return RSSM_ERR_CUDA;
-
-    // 3. verify
-    const int TBs = spec::tbl_floats(L, T);
-    int off = spec::TILE;
-    const int off_kq = off; off += 2 * T * spec::KD * sa;
-    const int off_v = off;  off += T * spec::VB * sa;
-    const int off_d = off;  off += L * spec::VB * 4;
-    const int off_tbl = off; off += TBs * 4;
-    const int stage_bytes = (off + 127) & ~127;
-    const long items = (long)d->batch * HV * NVB;
-    auto fill = [&](auto& va) {
-        va.state = state; va.q = q; va.k = k; va.v = v; va.ring_d = ring_d; va.ring_v = ring_v;
-        va.ci = cache_indices; va.slot_wp = slot_wp; va.slot_base = slot_base;
-        va.slot_flush = slot_flush; va.ws = static_cast<const float*>(workspace); va.o = o;
-        va.dev_err = dev_err; va.batch = d->batch; va.T = T; va.HV = HV; va.HK = HK; va.V = V;
-        va.L = L; va.num_slots = d->num_slots; va.act_bf16 = abf;
-        va.out_bf16 = d->out_dtype == RSSM_BF16;
-        va.off_kq = off_kq; va.off_v = off_v; va.off_d = off_d; va.off_tbl = off_tbl;
-    };
-    if (T <= 1) {
-        spec::VerPolicy<2>::Args va{};
-        fill(va);
-        return launch_pipe<spec::VerPolicy<2>>(va, stage_bytes, spec::kWarpScratch, spec::TILE, items, st);
+#define RSSM_SPEC_CASE(TT)                                                                        \
+    case TT:                                                                                      \
+        return spec_launch<TT>(d, state, q, k, v, beta, g, ring_d, ring_k, ring_g, ring_v,        \
+                               ring_beta, cache_indices, slot_wp, slot_base, slot_flush,          \
+                               workspace, o, dev_err, st);
+    switch (T) {
+        RSSM_SPEC_CASE(1)
+        RSSM_SPEC_CASE(2)
+        RSSM_SPEC_CASE(3)
+        RSSM_SPEC_CASE(4)
+        RSSM_SPEC_CASE(5)
+        RSSM_SPEC_CASE(6)
+        RSSM_SPEC_CASE(7)
+        RSSM_SPEC_CASE(8)
+        default:
+            return RSSM_ERR_UNSUPPORTED;
     }
-    if (T <= 2) {
-        spec::VerPolicy<4>::Args va{};
-        fill(va);
-        return launch_pipe<spec::VerPolicy<4>>(va, stage_bytes, spec::kWarpScratch, spec::TILE, items, st);
-    }
-    if (T <= 4) {
-        spec::VerPolicy<8>::Args va{};
-        fill(va);
-        return launch_pipe<spec::VerPolicy<8>>(va, stage_bytes, spec::kWarpScratch, spec::TILE, items, st);
-    }
-    spec::VerPolicy<16>::Args va{};
-    fill(va);
-    return launch_pipe<spec::VerPolicy<16>>(va, stage_bytes, spec::kWarpScratch, spec::TILE, items, st);
+#undef RSSM_SPEC_CASE
 }

@@ -116,7 +116,7 @@ def test_spec_small_all_rows():
     _check_spec(wl, rows=np.arange(5), rounds=16)
 
 
-@pytest.mark.parametrize("T,L", [(1, 2), (2, 5), (3, 8), (8, 16)])
+@pytest.mark.parametrize("T,L", [(1, 2), (2, 5), (3, 8), (5, 10), (6, 13), (7, 15), (8, 16)])
 def test_spec_draft_lengths(T, L):
     wl = W.gdn_spec(batch=4, num_v_heads=2, num_k_heads=1, num_slots=8, L=L, T=T, rounds=12,
                     act_dtype="fp32")
