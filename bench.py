@@ -239,7 +239,7 @@ def traffic_record(kernel_src, profile):
             rec[k.strip().strip("-* `")] = v.strip().strip("`")
     if rec.get("source_sha256") == sha and rec.get("traffic_bytes_per_launch"):
         return int(float(rec["traffic_bytes_per_launch"]))
-    return None
+    return None  # no summary, or the kernel source changed since the counters were taken
 
 
 def gdn_output_bytes(wl, row_wp, row_flush, out_bytes=2):

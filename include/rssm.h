@@ -439,6 +439,38 @@ int rssm_gdn_spec_verify(const rssm_gdn_dims* dims, int32_t T, float* state, con
                          size_t workspace_bytes, void* o, int32_t* dev_err,
                          rssm_stream_t stream);
 
+/* ------------------------------------------------------------------------- */
+
+/* rssm_mamba2_materialize_state -- test / debug: the current recurrent state of the
+ * dims->batch slots listed in slots[] (negative entries skipped), folded from the
+ * checkpoint and the slot's live ring entries 0..c-1 (c = slot_wp[s], the entries
+ * written since the last flush) into out [batch][H][P][N] float32, without
+ * touching the pool, the rings or the cursors ([M2] 实现拆解 item 1: a flush
+ * stores exactly this state):
+ *   S = P S0 + sum_{i<c} P_i dt_i x_i B_i^T,  P_i = exp(A_h sum_{i<j<c} dt_j),
+ *   P = exp(A_h sum_{j<c} dt_j).
+ * Accumulates in fp32 from the stored (possibly bf16) checkpoint; the result is not
+ * rounded. Slot or cursor out of range: skipped and flagged in dev_err. Not on the
+ * decode path (plain loads, one CTA per (slot, head)). */
+int rssm_mamba2_materialize_state(const rssm_mamba2_dims* dims, const void* state,
+                                  const float* A, const void* ring_x, const float* ring_dt,
+                                  const void* ring_B, const int32_t* slots,
+                                  const int32_t* slot_wp, float* out, int32_t* dev_err,
+                                  rssm_stream_t stream);
+
+/* rssm_gdn_materialize_state -- test / debug: the GDN counterpart. The live entries
+ * of slot s are c = slot_wp[s] entries at ring positions (base + i) % L with base =
+ * slot_base[s] (slot_base NULL: base 0, the decode ring; the spec ring passes its
+ * cache_base, and a pending fold's entries are included) ([GDN] 实现拆解 item 1;
+ * [SPEC] 实现拆解 item 2):
+ *   S = G S0 + sum_{i<c} Gamma_i d_i k_i^T,  Gamma_i = prod_{i<j<c} g_j,
+ *   G = prod_{j<c} g_j,
+ * into out [batch][HV][V][K] float32. Errors as rssm_mamba2_materialize_state. */
+int rssm_gdn_materialize_state(const rssm_gdn_dims* dims, const float* state, const void* ring_k,
+                               const float* ring_g, const float* ring_d, const int32_t* slots,
+                               const int32_t* slot_wp, const int32_t* slot_base, float* out,
+                               int32_t* dev_err, rssm_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

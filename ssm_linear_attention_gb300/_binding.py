@@ -26,6 +26,7 @@ EXPORTS = (
     "rssm_gdn_workspace_size", "rssm_gdn_precompute", "rssm_gdn_output", "rssm_gdn_decode",
     "rssm_gdn_prepare", "rssm_gdn_step",
     "rssm_gdn_full_state_decode", "rssm_gdn_spec_workspace_size", "rssm_gdn_spec_verify",
+    "rssm_mamba2_materialize_state", "rssm_gdn_materialize_state",
 )
 
 
@@ -93,6 +94,10 @@ def _declare(L):
         "rssm_gdn_full_state_decode": (_I, [gd, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                             _VP]),
         "rssm_gdn_spec_workspace_size": (_SZ, [gd, _I32]),
+        "rssm_mamba2_materialize_state": (_I, [m2, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                               _VP]),
+        "rssm_gdn_materialize_state": (_I, [gd, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                            _VP]),
         "rssm_gdn_spec_verify": (_I, [gd, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                       _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _VP, _VP]),
     }
@@ -293,3 +298,17 @@ def rssm_gdn_spec_verify(dims, T, state, q, k, v, beta, g, ring_d, ring_k, ring_
           _ptr(beta), _ptr(g), _ptr(ring_d), _ptr(ring_k), _ptr(ring_g), _ptr(ring_v),
           _ptr(ring_beta), _ptr(cache_indices), _ptr(slot_wp), _ptr(slot_base), _ptr(slot_flush),
           _ptr(workspace), workspace_bytes, _ptr(o), _ptr(dev_err), _stream(stream))
+
+
+def rssm_mamba2_materialize_state(dims, state, A, ring_x, ring_dt, ring_B, slots, slot_wp, out,
+                                  dev_err=None, stream=None):
+    _call("rssm_mamba2_materialize_state", ctypes.byref(dims), _ptr(state), _ptr(A), _ptr(ring_x),
+          _ptr(ring_dt), _ptr(ring_B), _ptr(slots), _ptr(slot_wp), _ptr(out), _ptr(dev_err),
+          _stream(stream))
+
+
+def rssm_gdn_materialize_state(dims, state, ring_k, ring_g, ring_d, slots, slot_wp, slot_base,
+                               out, dev_err=None, stream=None):
+    _call("rssm_gdn_materialize_state", ctypes.byref(dims), _ptr(state), _ptr(ring_k),
+          _ptr(ring_g), _ptr(ring_d), _ptr(slots), _ptr(slot_wp), _ptr(slot_base), _ptr(out),
+          _ptr(dev_err), _stream(stream))

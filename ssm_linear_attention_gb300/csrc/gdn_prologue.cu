@@ -37,53 +37,58 @@ struct RowArgs {
     float* ws;           // [batch][HV][TBL]
 };
 
-// Entry w of slot s's rings <- row b's k and g.
-__device__ void append_row(const RowArgs& a, int b, int s, int w) {
-    const int HV = a.HV, HK = a.HK, L = a.L;
+// Entry w of slot s's rings <- row b's k (key heads [k0, k1)) and g (their value
+// heads).
+__device__ void append_heads(const RowArgs& a, int b, int s, int w, int k0, int k1) {
+    const int HV = a.HV, HK = a.HK, L = a.L, vpk = HV / HK;
     const int sa = a.act_bf16 ? 2 : 4;
     const int kc = KD * sa / 16;
-    const uint4* ks =
-        reinterpret_cast<const uint4*>(static_cast<const char*>(a.k) + (size_t)b * HK * KD * sa);
-    for (int c = threadIdx.x; c < HK * kc; c += blockDim.x) {
-        const int kh = c / kc, j = c % kc;
+    const uint4* ks = reinterpret_cast<const uint4*>(static_cast<const char*>(a.k) +
+                                                     ((size_t)b * HK + k0) * KD * sa);
+    for (int c = threadIdx.x; c < (k1 - k0) * kc; c += blockDim.x) {
+        const int kh = k0 + c / kc, j = c % kc;
         reinterpret_cast<uint4*>(static_cast<char*>(a.ring_k) +
                                  (((size_t)s * HK + kh) * L + w) * KD * sa)[j] = ks[c];
     }
-    for (int hv = threadIdx.x; hv < HV; hv += blockDim.x)
+    for (int hv = k0 * vpk + threadIdx.x; hv < k1 * vpk; hv += blockDim.x)
         a.ring_g[((size_t)s * HV + hv) * L + w] = a.g[(size_t)b * HV + hv];
 }
 
-// Shared memory of precompute_row, in bytes.
-__host__ __device__ inline int precompute_smem(int HV, int HK, int L) {
-    return (((2 * HK * L + HK + 3) & ~3) + HV * tbl_floats(L) + HV * L) * 4;
+// Shared memory of precompute_heads for nk key heads and nv value heads, in bytes.
+__host__ __device__ inline int precompute_smem(int nv, int nk, int L) {
+    return (((2 * nk * L + nk + 3) & ~3) + nv * tbl_floats(L) + nv * L) * 4;
 }
 
-// Row b's tables from ring entries 0..w-1 (k, g) and the step's q, k, beta, g.
-// A warp per key head: lanes hold 4 key columns of k_t and q_t, and each ring key
-// k_i (i < w) is read with one coalesced warp load; the two dot products reduce
-// with a butterfly. Then per value head (key head kh = hv / (HV/HK)):
+// Row b's tables for the key heads [k0, k1) and their value heads, from ring
+// entries 0..w-1 (k, g) and the step's q, k, beta, g. A warp per key head: lanes
+// hold 4 key columns of k_t and q_t, and each ring key k_i (i < w) is read with
+// one coalesced warp load; the two dot products reduce with a butterfly. Then per
+// value head (key head kh = hv / (HV/HK)):
 //   gamma_i = prod_{j=i+1..w-1} g_j, Gamma_i = g_t gamma_i,
 //   t[i] = gamma_i (k_i . k_t), t[L+i] = Gamma_i (k_i . q_t), t[2L+i] = Gamma_i
 //   (Gamma_w = 1), Gu = gamma_{-1}, Go = g_t Gu, k_t . q_t, beta_t, g_t.
 // The ring entries read are never the one appended this step, so the fused
-// kernel needs no ordering between the append and these loads.
-__device__ void precompute_row(const RowArgs& a, int b, int s, int w, float* psm) {
-    const int HV = a.HV, HK = a.HK, L = a.L;
+// kernels need no ordering between the append and these loads.
+__device__ void precompute_heads(const RowArgs& a, int b, int s, int w, int k0, int k1,
+                                 float* psm) {
+    const int HV = a.HV, HK = a.HK, L = a.L, vpk = HV / HK;
+    const int nk = k1 - k0, nv = nk * vpk, v0 = k0 * vpk;
     const int TBL = tbl_floats(L);
     const bool bf = a.act_bf16;
     const int sa = bf ? 2 : 4;
-    float* kk = psm;            // [HK][L]
-    float* kq = kk + HK * L;    // [HK][L]
-    float* kqt = kq + HK * L;   // [HK]
-    float* tbl = psm + ((2 * HK * L + HK + 3) & ~3);  // [HV][TBL]
-    float* gs = tbl + HV * TBL;                        // gate ring [HV][L]
+    float* kk = psm;            // [nk][L]
+    float* kq = kk + nk * L;    // [nk][L]
+    float* kqt = kq + nk * L;   // [nk]
+    float* tbl = psm + ((2 * nk * L + nk + 3) & ~3);  // [nv][TBL]
+    float* gs = tbl + nv * TBL;                        // gate ring [nv][L]
 
-    for (int e = threadIdx.x; e < HV * w; e += blockDim.x) {
-        const int hv = e / w, i = e - (e / w) * w;
-        gs[hv * L + i] = a.ring_g[((size_t)s * HV + hv) * L + i];
+    for (int e = threadIdx.x; e < nv * w; e += blockDim.x) {
+        const int hl = e / w, i = e - (e / w) * w;
+        gs[hl * L + i] = a.ring_g[((size_t)s * HV + v0 + hl) * L + i];
     }
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-    for (int kh = warp; kh < HK; kh += nwarps) {
+    for (int kl = warp; kl < nk; kl += nwarps) {
+        const int kh = k0 + kl;
         float kt[4], qt[4];
         load4(static_cast<const char*>(a.k) + ((size_t)b * HK + kh) * KD * sa, lane * 4, bf, kt);
         load4(static_cast<const char*>(a.q) + ((size_t)b * HK + kh) * KD * sa, lane * 4, bf, qt);
@@ -91,7 +96,7 @@ __device__ void precompute_row(const RowArgs& a, int b, int s, int w, float* psm
         float t0 = kt[0] * qt[0] + kt[1] * qt[1] + kt[2] * qt[2] + kt[3] * qt[3];
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) t0 += __shfl_xor_sync(0xffffffffu, t0, o);
-        if (lane == 0) kqt[kh] = t0;
+        if (lane == 0) kqt[kl] = t0;
         for (int i0 = 0; i0 < w; i0 += 4) {
             float ki[4][4];
 #pragma unroll
@@ -108,26 +113,25 @@ __device__ void precompute_row(const RowArgs& a, int b, int s, int w, float* psm
                         d2 += __shfl_xor_sync(0xffffffffu, d2, o);
                     }
                     if (lane == 0) {
-                        kk[kh * L + i0 + u] = d1;
-                        kq[kh * L + i0 + u] = d2;
+                        kk[kl * L + i0 + u] = d1;
+                        kq[kl * L + i0 + u] = d2;
                     }
                 }
             }
         }
     }
     __syncthreads();
-    const int vpk = HV / HK;
-    for (int hv = threadIdx.x; hv < HV; hv += blockDim.x) {
-        const int kh = hv / vpk;
+    for (int hl = threadIdx.x; hl < nv; hl += blockDim.x) {
+        const int hv = v0 + hl, kl = hl / vpk;
         const float gt = a.g[(size_t)b * HV + hv];
         const float bt = a.beta[(size_t)b * HV + hv];
-        const float* gr = gs + hv * L;
-        float* t = tbl + hv * TBL;
+        const float* gr = gs + hl * L;
+        float* t = tbl + hl * TBL;
         float gam = 1.f;  // prod_{j=i+1..w-1} g_j
         for (int i = w - 1; i >= 0; --i) {
             const float Gi = gt * gam;
-            t[i] = gam * kk[kh * L + i];
-            t[L + i] = Gi * kq[kh * L + i];
+            t[i] = gam * kk[kl * L + i];
+            t[L + i] = Gi * kq[kl * L + i];
             t[2 * L + i] = Gi;
             gam *= gr[i];
         }
@@ -138,19 +142,19 @@ __device__ void precompute_row(const RowArgs& a, int b, int s, int w, float* psm
         }
         t[3 * L] = gam;
         t[3 * L + 1] = gt * gam;
-        t[3 * L + 2] = kqt[kh];
+        t[3 * L + 2] = kqt[kl];
         t[3 * L + 3] = bt;
         t[3 * L + 4] = gt;
         for (int i = 3 * L + 5; i < TBL; ++i) t[i] = 0.f;
     }
     __syncthreads();
-    float4* dst = reinterpret_cast<float4*>(a.ws + (size_t)b * HV * TBL);
+    float4* dst = reinterpret_cast<float4*>(a.ws + ((size_t)b * HV + v0) * TBL);
     const float4* src = reinterpret_cast<const float4*>(tbl);
-    for (int c = threadIdx.x; c < HV * TBL / 4; c += blockDim.x) dst[c] = src[c];
+    for (int c = threadIdx.x; c < nv * TBL / 4; c += blockDim.x) dst[c] = src[c];
 }
 
 // ----------------------------------------------------------------------------
-// prologue kernels (one CTA per row)
+// prologue kernels
 // ----------------------------------------------------------------------------
 
 __global__ void __launch_bounds__(128) ring_append_kernel(const RowArgs a, const int32_t* ci,
@@ -158,7 +162,7 @@ __global__ void __launch_bounds__(128) ring_append_kernel(const RowArgs a, const
     const int b = blockIdx.x;
     const int w = given_cursor(b, ci[b], a.num_slots, a.L, row_wp, threadIdx.x == 0 ? dev_err : nullptr);
     if (w < 0) return;
-    append_row(a, b, ci[b], w);
+    append_heads(a, b, ci[b], w, 0, a.HK);
 }
 
 __global__ void __launch_bounds__(512) precompute_kernel(const RowArgs a, const int32_t* ci,
@@ -168,7 +172,7 @@ __global__ void __launch_bounds__(512) precompute_kernel(const RowArgs a, const 
     // bad slots and cursors are reported by the append and output kernels
     const int w = given_cursor(b, ci[b], a.num_slots, a.L, row_wp, nullptr);
     if (w < 0) return;
-    precompute_row(a, b, ci[b], w, psm);
+    precompute_heads(a, b, ci[b], w, 0, a.HK, psm);
 }
 
 // Cursor advance (when `advance`), ring append and tables of one row in one CTA.
@@ -187,8 +191,47 @@ __global__ void __launch_bounds__(512) prepare_kernel(const RowArgs a, const int
     __syncthreads();
     const int w = sh_w;
     if (w < 0) return;
-    append_row(a, b, s, w);
-    precompute_row(a, b, s, w, psm);
+    append_heads(a, b, s, w, 0, a.HK);
+    precompute_heads(a, b, s, w, 0, a.HK, psm);
+}
+
+// The same with `cs` CTAs per row (a thread-block cluster), each owning HK/cs key
+// heads and their value heads: every CTA reads the slot's cursor, the cluster
+// barrier orders those reads before the cluster's first CTA advances it.
+__global__ void __launch_bounds__(128) prepare_cluster_kernel(const RowArgs a, const int32_t* ci,
+                                                              int cs, int advance,
+                                                              const uint8_t* force,
+                                                              int32_t* slot_wp, int32_t* row_wp,
+                                                              uint8_t* row_flush, int32_t* dev_err) {
+    extern __shared__ __align__(16) float psm[];
+    __shared__ int sh_w;
+    const int b = blockIdx.x / cs, part = blockIdx.x - (blockIdx.x / cs) * cs;
+    const int s = ci[b];
+    if (threadIdx.x == 0) {
+        int w = -1;
+        if (s >= 0 && s < a.num_slots) {
+            w = advance ? slot_wp[s] : row_wp[b];
+            if (w < 0 || w >= a.L) {
+                if (part == 0) set_dev_err(dev_err, RSSM_DEVERR_CURSOR);
+                w = -1;
+            }
+        } else if (s >= a.num_slots && part == 0) {
+            set_dev_err(dev_err, RSSM_DEVERR_SLOT);
+        }
+        sh_w = w;
+    }
+    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
+    const int w = sh_w;
+    if (advance && part == 0 && threadIdx.x == 0) {
+        const int f = w >= 0 && ((w == a.L - 1) || (force != nullptr && force[b] != 0));
+        row_wp[b] = w >= 0 ? w : 0;
+        row_flush[b] = static_cast<uint8_t>(f);
+        if (w >= 0) slot_wp[s] = f ? 0 : w + 1;
+    }
+    if (w < 0) return;
+    const int per = a.HK / cs;
+    append_heads(a, b, s, w, part * per, (part + 1) * per);
+    precompute_heads(a, b, s, w, part * per, (part + 1) * per, psm);
 }
 
 RowArgs row_args(const rssm_gdn_dims* d) {
@@ -232,8 +275,9 @@ extern "C" size_t rssm_gdn_workspace_size(const rssm_gdn_dims* d) {
 }
 
 // Shared-memory size of the table-building kernels, checked and opted in.
-static int gdn_prologue_smem(const rssm_gdn_dims* d, const void* kernel, int* smem) {
-    *smem = gdn::precompute_smem(d->num_v_heads, d->num_k_heads, d->ring_len);
+static int gdn_prologue_smem(const rssm_gdn_dims* d, const void* kernel, int key_heads, int* smem) {
+    *smem = gdn::precompute_smem(key_heads * (d->num_v_heads / d->num_k_heads), key_heads,
+                                 d->ring_len);
     DeviceInfo di;
     if (!device_info(&di)) return RSSM_ERR_CUDA;
     if (*smem > di.max_smem_optin) return RSSM_ERR_UNSUPPORTED;
@@ -255,7 +299,7 @@ extern "C" int rssm_gdn_precompute(const rssm_gdn_dims* d, const void* q, const 
         return RSSM_ERR_INVALID_ARG;
     if (workspace_bytes < rssm_gdn_workspace_size(d)) return RSSM_ERR_INVALID_ARG;
     int smem = 0;
-    rc = gdn_prologue_smem(d, reinterpret_cast<const void*>(gdn::precompute_kernel), &smem);
+    rc = gdn_prologue_smem(d, reinterpret_cast<const void*>(gdn::precompute_kernel), d->num_k_heads, &smem);
     if (rc) return rc;
     gdn::RowArgs ra = gdn::row_args(d);
     ra.q = q;
@@ -284,8 +328,6 @@ extern "C" int rssm_gdn_prepare(const rssm_gdn_dims* d, int advance, const uint8
         return RSSM_ERR_INVALID_ARG;
     if (workspace_bytes < rssm_gdn_workspace_size(d)) return RSSM_ERR_INVALID_ARG;
     int smem = 0;
-    rc = gdn_prologue_smem(d, reinterpret_cast<const void*>(gdn::prepare_kernel), &smem);
-    if (rc) return rc;
     gdn::RowArgs ra = gdn::row_args(d);
     ra.q = q;
     ra.k = k;
@@ -294,7 +336,36 @@ extern "C" int rssm_gdn_prepare(const rssm_gdn_dims* d, int advance, const uint8
     ra.ring_k = ring_k;
     ra.ring_g = ring_g;
     ra.ws = static_cast<float*>(workspace);
+    const int adv = advance ? 1 : 0;
+    int cs = 8;  // CTAs per row: the largest divisor of HK up to 8
+    while (d->num_k_heads % cs) --cs;
+    if (cs > 1) {
+        rc = gdn_prologue_smem(d, reinterpret_cast<const void*>(gdn::prepare_cluster_kernel),
+                               d->num_k_heads / cs, &smem);
+        if (rc) return rc;
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)d->batch * cs);
+        cfg.blockDim = dim3(128);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = (cudaStream_t)stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = cs;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, gdn::prepare_cluster_kernel, ra, cache_indices, cs, adv,
+                               force_flush, slot_wp, row_wp, row_flush, dev_err) != cudaSuccess) {
+            cudaGetLastError();
+            return RSSM_ERR_CUDA;
+        }
+        return launch_status();
+    }
+    rc = gdn_prologue_smem(d, reinterpret_cast<const void*>(gdn::prepare_kernel), d->num_k_heads,
+                           &smem);
+    if (rc) return rc;
     gdn::prepare_kernel<<<d->batch, 512, smem, (cudaStream_t)stream>>>(
-        ra, cache_indices, advance ? 1 : 0, force_flush, slot_wp, row_wp, row_flush, dev_err);
+        ra, cache_indices, adv, force_flush, slot_wp, row_wp, row_flush, dev_err);
     return launch_status();
 }

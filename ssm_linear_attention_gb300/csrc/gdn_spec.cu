@@ -90,9 +90,9 @@ struct ProArgs {
 __host__ __device__ inline int fold_smem_floats() { return kFoldChunk * (KD + VB + 2); }
 
 // Shared memory of the table role (floats): KK [L][T], KQ [L][T], gates
-// [HV/HK][L], the drafts' k and q [T][2][KD].
+// [HV/HK][L], the drafts' k and q [T][2][KD], the history keys [L][KD].
 __host__ __device__ inline int pre_smem_floats(int L, int T, int vpk) {
-    return ((2 * L * T + vpk * L + 3) & ~3) + 2 * T * KD;
+    return ((2 * L * T + vpk * L + 3) & ~3) + 2 * T * KD + L * KD;
 }
 
 // Exact fold of one (row, value head, 32-row block) tile. Thread t owns row t/4
@@ -152,17 +152,16 @@ __device__ void fold_tile(const ProArgs& a, int item, float* sm) {
         }
         __syncthreads();
         for (int i = 0; i < ne; ++i) {
-            float4 k4[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-                k4[u] = *reinterpret_cast<const float4*>(ks + i * KD + (qd + 4 * u) * 4);
+            const float* ki = ks + i * KD + qd * 4;
             float p0 = 0.f, p1 = 0.f;
 #pragma unroll
             for (int u = 0; u < 8; u += 2) {
-                p0 = fmaf(S[u][0], k4[u].x, p0); p0 = fmaf(S[u][1], k4[u].y, p0);
-                p0 = fmaf(S[u][2], k4[u].z, p0); p0 = fmaf(S[u][3], k4[u].w, p0);
-                p1 = fmaf(S[u + 1][0], k4[u + 1].x, p1); p1 = fmaf(S[u + 1][1], k4[u + 1].y, p1);
-                p1 = fmaf(S[u + 1][2], k4[u + 1].z, p1); p1 = fmaf(S[u + 1][3], k4[u + 1].w, p1);
+                const float4 ka = *reinterpret_cast<const float4*>(ki + 16 * u);
+                const float4 kb = *reinterpret_cast<const float4*>(ki + 16 * (u + 1));
+                p0 = fmaf(S[u][0], ka.x, p0); p0 = fmaf(S[u][1], ka.y, p0);
+                p0 = fmaf(S[u][2], ka.z, p0); p0 = fmaf(S[u][3], ka.w, p0);
+                p1 = fmaf(S[u + 1][0], kb.x, p1); p1 = fmaf(S[u + 1][1], kb.y, p1);
+                p1 = fmaf(S[u + 1][2], kb.z, p1); p1 = fmaf(S[u + 1][3], kb.w, p1);
             }
             float part = p0 + p1;
             part += __shfl_xor_sync(kFull, part, 1);
@@ -170,11 +169,12 @@ __device__ void fold_tile(const ProArgs& a, int item, float* sm) {
             const float ge = gs[i];
             const float dn = bs[i] * (vs[i * VB + r] - ge * part);
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                S[u][0] = fmaf(ge, S[u][0], dn * k4[u].x);
-                S[u][1] = fmaf(ge, S[u][1], dn * k4[u].y);
-                S[u][2] = fmaf(ge, S[u][2], dn * k4[u].z);
-                S[u][3] = fmaf(ge, S[u][3], dn * k4[u].w);
+            for (int u = 0; u < 8; ++u) {  // k re-read from shared memory: fewer registers
+                const float4 k4 = *reinterpret_cast<const float4*>(ki + 16 * u);
+                S[u][0] = fmaf(ge, S[u][0], dn * k4.x);
+                S[u][1] = fmaf(ge, S[u][1], dn * k4.y);
+                S[u][2] = fmaf(ge, S[u][2], dn * k4.z);
+                S[u][3] = fmaf(ge, S[u][3], dn * k4.w);
             }
         }
     }
@@ -208,6 +208,7 @@ __device__ void pre_head(const ProArgs& a, int idx, float* sm) {
     float* KQ = KK + L * T;                           // [L][T]   k_i . q_j
     float* gts = KQ + L * T;                          // [vpk][L] gates of the live entries
     float* kdq = sm + ((2 * L * T + vpk * L + 3) & ~3);  // [T][2][KD] drafts' k, q
+    float* hk = kdq + NV * KD;                           // [c][KD] history keys
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5, nwarps = blockDim.x >> 5;
 
     for (int e = t; e < NV * (KD / 4); e += blockDim.x) {
@@ -218,6 +219,13 @@ __device__ void pre_head(const ProArgs& a, int idx, float* sm) {
         load4(static_cast<const char*>(src) + (((size_t)b * T + j) * HK + kh) * KD * sa, c4 * 4, bf, f);
         *reinterpret_cast<float4*>(kdq + jv * KD + c4 * 4) = make_float4(f[0], f[1], f[2], f[3]);
     }
+    const char* kr = static_cast<const char*>(a.ring_k) + ((size_t)s * HK + kh) * L * KD * sa;
+    for (int e = t; e < c * (KD / 4); e += blockDim.x) {
+        const int i = e / (KD / 4), c4 = e - (e / (KD / 4)) * (KD / 4);
+        float f[4];
+        load4(kr + (size_t)((base_eff + i) % L) * KD * sa, c4 * 4, bf, f);
+        *reinterpret_cast<float4*>(hk + i * KD + c4 * 4) = make_float4(f[0], f[1], f[2], f[3]);
+    }
     for (int x = t; x < vpk * nk; x += blockDim.x) {
         const int hl = x / nk, m = x - (x / nk) * nk, hv = kh * vpk + hl;
         gts[hl * L + m] = m < c ? a.ring_g[((size_t)s * HV + hv) * L + (base_eff + m) % L]
@@ -227,13 +235,11 @@ __device__ void pre_head(const ProArgs& a, int idx, float* sm) {
 
     // a warp per live key: lane holds 4 columns; the 2T dots reduce with one
     // reduce-scatter (entry 2j: k_i . k_j, entry 2j+1: k_i . q_j)
-    const char* kr = static_cast<const char*>(a.ring_k) + ((size_t)s * HK + kh) * L * KD * sa;
     for (int i = warp; i < nk; i += nwarps) {
         float ki[4];
-        if (i < c) {
-            load4(kr + (size_t)((base_eff + i) % L) * KD * sa, lane * 4, bf, ki);
-        } else {
-            const float4 v = *reinterpret_cast<const float4*>(kdq + (2 * (i - c)) * KD + lane * 4);
+        {
+            const float* src = i < c ? hk + i * KD : kdq + (2 * (i - c)) * KD;
+            const float4 v = *reinterpret_cast<const float4*>(src + lane * 4);
             ki[0] = v.x; ki[1] = v.y; ki[2] = v.z; ki[3] = v.w;
         }
         float part[NVP];
@@ -287,7 +293,7 @@ __device__ void pre_head(const ProArgs& a, int idx, float* sm) {
 }
 
 template <int T>
-__global__ void __launch_bounds__(kThreads) prologue_kernel(const ProArgs a) {
+__global__ void __launch_bounds__(kThreads, 6) prologue_kernel(const ProArgs a) {
     extern __shared__ __align__(16) float psm[];
     if ((int)blockIdx.x < a.n_fold) fold_tile(a, blockIdx.x, psm);
     else pre_head<T>(a, blockIdx.x - a.n_fold, psm);

@@ -133,6 +133,18 @@ class Mamba2ReplayDecoder:
                                slots.shape[0], self.num_slots, self.L, 0, None, None, self.dev_err,
                                stream)
 
+    def materialize(self, slots, out=None, stream=None):
+        """Current fp32 state of the listed slots [n, H, P, N] (checkpoint folded with the
+        live ring entries); pool, rings and cursors are left untouched."""
+        n = slots.shape[0]
+        if out is None:
+            out = torch.empty(n, self.H, self.P, self.N, device=self.state.device,
+                              dtype=torch.float32)
+        B.rssm_mamba2_materialize_state(self.dims(n), self.state, self.A, self.ring_x,
+                                        self.ring_dt, self.ring_B, slots, self.slot_wp, out,
+                                        self.dev_err, stream)
+        return out
+
 
 class Mamba2FullStateDecoder:
     """The conventional Mamba2 decode step (whole state read and written every step)."""
@@ -253,6 +265,17 @@ class GDNReplayDecoder:
                                slots.shape[0], self.num_slots, self.L, 0, None, None, self.dev_err,
                                stream)
 
+    def materialize(self, slots, out=None, stream=None):
+        """Current fp32 state of the listed slots [n, HV, V, K]."""
+        n = slots.shape[0]
+        if out is None:
+            out = torch.empty(n, self.HV, self.V, self.K, device=self.state.device,
+                              dtype=torch.float32)
+        B.rssm_gdn_materialize_state(self.dims(n), self.state, self.ring_k, self.ring_g,
+                                     self.ring_d, slots, self.slot_wp, None, out, self.dev_err,
+                                     stream)
+        return out
+
 
 class GDNFullStateDecoder:
     """The conventional gated-delta-net decode step (state read and written every step)."""
@@ -338,3 +361,15 @@ class GDNSpecVerifier:
         B.rssm_advance_cursors(B.RSSM_CURSOR_RESET, self.slot_cnt, self.slot_base,
                                self.slot_flush, slots, None, None, slots.shape[0], self.num_slots,
                                self.L, self.T, None, None, self.dev_err, stream)
+
+    def materialize(self, slots, out=None, stream=None):
+        """Current fp32 state of the listed slots [n, HV, V, K]: the checkpoint folded with
+        the committed entries (including those of a pending fold)."""
+        n = slots.shape[0]
+        if out is None:
+            out = torch.empty(n, self.HV, self.V, self.K, device=self.state.device,
+                              dtype=torch.float32)
+        B.rssm_gdn_materialize_state(self.dims(n), self.state, self.ring_k, self.ring_g,
+                                     self.ring_d, slots, self.slot_cnt, self.slot_base, out,
+                                     self.dev_err, stream)
+        return out
