@@ -808,6 +808,46 @@ def run_spec(args, dist, sub=False):
     round_b = float(np.mean(vb)) + float(np.mean(fb))
     peak, peak_kind = read_peaks()
     per_ms = float(np.mean(per))
+
+    # the in-house conventional verify (a full-state snapshot per draft, commit copies
+    # the accepted one) on an identical pool, same drafts and accepted counts
+    full = None
+    if not args.no_full_state:
+        fver = ssm.GDNSpecFullStateVerifier(wl.num_v_heads, wl.num_k_heads, wl.head_k_dim,
+                                            wl.head_v_dim, T, wl.num_slots, wl.batch, act_dtype=bf,
+                                            out_dtype=bf, device=dev)
+        fver.state.copy_(ver.state)
+        del ver
+
+        def full_fn(j):
+            q, k, v, beta, g = sets[j]
+
+            def f():
+                fver.verify(q, k, v, beta, g, ci)
+                fver.commit(ci, acc_dev[j])
+            return f
+
+        for k in range(W0):
+            full_fn(k % G)()
+        torch.cuda.synchronize()
+        g_full = _graphs([full_fn(j) for j in range(G)])
+        Kf = max(50, K // 4)
+        f_el, _, _ = _timed_graphs(None, g_full, Kf, dist, dev, clocks=False)
+        assert int(fver.dev_err.abs().sum().item()) == 0
+        del g_full, fver
+        f_ms = f_el / Kf
+        HV, HK, Kd, Vd = wl.num_v_heads, wl.num_k_heads, wl.head_k_dim, wl.head_v_dim
+        sab = 2 if wl.act_dtype == "bf16" else 4
+        acc_mean = float(np.mean([(accs[k % G] > 0).mean() for k in range(Kf)]))
+        fb = wl.batch * (HV * Vd * Kd * 4 * (1 + T + 2 * acc_mean)
+                         + T * (2 * HK * Kd * sab + HV * Vd * sab + 8 * HV + HV * Vd * 2))
+        full = {"ms_per_round": f_ms, "us_per_round": f_ms * 1e3,
+                "rows_per_s": dist.world * wl.batch / (f_ms * 1e-3),
+                "bytes_per_round": int(fb), "achieved_gbs": fb / (f_ms * 1e-3) / 1e9,
+                "hbm_frac": fb / (f_ms * 1e-3) / 1e9 / peak,
+                "replay_speedup": f_ms / ms_round,
+                "snapshot_bytes": int(wl.batch * T * HV * Vd * Kd * 4)}
+
     line = {
         "metric": "gdn spec verify rows/s and µs/round at batch %d, T %d" % (wl.batch, T),
         "value": dist.world * wl.batch / (ms_round * 1e-3), "unit": UNIT,
@@ -817,14 +857,15 @@ def run_spec(args, dist, sub=False):
         "vs_baseline": None, "dtype": "f32", "data": "synthetic",
         "config": {"workload": SPEC_WORKLOAD, "global_batch": dist.world * wl.batch,
                    "batch_per_gpu": wl.batch, "T": T, "ring_len": L,
-                   "timing": "one CUDA graph per round (fold, precompute, verify, commit)",
+                   "timing": "one CUDA graph per round (fold + tables, verify, commit)",
                    "l2": "inputs larger than L2: 268 MB of fp32 checkpoint per round"},
-        "roofline": {"bound": "hbm", "kernel": "spec round (fold + precompute + verify + commit)",
+        "roofline": {"bound": "hbm", "kernel": "spec round (prologue + verify + commit)",
                      "achieved": round_b / (per_ms * 1e-3) / 1e9, "peak": peak, "unit": "GB/s",
                      "frac": round_b / (per_ms * 1e-3) / 1e9 / peak, "peak_source": peak_kind,
                      "traffic": None, "algorithmic_bytes_per_round": int(round_b),
                      "verify_bytes": float(np.mean(vb)), "fold_bytes": float(np.mean(fb))},
-        "gpu_launches": 4 * K,
+        "full_state": full,
+        "gpu_launches": 3 * K,
         "clocks": clocks,
     }
     return line
@@ -913,7 +954,11 @@ def run_sweep(args, dist):
                 del g_full, fdec
                 full_ms = fel / K
                 fb = full_state_bytes(wl, batch)
+                l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0)
+                tile_bytes = batch * wl.nheads * wl.headdim * wl.dstate * (4 if sdt == "fp32" else 2)
                 line = {"metric": "mamba2 sweep point", "workload": "sweep", "batch": batch,
+                        "state_bytes_per_step": tile_bytes,
+                        "possibly_l2_resident": bool(l2 and tile_bytes <= l2),
                         "ring_len": L, "state_dtype": sdt, "steps": K, "n_gpus": dist.world,
                         "replay_us_per_step": rep_ms * 1e3,
                         "replay_rows_per_s": dist.world * batch / (rep_ms * 1e-3),

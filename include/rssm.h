@@ -439,6 +439,31 @@ int rssm_gdn_spec_verify(const rssm_gdn_dims* dims, int32_t T, float* state, con
                          size_t workspace_bytes, void* o, int32_t* dev_err,
                          rssm_stream_t stream);
 
+/* rssm_gdn_spec_full_state_verify -- the conventional speculative verify, built as
+ * the in-house comparison for rssm_gdn_spec_verify ([SPEC] 功能与动机: the
+ * recurrent verify keeps a full-state snapshot per draft token, the
+ * intermediate_ssm buffers). For each row with s >= 0 the T drafts are applied in
+ * order to a copy of slot s's state: S_j = g_j S_{j-1} + beta_j (v_j - g_j S_{j-1}
+ * k_j) k_j^T, o_j = S_j q_j; S_j is stored as snapshots[b][j] ([batch][T][HV][V][K]
+ * float32, caller-allocated, size from rssm_gdn_spec_full_state_snapshot_bytes).
+ * The pool is not modified. Inputs, outputs and errors as rssm_gdn_spec_verify
+ * (ring_len unused). */
+size_t rssm_gdn_spec_full_state_snapshot_bytes(const rssm_gdn_dims* dims, int32_t T);
+int rssm_gdn_spec_full_state_verify(const rssm_gdn_dims* dims, int32_t T, const float* state,
+                                    const void* q, const void* k, const void* v,
+                                    const float* beta, const float* g,
+                                    const int32_t* cache_indices, float* snapshots,
+                                    size_t snapshot_bytes, void* o, int32_t* dev_err,
+                                    rssm_stream_t stream);
+
+/* rssm_gdn_spec_full_state_commit -- the commit of the conventional verify: for each
+ * row with s >= 0 and a = num_accepted[b] > 0, state[s] = snapshots[b][a-1]; rows
+ * with a = 0 keep their state. a outside 0..T: row skipped, RSSM_DEVERR_CURSOR. */
+int rssm_gdn_spec_full_state_commit(const rssm_gdn_dims* dims, int32_t T, float* state,
+                                    const float* snapshots, const int32_t* cache_indices,
+                                    const int32_t* num_accepted, int32_t* dev_err,
+                                    rssm_stream_t stream);
+
 /* ------------------------------------------------------------------------- */
 
 /* rssm_mamba2_materialize_state -- test / debug: the current recurrent state of the

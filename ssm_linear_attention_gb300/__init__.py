@@ -14,7 +14,8 @@ __all__ = [n for n in dir(_binding) if n.startswith(("rssm_", "RSSM_"))] + [
 def __getattr__(name):
     # decoder runners import torch; load them lazily
     if name in ("Mamba2ReplayDecoder", "Mamba2FullStateDecoder", "GDNReplayDecoder",
-                "GDNFullStateDecoder", "GDNSpecVerifier", "torch_dtype_code"):
+                "GDNFullStateDecoder", "GDNSpecVerifier", "GDNSpecFullStateVerifier",
+                "torch_dtype_code"):
         from . import decoder
         return getattr(decoder, name)
     raise AttributeError(name)

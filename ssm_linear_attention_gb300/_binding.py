@@ -27,6 +27,8 @@ EXPORTS = (
     "rssm_gdn_prepare", "rssm_gdn_step",
     "rssm_gdn_full_state_decode", "rssm_gdn_spec_workspace_size", "rssm_gdn_spec_verify",
     "rssm_mamba2_materialize_state", "rssm_gdn_materialize_state",
+    "rssm_gdn_spec_full_state_snapshot_bytes", "rssm_gdn_spec_full_state_verify",
+    "rssm_gdn_spec_full_state_commit",
 )
 
 
@@ -94,6 +96,10 @@ def _declare(L):
         "rssm_gdn_full_state_decode": (_I, [gd, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                             _VP]),
         "rssm_gdn_spec_workspace_size": (_SZ, [gd, _I32]),
+        "rssm_gdn_spec_full_state_snapshot_bytes": (_SZ, [gd, _I32]),
+        "rssm_gdn_spec_full_state_verify": (_I, [gd, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                                 _SZ, _VP, _VP, _VP]),
+        "rssm_gdn_spec_full_state_commit": (_I, [gd, _I32, _VP, _VP, _VP, _VP, _VP, _VP]),
         "rssm_mamba2_materialize_state": (_I, [m2, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                                _VP]),
         "rssm_gdn_materialize_state": (_I, [gd, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
@@ -312,3 +318,20 @@ def rssm_gdn_materialize_state(dims, state, ring_k, ring_g, ring_d, slots, slot_
     _call("rssm_gdn_materialize_state", ctypes.byref(dims), _ptr(state), _ptr(ring_k),
           _ptr(ring_g), _ptr(ring_d), _ptr(slots), _ptr(slot_wp), _ptr(slot_base), _ptr(out),
           _ptr(dev_err), _stream(stream))
+
+
+def rssm_gdn_spec_full_state_snapshot_bytes(dims, T):
+    return lib().rssm_gdn_spec_full_state_snapshot_bytes(ctypes.byref(dims), T)
+
+
+def rssm_gdn_spec_full_state_verify(dims, T, state, q, k, v, beta, g, cache_indices, snapshots,
+                                    snapshot_bytes, o, dev_err=None, stream=None):
+    _call("rssm_gdn_spec_full_state_verify", ctypes.byref(dims), T, _ptr(state), _ptr(q), _ptr(k),
+          _ptr(v), _ptr(beta), _ptr(g), _ptr(cache_indices), _ptr(snapshots), snapshot_bytes,
+          _ptr(o), _ptr(dev_err), _stream(stream))
+
+
+def rssm_gdn_spec_full_state_commit(dims, T, state, snapshots, cache_indices, num_accepted,
+                                    dev_err=None, stream=None):
+    _call("rssm_gdn_spec_full_state_commit", ctypes.byref(dims), T, _ptr(state), _ptr(snapshots),
+          _ptr(cache_indices), _ptr(num_accepted), _ptr(dev_err), _stream(stream))

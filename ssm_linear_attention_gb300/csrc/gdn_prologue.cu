@@ -195,45 +195,6 @@ __global__ void __launch_bounds__(512) prepare_kernel(const RowArgs a, const int
     precompute_heads(a, b, s, w, 0, a.HK, psm);
 }
 
-// The same with `cs` CTAs per row (a thread-block cluster), each owning HK/cs key
-// heads and their value heads: every CTA reads the slot's cursor, the cluster
-// barrier orders those reads before the cluster's first CTA advances it.
-__global__ void __launch_bounds__(128) prepare_cluster_kernel(const RowArgs a, const int32_t* ci,
-                                                              int cs, int advance,
-                                                              const uint8_t* force,
-                                                              int32_t* slot_wp, int32_t* row_wp,
-                                                              uint8_t* row_flush, int32_t* dev_err) {
-    extern __shared__ __align__(16) float psm[];
-    __shared__ int sh_w;
-    const int b = blockIdx.x / cs, part = blockIdx.x - (blockIdx.x / cs) * cs;
-    const int s = ci[b];
-    if (threadIdx.x == 0) {
-        int w = -1;
-        if (s >= 0 && s < a.num_slots) {
-            w = advance ? slot_wp[s] : row_wp[b];
-            if (w < 0 || w >= a.L) {
-                if (part == 0) set_dev_err(dev_err, RSSM_DEVERR_CURSOR);
-                w = -1;
-            }
-        } else if (s >= a.num_slots && part == 0) {
-            set_dev_err(dev_err, RSSM_DEVERR_SLOT);
-        }
-        sh_w = w;
-    }
-    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
-    const int w = sh_w;
-    if (advance && part == 0 && threadIdx.x == 0) {
-        const int f = w >= 0 && ((w == a.L - 1) || (force != nullptr && force[b] != 0));
-        row_wp[b] = w >= 0 ? w : 0;
-        row_flush[b] = static_cast<uint8_t>(f);
-        if (w >= 0) slot_wp[s] = f ? 0 : w + 1;
-    }
-    if (w < 0) return;
-    const int per = a.HK / cs;
-    append_heads(a, b, s, w, part * per, (part + 1) * per);
-    precompute_heads(a, b, s, w, part * per, (part + 1) * per, psm);
-}
-
 RowArgs row_args(const rssm_gdn_dims* d) {
     RowArgs a{};
     a.HV = d->num_v_heads;
@@ -337,31 +298,6 @@ extern "C" int rssm_gdn_prepare(const rssm_gdn_dims* d, int advance, const uint8
     ra.ring_g = ring_g;
     ra.ws = static_cast<float*>(workspace);
     const int adv = advance ? 1 : 0;
-    int cs = 8;  // CTAs per row: the largest divisor of HK up to 8
-    while (d->num_k_heads % cs) --cs;
-    if (cs > 1) {
-        rc = gdn_prologue_smem(d, reinterpret_cast<const void*>(gdn::prepare_cluster_kernel),
-                               d->num_k_heads / cs, &smem);
-        if (rc) return rc;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)d->batch * cs);
-        cfg.blockDim = dim3(128);
-        cfg.dynamicSmemBytes = smem;
-        cfg.stream = (cudaStream_t)stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = cs;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, gdn::prepare_cluster_kernel, ra, cache_indices, cs, adv,
-                               force_flush, slot_wp, row_wp, row_flush, dev_err) != cudaSuccess) {
-            cudaGetLastError();
-            return RSSM_ERR_CUDA;
-        }
-        return launch_status();
-    }
     rc = gdn_prologue_smem(d, reinterpret_cast<const void*>(gdn::prepare_kernel), d->num_k_heads,
                            &smem);
     if (rc) return rc;

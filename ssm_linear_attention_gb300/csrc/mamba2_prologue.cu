@@ -8,11 +8,16 @@
 // dt_cache, B_cache written at write_pos), 实现拆解 item 3 (per-row write_pos and
 // is_flush computed on the device).
 //
-// Kernels (one CTA of 256 threads per row):
+// Kernels (one CTA per row):
 //   ring_append_kernel  x, dt = softplus(dt_raw + dt_bias), B into ring entry w.
-//   precompute_kernel   B_i . C_t per group from the staged B run, decay suffix
+//   precompute_kernel   stages C_t and the slot's whole dt and B rings in shared
+//                       memory, then B_i . C_t per group and the decay suffix
 //                       products per head, written as per-(row, head) tables.
-//   prepare_kernel      cursor step + ring append + tables in one CTA.
+//   prepare_kernel      cursor step + ring append + tables: the slot's rings are
+//                       staged while the cursor is read, entry w is patched from
+//                       the step's inputs.
+// The tables are latency-bound work on a few tens of KB per row, so every load a
+// thread makes is issued before any of its results is used.
 #include "common.cuh"
 #include "cursor.cuh"
 #include "internal.h"
@@ -22,7 +27,7 @@ namespace rssm {
 namespace m2 {
 
 // ----------------------------------------------------------------------------
-// per-row prologue pieces: ring append, coefficient tables
+// per-row prologue pieces
 // ----------------------------------------------------------------------------
 
 struct RowArgs {
@@ -40,99 +45,128 @@ struct RowArgs {
     float* ws;             // [batch][H][TBL]
 };
 
-// Entry w of slot s's rings <- row b's x, dt = softplus(dt_raw + dt_bias), B, for
-// the groups [g0, g1) and their heads.
-__device__ void append_groups(const RowArgs& a, int b, int s, int w, int g0, int g1) {
+constexpr int kRowThreads = 512;
+
+// n elements from src to dst; each thread issues four loads before its four stores.
+template <class V>
+__device__ __forceinline__ void copy4(V* dst, const V* src, int n) {
+    for (int base = threadIdx.x; base < n; base += 4 * blockDim.x) {
+        V r[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = base + u * blockDim.x;
+            if (i < n) r[u] = __ldcg(src + i);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = base + u * blockDim.x;
+            if (i < n) dst[i] = r[u];
+        }
+    }
+}
+
+__device__ __forceinline__ float step_dt(const RowArgs& a, int b, int h) {
+    float v = a.dt_raw[(size_t)b * a.H + h] + (a.dt_bias ? a.dt_bias[h] : 0.f);
+    return a.softplus ? softplus_f(v) : v;
+}
+
+// Entry w of slot s's rings <- row b's x, dt = softplus(dt_raw + dt_bias), B.
+__device__ void append_row(const RowArgs& a, int b, int s, int w) {
     const int H = a.H, P = a.P, N = a.N, G = a.G, L = a.L;
-    const int hpg = H / G, h0 = g0 * hpg, nh = (g1 - g0) * hpg;
     const int sa = a.act_bf16 ? 2 : 4;
     const int xc = P * sa / 16;  // 16-byte chunks per head row
-    const uint4* xs = reinterpret_cast<const uint4*>(static_cast<const char*>(a.x) +
-                                                     ((size_t)b * H + h0) * P * sa);
-    for (int c = threadIdx.x; c < nh * xc; c += blockDim.x) {
-        const int h = h0 + c / xc, j = c % xc;
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<char*>(a.ring_x) +
-                                              (((size_t)s * H + h) * L + w) * P * sa) + j;
-        *dst = xs[c];
+    const uint4* xs =
+        reinterpret_cast<const uint4*>(static_cast<const char*>(a.x) + (size_t)b * H * P * sa);
+    for (int c = threadIdx.x; c < H * xc; c += blockDim.x) {
+        const int h = c / xc, j = c % xc;
+        reinterpret_cast<uint4*>(static_cast<char*>(a.ring_x) + (((size_t)s * H + h) * L + w) * P * sa)[j] =
+            xs[c];
     }
-    for (int hl = threadIdx.x; hl < nh; hl += blockDim.x) {
-        const int h = h0 + hl;
-        float v = a.dt_raw[(size_t)b * H + h] + (a.dt_bias ? a.dt_bias[h] : 0.f);
-        if (a.softplus) v = softplus_f(v);
-        a.ring_dt[((size_t)s * H + h) * L + w] = v;
-    }
+    for (int h = threadIdx.x; h < H; h += blockDim.x) a.ring_dt[((size_t)s * H + h) * L + w] = step_dt(a, b, h);
     const int bc = N * sa / 16;
-    const uint4* bs = reinterpret_cast<const uint4*>(static_cast<const char*>(a.B) +
-                                                     ((size_t)b * G + g0) * N * sa);
-    for (int c = threadIdx.x; c < (g1 - g0) * bc; c += blockDim.x) {
-        const int g = g0 + c / bc, j = c % bc;
-        uint4* dst = reinterpret_cast<uint4*>(static_cast<char*>(a.ring_B) +
-                                              (((size_t)s * G + g) * L + w) * N * sa) + j;
-        *dst = bs[c];
+    const uint4* bs =
+        reinterpret_cast<const uint4*>(static_cast<const char*>(a.B) + (size_t)b * G * N * sa);
+    for (int c = threadIdx.x; c < G * bc; c += blockDim.x) {
+        const int g = c / bc, j = c % bc;
+        reinterpret_cast<uint4*>(static_cast<char*>(a.ring_B) + (((size_t)s * G + g) * L + w) * N * sa)[j] =
+            bs[c];
     }
 }
 
-// Shared memory of precompute_groups for ng groups of hpg heads, in bytes.
-__host__ __device__ inline int precompute_smem(int nh, int N, int ng, int L, int sa) {
-    return (((ng * N + nh * L + ng * L + 3) & ~3) + nh * tbl_floats(L)) * 4 + ng * L * N * sa;
+// Shared memory of the table-building kernels, in bytes: C_t [G][N] f32, the dt
+// ring [H][L+1] f32 (rows padded to an odd stride), B . C [G][L] f32, the B ring
+// [G][L][N] (activation type).
+__host__ __device__ inline int prologue_smem(int H, int N, int G, int L, int sa) {
+    return ((G * N + H * (L + 1) + G * L + 3) & ~3) * 4 + G * L * N * sa;
 }
 
-// Row b's tables for the groups [g0, g1) from ring entries 0..w (read with
-// L2-coherent loads, so entries this block appended just before are seen):
+// Row b's C_t and slot s's whole dt and B rings into shared memory.
+__device__ void stage_slot(const RowArgs& a, int b, int s, float* sm) {
+    const int H = a.H, N = a.N, G = a.G, L = a.L;
+    const bool bf = a.act_bf16;
+    const int sa = bf ? 2 : 4;
+    float* cs = sm;
+    float* dts = cs + G * N;
+    char* braw = reinterpret_cast<char*>(sm + ((G * N + H * (L + 1) + G * L + 3) & ~3));
+    for (int e = threadIdx.x * 8; e < G * N; e += blockDim.x * 8)
+        load8(static_cast<const char*>(a.C) + ((size_t)b * G * N + e) * sa, bf, cs + e);
+    const float* dr = a.ring_dt + (size_t)s * H * L;
+    for (int base = threadIdx.x; base < H * L; base += 4 * blockDim.x) {
+        float r[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = base + u * blockDim.x;
+            if (i < H * L) r[u] = __ldcg(dr + i);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int i = base + u * blockDim.x;
+            if (i < H * L) dts[(i / L) * (L + 1) + (i - (i / L) * L)] = r[u];
+        }
+    }
+    copy4(reinterpret_cast<uint4*>(braw),
+          reinterpret_cast<const uint4*>(static_cast<const char*>(a.ring_B) + (size_t)s * G * L * N * sa),
+          G * L * N * sa / 16);
+}
+
+// Row b's tables from the staged rings (entries 0..w):
 //   P_i = exp(A_h sum_{j>i} dt_j), coef_i = P_i dt_i (B_i . C_t), a_i = P_i dt_i,
-//   Pm1 = exp(A_h sum_{j<=w} dt_j).
-__device__ void precompute_groups(const RowArgs& a, int b, int s, int w, int g0, int g1,
-                                  float* psm) {
+//   Pm1 = exp(A_h sum_{j<=w} dt_j), written straight to the workspace.
+__device__ void tables_from_smem(const RowArgs& a, int b, int w, float* sm) {
     const int H = a.H, N = a.N, G = a.G, L = a.L;
     const int TBL = tbl_floats(L);
     const bool bf = a.act_bf16;
     const int sa = bf ? 2 : 4;
-    const int hpg = H / G, ng = g1 - g0, nh = ng * hpg, h0 = g0 * hpg;
-    float* cs = psm;                                           // [ng][N] C_t in fp32
-    float* dts = cs + ng * N;                                  // [nh][L] dt of entries 0..w
-    float* bc = dts + nh * L;                                  // [ng][L] B_i . C_t
-    float* tbl = psm + ((ng * N + nh * L + ng * L + 3) & ~3);  // [nh][TBL]
-    char* braw = reinterpret_cast<char*>(tbl + nh * TBL);      // [ng][w+1][N] raw B entries
-
-    // stage C_t, the dt run and the B run of every group with coalesced loads
-    for (int e = threadIdx.x * 8; e < ng * N; e += blockDim.x * 8)
-        load8(static_cast<const char*>(a.C) + (((size_t)b * G + g0) * N + e) * sa, bf, cs + e);
-    for (int e = threadIdx.x; e < nh * (w + 1); e += blockDim.x) {
-        const int hl = e / (w + 1), i = e - (e / (w + 1)) * (w + 1);
-        dts[hl * L + i] = __ldcg(a.ring_dt + ((size_t)s * H + h0 + hl) * L + i);
-    }
-    const int run16 = (w + 1) * N * sa / 16;  // 16-byte chunks of one group's run
-    for (int e = threadIdx.x; e < ng * run16; e += blockDim.x) {
-        const int gl = e / run16, c = e - (e / run16) * run16;
-        reinterpret_cast<uint4*>(braw)[e] = __ldcg(reinterpret_cast<const uint4*>(
-            static_cast<const char*>(a.ring_B) + ((size_t)s * G + g0 + gl) * L * N * sa) + c);
-    }
-    __syncthreads();
+    const int hpg = H / G;
+    const float* cs = sm;
+    const float* dts = cs + G * N;
+    float* bc = sm + G * N + H * (L + 1);
+    const char* braw = reinterpret_cast<const char*>(sm + ((G * N + H * (L + 1) + G * L + 3) & ~3));
 
     // bc[g][i] = B_i . C_t: one warp per (group, entry), lanes over dstate
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-    for (int pair = warp; pair < ng * (w + 1); pair += nwarps) {
-        const int gl = pair / (w + 1), i = pair - (pair / (w + 1)) * (w + 1);
-        const char* Bi = braw + (size_t)(gl * (w + 1) + i) * N * sa;
-        const float* cg = cs + gl * N;
+    for (int pair = warp; pair < G * (w + 1); pair += nwarps) {
+        const int g = pair / (w + 1), i = pair - (pair / (w + 1)) * (w + 1);
+        const char* Bi = braw + ((size_t)g * L + i) * N * sa;
+        const float* cg = cs + g * N;
         float acc = 0.f;
         for (int n = lane; n < N; n += 32) acc = fmaf(load1(Bi, n, bf), cg[n], acc);
 #pragma unroll
         for (int o = 16; o >= 1; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        if (lane == 0) bc[gl * L + i] = acc;
+        if (lane == 0) bc[g * L + i] = acc;
     }
     __syncthreads();
 
-    for (int hl = threadIdx.x; hl < nh; hl += blockDim.x) {
-        const int gl = hl / hpg;
-        const float* dh = dts + hl * L;
-        float* t = tbl + hl * TBL;
-        const float Ah = a.A[h0 + hl];
+    for (int h = threadIdx.x; h < H; h += blockDim.x) {
+        const int g = h / hpg;
+        const float* dh = dts + h * (L + 1);
+        float* t = a.ws + ((size_t)b * H + h) * TBL;
+        const float Ah = a.A[h];
         float suffix = 0.f;
         for (int i = w; i >= 0; --i) {
             const float dti = dh[i];
             const float Pi = expf(Ah * suffix);
-            t[i] = Pi * dti * bc[gl * L + i];
+            t[i] = Pi * dti * bc[g * L + i];
             t[L + i] = Pi * dti;
             suffix += dti;
         }
@@ -143,10 +177,6 @@ __device__ void precompute_groups(const RowArgs& a, int b, int s, int w, int g0,
         t[2 * L] = expf(Ah * suffix);
         for (int i = 2 * L + 1; i < TBL; ++i) t[i] = 0.f;
     }
-    __syncthreads();
-    float4* dst = reinterpret_cast<float4*>(a.ws + ((size_t)b * H + h0) * TBL);
-    const float4* src = reinterpret_cast<const float4*>(tbl);
-    for (int c = threadIdx.x; c < nh * TBL / 4; c += blockDim.x) dst[c] = src[c];
 }
 
 // ----------------------------------------------------------------------------
@@ -158,24 +188,28 @@ __global__ void __launch_bounds__(256) ring_append_kernel(const RowArgs a, const
     const int b = blockIdx.x;
     const int w = given_cursor(b, ci[b], a.num_slots, a.L, row_wp, threadIdx.x == 0 ? dev_err : nullptr);
     if (w < 0) return;
-    append_groups(a, b, ci[b], w, 0, a.G);
+    append_row(a, b, ci[b], w);
 }
 
-__global__ void __launch_bounds__(256) precompute_kernel(const RowArgs a, const int32_t* ci,
-                                                         const int32_t* row_wp) {
+__global__ void __launch_bounds__(kRowThreads) precompute_kernel(const RowArgs a, const int32_t* ci,
+                                                                 const int32_t* row_wp) {
     extern __shared__ __align__(16) float psm[];
     const int b = blockIdx.x;
     // bad slots and cursors are reported by the append and output kernels
     const int w = given_cursor(b, ci[b], a.num_slots, a.L, row_wp, nullptr);
     if (w < 0) return;
-    precompute_groups(a, b, ci[b], w, 0, a.G, psm);
+    stage_slot(a, b, ci[b], psm);
+    __syncthreads();
+    tables_from_smem(a, b, w, psm);
 }
 
 // Cursor advance (when `advance`), ring append and tables of one row in one CTA.
-__global__ void __launch_bounds__(256) prepare_kernel(const RowArgs a, const int32_t* ci,
-                                                      int advance, const uint8_t* force,
-                                                      int32_t* slot_wp, int32_t* row_wp,
-                                                      uint8_t* row_flush, int32_t* dev_err) {
+// The slot's rings are staged while thread 0 reads the cursor; after the append,
+// entry w of the staged copy is patched with the step's dt and B.
+__global__ void __launch_bounds__(kRowThreads) prepare_kernel(const RowArgs a, const int32_t* ci,
+                                                              int advance, const uint8_t* force,
+                                                              int32_t* slot_wp, int32_t* row_wp,
+                                                              uint8_t* row_flush, int32_t* dev_err) {
     extern __shared__ __align__(16) float psm[];
     __shared__ int sh_w;
     const int b = blockIdx.x;
@@ -184,51 +218,24 @@ __global__ void __launch_bounds__(256) prepare_kernel(const RowArgs a, const int
         sh_w = advance ? standard_cursor(b, s, a.num_slots, a.L, slot_wp, force, row_wp, row_flush,
                                          dev_err)
                        : given_cursor(b, s, a.num_slots, a.L, row_wp, dev_err);
+    if (s >= 0 && s < a.num_slots) stage_slot(a, b, s, psm);
     __syncthreads();
     const int w = sh_w;
     if (w < 0) return;
-    append_groups(a, b, s, w, 0, a.G);
-    __syncthreads();  // the appended entry is visible to the whole block
-    precompute_groups(a, b, s, w, 0, a.G, psm);
-}
-
-// The same with one CTA per (row, group), the G CTAs of a row forming a thread-
-// block cluster: every CTA reads the slot's cursor, the cluster barrier orders
-// those reads before the cluster's first CTA advances it, and each CTA appends
-// and builds the tables of its own group.
-__global__ void __launch_bounds__(128) prepare_cluster_kernel(const RowArgs a, const int32_t* ci,
-                                                              int advance, const uint8_t* force,
-                                                              int32_t* slot_wp, int32_t* row_wp,
-                                                              uint8_t* row_flush, int32_t* dev_err) {
-    extern __shared__ __align__(16) float psm[];
-    __shared__ int sh_w;
-    const int b = blockIdx.x / a.G, g = blockIdx.x - (blockIdx.x / a.G) * a.G;
-    const int s = ci[b];
-    if (threadIdx.x == 0) {
-        int w = -1;
-        if (s >= 0 && s < a.num_slots) {
-            w = advance ? slot_wp[s] : row_wp[b];
-            if (w < 0 || w >= a.L) {
-                if (g == 0) set_dev_err(dev_err, RSSM_DEVERR_CURSOR);
-                w = -1;
-            }
-        } else if (s >= a.num_slots && g == 0) {
-            set_dev_err(dev_err, RSSM_DEVERR_SLOT);
-        }
-        sh_w = w;
+    append_row(a, b, s, w);
+    const int H = a.H, N = a.N, G = a.G, L = a.L;
+    const int sa = a.act_bf16 ? 2 : 4;
+    float* dts = psm + G * N;
+    for (int h = threadIdx.x; h < H; h += blockDim.x) dts[h * (L + 1) + w] = step_dt(a, b, h);
+    char* braw = reinterpret_cast<char*>(psm + ((G * N + H * (L + 1) + G * L + 3) & ~3));
+    const int bcn = N * sa / 16;
+    for (int c = threadIdx.x; c < G * bcn; c += blockDim.x) {
+        const int g = c / bcn, j = c - (c / bcn) * bcn;
+        reinterpret_cast<uint4*>(braw + ((size_t)g * L + w) * N * sa)[j] =
+            reinterpret_cast<const uint4*>(static_cast<const char*>(a.B) + (size_t)b * G * N * sa)[c];
     }
-    asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
-    const int w = sh_w;
-    if (advance && g == 0 && threadIdx.x == 0) {
-        const int f = w >= 0 && ((w == a.L - 1) || (force != nullptr && force[b] != 0));
-        row_wp[b] = w >= 0 ? w : 0;
-        row_flush[b] = static_cast<uint8_t>(f);
-        if (w >= 0) slot_wp[s] = f ? 0 : w + 1;
-    }
-    if (w < 0) return;
-    append_groups(a, b, s, w, g, g + 1);
-    __syncthreads();  // the appended entries are visible to the whole block
-    precompute_groups(a, b, s, w, g, g + 1, psm);
+    __syncthreads();
+    tables_from_smem(a, b, w, psm);
 }
 
 RowArgs row_args(const rssm_mamba2_dims* d) {
@@ -280,9 +287,9 @@ extern "C" size_t rssm_mamba2_workspace_size(const rssm_mamba2_dims* d) {
 }
 
 // Shared-memory size of the table-building kernels, checked and opted in.
-static int m2_prologue_smem(const rssm_mamba2_dims* d, const void* kernel, int groups, int* smem) {
-    *smem = m2::precompute_smem(groups * (d->nheads / d->ngroups), d->dstate, groups, d->ring_len,
-                                d->act_dtype == RSSM_BF16 ? 2 : 4);
+static int m2_prologue_smem(const rssm_mamba2_dims* d, const void* kernel, int* smem) {
+    *smem = m2::prologue_smem(d->nheads, d->dstate, d->ngroups, d->ring_len,
+                              d->act_dtype == RSSM_BF16 ? 2 : 4);
     DeviceInfo di;
     if (!device_info(&di)) return RSSM_ERR_CUDA;
     if (*smem > di.max_smem_optin) return RSSM_ERR_UNSUPPORTED;
@@ -304,7 +311,7 @@ extern "C" int rssm_mamba2_precompute(const rssm_mamba2_dims* d, const float* A,
         return RSSM_ERR_INVALID_ARG;
     if (workspace_bytes < rssm_mamba2_workspace_size(d)) return RSSM_ERR_INVALID_ARG;
     int smem = 0;
-    rc = m2_prologue_smem(d, reinterpret_cast<const void*>(m2::precompute_kernel), d->ngroups, &smem);
+    rc = m2_prologue_smem(d, reinterpret_cast<const void*>(m2::precompute_kernel), &smem);
     if (rc) return rc;
     m2::RowArgs ra = m2::row_args(d);
     ra.A = A;
@@ -312,7 +319,7 @@ extern "C" int rssm_mamba2_precompute(const rssm_mamba2_dims* d, const float* A,
     ra.ring_dt = const_cast<float*>(ring_dt);  // read only here
     ra.ring_B = const_cast<void*>(ring_B);
     ra.ws = static_cast<float*>(workspace);
-    m2::precompute_kernel<<<d->batch, 256, smem, (cudaStream_t)stream>>>(ra, cache_indices, row_wp);
+    m2::precompute_kernel<<<d->batch, m2::kRowThreads, smem, (cudaStream_t)stream>>>(ra, cache_indices, row_wp);
     return launch_status();
 }
 
@@ -346,33 +353,9 @@ extern "C" int rssm_mamba2_prepare(const rssm_mamba2_dims* d, int advance,
     ra.ring_dt = ring_dt;
     ra.ring_B = ring_B;
     ra.ws = static_cast<float*>(workspace);
-    const int adv = advance ? 1 : 0;
-    if (d->ngroups <= 8) {
-        // one CTA per (row, group); the row's CTAs form a cluster
-        rc = m2_prologue_smem(d, reinterpret_cast<const void*>(m2::prepare_cluster_kernel), 1, &smem);
-        if (rc) return rc;
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)d->batch * d->ngroups);
-        cfg.blockDim = dim3(128);
-        cfg.dynamicSmemBytes = smem;
-        cfg.stream = (cudaStream_t)stream;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = d->ngroups;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, m2::prepare_cluster_kernel, ra, cache_indices, adv, force_flush,
-                               slot_wp, row_wp, row_flush, dev_err) != cudaSuccess) {
-            cudaGetLastError();
-            return RSSM_ERR_CUDA;
-        }
-        return launch_status();
-    }
-    rc = m2_prologue_smem(d, reinterpret_cast<const void*>(m2::prepare_kernel), d->ngroups, &smem);
+    rc = m2_prologue_smem(d, reinterpret_cast<const void*>(m2::prepare_kernel), &smem);
     if (rc) return rc;
-    m2::prepare_kernel<<<d->batch, 256, smem, (cudaStream_t)stream>>>(
-        ra, cache_indices, adv, force_flush, slot_wp, row_wp, row_flush, dev_err);
+    m2::prepare_kernel<<<d->batch, m2::kRowThreads, smem, (cudaStream_t)stream>>>(
+        ra, cache_indices, advance ? 1 : 0, force_flush, slot_wp, row_wp, row_flush, dev_err);
     return launch_status();
 }

@@ -25,7 +25,8 @@ import torch
 from . import _binding as B
 
 __all__ = ["torch_dtype_code", "Mamba2ReplayDecoder", "Mamba2FullStateDecoder",
-           "GDNReplayDecoder", "GDNFullStateDecoder", "GDNSpecVerifier"]
+           "GDNReplayDecoder", "GDNFullStateDecoder", "GDNSpecVerifier",
+           "GDNSpecFullStateVerifier"]
 
 
 def torch_dtype_code(dt: torch.dtype) -> int:
@@ -373,3 +374,41 @@ class GDNSpecVerifier:
                                      self.ring_d, slots, self.slot_cnt, self.slot_base, out,
                                      self.dev_err, stream)
         return out
+
+
+class GDNSpecFullStateVerifier:
+    """The conventional speculative verify (in-house comparison): every draft's full
+    state is stored as a snapshot [max_batch, T, HV, V, K] float32; the commit copies the
+    accepted draft's snapshot into the slot."""
+
+    def __init__(self, num_v_heads, num_k_heads, head_k_dim, head_v_dim, T, num_slots, max_batch,
+                 act_dtype=torch.bfloat16, out_dtype=torch.bfloat16, device=None):
+        dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+        self.HV, self.HK, self.K, self.V, self.T = (num_v_heads, num_k_heads, head_k_dim,
+                                                    head_v_dim, T)
+        self.num_slots = num_slots
+        self.act_dtype, self.out_dtype = act_dtype, out_dtype
+        self.state = torch.zeros(num_slots, num_v_heads, head_v_dim, head_k_dim, device=dev,
+                                 dtype=torch.float32)
+        self.snap_bytes = B.rssm_gdn_spec_full_state_snapshot_bytes(self.dims(max_batch), T)
+        self.snapshots = torch.empty(max_batch, T, num_v_heads, head_v_dim, head_k_dim,
+                                     device=dev, dtype=torch.float32)
+        self.dev_err = torch.zeros(4, device=dev, dtype=torch.int32)
+        self.o = torch.empty(max_batch, T, num_v_heads, head_v_dim, device=dev, dtype=out_dtype)
+
+    def dims(self, batch):
+        return B.GDNDims(batch, self.HV, self.HK, self.K, self.V, 1, self.num_slots,
+                         torch_dtype_code(self.act_dtype), torch_dtype_code(self.out_dtype))
+
+    def verify(self, q, k, v, beta, g, cache_indices, o=None, stream=None):
+        b = q.shape[0]
+        o = self.o[:b] if o is None else o
+        B.rssm_gdn_spec_full_state_verify(self.dims(b), self.T, self.state, q, k, v, beta, g,
+                                          cache_indices, self.snapshots, self.snap_bytes, o,
+                                          self.dev_err, stream)
+        return o
+
+    def commit(self, cache_indices, num_accepted, stream=None):
+        B.rssm_gdn_spec_full_state_commit(self.dims(cache_indices.shape[0]), self.T, self.state,
+                                          self.snapshots, cache_indices, num_accepted,
+                                          self.dev_err, stream)

@@ -135,3 +135,32 @@ def test_spec_rejects_short_ring():
     with pytest.raises(ssm.RSSMError) as ei:
         Hn.run_gpu_spec(wl, rounds=1)
     assert ei.value.status == ssm.RSSM_ERR_CONFIG
+
+
+@pytest.mark.parametrize("T,L", [(4, 16), (2, 5), (8, 16)])
+def test_spec_full_state_baseline_matches_oracle(T, L):
+    # the conventional verify: per-draft outputs equal the recurrence, and after each
+    # commit the slot holds the state after the accepted prefix
+    from ssm_linear_attention_gb300 import GDNSpecFullStateVerifier
+    wl = W.gdn_spec(batch=5, num_v_heads=4, num_k_heads=2, num_slots=10, L=L, T=T, rounds=9)
+    ad = Hn.torch_dt(wl.act_dtype)
+    ver = GDNSpecFullStateVerifier(wl.num_v_heads, wl.num_k_heads, wl.head_k_dim, wl.head_v_dim,
+                                   T, wl.num_slots, wl.batch, act_dtype=ad,
+                                   out_dtype=torch.float32)
+    ci = wl.cache_indices()
+    for s in ci:
+        ver.state[int(s)] = Hn.to_dev(wl.slot_state(int(s)), torch.float32)
+    ci_d = Hn.to_dev(ci, torch.int32)
+    ref = oracle.gdn_spec_run(wl, rounds=wl.rounds)
+    for r in range(wl.rounds):
+        inp = wl.round_inputs(r)
+        o = ver.verify(Hn.to_dev(inp["q"], ad), Hn.to_dev(inp["k"], ad), Hn.to_dev(inp["v"], ad),
+                       Hn.to_dev(inp["beta"], torch.float32), Hn.to_dev(inp["g"], torch.float32),
+                       ci_d)
+        e = Hn.err(o.cpu().numpy(), ref["o"][r])
+        assert e <= TOL, "round %d: %.3g" % (r, e)
+        ver.commit(ci_d, Hn.to_dev(wl.accepted(r), torch.int32))
+    torch.cuda.synchronize()
+    st = ver.state[torch.as_tensor(ci.astype(np.int64), device="cuda")].cpu().numpy()
+    assert Hn.err(st, ref["state"]) <= TOL
+    assert int(ver.dev_err.abs().sum()) == 0
