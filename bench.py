@@ -52,6 +52,7 @@ if ROOT not in sys.path:
 
 METRIC = "decode rows/s and µs/step at batch 512; achieved HBM GB/s vs ~8 TB/s peak"
 UNIT = "rows/s"
+EVENT_EVERY = 8  # output-kernel events on every 8th timed step (an event record costs ~5 us)
 WORKLOAD = ("mamba2 replayssm decode: batch 512, nheads 128, headdim 64, dstate 128, ngroups 8, "
             "L 16, bf16 state pool 1024 slots, desync write_pos U{0..15}, 64 steps cycled")
 
@@ -327,16 +328,43 @@ def _bus_id(dev):
         return None
 
 
-def _timed_graphs(pre, main, K, dist, dev, offset=0, clocks=True):
-    """Replay K steps: pre[k % G] (may be None), an event, main[k % G], an event.
-    Returns (elapsed ms of the whole region, max over ranks; per-step main ms;
-    clock record)."""
+def _sampled_graphs(fns, kernel_fns):
+    """Per input set j two graphs: whole[j] runs fns[j]; samp[j] runs the same work
+    with external CUDA events recorded around kernel_fns[j] (the kernel being timed),
+    so the events are nodes of the graph and time that kernel alone. kernel_fns[j] is
+    a pair (before, kernel, after) of callables."""
+    import torch
+    whole = _graphs(fns)
+    samp, evs = [], []
+    for before, kern, after in kernel_fns:
+        a = torch.cuda.Event(enable_timing=True, external=True)
+        b = torch.cuda.Event(enable_timing=True, external=True)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            if before is not None:
+                before()
+            a.record()
+            kern()
+            b.record()
+            if after is not None:
+                after()
+        samp.append(g)
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    return whole, samp, evs
+
+
+def _timed_graphs(whole, samp, evs, K, dist, dev, offset=0, clocks=True, every=EVENT_EVERY):
+    """Replay K steps; step k runs input set j = (k + offset) % G, as samp[j] when
+    k % every == 0 (events around the timed kernel) and as whole[j] otherwise.
+    Returns (elapsed ms of the region, max over ranks; the timed kernel's ms from
+    the last sampled replay of each input set; clock record; the step index of each
+    of those samples)."""
     import torch
     stream = torch.cuda.current_stream()
-    G = len(main)
-    ev_a = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
-    ev_b = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    G = len(whole)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    last = {}
     dist.barrier()
     torch.cuda.synchronize()
     clk = ClockSampler() if clocks else None
@@ -345,17 +373,18 @@ def _timed_graphs(pre, main, K, dist, dev, offset=0, clocks=True):
     start.record(stream)
     for k in range(K):
         j = (k + offset) % G
-        if pre is not None:
-            pre[j].replay()
-        ev_a[k].record(stream)
-        main[j].replay()
-        ev_b[k].record(stream)
+        if k % every == 0:
+            samp[j].replay()
+            last[j] = k
+        else:
+            whole[j].replay()
     end.record(stream)
     torch.cuda.synchronize()
     dist.barrier()
     rec = clk.stop(_bus_id(dev)) if clk else None
-    per = [a.elapsed_time(b) for a, b in zip(ev_a, ev_b)]
-    return dist.max(start.elapsed_time(end)), per, rec
+    js = [j for j in sorted(last) if evs[j][0] is not None]
+    per = [evs[j][0].elapsed_time(evs[j][1]) for j in js]
+    return dist.max(start.elapsed_time(end)), per, rec, [last[j] for j in js]
 
 
 # --------------------------------------------------------------------------- #
@@ -479,24 +508,25 @@ def run_mamba2(args, dist):
         pre_fn(k % G)()
         out_fn(k % G)()
     torch.cuda.synchronize()
-    g_pre = _graphs([pre_fn(j) for j in range(G)])
-    g_out = _graphs([out_fn(j) for j in range(G)])
+    g_step, g_samp, evs = _sampled_graphs(
+        [(lambda j=j: (pre_fn(j)(), out_fn(j)())) for j in range(G)],
+        [(pre_fn(j), out_fn(j), None) for j in range(G)])
     # capture does not run the work: warm up the graphs themselves
     for k in range(max(args.warmup, 3)):
-        g_pre[k % G].replay()
-        g_out[k % G].replay()
+        g_step[k % G].replay()
     torch.cuda.synchronize()
     slot_wp0 = dec.slot_wp.cpu().numpy().astype(np.int64)
+    off = args.warmup + max(args.warmup, 3)
 
-    elapsed, out_ms, clocks = _timed_graphs(g_pre, g_out, K, dist, dev, offset=args.warmup)
+    elapsed, out_ms, clocks, ks = _timed_graphs(g_step, g_samp, evs, K, dist, dev, offset=off)
     assert int(dec.dev_err.abs().sum().item()) == 0, "device error flag set during the bench"
-    del g_pre, g_out
+    del g_step, g_samp
 
     ms_step = elapsed / K
     rows_s = dist.world * wl.batch / (ms_step * 1e-3)
 
     curs = simulate_cursors(slot_wp0, ci_np, wl.L, K)
-    out_b = np.mean([output_kernel_bytes(wl, w, f) for w, f in curs])
+    out_b = np.mean([output_kernel_bytes(wl, *curs[k]) for k in ks])
     step_b = np.mean([step_bytes(wl, w, f) for w, f in curs])
     out_avg_ms = float(np.mean(out_ms))
     peak, peak_kind = read_peaks()
@@ -559,10 +589,11 @@ def run_mamba2(args, dist):
         for k in range(max(args.warmup, 3)):
             full_fn(k % G)()
         torch.cuda.synchronize()
-        g_full = _graphs([full_fn(j) for j in range(G)])
+        g_full, g_fs, fevs = _sampled_graphs([full_fn(j) for j in range(G)],
+                                             [(None, full_fn(j), None) for j in range(G)])
         Kf = max(50, K // 4)
-        f_el, f_per, _ = _timed_graphs(None, g_full, Kf, dist, dev, clocks=False)
-        del g_full
+        f_el, f_per, _, _ = _timed_graphs(g_full, g_fs, fevs, Kf, dist, dev, clocks=False)
+        del g_full, g_fs
         f_ms = f_el / Kf
         fb = full_state_bytes(wl, wl.batch)
         full = {"ms_per_step": f_ms, "us_per_step": f_ms * 1e3,
@@ -586,7 +617,7 @@ def run_mamba2(args, dist):
                    "dstate": wl.dstate, "ngroups": wl.ngroups, "ring_len": wl.L,
                    "state_dtype": "bf16", "act_dtype": "bf16", "out_dtype": "bf16",
                    "parallelism": "independent replica per gpu (dp%d)" % dist.world,
-                   "timing": "CUDA graphs: prepare (cursor+append+tables) | output, events between",
+                   "timing": "CUDA graphs; every 8th step as prepare | output with CUDA events between (the output kernel's duration), the others as one prepare+output graph",
                    "l2": "inputs larger than L2: 1.07 GB of checkpoint tiles streamed per step"},
         "achieved_hbm_gbs": step_b / (ms_step * 1e-3) / 1e9,
         "hbm_frac_step": step_b / (ms_step * 1e-3) / 1e9 / peak,
@@ -659,21 +690,22 @@ def run_gdn(args, dist, sub=False):
         pre_fn(k % G)()
         out_fn(k % G)()
     torch.cuda.synchronize()
-    g_pre = _graphs([pre_fn(j) for j in range(G)])
-    g_out = _graphs([out_fn(j) for j in range(G)])
+    g_step, g_samp, evs = _sampled_graphs(
+        [(lambda j=j: (pre_fn(j)(), out_fn(j)())) for j in range(G)],
+        [(pre_fn(j), out_fn(j), None) for j in range(G)])
     for k in range(max(args.warmup, 3)):
-        g_pre[k % G].replay()
-        g_out[k % G].replay()
+        g_step[k % G].replay()
     torch.cuda.synchronize()
     slot_wp0 = dec.slot_wp.cpu().numpy().astype(np.int64)
-    elapsed, out_ms, clocks = _timed_graphs(g_pre, g_out, K, dist, dev, offset=args.warmup,
-                                            clocks=not sub)
+    off = args.warmup + max(args.warmup, 3)
+    elapsed, out_ms, clocks, ks = _timed_graphs(g_step, g_samp, evs, K, dist, dev, offset=off,
+                                                clocks=not sub)
     assert int(dec.dev_err.abs().sum().item()) == 0, "device error flag set during the gdn bench"
-    del g_pre, g_out
+    del g_step, g_samp
     ms_step = elapsed / K
     rows_s = dist.world * wl.batch / (ms_step * 1e-3)
     curs = simulate_cursors(slot_wp0, ci_np, wl.L, K)
-    out_b = np.mean([gdn_output_bytes(wl, w, f) for w, f in curs])
+    out_b = np.mean([gdn_output_bytes(wl, *curs[k]) for k in ks])
     out_avg_ms = float(np.mean(out_ms))
     peak, peak_kind = read_peaks()
     achieved = out_b / (out_avg_ms * 1e-3) / 1e9
@@ -693,10 +725,11 @@ def run_gdn(args, dist, sub=False):
         for k in range(max(args.warmup, 3)):
             full_fn(k % G)()
         torch.cuda.synchronize()
-        g_full = _graphs([full_fn(j) for j in range(G)])
+        g_full, g_fs, fevs = _sampled_graphs([full_fn(j) for j in range(G)],
+                                             [(None, full_fn(j), None) for j in range(G)])
         Kf = max(50, K // 4)
-        f_el, f_per, _ = _timed_graphs(None, g_full, Kf, dist, dev, clocks=False)
-        del g_full
+        f_el, f_per, _, _ = _timed_graphs(g_full, g_fs, fevs, Kf, dist, dev, clocks=False)
+        del g_full, g_fs
         f_ms = f_el / Kf
         fb = gdn_full_bytes(wl, wl.batch)
         full = {"ms_per_step": f_ms, "us_per_step": f_ms * 1e3,
@@ -713,7 +746,7 @@ def run_gdn(args, dist, sub=False):
         "config": {"workload": GDN_WORKLOAD, "global_batch": dist.world * wl.batch,
                    "batch_per_gpu": wl.batch, "HV": wl.num_v_heads, "HK": wl.num_k_heads,
                    "K": wl.head_k_dim, "V": wl.head_v_dim, "ring_len": wl.L,
-                   "timing": "CUDA graphs: prepare (cursor+append+tables) | output, events between",
+                   "timing": "CUDA graphs; every 8th step as prepare | output with CUDA events between (the output kernel's duration), the others as one prepare+output graph",
                    "l2": "inputs larger than L2: 537 MB of fp32 checkpoint tiles per step"},
         "roofline": {"bound": "hbm", "kernel": "gdn output kernel (fp32 state, 32-row tiles)",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
@@ -785,15 +818,16 @@ def run_spec(args, dist, sub=False):
     for k in range(W0):
         round_fn(k % G)()
     torch.cuda.synchronize()
-    graphs = _graphs([round_fn(j) for j in range(G)])
+    graphs, g_rs, revs = _sampled_graphs([round_fn(j) for j in range(G)],
+                                         [(None, round_fn(j), None) for j in range(G)])
     for k in range(W0):
         graphs[(W0 + k) % G].replay()
     torch.cuda.synchronize()
     offset = 2 * W0
-    elapsed, per, clocks = _timed_graphs(None, graphs, K, dist, dev, offset=offset,
-                                         clocks=not sub)
+    elapsed, per, clocks, ks = _timed_graphs(graphs, g_rs, revs, K, dist, dev, offset=offset,
+                                             clocks=not sub)
     assert int(ver.dev_err.abs().sum().item()) == 0, "device error flag set during the spec bench"
-    del graphs
+    del graphs, g_rs
     ms_round = elapsed / K
     # byte count from the cursor sequence of all rounds run so far
     seq = [accs[k % G] for k in range(offset + K)]
@@ -801,7 +835,7 @@ def run_spec(args, dist, sub=False):
     dev_cnt = ver.slot_cnt.cpu().numpy().astype(np.int64)
     assert np.array_equal(dev_cnt[ci_np], cnt_end[ci_np]), "spec cursor bookkeeping disagrees"
     vb, fb = [], []
-    for hist, fl, fold in sim[offset:]:
+    for hist, fl, fold in [sim[offset + k] for k in ks]:  # the rounds whose duration was sampled
         v_b, f_b = spec_round_bytes(wl, hist, fold)
         vb.append(v_b)
         fb.append(f_b)
@@ -830,11 +864,12 @@ def run_spec(args, dist, sub=False):
         for k in range(W0):
             full_fn(k % G)()
         torch.cuda.synchronize()
-        g_full = _graphs([full_fn(j) for j in range(G)])
+        g_full, g_fs, fevs = _sampled_graphs([full_fn(j) for j in range(G)],
+                                             [(None, full_fn(j), None) for j in range(G)])
         Kf = max(50, K // 4)
-        f_el, _, _ = _timed_graphs(None, g_full, Kf, dist, dev, clocks=False)
+        f_el, _, _, _ = _timed_graphs(g_full, g_fs, fevs, Kf, dist, dev, clocks=False)
         assert int(fver.dev_err.abs().sum().item()) == 0
-        del g_full, fver
+        del g_full, g_fs, fver
         f_ms = f_el / Kf
         HV, HK, Kd, Vd = wl.num_v_heads, wl.num_k_heads, wl.head_k_dim, wl.head_v_dim
         sab = 2 if wl.act_dtype == "bf16" else 4
@@ -929,7 +964,8 @@ def run_sweep(args, dist):
                 g_rep = _graphs([rep_fn(j) for j in range(nsets)])
                 for k in range(3):
                     g_rep[k].replay()
-                el, _, _ = _timed_graphs(None, g_rep, K, dist, dev, clocks=False)
+                el, _, _, _ = _timed_graphs(g_rep, g_rep, [(None, None)] * nsets, K, dist, dev,
+                                            clocks=False, every=K + 1)
                 assert int(dec.dev_err.abs().sum().item()) == 0
                 del g_rep
                 rep_ms = el / K
@@ -950,7 +986,8 @@ def run_sweep(args, dist):
                 g_full = _graphs([full_fn(j) for j in range(nsets)])
                 for k in range(3):
                     g_full[k].replay()
-                fel, _, _ = _timed_graphs(None, g_full, K, dist, dev, clocks=False)
+                fel, _, _, _ = _timed_graphs(g_full, g_full, [(None, None)] * nsets, K, dist, dev,
+                                             clocks=False, every=K + 1)
                 del g_full, fdec
                 full_ms = fel / K
                 fb = full_state_bytes(wl, batch)

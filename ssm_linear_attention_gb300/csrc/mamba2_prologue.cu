@@ -10,14 +10,16 @@
 //
 // Kernels (one CTA per row):
 //   ring_append_kernel  x, dt = softplus(dt_raw + dt_bias), B into ring entry w.
-//   precompute_kernel   stages C_t and the slot's whole dt and B rings in shared
-//                       memory, then B_i . C_t per group and the decay suffix
-//                       products per head, written as per-(row, head) tables.
-//   prepare_kernel      cursor step + ring append + tables: the slot's rings are
-//                       staged while the cursor is read, entry w is patched from
-//                       the step's inputs.
-// The tables are latency-bound work on a few tens of KB per row, so every load a
-// thread makes is issued before any of its results is used.
+//   precompute_kernel   stages C_t, A and the slot's whole dt and B rings in shared
+//                       memory with 1-D bulk copies on one mbarrier, then B_i . C_t
+//                       per group and the decay suffix products per head (a
+//                       segmented warp scan), written as per-(row, head) tables.
+//   prepare_kernel      cursor step + ring append + tables: the staging copies are
+//                       issued before the cursor is read and the step's inputs are
+//                       loaded into registers meanwhile; entry w of the staged
+//                       rings is patched from the inputs.
+// The prologue is latency-bound work on a few tens of KB per row, so each CTA
+// waits for one round trip to memory, not one per loop iteration.
 #include "common.cuh"
 #include "cursor.cuh"
 #include "internal.h"
@@ -47,24 +49,6 @@ struct RowArgs {
 
 constexpr int kRowThreads = 512;
 
-// n elements from src to dst; each thread issues four loads before its four stores.
-template <class V>
-__device__ __forceinline__ void copy4(V* dst, const V* src, int n) {
-    for (int base = threadIdx.x; base < n; base += 4 * blockDim.x) {
-        V r[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int i = base + u * blockDim.x;
-            if (i < n) r[u] = __ldcg(src + i);
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int i = base + u * blockDim.x;
-            if (i < n) dst[i] = r[u];
-        }
-    }
-}
-
 __device__ __forceinline__ float step_dt(const RowArgs& a, int b, int h) {
     float v = a.dt_raw[(size_t)b * a.H + h] + (a.dt_bias ? a.dt_bias[h] : 0.f);
     return a.softplus ? softplus_f(v) : v;
@@ -93,89 +77,151 @@ __device__ void append_row(const RowArgs& a, int b, int s, int w) {
     }
 }
 
-// Shared memory of the table-building kernels, in bytes: C_t [G][N] f32, the dt
-// ring [H][L+1] f32 (rows padded to an odd stride), B . C [G][L] f32, the B ring
-// [G][L][N] (activation type).
-__host__ __device__ inline int prologue_smem(int H, int N, int G, int L, int sa) {
-    return ((G * N + H * (L + 1) + G * L + 3) & ~3) * 4 + G * L * N * sa;
-}
-
-// Row b's C_t and slot s's whole dt and B rings into shared memory.
-__device__ void stage_slot(const RowArgs& a, int b, int s, float* sm) {
-    const int H = a.H, N = a.N, G = a.G, L = a.L;
-    const bool bf = a.act_bf16;
-    const int sa = bf ? 2 : 4;
-    float* cs = sm;
-    float* dts = cs + G * N;
-    char* braw = reinterpret_cast<char*>(sm + ((G * N + H * (L + 1) + G * L + 3) & ~3));
-    for (int e = threadIdx.x * 8; e < G * N; e += blockDim.x * 8)
-        load8(static_cast<const char*>(a.C) + ((size_t)b * G * N + e) * sa, bf, cs + e);
-    const float* dr = a.ring_dt + (size_t)s * H * L;
-    for (int base = threadIdx.x; base < H * L; base += 4 * blockDim.x) {
-        float r[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int i = base + u * blockDim.x;
-            if (i < H * L) r[u] = __ldcg(dr + i);
-        }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            const int i = base + u * blockDim.x;
-            if (i < H * L) dts[(i / L) * (L + 1) + (i - (i / L) * L)] = r[u];
-        }
+// Shared memory of the table-building kernels (byte offsets, 16-byte aligned):
+// C_t [G][N] and the slot's B ring [G][L][N] in the activation type, A [H], the
+// slot's dt ring [H][L] and B . C [G][L] in fp32.
+struct ProLayout {
+    int c, A, dt, bc, B, total;
+    __host__ __device__ ProLayout(int H, int N, int G, int L, int sa) {
+        auto up = [](int x) { return (x + 15) & ~15; };
+        c = 0;
+        A = up(G * N * sa);
+        dt = A + up(H * 4);
+        bc = dt + up(H * L * 4);
+        B = bc + up(G * L * 4);
+        total = B + G * L * N * sa;
     }
-    copy4(reinterpret_cast<uint4*>(braw),
-          reinterpret_cast<const uint4*>(static_cast<const char*>(a.ring_B) + (size_t)s * G * L * N * sa),
-          G * L * N * sa / 16);
+};
+
+// Stage row b's C_t, A and slot s's whole dt and B rings with 1-D bulk copies
+// completing on `bar` (issued by one thread; the dt ring and A fall back to plain
+// loads by that thread when their sizes are not multiples of 16 bytes). Returns the
+// bytes the barrier expects.
+__device__ void stage_issue(const RowArgs& a, int b, int s, uint8_t* sm, uint64_t* bar) {
+    const int H = a.H, N = a.N, G = a.G, L = a.L;
+    const int sa = a.act_bf16 ? 2 : 4;
+    const ProLayout lo(H, N, G, L, sa);
+    const bool bulk_dt = ((H * L) & 3) == 0 && (H & 3) == 0;
+    uint32_t bytes = G * N * sa + G * L * N * sa + (bulk_dt ? (H + H * L) * 4 : 0);
+    mbar_arrive_expect_tx(bar, bytes);
+    bulk_g2s(sm + lo.c, static_cast<const char*>(a.C) + (size_t)b * G * N * sa, G * N * sa, bar);
+    bulk_g2s(sm + lo.B, static_cast<const char*>(a.ring_B) + (size_t)s * G * L * N * sa,
+             G * L * N * sa, bar);
+    if (bulk_dt) {
+        bulk_g2s(sm + lo.A, a.A, H * 4, bar);
+        bulk_g2s(sm + lo.dt, a.ring_dt + (size_t)s * H * L, H * L * 4, bar);
+    } else {
+        float* As = reinterpret_cast<float*>(sm + lo.A);
+        float* dts = reinterpret_cast<float*>(sm + lo.dt);
+        for (int h = 0; h < H; ++h) As[h] = a.A[h];
+        for (int i = 0; i < H * L; ++i) dts[i] = a.ring_dt[(size_t)s * H * L + i];
+    }
 }
 
 // Row b's tables from the staged rings (entries 0..w):
-//   P_i = exp(A_h sum_{j>i} dt_j), coef_i = P_i dt_i (B_i . C_t), a_i = P_i dt_i,
+//   P_i = exp(A_h sum_{i<j<=w} dt_j), coef_i = P_i dt_i (B_i . C_t), a_i = P_i dt_i,
 //   Pm1 = exp(A_h sum_{j<=w} dt_j), written straight to the workspace.
-__device__ void tables_from_smem(const RowArgs& a, int b, int w, float* sm) {
+// B . C: eight lanes per entry (N/8 dstate columns each, three shuffle levels).
+// Tables: a segment of LS = pow2ceil(L) <= 32 lanes per head, lane i = entry i; the
+// suffix sums come from a segmented warp scan, so every entry's exp runs in
+// parallel and a head's table row is written by consecutive lanes.
+__device__ void tables_from_smem(const RowArgs& a, int b, int w, uint8_t* sm) {
     const int H = a.H, N = a.N, G = a.G, L = a.L;
     const int TBL = tbl_floats(L);
     const bool bf = a.act_bf16;
     const int sa = bf ? 2 : 4;
     const int hpg = H / G;
-    const float* cs = sm;
-    const float* dts = cs + G * N;
-    float* bc = sm + G * N + H * (L + 1);
-    const char* braw = reinterpret_cast<const char*>(sm + ((G * N + H * (L + 1) + G * L + 3) & ~3));
-
-    // bc[g][i] = B_i . C_t: one warp per (group, entry), lanes over dstate
+    const ProLayout lo(H, N, G, L, sa);
+    const char* craw = reinterpret_cast<const char*>(sm + lo.c);
+    const char* braw = reinterpret_cast<const char*>(sm + lo.B);
+    const float* As = reinterpret_cast<const float*>(sm + lo.A);
+    const float* dts = reinterpret_cast<const float*>(sm + lo.dt);
+    float* bc = reinterpret_cast<float*>(sm + lo.bc);
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
-    for (int pair = warp; pair < G * (w + 1); pair += nwarps) {
-        const int g = pair / (w + 1), i = pair - (pair / (w + 1)) * (w + 1);
-        const char* Bi = braw + ((size_t)g * L + i) * N * sa;
-        const float* cg = cs + g * N;
-        float acc = 0.f;
-        for (int n = lane; n < N; n += 32) acc = fmaf(load1(Bi, n, bf), cg[n], acc);
+
+    {  // bc[g][i] = B_i . C_t
+        const int sub = lane >> 3, part = lane & 7;  // 4 entries per warp, 8 lanes each
+        const int per = N / 8;                        // columns per lane
+        for (int p0 = warp * 4; p0 < G * (w + 1); p0 += nwarps * 4) {
+            const int pair = p0 + sub;
+            float acc = 0.f;
+            int g = 0, i = 0;
+            if (pair < G * (w + 1)) {
+                g = pair / (w + 1);
+                i = pair - g * (w + 1);
+                const char* Bi = braw + ((size_t)g * L + i) * N * sa;
+                const char* Cg = craw + (size_t)g * N * sa;
+                for (int n = part * per; n < (part + 1) * per; n += 8) {
+                    float fb[8], fc[8];
+                    load8(Bi + (size_t)n * sa, bf, fb);
+                    load8(Cg + (size_t)n * sa, bf, fc);
 #pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        if (lane == 0) bc[g * L + i] = acc;
+                    for (int u = 0; u < 8; ++u) acc = fmaf(fb[u], fc[u], acc);
+                }
+            }
+            acc += __shfl_xor_sync(0xffffffffu, acc, 4);
+            acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+            acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+            if (part == 0 && pair < G * (w + 1)) bc[g * L + i] = acc;
+        }
     }
     __syncthreads();
 
-    for (int h = threadIdx.x; h < H; h += blockDim.x) {
-        const int g = h / hpg;
-        const float* dh = dts + h * (L + 1);
-        float* t = a.ws + ((size_t)b * H + h) * TBL;
-        const float Ah = a.A[h];
-        float suffix = 0.f;
-        for (int i = w; i >= 0; --i) {
-            const float dti = dh[i];
-            const float Pi = expf(Ah * suffix);
-            t[i] = Pi * dti * bc[g * L + i];
-            t[L + i] = Pi * dti;
-            suffix += dti;
+    if (L <= 32) {
+        int LS = 1;
+        while (LS < L) LS <<= 1;
+        const int hpw = 32 / LS;  // heads per warp pass
+        const int i = lane & (LS - 1);
+        for (int h0 = warp * hpw; h0 < H; h0 += nwarps * hpw) {
+            const int h = h0 + lane / LS;
+            const bool live = h < H;
+            const float dti = (live && i <= w) ? dts[h * L + i] : 0.f;
+            float incl = dti;  // sum_{i<=j<=w} dt_j after the scan
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                if (off < LS) {
+                    const float v = __shfl_down_sync(0xffffffffu, incl, off, LS);
+                    if (i + off < LS) incl += v;
+                }
+            }
+            const float total = __shfl_sync(0xffffffffu, incl, 0, LS);
+            if (live) {
+                const float Ah = As[h];
+                float* t = a.ws + ((size_t)b * H + h) * TBL;
+                if (i < L) {
+                    float ci = 0.f, ai = 0.f;
+                    if (i <= w) {
+                        const float Pi = expf(Ah * (incl - dti));
+                        ai = Pi * dti;
+                        ci = ai * bc[(h / hpg) * L + i];
+                    }
+                    t[i] = ci;
+                    t[L + i] = ai;
+                }
+                for (int e = 2 * L + i; e < TBL; e += LS) t[e] = e == 2 * L ? expf(Ah * total) : 0.f;
+            }
         }
-        for (int i = w + 1; i < L; ++i) {
-            t[i] = 0.f;
-            t[L + i] = 0.f;
+    } else {
+        for (int h = threadIdx.x; h < H; h += blockDim.x) {
+            const int g = h / hpg;
+            const float* dh = dts + h * L;
+            float* t = a.ws + ((size_t)b * H + h) * TBL;
+            const float Ah = As[h];
+            float suffix = 0.f;
+            for (int i = w; i >= 0; --i) {
+                const float dti = dh[i];
+                const float Pi = expf(Ah * suffix);
+                t[i] = Pi * dti * bc[g * L + i];
+                t[L + i] = Pi * dti;
+                suffix += dti;
+            }
+            for (int i = w + 1; i < L; ++i) {
+                t[i] = 0.f;
+                t[L + i] = 0.f;
+            }
+            t[2 * L] = expf(Ah * suffix);
+            for (int i = 2 * L + 1; i < TBL; ++i) t[i] = 0.f;
         }
-        t[2 * L] = expf(Ah * suffix);
-        for (int i = 2 * L + 1; i < TBL; ++i) t[i] = 0.f;
     }
 }
 
@@ -192,47 +238,97 @@ __global__ void __launch_bounds__(256) ring_append_kernel(const RowArgs a, const
 }
 
 __global__ void __launch_bounds__(kRowThreads) precompute_kernel(const RowArgs a, const int32_t* ci,
-                                                                 const int32_t* row_wp) {
-    extern __shared__ __align__(16) float psm[];
+                                                                 const int32_t* row_wp,
+                                                                 int32_t* dev_err) {
+    extern __shared__ __align__(128) uint8_t psm[];
+    __shared__ uint64_t bar;
     const int b = blockIdx.x;
+    const int s = ci[b];
     // bad slots and cursors are reported by the append and output kernels
-    const int w = given_cursor(b, ci[b], a.num_slots, a.L, row_wp, nullptr);
+    const int w = given_cursor(b, s, a.num_slots, a.L, row_wp, nullptr);
     if (w < 0) return;
-    stage_slot(a, b, ci[b], psm);
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_barrier_init();
+        stage_issue(a, b, s, psm, &bar);
+    }
     __syncthreads();
+    if (!mbar_wait_bounded(&bar, 0)) {
+        if (threadIdx.x == 0) set_dev_err(dev_err, RSSM_DEVERR_TIMEOUT);
+        return;
+    }
     tables_from_smem(a, b, w, psm);
 }
 
 // Cursor advance (when `advance`), ring append and tables of one row in one CTA.
-// The slot's rings are staged while thread 0 reads the cursor; after the append,
-// entry w of the staged copy is patched with the step's dt and B.
+// Thread 0 issues the staging copies before it reads the cursor; meanwhile every
+// thread loads its share of the step's x, dt and B into registers. After the
+// append, entry w of the staged rings is patched with the step's dt and B.
+constexpr int kMaxXChunks = 8;  // 16-byte chunks of x per thread (H*P*sa/16 <= 8*512)
+
 __global__ void __launch_bounds__(kRowThreads) prepare_kernel(const RowArgs a, const int32_t* ci,
                                                               int advance, const uint8_t* force,
                                                               int32_t* slot_wp, int32_t* row_wp,
                                                               uint8_t* row_flush, int32_t* dev_err) {
-    extern __shared__ __align__(16) float psm[];
+    extern __shared__ __align__(128) uint8_t psm[];
+    __shared__ uint64_t bar;
     __shared__ int sh_w;
+    const int H = a.H, P = a.P, N = a.N, G = a.G, L = a.L;
+    const int sa = a.act_bf16 ? 2 : 4;
     const int b = blockIdx.x;
     const int s = ci[b];
-    if (threadIdx.x == 0)
-        sh_w = advance ? standard_cursor(b, s, a.num_slots, a.L, slot_wp, force, row_wp, row_flush,
+    const bool staged = s >= 0 && s < a.num_slots;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_barrier_init();
+        if (staged) stage_issue(a, b, s, psm, &bar);
+        sh_w = advance ? standard_cursor(b, s, a.num_slots, L, slot_wp, force, row_wp, row_flush,
                                          dev_err)
-                       : given_cursor(b, s, a.num_slots, a.L, row_wp, dev_err);
-    if (s >= 0 && s < a.num_slots) stage_slot(a, b, s, psm);
+                       : given_cursor(b, s, a.num_slots, L, row_wp, dev_err);
+    }
+    // the step's inputs, independent of the cursor
+    const int xc = P * sa / 16, nx = H * xc;
+    const uint4* xs = reinterpret_cast<const uint4*>(static_cast<const char*>(a.x) + (size_t)b * H * P * sa);
+    uint4 xr[kMaxXChunks];
+#pragma unroll
+    for (int u = 0; u < kMaxXChunks; ++u) {
+        const int c = threadIdx.x + u * blockDim.x;
+        if (c < nx) xr[u] = xs[c];
+    }
+    const int bcn = N * sa / 16;
+    uint4 br = make_uint4(0, 0, 0, 0);
+    if (threadIdx.x < G * bcn)
+        br = reinterpret_cast<const uint4*>(static_cast<const char*>(a.B) + (size_t)b * G * N * sa)[threadIdx.x];
+    float dtr = 0.f;
+    if (threadIdx.x < H) dtr = step_dt(a, b, threadIdx.x);
     __syncthreads();
     const int w = sh_w;
+    if (staged && !mbar_wait_bounded(&bar, 0)) {
+        if (threadIdx.x == 0) set_dev_err(dev_err, RSSM_DEVERR_TIMEOUT);
+        return;
+    }
     if (w < 0) return;
-    append_row(a, b, s, w);
-    const int H = a.H, N = a.N, G = a.G, L = a.L;
-    const int sa = a.act_bf16 ? 2 : 4;
-    float* dts = psm + G * N;
-    for (int h = threadIdx.x; h < H; h += blockDim.x) dts[h * (L + 1) + w] = step_dt(a, b, h);
-    char* braw = reinterpret_cast<char*>(psm + ((G * N + H * (L + 1) + G * L + 3) & ~3));
-    const int bcn = N * sa / 16;
-    for (int c = threadIdx.x; c < G * bcn; c += blockDim.x) {
-        const int g = c / bcn, j = c - (c / bcn) * bcn;
-        reinterpret_cast<uint4*>(braw + ((size_t)g * L + w) * N * sa)[j] =
-            reinterpret_cast<const uint4*>(static_cast<const char*>(a.B) + (size_t)b * G * N * sa)[c];
+    // append, from registers, and patch entry w of the staged rings
+    const ProLayout lo(H, N, G, L, sa);
+#pragma unroll
+    for (int u = 0; u < kMaxXChunks; ++u) {
+        const int c = threadIdx.x + u * blockDim.x;
+        if (c < nx) {
+            const int h = c / xc, j = c - (c / xc) * xc;
+            reinterpret_cast<uint4*>(static_cast<char*>(a.ring_x) + (((size_t)s * H + h) * L + w) * P * sa)[j] =
+                xr[u];
+        }
+    }
+    float* dts = reinterpret_cast<float*>(psm + lo.dt);
+    for (int h = threadIdx.x; h < H; h += blockDim.x) {
+        const float v = h == threadIdx.x ? dtr : step_dt(a, b, h);
+        a.ring_dt[((size_t)s * H + h) * L + w] = v;
+        dts[h * L + w] = v;
+    }
+    if (threadIdx.x < G * bcn) {
+        const int g = threadIdx.x / bcn, j = threadIdx.x - (threadIdx.x / bcn) * bcn;
+        reinterpret_cast<uint4*>(static_cast<char*>(a.ring_B) + (((size_t)s * G + g) * L + w) * N * sa)[j] = br;
+        reinterpret_cast<uint4*>(psm + lo.B + ((size_t)g * L + w) * N * sa)[j] = br;
     }
     __syncthreads();
     tables_from_smem(a, b, w, psm);
@@ -288,8 +384,11 @@ extern "C" size_t rssm_mamba2_workspace_size(const rssm_mamba2_dims* d) {
 
 // Shared-memory size of the table-building kernels, checked and opted in.
 static int m2_prologue_smem(const rssm_mamba2_dims* d, const void* kernel, int* smem) {
-    *smem = m2::prologue_smem(d->nheads, d->dstate, d->ngroups, d->ring_len,
-                              d->act_dtype == RSSM_BF16 ? 2 : 4);
+    *smem = m2::ProLayout(d->nheads, d->dstate, d->ngroups, d->ring_len,
+                          d->act_dtype == RSSM_BF16 ? 2 : 4).total;
+    if ((long)d->nheads * d->headdim * (d->act_dtype == RSSM_BF16 ? 2 : 4) / 16 >
+        (long)m2::kMaxXChunks * m2::kRowThreads)
+        return RSSM_ERR_UNSUPPORTED;
     DeviceInfo di;
     if (!device_info(&di)) return RSSM_ERR_CUDA;
     if (*smem > di.max_smem_optin) return RSSM_ERR_UNSUPPORTED;
@@ -302,7 +401,6 @@ extern "C" int rssm_mamba2_precompute(const rssm_mamba2_dims* d, const float* A,
                                       const int32_t* cache_indices, const int32_t* row_wp,
                                       void* workspace, size_t workspace_bytes, int32_t* dev_err,
                                       rssm_stream_t stream) {
-    (void)dev_err;
     int rc = m2::check_dims(d);
     if (rc) return rc;
     if (d->batch == 0) return RSSM_OK;
@@ -319,7 +417,8 @@ extern "C" int rssm_mamba2_precompute(const rssm_mamba2_dims* d, const float* A,
     ra.ring_dt = const_cast<float*>(ring_dt);  // read only here
     ra.ring_B = const_cast<void*>(ring_B);
     ra.ws = static_cast<float*>(workspace);
-    m2::precompute_kernel<<<d->batch, m2::kRowThreads, smem, (cudaStream_t)stream>>>(ra, cache_indices, row_wp);
+    m2::precompute_kernel<<<d->batch, m2::kRowThreads, smem, (cudaStream_t)stream>>>(ra, cache_indices, row_wp,
+                                                                                      dev_err);
     return launch_status();
 }
 
