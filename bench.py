@@ -52,7 +52,10 @@ if ROOT not in sys.path:
 
 METRIC = "decode rows/s and µs/step at batch 512; achieved HBM GB/s vs ~8 TB/s peak"
 UNIT = "rows/s"
-EVENT_EVERY = 8  # output-kernel events on every 8th timed step (an event record costs ~5 us)
+# The kernel of interest is timed with CUDA events on every 7th step (an event record
+# costs a few us). 7 is coprime with the 64 input sets and with ring lengths up to 16,
+# so the sampled steps cover every input set and every cursor phase of the ring.
+EVENT_EVERY = 7
 WORKLOAD = ("mamba2 replayssm decode: batch 512, nheads 128, headdim 64, dstate 128, ngroups 8, "
             "L 16, bf16 state pool 1024 slots, desync write_pos U{0..15}, 64 steps cycled")
 
@@ -75,6 +78,8 @@ def parse():
     ap.add_argument("--no-gdn", action="store_true",
                     help="mamba2 line only (skip the gdn_decode / gdn_spec sub-objects)")
     ap.add_argument("--sweep-steps", type=int, default=200)
+    ap.add_argument("--event-every", type=int, default=7,
+                    help="time the kernel of interest with CUDA events on every n-th step")
     return ap.parse_args()
 
 
@@ -354,13 +359,14 @@ def _sampled_graphs(fns, kernel_fns):
     return whole, samp, evs
 
 
-def _timed_graphs(whole, samp, evs, K, dist, dev, offset=0, clocks=True, every=EVENT_EVERY):
+def _timed_graphs(whole, samp, evs, K, dist, dev, offset=0, clocks=True, every=None):
     """Replay K steps; step k runs input set j = (k + offset) % G, as samp[j] when
     k % every == 0 (events around the timed kernel) and as whole[j] otherwise.
     Returns (elapsed ms of the region, max over ranks; the timed kernel's ms from
     the last sampled replay of each input set; clock record; the step index of each
     of those samples)."""
     import torch
+    every = EVENT_EVERY if every is None else every
     stream = torch.cuda.current_stream()
     G = len(whole)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -617,7 +623,7 @@ def run_mamba2(args, dist):
                    "dstate": wl.dstate, "ngroups": wl.ngroups, "ring_len": wl.L,
                    "state_dtype": "bf16", "act_dtype": "bf16", "out_dtype": "bf16",
                    "parallelism": "independent replica per gpu (dp%d)" % dist.world,
-                   "timing": "CUDA graphs; every 8th step as prepare | output with CUDA events between (the output kernel's duration), the others as one prepare+output graph",
+                   "timing": "one CUDA graph per step (prepare + output); on every 7th step the graph also holds CUDA events around the output kernel",
                    "l2": "inputs larger than L2: 1.07 GB of checkpoint tiles streamed per step"},
         "achieved_hbm_gbs": step_b / (ms_step * 1e-3) / 1e9,
         "hbm_frac_step": step_b / (ms_step * 1e-3) / 1e9 / peak,
@@ -625,7 +631,9 @@ def run_mamba2(args, dist):
         "roofline": {"bound": "hbm", "kernel": "mamba2 output_kernel<64,128,bf16>",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
                      "peak_source": peak_kind, "traffic": traffic,
-                     "algorithmic_bytes_per_launch": int(out_b), "avg_launch_ms": out_avg_ms},
+                     "algorithmic_bytes_per_launch": int(out_b), "avg_launch_ms": out_avg_ms,
+                     "launches_timed": len(out_ms), "min_launch_ms": float(np.min(out_ms)),
+                     "max_launch_ms": float(np.max(out_ms)), "event_every": EVENT_EVERY},
         "full_state": full,
         "e2e": e2e,
         "cpu_baseline": cpu,
@@ -746,7 +754,7 @@ def run_gdn(args, dist, sub=False):
         "config": {"workload": GDN_WORKLOAD, "global_batch": dist.world * wl.batch,
                    "batch_per_gpu": wl.batch, "HV": wl.num_v_heads, "HK": wl.num_k_heads,
                    "K": wl.head_k_dim, "V": wl.head_v_dim, "ring_len": wl.L,
-                   "timing": "CUDA graphs; every 8th step as prepare | output with CUDA events between (the output kernel's duration), the others as one prepare+output graph",
+                   "timing": "one CUDA graph per step (prepare + output); on every 7th step the graph also holds CUDA events around the output kernel",
                    "l2": "inputs larger than L2: 537 MB of fp32 checkpoint tiles per step"},
         "roofline": {"bound": "hbm", "kernel": "gdn output kernel (fp32 state, 32-row tiles)",
                      "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
@@ -1058,7 +1066,9 @@ def run_reference(args, dist):
 
 
 def main():
+    global EVENT_EVERY
     args = parse()
+    EVENT_EVERY = max(1, args.event_every)
     dist = Dist()
     try:
         if args.impl == "reference":

@@ -31,6 +31,8 @@
 // pending fold the drafts land on ring positions whose raw entries the fold
 // reads. The table role reads only history entries, which no draft overwrites,
 // so it shares the fold's launch; every ring write happens in the verify launch.
+#include <type_traits>
+
 #include "common.cuh"
 #include "internal.h"
 #include "pipeline.cuh"
@@ -44,6 +46,7 @@ constexpr int VB = 32;  // value rows per work item (a 16 KB fp32 tile)
 constexpr int TILE = VB * KD * 4;
 constexpr int kMaxT = 8;
 constexpr int kFoldChunk = 16;  // committed entries staged per pass of the fold
+constexpr int kFoldList = 256;  // fold items owned by one fold CTA, at most
 
 // table per (row, value head): au[T][L], ao[T][L], Gu[T], Go[T], beta[T], g[T], c, base'
 __host__ __device__ inline int tbl_floats(int L, int T) { return (2 * T * L + 4 * T + 2 + 3) & ~3; }
@@ -83,7 +86,8 @@ struct ProArgs {
     const uint8_t* slot_flush;
     float* ws;
     int T, HV, HK, V, L, num_slots, act_bf16;
-    int n_fold;  // fold CTAs (batch * HV * V/VB); table CTAs follow
+    int n_items;  // fold work items: batch * HV * V/VB tiles
+    int n_fold;   // fold CTAs (each owns the items it = blockIdx.x mod n_fold); table CTAs follow
 };
 
 // Shared memory of the fold role (floats): k [16][KD], raw v [16][VB], beta, g.
@@ -292,10 +296,29 @@ __device__ void pre_head(const ProArgs& a, int idx, float* sm) {
     }
 }
 
+// Fold role: the CTA's threads check its items' slots in parallel, then the CTA
+// folds the flagged tiles one after the other (most rows have no pending fold, so
+// a CTA per item would mostly launch, read two cursors and exit).
+__device__ void fold_role(const ProArgs& a, float* sm) {
+    __shared__ int nlist;
+    __shared__ int list[kFoldList];
+    if (threadIdx.x == 0) nlist = 0;
+    __syncthreads();
+    const int NVB = a.V / VB;
+    for (int it = blockIdx.x + threadIdx.x * a.n_fold; it < a.n_items; it += blockDim.x * a.n_fold) {
+        const int b = it / (a.HV * NVB);
+        const int s = a.ci[b];
+        if (s >= 0 && s < a.num_slots && a.slot_flush[s]) list[atomicAdd(&nlist, 1)] = it;
+    }
+    __syncthreads();
+    const int n = nlist;
+    for (int j = 0; j < n; ++j) fold_tile(a, list[j], sm);
+}
+
 template <int T>
 __global__ void __launch_bounds__(kThreads, 6) prologue_kernel(const ProArgs a) {
     extern __shared__ __align__(16) float psm[];
-    if ((int)blockIdx.x < a.n_fold) fold_tile(a, blockIdx.x, psm);
+    if ((int)blockIdx.x < a.n_fold) fold_role(a, psm);
     else pre_head<T>(a, blockIdx.x - a.n_fold, psm);
 }
 
@@ -307,7 +330,7 @@ constexpr int kGroupWarps = 2;
 constexpr int RW = VB / kGroupWarps;          // value rows per warp
 constexpr int kWarpScratch = 2 * kMaxT * RW * 4;  // W [2T][RW]: S0 . k_j, S0 . q_j
 
-template <int T>
+template <int T, bool BF>
 struct VerPolicy {
     static constexpr int kGroup = kGroupWarps;
     static constexpr int NV = 2 * T;  // vectors k_0, q_0, k_1, q_1, ...
@@ -370,7 +393,7 @@ struct VerPolicy {
             return;
         }
         const int L = a.L;
-        const int sa = a.act_bf16 ? 2 : 4;
+        constexpr int sa = BF ? 2 : 4;
         const int kh = hv / (a.HV / a.HK);
         const int TB = tbl_floats(L, T);
         const uint32_t kb = KD * sa;
@@ -397,8 +420,8 @@ struct VerPolicy {
     static __device__ void consume(const Args& a, int, const Meta& m, const uint8_t* sb,
                                    uint8_t* scratch, int lane, int wi) {
         if (!m.valid) return;
-        const bool bf = a.act_bf16;
-        const int sa = bf ? 2 : 4;
+        constexpr bool bf = BF;
+        constexpr int sa = BF ? 2 : 4;
         const int L = a.L, c = m.c;
         const float* tw = reinterpret_cast<const float*>(sb) + wi * RW * KD;  // this warp's rows
         const uint8_t* kq = sb + a.off_kq;
@@ -559,7 +582,14 @@ int spec_launch(const rssm_gdn_dims* d, float* state, const void* q, const void*
     pa.ws = static_cast<float*>(workspace);
     pa.T = T; pa.HV = HV; pa.HK = HK; pa.V = V; pa.L = L; pa.num_slots = d->num_slots;
     pa.act_bf16 = abf;
-    pa.n_fold = d->batch * HV * NVB;
+    pa.n_items = d->batch * HV * NVB;
+    {
+        const int per = (pa.n_items + spec::kFoldList - 1) / spec::kFoldList;  // CTAs for <= kFoldList each
+        int nf = di.sm_count * 6;
+        if (nf < per) nf = per;
+        if (nf > pa.n_items) nf = pa.n_items;
+        pa.n_fold = nf;
+    }
     const long blocks = (long)pa.n_fold + (long)d->batch * HK;
     spec::prologue_kernel<T><<<(unsigned)blocks, spec::kThreads, psmem, st>>>(pa);
     if (launch_status()) return RSSM_ERR_CUDA;
@@ -572,17 +602,22 @@ int spec_launch(const rssm_gdn_dims* d, float* state, const void* q, const void*
     const int off_d = off;  off += L * spec::VB * 4;
     const int off_tbl = off; off += TBs * 4;
     const int stage_bytes = (off + 127) & ~127;
-    typename spec::VerPolicy<T>::Args va{};
-    va.state = state; va.q = q; va.k = k; va.v = v; va.ring_d = ring_d; va.ring_v = ring_v;
-    va.ring_k = ring_k; va.ring_g = ring_g; va.ring_beta = ring_beta;
-    va.ci = cache_indices; va.slot_wp = slot_wp; va.slot_base = slot_base;
-    va.slot_flush = slot_flush; va.ws = static_cast<const float*>(workspace); va.o = o;
-    va.dev_err = dev_err; va.batch = d->batch; va.HV = HV; va.HK = HK; va.V = V;
-    va.L = L; va.num_slots = d->num_slots; va.act_bf16 = abf;
-    va.out_bf16 = d->out_dtype == RSSM_BF16;
-    va.off_kq = off_kq; va.off_v = off_v; va.off_d = off_d; va.off_tbl = off_tbl;
-    return launch_pipe<spec::VerPolicy<T>>(va, stage_bytes, spec::kWarpScratch, spec::TILE,
-                                           (long)d->batch * HV * NVB, st);
+    auto run = [&](auto* tag) {
+        using Pol = std::remove_pointer_t<decltype(tag)>;
+        typename Pol::Args va{};
+        va.state = state; va.q = q; va.k = k; va.v = v; va.ring_d = ring_d; va.ring_v = ring_v;
+        va.ring_k = ring_k; va.ring_g = ring_g; va.ring_beta = ring_beta;
+        va.ci = cache_indices; va.slot_wp = slot_wp; va.slot_base = slot_base;
+        va.slot_flush = slot_flush; va.ws = static_cast<const float*>(workspace); va.o = o;
+        va.dev_err = dev_err; va.batch = d->batch; va.HV = HV; va.HK = HK; va.V = V;
+        va.L = L; va.num_slots = d->num_slots; va.act_bf16 = abf;
+        va.out_bf16 = d->out_dtype == RSSM_BF16;
+        va.off_kq = off_kq; va.off_v = off_v; va.off_d = off_d; va.off_tbl = off_tbl;
+        return launch_pipe<Pol>(va, stage_bytes, spec::kWarpScratch, spec::TILE,
+                                (long)d->batch * HV * NVB, st);
+    };
+    if (abf) return run(static_cast<spec::VerPolicy<T, true>*>(nullptr));
+    return run(static_cast<spec::VerPolicy<T, false>*>(nullptr));
 }
 
 }  // namespace

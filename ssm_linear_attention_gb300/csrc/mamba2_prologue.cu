@@ -47,7 +47,8 @@ struct RowArgs {
     float* ws;             // [batch][H][TBL]
 };
 
-constexpr int kRowThreads = 512;
+constexpr int kRowThreads = 256;
+constexpr int kRowBlocksPerSM = 4;  // one wave for a batch of up to 4 x SMs rows
 
 __device__ __forceinline__ float step_dt(const RowArgs& a, int b, int h) {
     float v = a.dt_raw[(size_t)b * a.H + h] + (a.dt_bias ? a.dt_bias[h] : 0.f);
@@ -237,7 +238,7 @@ __global__ void __launch_bounds__(256) ring_append_kernel(const RowArgs a, const
     append_row(a, b, ci[b], w);
 }
 
-__global__ void __launch_bounds__(kRowThreads) precompute_kernel(const RowArgs a, const int32_t* ci,
+__global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSM) precompute_kernel(const RowArgs a, const int32_t* ci,
                                                                  const int32_t* row_wp,
                                                                  int32_t* dev_err) {
     extern __shared__ __align__(128) uint8_t psm[];
@@ -264,9 +265,9 @@ __global__ void __launch_bounds__(kRowThreads) precompute_kernel(const RowArgs a
 // Thread 0 issues the staging copies before it reads the cursor; meanwhile every
 // thread loads its share of the step's x, dt and B into registers. After the
 // append, entry w of the staged rings is patched with the step's dt and B.
-constexpr int kMaxXChunks = 8;  // 16-byte chunks of x per thread (H*P*sa/16 <= 8*512)
+constexpr int kMaxXChunks = 4;  // 16-byte chunks of x held in registers per thread
 
-__global__ void __launch_bounds__(kRowThreads) prepare_kernel(const RowArgs a, const int32_t* ci,
+__global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSM) prepare_kernel(const RowArgs a, const int32_t* ci,
                                                               int advance, const uint8_t* force,
                                                               int32_t* slot_wp, int32_t* row_wp,
                                                               uint8_t* row_flush, int32_t* dev_err) {
@@ -319,16 +320,23 @@ __global__ void __launch_bounds__(kRowThreads) prepare_kernel(const RowArgs a, c
                 xr[u];
         }
     }
+    for (int c = threadIdx.x + kMaxXChunks * blockDim.x; c < nx; c += blockDim.x) {  // wide rows
+        const int h = c / xc, j = c - (c / xc) * xc;
+        reinterpret_cast<uint4*>(static_cast<char*>(a.ring_x) + (((size_t)s * H + h) * L + w) * P * sa)[j] =
+            xs[c];
+    }
     float* dts = reinterpret_cast<float*>(psm + lo.dt);
     for (int h = threadIdx.x; h < H; h += blockDim.x) {
         const float v = h == threadIdx.x ? dtr : step_dt(a, b, h);
         a.ring_dt[((size_t)s * H + h) * L + w] = v;
         dts[h * L + w] = v;
     }
-    if (threadIdx.x < G * bcn) {
-        const int g = threadIdx.x / bcn, j = threadIdx.x - (threadIdx.x / bcn) * bcn;
-        reinterpret_cast<uint4*>(static_cast<char*>(a.ring_B) + (((size_t)s * G + g) * L + w) * N * sa)[j] = br;
-        reinterpret_cast<uint4*>(psm + lo.B + ((size_t)g * L + w) * N * sa)[j] = br;
+    for (int c = threadIdx.x; c < G * bcn; c += blockDim.x) {
+        const uint4 v = c == threadIdx.x ? br
+            : reinterpret_cast<const uint4*>(static_cast<const char*>(a.B) + (size_t)b * G * N * sa)[c];
+        const int g = c / bcn, j = c - (c / bcn) * bcn;
+        reinterpret_cast<uint4*>(static_cast<char*>(a.ring_B) + (((size_t)s * G + g) * L + w) * N * sa)[j] = v;
+        reinterpret_cast<uint4*>(psm + lo.B + ((size_t)g * L + w) * N * sa)[j] = v;
     }
     __syncthreads();
     tables_from_smem(a, b, w, psm);
@@ -386,9 +394,6 @@ extern "C" size_t rssm_mamba2_workspace_size(const rssm_mamba2_dims* d) {
 static int m2_prologue_smem(const rssm_mamba2_dims* d, const void* kernel, int* smem) {
     *smem = m2::ProLayout(d->nheads, d->dstate, d->ngroups, d->ring_len,
                           d->act_dtype == RSSM_BF16 ? 2 : 4).total;
-    if ((long)d->nheads * d->headdim * (d->act_dtype == RSSM_BF16 ? 2 : 4) / 16 >
-        (long)m2::kMaxXChunks * m2::kRowThreads)
-        return RSSM_ERR_UNSUPPORTED;
     DeviceInfo di;
     if (!device_info(&di)) return RSSM_ERR_CUDA;
     if (*smem > di.max_smem_optin) return RSSM_ERR_UNSUPPORTED;
