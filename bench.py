@@ -882,12 +882,12 @@ def run_spec(args, dist, sub=False):
         HV, HK, Kd, Vd = wl.num_v_heads, wl.num_k_heads, wl.head_k_dim, wl.head_v_dim
         sab = 2 if wl.act_dtype == "bf16" else 4
         acc_mean = float(np.mean([(accs[k % G] > 0).mean() for k in range(Kf)]))
-        fb = wl.batch * (HV * Vd * Kd * 4 * (1 + T + 2 * acc_mean)
-                         + T * (2 * HK * Kd * sab + HV * Vd * sab + 8 * HV + HV * Vd * 2))
+        fsb = wl.batch * (HV * Vd * Kd * 4 * (1 + T + 2 * acc_mean)
+                          + T * (2 * HK * Kd * sab + HV * Vd * sab + 8 * HV + HV * Vd * 2))
         full = {"ms_per_round": f_ms, "us_per_round": f_ms * 1e3,
                 "rows_per_s": dist.world * wl.batch / (f_ms * 1e-3),
-                "bytes_per_round": int(fb), "achieved_gbs": fb / (f_ms * 1e-3) / 1e9,
-                "hbm_frac": fb / (f_ms * 1e-3) / 1e9 / peak,
+                "bytes_per_round": int(fsb), "achieved_gbs": fsb / (f_ms * 1e-3) / 1e9,
+                "hbm_frac": fsb / (f_ms * 1e-3) / 1e9 / peak,
                 "replay_speedup": f_ms / ms_round,
                 "snapshot_bytes": int(wl.batch * T * HV * Vd * Kd * 4)}
 
