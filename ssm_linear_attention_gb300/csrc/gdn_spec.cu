@@ -47,6 +47,8 @@ constexpr int TILE = VB * KD * 4;
 constexpr int kMaxT = 8;
 constexpr int kFoldChunk = 16;  // committed entries staged per pass of the fold
 constexpr int kFoldList = 256;  // fold items owned by one fold CTA, at most
+static_assert(kFoldChunk * (KD / 4) % kThreads == 0 && kThreads == kFoldChunk * (VB / 4),
+              "fold staging: whole 16-byte chunks per thread");
 
 // table per (row, value head): au[T][L], ao[T][L], Gu[T], Go[T], beta[T], g[T], c, base'
 __host__ __device__ inline int tbl_floats(int L, int T) { return (2 * T * L + 4 * T + 2 + 3) & ~3; }
@@ -132,27 +134,36 @@ __device__ void fold_tile(const ProArgs& a, int item, float* sm) {
     const char* kr = static_cast<const char*>(a.ring_k) + ((size_t)s * a.HK + kh) * L * KD * sa;
     for (int e0 = 0; e0 < cnt; e0 += kFoldChunk) {
         const int ne = cnt - e0 < kFoldChunk ? cnt - e0 : kFoldChunk;
-        __syncthreads();  // the previous chunk is no longer read
-        for (int e = t; e < ne * (KD / 4); e += blockDim.x) {
-            const int i = e / (KD / 4), c4 = e - (e / (KD / 4)) * (KD / 4);
-            const int pos = (base + e0 + i) % L;
-            float f[4];
-            load4(kr + (size_t)pos * KD * sa, c4 * 4, bf, f);
-            *reinterpret_cast<float4*>(ks + i * KD + c4 * 4) = make_float4(f[0], f[1], f[2], f[3]);
+        // every load of the chunk is issued before any shared-memory store
+        constexpr int KU = kFoldChunk * (KD / 4) / kThreads;  // k chunks per thread
+        float kv[KU][4], vv[4], bv = 0.f, gv = 0.f;
+#pragma unroll
+        for (int u = 0; u < KU; ++u) {
+            const int e = t + u * kThreads, i = e / (KD / 4), c4 = e - (e / (KD / 4)) * (KD / 4);
+            if (i < ne) load4(kr + (size_t)((base + e0 + i) % L) * KD * sa, c4 * 4, bf, kv[u]);
         }
-        for (int e = t; e < ne * (VB / 4); e += blockDim.x) {
-            const int i = e / (VB / 4), c4 = e - (e / (VB / 4)) * (VB / 4);
-            const int pos = (base + e0 + i) % L;
-            float f[4];
+        const int vi = t / (VB / 4), vc = t - (t / (VB / 4)) * (VB / 4);  // kThreads == 16 * VB / 4
+        if (vi < ne)
             load4(static_cast<const char*>(a.ring_v) +
-                      ((((size_t)s * a.HV + hv) * L + pos) * a.V + (size_t)vb * VB) * sa,
-                  c4 * 4, bf, f);
-            *reinterpret_cast<float4*>(vs + i * VB + c4 * 4) = make_float4(f[0], f[1], f[2], f[3]);
-        }
+                      ((((size_t)s * a.HV + hv) * L + (base + e0 + vi) % L) * a.V + (size_t)vb * VB) * sa,
+                  vc * 4, bf, vv);
         if (t < ne) {
             const int pos = (base + e0 + t) % L;
-            bs[t] = a.ring_beta[((size_t)s * a.HV + hv) * L + pos];
-            gs[t] = a.ring_g[((size_t)s * a.HV + hv) * L + pos];
+            bv = a.ring_beta[((size_t)s * a.HV + hv) * L + pos];
+            gv = a.ring_g[((size_t)s * a.HV + hv) * L + pos];
+        }
+        __syncthreads();  // the previous chunk is no longer read
+#pragma unroll
+        for (int u = 0; u < KU; ++u) {
+            const int e = t + u * kThreads, i = e / (KD / 4), c4 = e - (e / (KD / 4)) * (KD / 4);
+            if (i < ne)
+                *reinterpret_cast<float4*>(ks + i * KD + c4 * 4) =
+                    make_float4(kv[u][0], kv[u][1], kv[u][2], kv[u][3]);
+        }
+        if (vi < ne) *reinterpret_cast<float4*>(vs + vi * VB + vc * 4) = make_float4(vv[0], vv[1], vv[2], vv[3]);
+        if (t < ne) {
+            bs[t] = bv;
+            gs[t] = gv;
         }
         __syncthreads();
         for (int i = 0; i < ne; ++i) {
@@ -215,16 +226,32 @@ __device__ void pre_head(const ProArgs& a, int idx, float* sm) {
     float* hk = kdq + NV * KD;                           // [c][KD] history keys
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5, nwarps = blockDim.x >> 5;
 
-    for (int e = t; e < NV * (KD / 4); e += blockDim.x) {
-        const int jv = e / (KD / 4), c4 = e - (e / (KD / 4)) * (KD / 4);
-        const int j = jv >> 1;
-        const void* src = (jv & 1) ? a.q : a.k;
-        float f[4];
-        load4(static_cast<const char*>(src) + (((size_t)b * T + j) * HK + kh) * KD * sa, c4 * 4, bf, f);
-        *reinterpret_cast<float4*>(kdq + jv * KD + c4 * 4) = make_float4(f[0], f[1], f[2], f[3]);
-    }
+    // every load is issued before any shared-memory store (one round trip)
     const char* kr = static_cast<const char*>(a.ring_k) + ((size_t)s * HK + kh) * L * KD * sa;
-    for (int e = t; e < c * (KD / 4); e += blockDim.x) {
+    constexpr int DU = (NV * (KD / 4) + kThreads - 1) / kThreads;  // draft chunks per thread
+    constexpr int HU = 16 * (KD / 4) / kThreads;  // history chunks held in registers (c <= 16)
+    float dv[DU][4];
+#pragma unroll
+    for (int u = 0; u < DU; ++u) {
+        const int e = t + u * kThreads;
+        if (e < NV * (KD / 4)) {
+            const int jv = e / (KD / 4), c4 = e - (e / (KD / 4)) * (KD / 4);
+            const void* src = (jv & 1) ? a.q : a.k;
+            load4(static_cast<const char*>(src) + (((size_t)b * T + (jv >> 1)) * HK + kh) * KD * sa,
+                  c4 * 4, bf, dv[u]);
+        }
+    }
+    float hv4[HU][4];
+    const int hn = c * (KD / 4);
+#pragma unroll
+    for (int u = 0; u < HU; ++u) {
+        const int e = t + u * kThreads;
+        if (e < hn) {
+            const int i = e / (KD / 4), c4 = e - (e / (KD / 4)) * (KD / 4);
+            load4(kr + (size_t)((base_eff + i) % L) * KD * sa, c4 * 4, bf, hv4[u]);
+        }
+    }
+    for (int e = t + HU * kThreads; e < hn; e += kThreads) {  // long rings: the rest directly
         const int i = e / (KD / 4), c4 = e - (e / (KD / 4)) * (KD / 4);
         float f[4];
         load4(kr + (size_t)((base_eff + i) % L) * KD * sa, c4 * 4, bf, f);
@@ -234,6 +261,17 @@ __device__ void pre_head(const ProArgs& a, int idx, float* sm) {
         const int hl = x / nk, m = x - (x / nk) * nk, hv = kh * vpk + hl;
         gts[hl * L + m] = m < c ? a.ring_g[((size_t)s * HV + hv) * L + (base_eff + m) % L]
                                 : a.g[((size_t)b * T + (m - c)) * HV + hv];
+    }
+#pragma unroll
+    for (int u = 0; u < DU; ++u) {
+        const int e = t + u * kThreads;
+        if (e < NV * (KD / 4))
+            *reinterpret_cast<float4*>(kdq + e * 4) = make_float4(dv[u][0], dv[u][1], dv[u][2], dv[u][3]);
+    }
+#pragma unroll
+    for (int u = 0; u < HU; ++u) {
+        const int e = t + u * kThreads;
+        if (e < hn) *reinterpret_cast<float4*>(hk + e * 4) = make_float4(hv4[u][0], hv4[u][1], hv4[u][2], hv4[u][3]);
     }
     __syncthreads();
 
