@@ -13,15 +13,15 @@
 //
 // Launches of one verify round:
 //   prologue_kernel    two kinds of CTA in one grid, independent of each other:
-//     fold role        one CTA per (row, value head, 32-row block) of a slot with
-//                      a pending fold: S0 rows in registers (4 threads per row),
-//                      the committed entries staged in shared memory, cnt
-//                      sequential delta-rule updates from ring k, raw v, beta, g;
-//                      S0 stored.
 //     table role       one CTA per (row, key head): dot products of every live
 //                      key (history and drafts) with the drafts' keys and
 //                      queries, products of gates, into a per-(row, value head)
-//                      table.
+//                      table. These CTAs come first in the grid (they are short).
+//     fold role        a persistent set of CTAs folds the (row, value head,
+//                      32-row block) tiles of the slots with a pending fold, dealt
+//                      evenly: S0 rows in registers (4 threads per row), the
+//                      committed entries staged in shared memory, cnt sequential
+//                      delta-rule updates from ring k, raw v, beta, g; S0 stored.
 //   verify_kernel<T>   persistent TMA pipeline over (row, value head, 32-row
 //                      block) tiles of S0: the 2T dot products per value row,
 //                      then the draft chain per row; writes o, the drafts' d and
@@ -46,7 +46,7 @@ constexpr int VB = 32;  // value rows per work item (a 16 KB fp32 tile)
 constexpr int TILE = VB * KD * 4;
 constexpr int kMaxT = 8;
 constexpr int kFoldChunk = 16;  // committed entries staged per pass of the fold
-constexpr int kFoldList = 256;  // fold items owned by one fold CTA, at most
+constexpr int kFoldList = 2048;  // fold items owned by one fold CTA, at most (fallback path)
 static_assert(kFoldChunk * (KD / 4) % kThreads == 0 && kThreads == kFoldChunk * (VB / 4),
               "fold staging: whole 16-byte chunks per thread");
 
@@ -88,8 +88,10 @@ struct ProArgs {
     const uint8_t* slot_flush;
     float* ws;
     int T, HV, HK, V, L, num_slots, act_bf16;
+    int batch;
     int n_items;  // fold work items: batch * HV * V/VB tiles
-    int n_fold;   // fold CTAs (each owns the items it = blockIdx.x mod n_fold); table CTAs follow
+    int n_pre;    // table CTAs (batch * HK), first in the grid: they are short
+    int n_fold;   // fold CTAs, after them (fold CTA f owns the items it = f mod n_fold)
 };
 
 // Shared memory of the fold role (floats): k [16][KD], raw v [16][VB], beta, g.
@@ -334,30 +336,62 @@ __device__ void pre_head(const ProArgs& a, int idx, float* sm) {
     }
 }
 
-// Fold role: the CTA's threads check its items' slots in parallel, then the CTA
-// folds the flagged tiles one after the other (most rows have no pending fold, so
-// a CTA per item would mostly launch, read two cursors and exit).
-__device__ void fold_role(const ProArgs& a, float* sm) {
-    __shared__ int nlist;
-    __shared__ int list[kFoldList];
-    if (threadIdx.x == 0) nlist = 0;
+// Fold role (CTA f of the n_fold fold CTAs). Every fold CTA builds the same
+// ascending list of the rows with a pending fold (ballots over the batch, one pass
+// per kThreads rows), and the list's tiles are dealt round-robin over the fold
+// CTAs, so each folds an even share. Batches larger than the list fall back to each CTA checking its own
+// items (it = f mod n_fold) and folding the flagged ones.
+constexpr int kFoldRowList = 2048;
+
+__device__ void fold_role(const ProArgs& a, int f, float* sm) {
+    __shared__ int rows[kFoldRowList];
+    __shared__ int wsum[kThreads / 32];
+    __shared__ int nrows;
+    const int NVB = a.V / VB, per_row = a.HV * NVB;
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    if (a.batch <= kFoldRowList) {
+        int base = 0;
+        for (int b0 = 0; b0 < a.batch; b0 += kThreads) {
+            const int b = b0 + t;
+            bool flag = false;
+            if (b < a.batch) {
+                const int s = a.ci[b];
+                flag = s >= 0 && s < a.num_slots && a.slot_flush[s];
+            }
+            const unsigned m = __ballot_sync(0xffffffffu, flag);
+            if (lane == 0) wsum[warp] = __popc(m);
+            __syncthreads();
+            int off = base;
+            for (int w = 0; w < warp; ++w) off += wsum[w];
+            if (flag) rows[off + __popc(m & ((1u << lane) - 1u))] = b;
+            int total = 0;
+            for (int w = 0; w < kThreads / 32; ++w) total += wsum[w];
+            base += total;
+            __syncthreads();
+        }
+        const int tiles = base * per_row;
+        for (int x = f; x < tiles; x += a.n_fold) {
+            const int ri = x / per_row;
+            fold_tile(a, rows[ri] * per_row + (x - ri * per_row), sm);
+        }
+        return;
+    }
+    if (t == 0) nrows = 0;
     __syncthreads();
-    const int NVB = a.V / VB;
-    for (int it = blockIdx.x + threadIdx.x * a.n_fold; it < a.n_items; it += blockDim.x * a.n_fold) {
-        const int b = it / (a.HV * NVB);
-        const int s = a.ci[b];
-        if (s >= 0 && s < a.num_slots && a.slot_flush[s]) list[atomicAdd(&nlist, 1)] = it;
+    for (int it = f + t * a.n_fold; it < a.n_items; it += kThreads * a.n_fold) {
+        const int s = a.ci[it / per_row];
+        if (s >= 0 && s < a.num_slots && a.slot_flush[s]) rows[atomicAdd(&nrows, 1)] = it;
     }
     __syncthreads();
-    const int n = nlist;
-    for (int j = 0; j < n; ++j) fold_tile(a, list[j], sm);
+    const int n = nrows;
+    for (int j = 0; j < n; ++j) fold_tile(a, rows[j], sm);
 }
 
 template <int T>
 __global__ void __launch_bounds__(kThreads, 6) prologue_kernel(const ProArgs a) {
     extern __shared__ __align__(16) float psm[];
-    if ((int)blockIdx.x < a.n_fold) fold_role(a, psm);
-    else pre_head<T>(a, blockIdx.x - a.n_fold, psm);
+    if ((int)blockIdx.x < a.n_pre) pre_head<T>(a, blockIdx.x, psm);
+    else fold_role(a, blockIdx.x - a.n_pre, psm);
 }
 
 // ----------------------------------------------------------------------------
@@ -365,7 +399,7 @@ __global__ void __launch_bounds__(kThreads, 6) prologue_kernel(const ProArgs a) 
 // ----------------------------------------------------------------------------
 
 constexpr int kGroupWarps = 2;
-constexpr int RW = VB / kGroupWarps;          // value rows per warp
+constexpr int RW = VB / kGroupWarps;              // value rows per warp
 constexpr int kWarpScratch = 2 * kMaxT * RW * 4;  // W [2T][RW]: S0 . k_j, S0 . q_j
 
 template <int T, bool BF>
@@ -620,6 +654,7 @@ int spec_launch(const rssm_gdn_dims* d, float* state, const void* q, const void*
     pa.ws = static_cast<float*>(workspace);
     pa.T = T; pa.HV = HV; pa.HK = HK; pa.V = V; pa.L = L; pa.num_slots = d->num_slots;
     pa.act_bf16 = abf;
+    pa.batch = d->batch;
     pa.n_items = d->batch * HV * NVB;
     {
         const int per = (pa.n_items + spec::kFoldList - 1) / spec::kFoldList;  // CTAs for <= kFoldList each
@@ -628,7 +663,8 @@ int spec_launch(const rssm_gdn_dims* d, float* state, const void* q, const void*
         if (nf > pa.n_items) nf = pa.n_items;
         pa.n_fold = nf;
     }
-    const long blocks = (long)pa.n_fold + (long)d->batch * HK;
+    pa.n_pre = d->batch * HK;
+    const long blocks = (long)pa.n_fold + pa.n_pre;
     spec::prologue_kernel<T><<<(unsigned)blocks, spec::kThreads, psmem, st>>>(pa);
     if (launch_status()) return RSSM_ERR_CUDA;
 
