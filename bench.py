@@ -550,33 +550,60 @@ def run_mamba2(args, dist):
                 tt = torch.from_numpy(inp[k2]).to(bf if k2 != "dt_raw" else torch.float32)
                 hs[k2] = tt.pin_memory()
             host_sets.append(hs)
-        dsts = {k2: v.clone() for k2, v in zip(("x", "dt_raw", "B", "C", "z"), sets[0])}
-        y_host = torch.empty(wl.batch, wl.nheads, wl.headdim, dtype=bf).pin_memory()
+        # two device input sets and two output buffers: the copies of step k+1 (host to
+        # device) and of step k-1 (device to host) run on their own streams while step k
+        # computes; every copy of every step is inside the timed region
+        names = ("x", "dt_raw", "B", "C", "z")
+        dsts = [{k2: v.clone() for k2, v in zip(names, sets[0])} for _ in range(2)]
+        ybuf = [torch.empty(wl.batch, wl.nheads, wl.headdim, device=dev, dtype=bf)
+                for _ in range(2)]
+        y_host = [torch.empty(wl.batch, wl.nheads, wl.headdim, dtype=bf).pin_memory()
+                  for _ in range(2)]
         h2d = sum(v.numel() * v.element_size() for v in host_sets[0].values())
-        d2h = y_host.numel() * y_host.element_size()
+        d2h = y_host[0].numel() * y_host[0].element_size()
         stream = torch.cuda.current_stream()
+        s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+        ev_in = [torch.cuda.Event() for _ in range(2)]
+        ev_done = [torch.cuda.Event() for _ in range(2)]
+        ev_out = [torch.cuda.Event() for _ in range(2)]
 
-        def e2e_step(k):
-            hs = host_sets[k % len(host_sets)]
-            for k2 in dsts:
-                dsts[k2].copy_(hs[k2], non_blocking=True)
-            y = dec.step(dsts["x"], dsts["dt_raw"], dsts["B"], dsts["C"], dsts["z"], ci)
-            y_host.copy_(y, non_blocking=True)
+        def e2e_run(n):
+            for k in range(n):
+                j = k & 1
+                hs = host_sets[k % len(host_sets)]
+                with torch.cuda.stream(s_in):
+                    if k >= 2:
+                        s_in.wait_event(ev_done[j])      # step k-2 has read buffer j
+                    for k2 in names:
+                        dsts[j][k2].copy_(hs[k2], non_blocking=True)
+                    ev_in[j].record(s_in)
+                stream.wait_event(ev_in[j])
+                if k >= 2:
+                    stream.wait_event(ev_out[j])         # y of step k-2 has left buffer j
+                d = dsts[j]
+                dec.step(d["x"], d["dt_raw"], d["B"], d["C"], d["z"], ci, y=ybuf[j],
+                         stream=stream)
+                ev_done[j].record(stream)
+                with torch.cuda.stream(s_out):
+                    s_out.wait_event(ev_done[j])
+                    y_host[j].copy_(ybuf[j], non_blocking=True)
+                    ev_out[j].record(s_out)
+            stream.wait_stream(s_out)
 
-        for k in range(3):
-            e2e_step(k)
+        e2e_run(4)
         torch.cuda.synchronize()
         dist.barrier()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
-        for k in range(args.e2e_steps):
-            e2e_step(k)
+        s_in.wait_event(e0)
+        e2e_run(args.e2e_steps)
         e1.record(stream)
         torch.cuda.synchronize()
         e_ms = dist.max(e0.elapsed_time(e1)) / args.e2e_steps
         e2e = {"value": dist.world * wl.batch / (e_ms * 1e-3), "unit": UNIT,
                "ms_per_step": e_ms, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "api": "Mamba2ReplayDecoder.step (eager; one rssm_mamba2_step call, 2 launches)"}
+               "api": "Mamba2ReplayDecoder.step (eager; one rssm_mamba2_step call, 2 launches); "
+                      "inputs and y copied on two side streams, double-buffered"}
 
     # the in-house conventional kernel on an identical pool
     full = None
