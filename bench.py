@@ -71,6 +71,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--no-cpu", action="store_true")
     ap.add_argument("--no-full-state", action="store_true")
+    ap.add_argument("--no-sr", action="store_true",
+                    help="skip the stochastic-rounding leg of the mamba2 workload")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--batch", type=int, default=None)
     ap.add_argument("--num-slots", type=int, default=None)
@@ -605,6 +607,31 @@ def run_mamba2(args, dist):
                "api": "Mamba2ReplayDecoder.step (eager; one rssm_mamba2_step call, 2 launches); "
                       "inputs and y copied on two side streams, double-buffered"}
 
+    # the same steps with stochastic rounding of the flush stores (bf16 state)
+    sr = None
+    if not args.no_sr:
+        dec.sr = torch.tensor([0x5EED, 0], device=dev, dtype=torch.int64)
+        for k in range(max(args.warmup, 3)):
+            pre_fn(k % G)()
+            out_fn(k % G)()
+        torch.cuda.synchronize()
+        g_sr, g_srs, srevs = _sampled_graphs(
+            [(lambda j=j: (pre_fn(j)(), out_fn(j)())) for j in range(G)],
+            [(pre_fn(j), out_fn(j), None) for j in range(G)])
+        for k in range(max(args.warmup, 3)):
+            g_sr[k % G].replay()
+        Ks = max(50, K // 4)
+        s_el, s_per, _, _ = _timed_graphs(g_sr, g_srs, srevs, Ks, dist, dev, clocks=False)
+        del g_sr, g_srs
+        dec.sr = None
+        s_ms = s_el / Ks
+        sr = {"us_per_step": s_ms * 1e3, "rows_per_s": dist.world * wl.batch / (s_ms * 1e-3),
+              "output_us": float(np.mean(s_per)) * 1e3,
+              "output_us_nearest": out_avg_ms * 1e3,
+              "step_overhead": s_ms / ms_step - 1.0,
+              "note": "flush stores rounded stochastically (Philox4x32-10 bits); the output "
+                      "launch is followed by a 1-thread launch advancing the generator offset"}
+
     # the in-house conventional kernel on an identical pool
     full = None
     if not args.no_full_state:
@@ -662,6 +689,7 @@ def run_mamba2(args, dist):
                      "launches_timed": len(out_ms), "min_launch_ms": float(np.min(out_ms)),
                      "max_launch_ms": float(np.max(out_ms)), "event_every": EVENT_EVERY},
         "full_state": full,
+        "stochastic_rounding": sr,
         "e2e": e2e,
         "cpu_baseline": cpu,
         "gpu_launches": 2 * K,
@@ -932,7 +960,8 @@ def run_spec(args, dist, sub=False):
         "roofline": {"bound": "hbm", "kernel": "spec round (prologue + verify + commit)",
                      "achieved": round_b / (per_ms * 1e-3) / 1e9, "peak": peak, "unit": "GB/s",
                      "frac": round_b / (per_ms * 1e-3) / 1e9 / peak, "peak_source": peak_kind,
-                     "traffic": None, "algorithmic_bytes_per_round": int(round_b),
+                     "traffic": traffic_record("gdn_spec.cu", "gdn_spec_verify_batch128_T4.md"),
+                     "algorithmic_bytes_per_round": int(round_b),
                      "verify_bytes": float(np.mean(vb)), "fold_bytes": float(np.mean(fb))},
         "full_state": full,
         "gpu_launches": 3 * K,

@@ -47,7 +47,8 @@
  *     net HV = value heads, HK = key heads, K = key dim, V = value dim.
  *
  * Storage dtypes: RSSM_F32 (IEEE float32) or RSSM_BF16 (bfloat16). State stores
- * round to nearest, ties to even. All arithmetic accumulates in float32.
+ * round to nearest, ties to even, except through the *_sr entry points (stochastic
+ * rounding of a bf16 Mamba2 state). All arithmetic accumulates in float32.
  */
 #ifndef RSSM_H
 #define RSSM_H
@@ -248,6 +249,50 @@ int rssm_mamba2_step(const rssm_mamba2_dims* dims, int advance, const uint8_t* f
                      void* workspace, size_t workspace_bytes, void* y, int32_t* dev_err,
                      rssm_stream_t stream);
 
+/* Stochastic rounding of the bf16 state store ([M2] 评论区精华: quantised models
+ * such as the NVFP4 Nemotron baseline rely on stochastic rounding of the state,
+ * and the report adds it as an option).
+ *
+ * sr_state is a DEVICE array of two uint64: {seed, offset}. A state element with
+ * float32 value f at element index e of the state pool (e = ((s * H + h) * P + p)
+ * * N + n) is stored as the bf16 obtained by adding r_e (16 random bits) to the
+ * bit pattern of f and dropping the low 16 bits, so it rounds up with probability
+ * equal to the dropped fraction (unbiased); NaN and +-Inf are stored as with
+ * round-to-nearest. The bits come from Philox4x32-10 (Salmon, Moraes, Dror and
+ * Shaw, "Parallel random numbers: as easy as 1, 2, 3", SC 2011) with key = seed
+ * (low word first) and counter = {e / 8 low, e / 8 high, offset low, offset high}:
+ * its four 32-bit outputs w0..w3 give r for the 8 elements e0 = 8 (e / 8) + j as
+ * the low (j even) or high (j odd) half of w_{j / 2}. After every launch that
+ * stores a state, the call adds 1 to offset (on the device, in stream order), so
+ * graph replays draw fresh bits. For a float32 state the generator is not used
+ * (offset still advances). sr_state must not be NULL; errors as in the call
+ * without _sr. */
+
+/* rssm_mamba2_output with stochastic rounding of the flush stores (see above). */
+int rssm_mamba2_output_sr(const rssm_mamba2_dims* dims, void* state, const void* C,
+                          const float* D, const void* z, const void* ring_x, const void* ring_B,
+                          const int32_t* cache_indices, const int32_t* row_wp,
+                          const uint8_t* row_flush, const void* workspace,
+                          size_t workspace_bytes, void* y, uint64_t* sr_state, int32_t* dev_err,
+                          rssm_stream_t stream);
+
+/* rssm_mamba2_step with stochastic rounding of the flush stores (see above). */
+int rssm_mamba2_step_sr(const rssm_mamba2_dims* dims, int advance, const uint8_t* force_flush,
+                        int32_t* slot_wp, int32_t* row_wp, uint8_t* row_flush, void* state,
+                        const void* x, const float* dt_raw, const float* dt_bias,
+                        int dt_softplus, const float* A, const void* B, const void* C,
+                        const float* D, const void* z, const int32_t* cache_indices,
+                        void* ring_x, float* ring_dt, void* ring_B, void* workspace,
+                        size_t workspace_bytes, void* y, uint64_t* sr_state, int32_t* dev_err,
+                        rssm_stream_t stream);
+
+/* rssm_philox4x32_fill -- out[4 g .. 4 g + 3] = Philox4x32-10(counter {g low,
+ * g high, offset low, offset high}, key {seed low, seed high}) for g < n_groups:
+ * the bits the stochastic rounding of 8-element group g draws at that offset (a
+ * debug / test entry point). out: device uint32 [4 n_groups]. */
+int rssm_philox4x32_fill(uint64_t seed, uint64_t offset, uint32_t* out, size_t n_groups,
+                         rssm_stream_t stream);
+
 /* Size of the device array rssm_mamba2_decode_noalloc keeps its workspace in. */
 #define RSSM_NOALLOC_WORKSPACE_BYTES (16u << 20)
 
@@ -291,6 +336,15 @@ int rssm_mamba2_full_state_update(const rssm_mamba2_dims* dims, void* state, con
                                   const float* A, const void* B, const void* C, const float* D,
                                   const void* z, const int32_t* cache_indices, void* y,
                                   int32_t* dev_err, rssm_stream_t stream);
+
+/* rssm_mamba2_full_state_update with stochastic rounding of the state store
+ * (the rounding of rssm_mamba2_output_sr). */
+int rssm_mamba2_full_state_update_sr(const rssm_mamba2_dims* dims, void* state, const void* x,
+                                     const float* dt_raw, const float* dt_bias, int dt_softplus,
+                                     const float* A, const void* B, const void* C,
+                                     const float* D, const void* z,
+                                     const int32_t* cache_indices, void* y, uint64_t* sr_state,
+                                     int32_t* dev_err, rssm_stream_t stream);
 
 /* ------------------------------------------------------------------------- */
 /* Gated delta net                                                            */

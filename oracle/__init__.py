@@ -38,7 +38,8 @@ from . import cursors
 
 __all__ = ["lib", "round_bf16", "round_f32", "softplus", "mamba2_step", "mamba2_replay",
            "gdn_step", "gdn_replay", "gdn_spec_round", "round_slots", "default_threads",
-           "mamba2_run", "gdn_run", "gdn_spec_run", "cursors"]
+           "mamba2_run", "gdn_run", "gdn_spec_run", "cursors", "philox4x32_10", "round_bf16_sr",
+           "sr_bits", "round_slots_sr"]
 
 _lib = None
 
@@ -71,6 +72,14 @@ def lib():
         L.orc_softplus.argtypes = [ctypes.c_double]
         L.orc_default_threads.restype = ctypes.c_int
         L.orc_round_slots.argtypes = [_dp, ctypes.c_long, _ip, ctypes.c_int, ctypes.c_int]
+        _u32p = ctypes.POINTER(ctypes.c_uint32)
+        L.orc_philox4x32_10.argtypes = [_u32p, _u32p, _u32p]
+        L.orc_round_bf16_sr.restype = ctypes.c_double
+        L.orc_round_bf16_sr.argtypes = [ctypes.c_double, ctypes.c_uint]
+        L.orc_sr_bits.restype = ctypes.c_uint
+        L.orc_sr_bits.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64]
+        L.orc_round_slots_sr.argtypes = [_dp, ctypes.c_long, _ip, ctypes.c_int, ctypes.c_uint64,
+                                         ctypes.c_uint64]
         L.orc_mamba2_step.argtypes = [ctypes.POINTER(_M2Dims), _dp, _dp, _dp, _dp, ctypes.c_int,
                                       _dp, _dp, _dp, _dp, _dp, _ip, _dp, ctypes.c_int]
         L.orc_mamba2_replay.argtypes = [ctypes.POINTER(_M2Dims), ctypes.c_int, _dp, _ip, _ip,
@@ -126,6 +135,36 @@ def round_slots(pool: np.ndarray, slots: Sequence[int], dtype: str) -> None:
         return
     lib().orc_round_slots(_p(pool), int(np.prod(pool.shape[1:])), _p(sl), len(sl),
                           2 if dtype == "bf16" else 1)
+
+
+def philox4x32_10(ctr: Sequence[int], key: Sequence[int]) -> list:
+    """Philox4x32-10 of a 4-word counter under a 2-word key (four uint32)."""
+    c = (ctypes.c_uint32 * 4)(*[int(v) & 0xFFFFFFFF for v in ctr])
+    k = (ctypes.c_uint32 * 2)(*[int(v) & 0xFFFFFFFF for v in key])
+    o = (ctypes.c_uint32 * 4)()
+    lib().orc_philox4x32_10(c, k, o)
+    return list(o)
+
+
+def round_bf16_sr(v: float, r: int) -> float:
+    """Stochastic rounding of v (taken to float32 first) to bf16 with 16 random bits r."""
+    return lib().orc_round_bf16_sr(float(v), int(r))
+
+
+def sr_bits(seed: int, offset: int, e: int) -> int:
+    """The 16 random bits element e of a state pool draws at (seed, offset)."""
+    return lib().orc_sr_bits(int(seed), int(offset), int(e))
+
+
+def round_slots_sr(pool: np.ndarray, slots: Sequence[int], seed: int, offset: int) -> None:
+    """Stochastically round the listed slots of a float64 pool (first axis = slot)
+    to bf16 in place, with the bits of generator (seed, offset)."""
+    assert pool.dtype == np.float64 and pool.flags.c_contiguous
+    sl = _i32(slots)
+    if len(sl) == 0:
+        return
+    lib().orc_round_slots_sr(_p(pool), int(np.prod(pool.shape[1:])), _p(sl), len(sl),
+                             int(seed), int(offset))
 
 
 def _check(rc):

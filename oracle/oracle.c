@@ -79,6 +79,93 @@ void orc_round_slots(double* pool, long slot_elems, const int* slots, int n, int
 }
 
 /* ------------------------------------------------------------------------- */
+/* Stochastic rounding of the bf16 state                                      */
+/* ------------------------------------------------------------------------- */
+
+/* [M2] 评论区精华: quantised models (the NVFP4 Nemotron baseline) rely on
+ * stochastic rounding (SR) of the bf16 state, and the report adds SR as an option.
+ * The pages give neither the generator nor the rounding rule; the library's
+ * interface fixes both, and this is that definition written out.
+ *
+ * Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as
+ * 1, 2, 3", SC 2011, section 3): a 4 x 32-bit counter and a 2 x 32-bit key; each of
+ * the 10 rounds multiplies counter words 0 and 2 by the two Philox constants,
+ * splits each 64-bit product into high and low halves, and outputs
+ *   (hi(M1 c2) ^ c1 ^ k0, lo(M1 c2), hi(M0 c0) ^ c3 ^ k1, lo(M0 c0));
+ * between rounds the key is bumped by the two Weyl constants (golden ratio and
+ * sqrt(3) - 1, times 2^32). */
+void orc_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]) {
+    const uint64_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u;
+    const uint32_t W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
+    uint32_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3];
+    uint32_t k0 = key[0], k1 = key[1];
+    for (int round = 0; round < 10; ++round) {
+        if (round > 0) { k0 += W0; k1 += W1; }
+        uint64_t p0 = M0 * (uint64_t)c0;
+        uint64_t p1 = M1 * (uint64_t)c2;
+        uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ k0;
+        uint32_t n1 = (uint32_t)p1;
+        uint32_t n2 = (uint32_t)(p0 >> 32) ^ c3 ^ k1;
+        uint32_t n3 = (uint32_t)p0;
+        c0 = n0; c1 = n1; c2 = n2; c3 = n3;
+    }
+    out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+/* Stochastic rounding of v to bfloat16 with 16 random bits r (0 <= r < 2^16).
+ * v is first taken to float32 (the precision the decode kernels accumulate the
+ * state in, so that both sides decide in the same precision). With lo = the bf16
+ * value next to v toward zero, u = the bf16 spacing there and
+ * f = (|v| - |lo|) / u in [0, 1) (a multiple of 2^-16 for a float32 v), the result
+ * is the neighbour away from zero when r + 2^16 f >= 2^16, else lo. Over all 2^16
+ * values of r it rounds away from zero exactly 2^16 f times, so its mean is v.
+ * 0, NaN and +-Inf are returned unchanged. */
+double orc_round_bf16_sr(double v, unsigned r) {
+    v = (double)(float)v;
+    if (v == 0.0 || !isfinite(v)) return v;
+    double a = fabs(v);
+    int e;
+    frexp(a, &e);                               /* a = m * 2^e, 0.5 <= m < 1 */
+    int ue = e - 8 < -133 ? -133 : e - 8;       /* bf16 spacing 2^ue (subnormals 2^-133) */
+    double u = ldexp(1.0, ue);
+    double lo = floor(a / u) * u;
+    double f = (a - lo) / u;
+    double q = (double)(r & 0xFFFFu) + ldexp(f, 16) >= 65536.0 ? lo + u : lo;
+    return v < 0 ? -q : q;
+}
+
+/* The 16 bits element e of a pool draws at generator (seed, offset): Philox
+ * counter {e / 8 low word, e / 8 high word, offset low, offset high}, key {seed
+ * low, seed high}; element j = e % 8 takes the low (j even) or high (j odd) half of
+ * output word j / 2. */
+unsigned orc_sr_bits(uint64_t seed, uint64_t offset, uint64_t e) {
+    uint64_t g = e / 8;
+    uint32_t ctr[4] = {(uint32_t)g, (uint32_t)(g >> 32), (uint32_t)offset,
+                       (uint32_t)(offset >> 32)};
+    uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+    uint32_t w[4];
+    orc_philox4x32_10(ctr, key, w);
+    unsigned j = (unsigned)(e % 8);
+    uint32_t word = w[j / 2];
+    return (j % 2 == 0 ? word : word >> 16) & 0xFFFFu;
+}
+
+/* Stochastically round every element of the listed slots of a slot-indexed pool
+ * to bf16: element j of slot s has pool index e = s * slot_elems + j and draws
+ * orc_sr_bits(seed, offset, e). A negative slot index is skipped. */
+void orc_round_slots_sr(double* pool, long slot_elems, const int* slots, int n, uint64_t seed,
+                        uint64_t offset) {
+    for (int i = 0; i < n; ++i) {
+        if (slots[i] < 0) continue;
+        for (long j = 0; j < slot_elems; ++j) {
+            uint64_t e = (uint64_t)slots[i] * (uint64_t)slot_elems + (uint64_t)j;
+            double* p = pool + e;
+            *p = orc_round_bf16_sr(*p, orc_sr_bits(seed, offset, e));
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------- */
 /* Row-parallel driver                                                       */
 /* ------------------------------------------------------------------------- */
 

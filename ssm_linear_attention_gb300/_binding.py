@@ -21,7 +21,8 @@ EXPORTS = (
     "rssm_status_string", "rssm_abi_version", "rssm_advance_cursors", "rssm_ring_append",
     "rssm_mamba2_workspace_size", "rssm_mamba2_precompute", "rssm_mamba2_output",
     "rssm_mamba2_decode", "rssm_mamba2_decode_noalloc", "rssm_mamba2_prepare", "rssm_mamba2_step",
-    "rssm_mamba2_full_state_update",
+    "rssm_mamba2_full_state_update", "rssm_mamba2_output_sr", "rssm_mamba2_step_sr",
+    "rssm_mamba2_full_state_update_sr", "rssm_philox4x32_fill",
     "rssm_gdn_ring_append",
     "rssm_gdn_workspace_size", "rssm_gdn_precompute", "rssm_gdn_output", "rssm_gdn_decode",
     "rssm_gdn_prepare", "rssm_gdn_step",
@@ -81,6 +82,14 @@ def _declare(L):
                                   _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _VP, _VP]),
         "rssm_mamba2_full_state_update": (_I, [m2, _VP, _VP, _VP, _VP, _I, _VP, _VP, _VP, _VP,
                                                _VP, _VP, _VP, _VP, _VP]),
+        "rssm_mamba2_output_sr": (_I, [m2, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                       _SZ, _VP, _VP, _VP, _VP]),
+        "rssm_mamba2_step_sr": (_I, [m2, _I, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _I, _VP, _VP,
+                                     _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _VP, _VP,
+                                     _VP]),
+        "rssm_mamba2_full_state_update_sr": (_I, [m2, _VP, _VP, _VP, _VP, _I, _VP, _VP, _VP,
+                                                  _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
+        "rssm_philox4x32_fill": (_I, [ctypes.c_uint64, ctypes.c_uint64, _VP, _SZ, _VP]),
         "rssm_gdn_ring_append": (_I, [gd, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
         "rssm_gdn_workspace_size": (_SZ, [gd]),
         "rssm_gdn_precompute": (_I, [gd, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP,
@@ -234,6 +243,43 @@ def rssm_mamba2_full_state_update(dims, state, x, dt_raw, dt_bias, dt_softplus, 
     _call("rssm_mamba2_full_state_update", ctypes.byref(dims), _ptr(state), _ptr(x),
           _ptr(dt_raw), _ptr(dt_bias), int(dt_softplus), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
           _ptr(z), _ptr(cache_indices), _ptr(y), _ptr(dev_err), _stream(stream))
+
+
+def rssm_mamba2_output_sr(dims, state, C, D, z, ring_x, ring_B, cache_indices, row_wp, row_flush,
+                          workspace, workspace_bytes, y, sr_state, dev_err=None, stream=None):
+    """rssm_mamba2_output with stochastic rounding of the bf16 flush stores; sr_state
+    is a device uint64 pair {seed, offset} whose offset the call advances."""
+    _call("rssm_mamba2_output_sr", ctypes.byref(dims), _ptr(state), _ptr(C), _ptr(D), _ptr(z),
+          _ptr(ring_x), _ptr(ring_B), _ptr(cache_indices), _ptr(row_wp), _ptr(row_flush),
+          _ptr(workspace), workspace_bytes, _ptr(y), _ptr(sr_state), _ptr(dev_err),
+          _stream(stream))
+
+
+def rssm_mamba2_step_sr(dims, advance, force_flush, slot_wp, row_wp, row_flush, state, x, dt_raw,
+                        dt_bias, dt_softplus, A, B, C, D, z, cache_indices, ring_x, ring_dt,
+                        ring_B, workspace, workspace_bytes, y, sr_state, dev_err=None,
+                        stream=None):
+    """rssm_mamba2_step with stochastic rounding of the bf16 flush stores."""
+    _call("rssm_mamba2_step_sr", ctypes.byref(dims), int(advance), _ptr(force_flush),
+          _ptr(slot_wp), _ptr(row_wp), _ptr(row_flush), _ptr(state), _ptr(x), _ptr(dt_raw),
+          _ptr(dt_bias), int(dt_softplus), _ptr(A), _ptr(B), _ptr(C), _ptr(D), _ptr(z),
+          _ptr(cache_indices), _ptr(ring_x), _ptr(ring_dt), _ptr(ring_B), _ptr(workspace),
+          workspace_bytes, _ptr(y), _ptr(sr_state), _ptr(dev_err), _stream(stream))
+
+
+def rssm_mamba2_full_state_update_sr(dims, state, x, dt_raw, dt_bias, dt_softplus, A, B, C, D, z,
+                                     cache_indices, y, sr_state, dev_err=None, stream=None):
+    """rssm_mamba2_full_state_update with stochastic rounding of the bf16 state store."""
+    _call("rssm_mamba2_full_state_update_sr", ctypes.byref(dims), _ptr(state), _ptr(x),
+          _ptr(dt_raw), _ptr(dt_bias), int(dt_softplus), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+          _ptr(z), _ptr(cache_indices), _ptr(y), _ptr(sr_state), _ptr(dev_err), _stream(stream))
+
+
+def rssm_philox4x32_fill(seed, offset, out, n_groups, stream=None):
+    """out (device uint32/int32 [4 n_groups]) = the Philox4x32-10 blocks the stochastic
+    rounding of groups 0..n_groups-1 draws at (seed, offset)."""
+    _call("rssm_philox4x32_fill", int(seed) & (2 ** 64 - 1), int(offset) & (2 ** 64 - 1),
+          _ptr(out), int(n_groups), _stream(stream))
 
 
 def rssm_gdn_ring_append(dims, k, g, cache_indices, row_wp, ring_k, ring_g, dev_err=None,

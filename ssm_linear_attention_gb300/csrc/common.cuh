@@ -184,14 +184,70 @@ __device__ __forceinline__ void store1(void* base, long idx, bool is_bf16, float
     else reinterpret_cast<float*>(base)[idx] = v;
 }
 
-// State element types for templated kernels.
+// ----------------------------------------------------------------------------
+// counter-based random bits and stochastic rounding to bfloat16
+// ----------------------------------------------------------------------------
+
+// Philox4x32-10 (Salmon, Moraes, Dror, Shaw, "Parallel random numbers: as easy as
+// 1, 2, 3", SC 2011): ten rounds of two 32x32->64 multiplies whose high halves are
+// xor-ed with the other counter words and the key, the key bumped by the Weyl
+// increments between rounds. Returns four 32-bit words for counter c, key k.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint2 k) {
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        // one widening multiply gives both halves of each product
+        const uint64_t p0 = static_cast<uint64_t>(0xD2511F53u) * c.x;
+        const uint64_t p1 = static_cast<uint64_t>(0xCD9E8D57u) * c.z;
+        c = make_uint4(static_cast<uint32_t>(p1 >> 32) ^ c.y ^ k.x, static_cast<uint32_t>(p1),
+                       static_cast<uint32_t>(p0 >> 32) ^ c.w ^ k.y, static_cast<uint32_t>(p0));
+        k.x += 0x9E3779B9u;
+        k.y += 0xBB67AE85u;
+    }
+    return c;
+}
+
+// Stochastic rounding of a float32 to bfloat16 with 16 random bits r: adding r to
+// the 16 bits that bfloat16 drops and truncating rounds away from zero with
+// probability (dropped bits) / 2^16, so the rounding is unbiased. Inf and NaN keep
+// round-to-nearest.
+__device__ __forceinline__ uint16_t f_to_bf16_sr(float f, uint32_t r) {
+    const uint32_t u = __float_as_uint(f);
+    if ((u & 0x7f800000u) == 0x7f800000u) return f_to_bf16(f);
+    return static_cast<uint16_t>((u + (r & 0xFFFFu)) >> 16);
+}
+
+// Store 8 float32 values as bfloat16 at p (16-byte aligned) with stochastic
+// rounding; the random bits are Philox4x32-10 at counter (group, offset), key seed,
+// where group numbers the 8-element groups of the destination array.
+__device__ __forceinline__ void store8_bf16_sr(void* p, const float* f, uint64_t group,
+                                               uint64_t seed, uint64_t offset) {
+    const uint4 r = philox4x32_10(
+        make_uint4((uint32_t)group, (uint32_t)(group >> 32), (uint32_t)offset, (uint32_t)(offset >> 32)),
+        make_uint2((uint32_t)seed, (uint32_t)(seed >> 32)));
+    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
+    uint4 v;
+    uint32_t* o = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        o[i] = uint32_t(f_to_bf16_sr(f[2 * i], w[i])) | (uint32_t(f_to_bf16_sr(f[2 * i + 1], w[i] >> 16)) << 16);
+    *reinterpret_cast<uint4*>(p) = v;
+}
+
+// State element types for templated kernels (sr: stores round stochastically).
 struct StF32 {
     static constexpr int bytes = 4;
     static constexpr bool bf16 = false;
+    static constexpr bool sr = false;
 };
 struct StBF16 {
     static constexpr int bytes = 2;
     static constexpr bool bf16 = true;
+    static constexpr bool sr = false;
+};
+struct StBF16SR {
+    static constexpr int bytes = 2;
+    static constexpr bool bf16 = true;
+    static constexpr bool sr = true;
 };
 
 // softplus(x) = log(1 + e^x); above 20 the correction is below float32 resolution.

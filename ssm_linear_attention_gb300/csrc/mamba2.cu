@@ -60,6 +60,25 @@ struct TileShape {
     static_assert(NCH >= 1 && ITER % NQ == 0, "tile shape");
 };
 
+// Store 8 state elements at element index e of the pool (e % 8 == 0): rounded to
+// nearest, or (StBF16SR) stochastically with the bits of Philox4x32-10 at counter
+// (e / 8, g.y), key g.x.
+template <class ST>
+__device__ __forceinline__ void store_state8(char* pool, size_t e, const float* f, ulonglong2 g) {
+    void* p = pool + e * ST::bytes;
+    if constexpr (ST::sr) store8_bf16_sr(p, f, e >> 3, g.x, g.y);
+    else store8(p, ST::bf16, f);
+}
+
+// The generator {seed, offset} of a stochastically rounding launch, read once per
+// tile before its stores (the state stores could alias it, so reading it inside the
+// store loop would reload it every time).
+template <class ST>
+__device__ __forceinline__ ulonglong2 load_generator(const uint64_t* sr) {
+    if constexpr (ST::sr) return make_ulonglong2(__ldg(sr), __ldg(sr + 1));
+    else return make_ulonglong2(0, 0);
+}
+
 template <int P, int N, class ST>
 struct OutPolicy {
     using Sh = TileShape<P, N, ST>;
@@ -77,6 +96,7 @@ struct OutPolicy {
         const float* ws;
         void* y;
         int32_t* dev_err;
+        const uint64_t* sr;  // {seed, offset}: stochastic rounding of a bf16 state; null: nearest
         int batch, H, G, L, num_slots, act_bf16, out_bf16;
         int stages, stage_bytes, stage_off, scratch_off, warp_scratch;
         int off_x, off_C, off_z, off_tbl, off_B;
@@ -194,7 +214,8 @@ struct OutPolicy {
             // S = Pm1 * S0 + sum_{i<=w} a_i x_i B_i^T, stored rounded to the state dtype
             const uint8_t* br = sb + a.off_B;
             const float* av = tbl + L;
-            char* tile_out = static_cast<char*>(a.state) + ((size_t)m.s * a.H + m.h) * Sh::TILE;
+            const size_t tile_e = ((size_t)m.s * a.H + m.h) * P * N;  // first element of the tile
+            const ulonglong2 gen = load_generator<ST>(a.sr);
             constexpr int RC = Sh::ITER < 8 ? Sh::ITER : 8;
 #pragma unroll 1
             for (int t0 = 0; t0 < Sh::ITER; t0 += RC) {
@@ -222,7 +243,8 @@ struct OutPolicy {
 #pragma unroll
                 for (int r = 0; r < RC; ++r) {
                     const int p = row0 + Sh::RPI * (t0 + r);
-                    store8(tile_out + ((size_t)p * N + q * 8) * Sh::SS, ST::bf16, acc[r]);
+                    store_state8<ST>(static_cast<char*>(a.state), tile_e + (size_t)p * N + q * 8, acc[r],
+                                     gen);
                 }
             }
         }
@@ -246,6 +268,7 @@ struct FullPolicy {
         const int32_t* ci;
         void* y;
         int32_t* dev_err;
+        const uint64_t* sr;  // {seed, offset}: stochastic rounding of a bf16 state; null: nearest
         int batch, H, G, num_slots, act_bf16, out_bf16, softplus;
         int stages, stage_bytes, stage_off, scratch_off, warp_scratch;
         int off_x, off_B, off_C, off_z;
@@ -307,7 +330,8 @@ struct FullPolicy {
         float c[8], bq[8];
         load8(sb + a.off_C + q * 8 * sa, bf, c);
         load8(sb + a.off_B + q * 8 * sa, bf, bq);
-        char* tile_out = static_cast<char*>(a.state) + ((size_t)m.s * a.H + m.h) * Sh::TILE;
+        const size_t tile_e = ((size_t)m.s * a.H + m.h) * P * N;  // first element of the tile
+        const ulonglong2 gen = load_generator<ST>(a.sr);
         float part[Sh::ITER];
 #pragma unroll
         for (int t = 0; t < Sh::ITER; ++t) {
@@ -322,7 +346,7 @@ struct FullPolicy {
                 acc = fmaf(s8[j], c[j], acc);
             }
             part[t] = acc;
-            store8(tile_out + ((size_t)p * N + q * 8) * Sh::SS, ST::bf16, s8);
+            store_state8<ST>(static_cast<char*>(a.state), tile_e + (size_t)p * N + q * 8, s8, gen);
         }
 #pragma unroll
         for (int ch = 0; ch < Sh::NCH; ++ch) reduce_scatter<Sh::NQ, Sh::NQ>(part + ch * Sh::NQ);
@@ -355,10 +379,12 @@ int check_dims(const rssm_mamba2_dims* d) {
 }
 
 
+// sr: a bf16 state is stored with stochastic rounding (a float32 state ignores it).
 template <class F>
-int dispatch_pn(int P, int N, int state_dtype, F&& f) {
+int dispatch_pn(int P, int N, int state_dtype, bool sr, F&& f) {
 #define RSSM_M2_CASE(PP, NN)                                                        \
     if (P == PP && N == NN) {                                                        \
+        if (state_dtype == RSSM_BF16 && sr) return f.template go<PP, NN, StBF16SR>(); \
         if (state_dtype == RSSM_BF16) return f.template go<PP, NN, StBF16>();        \
         return f.template go<PP, NN, StF32>();                                       \
     }
@@ -374,7 +400,7 @@ int dispatch_pn(int P, int N, int state_dtype, F&& f) {
 struct OutCommon {
     void* state; const void* C; const float* D; const void* z; const void* ring_x; const void* ring_B;
     const int32_t* ci; const int32_t* row_wp; const uint8_t* row_flush; const float* ws; void* y;
-    int32_t* dev_err; int batch, H, G, L, num_slots, act_bf16, out_bf16;
+    int32_t* dev_err; const uint64_t* sr; int batch, H, G, L, num_slots, act_bf16, out_bf16;
 };
 
 struct OutLaunch {
@@ -386,7 +412,7 @@ struct OutLaunch {
         typename Pol::Args a{};
         a.state = c.state; a.C = c.C; a.D = c.D; a.z = c.z; a.ring_x = c.ring_x; a.ring_B = c.ring_B;
         a.ci = c.ci; a.row_wp = c.row_wp; a.row_flush = c.row_flush; a.ws = c.ws; a.y = c.y;
-        a.dev_err = c.dev_err; a.batch = c.batch; a.H = c.H; a.G = c.G; a.L = c.L;
+        a.dev_err = c.dev_err; a.sr = c.sr; a.batch = c.batch; a.H = c.H; a.G = c.G; a.L = c.L;
         a.num_slots = c.num_slots; a.act_bf16 = c.act_bf16; a.out_bf16 = c.out_bf16;
         const int sa = c.act_bf16 ? 2 : 4;
         int off = Pol::Sh::TILE;
@@ -403,7 +429,7 @@ struct OutLaunch {
 struct FullCommon {
     void* state; const void* x; const float* dt_raw; const float* dt_bias; const float* A;
     const void* B; const void* C; const float* D; const void* z; const int32_t* ci; void* y;
-    int32_t* dev_err; int batch, H, G, num_slots, act_bf16, out_bf16, softplus;
+    int32_t* dev_err; const uint64_t* sr; int batch, H, G, num_slots, act_bf16, out_bf16, softplus;
 };
 
 struct FullLaunch {
@@ -415,6 +441,7 @@ struct FullLaunch {
         typename Pol::Args a{};
         a.state = c.state; a.x = c.x; a.dt_raw = c.dt_raw; a.dt_bias = c.dt_bias; a.A = c.A;
         a.B = c.B; a.C = c.C; a.D = c.D; a.z = c.z; a.ci = c.ci; a.y = c.y; a.dev_err = c.dev_err;
+        a.sr = c.sr;
         a.batch = c.batch; a.H = c.H; a.G = c.G; a.num_slots = c.num_slots;
         a.act_bf16 = c.act_bf16; a.out_bf16 = c.out_bf16; a.softplus = c.softplus;
         const int sa = c.act_bf16 ? 2 : 4;
@@ -428,23 +455,39 @@ struct FullLaunch {
     }
 };
 
+// The generator's offset moves on after each launch that drew from it, so the next
+// launch (eager or replayed from a graph) draws fresh bits.
+__global__ void sr_advance_kernel(uint64_t* sr) { sr[1] += 1; }
+
+// out[4 g .. 4 g + 3] = Philox4x32-10 at counter (g, offset), key seed: the bits the
+// stochastic rounding of 8-element group g draws (test / debug).
+__global__ void philox_fill_kernel(uint64_t seed, uint64_t offset, uint32_t* out, size_t n) {
+    const size_t g = (size_t)blockIdx.x * blockDim.x + threadIdx.x;
+    if (g >= n) return;
+    const uint4 r = philox4x32_10(
+        make_uint4((uint32_t)g, (uint32_t)(g >> 32), (uint32_t)offset, (uint32_t)(offset >> 32)),
+        make_uint2((uint32_t)seed, (uint32_t)(seed >> 32)));
+    reinterpret_cast<uint4*>(out)[g] = r;
+}
+
 }  // namespace m2
 }  // namespace rssm
 
 using namespace rssm;
 
-extern "C" int rssm_mamba2_output(const rssm_mamba2_dims* d, void* state, const void* C,
-                                  const float* D, const void* z, const void* ring_x,
-                                  const void* ring_B, const int32_t* cache_indices,
-                                  const int32_t* row_wp, const uint8_t* row_flush,
-                                  const void* workspace, size_t workspace_bytes, void* y,
-                                  int32_t* dev_err, rssm_stream_t stream) {
+namespace {
+
+int m2_output_impl(const rssm_mamba2_dims* d, void* state, const void* C, const float* D,
+                   const void* z, const void* ring_x, const void* ring_B,
+                   const int32_t* cache_indices, const int32_t* row_wp, const uint8_t* row_flush,
+                   const void* workspace, size_t workspace_bytes, void* y, int32_t* dev_err,
+                   uint64_t* sr, rssm_stream_t stream) {
     int rc = m2::check_dims(d);
     if (rc) return rc;
     if (d->batch == 0) return RSSM_OK;
     if (!ok_ptr(state) || !ok_ptr(C) || !ok_ptr(D) || !ok_opt_ptr(z) || !ok_ptr(ring_x) ||
         !ok_ptr(ring_B) || !ok_ptr(cache_indices) || !ok_ptr(row_wp) || !ok_ptr(row_flush) ||
-        !ok_ptr(workspace) || !ok_ptr(y))
+        !ok_ptr(workspace) || !ok_ptr(y) || !ok_opt_ptr(sr))
         return RSSM_ERR_INVALID_ARG;
     if (workspace_bytes < rssm_mamba2_workspace_size(d)) return RSSM_ERR_INVALID_ARG;
     m2::OutLaunch l{};
@@ -452,11 +495,62 @@ extern "C" int rssm_mamba2_output(const rssm_mamba2_dims* d, void* state, const 
     m2::OutCommon& a = l.c;
     a.state = state; a.C = C; a.D = D; a.z = z; a.ring_x = ring_x; a.ring_B = ring_B;
     a.ci = cache_indices; a.row_wp = row_wp; a.row_flush = row_flush;
-    a.ws = static_cast<const float*>(workspace); a.y = y; a.dev_err = dev_err;
+    a.ws = static_cast<const float*>(workspace); a.y = y; a.dev_err = dev_err; a.sr = sr;
     a.batch = d->batch; a.H = d->nheads; a.G = d->ngroups; a.L = d->ring_len;
     a.num_slots = d->num_slots; a.act_bf16 = d->act_dtype == RSSM_BF16;
     a.out_bf16 = d->out_dtype == RSSM_BF16;
-    return m2::dispatch_pn(d->headdim, d->dstate, d->state_dtype, l);
+    rc = m2::dispatch_pn(d->headdim, d->dstate, d->state_dtype, sr != nullptr, l);
+    if (rc || sr == nullptr) return rc;
+    m2::sr_advance_kernel<<<1, 1, 0, (cudaStream_t)stream>>>(sr);
+    return launch_status();
+}
+
+int m2_full_impl(const rssm_mamba2_dims* d, void* state, const void* x, const float* dt_raw,
+                 const float* dt_bias, int dt_softplus, const float* A, const void* B,
+                 const void* C, const float* D, const void* z, const int32_t* cache_indices,
+                 void* y, int32_t* dev_err, uint64_t* sr, rssm_stream_t stream) {
+    int rc = m2::check_dims(d);
+    if (rc) return rc;
+    if (d->batch == 0) return RSSM_OK;
+    if (!ok_ptr(state) || !ok_ptr(x) || !ok_ptr(dt_raw) || !ok_opt_ptr(dt_bias) || !ok_ptr(A) ||
+        !ok_ptr(B) || !ok_ptr(C) || !ok_ptr(D) || !ok_opt_ptr(z) || !ok_ptr(cache_indices) ||
+        !ok_ptr(y) || !ok_opt_ptr(sr))
+        return RSSM_ERR_INVALID_ARG;
+    m2::FullLaunch l{};
+    l.stream = (cudaStream_t)stream;
+    m2::FullCommon& a = l.c;
+    a.state = state; a.x = x; a.dt_raw = dt_raw; a.dt_bias = dt_bias; a.A = A; a.B = B; a.C = C;
+    a.D = D; a.z = z; a.ci = cache_indices; a.y = y; a.dev_err = dev_err; a.sr = sr;
+    a.batch = d->batch; a.H = d->nheads; a.G = d->ngroups; a.num_slots = d->num_slots;
+    a.act_bf16 = d->act_dtype == RSSM_BF16; a.out_bf16 = d->out_dtype == RSSM_BF16;
+    a.softplus = dt_softplus != 0;
+    rc = m2::dispatch_pn(d->headdim, d->dstate, d->state_dtype, sr != nullptr, l);
+    if (rc || sr == nullptr) return rc;
+    m2::sr_advance_kernel<<<1, 1, 0, (cudaStream_t)stream>>>(sr);
+    return launch_status();
+}
+
+}  // namespace
+
+extern "C" int rssm_mamba2_output(const rssm_mamba2_dims* d, void* state, const void* C,
+                                  const float* D, const void* z, const void* ring_x,
+                                  const void* ring_B, const int32_t* cache_indices,
+                                  const int32_t* row_wp, const uint8_t* row_flush,
+                                  const void* workspace, size_t workspace_bytes, void* y,
+                                  int32_t* dev_err, rssm_stream_t stream) {
+    return m2_output_impl(d, state, C, D, z, ring_x, ring_B, cache_indices, row_wp, row_flush,
+                          workspace, workspace_bytes, y, dev_err, nullptr, stream);
+}
+
+extern "C" int rssm_mamba2_output_sr(const rssm_mamba2_dims* d, void* state, const void* C,
+                                     const float* D, const void* z, const void* ring_x,
+                                     const void* ring_B, const int32_t* cache_indices,
+                                     const int32_t* row_wp, const uint8_t* row_flush,
+                                     const void* workspace, size_t workspace_bytes, void* y,
+                                     uint64_t* sr_state, int32_t* dev_err, rssm_stream_t stream) {
+    if (!ok_ptr(sr_state)) return RSSM_ERR_INVALID_ARG;
+    return m2_output_impl(d, state, C, D, z, ring_x, ring_B, cache_indices, row_wp, row_flush,
+                          workspace, workspace_bytes, y, dev_err, sr_state, stream);
 }
 
 extern "C" int rssm_mamba2_decode(const rssm_mamba2_dims* d, void* state, const float* A,
@@ -487,17 +581,33 @@ extern "C" int rssm_mamba2_step(const rssm_mamba2_dims* d, int advance, const ui
                                 void* ring_x, float* ring_dt, void* ring_B, void* workspace,
                                 size_t workspace_bytes, void* y, int32_t* dev_err,
                                 rssm_stream_t stream) {
+    return rssm_mamba2_step_sr(d, advance, force_flush, slot_wp, row_wp, row_flush, state, x,
+                               dt_raw, dt_bias, dt_softplus, A, B, C, D, z, cache_indices, ring_x,
+                               ring_dt, ring_B, workspace, workspace_bytes, y, nullptr, dev_err,
+                               stream);
+}
+
+extern "C" int rssm_mamba2_step_sr(const rssm_mamba2_dims* d, int advance,
+                                   const uint8_t* force_flush, int32_t* slot_wp, int32_t* row_wp,
+                                   uint8_t* row_flush, void* state, const void* x,
+                                   const float* dt_raw, const float* dt_bias, int dt_softplus,
+                                   const float* A, const void* B, const void* C, const float* D,
+                                   const void* z, const int32_t* cache_indices, void* ring_x,
+                                   float* ring_dt, void* ring_B, void* workspace,
+                                   size_t workspace_bytes, void* y, uint64_t* sr_state,
+                                   int32_t* dev_err, rssm_stream_t stream) {
     int rc = m2::check_dims(d);
     if (rc) return rc;
     if (d->batch == 0) return RSSM_OK;
-    if (!ok_ptr(state) || !ok_ptr(D) || !ok_opt_ptr(z) || !ok_ptr(y) || !ok_ptr(row_flush))
+    if (!ok_ptr(state) || !ok_ptr(D) || !ok_opt_ptr(z) || !ok_ptr(y) || !ok_ptr(row_flush) ||
+        !ok_opt_ptr(sr_state))
         return RSSM_ERR_INVALID_ARG;
     rc = rssm_mamba2_prepare(d, advance, force_flush, slot_wp, row_wp, row_flush, x, dt_raw, dt_bias,
                              dt_softplus, B, A, C, cache_indices, ring_x, ring_dt, ring_B,
                              workspace, workspace_bytes, dev_err, stream);
     if (rc) return rc;
-    return rssm_mamba2_output(d, state, C, D, z, ring_x, ring_B, cache_indices, row_wp, row_flush,
-                              workspace, workspace_bytes, y, dev_err, stream);
+    return m2_output_impl(d, state, C, D, z, ring_x, ring_B, cache_indices, row_wp, row_flush,
+                          workspace, workspace_bytes, y, dev_err, sr_state, stream);
 }
 
 extern "C" int rssm_mamba2_full_state_update(const rssm_mamba2_dims* d, void* state, const void* x,
@@ -506,20 +616,28 @@ extern "C" int rssm_mamba2_full_state_update(const rssm_mamba2_dims* d, void* st
                                              const void* C, const float* D, const void* z,
                                              const int32_t* cache_indices, void* y,
                                              int32_t* dev_err, rssm_stream_t stream) {
-    int rc = m2::check_dims(d);
-    if (rc) return rc;
-    if (d->batch == 0) return RSSM_OK;
-    if (!ok_ptr(state) || !ok_ptr(x) || !ok_ptr(dt_raw) || !ok_opt_ptr(dt_bias) || !ok_ptr(A) ||
-        !ok_ptr(B) || !ok_ptr(C) || !ok_ptr(D) || !ok_opt_ptr(z) || !ok_ptr(cache_indices) ||
-        !ok_ptr(y))
-        return RSSM_ERR_INVALID_ARG;
-    m2::FullLaunch l{};
-    l.stream = (cudaStream_t)stream;
-    m2::FullCommon& a = l.c;
-    a.state = state; a.x = x; a.dt_raw = dt_raw; a.dt_bias = dt_bias; a.A = A; a.B = B; a.C = C;
-    a.D = D; a.z = z; a.ci = cache_indices; a.y = y; a.dev_err = dev_err;
-    a.batch = d->batch; a.H = d->nheads; a.G = d->ngroups; a.num_slots = d->num_slots;
-    a.act_bf16 = d->act_dtype == RSSM_BF16; a.out_bf16 = d->out_dtype == RSSM_BF16;
-    a.softplus = dt_softplus != 0;
-    return m2::dispatch_pn(d->headdim, d->dstate, d->state_dtype, l);
+    return m2_full_impl(d, state, x, dt_raw, dt_bias, dt_softplus, A, B, C, D, z, cache_indices, y,
+                        dev_err, nullptr, stream);
+}
+
+extern "C" int rssm_mamba2_full_state_update_sr(const rssm_mamba2_dims* d, void* state,
+                                                const void* x, const float* dt_raw,
+                                                const float* dt_bias, int dt_softplus,
+                                                const float* A, const void* B, const void* C,
+                                                const float* D, const void* z,
+                                                const int32_t* cache_indices, void* y,
+                                                uint64_t* sr_state, int32_t* dev_err,
+                                                rssm_stream_t stream) {
+    if (!ok_ptr(sr_state)) return RSSM_ERR_INVALID_ARG;
+    return m2_full_impl(d, state, x, dt_raw, dt_bias, dt_softplus, A, B, C, D, z, cache_indices, y,
+                        dev_err, sr_state, stream);
+}
+
+extern "C" int rssm_philox4x32_fill(uint64_t seed, uint64_t offset, uint32_t* out, size_t n_groups,
+                                    rssm_stream_t stream) {
+    if (n_groups == 0) return RSSM_OK;
+    if (!ok_ptr(out)) return RSSM_ERR_INVALID_ARG;
+    const unsigned blocks = (unsigned)((n_groups + 255) / 256);
+    m2::philox_fill_kernel<<<blocks, 256, 0, (cudaStream_t)stream>>>(seed, offset, out, n_groups);
+    return launch_status();
 }

@@ -29,6 +29,16 @@ __all__ = ["torch_dtype_code", "Mamba2ReplayDecoder", "Mamba2FullStateDecoder",
            "GDNSpecFullStateVerifier"]
 
 
+def _sr_state(seed, device):
+    """Device {seed, offset} pair (uint64 bits kept in int64) for stochastic rounding,
+    or None for round-to-nearest."""
+    if seed is None:
+        return None
+    s = int(seed) & (2 ** 64 - 1)
+    s = s - 2 ** 64 if s >= 2 ** 63 else s
+    return torch.tensor([s, 0], device=device, dtype=torch.int64)
+
+
 def torch_dtype_code(dt: torch.dtype) -> int:
     if dt == torch.float32:
         return B.RSSM_F32
@@ -43,11 +53,12 @@ class Mamba2ReplayDecoder:
     Buffers: state [num_slots, H, P, N] (state_dtype), ring_x [num_slots, H, L, P],
     ring_dt [num_slots, H, L] float32, ring_B [num_slots, G, L, N], slot_wp
     [num_slots] int32, and per-row row_wp / row_flush / workspace / y for up to
-    max_batch rows."""
+    max_batch rows. With sr_seed set, bf16 state stores round stochastically
+    (Philox4x32-10 bits from {sr_seed, offset}; the offset advances each call)."""
 
     def __init__(self, nheads, headdim, dstate, ngroups, ring_len, num_slots, max_batch, A, D,
                  dt_bias=None, dt_softplus=True, state_dtype=torch.bfloat16,
-                 act_dtype=torch.bfloat16, out_dtype=torch.bfloat16, device=None):
+                 act_dtype=torch.bfloat16, out_dtype=torch.bfloat16, device=None, sr_seed=None):
         dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
         self.H, self.P, self.N, self.G, self.L = nheads, headdim, dstate, ngroups, ring_len
         self.num_slots, self.max_batch = num_slots, max_batch
@@ -68,6 +79,7 @@ class Mamba2ReplayDecoder:
         self.ws_bytes = B.rssm_mamba2_workspace_size(self.dims(max_batch))
         self.workspace = torch.empty(max(self.ws_bytes, 16), device=dev, dtype=torch.uint8)
         self.y = torch.empty(max_batch, nheads, headdim, device=dev, dtype=out_dtype)
+        self.sr = _sr_state(sr_seed, dev)
 
     def dims(self, batch):
         return B.Mamba2Dims(batch, self.H, self.P, self.N, self.G, self.L, self.num_slots,
@@ -94,6 +106,12 @@ class Mamba2ReplayDecoder:
     def output(self, C, z, cache_indices, y=None, stream=None):
         b = C.shape[0]
         y = self.y[:b] if y is None else y
+        if self.sr is not None:
+            B.rssm_mamba2_output_sr(self.dims(b), self.state, C, self.D, z, self.ring_x,
+                                    self.ring_B, cache_indices, self.row_wp, self.row_flush,
+                                    self.workspace, self.ws_bytes, y, self.sr, self.dev_err,
+                                    stream)
+            return y
         B.rssm_mamba2_output(self.dims(b), self.state, C, self.D, z, self.ring_x, self.ring_B,
                              cache_indices, self.row_wp, self.row_flush, self.workspace,
                              self.ws_bytes, y, self.dev_err, stream)
@@ -114,6 +132,13 @@ class Mamba2ReplayDecoder:
         rssm_mamba2_step call (two launches). Returns y [b, H, P]."""
         b = x.shape[0]
         y = self.y[:b] if y is None else y
+        if self.sr is not None:
+            B.rssm_mamba2_step_sr(self.dims(b), advance, force_flush, self.slot_wp, self.row_wp,
+                                  self.row_flush, self.state, x, dt_raw, self.dt_bias,
+                                  self.dt_softplus, self.A, Bm, C, self.D, z, cache_indices,
+                                  self.ring_x, self.ring_dt, self.ring_B, self.workspace,
+                                  self.ws_bytes, y, self.sr, self.dev_err, stream)
+            return y
         B.rssm_mamba2_step(self.dims(b), advance, force_flush, self.slot_wp, self.row_wp,
                            self.row_flush, self.state, x, dt_raw, self.dt_bias, self.dt_softplus,
                            self.A, Bm, C, self.D, z, cache_indices, self.ring_x, self.ring_dt,
@@ -148,11 +173,12 @@ class Mamba2ReplayDecoder:
 
 
 class Mamba2FullStateDecoder:
-    """The conventional Mamba2 decode step (whole state read and written every step)."""
+    """The conventional Mamba2 decode step (whole state read and written every step);
+    sr_seed as in Mamba2ReplayDecoder."""
 
     def __init__(self, nheads, headdim, dstate, ngroups, num_slots, max_batch, A, D, dt_bias=None,
                  dt_softplus=True, state_dtype=torch.bfloat16, act_dtype=torch.bfloat16,
-                 out_dtype=torch.bfloat16, device=None):
+                 out_dtype=torch.bfloat16, device=None, sr_seed=None):
         dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
         self.H, self.P, self.N, self.G = nheads, headdim, dstate, ngroups
         self.num_slots = num_slots
@@ -165,6 +191,7 @@ class Mamba2FullStateDecoder:
         self.state = torch.zeros(num_slots, nheads, headdim, dstate, device=dev, dtype=state_dtype)
         self.dev_err = torch.zeros(4, device=dev, dtype=torch.int32)
         self.y = torch.empty(max_batch, nheads, headdim, device=dev, dtype=out_dtype)
+        self.sr = _sr_state(sr_seed, dev)
 
     def dims(self, batch):
         return B.Mamba2Dims(batch, self.H, self.P, self.N, self.G, 1, self.num_slots,
@@ -174,6 +201,11 @@ class Mamba2FullStateDecoder:
     def step(self, x, dt_raw, Bm, C, z, cache_indices, y=None, stream=None):
         b = x.shape[0]
         y = self.y[:b] if y is None else y
+        if self.sr is not None:
+            B.rssm_mamba2_full_state_update_sr(self.dims(b), self.state, x, dt_raw, self.dt_bias,
+                                               self.dt_softplus, self.A, Bm, C, self.D, z,
+                                               cache_indices, y, self.sr, self.dev_err, stream)
+            return y
         B.rssm_mamba2_full_state_update(self.dims(b), self.state, x, dt_raw, self.dt_bias,
                                         self.dt_softplus, self.A, Bm, C, self.D, z, cache_indices,
                                         y, self.dev_err, stream)

@@ -66,12 +66,13 @@ def to_dev(a, dtype, device="cuda"):
 # Mamba2                                                                      #
 # --------------------------------------------------------------------------- #
 
-def make_mamba2_decoder(wl, out_dtype=torch.float32, full_state=False, max_batch=None):
+def make_mamba2_decoder(wl, out_dtype=torch.float32, full_state=False, max_batch=None,
+                        sr_seed=None):
     from ssm_linear_attention_gb300 import Mamba2FullStateDecoder, Mamba2ReplayDecoder
     prm = wl.params()
     kw = dict(A=prm["A"], D=prm["D"], dt_bias=prm["dt_bias"], dt_softplus=wl.dt_softplus,
               state_dtype=torch_dt(wl.state_dtype), act_dtype=torch_dt(wl.act_dtype),
-              out_dtype=out_dtype)
+              out_dtype=out_dtype, sr_seed=sr_seed)
     mb = wl.batch if max_batch is None else max_batch
     if full_state:
         dec = Mamba2FullStateDecoder(wl.nheads, wl.headdim, wl.dstate, wl.ngroups, wl.num_slots,
