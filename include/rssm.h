@@ -450,8 +450,9 @@ int rssm_gdn_full_state_decode(const rssm_gdn_dims* dims, float* state, const vo
 /* Gated delta net: speculative verify                                        */
 /* ------------------------------------------------------------------------- */
 
-/* Bytes of device workspace rssm_gdn_spec_verify needs for T drafts (per-(row,
- * value head) coefficient tables, float32). 0 for invalid dims or T. */
+/* Bytes of device workspace rssm_gdn_spec_verify needs for T drafts: per-(row,
+ * value head) coefficient tables, then float32 copies of the drafts' keys and
+ * queries per (row, key head). 0 for invalid dims or T. */
 size_t rssm_gdn_spec_workspace_size(const rssm_gdn_dims* dims, int32_t T);
 
 /* rssm_gdn_spec_verify -- score a linear chain of T draft tokens per row from the
@@ -460,9 +461,10 @@ size_t rssm_gdn_spec_workspace_size(const rssm_gdn_dims* dims, int32_t T);
  * folding, for slots whose fold is pending, the committed entries into the
  * checkpoint by replaying the recurrence sequentially from the raw inputs
  * ([SPEC] 实现拆解 item 3, gdn_replayssm_exact_fold_kernel; 评论区精华: the exact
- * fold removed the long-output drift). Three launches: exact fold; precompute
- * (key dot products and gate products into `workspace`, and the ring entries of
- * the drafts that do not depend on the state: k, g, beta); verify.
+ * fold removed the long-output drift). Two launches: a prologue whose CTAs either
+ * fold a pending slot's tile or compute a (row, key head)'s tables (key dot
+ * products and gate products, and float32 copies of the drafts' k and q, into
+ * `workspace`); then the verify, which also writes the drafts' ring entries.
  *
  * Cursors (read only here; see RSSM_CURSOR_SPEC_COMMIT): slot_wp = cnt,
  * slot_base = base, slot_flush = fold pending. Committed entries sit at ring

@@ -53,6 +53,15 @@ static_assert(kFoldChunk * (KD / 4) % kThreads == 0 && kThreads == kFoldChunk * 
 // table per (row, value head): au[T][L], ao[T][L], Gu[T], Go[T], beta[T], g[T], c, base'
 __host__ __device__ inline int tbl_floats(int L, int T) { return (2 * T * L + 4 * T + 2 + 3) & ~3; }
 
+// Workspace: the tables [batch][HV][tbl_floats], then the drafts' keys and queries in
+// float32 [batch][HK][2T][KD] (k_0, q_0, k_1, q_1, ...), written by the table CTAs.
+inline size_t vec_offset_floats(const rssm_gdn_dims* d, int T) {
+    return (size_t)d->batch * d->num_v_heads * tbl_floats(d->ring_len, T);
+}
+inline size_t workspace_floats(const rssm_gdn_dims* d, int T) {
+    return vec_offset_floats(d, T) + (size_t)d->batch * d->num_k_heads * 2 * T * KD;
+}
+
 // Effective history of a slot at verify time: (count, oldest position); false when
 // the cursors are outside the ring.
 __device__ __forceinline__ bool history(int cnt, int base, int flush, int L, int T, int* c,
@@ -87,6 +96,7 @@ struct ProArgs {
     const int32_t* slot_base;
     const uint8_t* slot_flush;
     float* ws;
+    float* wsv;  // [batch][HK][2T][KD] float32: the drafts' k_j, q_j (interleaved)
     int T, HV, HK, V, L, num_slots, act_bf16;
     int batch;
     int n_items;  // fold work items: batch * HV * V/VB tiles
@@ -264,11 +274,15 @@ __device__ void pre_head(const ProArgs& a, int idx, float* sm) {
         gts[hl * L + m] = m < c ? a.ring_g[((size_t)s * HV + hv) * L + (base_eff + m) % L]
                                 : a.g[((size_t)b * T + (m - c)) * HV + hv];
     }
+    float* gv = a.wsv + ((size_t)b * HK + kh) * NV * KD;  // the verify's float32 copy
 #pragma unroll
     for (int u = 0; u < DU; ++u) {
         const int e = t + u * kThreads;
-        if (e < NV * (KD / 4))
-            *reinterpret_cast<float4*>(kdq + e * 4) = make_float4(dv[u][0], dv[u][1], dv[u][2], dv[u][3]);
+        if (e < NV * (KD / 4)) {
+            const float4 f4 = make_float4(dv[u][0], dv[u][1], dv[u][2], dv[u][3]);
+            *reinterpret_cast<float4*>(kdq + e * 4) = f4;
+            reinterpret_cast<float4*>(gv)[e] = f4;
+        }
     }
 #pragma unroll
     for (int u = 0; u < HU; ++u) {
@@ -423,6 +437,7 @@ struct VerPolicy {
         const int32_t* slot_base;
         const uint8_t* slot_flush;
         const float* ws;
+        const float* wsv;  // the drafts' k_j, q_j in float32, from the prologue
         void* o;
         int32_t* dev_err;
         int batch, HV, HK, V, L, num_slots, act_bf16, out_bf16;
@@ -468,14 +483,12 @@ struct VerPolicy {
         constexpr int sa = BF ? 2 : 4;
         const int kh = hv / (a.HV / a.HK);
         const int TB = tbl_floats(L, T);
-        const uint32_t kb = KD * sa;
-        mbar_arrive_expect_tx(full, TILE + 2 * T * kb + T * VB * sa + m.c * VB * 4 + TB * 4);
+        constexpr uint32_t vb4 = NV * KD * 4;  // the 2T float32 vectors
+        mbar_arrive_expect_tx(full, TILE + vb4 + T * VB * sa + m.c * VB * 4 + TB * 4);
         bulk_g2s_hint(sb, a.state + (((size_t)m.s * a.HV + hv) * a.V + (size_t)vb * VB) * KD, TILE,
                       full, pol);
+        bulk_g2s(sb + a.off_kq, a.wsv + ((size_t)b * a.HK + kh) * NV * KD, vb4, full);
         for (int j = 0; j < T; ++j) {
-            const size_t src = (((size_t)b * T + j) * a.HK + kh) * kb;
-            bulk_g2s(sb + a.off_kq + (2 * j) * kb, static_cast<const char*>(a.k) + src, kb, full);
-            bulk_g2s(sb + a.off_kq + (2 * j + 1) * kb, static_cast<const char*>(a.q) + src, kb, full);
             bulk_g2s(sb + a.off_v + j * VB * sa,
                      static_cast<const char*>(a.v) +
                          ((((size_t)b * T + j) * a.HV + hv) * a.V + (size_t)vb * VB) * sa,
@@ -496,49 +509,52 @@ struct VerPolicy {
         constexpr int sa = BF ? 2 : 4;
         const int L = a.L, c = m.c;
         const float* tw = reinterpret_cast<const float*>(sb) + wi * RW * KD;  // this warp's rows
-        const uint8_t* kq = sb + a.off_kq;
+        const float* kqf = reinterpret_cast<const float*>(sb + a.off_kq);  // [2T][KD] float32
         float* W = reinterpret_cast<float*>(scratch);  // [2T][RW]
 
         // phase A: W[d][row] = S0_row . vec_d. Lane (rg, cg) = (lane/8, lane%8) owns
         // rows rg + 4i (i < 4) and the 4-column chunks at cg*4 + 32u (u < 4): within
         // each quarter-warp the 16-byte shared loads touch 32 distinct banks, and the
-        // sums reduce across the 8 lanes of a row group.
+        // sums reduce across the 8 lanes of a row group. The products run as packed
+        // two-wide float32 FMAs over column pairs (even and odd columns accumulate
+        // separately and are added at the end).
         const int cg = lane & 7, rg = lane >> 3;
 #pragma unroll
         for (int g8 = 0; g8 < NG; ++g8) {
-            float acc[4][NVP];
+            float2 acc2[4][NVP];
 #pragma unroll
             for (int i = 0; i < 4; ++i)
 #pragma unroll
-                for (int d = 0; d < NVP; ++d) acc[i][d] = 0.f;
+                for (int d = 0; d < NVP; ++d) acc2[i][d] = make_float2(0.f, 0.f);
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const int col = cg * 4 + 32 * u;
-                float vv[NVP][4];
+                float4 vv[NVP];
 #pragma unroll
                 for (int d = 0; d < NVP; ++d) {
-                    if (g8 * 8 + d < NV) load4(kq + (size_t)(g8 * 8 + d) * KD * sa, col, bf, vv[d]);
+                    if (g8 * 8 + d < NV)
+                        vv[d] = *reinterpret_cast<const float4*>(kqf + (g8 * 8 + d) * KD + col);
                 }
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const float4 s4 = *reinterpret_cast<const float4*>(tw + (rg + 4 * i) * KD + col);
+                    const float2 slo = make_float2(s4.x, s4.y), shi = make_float2(s4.z, s4.w);
 #pragma unroll
                     for (int d = 0; d < NVP; ++d) {
                         if (g8 * 8 + d < NV) {
-                            float x = acc[i][d];
-                            x = fmaf(s4.x, vv[d][0], x);
-                            x = fmaf(s4.y, vv[d][1], x);
-                            x = fmaf(s4.z, vv[d][2], x);
-                            x = fmaf(s4.w, vv[d][3], x);
-                            acc[i][d] = x;
+                            acc2[i][d] = __ffma2_rn(slo, make_float2(vv[d].x, vv[d].y), acc2[i][d]);
+                            acc2[i][d] = __ffma2_rn(shi, make_float2(vv[d].z, vv[d].w), acc2[i][d]);
                         }
                     }
                 }
             }
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const int e = g8 * 8 + reduce_scatter<NVP, 8>(acc[i]);
-                if ((cg & (8 / NVP - 1)) == 0 && e < NV) W[e * RW + rg + 4 * i] = acc[i][0];
+                float acc[NVP];
+#pragma unroll
+                for (int d = 0; d < NVP; ++d) acc[d] = acc2[i][d].x + acc2[i][d].y;
+                const int e = g8 * 8 + reduce_scatter<NVP, 8>(acc);
+                if ((cg & (8 / NVP - 1)) == 0 && e < NV) W[e * RW + rg + 4 * i] = acc[0];
             }
         }
         __syncwarp();
@@ -605,13 +621,20 @@ struct VerPolicy {
             const int vpk = a.HV / a.HK;
             if (m.hv % vpk == 0) {
                 const int kh = m.hv / vpk;
-                const int kc = KD * sa / 16;
+                constexpr int kc = KD / 4;  // 4-element chunks per key
                 for (int x = lane; x < T * kc; x += 32) {
                     const int j = x / kc, part = x - (x / kc) * kc;
                     const int pos = (pos0 + j) % L;
-                    reinterpret_cast<uint4*>(static_cast<char*>(a.ring_k) +
-                                             (((size_t)m.s * a.HK + kh) * L + pos) * KD * sa)[part] =
-                        reinterpret_cast<const uint4*>(kq + (size_t)(2 * j) * KD * sa)[part];
+                    const float4 f4 = reinterpret_cast<const float4*>(kqf + (size_t)(2 * j) * KD)[part];
+                    char* dst = static_cast<char*>(a.ring_k) + (((size_t)m.s * a.HK + kh) * L + pos) * KD * sa;
+                    if (bf) {  // exact: the values came from bf16
+                        const uint2 w2 = make_uint2(
+                            uint32_t(f_to_bf16(f4.x)) | (uint32_t(f_to_bf16(f4.y)) << 16),
+                            uint32_t(f_to_bf16(f4.z)) | (uint32_t(f_to_bf16(f4.w)) << 16));
+                        reinterpret_cast<uint2*>(dst)[part] = w2;
+                    } else {
+                        reinterpret_cast<float4*>(dst)[part] = f4;
+                    }
                 }
             }
         }
@@ -652,6 +675,7 @@ int spec_launch(const rssm_gdn_dims* d, float* state, const void* q, const void*
     pa.ring_v = ring_v; pa.ring_g = ring_g; pa.ring_beta = ring_beta; pa.ci = cache_indices;
     pa.slot_wp = slot_wp; pa.slot_base = slot_base; pa.slot_flush = slot_flush;
     pa.ws = static_cast<float*>(workspace);
+    pa.wsv = static_cast<float*>(workspace) + spec::vec_offset_floats(d, T);
     pa.T = T; pa.HV = HV; pa.HK = HK; pa.V = V; pa.L = L; pa.num_slots = d->num_slots;
     pa.act_bf16 = abf;
     pa.batch = d->batch;
@@ -671,7 +695,7 @@ int spec_launch(const rssm_gdn_dims* d, float* state, const void* q, const void*
     // 2. verify
     const int TBs = spec::tbl_floats(L, T);
     int off = spec::TILE;
-    const int off_kq = off; off += 2 * T * spec::KD * sa;
+    const int off_kq = off; off += 2 * T * spec::KD * 4;
     const int off_v = off;  off += T * spec::VB * sa;
     const int off_d = off;  off += L * spec::VB * 4;
     const int off_tbl = off; off += TBs * 4;
@@ -683,6 +707,7 @@ int spec_launch(const rssm_gdn_dims* d, float* state, const void* q, const void*
         va.ring_k = ring_k; va.ring_g = ring_g; va.ring_beta = ring_beta;
         va.ci = cache_indices; va.slot_wp = slot_wp; va.slot_base = slot_base;
         va.slot_flush = slot_flush; va.ws = static_cast<const float*>(workspace); va.o = o;
+        va.wsv = static_cast<const float*>(workspace) + spec::vec_offset_floats(d, T);
         va.dev_err = dev_err; va.batch = d->batch; va.HV = HV; va.HK = HK; va.V = V;
         va.L = L; va.num_slots = d->num_slots; va.act_bf16 = abf;
         va.out_bf16 = d->out_dtype == RSSM_BF16;
@@ -697,9 +722,10 @@ int spec_launch(const rssm_gdn_dims* d, float* state, const void* q, const void*
 }  // namespace
 
 extern "C" size_t rssm_gdn_spec_workspace_size(const rssm_gdn_dims* d, int32_t T) {
-    if (!d || d->batch < 0 || d->num_v_heads <= 0 || d->ring_len < 1 || T < 1 || T > spec::kMaxT)
+    if (!d || d->batch < 0 || d->num_v_heads <= 0 || d->num_k_heads <= 0 || d->ring_len < 1 ||
+        T < 1 || T > spec::kMaxT)
         return 0;
-    return (size_t)d->batch * d->num_v_heads * spec::tbl_floats(d->ring_len, T) * sizeof(float);
+    return spec::workspace_floats(d, T) * sizeof(float);
 }
 
 extern "C" int rssm_gdn_spec_verify(const rssm_gdn_dims* d, int32_t T, float* state, const void* q,
