@@ -137,6 +137,40 @@ int rssm_advance_cursors(int mode, int32_t* slot_wp, int32_t* slot_base, uint8_t
                          int32_t L, int32_t T, int32_t* row_wp, uint8_t* row_flush,
                          int32_t* dev_err, rssm_stream_t stream);
 
+/* Slot fork ("GDN ReplaySSM decode (Part A of RFC 28511)", 实现拆解 item 3: the
+ * memory pool's copy_from copies the ring buffers with the state and sets the
+ * cursors; 评论区精华: copying a slot whose ring still holds live entries must not
+ * lose them).
+ *
+ * A slot-indexed buffer: slot s occupies bytes [base + s * slot_bytes, base + (s+1)
+ * * slot_bytes) of a device array. */
+typedef struct rssm_slot_buffer {
+    void* base;        /* device pointer (16-byte aligned base and size copy fastest) */
+    size_t slot_bytes; /* bytes per slot, > 0 */
+} rssm_slot_buffer;
+
+#define RSSM_MAX_SLOT_BUFFERS 12
+
+/* rssm_copy_slots -- for i < n: copy slot src_slots[i]'s record into slot
+ * dst_slots[i] in every listed buffer. List every per-slot buffer of the cache --
+ * checkpoint, rings and cursors (Mamba2: state, ring_x, ring_dt, ring_B, slot_wp;
+ * gated delta net: state, ring_d, ring_k, ring_g, slot_wp; spec adds ring_v,
+ * ring_beta, slot_base, slot_flush) -- and the destination continues exactly as
+ * the source would (live ring entries and the cursor position are carried, so the
+ * source need not have flushed).
+ *   buffers: HOST array of n_buffers (1 .. RSSM_MAX_SLOT_BUFFERS) descriptors;
+ *     read during the call only.
+ *   src_slots, dst_slots: device int32 [n]. A pair with a negative entry is
+ *     skipped (padding); an entry >= num_slots skips the pair and sets
+ *     RSSM_DEVERR_SLOT; src == dst is a no-op. Destinations must be distinct and
+ *     must not be sources of the same call (undefined result otherwise).
+ * Errors: RSSM_ERR_INVALID_ARG for a NULL buffers array or base, n_buffers outside
+ * 1..RSSM_MAX_SLOT_BUFFERS, slot_bytes == 0, n < 0, num_slots <= 0, or (n > 0)
+ * NULL / misaligned slot arrays. */
+int rssm_copy_slots(const rssm_slot_buffer* buffers, int32_t n_buffers, const int32_t* src_slots,
+                    const int32_t* dst_slots, int32_t n, int32_t num_slots, int32_t* dev_err,
+                    rssm_stream_t stream);
+
 /* ------------------------------------------------------------------------- */
 /* Mamba2                                                                     */
 /* ------------------------------------------------------------------------- */

@@ -15,10 +15,12 @@ RSSM_F32, RSSM_BF16 = 0, 1
 RSSM_DEVERR_SLOT, RSSM_DEVERR_CURSOR, RSSM_DEVERR_TIMEOUT = 1, 2, 4
 RSSM_CURSOR_STANDARD, RSSM_CURSOR_SPEC_COMMIT, RSSM_CURSOR_RESET = 0, 1, 2
 RSSM_NOALLOC_WORKSPACE_BYTES = 16 << 20
+RSSM_MAX_SLOT_BUFFERS = 12
 
 # every symbol include/rssm.h declares
 EXPORTS = (
-    "rssm_status_string", "rssm_abi_version", "rssm_advance_cursors", "rssm_ring_append",
+    "rssm_status_string", "rssm_abi_version", "rssm_advance_cursors", "rssm_copy_slots",
+    "rssm_ring_append",
     "rssm_mamba2_workspace_size", "rssm_mamba2_precompute", "rssm_mamba2_output",
     "rssm_mamba2_decode", "rssm_mamba2_decode_noalloc", "rssm_mamba2_prepare", "rssm_mamba2_step",
     "rssm_mamba2_full_state_update", "rssm_mamba2_output_sr", "rssm_mamba2_step_sr",
@@ -38,6 +40,10 @@ class RSSMError(RuntimeError):
         self.status = status
         msg = _lib.rssm_status_string(status).decode() if _lib else str(status)
         super().__init__("%s failed: %s (status %d)" % (fn, msg, status))
+
+
+class SlotBuffer(ctypes.Structure):
+    _fields_ = [("base", ctypes.c_void_p), ("slot_bytes", ctypes.c_size_t)]
 
 
 class Mamba2Dims(ctypes.Structure):
@@ -67,6 +73,7 @@ def _declare(L):
         "rssm_abi_version": (_I, []),
         "rssm_advance_cursors": (_I, [_I, _VP, _VP, _VP, _VP, _VP, _VP, _I32, _I32, _I32, _I32,
                                       _VP, _VP, _VP, _VP]),
+        "rssm_copy_slots": (_I, [ctypes.POINTER(SlotBuffer), _I32, _VP, _VP, _I32, _I32, _VP, _VP]),
         "rssm_ring_append": (_I, [m2, _VP, _VP, _VP, _I, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
         "rssm_mamba2_workspace_size": (_SZ, [m2]),
         "rssm_mamba2_precompute": (_I, [m2, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _VP]),
@@ -173,6 +180,22 @@ def rssm_advance_cursors(mode, slot_wp, slot_base, slot_flush, cache_indices, fo
     _call("rssm_advance_cursors", mode, _ptr(slot_wp), _ptr(slot_base), _ptr(slot_flush),
           _ptr(cache_indices), _ptr(force_flush), _ptr(num_accepted), batch, num_slots, L, T,
           _ptr(row_wp), _ptr(row_flush), _ptr(dev_err), _stream(stream))
+
+
+def rssm_copy_slots(buffers, src_slots, dst_slots, n, num_slots, dev_err=None, stream=None):
+    """buffers: per-slot buffers, each a slot-major tensor (its first dimension is
+    the slot; slot_bytes = bytes of one slot) or a (pointer or tensor, slot_bytes)
+    pair."""
+    descs = []
+    for b in buffers:
+        if isinstance(b, tuple):
+            ptr, sb = b
+        else:
+            ptr, sb = b, b[0].numel() * b.element_size()
+        descs.append(SlotBuffer(_ptr(ptr), int(sb)))
+    arr = (SlotBuffer * max(len(descs), 1))(*descs)
+    _call("rssm_copy_slots", arr if descs else None, len(descs), _ptr(src_slots),
+          _ptr(dst_slots), int(n), int(num_slots), _ptr(dev_err), _stream(stream))
 
 
 def rssm_ring_append(dims, x, dt_raw, dt_bias, dt_softplus, B, cache_indices, row_wp, ring_x,

@@ -159,6 +159,11 @@ class Mamba2ReplayDecoder:
                                slots.shape[0], self.num_slots, self.L, 0, None, None, self.dev_err,
                                stream)
 
+    def copy_slots(self, src, dst, stream=None):
+        """Fork: slot dst[i] becomes a copy of slot src[i] (checkpoint, rings, cursor)."""
+        B.rssm_copy_slots([self.state, self.ring_x, self.ring_dt, self.ring_B, self.slot_wp],
+                          src, dst, src.shape[0], self.num_slots, self.dev_err, stream)
+
     def materialize(self, slots, out=None, stream=None):
         """Current fp32 state of the listed slots [n, H, P, N] (checkpoint folded with the
         live ring entries); pool, rings and cursors are left untouched."""
@@ -298,6 +303,11 @@ class GDNReplayDecoder:
                                slots.shape[0], self.num_slots, self.L, 0, None, None, self.dev_err,
                                stream)
 
+    def copy_slots(self, src, dst, stream=None):
+        """Fork: slot dst[i] becomes a copy of slot src[i] (checkpoint, rings, cursor)."""
+        B.rssm_copy_slots([self.state, self.ring_d, self.ring_k, self.ring_g, self.slot_wp],
+                          src, dst, src.shape[0], self.num_slots, self.dev_err, stream)
+
     def materialize(self, slots, out=None, stream=None):
         """Current fp32 state of the listed slots [n, HV, V, K]."""
         n = slots.shape[0]
@@ -394,6 +404,13 @@ class GDNSpecVerifier:
         B.rssm_advance_cursors(B.RSSM_CURSOR_RESET, self.slot_cnt, self.slot_base,
                                self.slot_flush, slots, None, None, slots.shape[0], self.num_slots,
                                self.L, self.T, None, None, self.dev_err, stream)
+
+    def copy_slots(self, src, dst, stream=None):
+        """Fork: slot dst[i] becomes a copy of slot src[i] (checkpoint, the five rings
+        and the three cursors, a pending fold included)."""
+        B.rssm_copy_slots([self.state, self.ring_d, self.ring_k, self.ring_g, self.ring_v,
+                           self.ring_beta, self.slot_cnt, self.slot_base, self.slot_flush],
+                          src, dst, src.shape[0], self.num_slots, self.dev_err, stream)
 
     def materialize(self, slots, out=None, stream=None):
         """Current fp32 state of the listed slots [n, HV, V, K]: the checkpoint folded with

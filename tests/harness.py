@@ -142,15 +142,16 @@ def cursor_reference(wl, steps=None):
 # gated delta net                                                             #
 # --------------------------------------------------------------------------- #
 
-def make_gdn_decoder(wl, out_dtype=torch.float32, full_state=False):
+def make_gdn_decoder(wl, out_dtype=torch.float32, full_state=False, max_batch=None):
     from ssm_linear_attention_gb300 import GDNFullStateDecoder, GDNReplayDecoder
     ad = torch_dt(wl.act_dtype)
+    mb = max(wl.batch if max_batch is None else max_batch, 1)
     if full_state:
         dec = GDNFullStateDecoder(wl.num_v_heads, wl.num_k_heads, wl.head_k_dim, wl.head_v_dim,
-                                  wl.num_slots, max(wl.batch, 1), act_dtype=ad, out_dtype=out_dtype)
+                                  wl.num_slots, mb, act_dtype=ad, out_dtype=out_dtype)
     else:
         dec = GDNReplayDecoder(wl.num_v_heads, wl.num_k_heads, wl.head_k_dim, wl.head_v_dim, wl.L,
-                               wl.num_slots, max(wl.batch, 1), act_dtype=ad, out_dtype=out_dtype)
+                               wl.num_slots, mb, act_dtype=ad, out_dtype=out_dtype)
     for s in wl.cache_indices():
         dec.state[int(s)] = to_dev(wl.slot_state(int(s)), torch.float32)
     return dec

@@ -110,3 +110,23 @@ def test_binding_raises_with_status(lib):
         ssm.rssm_advance_cursors(0, FAKE, None, None, FAKE, None, None, 4, 8, 0, 0, FAKE, FAKE,
                                  None, stream=0)
     assert ei.value.status == B.RSSM_ERR_CONFIG
+
+
+def test_copy_slots_validation(lib):
+    L = ssm.lib()
+    one = (B.SlotBuffer * 1)(B.SlotBuffer(FAKE, 64))
+    many = (B.SlotBuffer * 13)(*[B.SlotBuffer(FAKE, 64) for _ in range(13)])
+    zero = (B.SlotBuffer * 1)(B.SlotBuffer(FAKE, 0))
+    nul = (B.SlotBuffer * 1)(B.SlotBuffer(None, 64))
+    INV = B.RSSM_ERR_INVALID_ARG
+    assert L.rssm_copy_slots(None, 1, FAKE, FAKE, 2, 8, None, None) == INV
+    assert L.rssm_copy_slots(one, 0, FAKE, FAKE, 2, 8, None, None) == INV
+    assert L.rssm_copy_slots(many, 13, FAKE, FAKE, 2, 8, None, None) == INV
+    assert L.rssm_copy_slots(zero, 1, FAKE, FAKE, 2, 8, None, None) == INV
+    assert L.rssm_copy_slots(nul, 1, FAKE, FAKE, 2, 8, None, None) == INV
+    assert L.rssm_copy_slots(one, 1, FAKE, FAKE, -1, 8, None, None) == INV
+    assert L.rssm_copy_slots(one, 1, FAKE, FAKE, 2, 0, None, None) == INV
+    assert L.rssm_copy_slots(one, 1, None, FAKE, 2, 8, None, None) == INV
+    assert L.rssm_copy_slots(one, 1, FAKE, FAKE + 4, 2, 8, None, None) == INV
+    # nothing to copy: valid, launches nothing
+    assert L.rssm_copy_slots(one, 1, None, None, 0, 8, None, None) == B.RSSM_OK
