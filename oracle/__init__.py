@@ -39,7 +39,7 @@ from . import cursors
 __all__ = ["lib", "round_bf16", "round_f32", "softplus", "mamba2_step", "mamba2_replay",
            "gdn_step", "gdn_replay", "gdn_spec_round", "round_slots", "default_threads",
            "mamba2_run", "gdn_run", "gdn_spec_run", "cursors", "philox4x32_10", "round_bf16_sr",
-           "sr_bits", "round_slots_sr"]
+           "sr_bits", "round_slots_sr", "kda_step", "kda_replay", "kda_run"]
 
 _lib = None
 
@@ -88,6 +88,10 @@ def lib():
         L.orc_gdn_step.argtypes = [ctypes.POINTER(_GDims), _dp, _dp, _dp, _dp, _dp, _dp, _ip,
                                    _dp, ctypes.c_int]
         L.orc_gdn_replay.argtypes = [ctypes.POINTER(_GDims), ctypes.c_int, _dp, _ip, _ip, _dp,
+                                     _dp, _dp, _dp, _dp, _dp, _dp, _dp, ctypes.c_int]
+        L.orc_kda_step.argtypes = [ctypes.POINTER(_GDims), _dp, _dp, _dp, _dp, _dp, _dp, _ip,
+                                   _dp, ctypes.c_int]
+        L.orc_kda_replay.argtypes = [ctypes.POINTER(_GDims), ctypes.c_int, _dp, _ip, _ip, _dp,
                                      _dp, _dp, _dp, _dp, _dp, _dp, _dp, ctypes.c_int]
         L.orc_gdn_spec_round.argtypes = [ctypes.POINTER(_GDims), ctypes.c_int, _dp, _dp, _dp,
                                          _dp, _dp, _dp, _ip, _ip, _dp, ctypes.c_int]
@@ -255,6 +259,45 @@ def gdn_replay(L, S0, ci, wp, ek, ev, ebeta, eg, q, want_fold=False, want_d=Fals
     return out[0] if len(out) == 1 else tuple(out)
 
 
+def kda_step(state, q, k, v, beta, a, ci=None, nthreads=0):
+    """One KDA step (per-key-channel gate a [b,HV,K]) in place on ``state``
+    [slots,HV,V,K]. Returns o [b,HV,V]."""
+    assert state.dtype == np.float64 and state.flags.c_contiguous
+    q, k, v = _f64(q), _f64(k), _f64(v)
+    b, HK, K = q.shape
+    HV, V = v.shape[1], v.shape[2]
+    ci = _i32(np.arange(b) if ci is None else ci)
+    o = np.zeros((b, HV, V))
+    d = _GDims(b, HV, HK, K, V, state.shape[0])
+    be, aa = _f64(beta), _f64(a)
+    _check(lib().orc_kda_step(ctypes.byref(d), _p(state), _p(q), _p(k), _p(v), _p(be), _p(aa),
+                              _p(ci), _p(o), nthreads))
+    return o
+
+
+def kda_replay(L, S0, ci, wp, ek, ev, ebeta, ea, q, want_fold=False, want_d=False, nthreads=0):
+    """ReplaySSM closed form of the KDA step. Entries ek [b,L,HK,K], ev [b,L,HV,V],
+    ebeta [b,L,HV], ea [b,L,HV,K]; q = current query [b,HK,K]. Returns o (and the
+    folded state [b,HV,V,K], and d [b,L,HV,V])."""
+    S0 = _f64(S0)
+    ek, ev = _f64(ek), _f64(ev)
+    b, _, HK, K = ek.shape
+    HV, V = ev.shape[2], ev.shape[3]
+    o = np.zeros((b, HV, V))
+    Sf = np.zeros((b, HV, V, K)) if want_fold else None
+    dd = np.zeros((b, L, HV, V)) if want_d else None
+    d = _GDims(b, HV, HK, K, V, S0.shape[0])
+    a = [_i32(ci), _i32(wp), _f64(ebeta), _f64(ea), _f64(q)]
+    _check(lib().orc_kda_replay(ctypes.byref(d), L, _p(S0), _p(a[0]), _p(a[1]), _p(ek), _p(ev),
+                                _p(a[2]), _p(a[3]), _p(a[4]), _p(o), _p(Sf), _p(dd), nthreads))
+    out = [o]
+    if want_fold:
+        out.append(Sf)
+    if want_d:
+        out.append(dd)
+    return out[0] if len(out) == 1 else tuple(out)
+
+
 def gdn_spec_round(state, T, q, k, v, beta, g, acc, ci=None, nthreads=0):
     """One verify round over T drafts (inputs [b,T,...]); keeps the state after acc[b]
     drafts. Returns per-draft outputs o [b,T,HV,V]."""
@@ -347,6 +390,47 @@ def gdn_run(wl, rows: Optional[Sequence[int]] = None, steps: Optional[int] = Non
         rw, rf = cursors.advance_standard(slot_wp, ci_loc, force, wl.L)
         o = gdn_step(state, inp["q"][rows], inp["k"][rows], inp["v"][rows], inp["beta"][rows],
                      inp["g"][rows], ci_loc, nthreads)
+        if mode == "full":
+            upd = [int(s) for s in ci_loc if s >= 0]
+        else:
+            upd = [int(ci_loc[i]) for i in range(n) if ci_loc[i] >= 0 and rf[i]]
+        round_slots(state, upd, "fp32")
+        for s in upd:
+            ckpt[s] = state[s]
+        return o, rw, rf
+
+    for j in range(wl.max_history()):
+        one(wl.history_inputs(j), _local_ci(wl.history_ci(j), rows), None)
+    os_, wps, fls = [], [], []
+    for t in range(steps):
+        inp = wl.step_inputs(t)
+        force = wl.force_mask(t)
+        o, rw, rf = one(inp, _local_ci(ci_full, rows), None if force is None else force[rows])
+        if keep_o:
+            os_.append(o)
+        wps.append(rw)
+        fls.append(rf)
+    return dict(o=os_, row_wp=np.array(wps, dtype=np.int64).reshape(steps, n),
+                row_flush=np.array(fls, dtype=np.int64).reshape(steps, n), ckpt=ckpt,
+                state=state, slot_wp=np.array(slot_wp))
+
+
+def kda_run(wl, rows: Optional[Sequence[int]] = None, steps: Optional[int] = None,
+            mode: str = "replay", nthreads: int = 0, keep_o: bool = True) -> Dict:
+    """KDA counterpart of gdn_run (fp32 state; inputs carry the gate vector "a")."""
+    rows = np.arange(wl.batch) if rows is None else np.asarray(rows)
+    steps = wl.steps if steps is None else steps
+    n = len(rows)
+    ci_full = wl.cache_indices()
+    state = np.ascontiguousarray(
+        np.stack([wl.slot_state(int(ci_full[r])) for r in rows]).astype(np.float64))
+    ckpt = state.copy()
+    slot_wp = [0] * n
+
+    def one(inp, ci_loc, force):
+        rw, rf = cursors.advance_standard(slot_wp, ci_loc, force, wl.L)
+        o = kda_step(state, inp["q"][rows], inp["k"][rows], inp["v"][rows], inp["beta"][rows],
+                     inp["a"][rows], ci_loc, nthreads)
         if mode == "full":
             upd = [int(s) for s in ci_loc if s >= 0]
         else:

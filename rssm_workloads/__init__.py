@@ -27,6 +27,8 @@ state [HV, V, K] with grouped key heads):
                 N(0, 0.05), 512 slots, q and k L2-normalised per head.
   gdn_spec      batch 128, T 4 drafts per round, L 16, 32 rounds, accepted drafts
                 ~ U{0..4} per row and round.
+  kda_decode    gdn_decode's geometry with a per-key-channel gate a [HV, K] per
+                step instead of the scalar g.
 """
 from dataclasses import dataclass, field
 from typing import Dict, Optional
@@ -35,7 +37,8 @@ import numpy as np
 
 __all__ = [
     "round_bf16_f32", "Mamba2Workload", "GDNWorkload", "GDNSpecWorkload",
-    "mamba2_tiny", "mamba2_large", "mamba2_sweep", "gdn_decode", "gdn_spec",
+    "mamba2_tiny", "mamba2_large", "mamba2_sweep", "gdn_decode", "gdn_spec", "kda_decode",
+    "KDAWorkload",
 ]
 
 # stream tags
@@ -284,6 +287,28 @@ class GDNSpecWorkload(GDNWorkload):
     def accepted(self, r: int) -> np.ndarray:
         """Accepted draft count per row for round r, U{0..T}."""
         return _rng(self.seed, _T_ACC, r).integers(0, self.T + 1, self.batch).astype(np.int32)
+
+
+@dataclass
+class KDAWorkload(GDNWorkload):
+    """GDN geometry with a per-key-channel gate a [.., HV, K] in (0, 1) instead of the
+    scalar g: a = exp(-softplus(N(0, 1) - 2)) per element (mean ~0.87, so ring
+    entries several steps old still matter)."""
+    name: str = "kda"
+
+    def _token_inputs(self, rng, lead):
+        d = GDNWorkload._token_inputs(self, rng, lead)
+        x = rng.standard_normal(lead + (self.num_v_heads, self.head_k_dim)) - 2.0
+        sp = np.where(x > 0, x + np.log1p(np.exp(-np.abs(x))), np.log1p(np.exp(x)))
+        d["a"] = np.exp(-sp).astype(np.float32)
+        return d
+
+
+def kda_decode(**kw) -> KDAWorkload:
+    d = dict(batch=256, num_v_heads=32, num_k_heads=16, head_k_dim=128, head_v_dim=128, L=16,
+             num_slots=512, steps=64, act_dtype="bf16", state_std=0.05, name="kda_decode")
+    d.update(kw)
+    return KDAWorkload(**d)
 
 
 def gdn_decode(**kw) -> GDNWorkload:
