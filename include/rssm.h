@@ -481,6 +481,68 @@ int rssm_gdn_full_state_decode(const rssm_gdn_dims* dims, float* state, const vo
                                rssm_stream_t stream);
 
 /* ------------------------------------------------------------------------- */
+/* KDA: the gated delta rule with a per-key-channel gate                      */
+/* ------------------------------------------------------------------------- */
+
+/* [GDN] 实现拆解 item 1: one buffered decode kernel serves the scalar GDN gate and
+ * the KDA per-K gate (IS_KDA); 评论区精华: the KDA gate ring is g_cache [slots, HV,
+ * L, K] and the report saw no gain for KDA. Reading of the recurrence (the pages
+ * print none): the GDN rule with the scalar gate replaced by Diag(a), a in (0, 1]^K
+ * per value head:
+ *   S <- S Diag(a) + beta (v - S Diag(a) k) k^T,  o = S q.
+ * Dims are rssm_gdn_dims (K = 128, V a multiple of 32, L <= 64), fp32 state.
+ * Layouts (row-major, dense):
+ *   state   [num_slots][HV][V][K] float32  checkpoint S0 per slot
+ *   ring_d  [num_slots][HV][V/32][L][32] float32 (as the GDN ring d)
+ *   ring_k  [num_slots][HK][L][K] act_dtype
+ *   ring_a  [num_slots][HV][L][K] float32  the gates a_i
+ *   q, k    [batch][HK][K] act_dtype; v [batch][HV][V] act_dtype
+ *   beta    [batch][HV] float32; a [batch][HV][K] float32; o [batch][HV][V] out_dtype
+ * Cursors come from rssm_advance_cursors (STANDARD), as for the GDN. */
+
+/* Bytes of workspace rssm_kda_prepare / rssm_kda_output need: per (row, value
+ * head) the gated vectors Gam o k_t, Gam o q_t and Gam = prod_{j<=w} a_j, the
+ * k_i . (Gam_i o k_t) and k_i . (Gam_i o q_t) tables and beta; then per (row,
+ * value head) the gated keys Gam_i o k_i of flush rows. 0 for invalid dims. */
+size_t rssm_kda_workspace_size(const rssm_gdn_dims* dims);
+
+/* rssm_kda_prepare -- append a_t into ring_a and k_t into ring_k at entry
+ * row_wp[b], and build the tables of the current step (one CTA per (row, value
+ * head)). Needs the cursors of the step (row_wp, row_flush). */
+int rssm_kda_prepare(const rssm_gdn_dims* dims, const void* q, const void* k, const float* a,
+                     const float* beta, const int32_t* cache_indices, const int32_t* row_wp,
+                     const uint8_t* row_flush, void* ring_k, float* ring_a, void* workspace,
+                     size_t workspace_bytes, int32_t* dev_err, rssm_stream_t stream);
+
+/* rssm_kda_output -- the fused output / flush kernel: streams each (row, value
+ * head, 32 value rows) tile of S0 once,
+ *   u   = S0 (Gam o k_t) + sum_{i<w} (k_i . (Gam_i o k_t)) d_i,  d_t = beta (v - u),
+ *   o   = S0 (Gam o q_t) + sum_{i<=w} (k_i . (Gam_i o q_t)) d_i,
+ * (Gam_i = prod_{j=i+1..w} a_j per channel, Gam = prod_{j<=w} a_j), writes d_t into
+ * ring_d entry w and, on flush rows, S = S0 Diag(Gam) + sum_{i<=w} d_i (Gam_i o
+ * k_i)^T. Needs the tables of rssm_kda_prepare. */
+int rssm_kda_output(const rssm_gdn_dims* dims, float* state, const void* v, float* ring_d,
+                    const int32_t* cache_indices, const int32_t* row_wp,
+                    const uint8_t* row_flush, const void* workspace, size_t workspace_bytes,
+                    void* o, int32_t* dev_err, rssm_stream_t stream);
+
+/* rssm_kda_step -- one KDA ReplaySSM decode step: rssm_advance_cursors
+ * (STANDARD; skipped when advance == 0), rssm_kda_prepare, rssm_kda_output. */
+int rssm_kda_step(const rssm_gdn_dims* dims, int advance, const uint8_t* force_flush,
+                  int32_t* slot_wp, int32_t* row_wp, uint8_t* row_flush, float* state,
+                  const void* q, const void* k, const void* v, const float* beta, const float* a,
+                  const int32_t* cache_indices, void* ring_k, float* ring_a, float* ring_d,
+                  void* workspace, size_t workspace_bytes, void* o, int32_t* dev_err,
+                  rssm_stream_t stream);
+
+/* rssm_kda_full_state_decode -- the conventional KDA decode step: read S, apply
+ * S <- S Diag(a) + beta (v - S Diag(a) k) k^T, write S, o = S q. */
+int rssm_kda_full_state_decode(const rssm_gdn_dims* dims, float* state, const void* q,
+                               const void* k, const void* v, const float* beta, const float* a,
+                               const int32_t* cache_indices, void* o, int32_t* dev_err,
+                               rssm_stream_t stream);
+
+/* ------------------------------------------------------------------------- */
 /* Gated delta net: speculative verify                                        */
 /* ------------------------------------------------------------------------- */
 

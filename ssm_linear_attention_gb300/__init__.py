@@ -15,7 +15,7 @@ def __getattr__(name):
     # decoder runners import torch; load them lazily
     if name in ("Mamba2ReplayDecoder", "Mamba2FullStateDecoder", "GDNReplayDecoder",
                 "GDNFullStateDecoder", "GDNSpecVerifier", "GDNSpecFullStateVerifier",
-                "torch_dtype_code"):
+                "KDAReplayDecoder", "KDAFullStateDecoder", "torch_dtype_code"):
         from . import decoder
         return getattr(decoder, name)
     raise AttributeError(name)

@@ -31,7 +31,8 @@ EXPORTS = (
     "rssm_gdn_full_state_decode", "rssm_gdn_spec_workspace_size", "rssm_gdn_spec_verify",
     "rssm_mamba2_materialize_state", "rssm_gdn_materialize_state",
     "rssm_gdn_spec_full_state_snapshot_bytes", "rssm_gdn_spec_full_state_verify",
-    "rssm_gdn_spec_full_state_commit",
+    "rssm_gdn_spec_full_state_commit", "rssm_kda_workspace_size", "rssm_kda_prepare",
+    "rssm_kda_output", "rssm_kda_step", "rssm_kda_full_state_decode",
 )
 
 
@@ -119,6 +120,14 @@ def _declare(L):
         "rssm_mamba2_materialize_state": (_I, [m2, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                                _VP]),
         "rssm_gdn_materialize_state": (_I, [gd, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                                            _VP]),
+        "rssm_kda_workspace_size": (_SZ, [gd]),
+        "rssm_kda_prepare": (_I, [gd, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP,
+                                  _VP]),
+        "rssm_kda_output": (_I, [gd, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _VP, _VP]),
+        "rssm_kda_step": (_I, [gd, _I, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
+                               _VP, _VP, _VP, _VP, _SZ, _VP, _VP, _VP]),
+        "rssm_kda_full_state_decode": (_I, [gd, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                             _VP]),
         "rssm_gdn_spec_verify": (_I, [gd, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                       _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _VP, _VP]),
@@ -404,3 +413,37 @@ def rssm_gdn_spec_full_state_commit(dims, T, state, snapshots, cache_indices, nu
                                     dev_err=None, stream=None):
     _call("rssm_gdn_spec_full_state_commit", ctypes.byref(dims), T, _ptr(state), _ptr(snapshots),
           _ptr(cache_indices), _ptr(num_accepted), _ptr(dev_err), _stream(stream))
+
+
+def rssm_kda_workspace_size(dims):
+    return lib().rssm_kda_workspace_size(ctypes.byref(dims))
+
+
+def rssm_kda_prepare(dims, q, k, a, beta, cache_indices, row_wp, row_flush, ring_k, ring_a,
+                     workspace, workspace_bytes, dev_err=None, stream=None):
+    _call("rssm_kda_prepare", ctypes.byref(dims), _ptr(q), _ptr(k), _ptr(a), _ptr(beta),
+          _ptr(cache_indices), _ptr(row_wp), _ptr(row_flush), _ptr(ring_k), _ptr(ring_a),
+          _ptr(workspace), workspace_bytes, _ptr(dev_err), _stream(stream))
+
+
+def rssm_kda_output(dims, state, v, ring_d, cache_indices, row_wp, row_flush, workspace,
+                    workspace_bytes, o, dev_err=None, stream=None):
+    _call("rssm_kda_output", ctypes.byref(dims), _ptr(state), _ptr(v), _ptr(ring_d),
+          _ptr(cache_indices), _ptr(row_wp), _ptr(row_flush), _ptr(workspace), workspace_bytes,
+          _ptr(o), _ptr(dev_err), _stream(stream))
+
+
+def rssm_kda_step(dims, advance, force_flush, slot_wp, row_wp, row_flush, state, q, k, v, beta, a,
+                  cache_indices, ring_k, ring_a, ring_d, workspace, workspace_bytes, o,
+                  dev_err=None, stream=None):
+    _call("rssm_kda_step", ctypes.byref(dims), int(advance), _ptr(force_flush), _ptr(slot_wp),
+          _ptr(row_wp), _ptr(row_flush), _ptr(state), _ptr(q), _ptr(k), _ptr(v), _ptr(beta),
+          _ptr(a), _ptr(cache_indices), _ptr(ring_k), _ptr(ring_a), _ptr(ring_d), _ptr(workspace),
+          workspace_bytes, _ptr(o), _ptr(dev_err), _stream(stream))
+
+
+def rssm_kda_full_state_decode(dims, state, q, k, v, beta, a, cache_indices, o, dev_err=None,
+                               stream=None):
+    _call("rssm_kda_full_state_decode", ctypes.byref(dims), _ptr(state), _ptr(q), _ptr(k),
+          _ptr(v), _ptr(beta), _ptr(a), _ptr(cache_indices), _ptr(o), _ptr(dev_err),
+          _stream(stream))

@@ -346,6 +346,80 @@ class GDNFullStateDecoder:
         return o
 
 
+class KDAReplayDecoder(GDNReplayDecoder):
+    """ReplaySSM decode of the gated delta rule with a per-key-channel gate (KDA) for
+    one layer. Buffers as GDNReplayDecoder, with the gate ring ring_a [num_slots, HV,
+    L, K] float32 in place of ring_g. A step is rssm_kda_step (cursor advance,
+    prepare, output: three launches)."""
+
+    def __init__(self, num_v_heads, num_k_heads, head_k_dim, head_v_dim, ring_len, num_slots,
+                 max_batch, act_dtype=torch.bfloat16, out_dtype=torch.bfloat16, device=None):
+        super().__init__(num_v_heads, num_k_heads, head_k_dim, head_v_dim, ring_len, num_slots,
+                         max_batch, act_dtype, out_dtype, device)
+        dev = self.state.device
+        self.ring_g = None
+        self.ring_a = torch.zeros(num_slots, num_v_heads, ring_len, head_k_dim, device=dev,
+                                  dtype=torch.float32)
+        self.ws_bytes = B.rssm_kda_workspace_size(self.dims(max_batch))
+        self.workspace = torch.empty(max(self.ws_bytes, 16), device=dev, dtype=torch.uint8)
+
+    def prepare(self, q, k, a, beta, cache_indices, stream=None):
+        """Ring append and tables (the cursors of the step must be set: advance())."""
+        B.rssm_kda_prepare(self.dims(q.shape[0]), q, k, a, beta, cache_indices, self.row_wp,
+                           self.row_flush, self.ring_k, self.ring_a, self.workspace,
+                           self.ws_bytes, self.dev_err, stream)
+
+    def output(self, v, cache_indices, o=None, stream=None):
+        b = v.shape[0]
+        o = self.o[:b] if o is None else o
+        B.rssm_kda_output(self.dims(b), self.state, v, self.ring_d, cache_indices, self.row_wp,
+                          self.row_flush, self.workspace, self.ws_bytes, o, self.dev_err, stream)
+        return o
+
+    def step(self, q, k, v, beta, a, cache_indices, force_flush=None, o=None, stream=None,
+             advance=True):
+        """One decode step (gate vectors a [b, HV, K]). Returns o [b, HV, V]."""
+        b = q.shape[0]
+        o = self.o[:b] if o is None else o
+        B.rssm_kda_step(self.dims(b), advance, force_flush, self.slot_wp, self.row_wp,
+                        self.row_flush, self.state, q, k, v, beta, a, cache_indices, self.ring_k,
+                        self.ring_a, self.ring_d, self.workspace, self.ws_bytes, o, self.dev_err,
+                        stream)
+        return o
+
+    def step_staged(self, q, k, v, beta, a, cache_indices, force_flush=None, o=None, stream=None,
+                    advance=True):
+        """The same step as three calls (cursor, prepare, output)."""
+        if advance:
+            self.advance(cache_indices, force_flush, stream)
+        self.prepare(q, k, a, beta, cache_indices, stream)
+        return self.output(v, cache_indices, o, stream)
+
+    def copy_slots(self, src, dst, stream=None):
+        B.rssm_copy_slots([self.state, self.ring_d, self.ring_k, self.ring_a, self.slot_wp],
+                          src, dst, src.shape[0], self.num_slots, self.dev_err, stream)
+
+    def append(self, *args, **kw):
+        raise NotImplementedError("KDA appends inside prepare()")
+
+    def precompute(self, *args, **kw):
+        raise NotImplementedError("KDA builds its tables inside prepare()")
+
+    def materialize(self, *args, **kw):
+        raise NotImplementedError("no KDA materialize entry point")
+
+
+class KDAFullStateDecoder(GDNFullStateDecoder):
+    """The conventional KDA decode step (state read and written every step)."""
+
+    def step(self, q, k, v, beta, a, cache_indices, o=None, stream=None):
+        b = q.shape[0]
+        o = self.o[:b] if o is None else o
+        B.rssm_kda_full_state_decode(self.dims(b), self.state, q, k, v, beta, a, cache_indices, o,
+                                     self.dev_err, stream)
+        return o
+
+
 class GDNSpecVerifier:
     """ReplaySSM speculative verify for the gated delta net (linear draft chain of T).
 

@@ -213,3 +213,54 @@ def run_gpu_spec(wl, rounds=None, out_dtype=torch.float32, rows=None):
     torch.cuda.synchronize()
     c = np.array(curs, dtype=np.int64)   # [rounds+1, 3, batch]
     return dict(o=outs, cnt=c[:, 0], base=c[:, 1], flush=c[:, 2], ver=ver)
+
+
+# --------------------------------------------------------------------------- #
+# KDA (per-key-channel gate)                                                  #
+# --------------------------------------------------------------------------- #
+
+def make_kda_decoder(wl, out_dtype=torch.float32, full_state=False, max_batch=None):
+    from ssm_linear_attention_gb300 import KDAFullStateDecoder, KDAReplayDecoder
+    ad = torch_dt(wl.act_dtype)
+    mb = max(wl.batch if max_batch is None else max_batch, 1)
+    if full_state:
+        dec = KDAFullStateDecoder(wl.num_v_heads, wl.num_k_heads, wl.head_k_dim, wl.head_v_dim,
+                                  wl.num_slots, mb, act_dtype=ad, out_dtype=out_dtype)
+    else:
+        dec = KDAReplayDecoder(wl.num_v_heads, wl.num_k_heads, wl.head_k_dim, wl.head_v_dim, wl.L,
+                               wl.num_slots, mb, act_dtype=ad, out_dtype=out_dtype)
+    for s in wl.cache_indices():
+        dec.state[int(s)] = to_dev(wl.slot_state(int(s)), torch.float32)
+    return dec
+
+
+def kda_inputs_dev(wl, inp):
+    ad = torch_dt(wl.act_dtype)
+    return (to_dev(inp["q"], ad), to_dev(inp["k"], ad), to_dev(inp["v"], ad),
+            to_dev(inp["beta"], torch.float32), to_dev(inp["a"], torch.float32))
+
+
+def run_gpu_kda(wl, steps=None, out_dtype=torch.float32, full_state=False, rows=None,
+                staged=False):
+    steps = wl.steps if steps is None else steps
+    dec = make_kda_decoder(wl, out_dtype, full_state)
+    rows = np.arange(wl.batch) if rows is None else np.asarray(rows)
+    run = dec.step_staged if staged else dec.step
+    for j in range(wl.max_history()):
+        q, k, v, be, a = kda_inputs_dev(wl, wl.history_inputs(j))
+        (dec.step if full_state else run)(q, k, v, be, a, to_dev(wl.history_ci(j), torch.int32))
+    ci_d = to_dev(wl.cache_indices(), torch.int32)
+    os_, wps, fls = [], [], []
+    sel = torch.as_tensor(rows, device="cuda")
+    for t in range(steps):
+        q, k, v, be, a = kda_inputs_dev(wl, wl.step_inputs(t))
+        if full_state:
+            o = dec.step(q, k, v, be, a, ci_d)
+        else:
+            f = wl.force_mask(t)
+            o = run(q, k, v, be, a, ci_d, None if f is None else to_dev(f, torch.uint8))
+            wps.append(dec.row_wp[: wl.batch].cpu().numpy().copy())
+            fls.append(dec.row_flush[: wl.batch].cpu().numpy().copy())
+        os_.append(o[sel].float().cpu().numpy().astype(np.float64))
+    torch.cuda.synchronize()
+    return dict(o=os_, row_wp=np.array(wps), row_flush=np.array(fls), dec=dec)
