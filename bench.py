@@ -76,7 +76,8 @@ def parse():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--batch", type=int, default=None)
     ap.add_argument("--num-slots", type=int, default=None)
-    ap.add_argument("--workload", default="mamba2", choices=["mamba2", "gdn", "spec", "sweep"])
+    ap.add_argument("--workload", default="mamba2",
+                    choices=["mamba2", "gdn", "spec", "kda", "sweep"])
     ap.add_argument("--no-gdn", action="store_true",
                     help="mamba2 line only (skip the gdn_decode / gdn_spec sub-objects)")
     ap.add_argument("--sweep-steps", type=int, default=200)
@@ -267,6 +268,38 @@ def gdn_full_bytes(wl, batch, out_bytes=2):
     HV, HK, K, V = wl.num_v_heads, wl.num_k_heads, wl.head_k_dim, wl.head_v_dim
     sa = 2 if wl.act_dtype == "bf16" else 4
     return batch * (2 * HV * V * K * 4 + 2 * HK * K * sa + HV * V * sa + 2 * HV * 4
+                    + HV * V * out_bytes)
+
+
+def kda_output_bytes(wl, row_wp, row_flush, out_bytes=2):
+    """Algorithmic bytes of one KDA output-kernel launch: checkpoint read, d entries
+    0..w-1, v, o, the d write and, on flush rows, the state write. The prologue's
+    gated vectors and tables are excluded (as the GDN and Mamba2 tables are)."""
+    HV, V, K = wl.num_v_heads, wl.head_v_dim, wl.head_k_dim
+    sa = 2 if wl.act_dtype == "bf16" else 4
+    w = row_wp.astype(np.int64)
+    f = row_flush.astype(np.int64)
+    per_row = (HV * V * K * 4 + w * HV * V * 4 + HV * V * 4 + HV * V * sa + HV * V * out_bytes
+               + f * HV * V * K * 4)
+    return int(per_row.sum())
+
+
+def kda_step_bytes(wl, row_wp, row_flush, out_bytes=2):
+    """Algorithmic bytes of a whole KDA step: the output kernel's, plus the ring k and
+    gate entries 0..w-1 the prologue reads, the step's q, k, a, beta and the k and a
+    appends."""
+    HV, HK, K = wl.num_v_heads, wl.num_k_heads, wl.head_k_dim
+    sa = 2 if wl.act_dtype == "bf16" else 4
+    w = row_wp.astype(np.int64)
+    pro = w * (HK * K * sa + HV * K * 4) + 2 * HK * K * sa + HV * K * 4 + 4 * HV \
+        + HK * K * sa + HV * K * 4
+    return kda_output_bytes(wl, row_wp, row_flush, out_bytes) + int(pro.sum())
+
+
+def kda_full_bytes(wl, batch, out_bytes=2):
+    HV, HK, K, V = wl.num_v_heads, wl.num_k_heads, wl.head_k_dim, wl.head_v_dim
+    sa = 2 if wl.act_dtype == "bf16" else 4
+    return batch * (2 * HV * V * K * 4 + 2 * HK * K * sa + HV * V * sa + HV * K * 4 + HV * 4
                     + HV * V * out_bytes)
 
 
@@ -827,6 +860,134 @@ def run_gdn(args, dist, sub=False):
     return line
 
 
+KDA_WORKLOAD = ("kda replayssm decode: batch 256, HV 32, HK 16, K=V 128, L 16, fp32 state pool "
+                "512 slots ~N(0,0.05), bf16 q/k/v, fp32 beta, per-channel gates a [HV, K] in (0,1)")
+
+
+def run_kda(args, dist, sub=False):
+    """The KDA (per-key-channel gate) decode step against the conventional KDA kernel."""
+    import torch
+
+    import rssm_workloads as W
+    import ssm_linear_attention_gb300 as ssm
+
+    dev = _device(dist)
+    ssm.lib()
+    kw = {}
+    if not sub and args.batch:
+        kw["batch"] = args.batch
+    if not sub and args.num_slots:
+        kw["num_slots"] = args.num_slots
+    wl = W.kda_decode(seed=shard_seed(args.seed, dist.rank), **kw)
+    bf = torch.bfloat16
+    ci_np = wl.cache_indices()
+    ci = torch.from_numpy(ci_np).to(dev)
+    dec = ssm.KDAReplayDecoder(wl.num_v_heads, wl.num_k_heads, wl.head_k_dim, wl.head_v_dim, wl.L,
+                               wl.num_slots, wl.batch, act_dtype=bf, out_dtype=bf, device=dev)
+    for s in ci_np:
+        dec.state[int(s)] = torch.from_numpy(wl.slot_state(int(s))).to(dev)
+
+    def to_dev(inp):
+        return [torch.from_numpy(inp[k]).to(dev, bf if k in ("q", "k", "v") else torch.float32)
+                for k in ("q", "k", "v", "beta", "a")]
+
+    for j in range(wl.max_history()):
+        dec.step(*to_dev(wl.history_inputs(j)), torch.from_numpy(wl.history_ci(j)).to(dev))
+    nsets = min(args.input_sets, 32)
+    sets = [to_dev(wl.step_inputs(t)) for t in range(nsets)]
+    torch.cuda.synchronize()
+    K = args.steps
+    G = min(len(sets), max(K, 1))
+
+    def pre_fn(j):
+        q, k, v, beta, a = sets[j]
+
+        def f():
+            dec.advance(ci)
+            dec.prepare(q, k, a, beta, ci)
+        return f
+
+    def out_fn(j):
+        q, k, v, beta, a = sets[j]
+        return lambda: dec.output(v, ci)
+
+    for k in range(max(args.warmup, 3)):
+        pre_fn(k % G)()
+        out_fn(k % G)()
+    torch.cuda.synchronize()
+    g_step, g_samp, evs = _sampled_graphs(
+        [(lambda j=j: (pre_fn(j)(), out_fn(j)())) for j in range(G)],
+        [(pre_fn(j), out_fn(j), None) for j in range(G)])
+    for k in range(max(args.warmup, 3)):
+        g_step[k % G].replay()
+    torch.cuda.synchronize()
+    slot_wp0 = dec.slot_wp.cpu().numpy().astype(np.int64)
+    off = args.warmup + max(args.warmup, 3)
+    elapsed, out_ms, clocks, ks = _timed_graphs(g_step, g_samp, evs, K, dist, dev, offset=off,
+                                                clocks=not sub)
+    assert int(dec.dev_err.abs().sum().item()) == 0, "device error flag set during the kda bench"
+    del g_step, g_samp
+    ms_step = elapsed / K
+    rows_s = dist.world * wl.batch / (ms_step * 1e-3)
+    curs = simulate_cursors(slot_wp0, ci_np, wl.L, K)
+    out_b = np.mean([kda_output_bytes(wl, *curs[k]) for k in ks])
+    step_b = np.mean([kda_step_bytes(wl, w, f) for w, f in curs])
+    out_avg_ms = float(np.mean(out_ms))
+    peak, peak_kind = read_peaks()
+    achieved = out_b / (out_avg_ms * 1e-3) / 1e9
+
+    full = None
+    if not args.no_full_state:
+        fdec = ssm.KDAFullStateDecoder(wl.num_v_heads, wl.num_k_heads, wl.head_k_dim,
+                                       wl.head_v_dim, wl.num_slots, wl.batch, act_dtype=bf,
+                                       out_dtype=bf, device=dev)
+        fdec.state.copy_(dec.state)
+        del dec
+
+        def full_fn(j):
+            q, k, v, beta, a = sets[j]
+            return lambda: fdec.step(q, k, v, beta, a, ci)
+
+        for k in range(max(args.warmup, 3)):
+            full_fn(k % G)()
+        torch.cuda.synchronize()
+        g_full, g_fs, fevs = _sampled_graphs([full_fn(j) for j in range(G)],
+                                             [(None, full_fn(j), None) for j in range(G)])
+        Kf = max(50, K // 4)
+        f_el, f_per, _, _ = _timed_graphs(g_full, g_fs, fevs, Kf, dist, dev, clocks=False)
+        del g_full, g_fs
+        f_ms = f_el / Kf
+        fb = kda_full_bytes(wl, wl.batch)
+        full = {"ms_per_step": f_ms, "us_per_step": f_ms * 1e3,
+                "rows_per_s": dist.world * wl.batch / (f_ms * 1e-3),
+                "achieved_gbs": fb / (float(np.mean(f_per)) * 1e-3) / 1e9, "bytes_per_step": fb,
+                "hbm_frac": fb / (float(np.mean(f_per)) * 1e-3) / 1e9 / peak,
+                "replay_speedup": f_ms / ms_step}
+
+    return {
+        "metric": "kda decode rows/s and µs/step at batch %d; achieved HBM GB/s" % wl.batch,
+        "value": rows_s, "unit": UNIT, "n_gpus": dist.world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": ms_step, "us_per_step": ms_step * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": KDA_WORKLOAD, "global_batch": dist.world * wl.batch,
+                   "batch_per_gpu": wl.batch, "HV": wl.num_v_heads, "HK": wl.num_k_heads,
+                   "K": wl.head_k_dim, "V": wl.head_v_dim, "ring_len": wl.L,
+                   "timing": "one CUDA graph per step (cursor + prepare + output); on every 7th step the graph also holds CUDA events around the output kernel",
+                   "l2": "inputs larger than L2: 537 MB of fp32 checkpoint tiles per step"},
+        "achieved_hbm_gbs": step_b / (ms_step * 1e-3) / 1e9,
+        "hbm_frac_step": step_b / (ms_step * 1e-3) / 1e9 / peak,
+        "bytes_per_step": int(step_b),
+        "roofline": {"bound": "hbm", "kernel": "kda output kernel (fp32 state, 32-row tiles)",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "peak_source": peak_kind,
+                     "traffic": traffic_record("kda.cu", "kda_output_kernel_batch256.md"),
+                     "algorithmic_bytes_per_launch": int(out_b), "avg_launch_ms": out_avg_ms},
+        "full_state": full,
+        "gpu_launches": 3 * K,
+        "clocks": clocks,
+    }
+
+
 # --------------------------------------------------------------------------- #
 # gated delta net: speculative verify                                         #
 # --------------------------------------------------------------------------- #
@@ -1137,6 +1298,8 @@ def main():
             line = run_gdn(args, dist)
         elif args.workload == "spec":
             line = run_spec(args, dist)
+        elif args.workload == "kda":
+            line = run_kda(args, dist)
         elif args.workload == "sweep":
             line = run_sweep(args, dist)
         else:
@@ -1144,6 +1307,7 @@ def main():
             if not args.no_gdn:
                 line["gdn_decode"] = run_gdn(args, dist, sub=True)
                 line["gdn_spec"] = run_spec(args, dist, sub=True)
+                line["kda_decode"] = run_kda(args, dist, sub=True)
         if dist.rank == 0 and line is not None:
             print(json.dumps(line), flush=True)
     finally:

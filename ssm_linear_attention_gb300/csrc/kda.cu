@@ -54,8 +54,11 @@ int check_dims(const rssm_gdn_dims* d) {
 }
 
 // ----------------------------------------------------------------------------
-// prologue: ring append and tables, one CTA of KD threads per (row, value head)
+// prologue: ring append and tables, one warp per (row, value head)
 // ----------------------------------------------------------------------------
+
+constexpr int kPreWarps = 4;  // (row, value head) items per CTA
+constexpr int kChunkM = 16;   // ring entries whose dot products reduce together
 
 struct PreArgs {
     const void* q;
@@ -70,83 +73,98 @@ struct PreArgs {
     float* ws;
     float* ws_kg;
     int32_t* dev_err;
-    int HV, HK, L, num_slots, act_bf16;
+    int n_items, HV, HK, L, num_slots, act_bf16;
 };
 
-// Thread t owns key channel t. The ring entries are staged per channel in shared
-// memory (each thread reads back only its own column, so no barrier is needed
-// before the backward pass); the per-entry dot products reduce across the four
-// warps through shared memory.
-__global__ void __launch_bounds__(KD) prepare_kernel(const PreArgs a) {
-    extern __shared__ float psm[];
+// Lane l owns key channels 4l..4l+3. The ring entries are visited from the current
+// one (m = w) down to 0, carrying Gam_m per channel; the partial dot products of up
+// to 16 entries reduce together with one 32-way reduce-scatter (lanes 0..15 end up
+// with k_m . (Gam_m o k_t), lanes 16..31 with k_m . (Gam_m o q_t)).
+__global__ void __launch_bounds__(32 * kPreWarps) prepare_kernel(const PreArgs a) {
+    const int lane = threadIdx.x & 31;
+    const int item = blockIdx.x * kPreWarps + (threadIdx.x >> 5);
+    if (item >= a.n_items) return;
     const int L = a.L;
-    float* sa = psm;                 // [L][KD] gates a_m
-    float* sk = sa + L * KD;         // [L][KD] keys k_m
-    float* red = sk + L * KD;        // [L][4 warps][2]
-    const int item = blockIdx.x;
     const int b = item / a.HV, hv = item - (item / a.HV) * a.HV;
     const int vpk = a.HV / a.HK, kh = hv / vpk;
-    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
     const int s = a.ci[b];
     if (s < 0) return;
     if (s >= a.num_slots) {
-        if (t == 0 && hv == 0) set_dev_err(a.dev_err, RSSM_DEVERR_SLOT);
+        if (lane == 0 && hv == 0) set_dev_err(a.dev_err, RSSM_DEVERR_SLOT);
         return;
     }
     const int w = a.row_wp[b];
     if (w < 0 || w >= L) {
-        if (t == 0 && hv == 0) set_dev_err(a.dev_err, RSSM_DEVERR_CURSOR);
+        if (lane == 0 && hv == 0) set_dev_err(a.dev_err, RSSM_DEVERR_CURSOR);
         return;
     }
     const int f = a.row_flush[b];
     const bool bf = a.act_bf16;
+    const int c4 = lane * 4;
     const float* ra = a.ring_a + ((size_t)s * a.HV + hv) * L * KD;
     const size_t rk = ((size_t)s * a.HK + kh) * L * KD;
-    for (int m = 0; m < w; ++m) {
-        sa[m * KD + t] = ra[(size_t)m * KD + t];
-        sk[m * KD + t] = load1(a.ring_k, (long)(rk + (size_t)m * KD + t), bf);
-    }
-    const float aw = a.a[((size_t)b * a.HV + hv) * KD + t];
-    const float kw = load1(a.k, ((long)b * a.HK + kh) * KD + t, bf);
-    const float qw = load1(a.q, ((long)b * a.HK + kh) * KD + t, bf);
-    sa[w * KD + t] = aw;
-    sk[w * KD + t] = kw;
+    const float4 aw = *reinterpret_cast<const float4*>(a.a + ((size_t)b * a.HV + hv) * KD + c4);
+    const int sa = bf ? 2 : 4;
+    const char* krow = static_cast<const char*>(a.ring_k) + rk * sa;  // this key head's ring
+    float kw[4], qw[4];
+    load4(static_cast<const char*>(a.k) + ((size_t)b * a.HK + kh) * KD * sa, c4, bf, kw);
+    load4(static_cast<const char*>(a.q) + ((size_t)b * a.HK + kh) * KD * sa, c4, bf, qw);
     // ring append (the k entry once per key head)
-    a.ring_a[((size_t)s * a.HV + hv) * L * KD + (size_t)w * KD + t] = aw;
-    if (hv % vpk == 0) store1(a.ring_k, (long)(rk + (size_t)w * KD + t), bf, kw);
+    *reinterpret_cast<float4*>(a.ring_a + ((size_t)s * a.HV + hv) * L * KD + (size_t)w * KD + c4) = aw;
+    if (hv % vpk == 0) {
+        char* kd = static_cast<char*>(a.ring_k) + (rk + (size_t)w * KD + c4) * sa;
+        if (bf) {
+            *reinterpret_cast<uint2*>(kd) =
+                make_uint2(pack_bf16x2(kw[0], kw[1]), pack_bf16x2(kw[2], kw[3]));
+        } else {
+            *reinterpret_cast<float4*>(kd) = make_float4(kw[0], kw[1], kw[2], kw[3]);
+        }
+    }
 
     float* wsm = a.ws + ((size_t)b * a.HV + hv) * main_floats(L);
+    float* tb = wsm + 3 * KD;
     float* kgo = a.ws_kg + ((size_t)b * a.HV + hv) * L * KD;
-    float G = 1.f;  // Gam_m for the entry m being visited (Gam_w = 1)
-    for (int m = w; m >= 0; --m) {
-        const float km = sk[m * KD + t];
-        const float gk = G * km;
-        if (f) kgo[(size_t)m * KD + t] = gk;
-        float pkk = gk * kw, pkq = gk * qw;
+    float G[4] = {1.f, 1.f, 1.f, 1.f};  // Gam_m of the entry being visited
+    // chunks of entries [m0, m0 + 16) from the top: m0 = 16 * floor(w / 16), ..., 0
+    for (int m0 = (w / kChunkM) * kChunkM; m0 >= 0; m0 -= kChunkM) {
+        float part[32];
 #pragma unroll
-        for (int o = 16; o >= 1; o >>= 1) {
-            pkk += __shfl_xor_sync(kFull, pkk, o);
-            pkq += __shfl_xor_sync(kFull, pkq, o);
+        for (int j = 0; j < 32; ++j) part[j] = 0.f;
+#pragma unroll
+        for (int jj = kChunkM - 1; jj >= 0; --jj) {
+            const int m = m0 + jj;
+            if (m <= w) {
+                float km[4], am[4];
+                if (m == w) {
+                    km[0] = kw[0]; km[1] = kw[1]; km[2] = kw[2]; km[3] = kw[3];
+                    am[0] = aw.x; am[1] = aw.y; am[2] = aw.z; am[3] = aw.w;
+                } else {
+                    load4(krow + (size_t)m * KD * sa, c4, bf, km);
+                    const float4 a4 = *reinterpret_cast<const float4*>(ra + (size_t)m * KD + c4);
+                    am[0] = a4.x; am[1] = a4.y; am[2] = a4.z; am[3] = a4.w;
+                }
+                float gk[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) gk[e] = G[e] * km[e];
+                if (f)
+                    *reinterpret_cast<float4*>(kgo + (size_t)m * KD + c4) =
+                        make_float4(gk[0], gk[1], gk[2], gk[3]);
+                part[jj] = gk[0] * kw[0] + gk[1] * kw[1] + gk[2] * kw[2] + gk[3] * kw[3];
+                part[16 + jj] = gk[0] * qw[0] + gk[1] * qw[1] + gk[2] * qw[2] + gk[3] * qw[3];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) G[e] *= am[e];
+            }
         }
-        if (lane == 0) {
-            red[(m * 4 + warp) * 2] = pkk;
-            red[(m * 4 + warp) * 2 + 1] = pkq;
-        }
-        G *= sa[m * KD + t];
+        reduce_scatter<32, 32>(part);  // lane l holds entry l
+        const int m = m0 + (lane & 15);
+        if (m <= w) tb[(lane >> 4) * L + m] = part[0];  // kk_m / kq_m
     }
     // G = Gam_{-1}
-    wsm[t] = G * kw;
-    wsm[KD + t] = G * qw;
-    wsm[2 * KD + t] = G;
-    __syncthreads();
-    float* tb = wsm + 3 * KD;
-    if (t < 2 * (w + 1)) {
-        const int m = t >> 1, kind = t & 1;
-        const float v = red[(m * 4 + 0) * 2 + kind] + red[(m * 4 + 1) * 2 + kind] +
-                        red[(m * 4 + 2) * 2 + kind] + red[(m * 4 + 3) * 2 + kind];
-        tb[kind * L + m] = v;  // kk_m (m < w used) / kq_m
-    }
-    if (t == 0) tb[2 * L] = a.beta[(size_t)b * a.HV + hv];
+    *reinterpret_cast<float4*>(wsm + c4) = make_float4(G[0] * kw[0], G[1] * kw[1], G[2] * kw[2], G[3] * kw[3]);
+    *reinterpret_cast<float4*>(wsm + KD + c4) =
+        make_float4(G[0] * qw[0], G[1] * qw[1], G[2] * qw[2], G[3] * qw[3]);
+    *reinterpret_cast<float4*>(wsm + 2 * KD + c4) = make_float4(G[0], G[1], G[2], G[3]);
+    if (lane == 0) tb[2 * L] = a.beta[(size_t)b * a.HV + hv];
 }
 
 // ----------------------------------------------------------------------------
@@ -439,12 +457,9 @@ extern "C" int rssm_kda_prepare(const rssm_gdn_dims* d, const void* q, const voi
     pa.dev_err = dev_err;
     pa.HV = d->num_v_heads; pa.HK = d->num_k_heads; pa.L = d->ring_len;
     pa.num_slots = d->num_slots; pa.act_bf16 = d->act_dtype == RSSM_BF16;
-    const int smem = (2 * d->ring_len * kda::KD + d->ring_len * 8) * 4;
-    if (smem > 48 * 1024 &&
-        !ensure_smem_limit(reinterpret_cast<const void*>(kda::prepare_kernel), smem))
-        return RSSM_ERR_CUDA;
-    kda::prepare_kernel<<<(unsigned)(d->batch * d->num_v_heads), kda::KD, smem,
-                          (cudaStream_t)stream>>>(pa);
+    pa.n_items = d->batch * d->num_v_heads;
+    const unsigned blocks = (unsigned)((pa.n_items + kda::kPreWarps - 1) / kda::kPreWarps);
+    kda::prepare_kernel<<<blocks, 32 * kda::kPreWarps, 0, (cudaStream_t)stream>>>(pa);
     return launch_status();
 }
 
