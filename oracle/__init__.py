@@ -39,7 +39,8 @@ from . import cursors
 __all__ = ["lib", "round_bf16", "round_f32", "softplus", "mamba2_step", "mamba2_replay",
            "gdn_step", "gdn_replay", "gdn_spec_round", "round_slots", "default_threads",
            "mamba2_run", "gdn_run", "gdn_spec_run", "cursors", "philox4x32_10", "round_bf16_sr",
-           "sr_bits", "round_slots_sr", "kda_step", "kda_replay", "kda_run"]
+           "sr_bits", "round_slots_sr", "kda_step", "kda_replay", "kda_run",
+           "mamba2_spec_round", "mamba2_spec_run"]
 
 _lib = None
 
@@ -89,6 +90,9 @@ def lib():
                                    _dp, ctypes.c_int]
         L.orc_gdn_replay.argtypes = [ctypes.POINTER(_GDims), ctypes.c_int, _dp, _ip, _ip, _dp,
                                      _dp, _dp, _dp, _dp, _dp, _dp, _dp, ctypes.c_int]
+        L.orc_mamba2_spec_round.argtypes = [ctypes.POINTER(_M2Dims), ctypes.c_int, _dp, _dp, _dp,
+                                            _dp, ctypes.c_int, _dp, _dp, _dp, _dp, _dp, _ip, _ip,
+                                            _dp, ctypes.c_int]
         L.orc_kda_step.argtypes = [ctypes.POINTER(_GDims), _dp, _dp, _dp, _dp, _dp, _dp, _ip,
                                    _dp, ctypes.c_int]
         L.orc_kda_replay.argtypes = [ctypes.POINTER(_GDims), ctypes.c_int, _dp, _ip, _ip, _dp,
@@ -259,6 +263,28 @@ def gdn_replay(L, S0, ci, wp, ek, ev, ebeta, eg, q, want_fold=False, want_d=Fals
     return out[0] if len(out) == 1 else tuple(out)
 
 
+def mamba2_spec_round(state, T, x, dt_raw, A, B, C, D, acc, z=None, dt_bias=None,
+                      dt_softplus=True, ci=None, nthreads=0):
+    """One Mamba2 verify round over T drafts (inputs [b,T,...]); keeps the state after
+    acc[b] drafts. Returns per-draft outputs y [b,T,H,P]."""
+    assert state.dtype == np.float64 and state.flags.c_contiguous
+    x = _f64(x)
+    b, T_, H, P = x.shape
+    assert T_ == T
+    N = state.shape[3]
+    G = np.asarray(B).shape[2]
+    ci = _i32(np.arange(b) if ci is None else ci)
+    y = np.zeros((b, T, H, P))
+    d = _M2Dims(b, H, P, N, G, state.shape[0])
+    arrs = [_f64(dt_raw), None if dt_bias is None else _f64(dt_bias), _f64(A), _f64(B), _f64(C),
+            _f64(D), None if z is None else _f64(z), _i32(acc)]
+    _check(lib().orc_mamba2_spec_round(ctypes.byref(d), T, _p(state), _p(x), _p(arrs[0]),
+                                       _p(arrs[1]), int(dt_softplus), _p(arrs[2]), _p(arrs[3]),
+                                       _p(arrs[4]), _p(arrs[5]), _p(arrs[6]), _p(ci), _p(arrs[7]),
+                                       _p(y), nthreads))
+    return y
+
+
 def kda_step(state, q, k, v, beta, a, ci=None, nthreads=0):
     """One KDA step (per-key-channel gate a [b,HV,K]) in place on ``state``
     [slots,HV,V,K]. Returns o [b,HV,V]."""
@@ -413,6 +439,42 @@ def gdn_run(wl, rows: Optional[Sequence[int]] = None, steps: Optional[int] = Non
     return dict(o=os_, row_wp=np.array(wps, dtype=np.int64).reshape(steps, n),
                 row_flush=np.array(fls, dtype=np.int64).reshape(steps, n), ckpt=ckpt,
                 state=state, slot_wp=np.array(slot_wp))
+
+
+def mamba2_spec_run(wl, rows: Optional[Sequence[int]] = None, rounds: Optional[int] = None,
+                    nthreads: int = 0) -> Dict:
+    """Mamba2 speculative verify workload (the gdn_spec_run protocol): the checkpoint
+    is stored, rounded to the state dtype, when a round starts with the slot's flush
+    flag set, which is when the fold writes it. Returns dict: y [rounds][n,T,H,P],
+    ckpt, state, cnt / base / flush [rounds+1][n]."""
+    rows = np.arange(wl.batch) if rows is None else np.asarray(rows)
+    rounds = wl.rounds if rounds is None else rounds
+    n = len(rows)
+    ci_full = wl.cache_indices()
+    prm = wl.params()
+    state = np.ascontiguousarray(
+        np.stack([wl.slot_state(int(ci_full[r])) for r in rows]).astype(np.float64))
+    ckpt = state.copy()
+    cnt, base, flush = [0] * n, [0] * n, [0] * n
+    ci_loc = _local_ci(ci_full, rows)
+    outs, hist = [], []
+    for r in range(rounds):
+        hist.append((list(cnt), list(base), list(flush)))
+        fold = [i for i in range(n) if ci_loc[i] >= 0 and flush[i]]
+        round_slots(state, fold, wl.state_dtype)
+        for s in fold:
+            ckpt[s] = state[s]
+        inp = wl.round_inputs(r)
+        acc = wl.accepted(r)[rows]
+        y = mamba2_spec_round(state, wl.T, inp["x"][rows], inp["dt_raw"][rows], prm["A"],
+                              inp["B"][rows], inp["C"][rows], prm["D"], acc,
+                              None if inp["z"] is None else inp["z"][rows], prm["dt_bias"],
+                              wl.dt_softplus, ci_loc, nthreads)
+        outs.append(y)
+        cursors.spec_commit(cnt, base, flush, ci_loc, acc, wl.L, wl.T)
+    hist.append((list(cnt), list(base), list(flush)))
+    h = np.array(hist, dtype=np.int64)
+    return dict(y=outs, ckpt=ckpt, state=state, cnt=h[:, 0], base=h[:, 1], flush=h[:, 2])
 
 
 def kda_run(wl, rows: Optional[Sequence[int]] = None, steps: Optional[int] = None,

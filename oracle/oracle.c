@@ -368,6 +368,79 @@ int orc_mamba2_replay(const orc_m2_dims* d, int L, const double* S0, const int* 
 }
 
 /* ------------------------------------------------------------------------- */
+/* Mamba2: one speculative verify round                                       */
+/* ------------------------------------------------------------------------- */
+
+typedef struct {
+    const orc_m2_dims* d;
+    int T;
+    double* state;
+    const double *x, *dt_raw, *dt_bias, *A, *B, *C, *D, *z;
+    int dt_softplus;
+    const int *ci, *acc;
+    double* y;
+} m2_spec_ctx;
+
+/* The speculative round of the full ReplaySSM design ("ReplaySSM: cache SSM inputs
+ * for faster Mamba2 standard decode", 关联脉络: PR 47576 covers Mamba2 and GDN,
+ * standard and speculative decode), read the way the GDN spec verify page states
+ * it: draft j's output is the recurrence's output after the committed history and
+ * drafts 0..j (rejected drafts included); the commit keeps the state after the
+ * first acc[b] drafts (acc in 0..T). Inputs per row and draft: x [b][T][H][P],
+ * dt_raw [b][T][H], B, C [b][T][G][N], z [b][T][H][P] or NULL; y receives
+ * [b][T][H][P]. Each head runs on a private copy of its state tile. */
+static void m2_spec_row(const void* vctx, int b) {
+    const m2_spec_ctx* c = (const m2_spec_ctx*)vctx;
+    const orc_m2_dims* d = c->d;
+    const int H = d->nheads, P = d->headdim, N = d->dstate, G = d->ngroups, T = c->T;
+    const int s = c->ci[b];
+    if (s < 0 || s >= d->num_slots) return;
+    const int acc = c->acc[b];
+    const int hpg = H / G;
+    double* S = (double*)malloc(sizeof(double) * (long)P * N);
+    for (int h = 0; h < H; ++h) {
+        const int g = h / hpg;
+        double* Sslot = c->state + (((long)s * H + h) * P) * N;
+        memcpy(S, Sslot, sizeof(double) * (long)P * N);
+        for (int j = 0; j < T; ++j) {
+            const long bj = (long)b * T + j;
+            double dt = c->dt_raw[bj * H + h] + (c->dt_bias ? c->dt_bias[h] : 0.0);
+            if (c->dt_softplus) dt = orc_softplus(dt);
+            const double dA = exp(c->A[h] * dt);
+            const double* Bg = c->B + (bj * G + g) * N;
+            const double* Cg = c->C + (bj * G + g) * N;
+            for (int p = 0; p < P; ++p) {
+                const double xp = c->x[(bj * H + h) * P + p];
+                double a = 0.0;
+                for (int n = 0; n < N; ++n) {
+                    const double v = dA * S[(long)p * N + n] + dt * xp * Bg[n];
+                    S[(long)p * N + n] = v;
+                    a += v * Cg[n];
+                }
+                double yp = a + c->D[h] * xp;
+                if (c->z) yp *= silu(c->z[(bj * H + h) * P + p]);
+                c->y[(bj * H + h) * P + p] = yp;
+            }
+            if (j + 1 == acc) memcpy(Sslot, S, sizeof(double) * (long)P * N);
+        }
+    }
+    free(S);
+}
+
+int orc_mamba2_spec_round(const orc_m2_dims* d, int T, double* state, const double* x,
+                          const double* dt_raw, const double* dt_bias, int dt_softplus,
+                          const double* A, const double* B, const double* C, const double* D,
+                          const double* z, const int* ci, const int* acc, double* y,
+                          int nthreads) {
+    if (d->ngroups <= 0 || d->nheads % d->ngroups) return 3;
+    for (int b = 0; b < d->batch; ++b)
+        if (ci[b] >= 0 && (acc[b] < 0 || acc[b] > T)) return 1;
+    m2_spec_ctx c = {d, T, state, x, dt_raw, dt_bias, A, B, C, D, z, dt_softplus, ci, acc, y};
+    for_rows(m2_spec_row, &c, d->batch, nthreads);
+    return 0;
+}
+
+/* ------------------------------------------------------------------------- */
 /* Gated delta net: full-state recurrence                                    */
 /* ------------------------------------------------------------------------- */
 

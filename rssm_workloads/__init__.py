@@ -29,6 +29,8 @@ state [HV, V, K] with grouped key heads):
                 ~ U{0..4} per row and round.
   kda_decode    gdn_decode's geometry with a per-key-channel gate a [HV, K] per
                 step instead of the scalar g.
+  mamba2_spec   mamba2_large's geometry, batch 128, 256 slots, T 4 drafts per verify
+                round, L 16, accepted drafts ~ U{0..4}.
 """
 from dataclasses import dataclass, field
 from typing import Dict, Optional
@@ -38,7 +40,7 @@ import numpy as np
 __all__ = [
     "round_bf16_f32", "Mamba2Workload", "GDNWorkload", "GDNSpecWorkload",
     "mamba2_tiny", "mamba2_large", "mamba2_sweep", "gdn_decode", "gdn_spec", "kda_decode",
-    "KDAWorkload",
+    "KDAWorkload", "Mamba2SpecWorkload", "mamba2_spec",
 ]
 
 # stream tags
@@ -287,6 +289,35 @@ class GDNSpecWorkload(GDNWorkload):
     def accepted(self, r: int) -> np.ndarray:
         """Accepted draft count per row for round r, U{0..T}."""
         return _rng(self.seed, _T_ACC, r).integers(0, self.T + 1, self.batch).astype(np.int32)
+
+
+@dataclass
+class Mamba2SpecWorkload(Mamba2Workload):
+    """Mamba2 geometry with T draft tokens per verify round; accepted ~ U{0..T}."""
+    T: int = 4
+    rounds: int = 32
+
+    def round_inputs(self, r: int):
+        """Draft inputs of round r: x, z [b,T,H,P]; dt_raw [b,T,H]; B, C [b,T,G,N]."""
+        rng = _rng(self.seed, _T_STEP, r)
+        B_, T, H, P, N, G = self.batch, self.T, self.nheads, self.headdim, self.dstate, self.ngroups
+        x = _to_grid(_normal(rng, (B_, T, H, P)), self.act_dtype)
+        dt_raw = rng.standard_normal((B_, T, H), dtype=np.float32)
+        Bm = _to_grid(_normal(rng, (B_, T, G, N), 1.0 / np.sqrt(N)), self.act_dtype)
+        Cm = _to_grid(_normal(rng, (B_, T, G, N), 1.0 / np.sqrt(N)), self.act_dtype)
+        z = _to_grid(_normal(rng, (B_, T, H, P)), self.act_dtype) if self.with_z else None
+        return dict(x=x, dt_raw=dt_raw, B=Bm, C=Cm, z=z)
+
+    def accepted(self, r: int) -> np.ndarray:
+        return _rng(self.seed, _T_ACC, r).integers(0, self.T + 1, self.batch).astype(np.int32)
+
+
+def mamba2_spec(**kw) -> Mamba2SpecWorkload:
+    d = dict(batch=128, nheads=128, headdim=64, dstate=128, ngroups=8, L=16, num_slots=256,
+             T=4, rounds=32, steps=0, state_dtype="bf16", act_dtype="bf16", state_init="normal",
+             state_std=0.1, ci_mode="perm", wp_mode="zero", name="mamba2_spec")
+    d.update(kw)
+    return Mamba2SpecWorkload(**d)
 
 
 @dataclass

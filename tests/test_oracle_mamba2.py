@@ -263,3 +263,56 @@ def test_driver_history_and_checkpoints():
         assert np.allclose(res["state"][b], st[0], rtol=1e-6, atol=1e-7)
         assert np.allclose(res["ckpt"][b], ck[0], rtol=1e-6, atol=1e-7)
         assert res["slot_wp"][b] == wp
+
+
+# --------------------------------------------------------------------------- #
+# speculative verify round                                                    #
+# --------------------------------------------------------------------------- #
+
+def _spec_inputs(r, b, T, H, P, N, G):
+    return dict(x=r.standard_normal((b, T, H, P)), dt_raw=r.standard_normal((b, T, H)),
+                B=r.standard_normal((b, T, G, N)) / np.sqrt(N),
+                C=r.standard_normal((b, T, G, N)) / np.sqrt(N), z=r.standard_normal((b, T, H, P)))
+
+
+def test_mamba2_spec_round_equals_sequential_steps():
+    # draft j's output = the recurrence after drafts 0..j; the slot keeps the state
+    # after the accepted prefix only
+    r = np.random.default_rng(31)
+    b, T, H, P, N, G, slots = 3, 4, 4, 3, 5, 2, 6
+    A = -np.exp(r.uniform(0, 2, H))
+    D = r.standard_normal(H)
+    dtb = r.uniform(-3, -2, H)
+    S = r.standard_normal((slots, H, P, N))
+    ci = np.array([5, 1, 3], dtype=np.int32)
+    acc = np.array([2, 0, 4], dtype=np.int32)
+    inp = _spec_inputs(r, b, T, H, P, N, G)
+    S_spec = S.copy()
+    y = oracle.mamba2_spec_round(S_spec, T, inp["x"], inp["dt_raw"], A, inp["B"], inp["C"], D, acc,
+                                 inp["z"], dtb, True, ci)
+    for row in range(b):
+        St = S.copy()
+        for j in range(T):
+            sl = slice(row, row + 1)
+            yj = oracle.mamba2_step(St, inp["x"][sl, j], inp["dt_raw"][sl, j], A, inp["B"][sl, j],
+                                    inp["C"][sl, j], D, inp["z"][sl, j], dtb, True, ci=ci[sl])
+            assert np.allclose(y[row, j], yj[0], rtol=0, atol=1e-12)
+            if j + 1 == acc[row]:
+                keep = St[ci[row]].copy()
+        want = S[ci[row]] if acc[row] == 0 else keep
+        assert np.array_equal(S_spec[ci[row]], want)
+
+
+def test_mamba2_spec_run_t1_always_accept_equals_decode():
+    # T = 1 with every draft accepted is plain decode (flush every L - 1 rounds)
+    wl = W.mamba2_spec(batch=3, nheads=4, ngroups=2, num_slots=6, L=4, T=1, rounds=6,
+                       state_dtype="fp32", act_dtype="fp32")
+    wl.accepted = lambda r: np.ones(wl.batch, dtype=np.int32)
+    ref = oracle.mamba2_spec_run(wl)
+    prm = wl.params()
+    S = np.stack([wl.slot_state(int(s)) for s in wl.cache_indices()]).astype(np.float64)
+    for r in range(6):
+        inp = wl.round_inputs(r)
+        y = oracle.mamba2_step(S, inp["x"][:, 0], inp["dt_raw"][:, 0], prm["A"], inp["B"][:, 0],
+                               inp["C"][:, 0], prm["D"], inp["z"][:, 0], prm["dt_bias"], True)
+        assert np.allclose(ref["y"][r][:, 0], y, rtol=0, atol=1e-5)
