@@ -327,6 +327,41 @@ int rssm_mamba2_step_sr(const rssm_mamba2_dims* dims, int advance, const uint8_t
 int rssm_philox4x32_fill(uint64_t seed, uint64_t offset, uint32_t* out, size_t n_groups,
                          rssm_stream_t stream);
 
+/* Bytes of workspace rssm_mamba2_spec_verify needs for T drafts (per-(row, head)
+ * tables: T x L coefficients, T decay products, T draft dt). 0 for invalid dims
+ * or T outside 1..4. */
+size_t rssm_mamba2_spec_workspace_size(const rssm_mamba2_dims* dims, int32_t T);
+
+/* rssm_mamba2_spec_verify -- score T draft tokens per row from the checkpoint and
+ * the circular ring, without per-draft states ([M2] 关联脉络: the full ReplaySSM
+ * design covers Mamba2 speculative decode; the ring, cursors, fold and commit
+ * follow [SPEC] 实现拆解 items 2-4, as for rssm_gdn_spec_verify). Two launches: a
+ * prologue that folds, for slots whose fold is pending (slot_flush), the committed
+ * entries into the checkpoint (S0 <- prod dA_i S0 + sum_i (prod_{l>i} dA_l) dt_i
+ * x_i B_i^T, rounded to state_dtype) and builds the draft tables; then the verify,
+ * which reads each checkpoint tile once for all drafts:
+ *   y_j = (prod_{i<=m} dA_i) S0 C_j + sum_{i<=m} (prod_{l=i+1..m} dA_l) dt_i (B_i . C_j) x_i
+ *         + D x_j,  gated by silu(z_j),  m = history + j,
+ * over the history entries (ring positions (base + i) % L, i < cnt) and drafts
+ * 0..j, and writes draft j's x, dt (after softplus) and B at ring position
+ * (base + cnt + j) % L. Commit with rssm_advance_cursors(RSSM_CURSOR_SPEC_COMMIT).
+ * Cursors (read only here): slot_cnt = cnt, slot_base = base, slot_flush = fold
+ * pending (the ring length must hold twice the drafts).
+ * Inputs per draft: x, z [batch][T][H][P] (z nullable), dt_raw [batch][T][H]
+ * float32, B, C [batch][T][G][N] (act_dtype); A, D, dt_bias as in decode. Ring
+ * layouts as in decode. Output y [batch][T][H][P] (out_dtype).
+ * Errors: RSSM_ERR_UNSUPPORTED for T outside 1..4; RSSM_ERR_CONFIG for L < 2T; a
+ * slot whose cursors break cnt + T <= L (without a pending fold) is skipped and
+ * flagged RSSM_DEVERR_CURSOR. */
+int rssm_mamba2_spec_verify(const rssm_mamba2_dims* dims, int32_t T, void* state, const void* x,
+                            const float* dt_raw, const float* dt_bias, int dt_softplus,
+                            const float* A, const void* B, const void* C, const float* D,
+                            const void* z, void* ring_x, float* ring_dt, void* ring_B,
+                            const int32_t* cache_indices, const int32_t* slot_cnt,
+                            const int32_t* slot_base, const uint8_t* slot_flush, void* workspace,
+                            size_t workspace_bytes, void* y, int32_t* dev_err,
+                            rssm_stream_t stream);
+
 /* Size of the device array rssm_mamba2_decode_noalloc keeps its workspace in. */
 #define RSSM_NOALLOC_WORKSPACE_BYTES (16u << 20)
 

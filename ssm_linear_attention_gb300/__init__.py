@@ -15,7 +15,8 @@ def __getattr__(name):
     # decoder runners import torch; load them lazily
     if name in ("Mamba2ReplayDecoder", "Mamba2FullStateDecoder", "GDNReplayDecoder",
                 "GDNFullStateDecoder", "GDNSpecVerifier", "GDNSpecFullStateVerifier",
-                "KDAReplayDecoder", "KDAFullStateDecoder", "torch_dtype_code"):
+                "KDAReplayDecoder", "KDAFullStateDecoder", "Mamba2SpecVerifier",
+                "torch_dtype_code"):
         from . import decoder
         return getattr(decoder, name)
     raise AttributeError(name)

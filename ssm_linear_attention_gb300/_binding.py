@@ -24,7 +24,8 @@ EXPORTS = (
     "rssm_mamba2_workspace_size", "rssm_mamba2_precompute", "rssm_mamba2_output",
     "rssm_mamba2_decode", "rssm_mamba2_decode_noalloc", "rssm_mamba2_prepare", "rssm_mamba2_step",
     "rssm_mamba2_full_state_update", "rssm_mamba2_output_sr", "rssm_mamba2_step_sr",
-    "rssm_mamba2_full_state_update_sr", "rssm_philox4x32_fill",
+    "rssm_mamba2_full_state_update_sr", "rssm_philox4x32_fill", "rssm_mamba2_spec_workspace_size",
+    "rssm_mamba2_spec_verify",
     "rssm_gdn_ring_append",
     "rssm_gdn_workspace_size", "rssm_gdn_precompute", "rssm_gdn_output", "rssm_gdn_decode",
     "rssm_gdn_prepare", "rssm_gdn_step",
@@ -98,6 +99,10 @@ def _declare(L):
         "rssm_mamba2_full_state_update_sr": (_I, [m2, _VP, _VP, _VP, _VP, _I, _VP, _VP, _VP,
                                                   _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
         "rssm_philox4x32_fill": (_I, [ctypes.c_uint64, ctypes.c_uint64, _VP, _SZ, _VP]),
+        "rssm_mamba2_spec_workspace_size": (_SZ, [m2, _I32]),
+        "rssm_mamba2_spec_verify": (_I, [m2, _I32, _VP, _VP, _VP, _VP, _I, _VP, _VP, _VP, _VP, _VP,
+                                         _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _VP,
+                                         _VP]),
         "rssm_gdn_ring_append": (_I, [gd, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP]),
         "rssm_gdn_workspace_size": (_SZ, [gd]),
         "rssm_gdn_precompute": (_I, [gd, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP,
@@ -447,3 +452,17 @@ def rssm_kda_full_state_decode(dims, state, q, k, v, beta, a, cache_indices, o, 
     _call("rssm_kda_full_state_decode", ctypes.byref(dims), _ptr(state), _ptr(q), _ptr(k),
           _ptr(v), _ptr(beta), _ptr(a), _ptr(cache_indices), _ptr(o), _ptr(dev_err),
           _stream(stream))
+
+
+def rssm_mamba2_spec_workspace_size(dims, T):
+    return lib().rssm_mamba2_spec_workspace_size(ctypes.byref(dims), int(T))
+
+
+def rssm_mamba2_spec_verify(dims, T, state, x, dt_raw, dt_bias, dt_softplus, A, B, C, D, z, ring_x,
+                            ring_dt, ring_B, cache_indices, slot_cnt, slot_base, slot_flush,
+                            workspace, workspace_bytes, y, dev_err=None, stream=None):
+    _call("rssm_mamba2_spec_verify", ctypes.byref(dims), int(T), _ptr(state), _ptr(x),
+          _ptr(dt_raw), _ptr(dt_bias), int(dt_softplus), _ptr(A), _ptr(B), _ptr(C), _ptr(D),
+          _ptr(z), _ptr(ring_x), _ptr(ring_dt), _ptr(ring_B), _ptr(cache_indices), _ptr(slot_cnt),
+          _ptr(slot_base), _ptr(slot_flush), _ptr(workspace), workspace_bytes, _ptr(y),
+          _ptr(dev_err), _stream(stream))

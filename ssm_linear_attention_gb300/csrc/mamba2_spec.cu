@@ -1,0 +1,528 @@
+// mamba2_spec.cu -- speculative verify for Mamba2 on the circular ReplaySSM ring.
+//
+// Pages followed: "ReplaySSM: cache SSM inputs for faster Mamba2 standard decode",
+// 关联脉络 (the full design, PR 47576, covers Mamba2 and GDN with standard and
+// speculative decode); "[GDN] Support ReplaySSM Ring Spec-Verify", 实现拆解 items
+// 2-4 (circular ring with cursors write_pos / cache_base / is_flush, per-draft
+// outputs from checkpoint + ring without per-draft states, a fold of the committed
+// entries into the checkpoint before a round that would overrun the ring, a commit
+// that only moves cursors), read for Mamba2.
+//
+// Cursors per slot: cnt (committed, unfolded entries), base (oldest entry's ring
+// position), flush (fold pending). A round with history c = cnt entries at
+// positions (base + i) % L scores T drafts; draft j's entry goes to position
+// (base + c + j) % L. With m = c + j and entries i = 0..m (history, then drafts),
+// the recurrence h <- dA h + dt x B^T, y = h C + D x unrolls to
+//   y_j = (prod_{i<=m} dA_i) S0 C_j + sum_{i<=m} (prod_{l=i+1..m} dA_l) dt_i (B_i . C_j) x_i
+//         + D x_j,   gated by silu(z_j),
+// so each draft needs its own decay and B.C_j table but S0 is read once for all.
+// A pending fold is the Mamba2 flush over the committed entries:
+//   S0 <- (prod_{i<cnt} dA_i) S0 + sum_{i<cnt} (prod_{l=i+1..cnt-1} dA_l) dt_i x_i B_i^T.
+//
+// Two launches: a prologue whose CTAs either fold one (row, head) tile of a slot
+// with a pending fold or build one row's tables; then the verify (warp-specialised
+// pipeline over (row, head) tiles), which also appends the drafts to the ring.
+// The commit is rssm_advance_cursors(RSSM_CURSOR_SPEC_COMMIT).
+#include "common.cuh"
+#include "internal.h"
+#include "mamba2.cuh"
+#include "pipeline.cuh"
+
+namespace rssm {
+namespace m2spec {
+
+constexpr int kMaxT = 4;
+constexpr int kThreads = 256;  // prologue CTA
+
+// Per-(row, head) table: coef[T][L] (draft j's coefficient of entry i), Pm1[T],
+// the drafts' dt[T], padded to 4 floats.
+__host__ __device__ inline int tbl_floats(int L, int T) { return (T * L + 2 * T + 3) & ~3; }
+
+// Effective history at verify time (count, oldest position); false when the cursors
+// are outside the ring or the drafts would not fit.
+__device__ __forceinline__ bool history(int cnt, int base, int flush, int L, int T, int* c,
+                                        int* base_eff) {
+    if (cnt < 0 || cnt > L || base < 0 || base >= L) return false;
+    *c = flush ? 0 : cnt;
+    *base_eff = flush ? (base + cnt) % L : base;
+    return *c + T <= L;
+}
+
+struct ProArgs {
+    void* state;
+    const float* dt_raw;
+    const float* dt_bias;
+    const float* A;
+    const void* B;
+    const void* C;
+    const void* ring_x;
+    const float* ring_dt;
+    const void* ring_B;
+    const int32_t* ci;
+    const int32_t* slot_cnt;
+    const int32_t* slot_base;
+    const uint8_t* slot_flush;
+    float* ws;
+    int32_t* dev_err;
+    int batch, T, H, P, N, G, L, num_slots, act_bf16, state_bf16, softplus;
+};
+
+__device__ __forceinline__ float ring_dt_at(const ProArgs& a, int s, int h, int pos) {
+    return a.ring_dt[((size_t)s * a.H + h) * a.L + pos];
+}
+
+// Fold role: one (row, head) tile of a slot whose fold is pending. Thread t owns
+// the tile elements t, t + 256, ... (consecutive threads, consecutive dstate).
+__device__ void fold_tile(const ProArgs& a, int b, int h, float* sm) {
+    const int s = a.ci[b];
+    if (s < 0 || s >= a.num_slots || !a.slot_flush[s]) return;
+    const int cnt = a.slot_cnt[s], base = a.slot_base[s], L = a.L;
+    if (cnt < 0 || cnt > L || base < 0 || base >= L || cnt == 0) return;
+    const int P = a.P, N = a.N, g = h / (a.H / a.G);
+    const bool bf = a.act_bf16;
+    const int t = threadIdx.x;
+    float* xs = sm;              // [cnt][P]
+    float* bs = xs + L * P;      // [cnt][N]
+    float* cf = bs + L * N;      // [cnt] a_i, then Pm1
+    for (int e = t; e < cnt * P; e += kThreads) {
+        const int i = e / P, p = e - (e / P) * P;
+        const int pos = (base + i) % L;
+        xs[e] = load1(a.ring_x, (((long)s * a.H + h) * L + pos) * P + p, bf);
+    }
+    for (int e = t; e < cnt * N; e += kThreads) {
+        const int i = e / N, n = e - (e / N) * N;
+        const int pos = (base + i) % L;
+        bs[e] = load1(a.ring_B, (((long)s * a.G + g) * L + pos) * N + n, bf);
+    }
+    if (t == 0) {
+        const float Ah = a.A[h];
+        float cum = 0.f;  // sum of dt over entries after i
+        for (int i = cnt - 1; i >= 0; --i) {
+            const float dti = ring_dt_at(a, s, h, (base + i) % L);
+            cf[i] = expf(Ah * cum) * dti;
+            cum += dti;
+        }
+        cf[cnt] = expf(Ah * cum);
+    }
+    __syncthreads();
+    const float Pm1 = cf[cnt];
+    char* st = static_cast<char*>(a.state) + ((size_t)s * a.H + h) * P * N * (a.state_bf16 ? 2 : 4);
+    for (int e = t; e < P * N; e += kThreads) {
+        const int p = e / N, n = e - (e / N) * N;
+        float acc = Pm1 * load1(st, e, a.state_bf16);
+        for (int i = 0; i < cnt; ++i) acc = fmaf(cf[i] * xs[i * P + p], bs[i * N + n], acc);
+        store1(st, e, a.state_bf16, acc);
+    }
+}
+
+// Table role: one row. bc[g][i][j] = B_i . C_j for the row's entries i (history
+// from the ring, then the drafts' B) and drafts j; then per (head, draft) the
+// decay suffix sums give coef[j][i], Pm1[j], and the drafts' dt.
+__device__ void row_tables(const ProArgs& a, int b, float* sm) {
+    const int s = a.ci[b];
+    if (s < 0) return;
+    if (s >= a.num_slots) {
+        if (threadIdx.x == 0) set_dev_err(a.dev_err, RSSM_DEVERR_SLOT);
+        return;
+    }
+    const int L = a.L, T = a.T, H = a.H, N = a.N, G = a.G;
+    int c, base_eff;
+    if (!history(a.slot_cnt[s], a.slot_base[s], a.slot_flush[s], L, T, &c, &base_eff)) {
+        if (threadIdx.x == 0) set_dev_err(a.dev_err, RSSM_DEVERR_CURSOR);
+        return;
+    }
+    const int ne = c + T;  // entries: history, then drafts
+    const bool bf = a.act_bf16;
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    float* bc = sm;                    // [G][ne][T]
+    float* dts = bc + G * L * kMaxT;   // [H][ne]
+    // B_i . C_j: a warp per (g, i), lanes over dstate
+    for (int gi = warp; gi < G * ne; gi += kThreads / 32) {
+        const int g = gi / ne, i = gi - (gi / ne) * ne;
+        const char* bsrc;
+        if (i < c) {
+            bsrc = static_cast<const char*>(a.ring_B) +
+                   (((size_t)s * G + g) * L + (base_eff + i) % L) * N * (bf ? 2 : 4);
+        } else {
+            bsrc = static_cast<const char*>(a.B) +
+                   (((size_t)b * T + (i - c)) * G + g) * N * (bf ? 2 : 4);
+        }
+        float part[kMaxT];
+#pragma unroll
+        for (int j = 0; j < kMaxT; ++j) part[j] = 0.f;
+        for (int n = lane; n < N; n += 32) {
+            const float bv = load1(bsrc, n, bf);
+#pragma unroll
+            for (int j = 0; j < kMaxT; ++j)
+                if (j < T)
+                    part[j] = fmaf(bv, load1(a.C, (((long)b * T + j) * G + g) * N + n, bf), part[j]);
+        }
+#pragma unroll
+        for (int j = 0; j < kMaxT; ++j) {
+#pragma unroll
+            for (int o = 16; o >= 1; o >>= 1) part[j] += __shfl_xor_sync(kFull, part[j], o);
+        }
+        if (lane == 0)
+            for (int j = 0; j < T; ++j) bc[(g * ne + i) * T + j] = part[j];
+    }
+    for (int e = t; e < H * ne; e += kThreads) {
+        const int h = e / ne, i = e - (e / ne) * ne;
+        float dt;
+        if (i < c) {
+            dt = ring_dt_at(a, s, h, (base_eff + i) % L);
+        } else {
+            dt = a.dt_raw[((size_t)b * T + (i - c)) * H + h] + (a.dt_bias ? a.dt_bias[h] : 0.f);
+            if (a.softplus) dt = softplus_f(dt);
+        }
+        dts[h * ne + i] = dt;
+    }
+    __syncthreads();
+    const int TB = tbl_floats(L, T);
+    const int hpg = H / G;
+    for (int e = t; e < H * T; e += kThreads) {
+        const int h = e / T, j = e - (e / T) * T;
+        const int g = h / hpg, m = c + j;
+        const float Ah = a.A[h];
+        float* tb = a.ws + ((size_t)b * H + h) * TB;
+        float cum = 0.f;
+        for (int i = m; i >= 0; --i) {
+            const float dti = dts[h * ne + i];
+            tb[j * L + i] = expf(Ah * cum) * dti * bc[(g * ne + i) * T + j];
+            cum += dti;
+        }
+        tb[T * L + j] = expf(Ah * cum);
+        tb[T * L + T + j] = dts[h * ne + m];
+    }
+}
+
+__global__ void __launch_bounds__(kThreads) prologue_kernel(const ProArgs a) {
+    extern __shared__ float psm[];
+    const int blk = blockIdx.x;
+    if (blk < a.batch) {
+        row_tables(a, blk, psm);
+    } else {
+        const int it = blk - a.batch;
+        fold_tile(a, it / a.H, it - (it / a.H) * a.H, psm);
+    }
+}
+
+inline int pro_smem_floats(int H, int P, int N, int G, int L) {
+    const int tables = G * L * kMaxT + H * L;
+    const int fold = L * P + L * N + L + 1;
+    return tables > fold ? tables : fold;
+}
+
+// ----------------------------------------------------------------------------
+// verify: one (row, head) tile per item; a consumer group of two warps, each with
+// half of the headdim rows; lane = (row group hr, dstate chunk q) as in the decode
+// output kernel. The T dot products S0 . C_j per row reduce with reduce-scatters.
+// ----------------------------------------------------------------------------
+
+constexpr int kGroupWarps = 2;
+
+template <int P, int N, class ST, int T>
+struct VerPolicy {
+    static constexpr int kGroup = kGroupWarps;
+    static constexpr int SS = ST::bytes;
+    static constexpr int TILE = P * N * SS;
+    static constexpr int PW = P / kGroupWarps;
+    static constexpr int NQ = N / 8;
+    static constexpr int RPI = 32 / NQ;
+    static constexpr int ITER = PW / RPI;
+    static constexpr int NCH = ITER / NQ;
+    static_assert(NCH >= 1 && ITER % NQ == 0, "tile shape");
+    struct Args {
+        const void* state;
+        const void* x;
+        const float* D;
+        const void* z;
+        const void* B;
+        const void* C;
+        void* ring_x;
+        float* ring_dt;
+        void* ring_B;
+        const int32_t* ci;
+        const int32_t* slot_cnt;
+        const int32_t* slot_base;
+        const uint8_t* slot_flush;
+        const float* ws;
+        void* y;
+        int32_t* dev_err;
+        int batch, H, G, L, num_slots, act_bf16, out_bf16;
+        int stages, stage_bytes, stage_off, scratch_off, warp_scratch;
+        int off_xh, off_xd, off_z, off_C, off_tbl;
+    };
+    struct Meta {
+        int valid, s, b, h, c, base_eff;
+    };
+
+    static __device__ int n_items(const Args& a) { return a.batch * a.H; }
+
+    static __device__ int4 prefetch(const Args& a, int item) {
+        const int b = item / a.H;
+        const int s = a.ci[b];
+        int c = 0, be = 0;
+        if (s >= 0 && s < a.num_slots) {
+            if (!history(a.slot_cnt[s], a.slot_base[s], a.slot_flush[s], a.L, T, &c, &be)) c = -1;
+        }
+        return make_int4(s, c, be, b);
+    }
+
+    static __device__ void issue(const Args& a, int item, int4 r, Meta* meta, uint8_t* sb,
+                                 uint64_t* full, uint64_t pol) {
+        const int b = r.w, h = item - r.w * a.H;
+        Meta m{0, r.x, b, h, r.y, r.z};
+        if (r.x >= a.num_slots) {
+            set_dev_err(a.dev_err, RSSM_DEVERR_SLOT);
+        } else if (r.x >= 0) {
+            if (r.y < 0) set_dev_err(a.dev_err, RSSM_DEVERR_CURSOR);
+            else m.valid = 1;
+        }
+        *meta = m;
+        if (!m.valid) {
+            mbar_arrive_plain(full);
+            return;
+        }
+        const int sa = a.act_bf16 ? 2 : 4;
+        const int L = a.L, c = m.c;
+        const int g = h / (a.H / a.G);
+        const int TB = tbl_floats(L, T);
+        const uint32_t xb = P * sa, nb = N * sa;
+        mbar_arrive_expect_tx(full, TILE + (c + T) * xb + (a.z ? T * xb : 0) + T * nb + TB * 4);
+        bulk_g2s_hint(sb, static_cast<const char*>(a.state) + ((size_t)m.s * a.H + h) * TILE, TILE,
+                      full, pol);
+        // history x: ring positions base_eff .. base_eff + c - 1 (at most two runs)
+        const char* xr = static_cast<const char*>(a.ring_x) + ((size_t)m.s * a.H + h) * L * xb;
+        const int run1 = m.base_eff + c <= L ? c : L - m.base_eff;
+        if (run1 > 0) bulk_g2s(sb + a.off_xh, xr + (size_t)m.base_eff * xb, run1 * xb, full);
+        if (c > run1) bulk_g2s(sb + a.off_xh + run1 * xb, xr, (c - run1) * xb, full);
+#pragma unroll
+        for (int j = 0; j < T; ++j) {
+            const size_t bj = (size_t)b * T + j;
+            bulk_g2s(sb + a.off_xd + j * xb, static_cast<const char*>(a.x) + (bj * a.H + h) * xb, xb,
+                     full);
+            if (a.z)
+                bulk_g2s(sb + a.off_z + j * xb, static_cast<const char*>(a.z) + (bj * a.H + h) * xb,
+                         xb, full);
+            bulk_g2s(sb + a.off_C + j * nb, static_cast<const char*>(a.C) + (bj * a.G + g) * nb, nb,
+                     full);
+        }
+        bulk_g2s(sb + a.off_tbl, a.ws + ((size_t)b * a.H + h) * TB, TB * 4, full);
+    }
+
+    static __device__ void consume(const Args& a, int, const Meta& m, const uint8_t* sb, uint8_t*,
+                                   int lane, int wi) {
+        if (!m.valid) return;
+        const bool bf = a.act_bf16;
+        const int sa = bf ? 2 : 4;
+        const int L = a.L, c = m.c;
+        const int q = lane % NQ, hr = lane / NQ;
+        const int row0 = wi * PW + hr;
+        const float* tbl = reinterpret_cast<const float*>(sb + a.off_tbl);
+        const uint8_t* xh = sb + a.off_xh;
+        const uint8_t* xd = sb + a.off_xd;
+        float part[T][ITER];
+        if (ST::bf16 && bf) {
+            uint4 cpk[T];
+#pragma unroll
+            for (int j = 0; j < T; ++j)
+                cpk[j] = *reinterpret_cast<const uint4*>(sb + a.off_C + j * N * 2 + q * 16);
+#pragma unroll
+            for (int t = 0; t < ITER; ++t) {
+                const int p = row0 + RPI * t;
+                const uint4 s8 = *reinterpret_cast<const uint4*>(sb + ((size_t)p * N + q * 8) * SS);
+#pragma unroll
+                for (int j = 0; j < T; ++j) part[j][t] = dot8_bf16(s8, cpk[j], 0.f);
+            }
+        } else {
+            float cv[T][8];
+#pragma unroll
+            for (int j = 0; j < T; ++j) load8(sb + a.off_C + (j * N + q * 8) * sa, bf, cv[j]);
+#pragma unroll
+            for (int t = 0; t < ITER; ++t) {
+                const int p = row0 + RPI * t;
+                float s8[8];
+                load8(sb + ((size_t)p * N + q * 8) * SS, ST::bf16, s8);
+#pragma unroll
+                for (int j = 0; j < T; ++j) {
+                    float acc = s8[0] * cv[j][0];
+#pragma unroll
+                    for (int e = 1; e < 8; ++e) acc = fmaf(s8[e], cv[j][e], acc);
+                    part[j][t] = acc;
+                }
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < T; ++j)
+#pragma unroll
+            for (int ch = 0; ch < NCH; ++ch) reduce_scatter<NQ, NQ>(part[j] + ch * NQ);
+        const float Dh = __ldg(a.D + m.h);
+        const int pos0 = m.base_eff + c;
+#pragma unroll
+        for (int ch = 0; ch < NCH; ++ch) {
+            const int p = row0 + RPI * (ch * NQ + q);
+            float hist[T];
+#pragma unroll
+            for (int j = 0; j < T; ++j) hist[j] = 0.f;
+            for (int i = 0; i < c; ++i) {
+                const float xi = load1(xh, i * P + p, bf);
+#pragma unroll
+                for (int j = 0; j < T; ++j) hist[j] = fmaf(tbl[j * L + i], xi, hist[j]);
+            }
+            float xdv[T];
+#pragma unroll
+            for (int j = 0; j < T; ++j) xdv[j] = load1(xd, j * P + p, bf);
+#pragma unroll
+            for (int j = 0; j < T; ++j) {
+                float acc = fmaf(tbl[T * L + j], part[j][ch * NQ], hist[j]);
+#pragma unroll
+                for (int jj = 0; jj <= j; ++jj) acc = fmaf(tbl[j * L + c + jj], xdv[jj], acc);
+                acc = fmaf(Dh, xdv[j], acc);
+                if (a.z) acc *= silu_f(load1(sb + a.off_z, j * P + p, bf));
+                store1(a.y, (((size_t)m.b * T + j) * a.H + m.h) * P + p, a.out_bf16, acc);
+                // the draft's x into the ring (exact: the value came in this dtype)
+                store1(a.ring_x, (((size_t)m.s * a.H + m.h) * L + (pos0 + j) % L) * P + p, bf,
+                       xdv[j]);
+            }
+        }
+        // the drafts' dt (one lane) and B (first head of each group, warp 0)
+        if (wi == 0 && lane < T)
+            a.ring_dt[((size_t)m.s * a.H + m.h) * L + (pos0 + lane) % L] = tbl[T * L + T + lane];
+        if (wi == 0 && m.h % (a.H / a.G) == 0) {
+            const int g = m.h / (a.H / a.G);
+            for (int e = lane; e < T * N; e += 32) {
+                const int j = e / N, n = e - (e / N) * N;
+                const float v = load1(a.B, (((long)m.b * T + j) * a.G + g) * N + n, bf);
+                store1(a.ring_B, (((long)m.s * a.G + g) * L + (pos0 + j) % L) * N + n, bf, v);
+            }
+        }
+    }
+};
+
+}  // namespace m2spec
+}  // namespace rssm
+
+using namespace rssm;
+
+namespace {
+
+template <int T>
+struct VerLaunch {
+        const rssm_mamba2_dims* d;
+        const void *state, *x, *z, *B, *C;
+        const float *D, *ws;
+        void *ring_x, *ring_B, *y;
+        float* ring_dt;
+        const int32_t *ci, *slot_cnt, *slot_base;
+        const uint8_t* slot_flush;
+        int32_t* dev_err;
+        cudaStream_t st;
+        template <int PP, int NN, class ST>
+        int go() {
+            using Pol = m2spec::VerPolicy<PP, NN, ST, T>;
+            typename Pol::Args va{};
+            va.state = state; va.x = x; va.D = D; va.z = z; va.B = B; va.C = C;
+            va.ring_x = ring_x; va.ring_dt = ring_dt; va.ring_B = ring_B; va.ci = ci;
+            va.slot_cnt = slot_cnt; va.slot_base = slot_base; va.slot_flush = slot_flush;
+            va.ws = ws; va.y = y; va.dev_err = dev_err;
+            va.batch = d->batch; va.H = d->nheads; va.G = d->ngroups; va.L = d->ring_len;
+            va.num_slots = d->num_slots; va.act_bf16 = d->act_dtype == RSSM_BF16;
+            va.out_bf16 = d->out_dtype == RSSM_BF16;
+            const int sa = va.act_bf16 ? 2 : 4;
+            int off = Pol::TILE;
+            va.off_xh = off;  off += (d->ring_len - T) * PP * sa;
+            va.off_xd = off;  off += T * PP * sa;
+            va.off_z = off;   off += T * PP * sa;
+            va.off_C = off;   off += T * NN * sa;
+            va.off_tbl = off; off += m2spec::tbl_floats(d->ring_len, T) * 4;
+            const int stage_bytes = (off + 127) & ~127;
+            return launch_pipe<Pol>(va, stage_bytes, 0, Pol::TILE, (long)d->batch * d->nheads, st);
+        }
+};
+
+template <int T>
+int m2spec_launch(const rssm_mamba2_dims* d, void* state, const void* x, const float* dt_raw,
+                  const float* dt_bias, int dt_softplus, const float* A, const void* B,
+                  const void* C, const float* D, const void* z, void* ring_x, float* ring_dt,
+                  void* ring_B, const int32_t* ci, const int32_t* slot_cnt,
+                  const int32_t* slot_base, const uint8_t* slot_flush, void* workspace, void* y,
+                  int32_t* dev_err, cudaStream_t st) {
+    DeviceInfo di;
+    if (!device_info(&di)) return RSSM_ERR_CUDA;
+    const int H = d->nheads, P = d->headdim, N = d->dstate, G = d->ngroups, L = d->ring_len;
+    // 1. folds of slots with a pending fold, and the tables
+    m2spec::ProArgs pa{};
+    pa.state = state; pa.dt_raw = dt_raw; pa.dt_bias = dt_bias; pa.A = A; pa.B = B; pa.C = C;
+    pa.ring_x = ring_x; pa.ring_dt = ring_dt; pa.ring_B = ring_B; pa.ci = ci;
+    pa.slot_cnt = slot_cnt; pa.slot_base = slot_base; pa.slot_flush = slot_flush;
+    pa.ws = static_cast<float*>(workspace); pa.dev_err = dev_err;
+    pa.batch = d->batch; pa.T = T; pa.H = H; pa.P = P; pa.N = N; pa.G = G; pa.L = L;
+    pa.num_slots = d->num_slots; pa.act_bf16 = d->act_dtype == RSSM_BF16;
+    pa.state_bf16 = d->state_dtype == RSSM_BF16; pa.softplus = dt_softplus != 0;
+    const int psmem = m2spec::pro_smem_floats(H, P, N, G, L) * 4;
+    if (psmem > di.max_smem_optin) return RSSM_ERR_UNSUPPORTED;
+    if (psmem > 48 * 1024 &&
+        !ensure_smem_limit(reinterpret_cast<const void*>(m2spec::prologue_kernel), psmem))
+        return RSSM_ERR_CUDA;
+    const long blocks = (long)d->batch + (long)d->batch * H;
+    m2spec::prologue_kernel<<<(unsigned)blocks, m2spec::kThreads, psmem, st>>>(pa);
+    if (launch_status()) return RSSM_ERR_CUDA;
+
+    // 2. verify (and the drafts' ring entries)
+    VerLaunch<T> g{d, state, x, z, B, C, D, static_cast<const float*>(workspace), ring_x, ring_B, y, ring_dt,
+        ci, slot_cnt, slot_base, slot_flush, dev_err, st};
+    const bool sbf = d->state_dtype == RSSM_BF16;
+#define RSSM_M2S_CASE(PP, NN)                                                 \
+    if (P == PP && N == NN) return sbf ? g.template go<PP, NN, StBF16>()      \
+                                       : g.template go<PP, NN, StF32>();
+    RSSM_M2S_CASE(64, 128)
+    RSSM_M2S_CASE(128, 128)
+    RSSM_M2S_CASE(64, 64)
+    RSSM_M2S_CASE(128, 64)
+#undef RSSM_M2S_CASE
+    return RSSM_ERR_UNSUPPORTED;
+}
+
+}  // namespace
+
+extern "C" size_t rssm_mamba2_spec_workspace_size(const rssm_mamba2_dims* d, int32_t T) {
+    if (m2::check_dims(d) || T < 1 || T > m2spec::kMaxT) return 0;
+    return (size_t)d->batch * d->nheads * m2spec::tbl_floats(d->ring_len, T) * sizeof(float);
+}
+
+extern "C" int rssm_mamba2_spec_verify(const rssm_mamba2_dims* d, int32_t T, void* state,
+                                       const void* x, const float* dt_raw, const float* dt_bias,
+                                       int dt_softplus, const float* A, const void* B,
+                                       const void* C, const float* D, const void* z,
+                                       void* ring_x, float* ring_dt, void* ring_B,
+                                       const int32_t* cache_indices, const int32_t* slot_cnt,
+                                       const int32_t* slot_base, const uint8_t* slot_flush,
+                                       void* workspace, size_t workspace_bytes, void* y,
+                                       int32_t* dev_err, rssm_stream_t stream) {
+    int rc = m2::check_dims(d);
+    if (rc) return rc;
+    if (T < 1 || T > m2spec::kMaxT) return RSSM_ERR_UNSUPPORTED;
+    if (d->ring_len < 2 * T) return RSSM_ERR_CONFIG;
+    if (d->batch == 0) return RSSM_OK;
+    if (!ok_ptr(state) || !ok_ptr(x) || !ok_ptr(dt_raw) || !ok_opt_ptr(dt_bias) || !ok_ptr(A) ||
+        !ok_ptr(B) || !ok_ptr(C) || !ok_ptr(D) || !ok_opt_ptr(z) || !ok_ptr(ring_x) ||
+        !ok_ptr(ring_dt) || !ok_ptr(ring_B) || !ok_ptr(cache_indices) || !ok_ptr(slot_cnt) ||
+        !ok_ptr(slot_base) || !ok_ptr(slot_flush) || !ok_ptr(workspace) || !ok_ptr(y))
+        return RSSM_ERR_INVALID_ARG;
+    if (workspace_bytes < rssm_mamba2_spec_workspace_size(d, T)) return RSSM_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    switch (T) {
+        case 1: return m2spec_launch<1>(d, state, x, dt_raw, dt_bias, dt_softplus, A, B, C, D, z,
+                                        ring_x, ring_dt, ring_B, cache_indices, slot_cnt,
+                                        slot_base, slot_flush, workspace, y, dev_err, st);
+        case 2: return m2spec_launch<2>(d, state, x, dt_raw, dt_bias, dt_softplus, A, B, C, D, z,
+                                        ring_x, ring_dt, ring_B, cache_indices, slot_cnt,
+                                        slot_base, slot_flush, workspace, y, dev_err, st);
+        case 3: return m2spec_launch<3>(d, state, x, dt_raw, dt_bias, dt_softplus, A, B, C, D, z,
+                                        ring_x, ring_dt, ring_B, cache_indices, slot_cnt,
+                                        slot_base, slot_flush, workspace, y, dev_err, st);
+        default: return m2spec_launch<4>(d, state, x, dt_raw, dt_bias, dt_softplus, A, B, C, D, z,
+                                         ring_x, ring_dt, ring_B, cache_indices, slot_cnt,
+                                         slot_base, slot_flush, workspace, y, dev_err, st);
+    }
+}

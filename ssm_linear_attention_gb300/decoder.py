@@ -420,6 +420,70 @@ class KDAFullStateDecoder(GDNFullStateDecoder):
         return o
 
 
+class Mamba2SpecVerifier:
+    """ReplaySSM speculative verify for Mamba2: T draft tokens per row and round on the
+    circular ring (cursors cnt / base / flush per slot), then a commit of the accepted
+    prefix that only moves cursors. Buffers as Mamba2ReplayDecoder plus slot_base and
+    slot_flush; y [max_batch, T, H, P]."""
+
+    def __init__(self, nheads, headdim, dstate, ngroups, ring_len, T, num_slots, max_batch, A, D,
+                 dt_bias=None, dt_softplus=True, state_dtype=torch.bfloat16,
+                 act_dtype=torch.bfloat16, out_dtype=torch.bfloat16, device=None):
+        dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+        self.H, self.P, self.N, self.G, self.L, self.T = (nheads, headdim, dstate, ngroups,
+                                                          ring_len, T)
+        self.num_slots, self.max_batch = num_slots, max_batch
+        self.state_dtype, self.act_dtype, self.out_dtype = state_dtype, act_dtype, out_dtype
+        self.dt_softplus = dt_softplus
+        f32 = dict(device=dev, dtype=torch.float32)
+        self.A = torch.as_tensor(A, **f32).contiguous()
+        self.D = torch.as_tensor(D, **f32).contiguous()
+        self.dt_bias = None if dt_bias is None else torch.as_tensor(dt_bias, **f32).contiguous()
+        self.state = torch.zeros(num_slots, nheads, headdim, dstate, device=dev, dtype=state_dtype)
+        self.ring_x = torch.zeros(num_slots, nheads, ring_len, headdim, device=dev, dtype=act_dtype)
+        self.ring_dt = torch.zeros(num_slots, nheads, ring_len, **f32)
+        self.ring_B = torch.zeros(num_slots, ngroups, ring_len, dstate, device=dev, dtype=act_dtype)
+        self.slot_cnt = torch.zeros(num_slots, device=dev, dtype=torch.int32)
+        self.slot_base = torch.zeros(num_slots, device=dev, dtype=torch.int32)
+        self.slot_flush = torch.zeros(num_slots, device=dev, dtype=torch.uint8)
+        self.dev_err = torch.zeros(4, device=dev, dtype=torch.int32)
+        self.ws_bytes = B.rssm_mamba2_spec_workspace_size(self.dims(max_batch), T)
+        self.workspace = torch.empty(max(self.ws_bytes, 16), device=dev, dtype=torch.uint8)
+        self.y = torch.empty(max_batch, T, nheads, headdim, device=dev, dtype=out_dtype)
+
+    def dims(self, batch):
+        return B.Mamba2Dims(batch, self.H, self.P, self.N, self.G, self.L, self.num_slots,
+                            torch_dtype_code(self.state_dtype), torch_dtype_code(self.act_dtype),
+                            torch_dtype_code(self.out_dtype))
+
+    def verify(self, x, dt_raw, Bm, C, z, cache_indices, y=None, stream=None):
+        """Per-draft outputs y [b, T, H, P] for draft inputs [b, T, ...]."""
+        b = x.shape[0]
+        y = self.y[:b] if y is None else y
+        B.rssm_mamba2_spec_verify(self.dims(b), self.T, self.state, x, dt_raw, self.dt_bias,
+                                  self.dt_softplus, self.A, Bm, C, self.D, z, self.ring_x,
+                                  self.ring_dt, self.ring_B, cache_indices, self.slot_cnt,
+                                  self.slot_base, self.slot_flush, self.workspace, self.ws_bytes,
+                                  y, self.dev_err, stream)
+        return y
+
+    def commit(self, cache_indices, num_accepted, stream=None):
+        B.rssm_advance_cursors(B.RSSM_CURSOR_SPEC_COMMIT, self.slot_cnt, self.slot_base,
+                               self.slot_flush, cache_indices, None, num_accepted,
+                               cache_indices.shape[0], self.num_slots, self.L, self.T, None, None,
+                               self.dev_err, stream)
+
+    def reset_slots(self, slots, stream=None):
+        B.rssm_advance_cursors(B.RSSM_CURSOR_RESET, self.slot_cnt, self.slot_base,
+                               self.slot_flush, slots, None, None, slots.shape[0], self.num_slots,
+                               self.L, self.T, None, None, self.dev_err, stream)
+
+    def copy_slots(self, src, dst, stream=None):
+        B.rssm_copy_slots([self.state, self.ring_x, self.ring_dt, self.ring_B, self.slot_cnt,
+                           self.slot_base, self.slot_flush], src, dst, src.shape[0],
+                          self.num_slots, self.dev_err, stream)
+
+
 class GDNSpecVerifier:
     """ReplaySSM speculative verify for the gated delta net (linear draft chain of T).
 

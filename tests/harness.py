@@ -264,3 +264,39 @@ def run_gpu_kda(wl, steps=None, out_dtype=torch.float32, full_state=False, rows=
         os_.append(o[sel].float().cpu().numpy().astype(np.float64))
     torch.cuda.synchronize()
     return dict(o=os_, row_wp=np.array(wps), row_flush=np.array(fls), dec=dec)
+
+
+# --------------------------------------------------------------------------- #
+# Mamba2 speculative verify                                                   #
+# --------------------------------------------------------------------------- #
+
+def run_gpu_m2spec(wl, rounds=None, out_dtype=torch.float32, rows=None):
+    from ssm_linear_attention_gb300 import Mamba2SpecVerifier
+    rounds = wl.rounds if rounds is None else rounds
+    prm = wl.params()
+    ad = torch_dt(wl.act_dtype)
+    ver = Mamba2SpecVerifier(wl.nheads, wl.headdim, wl.dstate, wl.ngroups, wl.L, wl.T,
+                             wl.num_slots, max(wl.batch, 1), prm["A"], prm["D"], prm["dt_bias"],
+                             wl.dt_softplus, state_dtype=torch_dt(wl.state_dtype), act_dtype=ad,
+                             out_dtype=out_dtype)
+    ci = wl.cache_indices()
+    for s in ci:
+        ver.state[int(s)] = to_dev(wl.slot_state(int(s)), ver.state.dtype)
+    rows = np.arange(wl.batch) if rows is None else np.asarray(rows)
+    sel = torch.as_tensor(rows, device="cuda")
+    ci_d = to_dev(ci, torch.int32)
+    cidx = torch.as_tensor(ci.astype(np.int64), device="cuda")
+    outs, curs = [], []
+    for r in range(rounds):
+        curs.append((ver.slot_cnt[cidx].cpu().numpy(), ver.slot_base[cidx].cpu().numpy(),
+                     ver.slot_flush[cidx].cpu().numpy()))
+        inp = wl.round_inputs(r)
+        y = ver.verify(to_dev(inp["x"], ad), to_dev(inp["dt_raw"], torch.float32),
+                       to_dev(inp["B"], ad), to_dev(inp["C"], ad), to_dev(inp["z"], ad), ci_d)
+        outs.append(y[sel].float().cpu().numpy().astype(np.float64))
+        ver.commit(ci_d, to_dev(wl.accepted(r), torch.int32))
+    curs.append((ver.slot_cnt[cidx].cpu().numpy(), ver.slot_base[cidx].cpu().numpy(),
+                 ver.slot_flush[cidx].cpu().numpy()))
+    torch.cuda.synchronize()
+    c = np.array(curs, dtype=np.int64)
+    return dict(y=outs, cnt=c[:, 0], base=c[:, 1], flush=c[:, 2], ver=ver)

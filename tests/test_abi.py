@@ -130,3 +130,16 @@ def test_copy_slots_validation(lib):
     assert L.rssm_copy_slots(one, 1, FAKE, FAKE + 4, 2, 8, None, None) == INV
     # nothing to copy: valid, launches nothing
     assert L.rssm_copy_slots(one, 1, None, None, 0, 8, None, None) == B.RSSM_OK
+
+
+def test_binding_arity_matches_header(lib):
+    # every ctypes signature has as many arguments as the C declaration
+    import re
+    hdr = open(os.path.join(os.path.dirname(__file__), "..", "include", "rssm.h")).read()
+    decl = {}
+    for m in re.finditer(r"\n[a-z_ 0-9*]+?\b(rssm_\w+)\(([^;]*?)\);", hdr):
+        args = m.group(2).strip()
+        decl[m.group(1)] = 0 if args in ("void", "") else args.count(",") + 1
+    L = ssm.lib()
+    for name in B.EXPORTS:
+        assert len(getattr(L, name).argtypes or []) == decl[name], name

@@ -1,0 +1,81 @@
+"""GPU parity of the Mamba2 speculative verify (rssm_mamba2_spec_verify + the
+SPEC_COMMIT cursor step) against the oracle's round-by-round recurrence: per-draft
+outputs within the state dtype's bar (1e-4 fp32, 2e-3 bf16; harness metric),
+cursors bit-exact, the checkpoints written by the folds within the same bar."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import rssm_workloads as W
+from tests import harness as Hn
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    assert torch.cuda.is_available(), "the gpu tests need a CUDA device"
+    import ssm_linear_attention_gb300 as ssm
+    ssm.lib()
+
+
+def _check(wl, rows=None):
+    rows = np.arange(wl.batch) if rows is None else np.asarray(rows)
+    g = Hn.run_gpu_m2spec(wl, rows=rows)
+    ref = oracle.mamba2_spec_run(wl, rows=rows)
+    tol = Hn.tol_for(wl.state_dtype)
+    for r in range(wl.rounds):
+        e = Hn.err(g["y"][r], ref["y"][r])
+        assert e <= tol, (r, e)
+    assert np.array_equal(g["cnt"][:, rows], ref["cnt"])
+    assert np.array_equal(g["base"][:, rows], ref["base"])
+    assert np.array_equal(g["flush"][:, rows], ref["flush"])
+    # at least one fold happened, so the stored checkpoints were rewritten
+    assert ref["flush"][:-1].any()
+    ci = wl.cache_indices()[rows]
+    st = g["ver"].state[torch.as_tensor(ci.astype(np.int64), device="cuda")].float().cpu().numpy()
+    ok, e, flips = Hn.state_ok(st, ref["ckpt"], wl.state_dtype)
+    assert ok, (e, flips)
+    assert int(g["ver"].dev_err.abs().sum()) == 0
+
+
+@pytest.mark.parametrize("T,L", [(1, 2), (2, 5), (3, 8), (4, 8), (4, 16)])
+@pytest.mark.parametrize("sdt", ["bf16", "fp32"])
+def test_mamba2_spec_matches_oracle(T, L, sdt):
+    wl = W.mamba2_spec(batch=6, nheads=8, ngroups=2, num_slots=12, L=L, T=T, rounds=12,
+                       state_dtype=sdt)
+    _check(wl)
+
+
+def test_mamba2_spec_fp32_activations_and_other_tile():
+    wl = W.mamba2_spec(batch=4, nheads=4, ngroups=2, headdim=128, dstate=64, num_slots=8, L=8,
+                       T=3, rounds=10, state_dtype="fp32", act_dtype="fp32")
+    _check(wl)
+
+
+def test_mamba2_spec_bench_geometry_sampled_rows():
+    wl = W.mamba2_spec(batch=128, num_slots=256, rounds=8)
+    _check(wl, rows=[0, 57, 127])
+
+
+def test_mamba2_spec_padding_and_bad_slot():
+    import ssm_linear_attention_gb300 as ssm
+    from ssm_linear_attention_gb300 import Mamba2SpecVerifier
+    wl = W.mamba2_spec(batch=4, nheads=8, ngroups=2, num_slots=8, L=8, T=2, rounds=1)
+    prm = wl.params()
+    ver = Mamba2SpecVerifier(wl.nheads, wl.headdim, wl.dstate, wl.ngroups, wl.L, wl.T,
+                             wl.num_slots, wl.batch, prm["A"], prm["D"], prm["dt_bias"],
+                             out_dtype=torch.float32)
+    ci = wl.cache_indices().copy()
+    ci[1] = -1
+    ci[2] = wl.num_slots + 1
+    inp = wl.round_inputs(0)
+    bf = torch.bfloat16
+    y = torch.full((wl.batch, wl.T, wl.nheads, wl.headdim), 3.0, device="cuda")
+    ver.verify(Hn.to_dev(inp["x"], bf), Hn.to_dev(inp["dt_raw"], torch.float32),
+               Hn.to_dev(inp["B"], bf), Hn.to_dev(inp["C"], bf), Hn.to_dev(inp["z"], bf),
+               Hn.to_dev(ci, torch.int32), y=y)
+    torch.cuda.synchronize()
+    assert torch.all(y[1] == 3.0) and torch.all(y[2] == 3.0)
+    assert int(ver.dev_err[0].item()) & ssm.RSSM_DEVERR_SLOT
