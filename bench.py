@@ -78,7 +78,7 @@ def parse():
     ap.add_argument("--batch", type=int, default=None)
     ap.add_argument("--num-slots", type=int, default=None)
     ap.add_argument("--workload", default="mamba2",
-                    choices=["mamba2", "gdn", "spec", "kda", "sweep"])
+                    choices=["mamba2", "gdn", "spec", "kda", "m2spec", "sweep"])
     ap.add_argument("--no-gdn", action="store_true",
                     help="mamba2 line only (skip the gdn_decode / gdn_spec sub-objects)")
     ap.add_argument("--sweep-steps", type=int, default=200)
@@ -319,6 +319,17 @@ def spec_round_bytes(wl, hist, fold, out_bytes=2):
     return int(verify.sum()), int(fold["bytes"])
 
 
+def wl_cursor_view(wl):
+    """A stand-in with the fields simulate_spec reads (its GDN fold byte count is not
+    used for Mamba2)."""
+    class V:
+        pass
+    v = V()
+    v.num_v_heads, v.num_k_heads, v.head_k_dim, v.head_v_dim = 1, 1, 1, 1
+    v.act_dtype, v.num_slots = wl.act_dtype, wl.num_slots
+    return v
+
+
 def simulate_spec(wl, ci, accepted_seq, L, T):
     """Per-round (history count, pending fold, fold bytes) for a sequence of
     accepted counts, following the commit rule (a pending fold retires the
@@ -336,11 +347,28 @@ def simulate_spec(wl, ci, accepted_seq, L, T):
         cr = cnt[ci].copy()
         hist = np.where(fl == 1, 0, cr)
         fold_b = int((fl * (2 * HV * V * K * 4 + cr * (HK * K * sa + HV * V * sa + 2 * HV * 4))).sum())
-        out.append((hist, fl, {"bytes": fold_b}))
+        out.append((hist, fl, {"bytes": fold_b, "cnt": cr}))
         base[ci] = np.where(fl == 1, (base[ci] + cr) % L, base[ci])
         cnt[ci] = np.where(fl == 1, 0, cr) + acc
         flush[ci] = (cnt[ci] + T > L).astype(np.int64)
     return out, cnt
+
+
+def m2spec_round_bytes(wl, hist, fl, cr, out_bytes=2):
+    """Algorithmic bytes of one Mamba2 verify round, as (verify, fold) totals over the
+    rows. Verify: checkpoint read, the history x (and, in the prologue, the history B
+    and dt), the drafts' x, z, dt_raw, B, C, y, and the drafts' x, dt, B appended to
+    the ring. Fold (rows with a pending fold): state read and write plus the
+    committed entries' x, dt, B."""
+    H, P, N, G, T = wl.nheads, wl.headdim, wl.dstate, wl.ngroups, wl.T
+    sa = 2 if wl.act_dtype == "bf16" else 4
+    ss = 2 if wl.state_dtype == "bf16" else 4
+    c = hist.astype(np.int64)
+    entry = H * P * sa + 4 * H + G * N * sa
+    verify = (H * P * N * ss + c * entry + T * (2 * H * P * sa + 2 * G * N * sa + 4 * H)
+              + T * H * P * out_bytes + T * entry)
+    fold = fl.astype(np.int64) * (2 * H * P * N * ss + cr.astype(np.int64) * entry)
+    return int(verify.sum()), int(fold.sum())
 
 
 # --------------------------------------------------------------------------- #
@@ -1005,6 +1033,104 @@ def run_kda(args, dist, sub=False):
     }
 
 
+M2SPEC_WORKLOAD = ("mamba2 replayssm spec verify: batch 128, T 4 drafts, H 128, P 64, N 128, G 8, "
+                   "L 16, bf16 state pool 256 slots ~N(0,0.1), accepted ~U{0..4}")
+
+
+def run_m2spec(args, dist, sub=False):
+    """Mamba2 speculative verify rounds (prologue + verify + commit per round)."""
+    import torch
+
+    import rssm_workloads as W
+    import ssm_linear_attention_gb300 as ssm
+
+    dev = _device(dist)
+    ssm.lib()
+    kw = {}
+    if not sub and args.batch:
+        kw["batch"] = args.batch
+    if not sub and args.num_slots:
+        kw["num_slots"] = args.num_slots
+    wl = W.mamba2_spec(seed=shard_seed(args.seed, dist.rank), **kw)
+    prm = wl.params()
+    bf = torch.bfloat16
+    T, L = wl.T, wl.L
+    ci_np = wl.cache_indices()
+    ci = torch.from_numpy(ci_np).to(dev)
+    ver = ssm.Mamba2SpecVerifier(wl.nheads, wl.headdim, wl.dstate, wl.ngroups, L, T, wl.num_slots,
+                                 wl.batch, prm["A"], prm["D"], prm["dt_bias"], state_dtype=bf,
+                                 act_dtype=bf, out_dtype=bf, device=dev)
+    for s in ci_np:
+        ver.state[int(s)] = torch.from_numpy(wl.slot_state(int(s))).to(dev, bf)
+    nsets = min(args.input_sets, 32)
+    sets, accs = [], []
+    for r in range(nsets):
+        inp = wl.round_inputs(r)
+        sets.append([torch.from_numpy(inp[k]).to(dev, bf if k != "dt_raw" else torch.float32)
+                     for k in ("x", "dt_raw", "B", "C", "z")])
+        accs.append(wl.accepted(r))
+    acc_dev = [torch.from_numpy(a).to(dev) for a in accs]
+    torch.cuda.synchronize()
+    K = args.steps
+    G = min(nsets, max(K, 1))
+
+    def round_fn(j):
+        x, dt, Bm, C, z = sets[j]
+
+        def f():
+            ver.verify(x, dt, Bm, C, z, ci)
+            ver.commit(ci, acc_dev[j])
+        return f
+
+    W0 = max(args.warmup, 3)
+    for k in range(W0):
+        round_fn(k % G)()
+    torch.cuda.synchronize()
+    graphs, g_rs, revs = _sampled_graphs([round_fn(j) for j in range(G)],
+                                         [(None, round_fn(j), None) for j in range(G)])
+    for k in range(W0):
+        graphs[(W0 + k) % G].replay()
+    torch.cuda.synchronize()
+    offset = 2 * W0
+    elapsed, per, clocks, ks = _timed_graphs(graphs, g_rs, revs, K, dist, dev, offset=offset,
+                                             clocks=not sub)
+    assert int(ver.dev_err.abs().sum().item()) == 0, "device error flag set during the m2 spec bench"
+    del graphs, g_rs
+    ms_round = elapsed / K
+    seq = [accs[k % G] for k in range(offset + K)]
+    sim, cnt_end = simulate_spec(wl_cursor_view(wl), ci_np, seq, L, T)
+    dev_cnt = ver.slot_cnt.cpu().numpy().astype(np.int64)
+    assert np.array_equal(dev_cnt[ci_np], cnt_end[ci_np]), "spec cursor bookkeeping disagrees"
+    vb, fb = [], []
+    for k in ks:
+        hist, fl, fold = sim[offset + k]
+        v_b, f_b = m2spec_round_bytes(wl, hist, fl, fold["cnt"])
+        vb.append(v_b)
+        fb.append(f_b)
+    round_b = float(np.mean(vb)) + float(np.mean(fb))
+    peak, peak_kind = read_peaks()
+    per_ms = float(np.mean(per))
+    return {
+        "metric": "mamba2 spec verify rows/s and µs/round at batch %d, T %d" % (wl.batch, T),
+        "value": dist.world * wl.batch / (ms_round * 1e-3), "unit": UNIT,
+        "draft_tokens_per_s": dist.world * wl.batch * T / (ms_round * 1e-3),
+        "n_gpus": dist.world, "steps": K, "warmup": W0, "ms_per_step": ms_round,
+        "us_per_round": ms_round * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+        "config": {"workload": M2SPEC_WORKLOAD, "global_batch": dist.world * wl.batch,
+                   "batch_per_gpu": wl.batch, "T": T, "ring_len": L,
+                   "timing": "one CUDA graph per round (prologue, verify, commit)",
+                   "l2": "inputs larger than L2: 268 MB of bf16 checkpoint per round"},
+        "roofline": {"bound": "hbm", "kernel": "mamba2 spec round (prologue + verify + commit)",
+                     "achieved": round_b / (per_ms * 1e-3) / 1e9, "peak": peak, "unit": "GB/s",
+                     "frac": round_b / (per_ms * 1e-3) / 1e9 / peak, "peak_source": peak_kind,
+                     "traffic": None, "algorithmic_bytes_per_round": int(round_b),
+                     "verify_bytes": float(np.mean(vb)), "fold_bytes": float(np.mean(fb))},
+        "gpu_launches": 3 * K,
+        "clocks": clocks,
+    }
+
+
 # --------------------------------------------------------------------------- #
 # gated delta net: speculative verify                                         #
 # --------------------------------------------------------------------------- #
@@ -1317,6 +1443,8 @@ def main():
             line = run_spec(args, dist)
         elif args.workload == "kda":
             line = run_kda(args, dist)
+        elif args.workload == "m2spec":
+            line = run_m2spec(args, dist)
         elif args.workload == "sweep":
             line = run_sweep(args, dist)
         else:
@@ -1325,6 +1453,7 @@ def main():
                 line["gdn_decode"] = run_gdn(args, dist, sub=True)
                 line["gdn_spec"] = run_spec(args, dist, sub=True)
                 line["kda_decode"] = run_kda(args, dist, sub=True)
+                line["mamba2_spec"] = run_m2spec(args, dist, sub=True)
         if dist.rank == 0 and line is not None:
             print(json.dumps(line), flush=True)
     finally:

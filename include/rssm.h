@@ -350,7 +350,7 @@ size_t rssm_mamba2_spec_workspace_size(const rssm_mamba2_dims* dims, int32_t T);
  * Inputs per draft: x, z [batch][T][H][P] (z nullable), dt_raw [batch][T][H]
  * float32, B, C [batch][T][G][N] (act_dtype); A, D, dt_bias as in decode. Ring
  * layouts as in decode. Output y [batch][T][H][P] (out_dtype).
- * Errors: RSSM_ERR_UNSUPPORTED for T outside 1..4; RSSM_ERR_CONFIG for L < 2T; a
+ * Errors: RSSM_ERR_UNSUPPORTED for T outside 1..4 or L > 32; RSSM_ERR_CONFIG for L < 2T; a
  * slot whose cursors break cnt + T <= L (without a pending fold) is skipped and
  * flagged RSSM_DEVERR_CURSOR. */
 int rssm_mamba2_spec_verify(const rssm_mamba2_dims* dims, int32_t T, void* state, const void* x,

@@ -219,32 +219,36 @@ struct OutPolicy {
             constexpr int RC = Sh::ITER < 8 ? Sh::ITER : 8;
 #pragma unroll 1
             for (int t0 = 0; t0 < Sh::ITER; t0 += RC) {
-                float acc[RC][8];
+                // column pairs (2k, 2k+1) accumulate with packed two-wide FMAs
+                float2 acc[RC][4];
 #pragma unroll
                 for (int r = 0; r < RC; ++r) {
                     const int p = row0 + Sh::RPI * (t0 + r);
                     float s8[8];
                     load8(sb + ((size_t)p * N + q * 8) * Sh::SS, ST::bf16, s8);
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) acc[r][j] = Pm1 * s8[j];
+                    for (int k = 0; k < 4; ++k) acc[r][k] = make_float2(Pm1 * s8[2 * k], Pm1 * s8[2 * k + 1]);
                 }
                 for (int i = 0; i <= w; ++i) {
                     float bi[8];
                     load8(br + ((size_t)i * N + q * 8) * sa, bf, bi);
+                    const float2 b2[4] = {make_float2(bi[0], bi[1]), make_float2(bi[2], bi[3]),
+                                          make_float2(bi[4], bi[5]), make_float2(bi[6], bi[7])};
                     const float ai = av[i];
 #pragma unroll
                     for (int r = 0; r < RC; ++r) {
                         const int p = row0 + Sh::RPI * (t0 + r);
                         const float ax = ai * load1(xr, i * P + p, bf);
+                        const float2 ax2 = make_float2(ax, ax);
 #pragma unroll
-                        for (int j = 0; j < 8; ++j) acc[r][j] = fmaf(ax, bi[j], acc[r][j]);
+                        for (int k = 0; k < 4; ++k) acc[r][k] = __ffma2_rn(ax2, b2[k], acc[r][k]);
                     }
                 }
 #pragma unroll
                 for (int r = 0; r < RC; ++r) {
                     const int p = row0 + Sh::RPI * (t0 + r);
-                    store_state8<ST>(static_cast<char*>(a.state), tile_e + (size_t)p * N + q * 8, acc[r],
-                                     gen);
+                    store_state8<ST>(static_cast<char*>(a.state), tile_e + (size_t)p * N + q * 8,
+                                     reinterpret_cast<const float*>(acc[r]), gen);
                 }
             }
         }

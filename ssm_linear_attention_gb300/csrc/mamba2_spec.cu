@@ -71,8 +71,11 @@ __device__ __forceinline__ float ring_dt_at(const ProArgs& a, int s, int h, int 
     return a.ring_dt[((size_t)s * a.H + h) * a.L + pos];
 }
 
-// Fold role: one (row, head) tile of a slot whose fold is pending. Thread t owns
-// the tile elements t, t + 256, ... (consecutive threads, consecutive dstate).
+// Fold role: (row, head) tiles of slots whose fold is pending. A fold CTA owns the
+// items it = f, f + n_fold, ... of the batch * H tiles and skips tiles without a
+// pending fold. Per tile, thread t owns dstate column n = t % N and every
+// (256 / N)-th headdim row: the column's B entries stay in registers, the scaled
+// x entries a_i x_i[p] are staged in shared memory (read as broadcasts).
 __device__ void fold_tile(const ProArgs& a, int b, int h, float* sm) {
     const int s = a.ci[b];
     if (s < 0 || s >= a.num_slots || !a.slot_flush[s]) return;
@@ -81,36 +84,50 @@ __device__ void fold_tile(const ProArgs& a, int b, int h, float* sm) {
     const int P = a.P, N = a.N, g = h / (a.H / a.G);
     const bool bf = a.act_bf16;
     const int t = threadIdx.x;
-    float* xs = sm;              // [cnt][P]
-    float* bs = xs + L * P;      // [cnt][N]
-    float* cf = bs + L * N;      // [cnt] a_i, then Pm1
+    float* ax = sm;              // [cnt][P]: a_i x_i[p]
+    float* cf = ax + L * P;      // [cnt] a_i, then Pm1
+    __syncthreads();             // the previous tile's readers are done with ax / cf
+    if (t < 32) {
+        // a_i = prod_{l>i} dA_l * dt_i from a suffix sum over the committed entries
+        const float Ah = a.A[h];
+        float dti = t < cnt ? ring_dt_at(a, s, h, (base + t) % L) : 0.f;
+        float suf = dti;  // inclusive suffix sum: sum_{l>=t} dt_l
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const float v = __shfl_down_sync(kFull, suf, o);
+            if (t + o < 32) suf += v;
+        }
+        if (t < cnt) cf[t] = expf(Ah * (suf - dti)) * dti;
+        const float total = __shfl_sync(kFull, suf, 0);
+        if (t == 0) cf[cnt] = expf(Ah * total);
+    }
+    __syncthreads();
     for (int e = t; e < cnt * P; e += kThreads) {
         const int i = e / P, p = e - (e / P) * P;
-        const int pos = (base + i) % L;
-        xs[e] = load1(a.ring_x, (((long)s * a.H + h) * L + pos) * P + p, bf);
+        ax[e] = cf[i] * load1(a.ring_x, (((long)s * a.H + h) * L + (base + i) % L) * P + p, bf);
     }
-    for (int e = t; e < cnt * N; e += kThreads) {
-        const int i = e / N, n = e - (e / N) * N;
-        const int pos = (base + i) % L;
-        bs[e] = load1(a.ring_B, (((long)s * a.G + g) * L + pos) * N + n, bf);
-    }
-    if (t == 0) {
-        const float Ah = a.A[h];
-        float cum = 0.f;  // sum of dt over entries after i
-        for (int i = cnt - 1; i >= 0; --i) {
-            const float dti = ring_dt_at(a, s, h, (base + i) % L);
-            cf[i] = expf(Ah * cum) * dti;
-            cum += dti;
-        }
-        cf[cnt] = expf(Ah * cum);
-    }
+    const int n = t % N, p0 = t / N, pst = kThreads / N;
+    float bcol[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+        bcol[i] = i < cnt ? load1(a.ring_B, (((long)s * a.G + g) * L + (base + i) % L) * N + n, bf)
+                          : 0.f;
     __syncthreads();
     const float Pm1 = cf[cnt];
     char* st = static_cast<char*>(a.state) + ((size_t)s * a.H + h) * P * N * (a.state_bf16 ? 2 : 4);
-    for (int e = t; e < P * N; e += kThreads) {
-        const int p = e / N, n = e - (e / N) * N;
+    for (int p = p0; p < P; p += pst) {
+        const int e = p * N + n;
         float acc = Pm1 * load1(st, e, a.state_bf16);
-        for (int i = 0; i < cnt; ++i) acc = fmaf(cf[i] * xs[i * P + p], bs[i * N + n], acc);
+        if (cnt <= 16) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                if (i < cnt) acc = fmaf(ax[i * P + p], bcol[i], acc);
+        } else {
+            for (int i = 0; i < cnt; ++i)
+                acc = fmaf(ax[i * P + p],
+                           load1(a.ring_B, (((long)s * a.G + g) * L + (base + i) % L) * N + n, bf),
+                           acc);
+        }
         store1(st, e, a.state_bf16, acc);
     }
 }
@@ -195,20 +212,44 @@ __device__ void row_tables(const ProArgs& a, int b, float* sm) {
     }
 }
 
-__global__ void __launch_bounds__(kThreads) prologue_kernel(const ProArgs a) {
+// Whether (row, head) tile `it` belongs to a slot with a pending fold.
+__device__ __forceinline__ bool fold_pending(const ProArgs& a, int it) {
+    const int s = a.ci[it / a.H];
+    return s >= 0 && s < a.num_slots && a.slot_flush[s] != 0;
+}
+
+__global__ void __launch_bounds__(kThreads) prologue_kernel(const ProArgs a, int n_fold) {
     extern __shared__ float psm[];
+    __shared__ int list[kThreads];
+    __shared__ int n_list;
     const int blk = blockIdx.x;
     if (blk < a.batch) {
         row_tables(a, blk, psm);
-    } else {
-        const int it = blk - a.batch;
-        fold_tile(a, it / a.H, it - (it / a.H) * a.H, psm);
+        return;
+    }
+    // fold CTA f: its tiles it = f + k * n_fold; the pending ones are found in
+    // parallel (one thread per tile), listed, then folded one after another
+    const int f = blk - a.batch;
+    const int n_tiles = a.batch * a.H;
+    const int n_mine = n_tiles > f ? (n_tiles - f + n_fold - 1) / n_fold : 0;
+    for (int k0 = 0; k0 < n_mine; k0 += kThreads) {
+        if (threadIdx.x == 0) n_list = 0;
+        __syncthreads();
+        const int k = k0 + (int)threadIdx.x;
+        if (k < n_mine && fold_pending(a, f + k * n_fold)) list[atomicAdd(&n_list, 1)] = f + k * n_fold;
+        __syncthreads();
+        const int n = n_list;
+        for (int u = 0; u < n; ++u) {
+            const int it = list[u];
+            fold_tile(a, it / a.H, it - (it / a.H) * a.H, psm);
+        }
+        __syncthreads();
     }
 }
 
 inline int pro_smem_floats(int H, int P, int N, int G, int L) {
     const int tables = G * L * kMaxT + H * L;
-    const int fold = L * P + L * N + L + 1;
+    const int fold = L * P + L + 1;
     return tables > fold ? tables : fold;
 }
 
@@ -464,8 +505,10 @@ int m2spec_launch(const rssm_mamba2_dims* d, void* state, const void* x, const f
     if (psmem > 48 * 1024 &&
         !ensure_smem_limit(reinterpret_cast<const void*>(m2spec::prologue_kernel), psmem))
         return RSSM_ERR_CUDA;
-    const long blocks = (long)d->batch + (long)d->batch * H;
-    m2spec::prologue_kernel<<<(unsigned)blocks, m2spec::kThreads, psmem, st>>>(pa);
+    long n_fold = (long)di.sm_count * 4;  // persistent fold CTAs
+    if (n_fold > (long)d->batch * H) n_fold = (long)d->batch * H;
+    const long blocks = (long)d->batch + n_fold;
+    m2spec::prologue_kernel<<<(unsigned)blocks, m2spec::kThreads, psmem, st>>>(pa, (int)n_fold);
     if (launch_status()) return RSSM_ERR_CUDA;
 
     // 2. verify (and the drafts' ring entries)
@@ -501,7 +544,7 @@ extern "C" int rssm_mamba2_spec_verify(const rssm_mamba2_dims* d, int32_t T, voi
                                        int32_t* dev_err, rssm_stream_t stream) {
     int rc = m2::check_dims(d);
     if (rc) return rc;
-    if (T < 1 || T > m2spec::kMaxT) return RSSM_ERR_UNSUPPORTED;
+    if (T < 1 || T > m2spec::kMaxT || d->ring_len > 32) return RSSM_ERR_UNSUPPORTED;
     if (d->ring_len < 2 * T) return RSSM_ERR_CONFIG;
     if (d->batch == 0) return RSSM_OK;
     if (!ok_ptr(state) || !ok_ptr(x) || !ok_ptr(dt_raw) || !ok_opt_ptr(dt_bias) || !ok_ptr(A) ||
