@@ -72,25 +72,27 @@ __device__ __forceinline__ float ring_dt_at(const ProArgs& a, int s, int h, int 
 }
 
 // Fold role: (row, head) tiles of slots whose fold is pending. A fold CTA owns the
-// items it = f, f + n_fold, ... of the batch * H tiles and skips tiles without a
-// pending fold. Per tile, thread t owns dstate column n = t % N and every
-// (256 / N)-th headdim row: the column's B entries stay in registers, the scaled
-// x entries a_i x_i[p] are staged in shared memory (read as broadcasts).
+// items it = f, f + n_fold, ... of the batch * H tiles (the pending ones are listed
+// by the caller). Per tile the scaled x entries a_i x_i[p] and the B entries are
+// staged in shared memory; thread t owns 4 consecutive dstate columns of every
+// (256 / (N/4))-th headdim row, reads B as 16-byte vectors (consecutive threads,
+// consecutive columns) and the scaled x as broadcasts.
 __device__ void fold_tile(const ProArgs& a, int b, int h, float* sm) {
     const int s = a.ci[b];
     if (s < 0 || s >= a.num_slots || !a.slot_flush[s]) return;
     const int cnt = a.slot_cnt[s], base = a.slot_base[s], L = a.L;
     if (cnt < 0 || cnt > L || base < 0 || base >= L || cnt == 0) return;
     const int P = a.P, N = a.N, g = h / (a.H / a.G);
-    const bool bf = a.act_bf16;
+    const bool bf = a.act_bf16, sbf = a.state_bf16;
     const int t = threadIdx.x;
     float* ax = sm;              // [cnt][P]: a_i x_i[p]
-    float* cf = ax + L * P;      // [cnt] a_i, then Pm1
-    __syncthreads();             // the previous tile's readers are done with ax / cf
+    float* bs = ax + L * P;      // [cnt][N]
+    float* cf = bs + L * N;      // [cnt] a_i, then Pm1
+    __syncthreads();             // the previous tile's readers are done with the buffers
     if (t < 32) {
         // a_i = prod_{l>i} dA_l * dt_i from a suffix sum over the committed entries
         const float Ah = a.A[h];
-        float dti = t < cnt ? ring_dt_at(a, s, h, (base + t) % L) : 0.f;
+        const float dti = t < cnt ? ring_dt_at(a, s, h, (base + t) % L) : 0.f;
         float suf = dti;  // inclusive suffix sum: sum_{l>=t} dt_l
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -101,34 +103,59 @@ __device__ void fold_tile(const ProArgs& a, int b, int h, float* sm) {
         const float total = __shfl_sync(kFull, suf, 0);
         if (t == 0) cf[cnt] = expf(Ah * total);
     }
+    for (int e = t; e < cnt * N; e += kThreads) {
+        const int i = e / N, n = e - (e / N) * N;
+        bs[e] = load1(a.ring_B, (((long)s * a.G + g) * L + (base + i) % L) * N + n, bf);
+    }
     __syncthreads();
     for (int e = t; e < cnt * P; e += kThreads) {
         const int i = e / P, p = e - (e / P) * P;
         ax[e] = cf[i] * load1(a.ring_x, (((long)s * a.H + h) * L + (base + i) % L) * P + p, bf);
     }
-    const int n = t % N, p0 = t / N, pst = kThreads / N;
-    float bcol[16];
-#pragma unroll
-    for (int i = 0; i < 16; ++i)
-        bcol[i] = i < cnt ? load1(a.ring_B, (((long)s * a.G + g) * L + (base + i) % L) * N + n, bf)
-                          : 0.f;
     __syncthreads();
     const float Pm1 = cf[cnt];
-    char* st = static_cast<char*>(a.state) + ((size_t)s * a.H + h) * P * N * (a.state_bf16 ? 2 : 4);
-    for (int p = p0; p < P; p += pst) {
-        const int e = p * N + n;
-        float acc = Pm1 * load1(st, e, a.state_bf16);
-        if (cnt <= 16) {
+    const int ncg = N / 4;                 // column groups of 4
+    const int n0 = (t % ncg) * 4, r0 = t / ncg, rst = kThreads / ncg;
+    char* st = static_cast<char*>(a.state) + ((size_t)s * a.H + h) * P * N * (sbf ? 2 : 4);
+    for (int pb = r0; pb < P; pb += 8 * rst) {  // up to 8 rows of this thread at a time
+        float acc[8][4];
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-                if (i < cnt) acc = fmaf(ax[i * P + p], bcol[i], acc);
-        } else {
-            for (int i = 0; i < cnt; ++i)
-                acc = fmaf(ax[i * P + p],
-                           load1(a.ring_B, (((long)s * a.G + g) * L + (base + i) % L) * N + n, bf),
-                           acc);
+        for (int k = 0; k < 8; ++k) {
+            const int p = pb + k * rst;
+            if (p < P) {
+                float s4[4];
+                load4(st, p * N + n0, sbf, s4);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) acc[k][e] = Pm1 * s4[e];
+            }
         }
-        store1(st, e, a.state_bf16, acc);
+        for (int i = 0; i < cnt; ++i) {
+            const float4 b4 = *reinterpret_cast<const float4*>(bs + i * N + n0);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int p = pb + k * rst;
+                if (p < P) {
+                    const float xv = ax[i * P + p];
+                    acc[k][0] = fmaf(xv, b4.x, acc[k][0]);
+                    acc[k][1] = fmaf(xv, b4.y, acc[k][1]);
+                    acc[k][2] = fmaf(xv, b4.z, acc[k][2]);
+                    acc[k][3] = fmaf(xv, b4.w, acc[k][3]);
+                }
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int p = pb + k * rst;
+            if (p < P) {
+                char* d = st + (size_t)(p * N + n0) * (sbf ? 2 : 4);
+                if (sbf) {
+                    *reinterpret_cast<uint2*>(d) =
+                        make_uint2(pack_bf16x2(acc[k][0], acc[k][1]), pack_bf16x2(acc[k][2], acc[k][3]));
+                } else {
+                    *reinterpret_cast<float4*>(d) = make_float4(acc[k][0], acc[k][1], acc[k][2], acc[k][3]);
+                }
+            }
+        }
     }
 }
 
@@ -249,7 +276,7 @@ __global__ void __launch_bounds__(kThreads) prologue_kernel(const ProArgs a, int
 
 inline int pro_smem_floats(int H, int P, int N, int G, int L) {
     const int tables = G * L * kMaxT + H * L;
-    const int fold = L * P + L + 1;
+    const int fold = L * P + L * N + L + 1;
     return tables > fold ? tables : fold;
 }
 
@@ -291,7 +318,7 @@ struct VerPolicy {
         int32_t* dev_err;
         int batch, H, G, L, num_slots, act_bf16, out_bf16;
         int stages, stage_bytes, stage_off, scratch_off, warp_scratch;
-        int off_xh, off_xd, off_z, off_C, off_tbl;
+        int off_xh, off_xd, off_z, off_C, off_B, off_tbl;
     };
     struct Meta {
         int valid, s, b, h, c, base_eff;
@@ -329,7 +356,9 @@ struct VerPolicy {
         const int g = h / (a.H / a.G);
         const int TB = tbl_floats(L, T);
         const uint32_t xb = P * sa, nb = N * sa;
-        mbar_arrive_expect_tx(full, TILE + (c + T) * xb + (a.z ? T * xb : 0) + T * nb + TB * 4);
+        const bool wb = h % (a.H / a.G) == 0;  // this tile appends the group's drafts' B
+        mbar_arrive_expect_tx(full, TILE + (c + T) * xb + (a.z ? T * xb : 0) + (wb ? 2 : 1) * T * nb +
+                                        TB * 4);
         bulk_g2s_hint(sb, static_cast<const char*>(a.state) + ((size_t)m.s * a.H + h) * TILE, TILE,
                       full, pol);
         // history x: ring positions base_eff .. base_eff + c - 1 (at most two runs)
@@ -347,6 +376,9 @@ struct VerPolicy {
                          xb, full);
             bulk_g2s(sb + a.off_C + j * nb, static_cast<const char*>(a.C) + (bj * a.G + g) * nb, nb,
                      full);
+            if (wb)
+                bulk_g2s(sb + a.off_B + j * nb, static_cast<const char*>(a.B) + (bj * a.G + g) * nb,
+                         nb, full);
         }
         bulk_g2s(sb + a.off_tbl, a.ws + ((size_t)b * a.H + h) * TB, TB * 4, full);
     }
@@ -430,11 +462,15 @@ struct VerPolicy {
         if (wi == 0 && lane < T)
             a.ring_dt[((size_t)m.s * a.H + m.h) * L + (pos0 + lane) % L] = tbl[T * L + T + lane];
         if (wi == 0 && m.h % (a.H / a.G) == 0) {
+            // from the stage, 16 bytes per lane and store
             const int g = m.h / (a.H / a.G);
-            for (int e = lane; e < T * N; e += 32) {
-                const int j = e / N, n = e - (e / N) * N;
-                const float v = load1(a.B, (((long)m.b * T + j) * a.G + g) * N + n, bf);
-                store1(a.ring_B, (((long)m.s * a.G + g) * L + (pos0 + j) % L) * N + n, bf, v);
+            const int cpr = N * sa / 16;  // 16-byte chunks per entry
+            for (int e = lane; e < T * cpr; e += 32) {
+                const int j = e / cpr, c16 = e - (e / cpr) * cpr;
+                const uint4 v = *reinterpret_cast<const uint4*>(sb + a.off_B + (size_t)e * 16);
+                char* dst = static_cast<char*>(a.ring_B) +
+                            (((size_t)m.s * a.G + g) * L + (pos0 + j) % L) * N * sa;
+                reinterpret_cast<uint4*>(dst)[c16] = v;
             }
         }
     }
@@ -475,6 +511,7 @@ struct VerLaunch {
             va.off_xd = off;  off += T * PP * sa;
             va.off_z = off;   off += T * PP * sa;
             va.off_C = off;   off += T * NN * sa;
+            va.off_B = off;   off += T * NN * sa;
             va.off_tbl = off; off += m2spec::tbl_floats(d->ring_len, T) * 4;
             const int stage_bytes = (off + 127) & ~127;
             return launch_pipe<Pol>(va, stage_bytes, 0, Pol::TILE, (long)d->batch * d->nheads, st);
