@@ -117,10 +117,11 @@ __device__ void fold_tile(const ProArgs& a, int b, int h, float* sm) {
     const int ncg = N / 4;                 // column groups of 4
     const int n0 = (t % ncg) * 4, r0 = t / ncg, rst = kThreads / ncg;
     char* st = static_cast<char*>(a.state) + ((size_t)s * a.H + h) * P * N * (sbf ? 2 : 4);
-    for (int pb = r0; pb < P; pb += 8 * rst) {  // up to 8 rows of this thread at a time
-        float acc[8][4];
+    constexpr int RB = 4;  // rows of this thread per pass (keeps the CTA's registers low)
+    for (int pb = r0; pb < P; pb += RB * rst) {
+        float acc[RB][4];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
+        for (int k = 0; k < RB; ++k) {
             const int p = pb + k * rst;
             if (p < P) {
                 float s4[4];
@@ -132,7 +133,7 @@ __device__ void fold_tile(const ProArgs& a, int b, int h, float* sm) {
         for (int i = 0; i < cnt; ++i) {
             const float4 b4 = *reinterpret_cast<const float4*>(bs + i * N + n0);
 #pragma unroll
-            for (int k = 0; k < 8; ++k) {
+            for (int k = 0; k < RB; ++k) {
                 const int p = pb + k * rst;
                 if (p < P) {
                     const float xv = ax[i * P + p];
@@ -144,7 +145,7 @@ __device__ void fold_tile(const ProArgs& a, int b, int h, float* sm) {
             }
         }
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
+        for (int k = 0; k < RB; ++k) {
             const int p = pb + k * rst;
             if (p < P) {
                 char* d = st + (size_t)(p * N + n0) * (sbf ? 2 : 4);
@@ -245,7 +246,7 @@ __device__ __forceinline__ bool fold_pending(const ProArgs& a, int it) {
     return s >= 0 && s < a.num_slots && a.slot_flush[s] != 0;
 }
 
-__global__ void __launch_bounds__(kThreads) prologue_kernel(const ProArgs a, int n_fold) {
+__global__ void __launch_bounds__(kThreads, 6) prologue_kernel(const ProArgs a, int n_fold) {
     extern __shared__ float psm[];
     __shared__ int list[kThreads];
     __shared__ int n_list;
@@ -542,7 +543,7 @@ int m2spec_launch(const rssm_mamba2_dims* d, void* state, const void* x, const f
     if (psmem > 48 * 1024 &&
         !ensure_smem_limit(reinterpret_cast<const void*>(m2spec::prologue_kernel), psmem))
         return RSSM_ERR_CUDA;
-    long n_fold = (long)di.sm_count * 4;  // persistent fold CTAs
+    long n_fold = (long)di.sm_count * 6;  // persistent fold CTAs (6 resident per SM)
     if (n_fold > (long)d->batch * H) n_fold = (long)d->batch * H;
     const long blocks = (long)d->batch + n_fold;
     m2spec::prologue_kernel<<<(unsigned)blocks, m2spec::kThreads, psmem, st>>>(pa, (int)n_fold);
