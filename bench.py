@@ -1124,7 +1124,8 @@ def run_m2spec(args, dist, sub=False):
         "roofline": {"bound": "hbm", "kernel": "mamba2 spec round (prologue + verify + commit)",
                      "achieved": round_b / (per_ms * 1e-3) / 1e9, "peak": peak, "unit": "GB/s",
                      "frac": round_b / (per_ms * 1e-3) / 1e9 / peak, "peak_source": peak_kind,
-                     "traffic": None, "algorithmic_bytes_per_round": int(round_b),
+                     "traffic": traffic_record("mamba2_spec.cu", "mamba2_spec_verify_batch128_T4.md"),
+                     "algorithmic_bytes_per_round": int(round_b),
                      "verify_bytes": float(np.mean(vb)), "fold_bytes": float(np.mean(fb))},
         "gpu_launches": 3 * K,
         "clocks": clocks,
