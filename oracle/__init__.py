@@ -8,9 +8,12 @@ draws the seeded inputs and holds none of the method's arithmetic.
 
 Contents:
   * ``oracle.c`` (built into ``liborc.so`` by ``build.py``): the full-state
-    recurrences for Mamba2 and the gated delta rule, the ReplaySSM closed forms
-    (checkpoint + ring) of both, one speculative verify round, and the storage
-    rounding helpers. Every function cites the page passage it follows.
+    recurrences for Mamba2, the gated delta rule and its per-key-channel-gate
+    (KDA) form, the ReplaySSM closed forms (checkpoint + ring) of all three, one
+    speculative verify round for Mamba2 and for the gated delta rule, the storage
+    rounding helpers, and Philox4x32-10 with the stochastic rounding to bf16.
+    Every function cites the page passage (or the published definition) it
+    follows.
   * ``cursors.py``: the integer cursor model (write_pos / is_flush, the circular
     spec ring).
   * The drivers below run a whole workload (history steps, then the measured
@@ -25,7 +28,8 @@ Contents:
 
 Parity pins: every function here is checked in ``tests/test_oracle_*.py``
 against closed forms, library routines (scipy.signal.lfilter, numpy matrix
-algebra, torch's bfloat16 conversion), hand-worked examples and invariants.
+algebra, torch's bfloat16 conversion), hand-worked examples, invariants and
+published known-answer vectors (Philox4x32-10, ``tests/golden/``).
 """
 import ctypes
 import os
