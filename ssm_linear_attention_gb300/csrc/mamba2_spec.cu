@@ -71,10 +71,9 @@ __device__ __forceinline__ float ring_dt_at(const ProArgs& a, int s, int h, int 
     return a.ring_dt[((size_t)s * a.H + h) * a.L + pos];
 }
 
-// Fold role: (row, head) tiles of slots whose fold is pending. A fold CTA owns the
-// items it = f, f + n_fold, ... of the batch * H tiles (the pending ones are listed
-// by the caller). Per tile the scaled x entries a_i x_i[p] and the B entries are
-// staged in shared memory; thread t owns 4 consecutive dstate columns of every
+// Fold role: one (row, head) tile of a slot whose fold is pending. The scaled x
+// entries a_i x_i[p] and the B entries are staged in shared memory; thread t owns
+// 4 consecutive dstate columns of every
 // (256 / (N/4))-th headdim row, reads B as 16-byte vectors (consecutive threads,
 // consecutive columns) and the scaled x as broadcasts.
 __device__ void fold_tile(const ProArgs& a, int b, int h, float* sm) {
@@ -240,39 +239,18 @@ __device__ void row_tables(const ProArgs& a, int b, float* sm) {
     }
 }
 
-// Whether (row, head) tile `it` belongs to a slot with a pending fold.
-__device__ __forceinline__ bool fold_pending(const ProArgs& a, int it) {
-    const int s = a.ci[it / a.H];
-    return s >= 0 && s < a.num_slots && a.slot_flush[s] != 0;
-}
-
-__global__ void __launch_bounds__(kThreads, 6) prologue_kernel(const ProArgs a, int n_fold) {
+// Grid: the table CTAs (one per row), then one fold CTA per (row, head) tile; a
+// fold CTA whose slot has no pending fold exits at once, and the block scheduler
+// balances the pending tiles over the SMs.
+__global__ void __launch_bounds__(kThreads, 6) prologue_kernel(const ProArgs a) {
     extern __shared__ float psm[];
-    __shared__ int list[kThreads];
-    __shared__ int n_list;
     const int blk = blockIdx.x;
     if (blk < a.batch) {
         row_tables(a, blk, psm);
         return;
     }
-    // fold CTA f: its tiles it = f + k * n_fold; the pending ones are found in
-    // parallel (one thread per tile), listed, then folded one after another
-    const int f = blk - a.batch;
-    const int n_tiles = a.batch * a.H;
-    const int n_mine = n_tiles > f ? (n_tiles - f + n_fold - 1) / n_fold : 0;
-    for (int k0 = 0; k0 < n_mine; k0 += kThreads) {
-        if (threadIdx.x == 0) n_list = 0;
-        __syncthreads();
-        const int k = k0 + (int)threadIdx.x;
-        if (k < n_mine && fold_pending(a, f + k * n_fold)) list[atomicAdd(&n_list, 1)] = f + k * n_fold;
-        __syncthreads();
-        const int n = n_list;
-        for (int u = 0; u < n; ++u) {
-            const int it = list[u];
-            fold_tile(a, it / a.H, it - (it / a.H) * a.H, psm);
-        }
-        __syncthreads();
-    }
+    const int it = blk - a.batch;
+    fold_tile(a, it / a.H, it - (it / a.H) * a.H, psm);
 }
 
 inline int pro_smem_floats(int H, int P, int N, int G, int L) {
@@ -543,10 +521,8 @@ int m2spec_launch(const rssm_mamba2_dims* d, void* state, const void* x, const f
     if (psmem > 48 * 1024 &&
         !ensure_smem_limit(reinterpret_cast<const void*>(m2spec::prologue_kernel), psmem))
         return RSSM_ERR_CUDA;
-    long n_fold = (long)di.sm_count * 6;  // persistent fold CTAs (6 resident per SM)
-    if (n_fold > (long)d->batch * H) n_fold = (long)d->batch * H;
-    const long blocks = (long)d->batch + n_fold;
-    m2spec::prologue_kernel<<<(unsigned)blocks, m2spec::kThreads, psmem, st>>>(pa, (int)n_fold);
+    const long blocks = (long)d->batch + (long)d->batch * H;
+    m2spec::prologue_kernel<<<(unsigned)blocks, m2spec::kThreads, psmem, st>>>(pa);
     if (launch_status()) return RSSM_ERR_CUDA;
 
     // 2. verify (and the drafts' ring entries)
