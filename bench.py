@@ -304,50 +304,34 @@ def kda_full_bytes(wl, batch, out_bytes=2):
                     + HV * V * out_bytes)
 
 
-def spec_round_bytes(wl, hist, fold, out_bytes=2):
-    """Algorithmic bytes of one verify round (fold + verify) per row, given the
-    history count and pending-fold flag of each row, as (verify, fold) totals.
-    Verify: checkpoint read, the drafts' q, k, v, beta, g, the history d entries,
-    the drafts' d, raw v, k, g, beta written to the rings, o. Fold: state read and
-    write plus the committed entries' k, raw v, beta, g."""
+def spec_round_bytes(wl, hist, out_bytes=2):
+    """Algorithmic bytes of one GDN verify launch over the rows, given each row's
+    history count: checkpoint read, the drafts' q, k, v, beta, g, the history d
+    entries, the drafts' d, raw v, k, g, beta written to the rings, o (the folds are
+    counted by gdn_fold_bytes)."""
     HV, HK, K, V, T = wl.num_v_heads, wl.num_k_heads, wl.head_k_dim, wl.head_v_dim, wl.T
     sa = 2 if wl.act_dtype == "bf16" else 4
     c = hist.astype(np.int64)
     verify = (HV * V * K * 4 + T * (2 * HK * K * sa + HV * V * sa + 2 * HV * 4)
               + c * HV * V * 4 + T * (HV * V * 4 + HV * V * sa + HK * K * sa + 2 * HV * 4)
               + T * HV * V * out_bytes)
-    return int(verify.sum()), int(fold["bytes"])
+    return int(verify.sum())
 
 
-def wl_cursor_view(wl):
-    """A stand-in with the fields simulate_spec reads (its GDN fold byte count is not
-    used for Mamba2)."""
-    class V:
-        pass
-    v = V()
-    v.num_v_heads, v.num_k_heads, v.head_k_dim, v.head_v_dim = 1, 1, 1, 1
-    v.act_dtype, v.num_slots = wl.act_dtype, wl.num_slots
-    return v
-
-
-def simulate_spec(wl, ci, accepted_seq, L, T):
-    """Per-round (history count, pending fold, fold bytes) for a sequence of
-    accepted counts, following the commit rule (a pending fold retires the
-    committed run, then cnt += accepted and flush = cnt + T > L). Bookkeeping for
-    the byte count; the kernels keep their own cursors on the device."""
-    HV, HK, K, V = wl.num_v_heads, wl.num_k_heads, wl.head_k_dim, wl.head_v_dim
-    sa = 2 if wl.act_dtype == "bf16" else 4
-    n = wl.num_slots
-    cnt = np.zeros(n, np.int64)
-    base = np.zeros(n, np.int64)
-    flush = np.zeros(n, np.int64)
+def spec_cursor_rounds(num_slots, ci, accepted_seq, L, T):
+    """Per round (history count, pending fold flag, committed count) of the rows, for a
+    sequence of accepted counts, following the commit rule (a pending fold retires
+    the committed run, then cnt += accepted and flush = cnt + T > L); and the final
+    cnt of every slot. Bookkeeping for the byte counts; the kernels keep their own
+    cursors on the device."""
+    cnt = np.zeros(num_slots, np.int64)
+    base = np.zeros(num_slots, np.int64)
+    flush = np.zeros(num_slots, np.int64)
     out = []
     for acc in accepted_seq:
         fl = flush[ci].copy()
         cr = cnt[ci].copy()
-        hist = np.where(fl == 1, 0, cr)
-        fold_b = int((fl * (2 * HV * V * K * 4 + cr * (HK * K * sa + HV * V * sa + 2 * HV * 4))).sum())
-        out.append((hist, fl, {"bytes": fold_b, "cnt": cr}))
+        out.append((np.where(fl == 1, 0, cr), fl, cr))
         base[ci] = np.where(fl == 1, (base[ci] + cr) % L, base[ci])
         cnt[ci] = np.where(fl == 1, 0, cr) + acc
         flush[ci] = (cnt[ci] + T > L).astype(np.int64)
@@ -369,6 +353,14 @@ def m2spec_round_bytes(wl, hist, fl, cr, out_bytes=2):
               + T * H * P * out_bytes + T * entry)
     fold = fl.astype(np.int64) * (2 * H * P * N * ss + cr.astype(np.int64) * entry)
     return int(verify.sum()), int(fold.sum())
+
+
+def gdn_fold_bytes(wl, fl, cr):
+    """Algorithmic bytes of the GDN exact folds of one round: state read and write plus
+    the committed entries' k, raw v, beta and g, for the rows with a pending fold."""
+    HV, HK, K, V = wl.num_v_heads, wl.num_k_heads, wl.head_k_dim, wl.head_v_dim
+    sa = 2 if wl.act_dtype == "bf16" else 4
+    return int((fl * (2 * HV * V * K * 4 + cr * (HK * K * sa + HV * V * sa + 2 * HV * 4))).sum())
 
 
 # --------------------------------------------------------------------------- #
@@ -1098,13 +1090,13 @@ def run_m2spec(args, dist, sub=False):
     del graphs, g_rs
     ms_round = elapsed / K
     seq = [accs[k % G] for k in range(offset + K)]
-    sim, cnt_end = simulate_spec(wl_cursor_view(wl), ci_np, seq, L, T)
+    sim, cnt_end = spec_cursor_rounds(wl.num_slots, ci_np, seq, L, T)
     dev_cnt = ver.slot_cnt.cpu().numpy().astype(np.int64)
     assert np.array_equal(dev_cnt[ci_np], cnt_end[ci_np]), "spec cursor bookkeeping disagrees"
     vb, fb = [], []
     for k in ks:
-        hist, fl, fold = sim[offset + k]
-        v_b, f_b = m2spec_round_bytes(wl, hist, fl, fold["cnt"])
+        hist, fl, cr = sim[offset + k]
+        v_b, f_b = m2spec_round_bytes(wl, hist, fl, cr)
         vb.append(v_b)
         fb.append(f_b)
     round_b = float(np.mean(vb)) + float(np.mean(fb))
@@ -1199,14 +1191,13 @@ def run_spec(args, dist, sub=False):
     ms_round = elapsed / K
     # byte count from the cursor sequence of all rounds run so far
     seq = [accs[k % G] for k in range(offset + K)]
-    sim, cnt_end = simulate_spec(wl, ci_np, seq, L, T)
+    sim, cnt_end = spec_cursor_rounds(wl.num_slots, ci_np, seq, L, T)
     dev_cnt = ver.slot_cnt.cpu().numpy().astype(np.int64)
     assert np.array_equal(dev_cnt[ci_np], cnt_end[ci_np]), "spec cursor bookkeeping disagrees"
     vb, fb = [], []
-    for hist, fl, fold in [sim[offset + k] for k in ks]:  # the rounds whose duration was sampled
-        v_b, f_b = spec_round_bytes(wl, hist, fold)
-        vb.append(v_b)
-        fb.append(f_b)
+    for hist, fl, cr in [sim[offset + k] for k in ks]:  # the rounds whose duration was sampled
+        vb.append(spec_round_bytes(wl, hist))
+        fb.append(gdn_fold_bytes(wl, fl, cr))
     round_b = float(np.mean(vb)) + float(np.mean(fb))
     peak, peak_kind = read_peaks()
     per_ms = float(np.mean(per))
