@@ -13,13 +13,16 @@
  *          (precompute + output kernels, ring append, per-row write_pos/is_flush
  *          from the metadata builder), 关键源码片段 (the kernel call with
  *          ssm_state, x, dt, A, B, C, D, x_cache, dt_cache, B_cache, write_pos,
- *          is_flush, state_batch_indices, out, dt_bias, dt_softplus).
+ *          is_flush, state_batch_indices, out, dt_bias, dt_softplus), 评论区精华
+ *          (stochastic rounding of the state), 关联脉络 (the full design also
+ *          covers speculative decode).
  *   [FI]   "[Mamba] Add FlashInfer ReplaySSM backend" (vLLM PR 52506 report):
  *          实现拆解 items 1-2 (ring cursor update/reset kernels; one cursor
  *          advance shared by all layers of a cache group).
  *   [GDN]  "GDN ReplaySSM decode (Part A of RFC 28511)" (SGLang PR 28451 report):
  *          实现拆解 items 1-3 (decode kernel over the (d, k, g) ring, flush every L
- *          steps, CUDA-graph-safe write_pos and force-flush buffers).
+ *          steps, CUDA-graph-safe write_pos and force-flush buffers; the KDA
+ *          per-K gate; copy_from with the rings), 评论区精华 (KDA gate ring).
  *   [SPEC] "[GDN] Support ReplaySSM Ring Spec-Verify" (SGLang PR 28695 report):
  *          实现拆解 items 2-4 (circular ring, cursors write_pos / cache_base /
  *          is_flush, spec verify kernel, exact fold from raw inputs, commit that
