@@ -143,3 +143,60 @@ def test_binding_arity_matches_header(lib):
     L = ssm.lib()
     for name in B.EXPORTS:
         assert len(getattr(L, name).argtypes or []) == decl[name], name
+
+
+def _gdims(**kw):
+    d = dict(batch=4, num_v_heads=8, num_k_heads=4, head_k_dim=128, head_v_dim=128, ring_len=8,
+             num_slots=8, act_dtype=B.RSSM_BF16, out_dtype=B.RSSM_F32)
+    d.update(kw)
+    return B.GDNDims(**d)
+
+
+def test_mamba2_spec_validation(lib):
+    by = ctypes.byref
+    d = _m2(ring_len=8)
+    assert B.rssm_mamba2_spec_workspace_size(d, 0) == 0
+    assert B.rssm_mamba2_spec_workspace_size(d, 5) == 0
+    assert B.rssm_mamba2_spec_workspace_size(d, 3) == 4 * 8 * ((3 * 8 + 6 + 3) // 4 * 4) * 4
+
+    def call(dd, T, state=FAKE, ws_bytes=1 << 20):
+        return _rc("rssm_mamba2_spec_verify", by(dd), T, state, FAKE, FAKE, None, 1, FAKE, FAKE,
+                   FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, ws_bytes, FAKE,
+                   None, None)
+    assert call(d, 5) == B.RSSM_ERR_UNSUPPORTED          # T > 4
+    assert call(_m2(ring_len=40), 2) == B.RSSM_ERR_UNSUPPORTED   # L > 32
+    assert call(_m2(ring_len=5), 3) == B.RSSM_ERR_CONFIG          # L < 2T
+    assert call(d, 2, state=None) == B.RSSM_ERR_INVALID_ARG
+    assert call(d, 2, ws_bytes=16) == B.RSSM_ERR_INVALID_ARG       # workspace too small
+    assert call(_m2(ring_len=8, batch=0), 2) == B.RSSM_OK          # nothing to do
+
+
+def test_kda_validation(lib):
+    by = ctypes.byref
+    assert B.rssm_kda_workspace_size(_gdims()) > 0
+    assert B.rssm_kda_workspace_size(_gdims(head_k_dim=64)) == 0
+    assert B.rssm_kda_workspace_size(_gdims(ring_len=65)) == 0
+    out = lambda dd, st=FAKE: _rc("rssm_kda_output", by(dd), st, FAKE, FAKE, FAKE, FAKE, FAKE,
+                                  FAKE, 1 << 30, FAKE, None, None)
+    assert out(_gdims(), st=None) == B.RSSM_ERR_INVALID_ARG
+    assert out(_gdims(num_k_heads=3)) == B.RSSM_ERR_CONFIG
+    assert out(_gdims(head_v_dim=48)) == B.RSSM_ERR_UNSUPPORTED
+    pre = _rc("rssm_kda_prepare", by(_gdims()), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE,
+              FAKE, FAKE, 16, None, None)
+    assert pre == B.RSSM_ERR_INVALID_ARG                            # workspace too small
+    full = _rc("rssm_kda_full_state_decode", by(_gdims()), FAKE, FAKE, FAKE, FAKE, FAKE, None,
+               FAKE, FAKE, None, None)
+    assert full == B.RSSM_ERR_INVALID_ARG                           # gates missing
+
+
+def test_stochastic_rounding_validation(lib):
+    by = ctypes.byref
+    d = _m2()
+    rc = _rc("rssm_mamba2_output_sr", by(d), FAKE, FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, FAKE,
+             FAKE, 1 << 20, FAKE, None, None, None)
+    assert rc == B.RSSM_ERR_INVALID_ARG                             # no generator state
+    rc = _rc("rssm_mamba2_full_state_update_sr", by(d), FAKE, FAKE, FAKE, None, 1, FAKE, FAKE,
+             FAKE, FAKE, None, FAKE, FAKE, FAKE + 8, None, None)
+    assert rc == B.RSSM_ERR_INVALID_ARG                             # misaligned generator state
+    assert _rc("rssm_philox4x32_fill", 1, 2, None, 0, None) == B.RSSM_OK
+    assert _rc("rssm_philox4x32_fill", 1, 2, None, 4, None) == B.RSSM_ERR_INVALID_ARG
