@@ -82,8 +82,14 @@ def parse():
     ap.add_argument("--no-gdn", action="store_true",
                     help="mamba2 line only (skip the gdn_decode / gdn_spec sub-objects)")
     ap.add_argument("--sweep-steps", type=int, default=200)
+    ap.add_argument("--sweep-sub-steps", type=int, default=100,
+                    help="timed steps per point of the compact sweep in the default line")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the compact Mamba2 sweep sub-object of the default line")
     ap.add_argument("--event-every", type=int, default=7,
                     help="time the kernel of interest with CUDA events on every n-th step")
+    ap.add_argument("--source-hash", default=None, metavar="FILE.cu",
+                    help="print the combined sha256 of a kernel source and its headers and exit")
     return ap.parse_args()
 
 
@@ -233,14 +239,49 @@ def read_peaks():
     return 6800.0, "fallback"
 
 
+def _local_includes(path, seen):
+    """The file and every header it includes with #include "..." from the library's
+    csrc/ or include/ folders, recursively (sorted, each once)."""
+    if path in seen or not os.path.exists(path):
+        return
+    seen.add(path)
+    dirs = [os.path.dirname(path), os.path.join(ROOT, "ssm_linear_attention_gb300", "csrc"),
+            os.path.join(ROOT, "include")]
+    for line in open(path, encoding="utf-8"):
+        line = line.strip()
+        if line.startswith("#include") and '"' in line:
+            name = line.split('"')[1]
+            for d in dirs:
+                cand = os.path.normpath(os.path.join(d, name))
+                if os.path.exists(cand):
+                    _local_includes(cand, seen)
+                    break
+
+
+def source_hash(kernel_src):
+    """sha256 over a kernel's .cu file and every local header it includes (pipeline,
+    common helpers, cursor model, the C header), so that a change to any of them
+    invalidates counters taken before it."""
+    src = os.path.join(ROOT, "ssm_linear_attention_gb300", "csrc", kernel_src)
+    files = set()
+    _local_includes(src, files)
+    h = hashlib.sha256()
+    for f in sorted(files, key=lambda p: os.path.relpath(p, ROOT)):
+        h.update(os.path.relpath(f, ROOT).encode())
+        h.update(b"\0")
+        h.update(open(f, "rb").read())
+    return h.hexdigest()
+
+
 def traffic_record(kernel_src, profile):
     """DRAM bytes per launch of a kernel from its committed ncu summary, valid only
-    while the kernel source is unchanged (sha256 recorded beside it)."""
+    while the kernel source and the headers it includes are unchanged (their
+    combined sha256, source_hash(), recorded beside the figure)."""
     src = os.path.join(ROOT, "ssm_linear_attention_gb300", "csrc", kernel_src)
     prof = os.path.join(ROOT, "profiles", profile)
     if not (os.path.exists(src) and os.path.exists(prof)):
         return None
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()
+    sha = source_hash(kernel_src)
     rec = {}
     for line in open(prof):
         if ":" in line and line.strip().strip("-* `").startswith(("source_sha256",
@@ -249,7 +290,7 @@ def traffic_record(kernel_src, profile):
             rec[k.strip().strip("-* `")] = v.strip().strip("`")
     if rec.get("source_sha256") == sha and rec.get("traffic_bytes_per_launch"):
         return int(float(rec["traffic_bytes_per_launch"]))
-    return None  # no summary, or the kernel source changed since the counters were taken
+    return None  # no summary, or the kernel or a header changed since the counters were taken
 
 
 def gdn_output_bytes(wl, row_wp, row_flush, out_bytes=2):
@@ -463,6 +504,132 @@ def _timed_graphs(whole, samp, evs, K, dist, dev, offset=0, clocks=True, every=N
     return dist.max(start.elapsed_time(end)), per, rec, [last[j] for j in js]
 
 
+def _phase_complete(per, ks, samp, evs, K, offset, period, every=None):
+    """Launch times of the timed kernel that cover every cursor phase equally.
+
+    A step's cursor pattern repeats with the ring length L (every row's write_pos
+    advances by one per step), so a set of samples is representative when the step
+    indices cover each residue mod `period` equally often. The timed region samples
+    every `every`-th step (coprime with `period`) and keeps the last sample of each
+    input set, i.e. consecutive sampled steps; the last (n // period) * period of
+    them cover every residue exactly n // period times. When the region holds fewer
+    than `period` samples (a short --steps), a dedicated pass of consecutive steps
+    right after the region, every one carrying the events, supplies them instead.
+    Returns (list of (step index, ms), source description)."""
+    import math
+
+    import torch
+    every = EVENT_EVERY if every is None else every
+    pairs = sorted(zip(ks, per))
+    if math.gcd(every, period) == 1:
+        n_use = (len(pairs) // period) * period
+        if n_use >= period:
+            return pairs[-n_use:], "in the timed region: %d sampled launches (every %d-th step), " \
+                "each cursor phase of the %d-step cycle %d times" % (n_use, every, period,
+                                                                    n_use // period)
+    G = len(samp)
+    M = period * max(1, 32 // period)
+    out, k = [], K
+    while len(out) < M:
+        n = min(G, M - len(out))
+        js = []
+        for _ in range(n):
+            j = (k + offset) % G
+            samp[j].replay()
+            js.append((k, j))
+            k += 1
+        torch.cuda.synchronize()
+        out += [(kk, evs[j][0].elapsed_time(evs[j][1])) for kk, j in js]
+    return out, "dedicated pass of %d consecutive launches right after the timed region (the " \
+        "region's %d samples did not cover the %d cursor phases)" % (M, len(pairs), period)
+
+
+def _flush_split(samples, curs, bytes_fn):
+    """Launch-time and byte means of the sampled launches, overall and split into
+    launches whose rows flush and launches whose rows do not (rows that share one
+    cursor phase flush together, every L-th step)."""
+    fl = [(k, ms) for k, ms in samples if curs[k][1].any()]
+    nf = [(k, ms) for k, ms in samples if not curs[k][1].any()]
+
+    def mean(xs, f):
+        return float(np.mean([f(x) for x in xs])) if xs else None
+
+    return {
+        "flush_launches": len(fl), "nonflush_launches": len(nf),
+        "flush_launch_ms": mean(fl, lambda x: x[1]),
+        "nonflush_launch_ms": mean(nf, lambda x: x[1]),
+        "flush_bytes_per_launch": mean(fl, lambda x: bytes_fn(*curs[x[0]])),
+        "nonflush_bytes_per_launch": mean(nf, lambda x: bytes_fn(*curs[x[0]])),
+    }
+
+
+def _e2e_pipelined(dev, dist, n_steps, host_sets, dev_template, out_template, step_fn):
+    """End-to-end steps through a public API call with host buffers: every step copies
+    its inputs from pinned host memory to the device and its result back, all inside
+    the timed region. The copies of step k+1 (in) and k-1 (out) run on two side
+    streams, with double-buffered device inputs and outputs, while step k computes.
+
+    host_sets: list of {name: pinned host tensor}; dev_template: {name: device tensor}
+    (shapes and dtypes of the device copies); out_template: a device tensor like the
+    step's result; step_fn(d, out, stream) runs one step reading the device inputs d
+    and writing out. Returns (ms per step, max over ranks; H2D bytes; D2H bytes)."""
+    import torch
+    names = list(dev_template)
+    dsts = [{k: v.clone() for k, v in dev_template.items()} for _ in range(2)]
+    obuf = [torch.empty_like(out_template) for _ in range(2)]
+    o_host = [torch.empty(out_template.shape, dtype=out_template.dtype).pin_memory()
+              for _ in range(2)]
+    h2d = sum(v.numel() * v.element_size() for v in host_sets[0].values())
+    d2h = o_host[0].numel() * o_host[0].element_size()
+    stream = torch.cuda.current_stream()
+    s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+
+    def run(n):
+        for k in range(n):
+            j = k & 1
+            hs = host_sets[k % len(host_sets)]
+            with torch.cuda.stream(s_in):
+                if k >= 2:
+                    s_in.wait_event(ev_done[j])      # step k-2 has read buffer j
+                for name in names:
+                    dsts[j][name].copy_(hs[name], non_blocking=True)
+                ev_in[j].record(s_in)
+            stream.wait_event(ev_in[j])
+            if k >= 2:
+                stream.wait_event(ev_out[j])         # the result of step k-2 has left buffer j
+            step_fn(dsts[j], obuf[j], stream)
+            ev_done[j].record(stream)
+            with torch.cuda.stream(s_out):
+                s_out.wait_event(ev_done[j])
+                o_host[j].copy_(obuf[j], non_blocking=True)
+                ev_out[j].record(s_out)
+        stream.wait_stream(s_out)
+
+    run(4)
+    torch.cuda.synchronize()
+    dist.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    s_in.wait_event(e0)
+    run(n_steps)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return dist.max(e0.elapsed_time(e1)) / n_steps, int(h2d), int(d2h)
+
+
+def _pinned_sets(make_inputs, count, dtypes):
+    """Pinned host copies of `count` input sets; make_inputs(t) -> {name: numpy}."""
+    import torch
+    out = []
+    for t in range(count):
+        inp = make_inputs(t)
+        out.append({k: torch.from_numpy(inp[k]).to(dt).pin_memory() for k, dt in dtypes.items()})
+    return out
+
+
 # --------------------------------------------------------------------------- #
 # CPU baseline (the oracle)                                                   #
 # --------------------------------------------------------------------------- #
@@ -523,6 +690,73 @@ def cpu_oracle_rate_gdn(wl, seconds, max_rows=16):
     sample = "%d rows x %d steps of the float64 gated delta recurrence (%.1f s)" % (len(rows),
                                                                                     done, el)
     return rate, nth, sample
+
+
+def _cpu_rate(wl, seconds, max_rows, inputs_fn, step_fn, what):
+    """Time an oracle step over a sample of rows until `seconds` of work have run (at
+    least two steps). inputs_fn(t) -> {name: array over all rows}; step_fn(state,
+    inputs, local slot indices, threads) runs one step of the sampled rows. Returns
+    (rows/s, threads, sample text)."""
+    import oracle
+    nth = oracle.default_threads()
+    rows = np.arange(min(max_rows, wl.batch))
+    ci = wl.cache_indices()
+    state = np.ascontiguousarray(
+        np.stack([wl.slot_state(int(ci[r])) for r in rows]).astype(np.float64))
+    inputs = []
+    for t in range(4):
+        inp = inputs_fn(t)
+        inputs.append({k: (None if v is None else np.ascontiguousarray(v[rows]))
+                       for k, v in inp.items()})
+    loc = np.arange(len(rows), dtype=np.int32)
+    done, t0 = 0, time.perf_counter()
+    while True:
+        step_fn(state, inputs[done % len(inputs)], loc, nth)
+        done += 1
+        el = time.perf_counter() - t0
+        if done >= 2 and el >= seconds:
+            break
+    rate = done * len(rows) / el
+    return rate, nth, "%d rows x %d %s (%.1f s)" % (len(rows), done, what, el)
+
+
+def cpu_oracle_rate_kda(wl, seconds, max_rows=16):
+    import oracle
+    return _cpu_rate(wl, seconds, max_rows, wl.step_inputs,
+                     lambda st, i, loc, n: oracle.kda_step(st, i["q"], i["k"], i["v"], i["beta"],
+                                                           i["a"], loc, nthreads=n),
+                     "steps of the float64 per-channel-gate delta recurrence")
+
+
+def cpu_oracle_rate_spec(wl, seconds, max_rows=16):
+    import oracle
+
+    def inputs(t):
+        d = dict(wl.round_inputs(t))
+        d["acc"] = wl.accepted(t).astype(np.int32)
+        return d
+
+    return _cpu_rate(wl, seconds, max_rows, inputs,
+                     lambda st, i, loc, n: oracle.gdn_spec_round(
+                         st, wl.T, i["q"], i["k"], i["v"], i["beta"], i["g"], i["acc"], loc,
+                         nthreads=n),
+                     "verify rounds of the float64 gated delta recurrence (T %d drafts)" % wl.T)
+
+
+def cpu_oracle_rate_m2spec(wl, seconds, max_rows=16):
+    import oracle
+    prm = wl.params()
+
+    def inputs(t):
+        d = dict(wl.round_inputs(t))
+        d["acc"] = wl.accepted(t).astype(np.int32)
+        return d
+
+    return _cpu_rate(wl, seconds, max_rows, inputs,
+                     lambda st, i, loc, n: oracle.mamba2_spec_round(
+                         st, wl.T, i["x"], i["dt_raw"], prm["A"], i["B"], i["C"], prm["D"],
+                         i["acc"], i["z"], prm["dt_bias"], wl.dt_softplus, loc, n),
+                     "verify rounds of the float64 Mamba2 recurrence (T %d drafts)" % wl.T)
 
 
 # --------------------------------------------------------------------------- #
@@ -596,15 +830,17 @@ def run_mamba2(args, dist):
 
     elapsed, out_ms, clocks, ks = _timed_graphs(g_step, g_samp, evs, K, dist, dev, offset=off)
     seg_median = float(np.median(LAST_SEGMENTS))
+    samples, ksrc = _phase_complete(out_ms, ks, g_samp, evs, K, off, wl.L)
     assert int(dec.dev_err.abs().sum().item()) == 0, "device error flag set during the bench"
     del g_step, g_samp
 
     ms_step = elapsed / K
     rows_s = dist.world * wl.batch / (ms_step * 1e-3)
 
-    curs = simulate_cursors(slot_wp0, ci_np, wl.L, K)
-    out_b = np.mean([output_kernel_bytes(wl, *curs[k]) for k in ks])
-    step_b = np.mean([step_bytes(wl, w, f) for w, f in curs])
+    curs = simulate_cursors(slot_wp0, ci_np, wl.L, K + 64)
+    out_ms = [ms for _, ms in samples]
+    out_b = np.mean([output_kernel_bytes(wl, *curs[k]) for k, _ in samples])
+    step_b = np.mean([step_bytes(wl, w, f) for w, f in curs[:K]])
     out_avg_ms = float(np.mean(out_ms))
     peak, peak_kind = read_peaks()
     achieved = out_b / (out_avg_ms * 1e-3) / 1e9
@@ -613,66 +849,18 @@ def run_mamba2(args, dist):
     # end to end through the public API with pinned host buffers
     e2e = None
     if args.e2e_steps > 0:
-        host_sets = []
-        for t in range(min(8, args.input_sets)):
-            inp = wl.step_inputs(t)
-            hs = {}
-            for k2 in ("x", "dt_raw", "B", "C", "z"):
-                tt = torch.from_numpy(inp[k2]).to(bf if k2 != "dt_raw" else torch.float32)
-                hs[k2] = tt.pin_memory()
-            host_sets.append(hs)
-        # two device input sets and two output buffers: the copies of step k+1 (host to
-        # device) and of step k-1 (device to host) run on their own streams while step k
-        # computes; every copy of every step is inside the timed region
         names = ("x", "dt_raw", "B", "C", "z")
-        dsts = [{k2: v.clone() for k2, v in zip(names, sets[0])} for _ in range(2)]
-        ybuf = [torch.empty(wl.batch, wl.nheads, wl.headdim, device=dev, dtype=bf)
-                for _ in range(2)]
-        y_host = [torch.empty(wl.batch, wl.nheads, wl.headdim, dtype=bf).pin_memory()
-                  for _ in range(2)]
-        h2d = sum(v.numel() * v.element_size() for v in host_sets[0].values())
-        d2h = y_host[0].numel() * y_host[0].element_size()
-        stream = torch.cuda.current_stream()
-        s_in, s_out = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
-        ev_in = [torch.cuda.Event() for _ in range(2)]
-        ev_done = [torch.cuda.Event() for _ in range(2)]
-        ev_out = [torch.cuda.Event() for _ in range(2)]
+        dts = {k2: (bf if k2 != "dt_raw" else torch.float32) for k2 in names}
+        host_sets = _pinned_sets(wl.step_inputs, min(8, args.input_sets), dts)
+        ybuf0 = torch.empty(wl.batch, wl.nheads, wl.headdim, device=dev, dtype=bf)
 
-        def e2e_run(n):
-            for k in range(n):
-                j = k & 1
-                hs = host_sets[k % len(host_sets)]
-                with torch.cuda.stream(s_in):
-                    if k >= 2:
-                        s_in.wait_event(ev_done[j])      # step k-2 has read buffer j
-                    for k2 in names:
-                        dsts[j][k2].copy_(hs[k2], non_blocking=True)
-                    ev_in[j].record(s_in)
-                stream.wait_event(ev_in[j])
-                if k >= 2:
-                    stream.wait_event(ev_out[j])         # y of step k-2 has left buffer j
-                d = dsts[j]
-                dec.step(d["x"], d["dt_raw"], d["B"], d["C"], d["z"], ci, y=ybuf[j],
-                         stream=stream)
-                ev_done[j].record(stream)
-                with torch.cuda.stream(s_out):
-                    s_out.wait_event(ev_done[j])
-                    y_host[j].copy_(ybuf[j], non_blocking=True)
-                    ev_out[j].record(s_out)
-            stream.wait_stream(s_out)
+        def m2_step(d, y, stream):
+            dec.step(d["x"], d["dt_raw"], d["B"], d["C"], d["z"], ci, y=y, stream=stream)
 
-        e2e_run(4)
-        torch.cuda.synchronize()
-        dist.barrier()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        s_in.wait_event(e0)
-        e2e_run(args.e2e_steps)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        e_ms = dist.max(e0.elapsed_time(e1)) / args.e2e_steps
+        e_ms, h2d, d2h = _e2e_pipelined(dev, dist, args.e2e_steps, host_sets,
+                                        dict(zip(names, sets[0])), ybuf0, m2_step)
         e2e = {"value": dist.world * wl.batch / (e_ms * 1e-3), "unit": UNIT,
-               "ms_per_step": e_ms, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": e_ms, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                "api": "Mamba2ReplayDecoder.step (eager; one rssm_mamba2_step call, 2 launches); "
                       "inputs and y copied on two side streams, double-buffered"}
 
@@ -746,7 +934,7 @@ def run_mamba2(args, dist):
                    "dstate": wl.dstate, "ngroups": wl.ngroups, "ring_len": wl.L,
                    "state_dtype": "bf16", "act_dtype": "bf16", "out_dtype": "bf16",
                    "parallelism": "independent replica per gpu (dp%d)" % dist.world,
-                   "timing": "one CUDA graph per step (prepare + output); on every 7th step the graph also holds CUDA events around the output kernel",
+                   "timing": "one CUDA graph per step (prepare + output); on every 7th step the graph also holds CUDA events around the output kernel; the kernel figures use samples covering every cursor phase equally",
                    "l2": "inputs larger than L2: 1.07 GB of checkpoint tiles streamed per step"},
         "ms_per_step_median_of_5": seg_median,
         "achieved_hbm_gbs": step_b / (ms_step * 1e-3) / 1e9,
@@ -757,7 +945,8 @@ def run_mamba2(args, dist):
                      "peak_source": peak_kind, "traffic": traffic,
                      "algorithmic_bytes_per_launch": int(out_b), "avg_launch_ms": out_avg_ms,
                      "launches_timed": len(out_ms), "min_launch_ms": float(np.min(out_ms)),
-                     "max_launch_ms": float(np.max(out_ms)), "event_every": EVENT_EVERY},
+                     "max_launch_ms": float(np.max(out_ms)), "event_every": EVENT_EVERY,
+                     "kernel_timing": ksrc},
         "full_state": full,
         "stochastic_rounding": sr,
         "e2e": e2e,
@@ -833,15 +1022,35 @@ def run_gdn(args, dist, sub=False):
     off = args.warmup + max(args.warmup, 3)
     elapsed, out_ms, clocks, ks = _timed_graphs(g_step, g_samp, evs, K, dist, dev, offset=off,
                                                 clocks=not sub)
+    samples, ksrc = _phase_complete(out_ms, ks, g_samp, evs, K, off, wl.L)
     assert int(dec.dev_err.abs().sum().item()) == 0, "device error flag set during the gdn bench"
     del g_step, g_samp
     ms_step = elapsed / K
     rows_s = dist.world * wl.batch / (ms_step * 1e-3)
-    curs = simulate_cursors(slot_wp0, ci_np, wl.L, K)
-    out_b = np.mean([gdn_output_bytes(wl, *curs[k]) for k in ks])
+    curs = simulate_cursors(slot_wp0, ci_np, wl.L, K + 64)
+    out_ms = [ms for _, ms in samples]
+    out_b = np.mean([gdn_output_bytes(wl, *curs[k]) for k, _ in samples])
+    split = _flush_split(samples, curs, lambda w, f: gdn_output_bytes(wl, w, f))
     out_avg_ms = float(np.mean(out_ms))
     peak, peak_kind = read_peaks()
     achieved = out_b / (out_avg_ms * 1e-3) / 1e9
+
+    e2e = None
+    if args.e2e_steps > 0:
+        names = ("q", "k", "v", "beta", "g")
+        dts = {n_: (bf if n_ in ("q", "k", "v") else torch.float32) for n_ in names}
+        host_sets = _pinned_sets(wl.step_inputs, min(8, nsets), dts)
+        obuf0 = torch.empty(wl.batch, wl.num_v_heads, wl.head_v_dim, device=dev, dtype=bf)
+
+        def gdn_step(d, o, stream):
+            dec.step(d["q"], d["k"], d["v"], d["beta"], d["g"], ci, o=o, stream=stream)
+
+        e_ms, h2d, d2h = _e2e_pipelined(dev, dist, args.e2e_steps, host_sets,
+                                        dict(zip(names, sets[0])), obuf0, gdn_step)
+        e2e = {"value": dist.world * wl.batch / (e_ms * 1e-3), "unit": UNIT, "ms_per_step": e_ms,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "api": "GDNReplayDecoder.step (eager; one rssm_gdn_step call, 2 launches); inputs "
+                      "and o copied on two side streams, double-buffered"}
 
     full = None
     if not args.no_full_state:
@@ -879,19 +1088,21 @@ def run_gdn(args, dist, sub=False):
         "config": {"workload": GDN_WORKLOAD, "global_batch": dist.world * wl.batch,
                    "batch_per_gpu": wl.batch, "HV": wl.num_v_heads, "HK": wl.num_k_heads,
                    "K": wl.head_k_dim, "V": wl.head_v_dim, "ring_len": wl.L,
-                   "timing": "one CUDA graph per step (prepare + output); on every 7th step the graph also holds CUDA events around the output kernel",
+                   "timing": "one CUDA graph per step (prepare + output); on every 7th step the graph also holds CUDA events around the output kernel; the kernel figures use samples covering every cursor phase equally",
                    "l2": "inputs larger than L2: 537 MB of fp32 checkpoint tiles per step"},
-        "roofline": {"bound": "hbm", "kernel": "gdn output kernel (fp32 state, 32-row tiles)",
-                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "peak_source": peak_kind,
-                     "traffic": traffic_record("gdn.cu", "gdn_output_kernel_batch256.md"),
-                     "algorithmic_bytes_per_launch": int(out_b), "avg_launch_ms": out_avg_ms},
+        "roofline": dict({"bound": "hbm", "kernel": "gdn output kernel (fp32 state, 32-row tiles)",
+                          "achieved": achieved, "peak": peak, "unit": "GB/s",
+                          "frac": achieved / peak, "peak_source": peak_kind,
+                          "traffic": traffic_record("gdn.cu", "gdn_output_kernel_batch256.md"),
+                          "algorithmic_bytes_per_launch": int(out_b), "avg_launch_ms": out_avg_ms,
+                          "launches_timed": len(out_ms), "kernel_timing": ksrc}, **split),
         "full_state": full,
+        "e2e": e2e,
         "gpu_launches": 2 * K,
         "clocks": clocks,
     }
-    if not sub and dist.rank == 0 and dist.world == 1 and not args.no_cpu:
-        rate, nth, sample = cpu_oracle_rate_gdn(wl, args.cpu_seconds)
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu:
+        rate, nth, sample = cpu_oracle_rate_gdn(wl, args.cpu_seconds / 3 if sub else args.cpu_seconds)
         line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": nth, "kind": "oracle",
                                 "sample": sample}
     return line
@@ -962,16 +1173,36 @@ def run_kda(args, dist, sub=False):
     off = args.warmup + max(args.warmup, 3)
     elapsed, out_ms, clocks, ks = _timed_graphs(g_step, g_samp, evs, K, dist, dev, offset=off,
                                                 clocks=not sub)
+    samples, ksrc = _phase_complete(out_ms, ks, g_samp, evs, K, off, wl.L)
     assert int(dec.dev_err.abs().sum().item()) == 0, "device error flag set during the kda bench"
     del g_step, g_samp
     ms_step = elapsed / K
     rows_s = dist.world * wl.batch / (ms_step * 1e-3)
-    curs = simulate_cursors(slot_wp0, ci_np, wl.L, K)
-    out_b = np.mean([kda_output_bytes(wl, *curs[k]) for k in ks])
-    step_b = np.mean([kda_step_bytes(wl, w, f) for w, f in curs])
+    curs = simulate_cursors(slot_wp0, ci_np, wl.L, K + 64)
+    out_ms = [ms for _, ms in samples]
+    out_b = np.mean([kda_output_bytes(wl, *curs[k]) for k, _ in samples])
+    split = _flush_split(samples, curs, lambda w, f: kda_output_bytes(wl, w, f))
+    step_b = np.mean([kda_step_bytes(wl, w, f) for w, f in curs[:K]])
     out_avg_ms = float(np.mean(out_ms))
     peak, peak_kind = read_peaks()
     achieved = out_b / (out_avg_ms * 1e-3) / 1e9
+
+    e2e = None
+    if args.e2e_steps > 0:
+        names = ("q", "k", "v", "beta", "a")
+        dts = {n_: (bf if n_ in ("q", "k", "v") else torch.float32) for n_ in names}
+        host_sets = _pinned_sets(wl.step_inputs, min(8, nsets), dts)
+        obuf0 = torch.empty(wl.batch, wl.num_v_heads, wl.head_v_dim, device=dev, dtype=bf)
+
+        def kda_step(d, o, stream):
+            dec.step(d["q"], d["k"], d["v"], d["beta"], d["a"], ci, o=o, stream=stream)
+
+        e_ms, h2d, d2h = _e2e_pipelined(dev, dist, args.e2e_steps, host_sets,
+                                        dict(zip(names, sets[0])), obuf0, kda_step)
+        e2e = {"value": dist.world * wl.batch / (e_ms * 1e-3), "unit": UNIT, "ms_per_step": e_ms,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "api": "KDAReplayDecoder.step (eager; one rssm_kda_step call, 3 launches); inputs "
+                      "and o copied on two side streams, double-buffered"}
 
     full = None
     if not args.no_full_state:
@@ -1001,7 +1232,7 @@ def run_kda(args, dist, sub=False):
                 "hbm_frac": fb / (float(np.mean(f_per)) * 1e-3) / 1e9 / peak,
                 "replay_speedup": f_ms / ms_step}
 
-    return {
+    line = {
         "metric": "kda decode rows/s and µs/step at batch %d; achieved HBM GB/s" % wl.batch,
         "value": rows_s, "unit": UNIT, "n_gpus": dist.world, "steps": K, "warmup": args.warmup,
         "ms_per_step": ms_step, "us_per_step": ms_step * 1e3, "higher_is_better": True,
@@ -1009,20 +1240,27 @@ def run_kda(args, dist, sub=False):
         "config": {"workload": KDA_WORKLOAD, "global_batch": dist.world * wl.batch,
                    "batch_per_gpu": wl.batch, "HV": wl.num_v_heads, "HK": wl.num_k_heads,
                    "K": wl.head_k_dim, "V": wl.head_v_dim, "ring_len": wl.L,
-                   "timing": "one CUDA graph per step (cursor + prepare + output); on every 7th step the graph also holds CUDA events around the output kernel",
+                   "timing": "one CUDA graph per step (cursor + prepare + output); on every 7th step the graph also holds CUDA events around the output kernel; the kernel figures use samples covering every cursor phase equally",
                    "l2": "inputs larger than L2: 537 MB of fp32 checkpoint tiles per step"},
         "achieved_hbm_gbs": step_b / (ms_step * 1e-3) / 1e9,
         "hbm_frac_step": step_b / (ms_step * 1e-3) / 1e9 / peak,
         "bytes_per_step": int(step_b),
-        "roofline": {"bound": "hbm", "kernel": "kda output kernel (fp32 state, 32-row tiles)",
-                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
-                     "peak_source": peak_kind,
-                     "traffic": traffic_record("kda.cu", "kda_output_kernel_batch256.md"),
-                     "algorithmic_bytes_per_launch": int(out_b), "avg_launch_ms": out_avg_ms},
+        "roofline": dict({"bound": "hbm", "kernel": "kda output kernel (fp32 state, 32-row tiles)",
+                          "achieved": achieved, "peak": peak, "unit": "GB/s",
+                          "frac": achieved / peak, "peak_source": peak_kind,
+                          "traffic": traffic_record("kda.cu", "kda_output_kernel_batch256.md"),
+                          "algorithmic_bytes_per_launch": int(out_b), "avg_launch_ms": out_avg_ms,
+                          "launches_timed": len(out_ms), "kernel_timing": ksrc}, **split),
         "full_state": full,
+        "e2e": e2e,
         "gpu_launches": 3 * K,
         "clocks": clocks,
     }
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu:
+        rate, nth, sample = cpu_oracle_rate_kda(wl, args.cpu_seconds / 3 if sub else args.cpu_seconds)
+        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": nth, "kind": "oracle",
+                                "sample": sample}
+    return line
 
 
 M2SPEC_WORKLOAD = ("mamba2 replayssm spec verify: batch 128, T 4 drafts, H 128, P 64, N 128, G 8, "
@@ -1086,22 +1324,55 @@ def run_m2spec(args, dist, sub=False):
     offset = 2 * W0
     elapsed, per, clocks, ks = _timed_graphs(graphs, g_rs, revs, K, dist, dev, offset=offset,
                                              clocks=not sub)
+    samples, ksrc = _phase_complete(per, ks, g_rs, revs, K, offset, 16)
     assert int(ver.dev_err.abs().sum().item()) == 0, "device error flag set during the m2 spec bench"
     del graphs, g_rs
     ms_round = elapsed / K
-    seq = [accs[k % G] for k in range(offset + K)]
+    n_run = max(K, max(k for k, _ in samples) + 1)
+    seq = [accs[k % G] for k in range(offset + n_run)]
     sim, cnt_end = spec_cursor_rounds(wl.num_slots, ci_np, seq, L, T)
     dev_cnt = ver.slot_cnt.cpu().numpy().astype(np.int64)
     assert np.array_equal(dev_cnt[ci_np], cnt_end[ci_np]), "spec cursor bookkeeping disagrees"
     vb, fb = [], []
-    for k in ks:
+    for k, _ in samples:
         hist, fl, cr = sim[offset + k]
         v_b, f_b = m2spec_round_bytes(wl, hist, fl, cr)
         vb.append(v_b)
         fb.append(f_b)
     round_b = float(np.mean(vb)) + float(np.mean(fb))
     peak, peak_kind = read_peaks()
-    per_ms = float(np.mean(per))
+    per_ms = float(np.mean([ms for _, ms in samples]))
+
+    e2e = None
+    if args.e2e_steps > 0:
+        names = ("x", "dt_raw", "B", "C", "z", "acc")
+        dts = {n_: (torch.float32 if n_ == "dt_raw" else torch.int32 if n_ == "acc" else bf)
+               for n_ in names}
+
+        def inputs(t):
+            d = dict(wl.round_inputs(t))
+            d["acc"] = wl.accepted(t).astype(np.int32)
+            return d
+
+        host_sets = _pinned_sets(inputs, min(8, nsets), dts)
+        ybuf0 = torch.empty(wl.batch, T, wl.nheads, wl.headdim, device=dev, dtype=bf)
+
+        def m2spec_round(d, y, stream):
+            ver.verify(d["x"], d["dt_raw"], d["B"], d["C"], d["z"], ci, y=y, stream=stream)
+            ver.commit(ci, d["acc"], stream=stream)
+
+        e_ms, h2d, d2h = _e2e_pipelined(dev, dist, args.e2e_steps, host_sets,
+                                        dict(zip(names, sets[0] + [acc_dev[0]])), ybuf0,
+                                        m2spec_round)
+        e2e = {"value": dist.world * wl.batch / (e_ms * 1e-3), "unit": UNIT, "ms_per_step": e_ms,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "api": "Mamba2SpecVerifier.verify + commit (eager; 3 launches per round); drafts, "
+                      "accepted counts and y copied on two side streams, double-buffered"}
+    cpu = None
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu:
+        rate, nth, sample = cpu_oracle_rate_m2spec(wl, args.cpu_seconds / 3 if sub else
+                                                   args.cpu_seconds)
+        cpu = {"value": rate, "unit": UNIT, "cores": nth, "kind": "oracle", "sample": sample}
     return {
         "metric": "mamba2 spec verify rows/s and µs/round at batch %d, T %d" % (wl.batch, T),
         "value": dist.world * wl.batch / (ms_round * 1e-3), "unit": UNIT,
@@ -1117,8 +1388,11 @@ def run_m2spec(args, dist, sub=False):
                      "achieved": round_b / (per_ms * 1e-3) / 1e9, "peak": peak, "unit": "GB/s",
                      "frac": round_b / (per_ms * 1e-3) / 1e9 / peak, "peak_source": peak_kind,
                      "traffic": traffic_record("mamba2_spec.cu", "mamba2_spec_verify_batch128_T4.md"),
-                     "algorithmic_bytes_per_round": int(round_b),
-                     "verify_bytes": float(np.mean(vb)), "fold_bytes": float(np.mean(fb))},
+                     "algorithmic_bytes_per_round": int(round_b), "avg_round_ms": per_ms,
+                     "verify_bytes": float(np.mean(vb)), "fold_bytes": float(np.mean(fb)),
+                     "rounds_timed": len(samples), "kernel_timing": ksrc},
+        "e2e": e2e,
+        "cpu_baseline": cpu,
         "gpu_launches": 3 * K,
         "clocks": clocks,
     }
@@ -1186,21 +1460,49 @@ def run_spec(args, dist, sub=False):
     offset = 2 * W0
     elapsed, per, clocks, ks = _timed_graphs(graphs, g_rs, revs, K, dist, dev, offset=offset,
                                              clocks=not sub)
+    samples, ksrc = _phase_complete(per, ks, g_rs, revs, K, offset, 16)
     assert int(ver.dev_err.abs().sum().item()) == 0, "device error flag set during the spec bench"
     del graphs, g_rs
     ms_round = elapsed / K
     # byte count from the cursor sequence of all rounds run so far
-    seq = [accs[k % G] for k in range(offset + K)]
+    n_run = max(K, max(k for k, _ in samples) + 1)
+    seq = [accs[k % G] for k in range(offset + n_run)]
     sim, cnt_end = spec_cursor_rounds(wl.num_slots, ci_np, seq, L, T)
     dev_cnt = ver.slot_cnt.cpu().numpy().astype(np.int64)
     assert np.array_equal(dev_cnt[ci_np], cnt_end[ci_np]), "spec cursor bookkeeping disagrees"
     vb, fb = [], []
-    for hist, fl, cr in [sim[offset + k] for k in ks]:  # the rounds whose duration was sampled
+    for hist, fl, cr in [sim[offset + k] for k, _ in samples]:  # the sampled rounds
         vb.append(spec_round_bytes(wl, hist))
         fb.append(gdn_fold_bytes(wl, fl, cr))
     round_b = float(np.mean(vb)) + float(np.mean(fb))
     peak, peak_kind = read_peaks()
-    per_ms = float(np.mean(per))
+    per_ms = float(np.mean([ms for _, ms in samples]))
+
+    e2e = None
+    if args.e2e_steps > 0:
+        names = ("q", "k", "v", "beta", "g", "acc")
+        dts = {n_: (bf if n_ in ("q", "k", "v") else torch.int32 if n_ == "acc" else
+                    torch.float32) for n_ in names}
+
+        def inputs(t):
+            d = dict(wl.round_inputs(t))
+            d["acc"] = wl.accepted(t).astype(np.int32)
+            return d
+
+        host_sets = _pinned_sets(inputs, min(8, nsets), dts)
+        obuf0 = torch.empty(wl.batch, T, wl.num_v_heads, wl.head_v_dim, device=dev, dtype=bf)
+
+        def spec_round(d, o, stream):
+            ver.verify(d["q"], d["k"], d["v"], d["beta"], d["g"], ci, o=o, stream=stream)
+            ver.commit(ci, d["acc"], stream=stream)
+
+        e_ms, h2d, d2h = _e2e_pipelined(dev, dist, args.e2e_steps, host_sets,
+                                        dict(zip(names, sets[0] + [acc_dev[0]])), obuf0,
+                                        spec_round)
+        e2e = {"value": dist.world * wl.batch / (e_ms * 1e-3), "unit": UNIT, "ms_per_step": e_ms,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "api": "GDNSpecVerifier.verify + commit (eager; 3 launches per round); drafts, "
+                      "accepted counts and o copied on two side streams, double-buffered"}
 
     # the in-house conventional verify (a full-state snapshot per draft, commit copies
     # the accepted one) on an identical pool, same drafts and accepted counts
@@ -1257,12 +1559,19 @@ def run_spec(args, dist, sub=False):
                      "achieved": round_b / (per_ms * 1e-3) / 1e9, "peak": peak, "unit": "GB/s",
                      "frac": round_b / (per_ms * 1e-3) / 1e9 / peak, "peak_source": peak_kind,
                      "traffic": traffic_record("gdn_spec.cu", "gdn_spec_verify_batch128_T4.md"),
-                     "algorithmic_bytes_per_round": int(round_b),
-                     "verify_bytes": float(np.mean(vb)), "fold_bytes": float(np.mean(fb))},
+                     "algorithmic_bytes_per_round": int(round_b), "avg_round_ms": per_ms,
+                     "verify_bytes": float(np.mean(vb)), "fold_bytes": float(np.mean(fb)),
+                     "rounds_timed": len(samples), "kernel_timing": ksrc},
         "full_state": full,
+        "e2e": e2e,
         "gpu_launches": 3 * K,
         "clocks": clocks,
     }
+    if dist.rank == 0 and dist.world == 1 and not args.no_cpu:
+        rate, nth, sample = cpu_oracle_rate_spec(wl, args.cpu_seconds / 3 if sub else
+                                                 args.cpu_seconds)
+        line["cpu_baseline"] = {"value": rate, "unit": UNIT, "cores": nth, "kind": "oracle",
+                                "sample": sample}
     return line
 
 
@@ -1275,100 +1584,131 @@ SWEEP_L = (1, 4, 8, 16)
 SWEEP_DT = ("fp32", "bf16")
 
 
-def run_sweep(args, dist):
-    """One JSON line per (batch, L, state dtype): the ReplaySSM step (one CUDA graph
-    per step) and the full-state kernel on an identical pool, with 5% of rows per
-    step force-flushed. Pools are filled on the device from a seeded generator."""
+def sweep_point(args, dist, dev, batch, L, sdt, K):
+    """One Mamba2 sweep point (config-2 geometry: H 128, P 64, N 128, G 8, 5% of rows
+    force-flushed per step): the ReplaySSM step (one CUDA graph per step) and the
+    full-state kernel on an identical pool, K timed steps each. The pool is filled on
+    the device from a seeded generator."""
     import torch
 
     import rssm_workloads as W
     import ssm_linear_attention_gb300 as ssm
 
-    dev = _device(dist)
-    ssm.lib()
     peak, _ = read_peaks()
     bf = torch.bfloat16
-    K = args.sweep_steps
+    st = torch.float32 if sdt == "fp32" else bf
+    wl = W.mamba2_sweep(batch, L, sdt, seed=shard_seed(args.seed, dist.rank))
+    prm = wl.params()
+    ci_np = wl.cache_indices()
+    ci = torch.from_numpy(ci_np).to(dev)
+    dec = ssm.Mamba2ReplayDecoder(wl.nheads, wl.headdim, wl.dstate, wl.ngroups, L,
+                                  wl.num_slots, batch, prm["A"], prm["D"],
+                                  prm["dt_bias"], state_dtype=st, act_dtype=bf,
+                                  out_dtype=bf, device=dev)
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(shard_seed(args.seed, dist.rank) + batch * 131 + L)
+    dec.state.normal_(0.0, 0.1, generator=gen)
+    nsets = 8
+    sets = []
+    for t in range(nsets):
+        inp = wl.step_inputs(t)
+        xs = [torch.from_numpy(inp[k]).to(dev, bf if k != "dt_raw" else torch.float32)
+              for k in ("x", "dt_raw", "B", "C", "z")]
+        fm = wl.force_mask(t)
+        xs.append(None if fm is None else torch.from_numpy(fm).to(dev))
+        sets.append(xs)
+    torch.cuda.synchronize()
+
+    def rep_fn(j):
+        x, dt, Bm, C, z, fm = sets[j]
+        return lambda: dec.step(x, dt, Bm, C, z, ci, force_flush=fm)
+
+    for k in range(3):
+        rep_fn(k % nsets)()
+    g_rep = _graphs([rep_fn(j) for j in range(nsets)])
+    for k in range(3):
+        g_rep[k].replay()
+    el, _, _, _ = _timed_graphs(g_rep, g_rep, [(None, None)] * nsets, K, dist, dev,
+                                clocks=False, every=K + 1)
+    assert int(dec.dev_err.abs().sum().item()) == 0
+    del g_rep
+    rep_ms = el / K
+    fdec = ssm.Mamba2FullStateDecoder(wl.nheads, wl.headdim, wl.dstate, wl.ngroups,
+                                      wl.num_slots, batch, prm["A"], prm["D"],
+                                      prm["dt_bias"], state_dtype=st, act_dtype=bf,
+                                      out_dtype=bf, device=dev)
+    fdec.state.copy_(dec.state)
+    del dec
+
+    def full_fn(j):
+        x, dt, Bm, C, z, fm = sets[j]
+        return lambda: fdec.step(x, dt, Bm, C, z, ci)
+
+    for k in range(3):
+        full_fn(k % nsets)()
+    g_full = _graphs([full_fn(j) for j in range(nsets)])
+    for k in range(3):
+        g_full[k].replay()
+    fel, _, _, _ = _timed_graphs(g_full, g_full, [(None, None)] * nsets, K, dist, dev,
+                                 clocks=False, every=K + 1)
+    del g_full, fdec
+    full_ms = fel / K
+    fb = full_state_bytes(wl, batch)
+    l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0)
+    tile_bytes = batch * wl.nheads * wl.headdim * wl.dstate * (4 if sdt == "fp32" else 2)
+    del sets
+    torch.cuda.empty_cache()
+    return {"batch": batch, "ring_len": L, "state_dtype": sdt, "steps": K,
+            "state_bytes_per_step": tile_bytes,
+            "possibly_l2_resident": bool(l2 and tile_bytes <= l2),
+            "replay_us_per_step": rep_ms * 1e3,
+            "replay_rows_per_s": dist.world * batch / (rep_ms * 1e-3),
+            "full_state_us_per_step": full_ms * 1e3,
+            "full_state_gbs": fb / (full_ms * 1e-3) / 1e9,
+            "full_state_hbm_frac": fb / (full_ms * 1e-3) / 1e9 / peak,
+            "replay_speedup": full_ms / rep_ms}
+
+
+SWEEP_BATCH = (1, 16, 64, 128, 256, 512, 1024)
+SWEEP_L = (1, 4, 8, 16)
+SWEEP_DT = ("fp32", "bf16")
+# the points the default line carries: the batches the bar names (>= 64) at both ends
+# of the ring lengths, both state dtypes
+SWEEP_DEFAULT = [(b, L, d) for d in SWEEP_DT for L in (1, 16) for b in (64, 1024)]
+
+
+def run_sweep(args, dist):
+    """One JSON line per (batch, L, state dtype) of the Mamba2 sweep, each point beside
+    the full-state kernel."""
+    import ssm_linear_attention_gb300 as ssm
+
+    dev = _device(dist)
+    ssm.lib()
     for sdt in SWEEP_DT:
-        st = torch.float32 if sdt == "fp32" else bf
         for L in SWEEP_L:
             for batch in SWEEP_BATCH:
-                wl = W.mamba2_sweep(batch, L, sdt, seed=shard_seed(args.seed, dist.rank))
-                prm = wl.params()
-                ci_np = wl.cache_indices()
-                ci = torch.from_numpy(ci_np).to(dev)
-                dec = ssm.Mamba2ReplayDecoder(wl.nheads, wl.headdim, wl.dstate, wl.ngroups, L,
-                                              wl.num_slots, batch, prm["A"], prm["D"],
-                                              prm["dt_bias"], state_dtype=st, act_dtype=bf,
-                                              out_dtype=bf, device=dev)
-                gen = torch.Generator(device=dev)
-                gen.manual_seed(shard_seed(args.seed, dist.rank) + batch * 131 + L)
-                dec.state.normal_(0.0, 0.1, generator=gen)
-                nsets = 8
-                sets = []
-                for t in range(nsets):
-                    inp = wl.step_inputs(t)
-                    xs = [torch.from_numpy(inp[k]).to(dev, bf if k != "dt_raw" else torch.float32)
-                          for k in ("x", "dt_raw", "B", "C", "z")]
-                    fm = wl.force_mask(t)
-                    xs.append(None if fm is None else torch.from_numpy(fm).to(dev))
-                    sets.append(xs)
-                torch.cuda.synchronize()
-
-                def rep_fn(j):
-                    x, dt, Bm, C, z, fm = sets[j]
-                    return lambda: dec.step(x, dt, Bm, C, z, ci, force_flush=fm)
-
-                for k in range(3):
-                    rep_fn(k % nsets)()
-                g_rep = _graphs([rep_fn(j) for j in range(nsets)])
-                for k in range(3):
-                    g_rep[k].replay()
-                el, _, _, _ = _timed_graphs(g_rep, g_rep, [(None, None)] * nsets, K, dist, dev,
-                                            clocks=False, every=K + 1)
-                assert int(dec.dev_err.abs().sum().item()) == 0
-                del g_rep
-                rep_ms = el / K
-                # bytes: flush rate from the step pattern (w == L-1 or forced)
-                fdec = ssm.Mamba2FullStateDecoder(wl.nheads, wl.headdim, wl.dstate, wl.ngroups,
-                                                  wl.num_slots, batch, prm["A"], prm["D"],
-                                                  prm["dt_bias"], state_dtype=st, act_dtype=bf,
-                                                  out_dtype=bf, device=dev)
-                fdec.state.copy_(dec.state)
-                del dec
-
-                def full_fn(j):
-                    x, dt, Bm, C, z, fm = sets[j]
-                    return lambda: fdec.step(x, dt, Bm, C, z, ci)
-
-                for k in range(3):
-                    full_fn(k % nsets)()
-                g_full = _graphs([full_fn(j) for j in range(nsets)])
-                for k in range(3):
-                    g_full[k].replay()
-                fel, _, _, _ = _timed_graphs(g_full, g_full, [(None, None)] * nsets, K, dist, dev,
-                                             clocks=False, every=K + 1)
-                del g_full, fdec
-                full_ms = fel / K
-                fb = full_state_bytes(wl, batch)
-                l2 = getattr(torch.cuda.get_device_properties(dev), "L2_cache_size", 0)
-                tile_bytes = batch * wl.nheads * wl.headdim * wl.dstate * (4 if sdt == "fp32" else 2)
-                line = {"metric": "mamba2 sweep point", "workload": "sweep", "batch": batch,
-                        "state_bytes_per_step": tile_bytes,
-                        "possibly_l2_resident": bool(l2 and tile_bytes <= l2),
-                        "ring_len": L, "state_dtype": sdt, "steps": K, "n_gpus": dist.world,
-                        "replay_us_per_step": rep_ms * 1e3,
-                        "replay_rows_per_s": dist.world * batch / (rep_ms * 1e-3),
-                        "full_state_us_per_step": full_ms * 1e3,
-                        "full_state_gbs": fb / (full_ms * 1e-3) / 1e9,
-                        "full_state_hbm_frac": fb / (full_ms * 1e-3) / 1e9 / peak,
-                        "replay_speedup": full_ms / rep_ms,
-                        "timing": "one CUDA graph per step (2 launches); full state one graph"}
+                pt = sweep_point(args, dist, dev, batch, L, sdt, args.sweep_steps)
+                line = dict({"metric": "mamba2 sweep point", "workload": "sweep",
+                             "n_gpus": dist.world,
+                             "timing": "one CUDA graph per step (2 launches); full state one graph"},
+                            **pt)
                 if dist.rank == 0:
                     print(json.dumps(line), flush=True)
-                del sets
-                torch.cuda.empty_cache()
     return None
+
+
+def run_sweep_sub(args, dist):
+    """The compact sweep of the default line: SWEEP_DEFAULT's points."""
+    import ssm_linear_attention_gb300 as ssm
+
+    dev = _device(dist)
+    ssm.lib()
+    pts = [sweep_point(args, dist, dev, b, L, d, args.sweep_sub_steps) for b, L, d in SWEEP_DEFAULT]
+    return {"workload": "mamba2 sweep (H 128, P 64, N 128, G 8, 5% forced flushes per step), "
+                        "ReplaySSM step beside the full-state kernel on an identical pool",
+            "timing": "one CUDA graph per step; %d timed steps per point and kernel"
+                      % args.sweep_sub_steps,
+            "points": pts}
 
 
 def run_reference(args, dist):
@@ -1420,6 +1760,9 @@ def run_reference(args, dist):
 def main():
     global EVENT_EVERY
     args = parse()
+    if args.source_hash:
+        print(source_hash(args.source_hash))
+        return
     EVENT_EVERY = max(1, args.event_every)
     dist = Dist()
     try:
@@ -1446,6 +1789,8 @@ def main():
                 line["gdn_spec"] = run_spec(args, dist, sub=True)
                 line["kda_decode"] = run_kda(args, dist, sub=True)
                 line["mamba2_spec"] = run_m2spec(args, dist, sub=True)
+            if not args.no_sweep:
+                line["mamba2_sweep"] = run_sweep_sub(args, dist)
         if dist.rank == 0 and line is not None:
             print(json.dumps(line), flush=True)
     finally:

@@ -384,7 +384,11 @@ int rssm_mamba2_spec_verify(const rssm_mamba2_dims* dims, int32_t T, void* state
  *     needs 9 MiB); larger sizes return RSSM_ERR_UNSUPPORTED before any launch.
  *   - Set-up: the first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call before
- *     any stream capture. A failed look-up returns RSSM_ERR_CUDA.
+ *     any stream capture. A failed look-up returns RSSM_ERR_CUDA and is not cached:
+ *     the next call tries again. The address is kept per device together with the
+ *     id of the context it belongs to; after cudaDeviceReset (a new context, the
+ *     module loaded again) the next call looks it up again, so that call too should
+ *     come before any stream capture.
  *   - Sharing: every call on a device uses the same array and leaves its contents
  *     there; nothing in it needs to start at zero. Calls whose executions overlap on
  *     the GPU race on it, so keep them in one stream or order them.
@@ -685,6 +689,24 @@ int rssm_gdn_materialize_state(const rssm_gdn_dims* dims, const float* state, co
                                const float* ring_g, const float* ring_d, const int32_t* slots,
                                const int32_t* slot_wp, const int32_t* slot_base, float* out,
                                int32_t* dev_err, rssm_stream_t stream);
+
+/* rssm_debug_pipeline_copy -- test / debug: exercises the bounded waits of the
+ * streaming pipeline every decode kernel runs on. Copies n_tiles tiles of 16 KB
+ * from src to dst (float32, device, caller owned, 16-byte aligned) through that
+ * pipeline: each tile is staged in shared memory by a 1-D bulk copy whose arrival a
+ * stage barrier counts, then written out by the consumer warps. With stall_tile in
+ * 0..n_tiles-1 that tile's stage barrier is armed for 16 bytes more than its copy
+ * delivers, so it never completes although the copy lands: the waiting warp gives
+ * up after wait_us microseconds (1..2000000), ORs RSSM_DEVERR_TIMEOUT into *dev_err
+ * (when non-NULL), and its CTA winds down -- the other warps stop waiting, each
+ * producer waits (bounded) for the copies it issued -- so the kernel returns with no
+ * copy in flight and the context stays usable; dst is then only partly written.
+ * stall_tile < 0 copies every tile. The decode kernels wait 2 s before giving up;
+ * the pages have no counterpart (failure handling of this library). Errors:
+ * RSSM_ERR_INVALID_ARG (n_tiles < 0, stall_tile >= n_tiles, wait_us out of range,
+ * null or misaligned src/dst), RSSM_ERR_CUDA. */
+int rssm_debug_pipeline_copy(const float* src, float* dst, int n_tiles, int stall_tile,
+                             int wait_us, int32_t* dev_err, rssm_stream_t stream);
 
 #ifdef __cplusplus
 }

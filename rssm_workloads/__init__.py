@@ -52,11 +52,16 @@ def _rng(seed: int, tag: int, idx: int = 0) -> np.random.Generator:
 
 
 def round_bf16_f32(a: np.ndarray) -> np.ndarray:
-    """Round float32 values to the nearest bfloat16 (ties to even); returns float32."""
+    """Round float32 values to the nearest bfloat16 (ties to even); returns float32.
+    Finite values and infinities only (the sum below stays inside 32 bits for every
+    such bit pattern; the inputs never hold NaN)."""
     a = np.ascontiguousarray(a, dtype=np.float32)
-    u = a.view(np.uint32).astype(np.uint64)
-    u = (u + 0x7FFF + ((u >> 16) & 1)) & 0xFFFF0000
-    return u.astype(np.uint32).view(np.float32)
+    u = a.view(np.uint32)
+    r = (u >> 16) & 1
+    r += 0x7FFF
+    r += u
+    r &= 0xFFFF0000
+    return r.view(np.float32)
 
 
 def _to_grid(a: np.ndarray, dtype: str) -> np.ndarray:

@@ -34,6 +34,7 @@ EXPORTS = (
     "rssm_gdn_spec_full_state_snapshot_bytes", "rssm_gdn_spec_full_state_verify",
     "rssm_gdn_spec_full_state_commit", "rssm_kda_workspace_size", "rssm_kda_prepare",
     "rssm_kda_output", "rssm_kda_step", "rssm_kda_full_state_decode",
+    "rssm_debug_pipeline_copy",
 )
 
 
@@ -136,6 +137,7 @@ def _declare(L):
                                             _VP]),
         "rssm_gdn_spec_verify": (_I, [gd, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                       _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _VP, _VP]),
+        "rssm_debug_pipeline_copy": (_I, [_VP, _VP, _I, _I, _I, _VP, _VP]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -317,6 +319,13 @@ def rssm_philox4x32_fill(seed, offset, out, n_groups, stream=None):
     rounding of groups 0..n_groups-1 draws at (seed, offset)."""
     _call("rssm_philox4x32_fill", int(seed) & (2 ** 64 - 1), int(offset) & (2 ** 64 - 1),
           _ptr(out), int(n_groups), _stream(stream))
+
+
+def rssm_debug_pipeline_copy(src, dst, n_tiles, stall_tile, wait_us, dev_err=None, stream=None):
+    """Copy n_tiles 16 KB tiles src -> dst through the streaming pipeline; stall_tile >= 0
+    makes that tile's stage wait run out after wait_us (test of the bounded waits)."""
+    _call("rssm_debug_pipeline_copy", _ptr(src), _ptr(dst), int(n_tiles), int(stall_tile),
+          int(wait_us), _ptr(dev_err), _stream(stream))
 
 
 def rssm_gdn_ring_append(dims, k, g, cache_indices, row_wp, ring_k, ring_g, dev_err=None,

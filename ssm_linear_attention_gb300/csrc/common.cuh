@@ -62,13 +62,27 @@ __device__ __forceinline__ uint64_t global_ns() {
     return t;
 }
 
-// Wait for phase `parity` of `bar` to complete; false when RSSM_WAIT_NS elapsed.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+// Wait for phase `parity` of `bar` to complete; false when `limit_ns` elapsed.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity,
+                                                  uint64_t limit_ns = RSSM_WAIT_NS) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     while (true) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (global_ns() - t0 > RSSM_WAIT_NS) return false;
+        if (global_ns() - t0 > limit_ns) return false;
+    }
+}
+
+// As mbar_wait_bounded, but also gives up as soon as *abort is set by another warp.
+// Returns 1 (phase completed), 0 (limit elapsed) or -1 (aborted).
+__device__ __forceinline__ int mbar_wait_abortable(uint64_t* bar, uint32_t parity,
+                                                   uint64_t limit_ns, volatile int* abort) {
+    if (mbar_try_wait(bar, parity)) return 1;
+    const uint64_t t0 = global_ns();
+    while (true) {
+        if (mbar_try_wait(bar, parity)) return 1;
+        if (*abort) return -1;
+        if (global_ns() - t0 > limit_ns) return 0;
     }
 }
 

@@ -24,31 +24,88 @@ namespace {
 __device__ __align__(256) unsigned char g_noalloc_workspace[RSSM_NOALLOC_WORKSPACE_BYTES];
 
 constexpr int kMaxDevices = 64;
-std::once_flag g_once[kMaxDevices];
-void* g_ptr[kMaxDevices];
-cudaError_t g_err[kMaxDevices];
 
-// Device address of the array for the current device, looked up once per device
-// with that device current. Host code must not use the symbol itself as a pointer.
+// The array's device address per device, with the id of the context it was looked
+// up in. A device reset destroys that context and unloads the module, so a cached
+// address is reused only while the device's current context is still the same one.
+struct Cached {
+    bool valid;
+    unsigned long long ctx_id;
+    void* ptr;
+};
+std::mutex g_mu;
+Cached g_cache[kMaxDevices];
+
+// Driver entry points (looked up through the runtime, so the library keeps loading on
+// machines without a driver): the current context and its unique id.
+typedef int (*CtxGetCurrentFn)(void**);
+typedef int (*CtxGetIdFn)(void*, unsigned long long*);
+std::once_flag g_drv_once;
+CtxGetCurrentFn g_ctx_current = nullptr;
+CtxGetIdFn g_ctx_id = nullptr;
+
+// Id of the calling thread's current context; false when there is none yet (the
+// runtime creates it on first use) or the driver offers no such query.
+bool current_context_id(unsigned long long* id) {
+    std::call_once(g_drv_once, []() {
+        cudaDriverEntryPointQueryResult q;
+        void* f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_current = reinterpret_cast<CtxGetCurrentFn>(f);
+        else
+            cudaGetLastError();  // this lookup's own error
+        f = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_ctx_id = reinterpret_cast<CtxGetIdFn>(f);
+        else
+            cudaGetLastError();
+    });
+    if (!g_ctx_current || !g_ctx_id) return false;
+    void* ctx = nullptr;
+    if (g_ctx_current(&ctx) != 0 || ctx == nullptr) return false;
+    return g_ctx_id(ctx, id) == 0;
+}
+
+// Device address of the array for the current device. Host code must not use the
+// symbol itself as a pointer: it names a host-side stand-in. The address is looked
+// up with the device current, cached only when the look-up succeeds (a failed one,
+// for instance inside a stream capture that forbids it, is retried by the next
+// call), and looked up again when the device's context has changed since.
 void* workspace_address(int* status) {
     int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
-        cudaGetLastError();
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        cudaGetLastError();  // the error this call raised
         *status = RSSM_ERR_CUDA;
         return nullptr;
     }
-    std::call_once(g_once[dev], [dev]() {
-        void* p = nullptr;
-        g_err[dev] = cudaGetSymbolAddress(&p, g_noalloc_workspace);
-        if (g_err[dev] != cudaSuccess) cudaGetLastError();
-        g_ptr[dev] = p;
-    });
-    if (g_err[dev] != cudaSuccess || g_ptr[dev] == nullptr) {
+    if (dev < 0 || dev >= kMaxDevices) {
+        *status = RSSM_ERR_UNSUPPORTED;
+        return nullptr;
+    }
+    std::lock_guard<std::mutex> lk(g_mu);
+    unsigned long long id = 0;
+    const bool have_id = current_context_id(&id);
+    Cached& c = g_cache[dev];
+    if (c.valid && have_id && c.ctx_id == id) {
+        *status = RSSM_OK;
+        return c.ptr;
+    }
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_workspace) != cudaSuccess || p == nullptr) {
+        cudaGetLastError();  // the error this call raised
+        c.valid = false;
         *status = RSSM_ERR_CUDA;
         return nullptr;
     }
+    // the look-up made the context current if there was none: take its id now
+    c.valid = current_context_id(&c.ctx_id);
+    c.ptr = p;
     *status = RSSM_OK;
-    return g_ptr[dev];
+    return p;
 }
 
 }  // namespace

@@ -15,8 +15,12 @@
 // issue a tile's copies; with one producer per group the issue rate scales with
 // the groups, and an expensive item (a flush) only delays its own pipeline.
 //
-// Every wait is bounded (RSSM_WAIT_NS); a wait that expires sets an abort flag
-// and RSSM_DEVERR_TIMEOUT, and all warps wind down.
+// Every wait is bounded (RSSM_WAIT_NS, or the policy's Args::wait_ns when it has
+// one); a wait that expires sets an abort flag and RSSM_DEVERR_TIMEOUT, and all
+// warps wind down: waiting warps give up as soon as the flag is set, and each
+// producer, before it exits, waits (bounded again) for the copies it issued into
+// stages nobody consumed, so no bulk copy into this CTA's shared memory is left in
+// flight when the CTA exits.
 //
 // A kernel policy K provides:
 //   static constexpr int kGroup;          warps per consumer group
@@ -47,6 +51,16 @@ constexpr unsigned kFull = 0xffffffffu;
 __device__ __forceinline__ void mbar_arrive_plain(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
+
+// The wait limit of a policy: Args::wait_ns when the policy has it, else RSSM_WAIT_NS.
+template <class K, class = void>
+struct WaitLimit {
+    static __device__ __forceinline__ uint64_t ns(const typename K::Args&) { return RSSM_WAIT_NS; }
+};
+template <class K>
+struct WaitLimit<K, decltype(void(K::Args::wait_ns))> {
+    static __device__ __forceinline__ uint64_t ns(const typename K::Args& a) { return a.wait_ns; }
+};
 
 template <class K>
 __global__ void __launch_bounds__(32 * kPipeMaxGroups * (K::kGroup + 1), 1)
@@ -80,11 +94,13 @@ __global__ void __launch_bounds__(32 * kPipeMaxGroups * (K::kGroup + 1), 1)
     }
     __syncthreads();
 
+    const uint64_t wait_ns = WaitLimit<K>::ns(a);
+
     if (warp >= nc) {
         // ---------------- producer warp of pipeline g ----------------
         const int g = warp - nc;
         const uint64_t pol = policy_evict_first();
-        int pos = 0, lap = 0;  // next stage of this pipeline, completed laps of its stages
+        int pos = 0, lap = 0;  // stage position and lap of the next item to issue
         for (int u0 = 0;; u0 += 32) {
             const int my_item = blockIdx.x + (g + (u0 + lane) * ng) * gridDim.x;
             int4 info = make_int4(0, 0, 0, 0);
@@ -104,26 +120,37 @@ __global__ void __launch_bounds__(32 * kPipeMaxGroups * (K::kGroup + 1), 1)
                 int bad = 0;
                 if (lane == 0) {
                     const int st = g + ng * pos;
-                    if (lap > 0 && !mbar_wait_bounded(&emptyb[st], (lap - 1) & 1)) {
+                    int ok = 1;
+                    if (lap > 0) ok = mbar_wait_abortable(&emptyb[st], (lap - 1) & 1, wait_ns, abort_flag);
+                    if (ok == 0) {
                         *abort_flag = 1;
                         set_dev_err(a.dev_err, RSSM_DEVERR_TIMEOUT);
                     }
-                    if (*abort_flag)
+                    if (ok != 1 || *abort_flag)
                         bad = 1;
                     else
                         K::issue(a, item, r, meta_of(st), stage0 + (size_t)st * a.stage_bytes,
                                  &fullb[st], pol);
                 }
-                if (++pos == spg) {
-                    pos = 0;
-                    ++lap;
-                }
                 if (__shfl_sync(kFull, bad, 0)) {
                     stop = 1;
                     break;
                 }
+                if (++pos == spg) {
+                    pos = 0;
+                    ++lap;
+                }
             }
             if (stop) break;
+        }
+        // Wind-down after an abort: the last issue into each stage may still have copies
+        // in flight if no consumer waited for it. Stage position p has had
+        // lap + (p < pos) issues; wait (bounded) for the phase of the last one.
+        if (lane == 0 && *abort_flag) {
+            for (int p = 0; p < spg; ++p) {
+                const int cnt = lap + (p < pos ? 1 : 0);
+                if (cnt > 0) mbar_wait_bounded(&fullb[g + ng * p], (cnt - 1) & 1, wait_ns);
+            }
         }
         return;
     }
@@ -136,9 +163,11 @@ __global__ void __launch_bounds__(32 * kPipeMaxGroups * (K::kGroup + 1), 1)
         const int item = blockIdx.x + (g + u * ng) * gridDim.x;
         if (item >= n) break;
         const int st = g + ng * pos;
-        const bool ok = __all_sync(kFull, mbar_wait_bounded(&fullb[st], lap & 1));
-        if (!ok) {
-            if (lane == 0) {
+        const int ok = mbar_wait_abortable(&fullb[st], lap & 1, wait_ns, abort_flag);
+        if (__ballot_sync(kFull, ok == 1) != kFull) {
+            // a copy did not land in time (or another warp gave up): stop; the producer
+            // drains what it issued
+            if (__ballot_sync(kFull, ok == 0) && lane == 0) {
                 *abort_flag = 1;
                 set_dev_err(a.dev_err, RSSM_DEVERR_TIMEOUT);
             }

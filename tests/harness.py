@@ -56,6 +56,14 @@ def state_ok(gpu, ref, state_dtype: str):
     return bool(np.all(within)), e, flips
 
 
+def row_chunks(rows, size):
+    """Consecutive slices of `rows` of at most `size` entries, as (start, rows) pairs.
+    Rows are independent, so the oracle runs one chunk at a time and its float64
+    state stays bounded at the full configurations."""
+    rows = np.asarray(rows)
+    return [(i, rows[i:i + size]) for i in range(0, len(rows), size)]
+
+
 def to_dev(a, dtype, device="cuda"):
     if a is None:
         return None
@@ -117,8 +125,9 @@ def run_gpu_mamba2(wl, steps=None, out_dtype=torch.float32, full_state=False, ro
             y = dec.step(x, dt, Bm, C, z, ci_d, None if f is None else to_dev(f, torch.uint8))
             wps.append(dec.row_wp[: wl.batch].cpu().numpy().copy())
             fls.append(dec.row_flush[: wl.batch].cpu().numpy().copy())
+        # float32 on the host (exact for fp32 and bf16 outputs); compared in float64
         ys.append((y if keep_all_y else y[torch.as_tensor(rows, device=y.device)]).float().cpu()
-                  .numpy().astype(np.float64))
+                  .numpy())
     torch.cuda.synchronize()
     return dict(y=ys, row_wp=np.array(wps), row_flush=np.array(fls), dec=dec)
 
@@ -182,7 +191,7 @@ def run_gpu_gdn(wl, steps=None, out_dtype=torch.float32, full_state=False, rows=
             o = dec.step(q, k, v, be, g, ci_d, None if f is None else to_dev(f, torch.uint8))
             wps.append(dec.row_wp[: wl.batch].cpu().numpy().copy())
             fls.append(dec.row_flush[: wl.batch].cpu().numpy().copy())
-        os_.append(o[sel].float().cpu().numpy().astype(np.float64))
+        os_.append(o[sel].float().cpu().numpy())
     torch.cuda.synchronize()
     return dict(o=os_, row_wp=np.array(wps), row_flush=np.array(fls), dec=dec)
 
@@ -206,7 +215,7 @@ def run_gpu_spec(wl, rounds=None, out_dtype=torch.float32, rows=None):
                      ver.slot_flush[cidx].cpu().numpy()))
         q, k, v, be, g = gdn_inputs_dev(wl, wl.round_inputs(r))
         o = ver.verify(q, k, v, be, g, ci_d)
-        outs.append(o[sel].float().cpu().numpy().astype(np.float64))
+        outs.append(o[sel].float().cpu().numpy())
         ver.commit(ci_d, to_dev(wl.accepted(r), torch.int32))
     curs.append((ver.slot_cnt[cidx].cpu().numpy(), ver.slot_base[cidx].cpu().numpy(),
                  ver.slot_flush[cidx].cpu().numpy()))
@@ -261,7 +270,7 @@ def run_gpu_kda(wl, steps=None, out_dtype=torch.float32, full_state=False, rows=
             o = run(q, k, v, be, a, ci_d, None if f is None else to_dev(f, torch.uint8))
             wps.append(dec.row_wp[: wl.batch].cpu().numpy().copy())
             fls.append(dec.row_flush[: wl.batch].cpu().numpy().copy())
-        os_.append(o[sel].float().cpu().numpy().astype(np.float64))
+        os_.append(o[sel].float().cpu().numpy())
     torch.cuda.synchronize()
     return dict(o=os_, row_wp=np.array(wps), row_flush=np.array(fls), dec=dec)
 
@@ -293,7 +302,7 @@ def run_gpu_m2spec(wl, rounds=None, out_dtype=torch.float32, rows=None):
         inp = wl.round_inputs(r)
         y = ver.verify(to_dev(inp["x"], ad), to_dev(inp["dt_raw"], torch.float32),
                        to_dev(inp["B"], ad), to_dev(inp["C"], ad), to_dev(inp["z"], ad), ci_d)
-        outs.append(y[sel].float().cpu().numpy().astype(np.float64))
+        outs.append(y[sel].float().cpu().numpy())
         ver.commit(ci_d, to_dev(wl.accepted(r), torch.int32))
     curs.append((ver.slot_cnt[cidx].cpu().numpy(), ver.slot_base[cidx].cpu().numpy(),
                  ver.slot_flush[cidx].cpu().numpy()))

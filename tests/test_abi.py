@@ -200,3 +200,15 @@ def test_stochastic_rounding_validation(lib):
     assert rc == B.RSSM_ERR_INVALID_ARG                             # misaligned generator state
     assert _rc("rssm_philox4x32_fill", 1, 2, None, 0, None) == B.RSSM_OK
     assert _rc("rssm_philox4x32_fill", 1, 2, None, 4, None) == B.RSSM_ERR_INVALID_ARG
+
+
+def test_debug_pipeline_copy_validation(lib):
+    f = "rssm_debug_pipeline_copy"
+    bad = ssm.RSSM_ERR_INVALID_ARG
+    assert _rc(f, FAKE, FAKE, -1, -1, 1000, None, None) == bad          # negative count
+    assert _rc(f, FAKE, FAKE, 4, 4, 1000, None, None) == bad            # stall tile out of range
+    assert _rc(f, FAKE, FAKE, 4, -1, 0, None, None) == bad              # wait limit too short
+    assert _rc(f, FAKE, FAKE, 4, -1, 2000001, None, None) == bad        # wait limit too long
+    assert _rc(f, None, FAKE, 4, -1, 1000, None, None) == bad           # null source
+    assert _rc(f, FAKE, FAKE + 4, 4, -1, 1000, None, None) == bad       # misaligned destination
+    assert _rc(f, FAKE, FAKE, 0, -1, 1000, None, None) == ssm.RSSM_OK   # nothing to copy

@@ -39,3 +39,32 @@ def test_byte_formulas_reduce_to_their_parts():
     base = bench.kda_output_bytes(k, zero, zero)
     assert bench.kda_output_bytes(k, zero, np.array([1, 1])) - base == 2 * 4 * 128 * 128 * 4
     assert bench.kda_step_bytes(k, zero, zero) > base
+
+
+def test_phase_complete_keeps_whole_cycles_of_in_region_samples():
+    import bench
+    # the last sample of each of 64 input sets, taken every 7th step: 64 consecutive
+    # multiples of 7, whose residues mod 16 cover every phase 4 times
+    ks = [7 * i for i in range(100, 164)]
+    per = [1.0 + 0.001 * k for k in ks]
+    got, src = bench._phase_complete(per, ks, None, None, 0, 0, 16, every=7)
+    assert len(got) == 64 and "in the timed region" in src
+    res = np.bincount(np.array([k for k, _ in got]) % 16, minlength=16)
+    assert np.all(res == 4)
+    # 40 samples: the last 32 are kept (two whole cycles)
+    got, _ = bench._phase_complete(per[:40], ks[:40], None, None, 0, 0, 16, every=7)
+    assert len(got) == 32 and [k for k, _ in got] == ks[8:40]
+    assert np.all(np.bincount(np.array([k for k, _ in got]) % 16, minlength=16) == 2)
+
+
+def test_source_hash_covers_the_included_headers():
+    import os
+
+    import bench
+    files = set()
+    bench._local_includes(os.path.join(bench.ROOT, "ssm_linear_attention_gb300", "csrc",
+                                       "gdn.cu"), files)
+    names = {os.path.basename(f) for f in files}
+    assert {"gdn.cu", "pipeline.cuh", "common.cuh", "internal.h", "rssm.h"} <= names
+    assert bench.source_hash("gdn.cu") != bench.source_hash("kda.cu")
+    assert bench.source_hash("gdn.cu") == bench.source_hash("gdn.cu")

@@ -33,22 +33,30 @@ def _gdn_cursor_ref(wl, steps):
     return np.array(wps), np.array(fls)
 
 
-def _check_gdn(wl, rows, steps, out_dtype=torch.float32):
+def _check_gdn(wl, rows, steps, out_dtype=torch.float32, chunk=128):
+    """Run the GPU path once for `rows`, then the oracle chunk by chunk of rows, and
+    compare every output of every step and every stored checkpoint."""
+    rows = np.asarray(rows)
     g = Hn.run_gpu_gdn(wl, steps=steps, out_dtype=out_dtype, rows=rows)
-    ref = oracle.gdn_run(wl, rows=rows, steps=steps, mode="replay")
     cw, cf = _gdn_cursor_ref(wl, steps)
     assert np.array_equal(g["row_wp"], cw) and np.array_equal(g["row_flush"], cf)
-    for t in range(steps):
-        if out_dtype == torch.bfloat16:
-            d = np.abs(g["o"][t] - ref["o"][t])
-            assert np.all(d <= TOL * np.maximum(1, np.abs(ref["o"][t])) + Hn.bf16_spacing(ref["o"][t]))
-        else:
-            e = Hn.err(g["o"][t], ref["o"][t])
-            assert e <= TOL, "step %d: o error %.3g" % (t, e)
     ci = wl.cache_indices()
-    st = g["dec"].state[torch.as_tensor(ci[rows].astype(np.int64), device="cuda")].cpu().numpy()
-    ok, e, _ = Hn.state_ok(st, ref["ckpt"], "fp32")
-    assert ok, "checkpoint error %.3g" % e
+    for c0, sub in Hn.row_chunks(rows, chunk):
+        ref = oracle.gdn_run(wl, rows=sub, steps=steps, mode="replay")
+        sl = slice(c0, c0 + len(sub))
+        for t in range(steps):
+            ro, go = ref["o"][t], g["o"][t][sl]
+            if out_dtype == torch.bfloat16:
+                d = np.abs(go - ro)
+                assert np.all(d <= TOL * np.maximum(1, np.abs(ro)) + Hn.bf16_spacing(ro)), \
+                    "step %d rows %d..: bf16 output off by more than tol + 1 spacing" % (t, c0)
+            else:
+                e = Hn.err(go, ro)
+                assert e <= TOL, "step %d rows %d..: o error %.3g" % (t, c0, e)
+        st = g["dec"].state[torch.as_tensor(ci[sub].astype(np.int64), device="cuda")].cpu().numpy()
+        ok, e, _ = Hn.state_ok(st, ref["ckpt"], "fp32")
+        assert ok, "rows %d..: checkpoint error %.3g" % (c0, e)
+        del ref, st
     assert int(g["dec"].dev_err.abs().sum()) == 0
 
 
@@ -58,15 +66,16 @@ def test_gdn_small_desync_with_forced_flushes():
     _check_gdn(wl, rows=np.arange(6), steps=14)
 
 
-def test_gdn_decode_config_sampled_rows():
-    # batch 256, HV 32, HK 16, K = V = 128, L 16, 64 steps, fp32 state N(0, 0.05)
+def test_gdn_decode_config_all_rows():
+    # batch 256, HV 32, HK 16, K = V = 128, L 16, 64 steps, fp32 state N(0, 0.05): every
+    # row's output at every step (four flushes per row) and every stored checkpoint
     wl = W.gdn_decode()
-    _check_gdn(wl, rows=[0, 77, 255], steps=wl.steps)
+    _check_gdn(wl, rows=np.arange(wl.batch), steps=wl.steps)
 
 
 def test_gdn_decode_bf16_output_desync():
     wl = W.gdn_decode(batch=64, num_slots=128, steps=20, wp_mode="uniform")
-    _check_gdn(wl, rows=[1, 40, 63], steps=20, out_dtype=torch.bfloat16)
+    _check_gdn(wl, rows=np.arange(wl.batch), steps=20, out_dtype=torch.bfloat16)
 
 
 @pytest.mark.parametrize("L", [1, 2, 8])
@@ -87,26 +96,34 @@ def test_gdn_full_state_kernel():
     assert Hn.state_ok(st, ref["ckpt"], "fp32")[0]
 
 
-def _check_spec(wl, rows, rounds):
+def _check_spec(wl, rows, rounds, chunk=128):
+    rows = np.asarray(rows)
     g = Hn.run_gpu_spec(wl, rounds=rounds, rows=rows)
-    ref = oracle.gdn_spec_run(wl, rows=rows, rounds=rounds)
     # cursors: bit-exact against the integer model for every row
     cnt, base, fl = [0] * wl.num_slots, [0] * wl.num_slots, [0] * wl.num_slots
     ci = wl.cache_indices()
+    folds = 0
     for r in range(rounds + 1):
         assert np.array_equal(g["cnt"][r], [cnt[s] for s in ci]), r
         assert np.array_equal(g["base"][r], [base[s] for s in ci]), r
         assert np.array_equal(g["flush"][r], [fl[s] for s in ci]), r
         if r < rounds:
+            folds += int(np.count_nonzero(g["flush"][r][rows]))
             cursors.spec_commit(cnt, base, fl, ci, wl.accepted(r), wl.L, wl.T)
+    # an exact fold ran for the compared rows, so the stored checkpoints were rewritten
+    assert folds > 0, "no fold among the compared rows"
     worst = 0.0
-    for r in range(rounds):
-        e = Hn.err(g["o"][r], ref["o"][r])
-        worst = max(worst, e)
-        assert e <= TOL, "round %d: draft output error %.3g" % (r, e)
-    st = g["ver"].state[torch.as_tensor(ci[rows].astype(np.int64), device="cuda")].cpu().numpy()
-    ok, e, _ = Hn.state_ok(st, ref["ckpt"], "fp32")
-    assert ok, "folded checkpoint error %.3g" % e
+    for c0, sub in Hn.row_chunks(rows, chunk):
+        ref = oracle.gdn_spec_run(wl, rows=sub, rounds=rounds)
+        sl = slice(c0, c0 + len(sub))
+        for r in range(rounds):
+            e = Hn.err(g["o"][r][sl], ref["o"][r])
+            worst = max(worst, e)
+            assert e <= TOL, "round %d rows %d..: draft output error %.3g" % (r, c0, e)
+        st = g["ver"].state[torch.as_tensor(ci[sub].astype(np.int64), device="cuda")].cpu().numpy()
+        ok, e, _ = Hn.state_ok(st, ref["ckpt"], "fp32")
+        assert ok, "rows %d..: folded checkpoint error %.3g" % (c0, e)
+        del ref, st
     assert int(g["ver"].dev_err.abs().sum()) == 0
     return worst
 
@@ -123,10 +140,11 @@ def test_spec_draft_lengths(T, L):
     _check_spec(wl, rows=np.arange(4), rounds=12)
 
 
-def test_spec_config_sampled_rows():
-    # batch 128, T 4, HV 32, HK 16, K = V = 128, L 16, 32 rounds, accepted ~ U{0..4}
+def test_spec_config_all_rows():
+    # batch 128, T 4, HV 32, HK 16, K = V = 128, L 16, 32 rounds, accepted ~ U{0..4}:
+    # every row's draft outputs in every round and every folded checkpoint
     wl = W.gdn_spec()
-    _check_spec(wl, rows=[0, 64, 127], rounds=wl.rounds)
+    _check_spec(wl, rows=np.arange(wl.batch), rounds=wl.rounds)
 
 
 def test_spec_rejects_short_ring():

@@ -20,23 +20,33 @@ def _gpu():
     ssm.lib()
 
 
-def _check(wl, rows=None):
+def _check(wl, rows=None, chunk=64):
     rows = np.arange(wl.batch) if rows is None else np.asarray(rows)
     g = Hn.run_gpu_m2spec(wl, rows=rows)
-    ref = oracle.mamba2_spec_run(wl, rows=rows)
     tol = Hn.tol_for(wl.state_dtype)
-    for r in range(wl.rounds):
-        e = Hn.err(g["y"][r], ref["y"][r])
-        assert e <= tol, (r, e)
-    assert np.array_equal(g["cnt"][:, rows], ref["cnt"])
-    assert np.array_equal(g["base"][:, rows], ref["base"])
-    assert np.array_equal(g["flush"][:, rows], ref["flush"])
+    ci_all = wl.cache_indices()
+    flips, n_el, folds = 0, 0, 0
+    for c0, sub in Hn.row_chunks(rows, chunk):
+        ref = oracle.mamba2_spec_run(wl, rows=sub)
+        sl = slice(c0, c0 + len(sub))
+        for r in range(wl.rounds):
+            e = Hn.err(g["y"][r][sl], ref["y"][r])
+            assert e <= tol, (r, c0, e)
+        assert np.array_equal(g["cnt"][:, sub], ref["cnt"])
+        assert np.array_equal(g["base"][:, sub], ref["base"])
+        assert np.array_equal(g["flush"][:, sub], ref["flush"])
+        folds += int(np.count_nonzero(ref["flush"][:-1]))
+        ci = ci_all[sub]
+        st = g["ver"].state[torch.as_tensor(ci.astype(np.int64), device="cuda")].float().cpu().numpy()
+        ok, e, fl = Hn.state_ok(st, ref["ckpt"], wl.state_dtype)
+        assert ok, (c0, e, fl)
+        flips += fl
+        n_el += st.size
+        del ref, st
     # at least one fold happened, so the stored checkpoints were rewritten
-    assert ref["flush"][:-1].any()
-    ci = wl.cache_indices()[rows]
-    st = g["ver"].state[torch.as_tensor(ci.astype(np.int64), device="cuda")].float().cpu().numpy()
-    ok, e, flips = Hn.state_ok(st, ref["ckpt"], wl.state_dtype)
-    assert ok, (e, flips)
+    assert folds > 0
+    if wl.state_dtype == "bf16":
+        assert flips / max(1, n_el) < 1e-3, flips / max(1, n_el)
     assert int(g["ver"].dev_err.abs().sum()) == 0
 
 
@@ -54,9 +64,11 @@ def test_mamba2_spec_fp32_activations_and_other_tile():
     _check(wl)
 
 
-def test_mamba2_spec_bench_geometry_sampled_rows():
-    wl = W.mamba2_spec(batch=128, num_slots=256, rounds=8)
-    _check(wl, rows=[0, 57, 127])
+def test_mamba2_spec_bench_geometry_all_rows():
+    # batch 128, T 4, H 128, P 64, N 128, G 8, L 16, bf16 state: every row's draft
+    # outputs in every round and every folded checkpoint
+    wl = W.mamba2_spec(batch=128, num_slots=256, rounds=12)
+    _check(wl)
 
 
 def test_mamba2_spec_padding_and_bad_slot():

@@ -120,6 +120,85 @@ def test_replay_flush_sr_matches_oracle():
     assert int(dec.sr[1].item()) == 3
 
 
+def _boundary_window(exact, bound, seed, offset, elems):
+    """For the listed pool elements: (distance of the float32 value of `exact` to the
+    stochastic-rounding decision boundary its random bits set, allowed distance).
+    Rounding goes away from zero iff (low 16 bits of the float32) + r >= 2^16, so the
+    boundary sits (low + r - 2^16) float32 spacings from the value; the allowed
+    distance is the float32 error of a fold of at most L + 2 fused terms of total
+    magnitude `bound`, plus the float32 rounding of the exact value itself."""
+    f = exact.astype(np.float32)
+    u = f.view(np.uint32).astype(np.int64)
+    lo = u & 0xFFFF
+    r = np.array([oracle.sr_bits(seed, offset, int(e)) for e in elems], dtype=np.int64)
+    ulp = np.spacing(np.abs(f)).astype(np.float64)
+    dist = np.abs(lo + r - 65536).astype(np.float64) * ulp
+    return dist, bound * 2.0 ** -24 + ulp
+
+
+def test_replay_flush_sr_multi_entry_fold_matches_oracle():
+    # Rows start with desynchronised write_pos w ~ U{0..7} (w history entries in the
+    # ring, none of them flushing) and every row is forced to flush at the next step, so
+    # each stored state is the stochastic rounding of a fold of w + 1 ring entries into
+    # the checkpoint. Each element must equal the oracle's rounding of the exact state
+    # with the same bits, or (where the float32 fold sits within its accumulation error
+    # of the decision boundary) the neighbouring bf16 value.
+    wl = W.mamba2_large(batch=32, nheads=8, ngroups=2, num_slots=64, L=8, steps=1)
+    hist = wl.history_len()
+    assert hist.max() >= 5 and np.count_nonzero(hist >= 1) >= 24
+    dec = Hn.make_mamba2_decoder(wl, sr_seed=SEED)
+    for j in range(wl.max_history()):
+        x, dt, Bm, C, z = Hn.mamba2_inputs_dev(wl, wl.history_inputs(j))
+        dec.step(x, dt, Bm, C, z, Hn.to_dev(wl.history_ci(j), torch.int32))
+    torch.cuda.synchronize()
+    off = int(dec.sr[1].item())
+    ci = wl.cache_indices()
+    ci_d = Hn.to_dev(ci, torch.int32)
+    force = torch.ones(wl.batch, device="cuda", dtype=torch.uint8)
+    x, dt, Bm, C, z = Hn.mamba2_inputs_dev(wl, wl.step_inputs(0))
+    dec.step(x, dt, Bm, C, z, ci_d, force)
+    torch.cuda.synchronize()
+    assert np.array_equal(dec.row_wp[: wl.batch].cpu().numpy(), hist)
+    assert int(dec.row_flush[: wl.batch].sum()) == wl.batch
+    gpu = _slots_state(dec, wl).astype(np.float64)
+
+    # oracle: the exact state after the history and the step (no rounding before the
+    # flush), rounded stochastically with the generator the flush launch used
+    prm = wl.params()
+    pool = _oracle_pool(wl)
+    mag = np.abs(pool)
+
+    def run(pool_, absolute):
+        for j in range(wl.max_history() + 1):
+            inp = wl.history_inputs(j) if j < wl.max_history() else wl.step_inputs(0)
+            c = wl.history_ci(j) if j < wl.max_history() else ci
+            xx = np.abs(inp["x"]) if absolute else inp["x"]
+            bb = np.abs(inp["B"]) if absolute else inp["B"]
+            oracle.mamba2_step(pool_, xx, inp["dt_raw"], prm["A"], bb, inp["C"], prm["D"],
+                               inp["z"], prm["dt_bias"], wl.dt_softplus, ci=c)
+
+    run(pool, False)
+    run(mag, True)   # sum of the magnitudes of every term of each element's fold
+    exact = pool[ci].copy()
+    ref = pool.copy()
+    oracle.round_slots_sr(ref, ci, SEED, off)
+    ref = ref[ci]
+    d = np.abs(gpu - ref)
+    diff = np.nonzero(d.ravel() > 0)[0]
+    frac = diff.size / gpu.size
+    assert frac <= 1e-3, frac
+    if diff.size:
+        per_slot = wl.nheads * wl.headdim * wl.dstate
+        row = diff // per_slot
+        elems = ci[row].astype(np.int64) * per_slot + diff % per_slot
+        sp = Hn.bf16_spacing(ref.ravel()[diff])
+        assert np.all(d.ravel()[diff] <= sp * 1.0000001), "a stored value is not a bf16 neighbour"
+        dist, allow = _boundary_window(exact.ravel()[diff], (wl.L + 2) * mag[ci].ravel()[diff],
+                                       SEED, off, elems)
+        assert np.all(dist <= allow), "a rounding decision differs away from its boundary"
+    assert int(dec.dev_err.abs().sum()) == 0
+
+
 def test_staged_output_sr_equals_fused_step_sr():
     wl = W.mamba2_large(batch=12, nheads=8, ngroups=2, num_slots=32, L=4, steps=1,
                         wp_mode="zero")
