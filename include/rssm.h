@@ -690,6 +690,20 @@ int rssm_gdn_materialize_state(const rssm_gdn_dims* dims, const float* state, co
                                const int32_t* slot_wp, const int32_t* slot_base, float* out,
                                int32_t* dev_err, rssm_stream_t stream);
 
+/* rssm_debug_umma_fold -- test / debug: the tensor-core building block of the flush
+ * folds on its own. D[r][c] = sum_{i<=w} A[r][i] B[i][c] for r < 128, c < N
+ * (N = 64 or 128), computed by the 5th-generation tensor cores (tcgen05.mma, the
+ * accumulator in tensor memory): A is float32 [128][16] (device, caller owned;
+ * entries i > w ignored), split into three bf16 parts whose sum carries its 24-bit
+ * significand; B is bf16 [16][N] in the ring layout (entry-major; entries i > w
+ * ignored); D float32 [128][N]. 0 <= w < 16. One CTA of 128 threads. The pages have
+ * no counterpart: it pins the operand layouts the decode kernels' folds use (the
+ * fold itself is the flush of [M2] 实现拆解 item 1 and [GDN] 实现拆解 item 1).
+ * Errors: RSSM_ERR_INVALID_ARG (w or N out of range, null or misaligned pointers),
+ * RSSM_ERR_CUDA; a completion wait that runs out sets RSSM_DEVERR_TIMEOUT. */
+int rssm_debug_umma_fold(const float* A, const uint16_t* B, int w, int N, float* D,
+                         int32_t* dev_err, rssm_stream_t stream);
+
 /* rssm_debug_pipeline_copy -- test / debug: exercises the bounded waits of the
  * streaming pipeline every decode kernel runs on. Copies n_tiles tiles of 16 KB
  * from src to dst (float32, device, caller owned, 16-byte aligned) through that

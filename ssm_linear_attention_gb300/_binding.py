@@ -34,7 +34,7 @@ EXPORTS = (
     "rssm_gdn_spec_full_state_snapshot_bytes", "rssm_gdn_spec_full_state_verify",
     "rssm_gdn_spec_full_state_commit", "rssm_kda_workspace_size", "rssm_kda_prepare",
     "rssm_kda_output", "rssm_kda_step", "rssm_kda_full_state_decode",
-    "rssm_debug_pipeline_copy",
+    "rssm_debug_pipeline_copy", "rssm_debug_umma_fold",
 )
 
 
@@ -138,6 +138,7 @@ def _declare(L):
         "rssm_gdn_spec_verify": (_I, [gd, _I32, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP, _VP,
                                       _VP, _VP, _VP, _VP, _VP, _VP, _SZ, _VP, _VP, _VP]),
         "rssm_debug_pipeline_copy": (_I, [_VP, _VP, _I, _I, _I, _VP, _VP]),
+        "rssm_debug_umma_fold": (_I, [_VP, _VP, _I, _I, _VP, _VP, _VP]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)
@@ -326,6 +327,13 @@ def rssm_debug_pipeline_copy(src, dst, n_tiles, stall_tile, wait_us, dev_err=Non
     makes that tile's stage wait run out after wait_us (test of the bounded waits)."""
     _call("rssm_debug_pipeline_copy", _ptr(src), _ptr(dst), int(n_tiles), int(stall_tile),
           int(wait_us), _ptr(dev_err), _stream(stream))
+
+
+def rssm_debug_umma_fold(A, B, w, N, D, dev_err=None, stream=None):
+    """D [128][N] = A[:, :w+1] @ B[:w+1] on the tensor cores (A float32 [128][16], B bf16
+    [16][N]); test of the fold building block."""
+    _call("rssm_debug_umma_fold", _ptr(A), _ptr(B), int(w), int(N), _ptr(D), _ptr(dev_err),
+          _stream(stream))
 
 
 def rssm_gdn_ring_append(dims, k, g, cache_indices, row_wp, ring_k, ring_g, dev_err=None,

@@ -212,3 +212,13 @@ def test_debug_pipeline_copy_validation(lib):
     assert _rc(f, None, FAKE, 4, -1, 1000, None, None) == bad           # null source
     assert _rc(f, FAKE, FAKE + 4, 4, -1, 1000, None, None) == bad       # misaligned destination
     assert _rc(f, FAKE, FAKE, 0, -1, 1000, None, None) == ssm.RSSM_OK   # nothing to copy
+
+
+def test_debug_umma_fold_validation(lib):
+    f = "rssm_debug_umma_fold"
+    bad = ssm.RSSM_ERR_INVALID_ARG
+    assert _rc(f, FAKE, FAKE, 16, 128, FAKE, None, None) == bad     # w beyond the 16 entries
+    assert _rc(f, FAKE, FAKE, -1, 128, FAKE, None, None) == bad
+    assert _rc(f, FAKE, FAKE, 3, 96, FAKE, None, None) == bad       # N not 64 or 128
+    assert _rc(f, None, FAKE, 3, 64, FAKE, None, None) == bad
+    assert _rc(f, FAKE, FAKE, 3, 64, FAKE + 8, None, None) == bad   # misaligned D
