@@ -215,8 +215,12 @@ int rssm_ring_append(const rssm_mamba2_dims* dims, const void* x, const float* d
                      const int32_t* cache_indices, const int32_t* row_wp, void* ring_x,
                      float* ring_dt, void* ring_B, int32_t* dev_err, rssm_stream_t stream);
 
-/* Bytes of device workspace rssm_mamba2_precompute / rssm_mamba2_decode need
- * (per-(row, head) coefficient tables, float32). 0 for an invalid dims. */
+/* Bytes of device workspace rssm_mamba2_precompute / rssm_mamba2_decode need: the
+ * per-(row, head) coefficient tables, float32 (batch * nheads * round4(2L + 1) * 4
+ * bytes), then, at the next 256-byte boundary, 256 bytes for the output kernel's work
+ * counter (the table-building launches zero it every step; the output launch claims
+ * its tiles from it and leaves it at zero). A workspace serves one stream at a time.
+ * 0 for an invalid dims. */
 size_t rssm_mamba2_workspace_size(const rssm_mamba2_dims* dims);
 
 /* rssm_mamba2_precompute -- per-row scalar tables for the output kernel ([M2]
@@ -379,9 +383,10 @@ int rssm_mamba2_spec_verify(const rssm_mamba2_dims* dims, int32_t T, void* state
  * RSSM_NOALLOC_WORKSPACE_BYTES (16 MiB) inside the library's device image, held
  * by every GPU that loads the library until the process exits. It allocates
  * nothing and calls no allocating routine.
- *   - Limit: rssm_mamba2_workspace_size(dims) must not exceed the array
- *     (batch * nheads * round4(2L + 1) * 4 bytes; batch 512 x 128 heads at L = 16
- *     needs 9 MiB); larger sizes return RSSM_ERR_UNSUPPORTED before any launch.
+ *   - Limit: rssm_mamba2_workspace_size(dims) must not exceed the array (the
+ *     tables, batch * nheads * round4(2L + 1) * 4 bytes, plus 256 bytes rounded;
+ *     batch 512 x 128 heads at L = 16 needs 9 MiB); larger sizes return
+ *     RSSM_ERR_UNSUPPORTED before any launch.
  *   - Set-up: the first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call before
  *     any stream capture. A failed look-up returns RSSM_ERR_CUDA and is not cached:

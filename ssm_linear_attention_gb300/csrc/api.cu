@@ -82,13 +82,13 @@ bool ensure_smem_limit(const void* kernel, int bytes) {
 }
 
 bool pick_pipe(const DeviceInfo& di, int stage_bytes, int warp_scratch, int tile_bytes, int header,
-               int max_stages, int group_warps, int max_groups, PipeCfg* out) {
+               int max_stages, int group_warps, int max_groups, PipeCfg* out, int align) {
     const int budget = di.max_smem_optin;
     int want = (65536 + tile_bytes - 1) / tile_bytes;
     if (want < 2) want = 2;
     for (int ng = max_groups; ng >= 1; --ng) {
         const int scratch_off = header;
-        const int stage_off = (scratch_off + ng * group_warps * warp_scratch + 127) & ~127;
+        const int stage_off = (scratch_off + ng * group_warps * warp_scratch + align - 1) / align * align;
         int stages = (budget - stage_off) / stage_bytes;
         if (stages > max_stages) stages = max_stages;
         stages -= stages % ng;  // each stage always belongs to the same group
@@ -103,6 +103,40 @@ bool pick_pipe(const DeviceInfo& di, int stage_bytes, int warp_scratch, int tile
         }
     }
     return false;
+}
+
+namespace {
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                  CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                  CUtensorMapFloatOOBfill);
+std::once_flag g_encode_once;
+EncodeTiledFn g_encode = nullptr;
+}  // namespace
+
+bool make_tmap_rows128(CUtensorMap* out, const void* base, int elem_bytes, uint64_t rows,
+                       uint64_t cols, uint32_t box_rows) {
+    std::call_once(g_encode_once, []() {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<EncodeTiledFn>(f);
+        else
+            cudaGetLastError();  // this lookup's own error
+    });
+    if (!g_encode || (elem_bytes != 2 && elem_bytes != 4)) return false;
+    const cuuint64_t dims[2] = {cols, rows};
+    const cuuint64_t strides[1] = {cols * (cuuint64_t)elem_bytes};
+    const cuuint32_t box[2] = {(cuuint32_t)(128 / elem_bytes), box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUresult r = g_encode(out, elem_bytes == 2 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                                     : CU_TENSOR_MAP_DATA_TYPE_FLOAT32,
+                                2, const_cast<void*>(base), dims, strides, box, estr,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
 }
 
 // ----------------------------------------------------------------------------

@@ -113,6 +113,47 @@ __device__ __forceinline__ void bulk_g2s_hint(void* dst, const void* src, uint32
         : "memory");
 }
 
+// 2-D TMA tensor copy global -> shared of one box at element coordinates (x, y) of
+// the tensor map `tmap` (a __grid_constant__ kernel parameter), completion counted
+// on `bar`. x times the element size is a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int x, int y, uint64_t* bar,
+                                            uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint "
+        "[%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
+        "l"(tmap), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+// 2-D TMA tensor copy shared -> global of one box at (x, y) (x, y >= 0), in this
+// thread's bulk group.
+__device__ __forceinline__ void tma_store_2d(const void* tmap, int x, int y, const void* src) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(
+                     tmap),
+                 "r"(x), "r"(y), "r"(smem_addr(src))
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+
+// Wait until this thread's committed bulk stores have finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
+// Make this thread's generic-proxy shared-memory stores visible to the async proxy
+// (TMA stores and tensor-core operand reads go through it).
+__device__ __forceinline__ void fence_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_count(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(count)
+                 : "memory");
+}
+
 __device__ __forceinline__ void set_dev_err(int32_t* dev_err, int bit) {
     if (dev_err) atomicOr(dev_err, bit);
 }
@@ -230,11 +271,11 @@ __device__ __forceinline__ uint16_t f_to_bf16_sr(float f, uint32_t r) {
     return static_cast<uint16_t>((u + (r & 0xFFFFu)) >> 16);
 }
 
-// Store 8 float32 values as bfloat16 at p (16-byte aligned) with stochastic
-// rounding; the random bits are Philox4x32-10 at counter (group, offset), key seed,
-// where group numbers the 8-element groups of the destination array.
-__device__ __forceinline__ void store8_bf16_sr(void* p, const float* f, uint64_t group,
-                                               uint64_t seed, uint64_t offset) {
+// 8 float32 values as bfloat16 with stochastic rounding; the random bits are
+// Philox4x32-10 at counter (group, offset), key seed, where group numbers the
+// 8-element groups of the destination array.
+__device__ __forceinline__ uint4 pack8_bf16_sr(const float* f, uint64_t group, uint64_t seed,
+                                               uint64_t offset) {
     const uint4 r = philox4x32_10(
         make_uint4((uint32_t)group, (uint32_t)(group >> 32), (uint32_t)offset, (uint32_t)(offset >> 32)),
         make_uint2((uint32_t)seed, (uint32_t)(seed >> 32)));
@@ -244,7 +285,14 @@ __device__ __forceinline__ void store8_bf16_sr(void* p, const float* f, uint64_t
 #pragma unroll
     for (int i = 0; i < 4; ++i)
         o[i] = uint32_t(f_to_bf16_sr(f[2 * i], w[i])) | (uint32_t(f_to_bf16_sr(f[2 * i + 1], w[i] >> 16)) << 16);
-    *reinterpret_cast<uint4*>(p) = v;
+    return v;
+}
+
+// Store 8 float32 values as bfloat16 at p (16-byte aligned) with stochastic rounding
+// (bits as pack8_bf16_sr).
+__device__ __forceinline__ void store8_bf16_sr(void* p, const float* f, uint64_t group,
+                                               uint64_t seed, uint64_t offset) {
+    *reinterpret_cast<uint4*>(p) = pack8_bf16_sr(f, group, seed, offset);
 }
 
 // State element types for templated kernels (sr: stores round stochastically).

@@ -3,6 +3,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>  // CUtensorMap and its enums only: the driver is reached through the runtime
 #include <cuda_runtime.h>
 
 #include "rssm.h"
@@ -46,6 +47,15 @@ struct PipeCfg {
     int scratch_off;
 };
 bool pick_pipe(const DeviceInfo& di, int stage_bytes, int warp_scratch, int tile_bytes, int header,
-               int max_stages, int group_warps, int max_groups, PipeCfg* out);
+               int max_stages, int group_warps, int max_groups, PipeCfg* out, int align = 128);
+
+// A 2-D tensor map over a row-major matrix of `rows` x `cols` elements of
+// `elem_bytes` (2: bf16, 4: fp32) at `base` (16-byte aligned, rows of cols *
+// elem_bytes bytes, a multiple of 16), copied in boxes of box_rows x (128 /
+// elem_bytes) elements -- one 128-byte row segment per box row -- with the 128-byte
+// shared-memory swizzle (16-byte chunk j of box row r lands at chunk j ^ (r % 8)).
+// false when the driver offers no encoder or rejects the arguments.
+bool make_tmap_rows128(CUtensorMap* out, const void* base, int elem_bytes, uint64_t rows,
+                       uint64_t cols, uint32_t box_rows);
 
 }  // namespace rssm

@@ -79,11 +79,77 @@ __device__ __forceinline__ ulonglong2 load_generator(const uint64_t* sr) {
     else return make_ulonglong2(0, 0);
 }
 
+// ----------------------------------------------------------------------------
+// output / flush kernel
+// ----------------------------------------------------------------------------
+//
+// The producer copies a (row, head) checkpoint tile with 2-D TMA tensor copies and
+// the 128-byte shared-memory swizzle: the tile is N * SS / 128 boxes of [P rows][128
+// bytes], and row p's 16-byte chunk c lies at (c / 8) * P * 128 + p * 128 + 16 ((c % 8)
+// ^ (p % 8)). The lanes of a quarter-warp then hit different banks both when they
+// read different chunks of one row (the y dot products: 16 lanes per row) and when
+// they read the same chunk of different rows (the flush: one row per lane).
+// Tiles are claimed dynamically from a counter in the workspace: a flush tile costs
+// several plain tiles, and with a static share the groups that drew more of them set
+// the launch time.
+//
+// Flush rows fold the ring into the tile and write it back in place -- lane l of
+// consumer warp wi owns tile row(s) p = 32 wi + l (+ 64), same swizzle -- and one
+// thread stores the tile with TMA tensor stores. The fold is the product of
+// A[p][i] = a_i x_i[p] and the ring's B entries:
+//   * TC (64 x 128 tiles, bf16 ring, w + 1 <= 16): on the tensor cores. Each lane
+//     writes Pm1 S0 of its row into its TMEM lane of the group's 128 accumulator
+//     columns (M = 128: the group's 64 rows are the TMEM lanes its two warps may read,
+//     64 (g % 2) .. +63; the other 64 rows are unused), the group stages A (float32,
+//     three bf16 parts along K) and B^T in its scratch, one thread issues three
+//     tcgen05.mma of K = 16 accumulating onto it, and each lane reads its row back.
+//     Scratch of a pair of groups (4 warps x kTcWarpScratch):
+//       [B^T of the even group][A of both groups: 16 row blocks x 768 B][B^T of odd]
+//     so both groups' A descriptors start at the same address.
+//   * otherwise on CUDA cores, per lane in blocks of 32 columns.
 template <int P, int N, class ST>
+struct RowTile {
+    static constexpr int SS = ST::bytes;
+    static constexpr int TILE = P * N * SS;
+    static constexpr int BOXC = 128 / SS;   // columns per 128-byte box row
+    static constexpr int NBOX = N / BOXC;   // boxes per tile
+    static constexpr int BOXB = P * 128;    // bytes per box
+    static constexpr int CH = N * SS / 16;  // 16-byte chunks per row
+    static constexpr int EPC = 16 / SS;     // elements per chunk
+    static constexpr int RPL = P / 64;      // rows per lane (two warps of 32 lanes)
+    static_assert(N % BOXC == 0 && P % 64 == 0, "tile shape");
+    static __device__ __forceinline__ uint32_t off(int p, int c) {
+        return (uint32_t)(c >> 3) * BOXB + (uint32_t)p * 128u + ((uint32_t)((c & 7) ^ (p & 7)) << 4);
+    }
+};
+
+constexpr int kTcWarpScratch = 5120;
+constexpr int kTcBT = 4096;            // B^T: 128 rows x 16 entries, bf16, core matrices
+constexpr int kTcA = 16 * 768;         // A: 128 rows x 48 (3 parts x 16 entries), bf16
+constexpr uint32_t kTcALbo = 128, kTcASbo = 768, kTcBLbo = 128, kTcBSbo = 256;
+constexpr int kTcMaxEntries = 16;
+
+// The EPC elements of a 16-byte state chunk as float32.
+template <class ST>
+__device__ __forceinline__ void load_chunk(const uint8_t* p, float* f) {
+    if constexpr (ST::bf16) {
+        load8(p, true, f);
+    } else {
+        const float4 v = *reinterpret_cast<const float4*>(p);
+        f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
+    }
+}
+
+template <int P, int N, class ST, bool TC = false>
 struct OutPolicy {
-    using Sh = TileShape<P, N, ST>;
+    using Rt = RowTile<P, N, ST>;
     static constexpr int kGroup = kGroupWarps;
+    static constexpr int kTmemCols = TC ? 512 : 0;  // 128 accumulator columns per group
+    static constexpr bool kUsesCtx = true;
+    static constexpr bool kDynamic = true;  // tiles are claimed from a counter (flush tiles cost more)
+    static_assert(!TC || (P == 64 && N == 128), "the tensor-core fold takes 64 x 128 tiles");
     struct Args {
+        CUtensorMap tmap;  // the state pool as [slots * H * P rows][N], boxes of P x 128 bytes
         void* state;
         const void* C;
         const float* D;
@@ -97,6 +163,7 @@ struct OutPolicy {
         void* y;
         int32_t* dev_err;
         const uint64_t* sr;  // {seed, offset}: stochastic rounding of a bf16 state; null: nearest
+        unsigned int* sched; // the work counter (workspace, after the tables)
         int batch, H, G, L, num_slots, act_bf16, out_bf16;
         int stages, stage_bytes, stage_off, scratch_off, warp_scratch;
         int off_x, off_C, off_z, off_tbl, off_B;
@@ -138,9 +205,11 @@ struct OutPolicy {
         const int TBL = tbl_floats(a.L);
         const uint32_t xbytes = (m.w + 1) * P * sa;
         const uint32_t bbytes = m.f ? (m.w + 1) * N * sa : 0;
-        mbar_arrive_expect_tx(full, Sh::TILE + xbytes + N * sa + (a.z ? P * sa : 0) + TBL * 4 + bbytes);
-        bulk_g2s_hint(sb, static_cast<const char*>(a.state) + ((size_t)m.s * a.H + h) * Sh::TILE,
-                      Sh::TILE, full, pol);
+        mbar_arrive_expect_tx(full, Rt::TILE + xbytes + N * sa + (a.z ? P * sa : 0) + TBL * 4 + bbytes);
+        const int row0 = (m.s * a.H + h) * P;
+#pragma unroll
+        for (int bx = 0; bx < Rt::NBOX; ++bx)
+            tma_load_2d(sb + bx * Rt::BOXB, &a.tmap, bx * Rt::BOXC, row0, full, pol);
         bulk_g2s(sb + a.off_x,
                  static_cast<const char*>(a.ring_x) + ((size_t)m.s * a.H + h) * a.L * P * sa, xbytes,
                  full);
@@ -150,39 +219,51 @@ struct OutPolicy {
             bulk_g2s(sb + a.off_z, static_cast<const char*>(a.z) + ((size_t)b * a.H + h) * P * sa,
                      P * sa, full);
         bulk_g2s(sb + a.off_tbl, a.ws + ((size_t)b * a.H + h) * TBL, TBL * 4, full);
-        if (m.f)
+        if (bbytes)
             bulk_g2s(sb + a.off_B,
                      static_cast<const char*>(a.ring_B) + ((size_t)m.s * a.G + g) * a.L * N * sa,
                      bbytes, full);
     }
 
-    static __device__ void consume(const Args& a, int, const Meta& m, const uint8_t* sb, uint8_t*,
-                                   int lane, int wi) {
+    static __device__ void consume(const Args& a, int, const Meta& m, const uint8_t* sb,
+                                   uint8_t* scratch, int lane, int wi, PipeCtx& ctx) {
         if (!m.valid) return;
         const bool bf = a.act_bf16;
-        const int sa = bf ? 2 : 4;
         const int L = a.L, w = m.w;
-        const int q = lane % Sh::NQ, hr = lane / Sh::NQ;
-        const int row0 = wi * Sh::PW + hr;  // this lane's rows: row0 + RPI * t
         const float* tbl = reinterpret_cast<const float*>(sb + a.off_tbl);
         const uint8_t* xr = sb + a.off_x;
+        const uint8_t* Cs = sb + a.off_C;
+        const float Pm1 = tbl[2 * L];
+        const float Dh = __ldg(a.D + m.h);
+        // y: 16 lanes (N = 128) share a row, each reading one 16-byte chunk of it (8
+        // columns; two chunks for a float32 state) of RPI rows per load; the dot
+        // products reduce across a row's lanes with reduce-scatters, after which every
+        // lane holds whole results for NCH rows. The chunks a quarter-warp reads lie in
+        // different banks under the swizzle.
+        using Sh = TileShape<P, N, ST>;
+        const int q = lane % Sh::NQ, hr = lane / Sh::NQ;
+        const int row0 = wi * Sh::PW + hr;  // this lane's rows: row0 + RPI * t
         float part[Sh::ITER];
         if (ST::bf16 && bf) {
-            const uint4 cpk = *reinterpret_cast<const uint4*>(sb + a.off_C + q * 16);
+            const uint4 cpk = *reinterpret_cast<const uint4*>(Cs + q * 16);
 #pragma unroll
             for (int t = 0; t < Sh::ITER; ++t) {
-                const int p = row0 + Sh::RPI * t;
-                const uint4 s8 = *reinterpret_cast<const uint4*>(sb + ((size_t)p * N + q * 8) * Sh::SS);
+                const uint4 s8 = *reinterpret_cast<const uint4*>(sb + Rt::off(row0 + Sh::RPI * t, q));
                 part[t] = dot8_bf16(s8, cpk, 0.f);
             }
         } else {
             float c[8];
-            load8(sb + a.off_C + q * 8 * sa, bf, c);
+            load8(Cs + q * 8 * (bf ? 2 : 4), bf, c);
 #pragma unroll
             for (int t = 0; t < Sh::ITER; ++t) {
                 const int p = row0 + Sh::RPI * t;
                 float s8[8];
-                load8(sb + ((size_t)p * N + q * 8) * Sh::SS, ST::bf16, s8);
+                if constexpr (ST::bf16) {
+                    load8(sb + Rt::off(p, q), true, s8);
+                } else {
+                    load_chunk<ST>(sb + Rt::off(p, 2 * q), s8);
+                    load_chunk<ST>(sb + Rt::off(p, 2 * q + 1), s8 + 4);
+                }
                 float acc = s8[0] * c[0];
 #pragma unroll
                 for (int j = 1; j < 8; ++j) acc = fmaf(s8[j], c[j], acc);
@@ -191,69 +272,245 @@ struct OutPolicy {
         }
 #pragma unroll
         for (int ch = 0; ch < Sh::NCH; ++ch) reduce_scatter<Sh::NQ, Sh::NQ>(part + ch * Sh::NQ);
-        const float Pm1 = tbl[2 * L];
-        const float Dh = __ldg(a.D + m.h);
 #pragma unroll
         for (int ch = 0; ch < Sh::NCH; ++ch) {
             const int p = row0 + Sh::RPI * (ch * Sh::NQ + q);
-            float acc = Pm1 * part[ch * Sh::NQ];
-            float acc2 = 0.f;
+            float yv = Pm1 * part[ch * Sh::NQ];
+            float y2 = 0.f;
             int i = 0;
 #pragma unroll 1
             for (; i + 1 <= w; i += 2) {
-                acc = fmaf(tbl[i], load1(xr, i * P + p, bf), acc);
-                acc2 = fmaf(tbl[i + 1], load1(xr, (i + 1) * P + p, bf), acc2);
+                yv = fmaf(tbl[i], load1(xr, i * P + p, bf), yv);
+                y2 = fmaf(tbl[i + 1], load1(xr, (i + 1) * P + p, bf), y2);
             }
-            if (i == w) acc = fmaf(tbl[w], load1(xr, w * P + p, bf), acc);
-            acc += acc2;
-            acc = fmaf(Dh, load1(xr, w * P + p, bf), acc);
-            if (a.z) acc *= silu_f(load1(sb + a.off_z, p, bf));
-            store1(a.y, ((size_t)m.b * a.H + m.h) * P + p, a.out_bf16, acc);
+            if (i == w) yv = fmaf(tbl[w], load1(xr, w * P + p, bf), yv);
+            yv += y2;
+            yv = fmaf(Dh, load1(xr, w * P + p, bf), yv);
+            if (a.z) yv *= silu_f(load1(sb + a.off_z, p, bf));
+            store1(a.y, ((size_t)m.b * a.H + m.h) * P + p, a.out_bf16, yv);
         }
-        if (m.f) {
-            // S = Pm1 * S0 + sum_{i<=w} a_i x_i B_i^T, stored rounded to the state dtype
-            const uint8_t* br = sb + a.off_B;
-            const float* av = tbl + L;
-            const size_t tile_e = ((size_t)m.s * a.H + m.h) * P * N;  // first element of the tile
-            const ulonglong2 gen = load_generator<ST>(a.sr);
-            constexpr int RC = Sh::ITER < 8 ? Sh::ITER : 8;
+        if (!m.f) return;
+        if constexpr (TC) fold_tc(a, m, const_cast<uint8_t*>(sb), scratch, lane, wi, ctx, tbl);
+        else fold_fma(a, m, const_cast<uint8_t*>(sb), lane, wi, tbl);
+        store_tile(a, m, sb, lane, wi, ctx);
+    }
+
+    // S[p][:] = Pm1 S0[p][:] + sum_{i<=w} (a_i x_i[p]) B_i[:] on CUDA cores, written back
+    // over S0 in the stage (each lane its own rows), rounded to the state dtype.
+    static __device__ void fold_fma(const Args& a, const Meta& m, uint8_t* sb, int lane, int wi,
+                                    const float* tbl) {
+        const bool bf = a.act_bf16;
+        const int sa = bf ? 2 : 4;
+        const int L = a.L, w = m.w;
+        const float Pm1 = tbl[2 * L];
+        const float* av = tbl + L;
+        const uint8_t* xr = sb + a.off_x;
+        const uint8_t* br = sb + a.off_B;
+        const size_t tile_e = ((size_t)m.s * a.H + m.h) * P * N;
+        const ulonglong2 gen = load_generator<ST>(a.sr);
+        constexpr int CPB = 32 / Rt::EPC;  // chunks per block of 32 columns
 #pragma unroll 1
-            for (int t0 = 0; t0 < Sh::ITER; t0 += RC) {
-                // column pairs (2k, 2k+1) accumulate with packed two-wide FMAs
-                float2 acc[RC][4];
+        for (int rr = 0; rr < Rt::RPL; ++rr) {
+            const int p = 32 * wi + lane + 64 * rr;
+#pragma unroll 1
+            for (int cb = 0; cb < N / 32; ++cb) {
+                float2 acc[16];
 #pragma unroll
-                for (int r = 0; r < RC; ++r) {
-                    const int p = row0 + Sh::RPI * (t0 + r);
-                    float s8[8];
-                    load8(sb + ((size_t)p * N + q * 8) * Sh::SS, ST::bf16, s8);
+                for (int k = 0; k < CPB; ++k) {
+                    float e[Rt::EPC];
+                    load_chunk<ST>(sb + Rt::off(p, cb * CPB + k), e);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) acc[r][k] = make_float2(Pm1 * s8[2 * k], Pm1 * s8[2 * k + 1]);
+                    for (int j = 0; j < Rt::EPC / 2; ++j)
+                        acc[k * Rt::EPC / 2 + j] = make_float2(Pm1 * e[2 * j], Pm1 * e[2 * j + 1]);
                 }
                 for (int i = 0; i <= w; ++i) {
-                    float bi[8];
-                    load8(br + ((size_t)i * N + q * 8) * sa, bf, bi);
-                    const float2 b2[4] = {make_float2(bi[0], bi[1]), make_float2(bi[2], bi[3]),
-                                          make_float2(bi[4], bi[5]), make_float2(bi[6], bi[7])};
-                    const float ai = av[i];
+                    const float ax = av[i] * load1(xr, i * P + p, bf);
+                    const float2 ax2 = make_float2(ax, ax);
 #pragma unroll
-                    for (int r = 0; r < RC; ++r) {
-                        const int p = row0 + Sh::RPI * (t0 + r);
-                        const float ax = ai * load1(xr, i * P + p, bf);
-                        const float2 ax2 = make_float2(ax, ax);
+                    for (int k = 0; k < 4; ++k) {
+                        float b8[8];
+                        load8(br + ((size_t)i * N + 32 * cb + 8 * k) * sa, bf, b8);
 #pragma unroll
-                        for (int k = 0; k < 4; ++k) acc[r][k] = __ffma2_rn(ax2, b2[k], acc[r][k]);
+                        for (int j = 0; j < 4; ++j)
+                            acc[4 * k + j] = __ffma2_rn(ax2, make_float2(b8[2 * j], b8[2 * j + 1]),
+                                                        acc[4 * k + j]);
                     }
                 }
+                const float* f = reinterpret_cast<const float*>(acc);
 #pragma unroll
-                for (int r = 0; r < RC; ++r) {
-                    const int p = row0 + Sh::RPI * (t0 + r);
-                    store_state8<ST>(static_cast<char*>(a.state), tile_e + (size_t)p * N + q * 8,
-                                     reinterpret_cast<const float*>(acc[r]), gen);
-                }
+                for (int k = 0; k < CPB; ++k)
+                    pack_chunk(sb + Rt::off(p, cb * CPB + k), f + k * Rt::EPC,
+                               tile_e + (size_t)p * N + 32 * cb + k * Rt::EPC, gen);
             }
         }
     }
+
+    // One 16-byte chunk of a state row, rounded to the state dtype (stochastically for
+    // StBF16SR, with the bits of the chunk's pool element index e), into the stage.
+    static __device__ __forceinline__ void pack_chunk(uint8_t* dst, const float* f, size_t e,
+                                                      ulonglong2 gen) {
+        if constexpr (ST::bf16) {
+            if constexpr (ST::sr) *reinterpret_cast<uint4*>(dst) = pack8_bf16_sr(f, e >> 3, gen.x, gen.y);
+            else *reinterpret_cast<uint4*>(dst) = make_uint4(pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                                                             pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+        } else {
+            *reinterpret_cast<float4*>(dst) = make_float4(f[0], f[1], f[2], f[3]);
+        }
+    }
+
+    static __device__ void fold_tc(const Args& a, const Meta& m, uint8_t* sb, uint8_t* scratch,
+                                   int lane, int wi, PipeCtx& ctx, const float* tbl);
+
+    // The folded tile (in the stage, written by both warps) to the pool with TMA tensor
+    // stores; the issuing thread waits until they have read the stage and releases it
+    // for both warps. The hand-over is a bounded mbarrier wait (not bar.sync), so a
+    // group whose other warp left the loop on an abort cannot wait forever.
+    // Warp 1 waits until the issuing thread has taken the hand-over ("taken" barrier),
+    // so it can never arrive twice in one phase of the hand-over barrier.
+    static __device__ void store_tile(const Args& a, const Meta& m, const uint8_t* sb, int lane, int wi,
+                                      PipeCtx& ctx) {
+        fence_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_plain(ctx.grp_bar);
+        if (wi == 0 && lane == 0) {
+            const bool ok = mbar_wait_bounded(ctx.grp_bar, ctx.grp_phase);
+            if (ok) {
+                const int row0 = (m.s * a.H + m.h) * P;
+#pragma unroll
+                for (int bx = 0; bx < Rt::NBOX; ++bx)
+                    tma_store_2d(&a.tmap, bx * Rt::BOXC, row0, sb + bx * Rt::BOXB);
+                bulk_commit();
+            } else {
+                *ctx.abort_flag = 1;
+                set_dev_err(a.dev_err, RSSM_DEVERR_TIMEOUT);
+            }
+            mbar_arrive_plain(ctx.done_bar);
+            if (ok) bulk_wait_read_all();
+            mbar_arrive_count(ctx.empty_bar, kGroupWarps);  // the stage, for both warps
+        }
+        if (wi != 0 && !mbar_wait_bounded(ctx.done_bar, ctx.done_phase) && lane == 0) {
+            *ctx.abort_flag = 1;
+            set_dev_err(a.dev_err, RSSM_DEVERR_TIMEOUT);
+        }
+        ctx.grp_phase ^= 1;
+        ctx.done_phase ^= 1;
+        ctx.released = true;
+    }
 };
+
+template <int P, int N, class ST, bool TC>
+__device__ void OutPolicy<P, N, ST, TC>::fold_tc(const Args& a, const Meta& m, uint8_t* sb,
+                                                 uint8_t* scratch, int lane, int wi, PipeCtx& ctx,
+                                                 const float* tbl) {
+    if constexpr (TC) {
+        const int L = a.L, w = m.w;
+        const int g = ctx.group;
+        const int p = 32 * wi + lane;                  // this lane's tile row
+        const int t = p;
+        const uint32_t dcol = ctx.tmem + 128u * g;     // the group's accumulator columns
+        const uint32_t lanes = (uint32_t)(64 * (g & 1) + 32 * wi) << 16;  // this warp's TMEM lanes
+        const float Pm1 = tbl[2 * L];
+        // 1. D = Pm1 S0 for this row, into TMEM (the group's previous MMA and this lane's
+        //    previous TMEM reads are complete)
+#pragma unroll
+        for (int c0 = 0; c0 < N; c0 += 32) {
+            float v[32];
+#pragma unroll
+            for (int j = 0; j < 32 / Rt::EPC; ++j)
+                load_chunk<ST>(sb + Rt::off(p, c0 / Rt::EPC + j), v + Rt::EPC * j);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v[j] *= Pm1;
+            umma::st32(dcol + lanes + c0, v);
+        }
+        // 2. this row of A, a_i x_i[p] for i <= w (zero above), as three bf16 parts, into
+        //    the pair's A rows; B^T blocks t < N / 4 (n-block nb, entry block kb) from the
+        //    stage's ring rows (entries above w zero) into the group's B^T
+        uint8_t* pair = scratch - wi * a.warp_scratch - (g & 1) * kGroupWarps * a.warp_scratch;
+        uint8_t* Ab = pair + kTcBT;
+        uint8_t* BT = (g & 1) ? pair + kTcBT + kTcA : pair;
+        {
+            const float* av = tbl + L;
+            const uint16_t* xr = reinterpret_cast<const uint16_t*>(sb + a.off_x);
+            uint16_t part[3][kTcMaxEntries];
+#pragma unroll
+            for (int i = 0; i < kTcMaxEntries; ++i) {
+                float c = 0.f;
+                if (i <= w) c = av[i] * bf16_to_f(xr[i * P + p]);
+                umma::split3_bf16(c, part[0][i], part[1][i], part[2][i]);
+            }
+            const int arow = 64 * (g & 1) + p;
+#pragma unroll
+            for (int sp = 0; sp < 3; ++sp)
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const uint16_t* q = &part[sp][8 * h];
+                    *reinterpret_cast<uint4*>(Ab + umma::kmajor_offset(arow, 16 * sp + 8 * h, kTcALbo,
+                                                                       kTcASbo)) =
+                        make_uint4(q[0] | (uint32_t(q[1]) << 16), q[2] | (uint32_t(q[3]) << 16),
+                                   q[4] | (uint32_t(q[5]) << 16), q[6] | (uint32_t(q[7]) << 16));
+                }
+        }
+        if (t < N / 4) {
+            const int nb = t % (N / 8), kb = t / (N / 8);
+            const uint8_t* br = sb + a.off_B;
+            uint4 in[8], out[8];
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                const int e = 8 * kb + r;
+                in[r] = e <= w ? *reinterpret_cast<const uint4*>(br + ((size_t)e * N + 8 * nb) * 2)
+                               : make_uint4(0, 0, 0, 0);
+            }
+            umma::transpose8x8_b16(in, out);
+#pragma unroll
+            for (int c = 0; c < 8; ++c)
+                *reinterpret_cast<uint4*>(BT + umma::kmajor_offset(8 * nb + c, 8 * kb, kTcBLbo, kTcBSbo)) =
+                    out[c];
+        }
+        umma::wait_st();
+        // 3. hand the operands to the issuing thread: writers fence their stores for the
+        //    tensor core's (async) proxy and order their TMEM stores, then each warp
+        //    arrives once (bounded wait, as in store_tile)
+        umma::fence_smem_to_async();
+        umma::fence_before_sync();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_plain(ctx.grp_bar);
+        if (t == 0) {
+            if (mbar_wait_bounded(ctx.grp_bar, ctx.grp_phase)) {
+                umma::fence_after_sync();
+                constexpr uint32_t idesc = umma::idesc_bf16_f32(128, N);
+                const uint64_t bdesc = umma::smem_desc_kmajor(BT, kTcBLbo, kTcBSbo);
+#pragma unroll
+                for (int sp = 0; sp < 3; ++sp)
+                    umma::mma_bf16(dcol, umma::smem_desc_kmajor(Ab + sp * 2 * kTcALbo, kTcALbo, kTcASbo),
+                                   bdesc, idesc, true);
+                umma::commit_to(ctx.mma_bar);
+            }
+        }
+        ctx.grp_phase ^= 1;
+        const bool ok = mbar_wait_bounded(ctx.mma_bar, ctx.mma_phase);
+        ctx.mma_phase ^= 1;
+        umma::fence_after_sync();
+        if (!ok) {
+            if (lane == 0) {
+                *ctx.abort_flag = 1;
+                set_dev_err(a.dev_err, RSSM_DEVERR_TIMEOUT);
+            }
+            return;
+        }
+        // 4. the row back from TMEM, rounded to the state dtype, over S0 in the stage
+        const size_t row_e = ((size_t)m.s * a.H + m.h) * P * N + (size_t)p * N;
+        const ulonglong2 gen = load_generator<ST>(a.sr);
+#pragma unroll
+        for (int c0 = 0; c0 < N; c0 += 32) {
+            float v[32];
+            umma::ld32(dcol + lanes + c0, v);
+            umma::wait_ld();
+#pragma unroll
+            for (int j = 0; j < 32 / Rt::EPC; ++j)
+                pack_chunk(sb + Rt::off(p, c0 / Rt::EPC + j), v + Rt::EPC * j, row_e + c0 + Rt::EPC * j, gen);
+        }
+    }
+}
 
 template <int P, int N, class ST>
 struct FullPolicy {
@@ -412,21 +669,35 @@ struct OutLaunch {
     cudaStream_t stream;
     template <int P, int N, class ST>
     int go() {
-        using Pol = OutPolicy<P, N, ST>;
+        // the tensor-core fold takes 64 x 128 tiles, bf16 ring entries and at most 16 of them
+        if constexpr (P == 64 && N == 128) {
+            if (c.act_bf16 && c.L <= kTcMaxEntries) return run<OutPolicy<P, N, ST, true>, P, N>();
+        }
+        return run<OutPolicy<P, N, ST, false>, P, N>();
+    }
+    template <class Pol, int P, int N>
+    int run() {
         typename Pol::Args a{};
+        using Rt = typename Pol::Rt;
+        if (!make_tmap_rows128(&a.tmap, c.state, Rt::SS, (uint64_t)c.num_slots * c.H * P, N, P))
+            return RSSM_ERR_CUDA;
         a.state = c.state; a.C = c.C; a.D = c.D; a.z = c.z; a.ring_x = c.ring_x; a.ring_B = c.ring_B;
         a.ci = c.ci; a.row_wp = c.row_wp; a.row_flush = c.row_flush; a.ws = c.ws; a.y = c.y;
         a.dev_err = c.dev_err; a.sr = c.sr; a.batch = c.batch; a.H = c.H; a.G = c.G; a.L = c.L;
         a.num_slots = c.num_slots; a.act_bf16 = c.act_bf16; a.out_bf16 = c.out_bf16;
+        a.sched = reinterpret_cast<unsigned int*>(reinterpret_cast<char*>(const_cast<float*>(c.ws)) +
+                                                  sched_offset(c.batch, c.H, c.L));
         const int sa = c.act_bf16 ? 2 : 4;
-        int off = Pol::Sh::TILE;
+        int off = Rt::TILE;
         a.off_x = off;   off += c.L * P * sa;
         a.off_C = off;   off += N * sa;
         a.off_z = off;   off += P * sa;
         a.off_tbl = off; off += tbl_floats(c.L) * 4;
         a.off_B = off;   off += c.L * N * sa;
-        const int stage_bytes = (off + 127) & ~127;
-        return launch_pipe<Pol>(a, stage_bytes, 0, Pol::Sh::TILE, (long)c.batch * c.H, stream);
+        // 128-byte-swizzled boxes start on 1024-byte boundaries
+        const int stage_bytes = (off + 1023) & ~1023;
+        const int scratch = Pol::kTmemCols > 0 ? kTcWarpScratch : 0;
+        return launch_pipe<Pol>(a, stage_bytes, scratch, Rt::TILE, (long)c.batch * c.H, stream, 1024);
     }
 };
 

@@ -44,7 +44,8 @@ struct RowArgs {
     void* ring_x;          // [slots][H][L][P]
     float* ring_dt;        // [slots][H][L]
     void* ring_B;          // [slots][G][L][N]
-    float* ws;             // [batch][H][TBL]
+    float* ws;             // [batch][H][TBL], then the output kernel's work counter
+    unsigned int* sched;   // that counter (zeroed by block 0 of a table-building launch)
 };
 
 constexpr int kRowThreads = 256;
@@ -244,6 +245,7 @@ __global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSM) precompute_kerne
     extern __shared__ __align__(128) uint8_t psm[];
     __shared__ uint64_t bar;
     const int b = blockIdx.x;
+    if (b == 0 && threadIdx.x < 2) a.sched[threadIdx.x] = 0u;  // the output kernel's counter
     const int s = ci[b];
     // bad slots and cursors are reported by the append and output kernels
     const int w = given_cursor(b, s, a.num_slots, a.L, row_wp, nullptr);
@@ -277,6 +279,7 @@ __global__ void __launch_bounds__(kRowThreads, kRowBlocksPerSM) prepare_kernel(c
     const int H = a.H, P = a.P, N = a.N, G = a.G, L = a.L;
     const int sa = a.act_bf16 ? 2 : 4;
     const int b = blockIdx.x;
+    if (b == 0 && threadIdx.x < 2) a.sched[threadIdx.x] = 0u;  // the output kernel's counter
     const int s = ci[b];
     const bool staged = s >= 0 && s < a.num_slots;
     if (threadIdx.x == 0) {
@@ -387,7 +390,7 @@ extern "C" int rssm_ring_append(const rssm_mamba2_dims* d, const void* x, const 
 
 extern "C" size_t rssm_mamba2_workspace_size(const rssm_mamba2_dims* d) {
     if (m2::check_dims(d)) return 0;
-    return (size_t)d->batch * d->nheads * m2::tbl_floats(d->ring_len) * sizeof(float);
+    return m2::sched_offset(d->batch, d->nheads, d->ring_len) + m2::kSchedBytes;
 }
 
 // Shared-memory size of the table-building kernels, checked and opted in.
@@ -422,6 +425,8 @@ extern "C" int rssm_mamba2_precompute(const rssm_mamba2_dims* d, const float* A,
     ra.ring_dt = const_cast<float*>(ring_dt);  // read only here
     ra.ring_B = const_cast<void*>(ring_B);
     ra.ws = static_cast<float*>(workspace);
+    ra.sched = reinterpret_cast<unsigned int*>(static_cast<char*>(workspace) +
+                                               m2::sched_offset(d->batch, d->nheads, d->ring_len));
     m2::precompute_kernel<<<d->batch, m2::kRowThreads, smem, (cudaStream_t)stream>>>(ra, cache_indices, row_wp,
                                                                                       dev_err);
     return launch_status();
@@ -457,6 +462,8 @@ extern "C" int rssm_mamba2_prepare(const rssm_mamba2_dims* d, int advance,
     ra.ring_dt = ring_dt;
     ra.ring_B = ring_B;
     ra.ws = static_cast<float*>(workspace);
+    ra.sched = reinterpret_cast<unsigned int*>(static_cast<char*>(workspace) +
+                                               m2::sched_offset(d->batch, d->nheads, d->ring_len));
     rc = m2_prologue_smem(d, reinterpret_cast<const void*>(m2::prepare_kernel), &smem);
     if (rc) return rc;
     m2::prepare_kernel<<<d->batch, m2::kRowThreads, smem, (cudaStream_t)stream>>>(

@@ -39,6 +39,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "umma.cuh"
 
 namespace rssm {
 
@@ -52,6 +53,77 @@ __device__ __forceinline__ void mbar_arrive_plain(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
+// Tensor memory: a policy with `static constexpr int kTmemCols > 0` gets that many
+// TMEM columns (allocated by consumer warp 0 when the CTA starts, freed when every
+// consumer warp is done). A policy with kTmemCols > 0 or `kUsesCtx = true` gets a
+// PipeCtx as the last argument of consume(): per consumer group a tensor-core
+// completion mbarrier, a hand-over mbarrier (one arrival per warp) and a "taken"
+// mbarrier (one arrival), and the means to release the stage itself.
+template <class K, class = void>
+struct TmemCols {
+    static constexpr int value = 0;
+};
+template <class K>
+struct TmemCols<K, decltype(void(K::kTmemCols))> {
+    static constexpr int value = K::kTmemCols;
+};
+
+// Dynamic work distribution: a policy with `static constexpr bool kDynamic = true` and
+// an Args member `unsigned int* sched` (two words, zero before the launch) has its
+// producers claim kClaim items at a time from the counter sched[0] instead of taking
+// every (gridDim.x * groups)-th item, so consumer groups that met expensive items take
+// fewer. Each producer ends its pipeline with an end marker (item -1) and then counts
+// itself in sched[1]; the last producer of the launch sets both words back to zero.
+template <class K, class = void>
+struct DynSched {
+    static constexpr bool value = false;
+};
+template <class K>
+struct DynSched<K, decltype(void(K::kDynamic))> {
+    static constexpr bool value = K::kDynamic;
+};
+constexpr int kClaim = 4;
+
+template <class K, class = void>
+struct UsesCtx {
+    static constexpr bool value = TmemCols<K>::value > 0;
+};
+template <class K>
+struct UsesCtx<K, decltype(void(K::kUsesCtx))> {
+    static constexpr bool value = K::kUsesCtx || TmemCols<K>::value > 0;
+};
+
+struct PipeCtx {
+    uint32_t tmem;       // TMEM base address of the CTA's allocation
+    uint64_t* mma_bar;   // this group's tensor-core completion barrier (one commit)
+    uint64_t* grp_bar;   // this group's hand-over barrier (one arrival per warp)
+    uint64_t* done_bar;  // the issuing thread has taken a hand-over (one arrival)
+    uint32_t mma_phase;  // parities of those barriers' next completions (the policy
+    uint32_t grp_phase;  // flips them as it uses them)
+    uint32_t done_phase;
+    int group;           // consumer group index
+    int groups;          // consumer groups in the CTA
+    volatile int* abort_flag;
+    uint64_t* empty_bar;  // the current stage's "empty" barrier
+    bool released;        // the policy already gave the stage back (release_stage)
+};
+
+// Give the current stage back to the producer before consume() returns: the policy
+// must not touch the stage's shared memory afterwards. Whole warp.
+__device__ __forceinline__ void release_stage(PipeCtx& ctx) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(
+                                                  smem_addr(ctx.empty_bar))
+                                              : "memory");
+    ctx.released = true;
+}
+
+constexpr int kPipeTmemSlot = 1296;  // header offsets: TMEM base address,
+constexpr int kPipeMmaBars = 1312;   // the groups' completion barriers,
+constexpr int kPipeGrpBars = 1344;   // their hand-over barriers,
+constexpr int kPipeDoneBars = 1376;  // their "taken" barriers,
+constexpr int kPipeItems = 1408;     // and (dynamic distribution) each stage's item
+
 // The wait limit of a policy: Args::wait_ns when the policy has it, else RSSM_WAIT_NS.
 template <class K, class = void>
 struct WaitLimit {
@@ -64,8 +136,8 @@ struct WaitLimit<K, decltype(void(K::Args::wait_ns))> {
 
 template <class K>
 __global__ void __launch_bounds__(32 * kPipeMaxGroups * (K::kGroup + 1), 1)
-    pipe_kernel(const typename K::Args a) {
-    extern __shared__ __align__(128) uint8_t smem[];
+    pipe_kernel(const __grid_constant__ typename K::Args a) {
+    extern __shared__ __align__(1024) uint8_t smem[];
     static_assert(sizeof(typename K::Meta) <= kPipeMetaBytes, "meta too large");
     uint64_t* fullb = reinterpret_cast<uint64_t*>(smem);
     uint64_t* emptyb = fullb + kPipeMaxStages;
@@ -84,23 +156,92 @@ __global__ void __launch_bounds__(32 * kPipeMaxGroups * (K::kGroup + 1), 1)
         return reinterpret_cast<typename K::Meta*>(meta_base + st * kPipeMetaBytes);
     };
 
+    constexpr int kTmem = TmemCols<K>::value;
+    constexpr bool kCtx = UsesCtx<K>::value;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + kPipeTmemSlot);
+    uint64_t* mma_bars = reinterpret_cast<uint64_t*>(smem + kPipeMmaBars);
+    uint64_t* grp_bars = reinterpret_cast<uint64_t*>(smem + kPipeGrpBars);
+    uint64_t* done_bars = reinterpret_cast<uint64_t*>(smem + kPipeDoneBars);
+    if constexpr (kTmem > 0) {
+        if (warp == 0) umma::tmem_alloc(tmem_slot, kTmem);
+    }
     if (threadIdx.x == 0) {
         for (int st = 0; st < NST; ++st) {
             mbar_init(&fullb[st], 1);
             mbar_init(&emptyb[st], K::kGroup);
         }
+        if constexpr (kCtx)
+            for (int g = 0; g < ng; ++g) {
+                mbar_init(&mma_bars[g], 1);
+                mbar_init(&grp_bars[g], K::kGroup);
+                mbar_init(&done_bars[g], 1);
+            }
         *abort_flag = 0;
         fence_barrier_init();
     }
+    if constexpr (kTmem > 0) umma::fence_before_sync();
     __syncthreads();
 
     const uint64_t wait_ns = WaitLimit<K>::ns(a);
+
+    constexpr bool kDyn = DynSched<K>::value;
+    volatile int* stage_item = reinterpret_cast<volatile int*>(smem + kPipeItems);
 
     if (warp >= nc) {
         // ---------------- producer warp of pipeline g ----------------
         const int g = warp - nc;
         const uint64_t pol = policy_evict_first();
         int pos = 0, lap = 0;  // stage position and lap of the next item to issue
+        if constexpr (kDyn) {
+            // claim kClaim items at a time; the next claim is made while this one issues
+            int base = 0;
+            if (lane == 0) base = (int)atomicAdd(a.sched, (unsigned)kClaim);
+            base = __shfl_sync(kFull, base, 0);
+            for (bool stop = false; !stop;) {
+                int nxt = 0;
+                if (lane == 0 && base < n) nxt = (int)atomicAdd(a.sched, (unsigned)kClaim);
+                int4 info = make_int4(0, 0, 0, 0);
+                if (lane < kClaim && base + lane < n) info = K::prefetch(a, base + lane);
+                for (int j = 0; j < kClaim && !stop; ++j) {
+                    const int item = base + j;
+                    int4 r;
+                    r.x = __shfl_sync(kFull, info.x, j);
+                    r.y = __shfl_sync(kFull, info.y, j);
+                    r.z = __shfl_sync(kFull, info.z, j);
+                    r.w = __shfl_sync(kFull, info.w, j);
+                    int bad = 0;
+                    if (lane == 0) {
+                        const int st = g + ng * pos;
+                        int ok = 1;
+                        if (lap > 0) ok = mbar_wait_abortable(&emptyb[st], (lap - 1) & 1, wait_ns, abort_flag);
+                        if (ok == 0) {
+                            *abort_flag = 1;
+                            set_dev_err(a.dev_err, RSSM_DEVERR_TIMEOUT);
+                        }
+                        if (ok != 1 || *abort_flag) {
+                            bad = 1;
+                        } else if (item >= n) {
+                            stage_item[st] = -1;  // end marker
+                            mbar_arrive_plain(&fullb[st]);
+                        } else {
+                            stage_item[st] = item;
+                            K::issue(a, item, r, meta_of(st), stage0 + (size_t)st * a.stage_bytes,
+                                     &fullb[st], pol);
+                        }
+                    }
+                    if (__shfl_sync(kFull, bad, 0)) {
+                        stop = true;
+                        break;
+                    }
+                    if (++pos == spg) {
+                        pos = 0;
+                        ++lap;
+                    }
+                    if (item >= n) stop = true;
+                }
+                base = __shfl_sync(kFull, nxt, 0);
+            }
+        } else {
         for (int u0 = 0;; u0 += 32) {
             const int my_item = blockIdx.x + (g + (u0 + lane) * ng) * gridDim.x;
             int4 info = make_int4(0, 0, 0, 0);
@@ -143,6 +284,7 @@ __global__ void __launch_bounds__(32 * kPipeMaxGroups * (K::kGroup + 1), 1)
             }
             if (stop) break;
         }
+        }
         // Wind-down after an abort: the last issue into each stage may still have copies
         // in flight if no consumer waited for it. Stage position p has had
         // lap + (p < pos) issues; wait (bounded) for the phase of the last one.
@@ -152,16 +294,45 @@ __global__ void __launch_bounds__(32 * kPipeMaxGroups * (K::kGroup + 1), 1)
                 if (cnt > 0) mbar_wait_bounded(&fullb[g + ng * p], (cnt - 1) & 1, wait_ns);
             }
         }
+        if constexpr (kDyn) {
+            // every producer has made its last claim once all have counted themselves:
+            // the last one resets the counter for the next launch
+            if (lane == 0) {
+                __threadfence();
+                const unsigned prev = atomicAdd(a.sched + 1, 1u);
+                if (prev == gridDim.x * (unsigned)ng - 1u) {
+                    atomicExch(a.sched, 0u);
+                    atomicExch(a.sched + 1, 0u);
+                    __threadfence();
+                }
+            }
+        }
         return;
     }
 
     // ---------------- consumer warps of pipeline g ----------------
     uint8_t* scratch = smem + a.scratch_off + warp * a.warp_scratch;
     const int g = warp / K::kGroup, wi = warp % K::kGroup;
+    PipeCtx ctx{};
+    if constexpr (kCtx) {
+        if constexpr (kTmem > 0) {
+            umma::fence_after_sync();
+            ctx.tmem = *tmem_slot;
+        }
+        ctx.mma_bar = &mma_bars[g];
+        ctx.grp_bar = &grp_bars[g];
+        ctx.done_bar = &done_bars[g];
+        ctx.mma_phase = 0;
+        ctx.grp_phase = 0;
+        ctx.done_phase = 0;
+        ctx.group = g;
+        ctx.groups = ng;
+        ctx.abort_flag = abort_flag;
+    }
     int pos = 0, lap = 0;
     for (int u = 0;; ++u) {
-        const int item = blockIdx.x + (g + u * ng) * gridDim.x;
-        if (item >= n) break;
+        int item = blockIdx.x + (g + u * ng) * gridDim.x;
+        if (!kDyn && item >= n) break;
         const int st = g + ng * pos;
         const int ok = mbar_wait_abortable(&fullb[st], lap & 1, wait_ns, abort_flag);
         if (__ballot_sync(kFull, ok == 1) != kFull) {
@@ -173,29 +344,54 @@ __global__ void __launch_bounds__(32 * kPipeMaxGroups * (K::kGroup + 1), 1)
             }
             break;
         }
+        if constexpr (kDyn) {
+            item = stage_item[st];
+            if (item < 0) break;  // end marker: no more items for this pipeline
+        }
         const typename K::Meta m = *meta_of(st);
-        K::consume(a, item, m, stage0 + (size_t)st * a.stage_bytes, scratch, lane, wi);
+        if constexpr (kCtx) {
+            ctx.empty_bar = &emptyb[st];
+            ctx.released = false;
+            K::consume(a, item, m, stage0 + (size_t)st * a.stage_bytes, scratch, lane, wi, ctx);
+        } else {
+            K::consume(a, item, m, stage0 + (size_t)st * a.stage_bytes, scratch, lane, wi);
+        }
         __syncwarp();
-        if (lane == 0) mbar_arrive_plain(&emptyb[st]);
+        if constexpr (kCtx) {
+            if (!ctx.released && lane == 0) mbar_arrive_plain(&emptyb[st]);
+        } else {
+            if (lane == 0) mbar_arrive_plain(&emptyb[st]);
+        }
         if (++pos == spg) {
             pos = 0;
             ++lap;
         }
         if (*abort_flag) break;
     }
+    if constexpr (kTmem > 0) {
+        // every consumer warp is done with tensor memory: warp 0 frees it
+        umma::fence_before_sync();
+        umma::named_sync(15, nc * 32);
+        if (warp == 0) {
+            umma::fence_after_sync();
+            umma::tmem_dealloc(ctx.tmem, kTmem);
+        }
+    }
 }
 
 // Host side: pick the pipeline shape, raise the shared-memory limit once, launch
 // one CTA per SM (fewer when there are fewer items).
+// `align`: alignment of the stages' start (1024 for 128-byte-swizzled TMA boxes; the
+// stage size is then a multiple of it too).
 template <class K>
 int launch_pipe(typename K::Args a, int stage_bytes, int warp_scratch, int tile_bytes, long n_items,
-                cudaStream_t stream) {
+                cudaStream_t stream, int align = 128) {
     if (n_items <= 0) return RSSM_OK;
     DeviceInfo di;
     if (!device_info(&di)) return RSSM_ERR_CUDA;
     PipeCfg pc;
     if (!pick_pipe(di, stage_bytes, warp_scratch, tile_bytes, kPipeHeader, kPipeMaxStages,
-                   K::kGroup, kPipeMaxGroups, &pc))
+                   K::kGroup, kPipeMaxGroups, &pc, align))
         return RSSM_ERR_UNSUPPORTED;
     a.stages = pc.stages;
     a.stage_bytes = stage_bytes;
