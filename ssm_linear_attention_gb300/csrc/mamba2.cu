@@ -501,12 +501,12 @@ __device__ void OutPolicy<P, N, ST, TC>::fold_tc(const Args& a, const Meta& m, u
         const size_t row_e = ((size_t)m.s * a.H + m.h) * P * N + (size_t)p * N;
         const ulonglong2 gen = load_generator<ST>(a.sr);
 #pragma unroll
-        for (int c0 = 0; c0 < N; c0 += 32) {
-            float v[32];
-            umma::ld32(dcol + lanes + c0, v);
+        for (int c0 = 0; c0 < N; c0 += 64) {
+            float v[64];
+            umma::ld64(dcol + lanes + c0, v);
             umma::wait_ld();
 #pragma unroll
-            for (int j = 0; j < 32 / Rt::EPC; ++j)
+            for (int j = 0; j < 64 / Rt::EPC; ++j)
                 pack_chunk(sb + Rt::off(p, c0 / Rt::EPC + j), v + Rt::EPC * j, row_e + c0 + Rt::EPC * j, gen);
         }
     }

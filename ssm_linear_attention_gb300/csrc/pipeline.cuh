@@ -82,7 +82,7 @@ template <class K>
 struct DynSched<K, decltype(void(K::kDynamic))> {
     static constexpr bool value = K::kDynamic;
 };
-constexpr int kClaim = 4;
+constexpr int kClaim = 2;
 
 template <class K, class = void>
 struct UsesCtx {

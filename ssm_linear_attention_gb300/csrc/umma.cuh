@@ -131,6 +131,13 @@ __device__ __forceinline__ void ld32(uint32_t taddr, float* v) {
     for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+// 64 consecutive 32-bit columns of this thread's TMEM lane (two 32x32b.x32 loads
+// issued back to back; one wait covers both).
+__device__ __forceinline__ void ld64(uint32_t taddr, float* v) {
+    ld32(taddr, v);
+    ld32(taddr + 32, v + 32);
+}
+
 __device__ __forceinline__ void wait_ld() {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
