@@ -106,7 +106,9 @@ __device__ __forceinline__ ulonglong2 load_generator(const uint64_t* sr) {
 //     Scratch of a pair of groups (4 warps x kTcWarpScratch):
 //       [B^T of the even group][A of both groups: 16 row blocks x 768 B][B^T of odd]
 //     so both groups' A descriptors start at the same address.
-//   * otherwise on CUDA cores, per lane in blocks of 32 columns.
+//   * otherwise (and for folds of fewer than kTcMinEntries entries, where the tensor
+//     cores' fixed cost does not pay) on CUDA cores in the y mapping, stored from
+//     registers with coalesced 16-byte stores.
 template <int P, int N, class ST>
 struct RowTile {
     static constexpr int SS = ST::bytes;
@@ -128,6 +130,7 @@ constexpr int kTcBT = 4096;            // B^T: 128 rows x 16 entries, bf16, core
 constexpr int kTcA = 16 * 768;         // A: 128 rows x 48 (3 parts x 16 entries), bf16
 constexpr uint32_t kTcALbo = 128, kTcASbo = 768, kTcBLbo = 128, kTcBSbo = 256;
 constexpr int kTcMaxEntries = 16;
+constexpr int kTcMinEntries = 8;  // flushes of fewer entries take the CUDA-core fold
 
 // The EPC elements of a 16-byte state chunk as float32.
 template <class ST>
@@ -290,57 +293,72 @@ struct OutPolicy {
             store1(a.y, ((size_t)m.b * a.H + m.h) * P + p, a.out_bf16, yv);
         }
         if (!m.f) return;
-        if constexpr (TC) fold_tc(a, m, const_cast<uint8_t*>(sb), scratch, lane, wi, ctx, tbl);
-        else fold_fma(a, m, const_cast<uint8_t*>(sb), lane, wi, tbl);
-        store_tile(a, m, sb, lane, wi, ctx);
+        if constexpr (TC) {
+            // the tensor-core fold has a fixed cost; short rings fold faster on CUDA cores
+            if (w + 1 >= kTcMinEntries) {
+                fold_tc(a, m, const_cast<uint8_t*>(sb), scratch, lane, wi, ctx, tbl);
+                store_tile(a, m, sb, lane, wi, ctx);
+                return;
+            }
+        }
+        fold_fma(a, m, sb, lane, wi, tbl);
     }
 
-    // S[p][:] = Pm1 S0[p][:] + sum_{i<=w} (a_i x_i[p]) B_i[:] on CUDA cores, written back
-    // over S0 in the stage (each lane its own rows), rounded to the state dtype.
-    static __device__ void fold_fma(const Args& a, const Meta& m, uint8_t* sb, int lane, int wi,
+    // S = Pm1 S0 + sum_{i<=w} a_i x_i B_i^T on CUDA cores, in the y mapping (a lane owns 8
+    // columns of rows row0 + RPI t), stored from registers: 16 lanes cover a row's
+    // contiguous bytes, so the stores coalesce. Columns pairs accumulate with packed
+    // two-wide FMAs.
+    static __device__ void fold_fma(const Args& a, const Meta& m, const uint8_t* sb, int lane, int wi,
                                     const float* tbl) {
+        using Sh = TileShape<P, N, ST>;
         const bool bf = a.act_bf16;
         const int sa = bf ? 2 : 4;
         const int L = a.L, w = m.w;
-        const float Pm1 = tbl[2 * L];
-        const float* av = tbl + L;
+        const int q = lane % Sh::NQ, hr = lane / Sh::NQ;
+        const int row0 = wi * Sh::PW + hr;
         const uint8_t* xr = sb + a.off_x;
         const uint8_t* br = sb + a.off_B;
+        const float Pm1 = tbl[2 * L];
+        const float* av = tbl + L;
         const size_t tile_e = ((size_t)m.s * a.H + m.h) * P * N;
         const ulonglong2 gen = load_generator<ST>(a.sr);
-        constexpr int CPB = 32 / Rt::EPC;  // chunks per block of 32 columns
+        constexpr int RC = Sh::ITER < 8 ? Sh::ITER : 8;
 #pragma unroll 1
-        for (int rr = 0; rr < Rt::RPL; ++rr) {
-            const int p = 32 * wi + lane + 64 * rr;
-#pragma unroll 1
-            for (int cb = 0; cb < N / 32; ++cb) {
-                float2 acc[16];
+        for (int t0 = 0; t0 < Sh::ITER; t0 += RC) {
+            float2 acc[RC][4];
 #pragma unroll
-                for (int k = 0; k < CPB; ++k) {
-                    float e[Rt::EPC];
-                    load_chunk<ST>(sb + Rt::off(p, cb * CPB + k), e);
-#pragma unroll
-                    for (int j = 0; j < Rt::EPC / 2; ++j)
-                        acc[k * Rt::EPC / 2 + j] = make_float2(Pm1 * e[2 * j], Pm1 * e[2 * j + 1]);
+            for (int r = 0; r < RC; ++r) {
+                const int p = row0 + Sh::RPI * (t0 + r);
+                float s8[8];
+                if constexpr (ST::bf16) {
+                    load8(sb + Rt::off(p, q), true, s8);
+                } else {
+                    load_chunk<ST>(sb + Rt::off(p, 2 * q), s8);
+                    load_chunk<ST>(sb + Rt::off(p, 2 * q + 1), s8 + 4);
                 }
-                for (int i = 0; i <= w; ++i) {
-                    const float ax = av[i] * load1(xr, i * P + p, bf);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) acc[r][k] = make_float2(Pm1 * s8[2 * k], Pm1 * s8[2 * k + 1]);
+            }
+            for (int i = 0; i <= w; ++i) {
+                float bi[8];
+                load8(br + ((size_t)i * N + q * 8) * sa, bf, bi);
+                const float2 b2[4] = {make_float2(bi[0], bi[1]), make_float2(bi[2], bi[3]),
+                                      make_float2(bi[4], bi[5]), make_float2(bi[6], bi[7])};
+                const float ai = av[i];
+#pragma unroll
+                for (int r = 0; r < RC; ++r) {
+                    const int p = row0 + Sh::RPI * (t0 + r);
+                    const float ax = ai * load1(xr, i * P + p, bf);
                     const float2 ax2 = make_float2(ax, ax);
 #pragma unroll
-                    for (int k = 0; k < 4; ++k) {
-                        float b8[8];
-                        load8(br + ((size_t)i * N + 32 * cb + 8 * k) * sa, bf, b8);
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            acc[4 * k + j] = __ffma2_rn(ax2, make_float2(b8[2 * j], b8[2 * j + 1]),
-                                                        acc[4 * k + j]);
-                    }
+                    for (int k = 0; k < 4; ++k) acc[r][k] = __ffma2_rn(ax2, b2[k], acc[r][k]);
                 }
-                const float* f = reinterpret_cast<const float*>(acc);
+            }
 #pragma unroll
-                for (int k = 0; k < CPB; ++k)
-                    pack_chunk(sb + Rt::off(p, cb * CPB + k), f + k * Rt::EPC,
-                               tile_e + (size_t)p * N + 32 * cb + k * Rt::EPC, gen);
+            for (int r = 0; r < RC; ++r) {
+                const int p = row0 + Sh::RPI * (t0 + r);
+                store_state8<ST>(static_cast<char*>(a.state), tile_e + (size_t)p * N + q * 8,
+                                 reinterpret_cast<const float*>(acc[r]), gen);
             }
         }
     }
@@ -669,9 +687,11 @@ struct OutLaunch {
     cudaStream_t stream;
     template <int P, int N, class ST>
     int go() {
-        // the tensor-core fold takes 64 x 128 tiles, bf16 ring entries and at most 16 of them
+        // the tensor-core fold takes 64 x 128 tiles, bf16 ring entries and at most 16 of
+        // them; rings too short to reach kTcMinEntries entries keep the leaner kernel
         if constexpr (P == 64 && N == 128) {
-            if (c.act_bf16 && c.L <= kTcMaxEntries) return run<OutPolicy<P, N, ST, true>, P, N>();
+            if (c.act_bf16 && c.L >= kTcMinEntries && c.L <= kTcMaxEntries)
+                return run<OutPolicy<P, N, ST, true>, P, N>();
         }
         return run<OutPolicy<P, N, ST, false>, P, N>();
     }

@@ -193,16 +193,32 @@ __global__ void __launch_bounds__(32 * kPipeMaxGroups * (K::kGroup + 1), 1)
         const uint64_t pol = policy_evict_first();
         int pos = 0, lap = 0;  // stage position and lap of the next item to issue
         if constexpr (kDyn) {
-            // claim kClaim items at a time; the next claim is made while this one issues
-            int base = 0;
-            if (lane == 0) base = (int)atomicAdd(a.sched, (unsigned)kClaim);
-            base = __shfl_sync(kFull, base, 0);
+            // About three quarters of the items are dealt round-robin as in the static
+            // scheme (producer (block, g) takes items block + (g + u * groups) * gridDim.x
+            // for u < U, in order, with no atomic before its first copy); the rest are
+            // claimed kClaim at a time from the counter, the next claim made while the
+            // current one issues. The counter thus only balances the tail of the launch,
+            // where differences between groups add up, with few atomics.
+            const int stride = (int)(gridDim.x * ng);
+            const int U = (3 * n / 4) / stride;
+            const int first = U * stride;
+            int u = 0;
+            int base = U > 0 ? (int)blockIdx.x + g * (int)gridDim.x : 0;
+            if (U == 0) {
+                if (lane == 0) base = first + (int)atomicAdd(a.sched, (unsigned)kClaim);
+                base = __shfl_sync(kFull, base, 0);
+            }
             for (bool stop = false; !stop;) {
+                // this round: one static item (u < U) or kClaim claimed ones
+                const bool stat = u < U;
+                const int cnt = stat ? 1 : kClaim;
                 int nxt = 0;
-                if (lane == 0 && base < n) nxt = (int)atomicAdd(a.sched, (unsigned)kClaim);
+                if (u + 1 < U) nxt = (int)blockIdx.x + (g + (u + 1) * ng) * (int)gridDim.x;
+                else if (lane == 0 && base < n) nxt = first + (int)atomicAdd(a.sched, (unsigned)kClaim);
+                ++u;
                 int4 info = make_int4(0, 0, 0, 0);
-                if (lane < kClaim && base + lane < n) info = K::prefetch(a, base + lane);
-                for (int j = 0; j < kClaim && !stop; ++j) {
+                if (lane < cnt && base + lane < n) info = K::prefetch(a, base + lane);
+                for (int j = 0; j < cnt && !stop; ++j) {
                     const int item = base + j;
                     int4 r;
                     r.x = __shfl_sync(kFull, info.x, j);
