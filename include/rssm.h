@@ -281,7 +281,16 @@ int rssm_mamba2_prepare(const rssm_mamba2_dims* dims, int advance, const uint8_t
  * rssm_mamba2_prepare then rssm_mamba2_output ([M2] 关键源码片段: the decode
  * path calls the ReplaySSM update once per step in place of
  * selective_state_update). row_flush is always required (the output kernel reads
- * it). Arguments, layouts and errors as in those two calls. */
+ * it). Arguments, layouts and errors as in those two calls.
+ * Small batches (batch <= 16, advance = 1, ring_len <= 64) take one launch
+ * instead ([M2] 风险与影响 item 3: at batch 1-8 the step is bound by launch
+ * latency): a CTA per (row, head) advances the cursor, appends the row's entry,
+ * builds its head's table and computes y and the fold, with identical results up
+ * to float32 rounding order (the tables are not left in the workspace). The last
+ * CTA of a row advances the slot cursor through a per-row counter in the
+ * workspace's 256-byte counter block (rssm_mamba2_workspace_size), so the
+ * workspace must be zero-filled before its first use with this call; the call
+ * leaves those counters at zero. */
 int rssm_mamba2_step(const rssm_mamba2_dims* dims, int advance, const uint8_t* force_flush,
                      int32_t* slot_wp, int32_t* row_wp, uint8_t* row_flush, void* state,
                      const void* x, const float* dt_raw, const float* dt_bias, int dt_softplus,

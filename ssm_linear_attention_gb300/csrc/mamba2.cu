@@ -897,6 +897,20 @@ extern "C" int rssm_mamba2_step_sr(const rssm_mamba2_dims* d, int advance,
     if (!ok_ptr(state) || !ok_ptr(D) || !ok_opt_ptr(z) || !ok_ptr(y) || !ok_ptr(row_flush) ||
         !ok_opt_ptr(sr_state))
         return RSSM_ERR_INVALID_ARG;
+    // a few rows: the whole step in one launch (round-to-nearest stores, cursor advanced here)
+    if (sr_state == nullptr && advance && d->batch <= m2::kSmallStepMaxBatch &&
+        d->ring_len <= m2::kSmallStepMaxRing) {
+        if (!ok_ptr(x) || !ok_ptr(dt_raw) || !ok_opt_ptr(dt_bias) || !ok_ptr(A) || !ok_ptr(B) ||
+            !ok_ptr(C) || !ok_ptr(cache_indices) || !ok_opt_ptr(force_flush) || !ok_ptr(slot_wp) ||
+            !ok_ptr(row_wp) || !ok_ptr(ring_x) || !ok_ptr(ring_dt) || !ok_ptr(ring_B) ||
+            !ok_ptr(workspace))
+            return RSSM_ERR_INVALID_ARG;
+        if (workspace_bytes < rssm_mamba2_workspace_size(d)) return RSSM_ERR_INVALID_ARG;
+        rc = m2_step_small(d, force_flush, slot_wp, row_wp, row_flush, state, x, dt_raw, dt_bias,
+                           dt_softplus, A, B, C, D, z, cache_indices, ring_x, ring_dt, ring_B,
+                           workspace, y, dev_err, (cudaStream_t)stream);
+        if (rc != RSSM_ERR_UNSUPPORTED) return rc;
+    }
     rc = rssm_mamba2_prepare(d, advance, force_flush, slot_wp, row_wp, row_flush, x, dt_raw, dt_bias,
                              dt_softplus, B, A, C, cache_indices, ring_x, ring_dt, ring_B,
                              workspace, workspace_bytes, dev_err, stream);

@@ -49,9 +49,6 @@ constexpr int kPipeMaxGroups = 4;
 constexpr int kPipeHeader = 2048;  // barriers + metadata + control, before the scratch
 constexpr unsigned kFull = 0xffffffffu;
 
-__device__ __forceinline__ void mbar_arrive_plain(uint64_t* bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
-}
 
 // Tensor memory: a policy with `static constexpr int kTmemCols > 0` gets that many
 // TMEM columns (allocated by consumer warp 0 when the CTA starts, freed when every

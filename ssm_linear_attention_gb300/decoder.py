@@ -77,7 +77,8 @@ class Mamba2ReplayDecoder:
         self.row_flush = torch.zeros(max_batch, device=dev, dtype=torch.uint8)
         self.dev_err = torch.zeros(4, device=dev, dtype=torch.int32)
         self.ws_bytes = B.rssm_mamba2_workspace_size(self.dims(max_batch))
-        self.workspace = torch.empty(max(self.ws_bytes, 16), device=dev, dtype=torch.uint8)
+        # zero-filled: the one-launch small-batch step keeps per-row counters here
+        self.workspace = torch.zeros(max(self.ws_bytes, 16), device=dev, dtype=torch.uint8)
         self.y = torch.empty(max_batch, nheads, headdim, device=dev, dtype=out_dtype)
         self.sr = _sr_state(sr_seed, dev)
 

@@ -254,3 +254,36 @@ def test_batch_zero_is_a_no_op():
                            dec.ring_dt, dec.ring_B, e, dec.row_wp, dec.row_flush, dec.workspace,
                            dec.ws_bytes, dec.y)
     torch.cuda.synchronize()
+
+
+@pytest.mark.parametrize("batch,L,sdt", [(16, 16, "bf16"), (1, 16, "fp32"), (7, 5, "bf16")])
+def test_small_batch_step_matches_staged_calls(batch, L, sdt):
+    # Batches of up to 16 rows run the whole step in one launch; the staged calls
+    # (cursor, append, precompute, output) are the two-launch path. Cursors and ring
+    # entries are copies and must be equal; outputs and flushed states agree within the
+    # state dtype's bar (the tables' float32 sums run in a different order).
+    wl = W.mamba2_large(batch=batch, num_slots=2 * batch + 3, L=L, steps=2 * L + 3,
+                        state_dtype=sdt, force_rate=0.2)
+    one = Hn.make_mamba2_decoder(wl)
+    two = Hn.make_mamba2_decoder(wl)
+    for j in range(wl.max_history()):
+        x, dt, Bm, C, z = Hn.mamba2_inputs_dev(wl, wl.history_inputs(j))
+        hci = Hn.to_dev(wl.history_ci(j), torch.int32)
+        one.step(x, dt, Bm, C, z, hci)
+        two.step_staged(x, dt, Bm, C, z, hci)
+    ci = Hn.to_dev(wl.cache_indices(), torch.int32)
+    tol = Hn.tol_for(sdt)
+    for t in range(wl.steps):
+        x, dt, Bm, C, z = Hn.mamba2_inputs_dev(wl, wl.step_inputs(t))
+        f = Hn.to_dev(wl.force_mask(t), torch.uint8)
+        ya = one.step(x, dt, Bm, C, z, ci, f).float().cpu().numpy()
+        yb = two.step_staged(x, dt, Bm, C, z, ci, f).float().cpu().numpy()
+        assert Hn.err(ya, yb) <= tol, t
+        assert torch.equal(one.row_wp[:batch], two.row_wp[:batch])
+        assert torch.equal(one.row_flush[:batch], two.row_flush[:batch])
+    torch.cuda.synchronize()
+    for name in ("ring_x", "ring_dt", "ring_B", "slot_wp"):
+        assert torch.equal(getattr(one, name), getattr(two, name)), name
+    ok, e, flips = Hn.state_ok(one.state.float().cpu().numpy(), two.state.float().cpu().numpy(), sdt)
+    assert ok, (e, flips)
+    assert int(one.dev_err.abs().sum()) == 0 and int(two.dev_err.abs().sum()) == 0
