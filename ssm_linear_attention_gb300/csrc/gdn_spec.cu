@@ -137,11 +137,12 @@ __device__ void fold_tile(const ProArgs& a, int item, float* sm) {
     float* bs = vs + kFoldChunk * VB;     // [16]
     float* gs = bs + kFoldChunk;          // [16]
     float* tile = a.state + (((size_t)s * a.HV + hv) * a.V + (size_t)vb * VB) * KD;
-    float S[8][4];
+    float2 S2[16];  // chunk u: columns (qd + 4u)*4 .. +3 as two pairs
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
         const float4 v4 = *reinterpret_cast<const float4*>(tile + r * KD + (qd + 4 * u) * 4);
-        S[u][0] = v4.x; S[u][1] = v4.y; S[u][2] = v4.z; S[u][3] = v4.w;
+        S2[2 * u] = make_float2(v4.x, v4.y);
+        S2[2 * u + 1] = make_float2(v4.z, v4.w);
     }
     const char* kr = static_cast<const char*>(a.ring_k) + ((size_t)s * a.HK + kh) * L * KD * sa;
     for (int e0 = 0; e0 < cnt; e0 += kFoldChunk) {
@@ -179,36 +180,37 @@ __device__ void fold_tile(const ProArgs& a, int item, float* sm) {
         }
         __syncthreads();
         for (int i = 0; i < ne; ++i) {
+            // the dot and the update run as packed two-wide float32 FMAs over column
+            // pairs; the key chunks are read again for the update (fewer registers)
             const float* ki = ks + i * KD + qd * 4;
-            float p0 = 0.f, p1 = 0.f;
+            float2 pa = make_float2(0.f, 0.f), pb = pa, pc = pa, pd = pa;
 #pragma unroll
             for (int u = 0; u < 8; u += 2) {
                 const float4 ka = *reinterpret_cast<const float4*>(ki + 16 * u);
                 const float4 kb = *reinterpret_cast<const float4*>(ki + 16 * (u + 1));
-                p0 = fmaf(S[u][0], ka.x, p0); p0 = fmaf(S[u][1], ka.y, p0);
-                p0 = fmaf(S[u][2], ka.z, p0); p0 = fmaf(S[u][3], ka.w, p0);
-                p1 = fmaf(S[u + 1][0], kb.x, p1); p1 = fmaf(S[u + 1][1], kb.y, p1);
-                p1 = fmaf(S[u + 1][2], kb.z, p1); p1 = fmaf(S[u + 1][3], kb.w, p1);
+                pa = __ffma2_rn(S2[2 * u], make_float2(ka.x, ka.y), pa);
+                pb = __ffma2_rn(S2[2 * u + 1], make_float2(ka.z, ka.w), pb);
+                pc = __ffma2_rn(S2[2 * u + 2], make_float2(kb.x, kb.y), pc);
+                pd = __ffma2_rn(S2[2 * u + 3], make_float2(kb.z, kb.w), pd);
             }
-            float part = p0 + p1;
+            float part = ((pa.x + pa.y) + (pb.x + pb.y)) + ((pc.x + pc.y) + (pd.x + pd.y));
             part += __shfl_xor_sync(kFull, part, 1);
             part += __shfl_xor_sync(kFull, part, 2);
             const float ge = gs[i];
             const float dn = bs[i] * (vs[i * VB + r] - ge * part);
+            const float2 g2 = make_float2(ge, ge), d2 = make_float2(dn, dn);
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {  // k re-read from shared memory: fewer registers
+            for (int u = 0; u < 8; ++u) {
                 const float4 k4 = *reinterpret_cast<const float4*>(ki + 16 * u);
-                S[u][0] = fmaf(ge, S[u][0], dn * k4.x);
-                S[u][1] = fmaf(ge, S[u][1], dn * k4.y);
-                S[u][2] = fmaf(ge, S[u][2], dn * k4.z);
-                S[u][3] = fmaf(ge, S[u][3], dn * k4.w);
+                S2[2 * u] = __ffma2_rn(g2, S2[2 * u], __fmul2_rn(d2, make_float2(k4.x, k4.y)));
+                S2[2 * u + 1] = __ffma2_rn(g2, S2[2 * u + 1], __fmul2_rn(d2, make_float2(k4.z, k4.w)));
             }
         }
     }
 #pragma unroll
     for (int u = 0; u < 8; ++u)
         *reinterpret_cast<float4*>(tile + r * KD + (qd + 4 * u) * 4) =
-            make_float4(S[u][0], S[u][1], S[u][2], S[u][3]);
+            make_float4(S2[2 * u].x, S2[2 * u].y, S2[2 * u + 1].x, S2[2 * u + 1].y);
 }
 
 // Tables of one (row, key head): the dot products of every live key (history,
@@ -584,29 +586,45 @@ struct VerPolicy {
             ho[j] += __shfl_xor_sync(kFull, ho[j], 16);
         }
         const float* ex = tb + 2 * T * L;  // Gu[T], Go[T], beta[T], g[T]
-        float dd[T];
+        // the chain itself (the dependent part) first, the stores after it
+        float dd[T], oo[T], vr[T];
 #pragma unroll
         for (int j = 0; j < T; ++j) {
             const float* au = tb + j * L + c;          // au over the drafts' entries
             const float* ao = tb + T * L + j * L + c;
             float u = fmaf(ex[j], W[(2 * j) * RW + r], hu[j]);
-            float oo = fmaf(ex[T + j], W[(2 * j + 1) * RW + r], ho[j]);
+            float o_ = fmaf(ex[T + j], W[(2 * j + 1) * RW + r], ho[j]);
 #pragma unroll
             for (int jj = 0; jj < j; ++jj) {
                 u = fmaf(au[jj], dd[jj], u);
-                oo = fmaf(ao[jj], dd[jj], oo);
+                o_ = fmaf(ao[jj], dd[jj], o_);
             }
-            const float vr = load1(sb + a.off_v + j * VB * sa, rr, bf);
-            const float dn = ex[2 * T + j] * (vr - ex[3 * T + j] * u);
+            vr[j] = load1(sb + a.off_v + j * VB * sa, rr, bf);
+            const float dn = ex[2 * T + j] * (vr[j] - ex[3 * T + j] * u);
             dd[j] = dn;
-            oo = fmaf(ao[j], dn, oo);
-            const int pos = (m.base_eff + c + j) % L;
-            if (h == 0) {
-                store1(a.o, (((size_t)m.b * T + j) * a.HV + m.hv) * a.V + vi, a.out_bf16, oo);
+            oo[j] = fmaf(ao[j], dn, o_);
+        }
+        // lane half 0 stores o, half 1 the drafts' d and raw v into the ring (positions
+        // base' + c + j, wrapping). When o and raw v share a dtype, one store serves
+        // both halves.
+        const size_t o0 = (((size_t)m.b * T) * a.HV + m.hv) * a.V + vi, ostep = (size_t)a.HV * a.V;
+        float* rd = a.ring_d + (((size_t)m.s * a.HV + m.hv) * (a.V / VB) + m.vb) * L * VB + rr;
+        const size_t v0 = ((size_t)m.s * a.HV + m.hv) * L * a.V + vi;
+        const bool same = (a.out_bf16 != 0) == BF;
+        int pos = m.base_eff + c;
+        pos -= pos >= L ? L : 0;
+#pragma unroll
+        for (int j = 0; j < T; ++j) {
+            if (same) {
+                const size_t e = h ? v0 + (size_t)pos * a.V : o0 + j * ostep;
+                store1(h ? a.ring_v : a.o, (long)e, bf, h ? vr[j] : oo[j]);
+            } else if (h == 0) {
+                store1(a.o, (long)(o0 + j * ostep), a.out_bf16, oo[j]);
             } else {
-                a.ring_d[((((size_t)m.s * a.HV + m.hv) * (a.V / VB) + m.vb) * L + pos) * VB + rr] = dn;
-                store1(a.ring_v, (((size_t)m.s * a.HV + m.hv) * L + pos) * a.V + vi, bf, vr);
+                store1(a.ring_v, (long)(v0 + (size_t)pos * a.V), bf, vr[j]);
             }
+            if (h) rd[pos * VB] = dd[j];
+            pos = pos + 1 == L ? 0 : pos + 1;
         }
 
         // the drafts' g and beta (first tile of each value head) and k (first tile
