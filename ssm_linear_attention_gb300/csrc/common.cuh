@@ -228,6 +228,15 @@ __device__ __forceinline__ float dot8_bf16(const uint4 s, const uint4 c, float a
     return acc;
 }
 
+// 16-byte asynchronous copy global -> shared without registers (cp.async, L2 only),
+// its group commit and the wait for all of this thread's copies.
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gsrc) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(smem_dst)), "l"(gsrc)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+
 __device__ __forceinline__ float load1(const void* base, long idx, bool is_bf16) {
     return is_bf16 ? bf16_to_f(reinterpret_cast<const uint16_t*>(base)[idx])
                    : reinterpret_cast<const float*>(base)[idx];

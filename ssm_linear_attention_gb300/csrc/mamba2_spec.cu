@@ -32,7 +32,7 @@ namespace rssm {
 namespace m2spec {
 
 constexpr int kMaxT = 4;
-constexpr int kThreads = 256;  // prologue CTA
+constexpr int kThreads = 128;  // prologue CTA
 
 // Per-(row, head) table: coef[T][L] (draft j's coefficient of entry i), Pm1[T],
 // the drafts' dt[T], padded to 4 floats.
@@ -65,33 +65,94 @@ struct ProArgs {
     float* ws;
     int32_t* dev_err;
     int batch, T, H, P, N, G, L, num_slots, act_bf16, state_bf16, softplus;
+    int n_tbl;   // table CTAs (batch * G), after the fold CTAs
+    int n_fold;  // persistent fold CTAs, first in the grid
 };
 
 __device__ __forceinline__ float ring_dt_at(const ProArgs& a, int s, int h, int pos) {
     return a.ring_dt[((size_t)s * a.H + h) * a.L + pos];
 }
 
-// Fold role: one (row, head) tile of a slot whose fold is pending. The scaled x
-// entries a_i x_i[p] and the B entries are staged in shared memory; thread t owns
-// 4 consecutive dstate columns of every
-// (256 / (N/4))-th headdim row, reads B as 16-byte vectors (consecutive threads,
-// consecutive columns) and the scaled x as broadcasts.
+// Fold of one (row, head) tile of a slot whose fold is pending:
+//   S0 <- Pm1 S0 + sum_{i<cnt} a_i x_i B_i^T,  a_i = exp(A sum_{l>i} dt_l) dt_i.
+// Thread t owns 4 consecutive dstate columns (n0 = 4 (t mod N/4)) of RPT consecutive
+// headdim rows (RPT = P N / 512: 8, 16 or 32, a multiple of 4). One round trip: the
+// committed x and B entries are copied into shared memory asynchronously (no
+// registers) while the thread's state rows (up to 16 of them; a float32 state: 8)
+// and the entries' dt are loaded into registers. A short pass then turns the staged
+// entries into float32 (x scaled by a_i), and the update runs 4 rows per pass as
+// packed two-wide FMAs. SBF / ABF: the state / the activations are bf16.
+template <bool V, bool BF>
+struct Raw4 {  // 4 state elements as loaded: bf16 pairs or float32
+    uint2 u;
+    __device__ __forceinline__ void load(const void* base, long i) {
+        u = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(base) + i);
+    }
+    __device__ __forceinline__ float4 f() const {
+        return make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
+    }
+};
+template <bool V>
+struct Raw4<V, false> {
+    float4 v;
+    __device__ __forceinline__ void load(const void* base, long i) {
+        v = *reinterpret_cast<const float4*>(static_cast<const float*>(base) + i);
+    }
+    __device__ __forceinline__ float4 f() const { return v; }
+};
+
+// Shared memory of the fold role (floats): x [L][P] and B [L][N] in float32, a_i and
+// Pm1 [L + 1] (padded to 4), then the raw staged entries (activation dtype).
+__host__ __device__ inline int fold_smem_floats(int P, int N, int L) {
+    return L * P + L * N + ((L + 1 + 3) & ~3) + L * (P + N);
+}
+
+template <bool SBF, bool ABF>
 __device__ void fold_tile(const ProArgs& a, int b, int h, float* sm) {
     const int s = a.ci[b];
-    if (s < 0 || s >= a.num_slots || !a.slot_flush[s]) return;
     const int cnt = a.slot_cnt[s], base = a.slot_base[s], L = a.L;
-    if (cnt < 0 || cnt > L || base < 0 || base >= L || cnt == 0) return;
+    if (cnt <= 0 || cnt > L || base < 0 || base >= L) return;
     const int P = a.P, N = a.N, g = h / (a.H / a.G);
-    const bool bf = a.act_bf16, sbf = a.state_bf16;
+    constexpr int ss = SBF ? 2 : 4, sa = ABF ? 2 : 4;
     const int t = threadIdx.x;
-    float* ax = sm;              // [cnt][P]: a_i x_i[p]
-    float* bs = ax + L * P;      // [cnt][N]
-    float* cf = bs + L * N;      // [cnt] a_i, then Pm1
-    __syncthreads();             // the previous tile's readers are done with the buffers
+    float* xs = sm;                                  // [cnt][P]: a_i x_i[p]
+    float* bs = xs + L * P;                          // [cnt][N]
+    float* cf = bs + L * N;                          // [cnt] a_i, then Pm1
+    uint8_t* xr = reinterpret_cast<uint8_t*>(cf + ((L + 1 + 3) & ~3));  // [cnt][P] raw
+    uint8_t* br = xr + (size_t)L * P * sa;                             // [cnt][N] raw
+    const int ncg = N / 4;
+    const int n0 = (t % ncg) * 4, rg = t / ncg;
+    const int RPT = P * ncg / kThreads;
+    const int p0 = rg * RPT;
+    char* st = static_cast<char*>(a.state) + ((size_t)s * a.H + h) * P * N * ss;
+    constexpr int RB = 4;               // rows per pass (few live accumulators)
+    constexpr int RMAX = SBF ? 16 : 8;  // rows loaded per round trip, held in registers
+    const int rl = RPT < RMAX ? RPT : RMAX;
+
+    __syncthreads();  // the previous tile's readers are done with the buffers
+    {
+        const int xc = P * sa / 16, bc_ = N * sa / 16;  // 16-byte chunks per entry
+        const char* xsrc = static_cast<const char*>(a.ring_x) + ((size_t)s * a.H + h) * L * P * sa;
+        const char* bsrc = static_cast<const char*>(a.ring_B) + ((size_t)s * a.G + g) * L * N * sa;
+        for (int e = t; e < cnt * (xc + bc_); e += kThreads) {
+            if (e < cnt * xc) {
+                const int i = e / xc, c16 = e - i * xc;
+                cp_async16(xr + (size_t)e * 16, xsrc + (size_t)((base + i) % L) * P * sa + c16 * 16);
+            } else {
+                const int e2 = e - cnt * xc, i = e2 / bc_, c16 = e2 - i * bc_;
+                cp_async16(br + (size_t)e2 * 16, bsrc + (size_t)((base + i) % L) * N * sa + c16 * 16);
+            }
+        }
+        cp_async_commit();
+    }
+    Raw4<true, SBF> sv[RMAX];
+#pragma unroll
+    for (int k = 0; k < RMAX; ++k)
+        if (k < rl) sv[k].load(st, (long)(p0 + k) * N + n0);
+    const float dti = t < cnt ? ring_dt_at(a, s, h, (base + t) % L) : 0.f;
     if (t < 32) {
         // a_i = prod_{l>i} dA_l * dt_i from a suffix sum over the committed entries
         const float Ah = a.A[h];
-        const float dti = t < cnt ? ring_dt_at(a, s, h, (base + t) % L) : 0.f;
         float suf = dti;  // inclusive suffix sum: sum_{l>=t} dt_l
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
@@ -102,160 +163,246 @@ __device__ void fold_tile(const ProArgs& a, int b, int h, float* sm) {
         const float total = __shfl_sync(kFull, suf, 0);
         if (t == 0) cf[cnt] = expf(Ah * total);
     }
-    for (int e = t; e < cnt * N; e += kThreads) {
-        const int i = e / N, n = e - (e / N) * N;
-        bs[e] = load1(a.ring_B, (((long)s * a.G + g) * L + (base + i) % L) * N + n, bf);
-    }
+    cp_async_wait_all();
     __syncthreads();
-    for (int e = t; e < cnt * P; e += kThreads) {
-        const int i = e / P, p = e - (e / P) * P;
-        ax[e] = cf[i] * load1(a.ring_x, (((long)s * a.H + h) * L + (base + i) % L) * P + p, bf);
+    // the staged entries in float32, x scaled by a_i (4 elements at a time)
+    for (int e = t; e < cnt * (P + N) / 4; e += kThreads) {
+        float f[4];
+        if (e < cnt * P / 4) {
+            load4(xr, e * 4, ABF, f);
+            const float c_ = cf[e / (P / 4)];
+            *reinterpret_cast<float4*>(xs + e * 4) = make_float4(c_ * f[0], c_ * f[1], c_ * f[2], c_ * f[3]);
+        } else {
+            const int e2 = e - cnt * P / 4;
+            load4(br, e2 * 4, ABF, f);
+            *reinterpret_cast<float4*>(bs + e2 * 4) = make_float4(f[0], f[1], f[2], f[3]);
+        }
     }
     __syncthreads();
     const float Pm1 = cf[cnt];
-    const int ncg = N / 4;                 // column groups of 4
-    const int n0 = (t % ncg) * 4, r0 = t / ncg, rst = kThreads / ncg;
-    char* st = static_cast<char*>(a.state) + ((size_t)s * a.H + h) * P * N * (sbf ? 2 : 4);
-    constexpr int RB = 4;  // rows of this thread per pass (keeps the CTA's registers low)
-    for (int pb = r0; pb < P; pb += RB * rst) {
-        float acc[RB][4];
+    for (int r0 = 0; r0 < RPT; r0 += RMAX) {
+        if (r0 > 0) {  // only when the thread has more rows than one round holds
 #pragma unroll
-        for (int k = 0; k < RB; ++k) {
-            const int p = pb + k * rst;
-            if (p < P) {
-                float s4[4];
-                load4(st, p * N + n0, sbf, s4);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) acc[k][e] = Pm1 * s4[e];
-            }
+            for (int k = 0; k < RMAX; ++k)
+                if (r0 + k < RPT) sv[k].load(st, (long)(p0 + r0 + k) * N + n0);
         }
-        for (int i = 0; i < cnt; ++i) {
-            const float4 b4 = *reinterpret_cast<const float4*>(bs + i * N + n0);
+#pragma unroll
+        for (int q = 0; q < RMAX; q += RB) {
+            if (r0 + q >= RPT) break;
+            float2 acc[RB][2];
 #pragma unroll
             for (int k = 0; k < RB; ++k) {
-                const int p = pb + k * rst;
-                if (p < P) {
-                    const float xv = ax[i * P + p];
-                    acc[k][0] = fmaf(xv, b4.x, acc[k][0]);
-                    acc[k][1] = fmaf(xv, b4.y, acc[k][1]);
-                    acc[k][2] = fmaf(xv, b4.z, acc[k][2]);
-                    acc[k][3] = fmaf(xv, b4.w, acc[k][3]);
+                const float4 f = sv[q + k].f();
+                acc[k][0] = make_float2(Pm1 * f.x, Pm1 * f.y);
+                acc[k][1] = make_float2(Pm1 * f.z, Pm1 * f.w);
+            }
+            const int pr = p0 + r0 + q;  // first row of this pass
+            for (int i = 0; i < cnt; ++i) {
+                const float4 b4 = *reinterpret_cast<const float4*>(bs + i * N + n0);
+                const float4 x4 = *reinterpret_cast<const float4*>(xs + i * P + pr);
+                const float2 blo = make_float2(b4.x, b4.y), bhi = make_float2(b4.z, b4.w);
+                const float xk[RB] = {x4.x, x4.y, x4.z, x4.w};
+#pragma unroll
+                for (int k = 0; k < RB; ++k) {
+                    const float2 x2 = make_float2(xk[k], xk[k]);
+                    acc[k][0] = __ffma2_rn(x2, blo, acc[k][0]);
+                    acc[k][1] = __ffma2_rn(x2, bhi, acc[k][1]);
                 }
             }
-        }
 #pragma unroll
-        for (int k = 0; k < RB; ++k) {
-            const int p = pb + k * rst;
-            if (p < P) {
-                char* d = st + (size_t)(p * N + n0) * (sbf ? 2 : 4);
-                if (sbf) {
-                    *reinterpret_cast<uint2*>(d) =
-                        make_uint2(pack_bf16x2(acc[k][0], acc[k][1]), pack_bf16x2(acc[k][2], acc[k][3]));
+            for (int k = 0; k < RB; ++k) {
+                char* d = st + (size_t)((pr + k) * N + n0) * ss;
+                if constexpr (SBF) {
+                    *reinterpret_cast<uint2*>(d) = make_uint2(pack_bf16x2(acc[k][0].x, acc[k][0].y),
+                                                              pack_bf16x2(acc[k][1].x, acc[k][1].y));
                 } else {
-                    *reinterpret_cast<float4*>(d) = make_float4(acc[k][0], acc[k][1], acc[k][2], acc[k][3]);
+                    *reinterpret_cast<float4*>(d) =
+                        make_float4(acc[k][0].x, acc[k][0].y, acc[k][1].x, acc[k][1].y);
                 }
             }
         }
     }
 }
 
-// Table role: one row. bc[g][i][j] = B_i . C_j for the row's entries i (history
-// from the ring, then the drafts' B) and drafts j; then per (head, draft) the
-// decay suffix sums give coef[j][i], Pm1[j], and the drafts' dt.
-__device__ void row_tables(const ProArgs& a, int b, float* sm) {
+// Fold role (CTA f of n_fold): every fold CTA builds the same ascending list of the
+// rows with a pending fold (ballots over the batch), and the list's (row, head)
+// tiles are dealt round-robin over the fold CTAs. Rows beyond kFoldRows are
+// checked per tile instead.
+constexpr int kFoldRows = 1024;
+
+template <bool SBF, bool ABF>
+__device__ void fold_role(const ProArgs& a, int f, float* sm) {
+    __shared__ int rows[kFoldRows];
+    __shared__ int wsum[kThreads / 32];
+    const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
+    auto pending = [&](int b) {
+        const int s = a.ci[b];
+        return s >= 0 && s < a.num_slots && a.slot_flush[s];
+    };
+    const int nl = a.batch < kFoldRows ? a.batch : kFoldRows;  // rows taken into the list
+    int base = 0;
+    for (int b0 = 0; b0 < nl; b0 += kThreads) {
+        const int b = b0 + t;
+        const bool flag = b < nl && pending(b);
+        const unsigned m = __ballot_sync(kFull, flag);
+        if (lane == 0) wsum[warp] = __popc(m);
+        __syncthreads();
+        int off = base;
+        for (int w = 0; w < warp; ++w) off += wsum[w];
+        if (flag) rows[off + __popc(m & ((1u << lane) - 1u))] = b;
+        int total = 0;
+        for (int w = 0; w < kThreads / 32; ++w) total += wsum[w];
+        base += total;
+        __syncthreads();
+    }
+    const int tiles = base * a.H;
+    for (int x = f; x < tiles; x += a.n_fold) {
+        const int ri = x / a.H;
+        fold_tile<SBF, ABF>(a, rows[ri], x - ri * a.H, sm);
+    }
+    // rows past the list (batches above kFoldRows): tile by tile
+    const long rest = (long)(a.batch - nl) * a.H;
+    for (long x = f; x < rest; x += a.n_fold) {
+        const int b = nl + (int)(x / a.H);
+        if (pending(b)) fold_tile<SBF, ABF>(a, b, (int)(x - (long)(b - nl) * a.H), sm);
+    }
+}
+
+// Table role: one (row, group). bc[i][j] = B_i . C_j for the row's entries i
+// (history from the ring, then the drafts' B) and drafts j; then per (head of the
+// group, draft) the decay suffix sums give coef[j][i], Pm1[j], and the drafts' dt.
+// Every global load is issued before the first use.
+__device__ void group_tables(const ProArgs& a, int b, int g, float* sm) {
     const int s = a.ci[b];
     if (s < 0) return;
     if (s >= a.num_slots) {
-        if (threadIdx.x == 0) set_dev_err(a.dev_err, RSSM_DEVERR_SLOT);
+        if (threadIdx.x == 0 && g == 0) set_dev_err(a.dev_err, RSSM_DEVERR_SLOT);
         return;
     }
     const int L = a.L, T = a.T, H = a.H, N = a.N, G = a.G;
     int c, base_eff;
     if (!history(a.slot_cnt[s], a.slot_base[s], a.slot_flush[s], L, T, &c, &base_eff)) {
-        if (threadIdx.x == 0) set_dev_err(a.dev_err, RSSM_DEVERR_CURSOR);
+        if (threadIdx.x == 0 && g == 0) set_dev_err(a.dev_err, RSSM_DEVERR_CURSOR);
         return;
     }
     const int ne = c + T;  // entries: history, then drafts
+    const int hpg = H / G;
     const bool bf = a.act_bf16;
     const int t = threadIdx.x, lane = t & 31, warp = t >> 5;
-    float* bc = sm;                    // [G][ne][T]
-    float* dts = bc + G * L * kMaxT;   // [H][ne]
-    // B_i . C_j: a warp per (g, i), lanes over dstate
-    for (int gi = warp; gi < G * ne; gi += kThreads / 32) {
-        const int g = gi / ne, i = gi - (gi / ne) * ne;
-        const char* bsrc;
-        if (i < c) {
-            bsrc = static_cast<const char*>(a.ring_B) +
-                   (((size_t)s * G + g) * L + (base_eff + i) % L) * N * (bf ? 2 : 4);
-        } else {
-            bsrc = static_cast<const char*>(a.B) +
-                   (((size_t)b * T + (i - c)) * G + g) * N * (bf ? 2 : 4);
+    float* Cs = sm;                 // [T][N]
+    float* Bs = Cs + kMaxT * N;     // [ne][N]
+    float* dts = Bs + L * N;        // [hpg][ne]
+    float* bc = dts + hpg * L;      // [ne][T]
+    const int nc4 = T * (N / 4), nb4 = ne * (N / 4), nd = hpg * ne;
+    constexpr int KC = (kMaxT * 128 / 4 + kThreads - 1) / kThreads;
+    constexpr int KB = (32 * 128 / 4 + kThreads - 1) / kThreads;
+    float cv[KC][4], bv[KB][4];
+#pragma unroll
+    for (int u = 0; u < KC; ++u) {
+        const int e = t + u * kThreads;
+        if (e < nc4) {
+            const int j = e / (N / 4), c4 = e - j * (N / 4);
+            load4(a.C, (int)((((size_t)b * T + j) * G + g) * N) + c4 * 4, bf, cv[u]);
         }
+    }
+#pragma unroll
+    for (int u = 0; u < KB; ++u) {
+        const int e = t + u * kThreads;
+        if (e < nb4) {
+            const int i = e / (N / 4), c4 = e - i * (N / 4);
+            if (i < c)
+                load4(a.ring_B, (int)((((size_t)s * G + g) * L + (base_eff + i) % L) * N) + c4 * 4, bf, bv[u]);
+            else
+                load4(a.B, (int)((((size_t)b * T + (i - c)) * G + g) * N) + c4 * 4, bf, bv[u]);
+        }
+    }
+    for (int e0 = t; e0 < nd; e0 += 4 * kThreads) {  // four loads in flight per thread
+        float dv[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int e = e0 + u * kThreads;
+            if (e < nd) {
+                const int hl = e / ne, i = e - (e / ne) * ne, h = g * hpg + hl;
+                dv[u] = i < c ? ring_dt_at(a, s, h, (base_eff + i) % L)
+                              : a.dt_raw[((size_t)b * T + (i - c)) * H + h] + (a.dt_bias ? a.dt_bias[h] : 0.f);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int e = e0 + u * kThreads;
+            if (e < nd) {
+                const int i = e - (e / ne) * ne;
+                dts[e] = (i >= c && a.softplus) ? softplus_f(dv[u]) : dv[u];
+            }
+        }
+    }
+#pragma unroll
+    for (int u = 0; u < KC; ++u) {
+        const int e = t + u * kThreads;
+        if (e < nc4) *reinterpret_cast<float4*>(Cs + e * 4) = make_float4(cv[u][0], cv[u][1], cv[u][2], cv[u][3]);
+    }
+#pragma unroll
+    for (int u = 0; u < KB; ++u) {
+        const int e = t + u * kThreads;
+        if (e < nb4) *reinterpret_cast<float4*>(Bs + e * 4) = make_float4(bv[u][0], bv[u][1], bv[u][2], bv[u][3]);
+    }
+    __syncthreads();
+    // B_i . C_j: a warp per entry i, lanes over dstate (4 columns each), one
+    // reduce-scatter over the T dots
+    for (int i = warp; i < ne; i += kThreads / 32) {
         float part[kMaxT];
 #pragma unroll
         for (int j = 0; j < kMaxT; ++j) part[j] = 0.f;
-        for (int n = lane; n < N; n += 32) {
-            const float bv = load1(bsrc, n, bf);
+        for (int n = lane * 4; n < N; n += 128) {
+            const float4 b4 = *reinterpret_cast<const float4*>(Bs + i * N + n);
 #pragma unroll
-            for (int j = 0; j < kMaxT; ++j)
-                if (j < T)
-                    part[j] = fmaf(bv, load1(a.C, (((long)b * T + j) * G + g) * N + n, bf), part[j]);
+            for (int j = 0; j < kMaxT; ++j) {
+                if (j < T) {
+                    const float4 c4 = *reinterpret_cast<const float4*>(Cs + j * N + n);
+                    part[j] = fmaf(b4.x, c4.x, fmaf(b4.y, c4.y, fmaf(b4.z, c4.z, fmaf(b4.w, c4.w, part[j]))));
+                }
+            }
         }
-#pragma unroll
-        for (int j = 0; j < kMaxT; ++j) {
-#pragma unroll
-            for (int o = 16; o >= 1; o >>= 1) part[j] += __shfl_xor_sync(kFull, part[j], o);
-        }
-        if (lane == 0)
-            for (int j = 0; j < T; ++j) bc[(g * ne + i) * T + j] = part[j];
-    }
-    for (int e = t; e < H * ne; e += kThreads) {
-        const int h = e / ne, i = e - (e / ne) * ne;
-        float dt;
-        if (i < c) {
-            dt = ring_dt_at(a, s, h, (base_eff + i) % L);
-        } else {
-            dt = a.dt_raw[((size_t)b * T + (i - c)) * H + h] + (a.dt_bias ? a.dt_bias[h] : 0.f);
-            if (a.softplus) dt = softplus_f(dt);
-        }
-        dts[h * ne + i] = dt;
+        const int e = reduce_scatter<kMaxT, 32>(part);
+        if ((lane & 7) == 0 && e < T) bc[i * T + e] = part[0];
     }
     __syncthreads();
     const int TB = tbl_floats(L, T);
-    const int hpg = H / G;
-    for (int e = t; e < H * T; e += kThreads) {
-        const int h = e / T, j = e - (e / T) * T;
-        const int g = h / hpg, m = c + j;
+    for (int e = t; e < hpg * T; e += kThreads) {
+        const int hl = e / T, j = e - (e / T) * T, h = g * hpg + hl;
+        const int m = c + j;
         const float Ah = a.A[h];
         float* tb = a.ws + ((size_t)b * H + h) * TB;
+        const float* dh = dts + hl * ne;
         float cum = 0.f;
         for (int i = m; i >= 0; --i) {
-            const float dti = dts[h * ne + i];
-            tb[j * L + i] = expf(Ah * cum) * dti * bc[(g * ne + i) * T + j];
+            const float dti = dh[i];
+            tb[j * L + i] = expf(Ah * cum) * dti * bc[i * T + j];
             cum += dti;
         }
         tb[T * L + j] = expf(Ah * cum);
-        tb[T * L + T + j] = dts[h * ne + m];
+        tb[T * L + T + j] = dh[m];
     }
 }
 
-// Grid: the table CTAs (one per row), then one fold CTA per (row, head) tile; a
-// fold CTA whose slot has no pending fold exits at once, and the block scheduler
-// balances the pending tiles over the SMs.
+// Grid: the persistent fold CTAs (the long ones, they start first and hold part of
+// each SM), then the table CTAs (one per (row, group)), which fill the other slots.
+// One instance per state / activation dtype pair.
+template <bool SBF, bool ABF>
 __global__ void __launch_bounds__(kThreads, 6) prologue_kernel(const ProArgs a) {
-    extern __shared__ float psm[];
+    extern __shared__ __align__(16) float psm[];
     const int blk = blockIdx.x;
-    if (blk < a.batch) {
-        row_tables(a, blk, psm);
+    if (blk < a.n_fold) {
+        fold_role<SBF, ABF>(a, blk, psm);
         return;
     }
-    const int it = blk - a.batch;
-    fold_tile(a, it / a.H, it - (it / a.H) * a.H, psm);
+    const int tb = blk - a.n_fold;
+    group_tables(a, tb / a.G, tb - (tb / a.G) * a.G, psm);
 }
 
 inline int pro_smem_floats(int H, int P, int N, int G, int L) {
-    const int tables = G * L * kMaxT + H * L;
-    const int fold = L * P + L * N + L + 1;
+    const int tables = kMaxT * N + L * N + (H / G) * L + L * kMaxT;
+    const int fold = fold_smem_floats(P, N, L);
     return tables > fold ? tables : fold;
 }
 
@@ -410,6 +557,16 @@ struct VerPolicy {
             for (int ch = 0; ch < NCH; ++ch) reduce_scatter<NQ, NQ>(part[j] + ch * NQ);
         const float Dh = __ldg(a.D + m.h);
         const int pos0 = m.base_eff + c;
+        int posj[T];  // the drafts' ring positions
+        {
+            int p_ = pos0 >= L ? pos0 - L : pos0;
+#pragma unroll
+            for (int j = 0; j < T; ++j) {
+                posj[j] = p_;
+                p_ = p_ + 1 == L ? 0 : p_ + 1;
+            }
+        }
+        const size_t ystep = (size_t)a.H * P;
 #pragma unroll
         for (int ch = 0; ch < NCH; ++ch) {
             const int p = row0 + RPI * (ch * NQ + q);
@@ -421,7 +578,7 @@ struct VerPolicy {
 #pragma unroll
                 for (int j = 0; j < T; ++j) hist[j] = fmaf(tbl[j * L + i], xi, hist[j]);
             }
-            float xdv[T];
+            float xdv[T], yv[T];
 #pragma unroll
             for (int j = 0; j < T; ++j) xdv[j] = load1(xd, j * P + p, bf);
 #pragma unroll
@@ -431,10 +588,16 @@ struct VerPolicy {
                 for (int jj = 0; jj <= j; ++jj) acc = fmaf(tbl[j * L + c + jj], xdv[jj], acc);
                 acc = fmaf(Dh, xdv[j], acc);
                 if (a.z) acc *= silu_f(load1(sb + a.off_z, j * P + p, bf));
-                store1(a.y, (((size_t)m.b * T + j) * a.H + m.h) * P + p, a.out_bf16, acc);
-                // the draft's x into the ring (exact: the value came in this dtype)
-                store1(a.ring_x, (((size_t)m.s * a.H + m.h) * L + (pos0 + j) % L) * P + p, bf,
-                       xdv[j]);
+                yv[j] = acc;
+            }
+            // the outputs, then the drafts' x into the ring (exact: the value came in
+            // this dtype)
+            const size_t y0 = (((size_t)m.b * T) * a.H + m.h) * P + p;
+            const size_t x0 = ((size_t)m.s * a.H + m.h) * L * P + p;
+#pragma unroll
+            for (int j = 0; j < T; ++j) {
+                store1(a.y, (long)(y0 + j * ystep), a.out_bf16, yv[j]);
+                store1(a.ring_x, (long)(x0 + (size_t)posj[j] * P), bf, xdv[j]);
             }
         }
         // the drafts' dt (one lane) and B (first head of each group, warp 0)
@@ -518,17 +681,25 @@ int m2spec_launch(const rssm_mamba2_dims* d, void* state, const void* x, const f
     pa.state_bf16 = d->state_dtype == RSSM_BF16; pa.softplus = dt_softplus != 0;
     const int psmem = m2spec::pro_smem_floats(H, P, N, G, L) * 4;
     if (psmem > di.max_smem_optin) return RSSM_ERR_UNSUPPORTED;
-    if (psmem > 48 * 1024 &&
-        !ensure_smem_limit(reinterpret_cast<const void*>(m2spec::prologue_kernel), psmem))
+    const bool sbf = d->state_dtype == RSSM_BF16, abf = d->act_dtype == RSSM_BF16;
+    auto kern = sbf ? (abf ? m2spec::prologue_kernel<true, true> : m2spec::prologue_kernel<true, false>)
+                    : (abf ? m2spec::prologue_kernel<false, true> : m2spec::prologue_kernel<false, false>);
+    if (psmem > 48 * 1024 && !ensure_smem_limit(reinterpret_cast<const void*>(kern), psmem))
         return RSSM_ERR_CUDA;
-    const long blocks = (long)d->batch + (long)d->batch * H;
-    m2spec::prologue_kernel<<<(unsigned)blocks, m2spec::kThreads, psmem, st>>>(pa);
+    pa.n_tbl = d->batch * G;
+    {
+        long nf = (long)di.sm_count * 4;  // four of the six CTA slots of an SM
+        const long tiles = (long)d->batch * H;
+        if (nf > tiles) nf = tiles;
+        pa.n_fold = (int)nf;
+    }
+    const long blocks = (long)pa.n_tbl + pa.n_fold;
+    kern<<<(unsigned)blocks, m2spec::kThreads, psmem, st>>>(pa);
     if (launch_status()) return RSSM_ERR_CUDA;
 
     // 2. verify (and the drafts' ring entries)
     VerLaunch<T> g{d, state, x, z, B, C, D, static_cast<const float*>(workspace), ring_x, ring_B, y, ring_dt,
         ci, slot_cnt, slot_base, slot_flush, dev_err, st};
-    const bool sbf = d->state_dtype == RSSM_BF16;
 #define RSSM_M2S_CASE(PP, NN)                                                 \
     if (P == PP && N == NN) return sbf ? g.template go<PP, NN, StBF16>()      \
                                        : g.template go<PP, NN, StF32>();
