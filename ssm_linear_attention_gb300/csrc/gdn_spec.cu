@@ -13,15 +13,17 @@
 //
 // Launches of one verify round:
 //   prologue_kernel    two kinds of CTA in one grid, independent of each other:
-//     table role       one CTA per (row, key head): dot products of every live
-//                      key (history and drafts) with the drafts' keys and
-//                      queries, products of gates, into a per-(row, value head)
-//                      table. These CTAs come first in the grid (they are short).
-//     fold role        a persistent set of CTAs folds the (row, value head,
-//                      32-row block) tiles of the slots with a pending fold, dealt
-//                      evenly: S0 rows in registers (4 threads per row), the
-//                      committed entries staged in shared memory, cnt sequential
+//     fold role        a persistent set of CTAs, first in the grid (they are the
+//                      long ones) on four of the six CTA slots of an SM, folds the
+//                      (row, value head, 32-row block) tiles of the slots with a
+//                      pending fold, dealt evenly: S0 rows in registers (4 threads
+//                      per row), the committed entries copied into shared memory
+//                      asynchronously while those rows load, cnt sequential
 //                      delta-rule updates from ring k, raw v, beta, g; S0 stored.
+//     table role       one CTA per (row, key head), on the remaining slots: dot
+//                      products of every live key (history and drafts) with the
+//                      drafts' keys and queries, products of gates, into a
+//                      per-(row, value head) table.
 //   verify_kernel<T>   persistent TMA pipeline over (row, value head, 32-row
 //                      block) tiles of S0: the 2T dot products per value row,
 //                      then the draft chain per row; writes o, the drafts' d and
@@ -100,12 +102,13 @@ struct ProArgs {
     int T, HV, HK, V, L, num_slots, act_bf16;
     int batch;
     int n_items;  // fold work items: batch * HV * V/VB tiles
-    int n_pre;    // table CTAs (batch * HK), first in the grid: they are short
-    int n_fold;   // fold CTAs, after them (fold CTA f owns the items it = f mod n_fold)
+    int n_pre;    // table CTAs (batch * HK), after the fold CTAs
+    int n_fold;   // persistent fold CTAs, first in the grid (they are the long ones)
 };
 
-// Shared memory of the fold role (floats): k [16][KD], raw v [16][VB], beta, g.
-__host__ __device__ inline int fold_smem_floats() { return kFoldChunk * (KD + VB + 2); }
+// Shared memory of the fold role (floats): k [16][KD], raw v [16][VB], beta, g in
+// float32, then the chunk's keys and values as copied (activation dtype).
+__host__ __device__ inline int fold_smem_floats() { return kFoldChunk * (KD + VB + 2) + kFoldChunk * (KD + VB); }
 
 // Shared memory of the table role (floats): KK [L][T], KQ [L][T], gates
 // [HV/HK][L], the drafts' k and q [T][2][KD], the history keys [L][KD].
@@ -145,35 +148,45 @@ __device__ void fold_tile(const ProArgs& a, int item, float* sm) {
         S2[2 * u + 1] = make_float2(v4.z, v4.w);
     }
     const char* kr = static_cast<const char*>(a.ring_k) + ((size_t)s * a.HK + kh) * L * KD * sa;
+    const char* vr = static_cast<const char*>(a.ring_v) + (((size_t)s * a.HV + hv) * L * a.V + (size_t)vb * VB) * sa;
+    uint8_t* kraw = reinterpret_cast<uint8_t*>(gs + kFoldChunk);  // [16][KD] as copied
+    uint8_t* vraw = kraw + kFoldChunk * KD * 4;                    // [16][VB] as copied
     for (int e0 = 0; e0 < cnt; e0 += kFoldChunk) {
         const int ne = cnt - e0 < kFoldChunk ? cnt - e0 : kFoldChunk;
-        // every load of the chunk is issued before any shared-memory store
-        constexpr int KU = kFoldChunk * (KD / 4) / kThreads;  // k chunks per thread
-        float kv[KU][4], vv[4], bv = 0.f, gv = 0.f;
-#pragma unroll
-        for (int u = 0; u < KU; ++u) {
-            const int e = t + u * kThreads, i = e / (KD / 4), c4 = e - (e / (KD / 4)) * (KD / 4);
-            if (i < ne) load4(kr + (size_t)((base + e0 + i) % L) * KD * sa, c4 * 4, bf, kv[u]);
+        __syncthreads();  // the previous chunk (or tile) is no longer read
+        // the chunk's keys and raw values by asynchronous copies (no registers, in
+        // flight together with the state rows), beta and g into registers
+        const int kc16 = KD * sa / 16, vc16 = VB * sa / 16;
+        for (int e = t; e < ne * (kc16 + vc16); e += kThreads) {
+            if (e < ne * kc16) {
+                const int i = e / kc16, c16 = e - i * kc16;
+                cp_async16(kraw + (size_t)e * 16, kr + (size_t)((base + e0 + i) % L) * KD * sa + c16 * 16);
+            } else {
+                const int e2 = e - ne * kc16, i = e2 / vc16, c16 = e2 - i * vc16;
+                cp_async16(vraw + (size_t)e2 * 16,
+                           vr + (size_t)((base + e0 + i) % L) * a.V * sa + c16 * 16);
+            }
         }
-        const int vi = t / (VB / 4), vc = t - (t / (VB / 4)) * (VB / 4);  // kThreads == 16 * VB / 4
-        if (vi < ne)
-            load4(static_cast<const char*>(a.ring_v) +
-                      ((((size_t)s * a.HV + hv) * L + (base + e0 + vi) % L) * a.V + (size_t)vb * VB) * sa,
-                  vc * 4, bf, vv);
+        cp_async_commit();
+        float bv = 0.f, gv = 0.f;
         if (t < ne) {
             const int pos = (base + e0 + t) % L;
             bv = a.ring_beta[((size_t)s * a.HV + hv) * L + pos];
             gv = a.ring_g[((size_t)s * a.HV + hv) * L + pos];
         }
-        __syncthreads();  // the previous chunk is no longer read
-#pragma unroll
-        for (int u = 0; u < KU; ++u) {
-            const int e = t + u * kThreads, i = e / (KD / 4), c4 = e - (e / (KD / 4)) * (KD / 4);
-            if (i < ne)
-                *reinterpret_cast<float4*>(ks + i * KD + c4 * 4) =
-                    make_float4(kv[u][0], kv[u][1], kv[u][2], kv[u][3]);
+        cp_async_wait_all();
+        __syncthreads();
+        for (int e = t; e < ne * (KD + VB) / 4; e += kThreads) {  // float32 copies
+            float f[4];
+            if (e < ne * KD / 4) {
+                load4(kraw, e * 4, bf, f);
+                *reinterpret_cast<float4*>(ks + e * 4) = make_float4(f[0], f[1], f[2], f[3]);
+            } else {
+                const int e2 = e - ne * KD / 4;
+                load4(vraw, e2 * 4, bf, f);
+                *reinterpret_cast<float4*>(vs + e2 * 4) = make_float4(f[0], f[1], f[2], f[3]);
+            }
         }
-        if (vi < ne) *reinterpret_cast<float4*>(vs + vi * VB + vc * 4) = make_float4(vv[0], vv[1], vv[2], vv[3]);
         if (t < ne) {
             bs[t] = bv;
             gs[t] = gv;
@@ -406,8 +419,8 @@ __device__ void fold_role(const ProArgs& a, int f, float* sm) {
 template <int T>
 __global__ void __launch_bounds__(kThreads, 6) prologue_kernel(const ProArgs a) {
     extern __shared__ __align__(16) float psm[];
-    if ((int)blockIdx.x < a.n_pre) pre_head<T>(a, blockIdx.x, psm);
-    else fold_role(a, blockIdx.x - a.n_pre, psm);
+    if ((int)blockIdx.x < a.n_fold) fold_role(a, blockIdx.x, psm);
+    else pre_head<T>(a, blockIdx.x - a.n_fold, psm);
 }
 
 // ----------------------------------------------------------------------------
@@ -700,7 +713,7 @@ int spec_launch(const rssm_gdn_dims* d, float* state, const void* q, const void*
     pa.n_items = d->batch * HV * NVB;
     {
         const int per = (pa.n_items + spec::kFoldList - 1) / spec::kFoldList;  // CTAs for <= kFoldList each
-        int nf = di.sm_count * 6;
+        int nf = di.sm_count * 4;  // four of the six CTA slots of an SM; tables fill the rest
         if (nf < per) nf = per;
         if (nf > pa.n_items) nf = pa.n_items;
         pa.n_fold = nf;
