@@ -336,6 +336,9 @@ struct StBF16SR {
 __device__ __forceinline__ float softplus_f(float x) { return x > 20.f ? x : log1pf(expf(x)); }
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.f + expf(-z)); }
+// The same gate through the fast exponential and division intrinsics (a few ulp):
+// for per-draft epilogues where the accurate path's latency shows.
+__device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.f + __expf(-z)); }
 
 // ----------------------------------------------------------------------------
 // warp reduce-scatter

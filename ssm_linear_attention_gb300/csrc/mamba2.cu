@@ -289,7 +289,7 @@ struct OutPolicy {
             if (i == w) yv = fmaf(tbl[w], load1(xr, w * P + p, bf), yv);
             yv += y2;
             yv = fmaf(Dh, load1(xr, w * P + p, bf), yv);
-            if (a.z) yv *= silu_f(load1(sb + a.off_z, p, bf));
+            if (a.z) yv *= silu_fast(load1(sb + a.off_z, p, bf));
             store1(a.y, ((size_t)m.b * a.H + m.h) * P + p, a.out_bf16, yv);
         }
         if (!m.f) return;
@@ -634,7 +634,7 @@ struct FullPolicy {
         for (int ch = 0; ch < Sh::NCH; ++ch) {
             const int p = row0 + Sh::RPI * (ch * Sh::NQ + q);
             float acc = fmaf(Dh, load1(sb + a.off_x, p, bf), part[ch * Sh::NQ]);
-            if (a.z) acc *= silu_f(load1(sb + a.off_z, p, bf));
+            if (a.z) acc *= silu_fast(load1(sb + a.off_z, p, bf));
             store1(a.y, ((size_t)m.b * a.H + m.h) * P + p, a.out_bf16, acc);
         }
     }

@@ -259,7 +259,7 @@ __global__ void __launch_bounds__(kThreads) step_kernel(const Args a) {
         float yv = Pm1 * part[ch * NQ];
         for (int i = 0; i <= w; ++i) yv = fmaf(coef[i], load1(xr, i * P + p, bf), yv);
         yv = fmaf(Dh, load1(xr, w * P + p, bf), yv);
-        if (a.z) yv *= silu_f(load1(sm + lo.z, p, bf));
+        if (a.z) yv *= silu_fast(load1(sm + lo.z, p, bf));
         store1(a.y, ((size_t)b * H + h) * P + p, a.out_bf16, yv);
     }
     if (!f) return;

@@ -587,7 +587,7 @@ struct VerPolicy {
 #pragma unroll
                 for (int jj = 0; jj <= j; ++jj) acc = fmaf(tbl[j * L + c + jj], xdv[jj], acc);
                 acc = fmaf(Dh, xdv[j], acc);
-                if (a.z) acc *= silu_f(load1(sb + a.off_z, j * P + p, bf));
+                if (a.z) acc *= silu_fast(load1(sb + a.off_z, j * P + p, bf));
                 yv[j] = acc;
             }
             // the outputs, then the drafts' x into the ring (exact: the value came in
