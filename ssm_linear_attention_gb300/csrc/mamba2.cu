@@ -690,7 +690,7 @@ struct OutLaunch {
         // the tensor-core fold takes 64 x 128 tiles, bf16 ring entries and at most 16 of
         // them; rings too short to reach kTcMinEntries entries keep the leaner kernel
         if constexpr (P == 64 && N == 128) {
-            if (c.act_bf16 && c.L >= kTcMinEntries && c.L <= kTcMaxEntries)
+            if (!ST::sr && c.act_bf16 && c.L >= kTcMinEntries && c.L <= kTcMaxEntries)
                 return run<OutPolicy<P, N, ST, true>, P, N>();
         }
         return run<OutPolicy<P, N, ST, false>, P, N>();
