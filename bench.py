@@ -6,13 +6,12 @@ pool of 1024 slots ~ N(0, 0.1), cache indices = first 512 of a seeded
 permutation, desynchronised initial write_pos ~ U{0..15}, x/z/B/C bf16, dt/A/D
 fp32, bf16 output; 64 distinct seeded input sets resident in HBM and cycled. One
 step = cursor advance, ring append, precompute, output/flush for the whole batch.
-The same line carries the gated-delta-net decode (`gdn_decode`) and speculative
-verify (`gdn_spec`) results of their own workloads as sub-objects.
 
-Each step is replayed from CUDA graphs: one graph holds the fused prologue (cursor
-advance + ring append + tables, one launch), a second the output kernel, and CUDA
-events recorded on the stream between them time the output kernel inside the
-timed region.
+Each step is replayed from a CUDA graph holding the fused prologue (cursor advance
++ ring append + tables, one launch) and the output kernel. Every 7th step's graph
+also holds two CUDA events around the output kernel; the kernel's duration is the
+mean over a phase-complete set of those samples (each residue of the step index
+mod the ring length equally often: the flushing rows repeat with that period).
 
 Keys of the JSON line (rank 0):
   value       decode rows/s over all ranks (device-timed, inputs resident)
@@ -21,14 +20,23 @@ Keys of the JSON line (rank 0):
               device->host copy of y inside the timed region
   roofline    output kernel: algorithmic bytes per launch / CUDA-event duration
               of that kernel inside the timed region, against the measured HBM
-              copy bandwidth
+              copy bandwidth; traffic = DRAM bytes per launch from the committed
+              ncu summary while the kernel source and its headers are unchanged
   cpu_baseline  the float64 oracle (full recurrence) on this host's cores over a
               bounded sample of the same workload
   full_state  the in-house conventional kernel (whole state read+written per
               step) on an identical pool, same inputs
+  stochastic_rounding  the same steps with the bf16 state stored by stochastic
+              rounding
+  gdn_decode, gdn_spec, kda_decode, mamba2_spec  full lines of their own
+              workloads (GDN decode batch 256, GDN spec verify batch 128 T 4, KDA
+              decode batch 256, Mamba2 spec verify batch 128 T 4), each with its
+              roofline, e2e, cpu_baseline and comparison
+  mamba2_sweep  a compact sweep (batch 64 / 1024 x L 1 / 16 x fp32 / bf16 state),
+              each point beside the full-state kernel
 
-`--workload gdn` / `--workload spec` print the gated-delta-net lines as the main
-line; `--workload sweep` prints one line per point of the Mamba2 sweep (batch x L
+`--workload gdn|spec|kda|m2spec` prints one of the sub-objects as the main line;
+`--workload sweep` prints one line per point of the full Mamba2 sweep (batch x L
 x state dtype, 5% forced flushes), each with the full-state kernel beside it.
 `--impl reference` runs the oracle arm (the only reference implementation this
 method has here) on the same metric and workload.
