@@ -140,6 +140,15 @@ def test_spec_draft_lengths(T, L):
     _check_spec(wl, rows=np.arange(4), rounds=12)
 
 
+@pytest.mark.parametrize("T,L,adt,rounds", [(4, 24, "bf16", 22), (8, 32, "fp32", 16)])
+def test_spec_long_rings(T, L, adt, rounds):
+    # more than 16 committed entries: the fold stages them in two chunks and the table
+    # CTAs read the history keys past the ones they hold in registers
+    wl = W.gdn_spec(batch=4, num_v_heads=4, num_k_heads=2, num_slots=8, L=L, T=T, rounds=rounds,
+                    act_dtype=adt)
+    _check_spec(wl, rows=np.arange(4), rounds=rounds)
+
+
 def test_spec_config_all_rows():
     # batch 128, T 4, HV 32, HK 16, K = V = 128, L 16, 32 rounds, accepted ~ U{0..4}:
     # every row's draft outputs in every round and every folded checkpoint

@@ -64,6 +64,18 @@ def test_mamba2_spec_fp32_activations_and_other_tile():
     _check(wl)
 
 
+@pytest.mark.parametrize("headdim,dstate,L,T,sdt,adt,rounds", [
+    (128, 128, 32, 4, "bf16", "fp32", 26),  # bf16 state with float32 activations; 32 rows a thread
+    (64, 64, 20, 3, "bf16", "bf16", 18),    # 8 rows a thread; a ring longer than 16 entries
+    (128, 128, 12, 2, "fp32", "bf16", 20),  # float32 state with 32 rows a thread
+])
+def test_mamba2_spec_fold_shapes(headdim, dstate, L, T, sdt, adt, rounds):
+    # the prologue's fold paths: staging batches, rows held per thread, dtype pairs
+    wl = W.mamba2_spec(batch=5, nheads=8, ngroups=2, headdim=headdim, dstate=dstate,
+                       num_slots=10, L=L, T=T, rounds=rounds, state_dtype=sdt, act_dtype=adt)
+    _check(wl)
+
+
 def test_mamba2_spec_bench_geometry_all_rows():
     # batch 128, T 4, H 128, P 64, N 128, G 8, L 16, bf16 state: every row's draft
     # outputs in every round and every folded checkpoint
