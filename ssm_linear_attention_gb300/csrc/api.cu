@@ -194,7 +194,7 @@ extern "C" const char* rssm_status_string(int status) {
     switch (status) {
         case RSSM_OK: return "ok";
         case RSSM_ERR_INVALID_ARG: return "invalid argument (null or misaligned pointer, bad enum or size)";
-        case RSSM_ERR_UNSUPPORTED: return "unsupported shape or dtype for this build";
+        case RSSM_ERR_UNSUPPORTED: return "unsupported shape or dtype (no kernel instance in the library)";
         case RSSM_ERR_CONFIG: return "inconsistent configuration";
         case RSSM_ERR_CUDA: return "CUDA launch error";
         default: return "unknown status";
