@@ -82,7 +82,7 @@ __device__ __forceinline__ float ring_dt_at(const ProArgs& a, int s, int h, int 
 // and the entries' dt are loaded into registers. A short pass then turns the staged
 // entries into float32 (x scaled by a_i), and the update runs 4 rows per pass as
 // packed two-wide FMAs. SBF / ABF: the state / the activations are bf16.
-template <bool V, bool BF>
+template <bool BF>
 struct Raw4 {  // 4 state elements as loaded: bf16 pairs or float32
     uint2 u;
     __device__ __forceinline__ void load(const void* base, long i) {
@@ -92,8 +92,8 @@ struct Raw4 {  // 4 state elements as loaded: bf16 pairs or float32
         return make_float4(bf16_lo(u.x), bf16_hi(u.x), bf16_lo(u.y), bf16_hi(u.y));
     }
 };
-template <bool V>
-struct Raw4<V, false> {
+template <>
+struct Raw4<false> {
     float4 v;
     __device__ __forceinline__ void load(const void* base, long i) {
         v = *reinterpret_cast<const float4*>(static_cast<const float*>(base) + i);
@@ -145,7 +145,7 @@ __device__ void fold_tile(const ProArgs& a, int b, int h, float* sm) {
         }
         cp_async_commit();
     }
-    Raw4<true, SBF> sv[RMAX];
+    Raw4<SBF> sv[RMAX];
 #pragma unroll
     for (int k = 0; k < RMAX; ++k)
         if (k < rl) sv[k].load(st, (long)(p0 + k) * N + n0);
