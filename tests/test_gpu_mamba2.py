@@ -216,6 +216,32 @@ def test_padding_rows_are_untouched_and_bad_slots_flagged():
     assert torch.equal(dec.state, before)
 
 
+def test_small_batch_bad_cursor_is_flagged_and_skipped():
+    # the one-launch step (batch <= 16) reads the cursor itself: a slot whose write_pos is
+    # outside the ring is skipped (its output, state and cursor untouched) and flagged,
+    # while the other rows advance as usual
+    import ssm_linear_attention_gb300 as ssm
+    wl = W.mamba2_large(batch=6, nheads=8, ngroups=2, num_slots=12, L=4, steps=1, wp_mode="zero")
+    dec = Hn.make_mamba2_decoder(wl)
+    ci = wl.cache_indices()
+    bad = int(ci[3])
+    dec.slot_wp[bad] = wl.L + 2
+    before = dec.state.clone()
+    inp = wl.step_inputs(0)
+    x, dt, Bm, C, z = Hn.mamba2_inputs_dev(wl, inp)
+    y = torch.full((6, wl.nheads, wl.headdim), 7.0, device="cuda")
+    dec.step(x, dt, Bm, C, z, Hn.to_dev(ci, torch.int32), y=y)
+    torch.cuda.synchronize()
+    assert int(dec.dev_err[0].item()) & ssm.RSSM_DEVERR_CURSOR
+    assert torch.all(y[3] == 7.0)
+    assert int(dec.slot_wp[bad].item()) == wl.L + 2
+    assert torch.equal(dec.state, before)  # write_pos 0, L 4: no row flushes
+    for r in (0, 1, 2, 4, 5):
+        assert int(dec.slot_wp[int(ci[r])].item()) == 1
+    ref = oracle.mamba2_run(wl, rows=[0, 1, 2, 4, 5], steps=1)
+    assert Hn.err(y[[0, 1, 2, 4, 5]].cpu().numpy(), ref["y"][0]) <= 2e-3
+
+
 def test_desync_rows_are_independent():
     # Permuting the rows of a batch changes no row's output bit (no cross-row coupling).
     wl = W.mamba2_large(batch=48, num_slots=96, steps=6, force_rate=0.1)
